@@ -455,8 +455,9 @@ int or_table_writable(or_pool *p, int32_t *table, int pos, int block_size) {
  *              a = silu(Wg rmsnorm(x)) * (Wu rmsnorm(x)); x += Wd a
  *   logits = Whead rmsnorm(x); token' = argmax(logits)
  * READING: the token at 0-based position pos writes its K/V at slot pos and attends to
- * positions 0..pos (ctx = pos + 1); scale = fp32(1/sqrt(hd)).  With act_bf16 the GEMV
- * input vectors (the normed x and a) are rounded to bf16 before each product.
+ * positions 0..pos (ctx = pos + 1); scale = fp32(1/sqrt(hd)).  With act_bf16 every GEMV
+ * input vector (the normed x, the attention output, a) is rounded to bf16 before the
+ * product; the residual stream stays fp32.
  * KV pool layout: [n_blocks][n_layers][2 (k, v)][Hkv][block_size][hd] bf16. */
 typedef struct {
   int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab, block_size, act_bf16;
@@ -609,6 +610,7 @@ int or_decode_step(or_model *m, int token, int pos, const int32_t *block_table, 
       }
     or_attention_paged(q, m->kv + (int64_t)l * 2 * kv_half, m->kv + (int64_t)l * 2 * kv_half + kv_half,
                        blk_elems, block_table, pos + 1, Hq, Hkv, hd, c->block_size, scale, s.att);
+    maybe_bf16(m, s.att, Hq * hd);
     gemv_mat(&L[T_O], s.att, s.tmp);
     add_into(s.x, s.tmp, d);
     mlp_block(m, l, s.x, s.xn, s.g, s.u, s.tmp);
@@ -655,6 +657,7 @@ int or_forward_nocache(const or_model *m, const int32_t *tokens, int n, float *l
     for (int t = 0; t < n; ++t) {
       float *x = X + (int64_t)t * d;
       or_attention_contig(QKV + (int64_t)t * nq, K, V, t + 1, Hq, Hkv, hd, scale, s.att);
+      maybe_bf16(m, s.att, Hq * hd);
       gemv_mat(&L[T_O], s.att, s.tmp);
       add_into(x, s.tmp, d);
       mlp_block(m, l, x, s.xn, s.g, s.u, s.tmp);
