@@ -1,0 +1,257 @@
+/*
+ * mie.h -- C ABI of the GB300 decode-step library (libmie.so).
+ *
+ * The library runs the batch-1 and few-slot decode step of a Llama-style GQA decoder
+ * on one GPU: fused-dequant GEMVs over bf16, int8 per-row and Q4_0 weights, RoPE and
+ * a K/V write into a paged cache, split-context paged decode attention, RMSNorm,
+ * SwiGLU, the LM head and argmax, the whole step captured in a CUDA graph.
+ *
+ * Pages cited (titles):
+ *  [RUST]  "Writing an LLM inference engine from scratch in Rust"
+ *  [MIE]   "Mini Inference Engine"
+ *  [INFER] "infer" -- an LLM inference engine in C++ and CUDA for Llama-3.2-1B
+ *
+ * Conventions (every entry point):
+ *  - Status codes, never exceptions or aborts ([MIE]: an exhausted pool returns a
+ *    sentinel instead of throwing).  After a failure mie_last_error() returns a
+ *    message for the calling thread.
+ *  - Pointers documented "device" are CUDA device pointers (for example a torch
+ *    tensor's data_ptr()); "host" pointers are ordinary process memory.  The caller
+ *    owns every pointer it passes; the library keeps none of them after the call
+ *    returns, except where stated (mie_decode_step's block table and outputs are read
+ *    or written by work that is still queued on the stream).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *    Kernel entry points only enqueue work: results are ready once the stream is
+ *    synchronised.  Arguments are validated on the host before anything is enqueued.
+ *  - Storage formats: MIE_FMT_BF16 (uint16 bit patterns), MIE_FMT_I8 (int8 plus one
+ *    fp32 scale per row), MIE_FMT_Q4_0 (blocks of 32 four-bit codes plus one f16
+ *    scale), MIE_FMT_F32.
+ */
+#ifndef MIE_H_
+#define MIE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mie_status {
+  MIE_OK = 0,
+  MIE_E_ARG = 1,     /* null pointer, unknown name/format, id or value out of range */
+  MIE_E_SHAPE = 2,   /* a size or alignment the entry point does not support */
+  MIE_E_OOM = 3,     /* a device allocation failed, or the KV block pool is exhausted */
+  MIE_E_CUDA = 4,    /* a CUDA runtime call failed (the message names it) */
+  MIE_E_TIMEOUT = 5, /* a bounded device-side wait gave up */
+  MIE_E_STATE = 6,   /* call out of order, e.g. a step before all weights are loaded */
+  MIE_E_DEVICE = 7   /* a kernel's own bounds check rejected an index (see mie_check) */
+} mie_status;
+
+typedef enum mie_format {
+  MIE_FMT_BF16 = 0,
+  MIE_FMT_I8 = 1,
+  MIE_FMT_Q4_0 = 2,
+  MIE_FMT_F32 = 3
+} mie_format;
+
+/* Message for the last failure on the calling thread ("" if none). */
+const char *mie_last_error(void);
+const char *mie_status_string(mie_status s);
+
+/* ======================================================================== load time */
+
+/* fp32 -> bf16, round to nearest even.  w, out: device, n elements. */
+mie_status mie_convert_bf16(const float *w, int64_t n, uint16_t *out, void *stream);
+
+/* int8 with one scale per row ([INFER] design notes: weight-only quantization, "int8
+ * per row").  Per row: s = max|w| / 127 (fp32), q = round-half-away(w / s) clamped to
+ * [-127, 127]; a zero row gives s = 0, q = 0.  w: device [M][K] fp32 row-major;
+ * q: device [M][K]; scale: device [M]. */
+mie_status mie_quantize_i8(const float *w, int M, int K, int8_t *q, float *scale, void *stream);
+
+/* Q4_0 ([RUST] "Lesson 1" and "Is the 4-bit model still good?"; [INFER] design notes):
+ * blocks of 32 weights; the element of largest magnitude (first on ties), sign kept,
+ * divided by -8 gives d; h = f16(d) rounded to nearest even is stored; codes are
+ * q = clamp(floor(w * (1/h) + 8.5), 0, 15) (0 for h == 0), each step rounded in fp32.
+ * A row is zero-padded to a whole number of blocks.  Output is the canonical block
+ * layout [M][ceil(K/32)][18]: f16 scale little-endian, then 16 bytes whose byte j holds
+ * element j in the low nibble and element j+16 in the high nibble.
+ * w: device [M][K] fp32; blocks: device. */
+mie_status mie_quantize_q4_0(const float *w, int M, int K, uint8_t *blocks, void *stream);
+
+/* Size of the GPU layout of an M x K Q4_0 matrix: a nibble plane [M][nb][16] followed,
+ * at the next 256-byte boundary, by a scale plane [M][nb] of f16 (nb = ceil(K/32)). */
+size_t mie_q4_0_packed_bytes(int M, int K);
+
+/* Canonical blocks (device) -> GPU layout (device, mie_q4_0_packed_bytes(M, K) bytes). */
+mie_status mie_q4_0_pack(const uint8_t *blocks, int M, int K, void *packed, void *stream);
+
+/* ============================================================================ GEMV */
+
+/* y = W x with fp32 accumulation ([INFER] per-kernel table, "gemv"; [RUST] "Lesson 1":
+ * each weight is read once, so the kernel streams W at memory bandwidth).
+ *   mie_gemv_bf16: W device [M][K] bf16 row-major, K % 8 == 0, W 16-byte aligned.
+ *   mie_gemv_i8:   W device [M][K] int8 row-major, K % 16 == 0; row_scale device [M];
+ *                  y_i = s_i * sum_k q_ik x_k.
+ *   mie_gemv_q4_0: packed: device GPU layout from mie_q4_0_pack; any K >= 1.
+ * x: device [K] fp32; y: device [M] fp32 (must not alias x).  1 <= K <= 16384,
+ * M >= 1.  MIE_E_SHAPE for other sizes or misaligned pointers. */
+mie_status mie_gemv_bf16(const uint16_t *W, const float *x, float *y, int M, int K, void *stream);
+mie_status mie_gemv_i8(const int8_t *W, const float *row_scale, const float *x, float *y, int M,
+                       int K, void *stream);
+mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y, int M, int K, void *stream);
+
+/* ======================================================================= attention */
+
+/* Workspace bytes that mie_paged_attn_decode needs for these sizes. */
+size_t mie_paged_attn_workspace_bytes(int n_q_heads, int n_kv_heads, int head_dim, int ctx_len,
+                                      int block_size);
+
+/* Paged GQA decode attention, split over the context with an online softmax and a
+ * merge ([MIE] "The KV cache, paged like virtual memory"; [INFER] "GQA-aware split-KV
+ * attention"; [RUST] "Lesson 4": running maximum and sum, query heads sharing a KV
+ * head read it together).
+ *   out[h][d] = sum_{t < ctx_len} softmax_t(scale * q_h . k_{g,t}) v_{g,t}[d],
+ *   g = h / (n_q_heads / n_kv_heads).
+ * Key t of KV head g is at k_pool[block_table[t / block_size] * block_stride
+ *   + (g * block_size + t % block_size) * head_dim + d] (bf16); v_pool likewise.
+ * q: device [n_q_heads][head_dim] fp32; out: device, same shape; block_table: device
+ * int32 [n_table], entries in [0, n_pool_blocks).  head_dim in {32, 64, 128},
+ * n_q_heads % n_kv_heads == 0, group size <= 8, ctx_len <= n_table * block_size,
+ * block_size in {8, 16, 32}.  ctx_len == 0 gives a zero output.  workspace: device,
+ * at least mie_paged_attn_workspace_bytes(...) bytes, 256-byte aligned; its contents
+ * need not be initialised and are overwritten.  Calls sharing one workspace must not
+ * overlap on the GPU.  A block-table entry outside [0, n_pool_blocks) is skipped and
+ * latched as a device error, reported by mie_check as MIE_E_DEVICE. */
+mie_status mie_paged_attn_decode(const float *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                                 int64_t block_stride, int n_pool_blocks,
+                                 const int32_t *block_table, int n_table, int ctx_len,
+                                 int n_q_heads, int n_kv_heads, int head_dim, int block_size,
+                                 float scale, float *out, void *workspace,
+                                 size_t workspace_bytes, void *stream);
+
+/* ========================================================================== argmax */
+
+size_t mie_argmax_workspace_bytes(int n);
+
+/* Index of the largest of v[0..n) (device fp32); the lowest index wins a tie.
+ * out: device int32.  workspace: device, mie_argmax_workspace_bytes(n) bytes, need
+ * not be initialised.  n >= 1. */
+mie_status mie_argmax(const float *v, int n, int32_t *out, void *workspace, size_t workspace_bytes,
+                      void *stream);
+
+/* Reads and clears the device error flag that kernels latch when a bounds check
+ * fails (stateless kernels share one flag per device).  Synchronises `stream`.
+ * MIE_E_DEVICE if a check fired since the last call. */
+mie_status mie_check(void *stream);
+
+/* ============================================================ KV block pool (host) */
+
+/* Reference-counted pool of KV blocks ([MIE] "The KV cache, paged like virtual
+ * memory" and "Prefix sharing and copy-on-write"): a refcount per block id, a LIFO
+ * free list; a fresh pool hands out 0, 1, 2, ...  Host bookkeeping only: the block
+ * contents live in the model context's device KV pool. */
+typedef struct mie_pool mie_pool;
+
+mie_status mie_pool_create(int n_blocks, mie_pool **out);
+void mie_pool_destroy(mie_pool *p);
+/* *id = a block with refcount 1, or -1 and MIE_E_OOM when the pool is exhausted. */
+mie_status mie_pool_alloc(mie_pool *p, int32_t *id);
+mie_status mie_pool_incref(mie_pool *p, int32_t id);
+/* Drops one reference; a block reaching 0 returns to the free list. */
+mie_status mie_pool_decref(mie_pool *p, int32_t id);
+int mie_pool_refcount(const mie_pool *p, int32_t id); /* -1 for an id out of range */
+int mie_pool_free_count(const mie_pool *p);
+/* Copy-on-write for a write at logical position pos of a sequence whose block table
+ * (host int32, updated in place) is `table`: a private block is returned as is; a
+ * shared block is split -- allocate, (caller copies contents src -> dst), drop one
+ * reference to the old block, point the table at the new one.  *copy_src / *copy_dst
+ * are the split's blocks, or -1 when no copy is needed.  MIE_E_OOM with the table and
+ * counts untouched when no block is free.  The contents copy is the caller's
+ * (mie_kv_copy_block does it for a model context's pool) and must be enqueued before
+ * any write into the new block. */
+mie_status mie_pool_writable(mie_pool *p, int32_t *table, int pos, int block_size, int32_t *block,
+                             int32_t *copy_src, int32_t *copy_dst);
+
+/* ============================================================== model and step */
+
+typedef struct mie_ctx mie_ctx;
+
+typedef struct mie_config {
+  int n_layers, d_model, n_heads, n_kv_heads, head_dim, ffn, vocab;
+  int tied;        /* 1: the LM head matrix doubles as the embedding table */
+  int block_size;  /* tokens per KV block (16) */
+  int act_bf16;    /* 1: round each GEMV input vector to bf16 (residual stays fp32) */
+  float rms_eps;
+  float rope_theta;
+  int wfmt;        /* format of the layer matrices (mie_format) */
+  int head_fmt;    /* format of the LM head (and of the embedding when tied) */
+  int embed_fmt;   /* format of an untied embedding table */
+  int n_kv_blocks; /* device KV pool size in blocks */
+  int max_slots;   /* largest n_slots of mie_decode_step_slots (>= 1, <= 8) */
+  int max_pos;     /* positions 0 .. max_pos-1 are valid */
+} mie_config;
+
+/* Creates a context on the current CUDA device: device KV pool
+ * [n_kv_blocks][n_layers][2][n_kv_heads][block_size][head_dim] bf16 (zeroed), RoPE
+ * tables, activations, a host block pool of n_kv_blocks blocks.  stream: the stream
+ * every step of this context runs on. */
+mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **out);
+void mie_destroy(mie_ctx *ctx);
+
+/* Copies one weight from host memory into the context and repacks it for the
+ * kernels.  name: "l<i>.qkv" [(Hq+2Hkv)*hd][d] (rows q heads, then k, then v),
+ * "l<i>.o" [d][Hq*hd], "l<i>.gate" [ffn][d], "l<i>.up" [ffn][d], "l<i>.down" [d][ffn],
+ * "head" [vocab][d], "embed" [vocab][d] (untied only), "l<i>.attn_norm",
+ * "l<i>.mlp_norm", "final_norm" [d] (fp32 gains; all default to 1).
+ * fmt: MIE_FMT_F32 (fp32 [rows][cols]; quantised on the device into the context's
+ * format for that tensor) or that format itself in canonical layout (bf16 [rows][cols];
+ * i8 [rows][cols] with host_scale [rows]; Q4_0 blocks [rows][ceil(cols/32)][18]).
+ * bytes must equal the canonical size.  shape: {rows, cols} (gains: {d}). */
+mie_status mie_load_weights(mie_ctx *ctx, const char *name, int fmt, const void *host_data,
+                            size_t bytes, const int64_t *shape, int ndim,
+                            const float *host_scale);
+
+mie_pool *mie_ctx_pool(mie_ctx *ctx);
+/* Device pointer of the KV pool and the elements of one block (all layers, k and v). */
+uint16_t *mie_kv_pool(mie_ctx *ctx);
+int64_t mie_kv_block_elems(const mie_ctx *ctx);
+/* Enqueues a device copy of block src into block dst (copy-on-write). */
+mie_status mie_kv_copy_block(mie_ctx *ctx, int32_t src, int32_t dst);
+
+/* One decode step ([INFER] data-flow figure; [RUST] "How a Llama model generates
+ * text"): the token at 0-based position pos writes its K/V into block
+ * block_table[pos / block_size] and attends to positions 0..pos.  block_table: device
+ * int32 [n_blocks] (entries < n_kv_blocks).  logits_out: device fp32 [vocab] or NULL;
+ * argmax_out: device int32 or NULL (lowest index on ties).  The first call captures
+ * the step into a CUDA graph (call it outside any stream capture); later calls replay
+ * it.  The step reads token/pos/table from device memory, so one graph serves every
+ * step.  Asynchronous on the context's stream. */
+mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, const int32_t *block_table,
+                           int n_blocks, float *logits_out, int32_t *argmax_out);
+
+/* Greedy continuation: replays the step n_steps times with token = previous argmax
+ * and pos = previous pos + 1, all on the device.  Requires one mie_decode_step first
+ * (which fixes block table and outputs); the outputs hold the last step's results. */
+mie_status mie_decode_continue(mie_ctx *ctx, int n_steps);
+
+/* Few-slot step ([MIE] "Continuous batching"): every slot s advances one token,
+ * tokens[s] at pos[s] (host arrays), through row s of block_tables (device int32
+ * [n_slots][max_blocks]).  The weights are read once for all slots.  logits_out:
+ * device [n_slots][vocab] or NULL; argmax_out: device [n_slots] or NULL. */
+mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int32_t *tokens,
+                                 const int32_t *pos, const int32_t *block_tables, int max_blocks,
+                                 float *logits_out, int32_t *argmax_out);
+
+/* Synchronises the context's stream, then reads and clears its device error flag. */
+mie_status mie_sync(mie_ctx *ctx);
+
+/* Kernel launches one mie_decode_step replay performs (for launch accounting). */
+int mie_step_launches(const mie_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MIE_H_ */

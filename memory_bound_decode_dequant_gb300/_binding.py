@@ -1,0 +1,395 @@
+"""ctypes binding of libmie.so; names follow the C ABI in include/mie.h."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import numpy as np
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmie.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "mie.h")
+
+FMT = {"bf16": 0, "i8": 1, "q4_0": 2, "f32": 3}
+STATUS = {0: "MIE_OK", 1: "MIE_E_ARG", 2: "MIE_E_SHAPE", 3: "MIE_E_OOM", 4: "MIE_E_CUDA",
+          5: "MIE_E_TIMEOUT", 6: "MIE_E_STATE", 7: "MIE_E_DEVICE"}
+
+__all__ = ["lib", "MieError", "FMT", "LIB_PATH", "exported_names", "header_functions",
+           "mie_convert_bf16", "mie_quantize_i8", "mie_quantize_q4_0", "mie_q4_0_pack",
+           "mie_q4_0_packed_bytes", "mie_gemv_bf16", "mie_gemv_i8", "mie_gemv_q4_0",
+           "mie_paged_attn_decode", "mie_paged_attn_workspace_bytes", "mie_argmax",
+           "mie_argmax_workspace_bytes", "mie_check", "Pool", "Config", "Model", "DeviceArray"]
+
+
+class MieError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+P = ctypes.c_void_p
+I, I64, F, SZ = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+
+
+class Config(ctypes.Structure):
+    """mie_config."""
+    _fields_ = [("n_layers", I), ("d_model", I), ("n_heads", I), ("n_kv_heads", I),
+                ("head_dim", I), ("ffn", I), ("vocab", I), ("tied", I), ("block_size", I),
+                ("act_bf16", I), ("rms_eps", F), ("rope_theta", F), ("wfmt", I), ("head_fmt", I),
+                ("embed_fmt", I), ("n_kv_blocks", I), ("max_slots", I), ("max_pos", I)]
+
+
+_SIGS = {
+    "mie_last_error": (ctypes.c_char_p, []),
+    "mie_status_string": (ctypes.c_char_p, [I]),
+    "mie_convert_bf16": (I, [P, I64, P, P]),
+    "mie_quantize_i8": (I, [P, I, I, P, P, P]),
+    "mie_quantize_q4_0": (I, [P, I, I, P, P]),
+    "mie_q4_0_packed_bytes": (SZ, [I, I]),
+    "mie_q4_0_pack": (I, [P, I, I, P, P]),
+    "mie_gemv_bf16": (I, [P, P, P, I, I, P]),
+    "mie_gemv_i8": (I, [P, P, P, P, I, I, P]),
+    "mie_gemv_q4_0": (I, [P, P, P, I, I, P]),
+    "mie_paged_attn_workspace_bytes": (SZ, [I, I, I, I, I]),
+    "mie_paged_attn_decode": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, F, P, P, SZ, P]),
+    "mie_argmax_workspace_bytes": (SZ, [I]),
+    "mie_argmax": (I, [P, I, P, P, SZ, P]),
+    "mie_check": (I, [P]),
+    "mie_pool_create": (I, [I, ctypes.POINTER(P)]),
+    "mie_pool_destroy": (None, [P]),
+    "mie_pool_alloc": (I, [P, ctypes.POINTER(ctypes.c_int32)]),
+    "mie_pool_incref": (I, [P, ctypes.c_int32]),
+    "mie_pool_decref": (I, [P, ctypes.c_int32]),
+    "mie_pool_refcount": (I, [P, ctypes.c_int32]),
+    "mie_pool_free_count": (I, [P]),
+    "mie_pool_writable": (I, [P, P, I, I, ctypes.POINTER(ctypes.c_int32),
+                              ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)]),
+    "mie_create": (I, [ctypes.POINTER(Config), P, ctypes.POINTER(P)]),
+    "mie_destroy": (None, [P]),
+    "mie_load_weights": (I, [P, ctypes.c_char_p, I, P, SZ, ctypes.POINTER(ctypes.c_int64), I, P]),
+    "mie_ctx_pool": (P, [P]),
+    "mie_kv_pool": (P, [P]),
+    "mie_kv_block_elems": (I64, [P]),
+    "mie_kv_copy_block": (I, [P, ctypes.c_int32, ctypes.c_int32]),
+    "mie_decode_step": (I, [P, ctypes.c_int32, ctypes.c_int32, P, I, P, P]),
+    "mie_decode_continue": (I, [P, I]),
+    "mie_decode_step_slots": (I, [P, I, P, P, P, I, P, P]),
+    "mie_sync": (I, [P]),
+    "mie_step_launches": (I, [P]),
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libmie.so.  Raises if it has not been built: there is no fallback."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def header_functions() -> list[str]:
+    """Every function name that include/mie.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mie_[a-z0-9_]+)\s*\(", text)))
+
+
+def exported_names() -> list[str]:
+    return [n for n in header_functions() if hasattr(lib(), n)]
+
+
+def _check(status: int, what: str = ""):
+    if status != 0:
+        msg = lib().mie_last_error().decode(errors="replace")
+        raise MieError(status, f"{what}: {msg}" if what else msg)
+
+
+# --------------------------------------------------------------------- torch glue
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dev(t, dtype=None, name="tensor"):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def mie_convert_bf16(w, out=None, stream=None):
+    torch = _torch()
+    out = torch.empty(w.shape, dtype=torch.bfloat16, device=w.device) if out is None else out
+    _check(lib().mie_convert_bf16(_dev(w, torch.float32, "w"), w.numel(), _dev(out, torch.bfloat16, "out"),
+                                  _stream(stream)), "mie_convert_bf16")
+    return out
+
+
+def mie_quantize_i8(w, stream=None):
+    torch = _torch()
+    M, K = w.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=w.device)
+    s = torch.empty((M,), dtype=torch.float32, device=w.device)
+    _check(lib().mie_quantize_i8(_dev(w, torch.float32, "w"), M, K, q.data_ptr(), s.data_ptr(), _stream(stream)),
+           "mie_quantize_i8")
+    return q, s
+
+
+def mie_quantize_q4_0(w, stream=None):
+    torch = _torch()
+    M, K = w.shape
+    out = torch.empty((M, (K + 31) // 32, 18), dtype=torch.uint8, device=w.device)
+    _check(lib().mie_quantize_q4_0(_dev(w, torch.float32, "w"), M, K, out.data_ptr(), _stream(stream)),
+           "mie_quantize_q4_0")
+    return out
+
+
+def mie_q4_0_packed_bytes(M: int, K: int) -> int:
+    return int(lib().mie_q4_0_packed_bytes(M, K))
+
+
+def mie_q4_0_pack(blocks, M: int, K: int, stream=None):
+    torch = _torch()
+    out = torch.empty(mie_q4_0_packed_bytes(M, K), dtype=torch.uint8, device=blocks.device)
+    _check(lib().mie_q4_0_pack(_dev(blocks, torch.uint8, "blocks"), M, K, out.data_ptr(), _stream(stream)),
+           "mie_q4_0_pack")
+    return out
+
+
+def _y(y, M, device):
+    torch = _torch()
+    return torch.empty(M, dtype=torch.float32, device=device) if y is None else y
+
+
+def mie_gemv_bf16(W, x, y=None, stream=None):
+    torch = _torch()
+    M, K = W.shape
+    y = _y(y, M, W.device)
+    _check(lib().mie_gemv_bf16(_dev(W, torch.bfloat16, "W"), _dev(x, torch.float32, "x"),
+                               _dev(y, torch.float32, "y"), M, K, _stream(stream)), "mie_gemv_bf16")
+    return y
+
+
+def mie_gemv_i8(W, scale, x, y=None, stream=None):
+    torch = _torch()
+    M, K = W.shape
+    y = _y(y, M, W.device)
+    _check(lib().mie_gemv_i8(_dev(W, torch.int8, "W"), _dev(scale, torch.float32, "scale"),
+                             _dev(x, torch.float32, "x"), _dev(y, torch.float32, "y"), M, K, _stream(stream)),
+           "mie_gemv_i8")
+    return y
+
+
+def mie_gemv_q4_0(packed, x, M: int, K: int, y=None, stream=None):
+    torch = _torch()
+    y = _y(y, M, packed.device)
+    _check(lib().mie_gemv_q4_0(_dev(packed, torch.uint8, "packed"), _dev(x, torch.float32, "x"),
+                               _dev(y, torch.float32, "y"), M, K, _stream(stream)), "mie_gemv_q4_0")
+    return y
+
+
+def mie_paged_attn_workspace_bytes(Hq, Hkv, hd, ctx_len, bs) -> int:
+    return int(lib().mie_paged_attn_workspace_bytes(Hq, Hkv, hd, ctx_len, bs))
+
+
+def mie_paged_attn_decode(q, k_pool, v_pool, block_stride: int, n_pool_blocks: int, block_table,
+                          ctx_len: int, Hq: int, Hkv: int, hd: int, bs: int, scale: float,
+                          out=None, workspace=None, stream=None):
+    torch = _torch()
+    if out is None:
+        out = torch.empty(Hq * hd, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        nbytes = max(mie_paged_attn_workspace_bytes(Hq, Hkv, hd, ctx_len, bs), 256)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+    _check(lib().mie_paged_attn_decode(
+        _dev(q, torch.float32, "q"), _dev(k_pool, None, "k_pool"), _dev(v_pool, None, "v_pool"),
+        block_stride, n_pool_blocks, _dev(block_table, torch.int32, "block_table"), block_table.numel(),
+        ctx_len, Hq, Hkv, hd, bs, scale, _dev(out, torch.float32, "out"), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(stream)), "mie_paged_attn_decode")
+    return out
+
+
+def mie_argmax_workspace_bytes(n: int) -> int:
+    return int(lib().mie_argmax_workspace_bytes(n))
+
+
+def mie_argmax(v, out=None, workspace=None, stream=None):
+    torch = _torch()
+    if out is None:
+        out = torch.empty(1, dtype=torch.int32, device=v.device)
+    if workspace is None:
+        workspace = torch.empty(mie_argmax_workspace_bytes(v.numel()), dtype=torch.uint8, device=v.device)
+    _check(lib().mie_argmax(_dev(v, torch.float32, "v"), v.numel(), _dev(out, torch.int32, "out"),
+                            workspace.data_ptr(), workspace.numel(), _stream(stream)), "mie_argmax")
+    return out
+
+
+def mie_check(stream=None):
+    _check(lib().mie_check(_stream(stream)), "mie_check")
+
+
+# --------------------------------------------------------------------- block pool
+
+class Pool:
+    """mie_pool: refcounted KV block ids with a LIFO free list (host only)."""
+
+    def __init__(self, n_blocks: int = 0, handle=None):
+        self._own = handle is None
+        if handle is None:
+            h = P()
+            _check(lib().mie_pool_create(n_blocks, ctypes.byref(h)), "mie_pool_create")
+            handle = h.value
+        self.h = handle
+
+    def __del__(self):
+        if getattr(self, "_own", False) and getattr(self, "h", None):
+            lib().mie_pool_destroy(self.h)
+            self.h = None
+
+    def alloc(self) -> int:
+        i = ctypes.c_int32(-1)
+        st = lib().mie_pool_alloc(self.h, ctypes.byref(i))
+        if st not in (0, 3):
+            _check(st, "mie_pool_alloc")
+        return i.value
+
+    def incref(self, i: int) -> int:
+        return lib().mie_pool_incref(self.h, i)
+
+    def decref(self, i: int) -> int:
+        return lib().mie_pool_decref(self.h, i)
+
+    def refcount(self, i: int) -> int:
+        return lib().mie_pool_refcount(self.h, i)
+
+    def free_count(self) -> int:
+        return lib().mie_pool_free_count(self.h)
+
+    def writable(self, table: np.ndarray, pos: int, block_size: int):
+        """(status, block, copy_src, copy_dst); the table is updated in place."""
+        assert table.dtype == np.int32 and table.flags.c_contiguous
+        b, s, d = ctypes.c_int32(-1), ctypes.c_int32(-1), ctypes.c_int32(-1)
+        st = lib().mie_pool_writable(self.h, table.ctypes.data, pos, block_size, ctypes.byref(b),
+                                     ctypes.byref(s), ctypes.byref(d))
+        return st, b.value, s.value, d.value
+
+
+# --------------------------------------------------------------------- model
+
+class DeviceArray:
+    """A device buffer owned by the library, exposed to torch via __cuda_array_interface__."""
+
+    def __init__(self, ptr: int, shape, typestr: str, owner):
+        self._owner = owner
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (ptr, False), "version": 3, "strides": None}
+
+
+class Model:
+    """mie_ctx: weights in GPU layouts, the paged KV pool and the graph-captured step."""
+
+    def __init__(self, cfg: dict, stream=None):
+        c = Config(**cfg)
+        self.cfg = dict(cfg)
+        h = P()
+        _check(lib().mie_create(ctypes.byref(c), _stream(stream) if stream is not None else None, ctypes.byref(h)),
+               "mie_create")
+        self.h = h.value
+        self.pool = Pool(handle=lib().mie_ctx_pool(self.h))
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().mie_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        self.close()
+
+    def load_weights(self, name: str, data: np.ndarray, fmt: str = "f32", scale: np.ndarray | None = None,
+                     cols: int | None = None):
+        """Copies host data (numpy) into the context: fp32 [rows, cols] (quantised on the
+        GPU), or the tensor's own format in canonical layout."""
+        data = np.ascontiguousarray(data)
+        if data.ndim == 1:
+            shape = (data.shape[0],)
+        elif fmt == "q4_0":
+            shape = (data.shape[0], cols)
+        else:
+            shape = data.shape[:2]
+        arr = (ctypes.c_int64 * len(shape))(*shape)
+        sc = None
+        if scale is not None:
+            scale = np.ascontiguousarray(scale, dtype=np.float32)
+            sc = scale.ctypes.data
+        _check(lib().mie_load_weights(self.h, name.encode(), FMT[fmt], data.ctypes.data, data.nbytes, arr,
+                                      len(shape), sc), f"mie_load_weights({name})")
+
+    @property
+    def block_elems(self) -> int:
+        return int(lib().mie_kv_block_elems(self.h))
+
+    def kv(self):
+        """The device KV pool as a torch uint16-bits tensor
+        [n_kv_blocks, n_layers, 2, n_kv_heads, block_size, head_dim] (bf16 bit patterns)."""
+        torch = _torch()
+        c = self.cfg
+        shape = (c["n_kv_blocks"], c["n_layers"], 2, c["n_kv_heads"], c["block_size"], c["head_dim"])
+        arr = DeviceArray(lib().mie_kv_pool(self.h), shape, "<i2", self)
+        return torch.as_tensor(arr, device="cuda")
+
+    def kv_copy_block(self, src: int, dst: int):
+        _check(lib().mie_kv_copy_block(self.h, src, dst), "mie_kv_copy_block")
+
+    def decode_step(self, token: int, pos: int, block_table, logits_out=None, argmax_out=None):
+        torch = _torch()
+        _check(lib().mie_decode_step(self.h, int(token), int(pos), _dev(block_table, torch.int32, "block_table"),
+                                     block_table.numel(),
+                                     None if logits_out is None else _dev(logits_out, torch.float32, "logits"),
+                                     None if argmax_out is None else _dev(argmax_out, torch.int32, "argmax")),
+               "mie_decode_step")
+
+    def decode_continue(self, n_steps: int):
+        _check(lib().mie_decode_continue(self.h, n_steps), "mie_decode_continue")
+
+    def decode_step_slots(self, tokens, pos, block_tables, logits_out=None, argmax_out=None):
+        torch = _torch()
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        p = np.ascontiguousarray(pos, dtype=np.int32)
+        n_slots, max_blocks = block_tables.shape
+        _check(lib().mie_decode_step_slots(self.h, n_slots, t.ctypes.data, p.ctypes.data,
+                                           _dev(block_tables, torch.int32, "block_tables"), max_blocks,
+                                           None if logits_out is None else _dev(logits_out, torch.float32, "logits"),
+                                           None if argmax_out is None else _dev(argmax_out, torch.int32, "argmax")),
+               "mie_decode_step_slots")
+
+    def sync(self):
+        _check(lib().mie_sync(self.h), "mie_sync")
+
+    @property
+    def launches(self) -> int:
+        return int(lib().mie_step_launches(self.h))

@@ -1,0 +1,551 @@
+// gemv.cu -- fused-dequant GEMV kernels for batch-1 decode on sm_103a.
+//
+// y = W x with W in bf16, int8 (one fp32 scale per row) or Q4_0 (32-weight blocks of
+// 4-bit codes with one f16 scale), fp32 activations and accumulation ("infer" page:
+// decode GEMV with fused norm, residual and SwiGLU; weight-only quantization with
+// dequant in registers; "Writing an LLM inference engine from scratch in Rust",
+// Lesson 1: decode speed is set by how fast the weights stream from memory).
+//
+// Design (GB300): the weights are read exactly once, so the kernel is a stream of
+// 16-byte non-caching loads spread over all SMs.
+//  * A CTA owns a contiguous range of rows; each warp owns one 2048-column slice of
+//    K and walks its rows.  The warp's slice of the (normalised) input vector sits in
+//    64 registers per lane for the whole kernel, so the inner loop reads no shared
+//    memory: per 16-byte chunk it is loads, in-register unpack and packed fp32x2 FMAs.
+//  * Unpack without int->float conversions: a code is moved into the mantissa of
+//    2^23 by one LOP3 (Q4_0) or PRMT (int8), and one packed fp32x2 add removes both
+//    the 2^23 and the stored bias (+8 for Q4_0, +128 after flipping the int8 sign
+//    bit) exactly.  Q4_0 codes are masked in place at bit offset p and the matching
+//    input element is pre-scaled by 2^-p, which is exact.
+//  * Rows of a CTA are reduced across lanes with shuffles and across K slices through
+//    shared memory in a fixed order, then an epilogue applies the row scale and the
+//    fused operation (residual add, SwiGLU, RoPE + paged K/V write, argmax).
+//  * The first rows' weight loads are issued before griddepcontrol.wait, so inside
+//    the step graph they overlap the previous kernel's tail.
+#include <cstdarg>
+#include <cstdio>
+
+#include "internal.h"
+
+namespace mie {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+template <int F> struct FmtT;
+// EPC: elements per 16-byte chunk; CPL: chunks per lane per slice; U: rows in flight.
+template <> struct FmtT<MIE_FMT_BF16> { static constexpr int EPC = 8, CPL = 8, U = 1; };
+template <> struct FmtT<MIE_FMT_I8> { static constexpr int EPC = 16, CPL = 4, U = 2; };
+template <> struct FmtT<MIE_FMT_Q4_0> { static constexpr int EPC = 32, CPL = 2, U = 3; };
+constexpr int kSlice = 2048;  // = 32 * EPC * CPL for every format
+constexpr int kMaxK = kSlice * kWarps;
+
+int gemv_chunk_elems(int fmt) {
+  return fmt == MIE_FMT_BF16 ? 8 : fmt == MIE_FMT_I8 ? 16 : fmt == MIE_FMT_Q4_0 ? 32 : 0;
+}
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+// --------------------------------------------------------------- element decoding
+
+__device__ __forceinline__ float embed_at(const DevMat &m, int row, int k) {
+  if (m.fmt == MIE_FMT_BF16) {
+    return bf16_bits_to_f32(reinterpret_cast<const uint16_t *>(m.w + (int64_t)row * m.row_bytes)[k]);
+  } else if (m.fmt == MIE_FMT_I8) {
+    const int8_t q = reinterpret_cast<const int8_t *>(m.w + (int64_t)row * m.row_bytes)[k];
+    return reinterpret_cast<const float *>(m.s)[row] * (float)q;
+  } else {
+    const int nb = m.kp / 32;
+    const uint8_t byte = m.w[(int64_t)row * m.row_bytes + (k >> 5) * 16 + (k & 15)];
+    const int code = ((k & 31) < 16) ? (byte & 0xF) : (byte >> 4);
+    const float h = __half2float(reinterpret_cast<const __half *>(m.s)[(int64_t)row * nb + (k >> 5)]);
+    return h * (float)(code - 8);
+  }
+}
+
+// Dot product of one 16-byte chunk with the lane's input registers.
+template <int F>
+__device__ __forceinline__ void chunk_fma(const uint4 &w, const float2 *xr, float2 *acc);
+
+template <>
+__device__ __forceinline__ void chunk_fma<MIE_FMT_BF16>(const uint4 &w, const float2 *xr, float2 *acc) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 wf = make_float2(__uint_as_float(v[t] << 16), __uint_as_float(v[t] & 0xffff0000u));
+    acc[t] = __ffma2_rn(wf, xr[t], acc[t]);
+  }
+}
+
+template <>
+__device__ __forceinline__ void chunk_fma<MIE_FMT_I8>(const uint4 &w, const float2 *xr, float2 *acc) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+  const float2 bias = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t u = v[t] ^ 0x80808080u;  // int8 b -> b + 128 in 0..255
+    const float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
+    const float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
+    acc[t] = __ffma2_rn(__fadd2_rn(a, bias), xr[2 * t], acc[t]);
+    acc[t] = __ffma2_rn(__fadd2_rn(b, bias), xr[2 * t + 1], acc[t]);
+  }
+}
+
+// Q4_0 chunk = one block: word t holds bytes 4t..4t+3; byte j carries element j (low
+// nibble) and element j+16 (high nibble).  Unpack order per word, with the bit offset
+// p the code sits at: 4t(p0) 4t+16(p4) 4t+1(p8) 4t+17(p12) 4t+2(p16), then from
+// w >> 12: 4t+18(p8) 4t+3(p12) 4t+19(p16).  The input registers hold x * 2^-p in
+// that order, so (2^23 + n 2^p) - (2^23 + 8 2^p) = (n - 8) 2^p times them is
+// (n - 8) x.
+template <>
+__device__ __forceinline__ void chunk_fma<MIE_FMT_Q4_0>(const uint4 &w, const float2 *xr, float2 *acc) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t M = 0x4B000000u;
+  const float2 b01 = make_float2(-8388616.f, -8388736.f);  // -(2^23 + 8 * {1, 16})
+  const float2 b23 = make_float2(-8390656.f, -8421376.f);  // -(2^23 + 8 * {256, 4096})
+  const float2 b45 = make_float2(-8912896.f, -8390656.f);  // -(2^23 + 8 * {65536, 256})
+  const float2 b67 = make_float2(-8421376.f, -8912896.f);  // -(2^23 + 8 * {4096, 65536})
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t a = v[t], s = v[t] >> 12;
+    const float2 d01 = __fadd2_rn(make_float2(__uint_as_float((a & 0xFu) | M), __uint_as_float((a & 0xF0u) | M)), b01);
+    const float2 d23 = __fadd2_rn(make_float2(__uint_as_float((a & 0xF00u) | M), __uint_as_float((a & 0xF000u) | M)), b23);
+    const float2 d45 = __fadd2_rn(make_float2(__uint_as_float((a & 0xF0000u) | M), __uint_as_float((s & 0xF00u) | M)), b45);
+    const float2 d67 = __fadd2_rn(make_float2(__uint_as_float((s & 0xF000u) | M), __uint_as_float((s & 0xF0000u) | M)), b67);
+    acc[t] = __ffma2_rn(d01, xr[4 * t + 0], acc[t]);
+    acc[t] = __ffma2_rn(d23, xr[4 * t + 1], acc[t]);
+    acc[t] = __ffma2_rn(d45, xr[4 * t + 2], acc[t]);
+    acc[t] = __ffma2_rn(d67, xr[4 * t + 3], acc[t]);
+  }
+}
+
+// Input registers of one chunk from the staged vector xs (natural order).
+template <int F>
+__device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr) {
+  if constexpr (F == MIE_FMT_Q4_0) {
+    const float sc[8] = {1.f, 0.0625f, 0.00390625f, 0.000244140625f, 1.52587890625e-05f,
+                         0.00390625f, 0.000244140625f, 1.52587890625e-05f};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int src[8] = {4 * t, 4 * t + 16, 4 * t + 1, 4 * t + 17, 4 * t + 2, 4 * t + 18, 4 * t + 3, 4 * t + 19};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        xr[4 * t + i] = make_float2(xs[e + src[2 * i]] * sc[2 * i], xs[e + src[2 * i + 1]] * sc[2 * i + 1]);
+    }
+  } else {
+    constexpr int EPC = FmtT<F>::EPC;
+#pragma unroll
+    for (int i = 0; i < EPC / 4; ++i) {
+      const float4 q = *reinterpret_cast<const float4 *>(xs + e + 4 * i);
+      xr[2 * i] = make_float2(q.x, q.y);
+      xr[2 * i + 1] = make_float2(q.z, q.w);
+    }
+  }
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// --------------------------------------------------------------- the kernel
+
+template <int F, int PRO, int EPI>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
+  using T = FmtT<F>;
+  constexpr int EPC = T::EPC, CPL = T::CPL, U = T::U;
+  constexpr int RU = (EPI == EPI_SWIGLU || EPI == EPI_QKV) ? 2 : 1;
+  extern __shared__ __align__(16) float smem[];
+  __shared__ float red[kWarps];
+  __shared__ float s_scale;
+  __shared__ float s_bv[kWarps];
+  __shared__ int s_bi[kWarps];
+  __shared__ unsigned s_last;
+
+  pdl_trigger();
+
+  const DevMat &m = a.m;
+  const int Kp = m.kp, K = m.cols, M = m.rows;
+  const int KS = (Kp + kSlice - 1) / kSlice;
+  float *xs = smem;       // [Kp] staged input vector
+  float *part = smem + Kp; // [rows of this CTA][KS]
+
+  const int n_units = (M + RU - 1) / RU;
+  const int u0 = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+  const int u1 = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+  const int row0 = u0 * RU, row1 = min(u1 * RU, M);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ks = warp % KS, rw = warp / KS, nrw = kWarps / KS;
+  const int nrows_w = (row1 - row0 > rw) ? (row1 - row0 - rw + nrw - 1) / nrw : 0;
+
+  // element offset of this lane's chunk c within a row
+  const int e0 = ks * kSlice + lane * EPC;
+  constexpr int kChunkStride = 32 * EPC;
+  constexpr int kBitsPerElem = (F == MIE_FMT_BF16) ? 16 : (F == MIE_FMT_I8 ? 8 : 4);
+
+  uint4 wbuf[U][CPL];
+  float hbuf[U][CPL];
+  auto issue = [&](int j, int slot) {
+    if (j < nrows_w) {
+      const int r = row0 + rw + j * nrw;
+      const uint8_t *row = m.w + (int64_t)r * m.row_bytes;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int e = e0 + c * kChunkStride;
+        if (e < Kp) {
+          wbuf[slot][c] = ldg_stream(row + (int64_t)e * kBitsPerElem / 8);
+          if constexpr (F == MIE_FMT_Q4_0)
+            hbuf[slot][c] = __half2float(__ushort_as_half(
+                ldg_u16(reinterpret_cast<const __half *>(m.s) + (int64_t)r * (Kp / 32) + (e >> 5))));
+        } else {
+          wbuf[slot][c] = make_uint4(0, 0, 0, 0);
+          hbuf[slot][c] = 0.f;
+        }
+      }
+    }
+  };
+#pragma unroll
+  for (int u = 0; u < U; ++u) issue(u, u);
+
+  pdl_wait();
+
+  // ---------------------------------------------------------------- prologue
+  const int tid = threadIdx.x;
+  if constexpr (PRO == PRO_EMBED_NORM) {
+    int tok = a.sp ? a.sp->token[a.slot] : 0;
+    if (tok < 0 || tok >= a.vocab) {
+      if (tid == 0 && blockIdx.x == 0) latch_error(a.err, ERR_TOKEN);
+      tok = 0;
+    }
+    for (int k = tid; k < Kp; k += kThreads) {
+      const float v = (k < K) ? embed_at(a.embed, tok, k) : 0.f;
+      xs[k] = v;
+      if (blockIdx.x == 0 && k < K) a.x_store[k] = v;
+    }
+  } else {
+    for (int k = tid; k < Kp; k += kThreads) xs[k] = (k < K) ? a.x[k] : 0.f;
+  }
+  if constexpr (PRO != PRO_PLAIN) {
+    float ss = 0.f;
+    for (int k = tid; k < K; k += kThreads) ss += xs[k] * xs[k];
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    __syncthreads();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < kWarps; ++w) t += red[w];
+      s_scale = 1.0f / sqrtf(t / (float)K + a.eps);
+    }
+    __syncthreads();
+    const float r = s_scale;
+    for (int k = tid; k < K; k += kThreads) {
+      float v = xs[k] * r * a.gain[k];
+      if (a.act_bf16) v = round_bf16(v);
+      xs[k] = v;
+    }
+  } else {
+    if (a.act_bf16)
+      for (int k = tid; k < K; k += kThreads) xs[k] = round_bf16(xs[k]);
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- main loop
+  float2 xr[CPL * EPC / 2];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const int e = e0 + c * kChunkStride;
+    if (e < Kp) {
+      load_xr<F>(xs, e, xr + c * (EPC / 2));
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPC / 2; ++i) xr[c * (EPC / 2) + i] = make_float2(0.f, 0.f);
+    }
+  }
+
+  for (int j0 = 0; j0 < nrows_w; j0 += U) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int j = j0 + u;
+      if (j < nrows_w) {
+        float sum = 0.f;
+        if constexpr (F == MIE_FMT_Q4_0) {
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) {
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            chunk_fma<F>(wbuf[u][c], xr + c * (EPC / 2), acc);
+            const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+            sum = fmaf(hbuf[u][c], cs, sum);
+          }
+        } else {
+          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) chunk_fma<F>(wbuf[u][c], xr + c * (EPC / 2), acc);
+          sum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+        }
+        issue(j + U, u);
+        sum = warp_sum(sum);
+        if (lane == 0) part[(rw + j * nrw) * KS + ks] = sum;
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- epilogue
+  auto row_value = [&](int r) {
+    float v = 0.f;
+    for (int s = 0; s < KS; ++s) v += part[(r - row0) * KS + s];
+    if constexpr (F == MIE_FMT_I8) v *= reinterpret_cast<const float *>(m.s)[r];
+    return v;
+  };
+
+  if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
+    for (int r = row0 + tid; r < row1; r += kThreads) {
+      const float v = row_value(r);
+      if constexpr (EPI == EPI_STORE) a.y[r] = v;
+      else a.y[r] = a.y[r] + v;
+    }
+  } else if constexpr (EPI == EPI_SWIGLU) {
+    // packed rows 2i = gate_i, 2i+1 = up_i -> y_i = silu(gate_i) * up_i
+    for (int u = u0 + tid; u < u1; u += kThreads) {
+      const float g = row_value(2 * u), up = row_value(2 * u + 1);
+      float v = g / (1.0f + expf(-g)) * up;
+      a.y[u] = v;
+    }
+  } else if constexpr (EPI == EPI_QKV) {
+    // packed rows 2p, 2p+1 = rows i and i + hd/2 of head h (p = h * hd/2 + i)
+    const int pos = a.sp->pos[a.slot];
+    const int h2 = a.hd / 2;
+    const int32_t *bt = a.sp->block_table + (int64_t)a.slot * a.sp->max_blocks;
+    const bool pos_ok = pos >= 0 && pos < a.max_pos && pos / a.bs < a.sp->max_blocks;
+    int blk = -1;
+    if (pos_ok) blk = bt[pos / a.bs];
+    const bool blk_ok = pos_ok && blk >= 0 && blk < a.n_kv_blocks;
+    if (tid == 0 && blockIdx.x == 0 && !blk_ok) latch_error(a.err, pos_ok ? ERR_BLOCK_ID : ERR_POS);
+    for (int u = u0 + tid; u < u1; u += kThreads) {
+      const int h = u / h2, i = u % h2;
+      float x0 = row_value(2 * u), x1 = row_value(2 * u + 1);
+      if (h < a.Hq + a.Hkv && pos_ok) {
+        const float c = a.rope_cos[(int64_t)pos * h2 + i], s = a.rope_sin[(int64_t)pos * h2 + i];
+        const float r0 = x0 * c - x1 * s, r1 = x1 * c + x0 * s;
+        x0 = r0;
+        x1 = r1;
+      }
+      if (h < a.Hq) {
+        a.q_out[h * a.hd + i] = x0;
+        a.q_out[h * a.hd + i + h2] = x1;
+      } else if (blk_ok) {
+        const int isv = h >= a.Hq + a.Hkv;
+        const int g = h - a.Hq - (isv ? a.Hkv : 0);
+        uint16_t *dst = a.kv_layer + (int64_t)blk * a.block_stride + (int64_t)isv * a.Hkv * a.bs * a.hd +
+                        ((int64_t)g * a.bs + pos % a.bs) * a.hd;
+        dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
+        dst[i + h2] = __bfloat16_as_ushort(__float2bfloat16_rn(x1));
+      }
+    }
+  } else if constexpr (EPI == EPI_ARGMAX) {
+    float *logits = a.y ? a.y : (a.sp ? a.sp->logits_out : nullptr);
+    if (logits && a.sp && !a.y) logits += (int64_t)a.slot * M;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int r = row0 + tid; r < row1; r += kThreads) {
+      const float v = row_value(r);
+      if (logits) logits[r] = v;
+      if (better(v, r, bv, bi)) { bv = v; bi = r; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
+    __syncthreads();
+    if (tid == 0) {
+      for (int w = 1; w < kWarps; ++w)
+        if (better(s_bv[w], s_bi[w], bv, bi)) { bv = s_bv[w]; bi = s_bi[w]; }
+      a.am_part[blockIdx.x] = make_float2(bv, __int_as_float(bi));
+      __threadfence();
+      s_last = (atomicAdd(a.am_count, 1u) == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      float fv = -INFINITY;
+      int fi = 0x7fffffff;
+      for (int b = tid; b < (int)gridDim.x; b += kThreads) {
+        const float2 p = __ldcg(a.am_part + b);
+        if (better(p.x, __float_as_int(p.y), fv, fi)) { fv = p.x; fi = __float_as_int(p.y); }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, fv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, fi, o);
+        if (better(ov, oi, fv, fi)) { fv = ov; fi = oi; }
+      }
+      __syncthreads();
+      if (lane == 0) { s_bv[warp] = fv; s_bi[warp] = fi; }
+      __syncthreads();
+      if (tid == 0) {
+        for (int w = 1; w < kWarps; ++w)
+          if (better(s_bv[w], s_bi[w], fv, fi)) { fv = s_bv[w]; fi = s_bi[w]; }
+        if (fi == 0x7fffffff) fi = 0;  // all values NaN: fall back to index 0
+        if (a.am_out) a.am_out[a.slot] = fi;
+        if (a.sp) {
+          if (a.sp->argmax_out) a.sp->argmax_out[a.slot] = fi;
+          if (a.sp->advance) {
+            a.sp->token[a.slot] = fi;
+            a.sp->pos[a.slot] += 1;
+          }
+        }
+        *a.am_count = 0u;
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------- launching
+
+template <int F, int PRO, int EPI>
+static mie_status launch_t(const GemvArgs &a, int grid, cudaStream_t st, bool pdl) {
+  const int RU = (EPI == EPI_SWIGLU || EPI == EPI_QKV) ? 2 : 1;
+  const int n_units = (a.m.rows + RU - 1) / RU;
+  const int KS = (a.m.kp + kSlice - 1) / kSlice;
+  const int rows_max = ((n_units + grid - 1) / grid) * RU;
+  const size_t smem = sizeof(float) * ((size_t)a.m.kp + (size_t)rows_max * KS);
+  auto kern = gemv_kernel<F, PRO, EPI>;
+  static bool configured[64] = {false};
+  static size_t configured_bytes[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && (!configured[dev] || configured_bytes[dev] < smem) && smem > 48 * 1024) {
+    MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+    configured[dev] = true;
+    configured_bytes[dev] = 200 * 1024;
+  }
+  if (smem > 200 * 1024) return fail(MIE_E_SHAPE, "gemv: %zu bytes of shared memory needed", smem);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  MIE_CUDA(cudaLaunchKernelEx(&cfg, kern, a));
+  return MIE_OK;
+}
+
+template <int F>
+static mie_status launch_f(int pro, int epi, const GemvArgs &a, int grid, cudaStream_t st, bool pdl) {
+#define MIE_CASE(P, E) \
+  if (pro == P && epi == E) return launch_t<F, P, E>(a, grid, st, pdl);
+  MIE_CASE(PRO_PLAIN, EPI_STORE)
+  MIE_CASE(PRO_PLAIN, EPI_RESID)
+  MIE_CASE(PRO_NORM, EPI_SWIGLU)
+  MIE_CASE(PRO_NORM, EPI_QKV)
+  MIE_CASE(PRO_EMBED_NORM, EPI_QKV)
+  MIE_CASE(PRO_NORM, EPI_ARGMAX)
+  MIE_CASE(PRO_PLAIN, EPI_ARGMAX)
+  MIE_CASE(PRO_NORM, EPI_STORE)
+#undef MIE_CASE
+  return fail(MIE_E_ARG, "gemv: unsupported prologue/epilogue %d/%d", pro, epi);
+}
+
+int gemv_default_grid(const DevMat &m, int epi) {
+  const int RU = (epi == EPI_SWIGLU || epi == EPI_QKV) ? 2 : 1;
+  const int n_units = (m.rows + RU - 1) / RU;
+  const int target = 2 * sm_count();
+  return n_units < target ? n_units : target;
+}
+
+mie_status launch_gemv(int pro, int epi, const GemvArgs &a, int grid, cudaStream_t st, bool pdl) {
+  if (a.m.kp > kMaxK) return fail(MIE_E_SHAPE, "gemv: K = %d exceeds %d", a.m.kp, kMaxK);
+  if (grid < 1) grid = 1;
+  switch (a.m.fmt) {
+    case MIE_FMT_BF16: return launch_f<MIE_FMT_BF16>(pro, epi, a, grid, st, pdl);
+    case MIE_FMT_I8: return launch_f<MIE_FMT_I8>(pro, epi, a, grid, st, pdl);
+    case MIE_FMT_Q4_0: return launch_f<MIE_FMT_Q4_0>(pro, epi, a, grid, st, pdl);
+    default: return fail(MIE_E_ARG, "gemv: unknown weight format %d", a.m.fmt);
+  }
+}
+
+}  // namespace mie
+
+// --------------------------------------------------------------- C ABI: stateless GEMVs
+
+using namespace mie;
+
+static mie_status gemv_entry(DevMat m, const float *x, float *y, void *stream) {
+  if (!m.w || !x || !y) return fail(MIE_E_ARG, "gemv: null pointer");
+  if (m.rows < 1 || m.cols < 1 || m.cols > kMaxK) return fail(MIE_E_SHAPE, "gemv: bad shape %d x %d", m.rows, m.cols);
+  if (((uintptr_t)m.w & 15) != 0) return fail(MIE_E_SHAPE, "gemv: weights not 16-byte aligned");
+  if ((const void *)x == (const void *)y) return fail(MIE_E_ARG, "gemv: y aliases x");
+  GemvArgs a;
+  a.m = m;
+  a.x = x;
+  a.y = y;
+  return launch_gemv(PRO_PLAIN, EPI_STORE, a, gemv_default_grid(m, EPI_STORE), (cudaStream_t)stream, false);
+}
+
+extern "C" mie_status mie_gemv_bf16(const uint16_t *W, const float *x, float *y, int M, int K, void *stream) {
+  if (K % 8 != 0) return fail(MIE_E_SHAPE, "mie_gemv_bf16: K = %d is not a multiple of 8", K);
+  DevMat m;
+  m.fmt = MIE_FMT_BF16;
+  m.rows = M;
+  m.cols = K;
+  m.kp = K;
+  m.w = reinterpret_cast<const uint8_t *>(W);
+  m.row_bytes = (int64_t)K * 2;
+  return gemv_entry(m, x, y, stream);
+}
+
+extern "C" mie_status mie_gemv_i8(const int8_t *W, const float *row_scale, const float *x, float *y, int M, int K,
+                                  void *stream) {
+  if (K % 16 != 0) return fail(MIE_E_SHAPE, "mie_gemv_i8: K = %d is not a multiple of 16", K);
+  if (!row_scale) return fail(MIE_E_ARG, "mie_gemv_i8: null row_scale");
+  DevMat m;
+  m.fmt = MIE_FMT_I8;
+  m.rows = M;
+  m.cols = K;
+  m.kp = K;
+  m.w = reinterpret_cast<const uint8_t *>(W);
+  m.s = row_scale;
+  m.row_bytes = K;
+  return gemv_entry(m, x, y, stream);
+}
+
+extern "C" size_t mie_q4_0_packed_bytes(int M, int K) {
+  if (M < 1 || K < 1) return 0;
+  const size_t nb = (size_t)(K + 31) / 32;
+  const size_t nib = ((size_t)M * nb * 16 + 255) & ~(size_t)255;
+  return nib + (size_t)M * nb * 2;
+}
+
+extern "C" mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y, int M, int K, void *stream) {
+  if (M < 1 || K < 1) return fail(MIE_E_SHAPE, "mie_gemv_q4_0: bad shape %d x %d", M, K);
+  const int nb = (K + 31) / 32;
+  DevMat m;
+  m.fmt = MIE_FMT_Q4_0;
+  m.rows = M;
+  m.cols = K;
+  m.kp = nb * 32;
+  m.w = reinterpret_cast<const uint8_t *>(packed);
+  m.row_bytes = (int64_t)nb * 16;
+  const size_t nib = ((size_t)M * nb * 16 + 255) & ~(size_t)255;
+  m.s = reinterpret_cast<const uint8_t *>(packed) + nib;
+  return gemv_entry(m, x, y, stream);
+}

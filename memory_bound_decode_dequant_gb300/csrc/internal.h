@@ -1,0 +1,95 @@
+// internal.h -- host-side interfaces shared by the translation units of libmie.so.
+#pragma once
+
+#include "common.cuh"
+
+namespace mie {
+
+enum Prologue { PRO_PLAIN = 0, PRO_NORM = 1, PRO_EMBED_NORM = 2 };
+enum Epilogue { EPI_STORE = 0, EPI_RESID = 1, EPI_SWIGLU = 2, EPI_QKV = 3, EPI_ARGMAX = 4 };
+
+// One weight matrix in its GPU layout.
+struct DevMat {
+  int fmt = -1;            // mie_format
+  int rows = 0, cols = 0;  // logical shape
+  int kp = 0;              // padded columns (multiple of the format's chunk)
+  const uint8_t *w = nullptr;  // bf16/i8 row-major [rows][kp]; Q4_0 nibble plane [rows][kp/32][16]
+  const void *s = nullptr;     // i8: float[rows]; Q4_0: half[rows][kp/32]
+  int64_t row_bytes = 0;
+};
+
+// Arguments of one GEMV launch (plain or fused).
+struct GemvArgs {
+  DevMat m;
+  const float *x = nullptr;     // input vector [cols] (PRO_PLAIN, PRO_NORM)
+  const float *gain = nullptr;  // RMSNorm gain [cols]
+  float eps = 0.f;
+  int act_bf16 = 0;
+  DevMat embed;                 // PRO_EMBED_NORM: table to gather token sp->token[slot] from
+  float *x_store = nullptr;     // PRO_EMBED_NORM: residual stream written by CTA 0
+  int vocab = 0;
+  float *y = nullptr;           // STORE/RESID/SWIGLU output; ARGMAX logits (nullable)
+  // EPI_QKV
+  float *q_out = nullptr;
+  uint16_t *kv_layer = nullptr; // this layer's K half of block 0; V follows after Hkv*bs*hd
+  int64_t block_stride = 0;     // elements between consecutive KV blocks
+  int n_kv_blocks = 0;
+  const float *rope_cos = nullptr, *rope_sin = nullptr;  // [max_pos][hd/2]
+  int max_pos = 0;
+  int Hq = 0, Hkv = 0, hd = 0, bs = 0;
+  // EPI_ARGMAX
+  float2 *am_part = nullptr;    // [grid] (value, index bits)
+  unsigned *am_count = nullptr; // zero before the first launch; the kernel resets it
+  int32_t *am_out = nullptr;    // argmax written here (besides sp->argmax_out)
+  StepParams *sp = nullptr;
+  int slot = 0;
+  int *err = nullptr;
+};
+
+int gemv_chunk_elems(int fmt);  // elements per 16-byte chunk: 8 / 16 / 32
+int sm_count();
+
+// Launches one GEMV; `pdl` adds the programmatic-dependent-launch attribute.
+mie_status launch_gemv(int pro, int epi, const GemvArgs &a, int grid, cudaStream_t st, bool pdl);
+int gemv_default_grid(const DevMat &m, int epi);
+
+// Attention (split context, merge by the last CTA of each KV head).
+struct AttnArgs {
+  const float *q = nullptr;
+  const uint16_t *k = nullptr, *v = nullptr;  // this layer's K and V bases
+  int64_t block_stride = 0;
+  int n_pool_blocks = 0;
+  const int32_t *block_table = nullptr;  // used when sp == nullptr
+  int n_table = 0;
+  int ctx = 0;                           // used when sp == nullptr
+  StepParams *sp = nullptr;
+  int slot = 0;
+  int Hq = 0, Hkv = 0, hd = 0, bs = 0;
+  float scale = 0.f;
+  float *out = nullptr;
+  float *ws_part = nullptr;
+  unsigned *ws_count = nullptr;
+  int n_splits = 1;
+  int *err = nullptr;
+};
+size_t attn_workspace_bytes(int Hq, int Hkv, int hd, int n_splits);
+int attn_splits_for(int Hkv, int max_ctx, int bs);
+mie_status launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl);
+
+// Load-time kernels.
+mie_status launch_convert_bf16(const float *w, int64_t n, uint16_t *out, cudaStream_t st);
+mie_status launch_quantize_i8(const float *w, int M, int K, int8_t *q, float *s, cudaStream_t st);
+mie_status launch_quantize_q4_0(const float *w, int M, int K, uint8_t *blocks, cudaStream_t st);
+mie_status launch_q4_0_pack(const uint8_t *blocks, int M, int K, uint8_t *nib, __half *scales,
+                            const int *row_map, cudaStream_t st);
+mie_status launch_row_permute(const uint8_t *src, uint8_t *dst, int64_t row_bytes, int M,
+                              const int *row_map, cudaStream_t st);
+mie_status launch_pad_rows(const uint8_t *src, int64_t src_row_bytes, uint8_t *dst,
+                           int64_t dst_row_bytes, int M, const int *row_map, cudaStream_t st);
+mie_status launch_rope_table(float *cos_t, float *sin_t, int n_pos, int hd, double base,
+                             cudaStream_t st);
+mie_status launch_argmax(const float *v, int n, int32_t *out, float2 *part, unsigned *count,
+                         int grid, cudaStream_t st);
+int argmax_grid(int n);
+
+}  // namespace mie

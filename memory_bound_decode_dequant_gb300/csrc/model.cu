@@ -1,0 +1,653 @@
+// model.cu -- the decode-step context: weights in GPU layouts, the paged KV pool, the
+// step as a chain of fused kernels captured once into a CUDA graph.
+//
+// Step ("infer" page, data-flow figure; "Writing an LLM inference engine from scratch
+// in Rust", "How a Llama model generates text"), per layer:
+//   qkv   : RMSNorm(x) staged in the GEMV prologue (layer 0 gathers x = E[token]
+//           first), Wqkv rows paired (i, i + hd/2) so the epilogue applies RoPE and
+//           writes bf16 K/V into the paged pool through the block table
+//   attn  : split-context paged GQA attention, merged by the last CTA of each KV head
+//   o     : x += Wo o (residual epilogue)
+//   gu    : RMSNorm(x), gate/up rows interleaved, epilogue silu(gate) * up
+//   down  : x += Wd a
+// then the LM head with RMSNorm prologue and an argmax epilogue.  Every kernel is
+// launched with programmatic dependent launch, so inside the graph each one issues
+// its first weight loads while its predecessor drains.  Token, position and block
+// table are read from device memory (StepParams), so one graph serves every step.
+#include <cstdarg>
+#include <cstdio>
+#include <cmath>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace mie {
+
+static thread_local std::string g_last_error;
+
+void set_error(const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+}
+
+mie_status fail(mie_status s, const char *fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+mie_status cuda_fail(cudaError_t e, const char *what) {
+  return fail(MIE_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace mie
+
+using namespace mie;
+
+extern "C" const char *mie_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" const char *mie_status_string(mie_status s) {
+  switch (s) {
+    case MIE_OK: return "ok";
+    case MIE_E_ARG: return "invalid argument";
+    case MIE_E_SHAPE: return "unsupported shape";
+    case MIE_E_OOM: return "out of memory";
+    case MIE_E_CUDA: return "CUDA error";
+    case MIE_E_TIMEOUT: return "timeout";
+    case MIE_E_STATE: return "invalid state";
+    case MIE_E_DEVICE: return "device bounds check";
+  }
+  return "unknown status";
+}
+
+namespace {
+
+enum { T_QKV = 0, T_O, T_GATE, T_UP, T_DOWN, T_ANORM, T_MNORM, T_COUNT };
+
+struct Layer {
+  DevMat qkv, o, gu, down;
+  float *attn_norm = nullptr, *mlp_norm = nullptr;
+  bool loaded[T_COUNT] = {false, false, false, false, false, true, true};
+};
+
+int pad_to(int v, int m) { return (v + m - 1) / m * m; }
+
+}  // namespace
+
+struct mie_ctx {
+  mie_config cfg{};
+  cudaStream_t stream = nullptr;
+  bool own_stream = false;
+  std::vector<void *> allocs;
+  std::vector<Layer> layers;
+  DevMat head, embed;
+  bool head_loaded = false, embed_loaded = false;
+  float *final_norm = nullptr;
+  uint16_t *kv = nullptr;
+  int64_t block_elems = 0;
+  float *x = nullptr, *q = nullptr, *att = nullptr, *act = nullptr;
+  float *rope_cos = nullptr, *rope_sin = nullptr;
+  float *attn_part = nullptr;
+  unsigned *attn_count = nullptr;
+  int attn_splits = 1;
+  float2 *am_part = nullptr;
+  unsigned *am_count = nullptr;
+  StepParams *sp = nullptr;
+  StepParams sp_host{};
+  int *err = nullptr;
+  cudaGraphExec_t graph = nullptr;
+  int launches = 0;
+  bool primed = false;
+  mie_pool *pool = nullptr;
+
+  void *dalloc(size_t bytes) {
+    void *p = nullptr;
+    if (cudaMalloc(&p, bytes ? bytes : 16) != cudaSuccess) return nullptr;
+    allocs.push_back(p);
+    return p;
+  }
+};
+
+static mie_status check_config(const mie_config &c) {
+  if (c.n_layers < 1 || c.d_model < 1 || c.n_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 1 || c.ffn < 1 ||
+      c.vocab < 1)
+    return fail(MIE_E_ARG, "mie_create: non-positive model dimension");
+  if (c.n_heads % c.n_kv_heads) return fail(MIE_E_SHAPE, "mie_create: n_heads %% n_kv_heads != 0");
+  const int G = c.n_heads / c.n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return fail(MIE_E_SHAPE, "mie_create: group size %d", G);
+  if (c.head_dim != 32 && c.head_dim != 64 && c.head_dim != 128)
+    return fail(MIE_E_SHAPE, "mie_create: head_dim %d", c.head_dim);
+  if (c.block_size != 8 && c.block_size != 16 && c.block_size != 32)
+    return fail(MIE_E_SHAPE, "mie_create: block_size %d", c.block_size);
+  const int kmax = 16384;
+  if (c.d_model > kmax || c.ffn > kmax || c.n_heads * c.head_dim > kmax)
+    return fail(MIE_E_SHAPE, "mie_create: a GEMV input is longer than %d", kmax);
+  if (c.max_slots < 1 || c.max_slots > kMaxSlots) return fail(MIE_E_SHAPE, "mie_create: max_slots %d", c.max_slots);
+  if (c.n_kv_blocks < 1 || c.max_pos < 1) return fail(MIE_E_ARG, "mie_create: n_kv_blocks / max_pos");
+  for (int f : {c.wfmt, c.head_fmt})
+    if (f != MIE_FMT_BF16 && f != MIE_FMT_I8 && f != MIE_FMT_Q4_0) return fail(MIE_E_ARG, "mie_create: format %d", f);
+  if (!c.tied && c.embed_fmt != MIE_FMT_BF16 && c.embed_fmt != MIE_FMT_I8 && c.embed_fmt != MIE_FMT_Q4_0)
+    return fail(MIE_E_ARG, "mie_create: embed format %d", c.embed_fmt);
+  return MIE_OK;
+}
+
+extern "C" void mie_destroy(mie_ctx *ctx) {
+  if (!ctx) return;
+  if (ctx->stream) cudaStreamSynchronize(ctx->stream);
+  if (ctx->graph) cudaGraphExecDestroy(ctx->graph);
+  for (void *p : ctx->allocs) cudaFree(p);
+  if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
+  mie_pool_destroy(ctx->pool);
+  delete ctx;
+}
+
+extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **out) {
+  if (!cfg || !out) return fail(MIE_E_ARG, "mie_create: null pointer");
+  *out = nullptr;
+  mie_status s = check_config(*cfg);
+  if (s != MIE_OK) return s;
+  mie_ctx *ctx = new (std::nothrow) mie_ctx;
+  if (!ctx) return fail(MIE_E_OOM, "mie_create: host allocation");
+  ctx->cfg = *cfg;
+  const mie_config &c = ctx->cfg;
+  if (stream) {
+    ctx->stream = (cudaStream_t)stream;
+  } else {
+    if (cudaStreamCreateWithFlags(&ctx->stream, cudaStreamNonBlocking) != cudaSuccess) {
+      delete ctx;
+      return fail(MIE_E_CUDA, "mie_create: cudaStreamCreate");
+    }
+    ctx->own_stream = true;
+  }
+  ctx->layers.resize((size_t)c.n_layers);
+  ctx->block_elems = (int64_t)c.n_layers * 2 * c.n_kv_heads * c.block_size * c.head_dim;
+  const size_t kv_bytes = (size_t)c.n_kv_blocks * ctx->block_elems * 2;
+  const int S = c.max_slots;
+  ctx->kv = (uint16_t *)ctx->dalloc(kv_bytes);
+  ctx->x = (float *)ctx->dalloc(sizeof(float) * S * c.d_model);
+  ctx->q = (float *)ctx->dalloc(sizeof(float) * S * c.n_heads * c.head_dim);
+  ctx->att = (float *)ctx->dalloc(sizeof(float) * S * c.n_heads * c.head_dim);
+  ctx->act = (float *)ctx->dalloc(sizeof(float) * S * c.ffn);
+  ctx->rope_cos = (float *)ctx->dalloc(sizeof(float) * (size_t)c.max_pos * (c.head_dim / 2));
+  ctx->rope_sin = (float *)ctx->dalloc(sizeof(float) * (size_t)c.max_pos * (c.head_dim / 2));
+  ctx->attn_splits = attn_splits_for(c.n_kv_heads, c.max_pos, c.block_size);
+  const size_t aws = attn_workspace_bytes(c.n_heads, c.n_kv_heads, c.head_dim, ctx->attn_splits);
+  uint8_t *ws = (uint8_t *)ctx->dalloc(aws * S);
+  ctx->am_part = (float2 *)ctx->dalloc(sizeof(float2) * 4 * sm_count() * S);
+  ctx->am_count = (unsigned *)ctx->dalloc(sizeof(unsigned) * 64);
+  ctx->sp = (StepParams *)ctx->dalloc(sizeof(StepParams));
+  ctx->err = (int *)ctx->dalloc(sizeof(int) * 4);
+  std::vector<float> ones((size_t)c.d_model, 1.0f);
+  for (auto &L : ctx->layers) {
+    L.attn_norm = (float *)ctx->dalloc(sizeof(float) * c.d_model);
+    L.mlp_norm = (float *)ctx->dalloc(sizeof(float) * c.d_model);
+  }
+  ctx->final_norm = (float *)ctx->dalloc(sizeof(float) * c.d_model);
+  bool ok = ctx->kv && ctx->x && ctx->q && ctx->att && ctx->act && ctx->rope_cos && ctx->rope_sin && ws &&
+            ctx->am_part && ctx->am_count && ctx->sp && ctx->err && ctx->final_norm;
+  for (auto &L : ctx->layers) ok = ok && L.attn_norm && L.mlp_norm;
+  if (!ok) {
+    mie_destroy(ctx);
+    return fail(MIE_E_OOM, "mie_create: device allocation of %zu KV bytes failed", kv_bytes);
+  }
+  ctx->attn_count = (unsigned *)ws;
+  ctx->attn_part = (float *)(ws + 256 + ((size_t)c.n_kv_heads * 4 + 255) / 256 * 256);
+  cudaError_t e = cudaSuccess;
+  auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+  chk(cudaMemsetAsync(ctx->kv, 0, kv_bytes, ctx->stream));
+  chk(cudaMemsetAsync(ws, 0, aws * S, ctx->stream));
+  chk(cudaMemsetAsync(ctx->am_count, 0, sizeof(unsigned) * 64, ctx->stream));
+  chk(cudaMemsetAsync(ctx->err, 0, sizeof(int) * 4, ctx->stream));
+  chk(cudaMemsetAsync(ctx->sp, 0, sizeof(StepParams), ctx->stream));
+  for (auto &L : ctx->layers) {
+    chk(cudaMemcpyAsync(L.attn_norm, ones.data(), sizeof(float) * c.d_model, cudaMemcpyHostToDevice, ctx->stream));
+    chk(cudaMemcpyAsync(L.mlp_norm, ones.data(), sizeof(float) * c.d_model, cudaMemcpyHostToDevice, ctx->stream));
+  }
+  chk(cudaMemcpyAsync(ctx->final_norm, ones.data(), sizeof(float) * c.d_model, cudaMemcpyHostToDevice, ctx->stream));
+  if (e != cudaSuccess) {
+    mie_destroy(ctx);
+    return cuda_fail(e, "mie_create: initialisation");
+  }
+  s = launch_rope_table(ctx->rope_cos, ctx->rope_sin, c.max_pos, c.head_dim, (double)c.rope_theta, ctx->stream);
+  if (s == MIE_OK && cudaStreamSynchronize(ctx->stream) != cudaSuccess) s = fail(MIE_E_CUDA, "mie_create: sync");
+  if (s == MIE_OK) s = mie_pool_create(c.n_kv_blocks, &ctx->pool);
+  if (s != MIE_OK) {
+    mie_destroy(ctx);
+    return s;
+  }
+  *out = ctx;
+  return MIE_OK;
+}
+
+// ------------------------------------------------------------------ weight loading
+
+namespace {
+
+// Allocates a matrix in its GPU layout (zero-filled so padding reads as zeros).
+mie_status alloc_mat(mie_ctx *ctx, DevMat &m, int fmt, int rows, int cols) {
+  m.fmt = fmt;
+  m.rows = rows;
+  m.cols = cols;
+  size_t wbytes = 0, sbytes = 0;
+  if (fmt == MIE_FMT_BF16) {
+    m.kp = pad_to(cols, 8);
+    m.row_bytes = (int64_t)m.kp * 2;
+  } else if (fmt == MIE_FMT_I8) {
+    m.kp = pad_to(cols, 16);
+    m.row_bytes = m.kp;
+    sbytes = sizeof(float) * rows;
+  } else {
+    m.kp = pad_to(cols, 32);
+    m.row_bytes = (int64_t)(m.kp / 32) * 16;
+    sbytes = sizeof(__half) * (size_t)rows * (m.kp / 32);
+  }
+  wbytes = (size_t)rows * m.row_bytes;
+  uint8_t *w = (uint8_t *)ctx->dalloc(wbytes);
+  void *s = sbytes ? ctx->dalloc(sbytes) : nullptr;
+  if (!w || (sbytes && !s)) return fail(MIE_E_OOM, "weights: device allocation of %zu bytes", wbytes + sbytes);
+  if (cudaMemsetAsync(w, 0, wbytes, ctx->stream) != cudaSuccess) return fail(MIE_E_CUDA, "weights: memset");
+  if (s && cudaMemsetAsync(s, 0, sbytes, ctx->stream) != cudaSuccess) return fail(MIE_E_CUDA, "weights: memset");
+  m.w = w;
+  m.s = s;
+  return MIE_OK;
+}
+
+struct Temp {
+  std::vector<void *> p;
+  ~Temp() {
+    for (void *q : p) cudaFree(q);
+  }
+  void *get(size_t n) {
+    void *q = nullptr;
+    if (cudaMalloc(&q, n ? n : 16) != cudaSuccess) return nullptr;
+    p.push_back(q);
+    return q;
+  }
+};
+
+// Writes source rows [rows][cols] given as host data in `fmt` (F32 or the matrix's own
+// canonical format) into matrix m, source row r landing on row map[r].
+mie_status fill_mat_body(mie_ctx *ctx, Temp &tmp, DevMat &m, int fmt, const void *host, size_t bytes,
+                         const float *host_scale, int rows, int cols, const std::vector<int> &map) {
+  cudaStream_t st = ctx->stream;
+  const int nb = (cols + 31) / 32;
+  size_t expect = 0;
+  if (fmt == MIE_FMT_F32) expect = (size_t)rows * cols * 4;
+  else if (fmt == MIE_FMT_BF16) expect = (size_t)rows * cols * 2;
+  else if (fmt == MIE_FMT_I8) expect = (size_t)rows * cols;
+  else if (fmt == MIE_FMT_Q4_0) expect = (size_t)rows * nb * 18;
+  if (fmt != MIE_FMT_F32 && fmt != m.fmt)
+    return fail(MIE_E_ARG, "weights: host format %d is neither F32 nor the tensor's format %d", fmt, m.fmt);
+  if (bytes != expect) return fail(MIE_E_ARG, "weights: %zu bytes given, %zu expected", bytes, expect);
+  if (fmt == MIE_FMT_I8 && !host_scale) return fail(MIE_E_ARG, "weights: int8 data without row scales");
+  void *src = tmp.get(bytes);
+  int *dmap = nullptr;
+  if (!map.empty()) dmap = (int *)tmp.get(sizeof(int) * map.size());
+  if (!src || (!map.empty() && !dmap)) return fail(MIE_E_OOM, "weights: staging allocation");
+  MIE_CUDA(cudaMemcpyAsync(src, host, bytes, cudaMemcpyHostToDevice, st));
+  if (dmap) MIE_CUDA(cudaMemcpyAsync(dmap, map.data(), sizeof(int) * map.size(), cudaMemcpyHostToDevice, st));
+  // bring the data into the canonical layout of the matrix's format
+  const void *canon = src;
+  const float *canon_scale = nullptr;
+  mie_status s = MIE_OK;
+  if (m.fmt == MIE_FMT_BF16) {
+    if (fmt == MIE_FMT_F32) {
+      uint16_t *b = (uint16_t *)tmp.get((size_t)rows * cols * 2);
+      if (!b) return fail(MIE_E_OOM, "weights: staging allocation");
+      if ((s = launch_convert_bf16((const float *)src, (int64_t)rows * cols, b, st)) != MIE_OK) return s;
+      canon = b;
+    }
+    return launch_pad_rows((const uint8_t *)canon, (int64_t)cols * 2, const_cast<uint8_t *>(m.w), m.row_bytes, rows,
+                           dmap, st);
+  }
+  if (m.fmt == MIE_FMT_I8) {
+    float *sc = (float *)tmp.get(sizeof(float) * rows);
+    if (!sc) return fail(MIE_E_OOM, "weights: staging allocation");
+    if (fmt == MIE_FMT_F32) {
+      int8_t *q = (int8_t *)tmp.get((size_t)rows * cols);
+      if (!q) return fail(MIE_E_OOM, "weights: staging allocation");
+      if ((s = launch_quantize_i8((const float *)src, rows, cols, q, sc, st)) != MIE_OK) return s;
+      canon = q;
+    } else {
+      MIE_CUDA(cudaMemcpyAsync(sc, host_scale, sizeof(float) * rows, cudaMemcpyHostToDevice, st));
+    }
+    canon_scale = sc;
+    if ((s = launch_pad_rows((const uint8_t *)canon, cols, const_cast<uint8_t *>(m.w), m.row_bytes, rows, dmap, st)) !=
+        MIE_OK)
+      return s;
+    return launch_pad_rows((const uint8_t *)canon_scale, 4, (uint8_t *)const_cast<void *>(m.s), 4, rows, dmap, st);
+  }
+  // Q4_0
+  if (fmt == MIE_FMT_F32) {
+    uint8_t *b = (uint8_t *)tmp.get((size_t)rows * nb * 18);
+    if (!b) return fail(MIE_E_OOM, "weights: staging allocation");
+    if ((s = launch_quantize_q4_0((const float *)src, rows, cols, b, st)) != MIE_OK) return s;
+    canon = b;
+  }
+  if (m.kp / 32 != nb) return fail(MIE_E_SHAPE, "weights: Q4_0 block count mismatch");
+  return launch_q4_0_pack((const uint8_t *)canon, rows, cols, const_cast<uint8_t *>(m.w),
+                          (__half *)const_cast<void *>(m.s), dmap, st);
+}
+
+mie_status fill_mat(mie_ctx *ctx, DevMat &m, int fmt, const void *host, size_t bytes, const float *host_scale, int rows,
+                    int cols, const std::vector<int> &map) {
+  Temp tmp;
+  const mie_status s = fill_mat_body(ctx, tmp, m, fmt, host, bytes, host_scale, rows, cols, map);
+  // the staging buffers are freed on return: let the work that reads them finish
+  const cudaError_t e = cudaStreamSynchronize(ctx->stream);
+  if (s != MIE_OK) return s;
+  if (e != cudaSuccess) return cuda_fail(e, "weights: cudaStreamSynchronize");
+  return MIE_OK;
+}
+
+}  // namespace
+
+extern "C" mie_status mie_load_weights(mie_ctx *ctx, const char *name, int fmt, const void *host_data, size_t bytes,
+                                       const int64_t *shape, int ndim, const float *host_scale) {
+  if (!ctx || !name || !host_data || !shape) return fail(MIE_E_ARG, "mie_load_weights: null pointer");
+  const mie_config &c = ctx->cfg;
+  std::string n(name);
+  // norm gains
+  auto load_gain = [&](float *dst) -> mie_status {
+    if (fmt != MIE_FMT_F32 || ndim != 1 || shape[0] != c.d_model || bytes != sizeof(float) * c.d_model)
+      return fail(MIE_E_ARG, "mie_load_weights(%s): gains are fp32 [d_model]", name);
+    MIE_CUDA(cudaMemcpyAsync(dst, host_data, bytes, cudaMemcpyHostToDevice, ctx->stream));
+    MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+    return MIE_OK;
+  };
+  if (n == "final_norm") return load_gain(ctx->final_norm);
+  if (ndim != 2) return fail(MIE_E_ARG, "mie_load_weights(%s): ndim %d", name, ndim);
+  const int rows = (int)shape[0], cols = (int)shape[1];
+  const int hd = c.head_dim, Hq = c.n_heads, Hkv = c.n_kv_heads, d = c.d_model;
+  auto want = [&](int r, int k) -> mie_status {
+    if (rows != r || cols != k) return fail(MIE_E_SHAPE, "mie_load_weights(%s): shape %d x %d, expected %d x %d", name, rows, cols, r, k);
+    return MIE_OK;
+  };
+  mie_status s;
+  std::vector<int> none;
+  ctx->primed = false;  // weights changed: the next step re-captures
+  if (n == "head" || n == "embed") {
+    const bool is_head = n == "head";
+    if (!is_head && c.tied) return fail(MIE_E_ARG, "mie_load_weights: tied model has no separate embedding");
+    if ((s = want(c.vocab, d)) != MIE_OK) return s;
+    DevMat &m = is_head ? ctx->head : ctx->embed;
+    if (!m.w && (s = alloc_mat(ctx, m, is_head ? c.head_fmt : c.embed_fmt, rows, cols)) != MIE_OK) return s;
+    if ((s = fill_mat(ctx, m, fmt, host_data, bytes, host_scale, rows, cols, none)) != MIE_OK) return s;
+    if (is_head) ctx->head_loaded = true;
+    else ctx->embed_loaded = true;
+    if (is_head && c.tied) {
+      ctx->embed = ctx->head;
+      ctx->embed_loaded = true;
+    }
+    MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+    return MIE_OK;
+  }
+  int layer = -1;
+  char part[32] = {0};
+  if (sscanf(name, "l%d.%31s", &layer, part) != 2 || layer < 0 || layer >= c.n_layers)
+    return fail(MIE_E_ARG, "mie_load_weights: unknown tensor name '%s'", name);
+  Layer &L = ctx->layers[(size_t)layer];
+  std::string p(part);
+  if (p == "attn_norm") return load_gain(L.attn_norm);
+  if (p == "mlp_norm") return load_gain(L.mlp_norm);
+  if (p == "qkv") {
+    const int R = (Hq + 2 * Hkv) * hd;
+    if ((s = want(R, d)) != MIE_OK) return s;
+    // row R' of head h, index i' -> pair slot p = h*hd/2 + i' % (hd/2), half i' / (hd/2)
+    std::vector<int> map((size_t)R);
+    for (int r = 0; r < R; ++r) {
+      const int h = r / hd, i = r % hd, half = hd / 2;
+      map[(size_t)r] = 2 * (h * half + (i % half)) + (i >= half ? 1 : 0);
+    }
+    if (!L.qkv.w && (s = alloc_mat(ctx, L.qkv, c.wfmt, R, d)) != MIE_OK) return s;
+    if ((s = fill_mat(ctx, L.qkv, fmt, host_data, bytes, host_scale, rows, cols, map)) != MIE_OK) return s;
+    L.loaded[T_QKV] = true;
+  } else if (p == "o") {
+    if ((s = want(d, Hq * hd)) != MIE_OK) return s;
+    if (!L.o.w && (s = alloc_mat(ctx, L.o, c.wfmt, d, Hq * hd)) != MIE_OK) return s;
+    if ((s = fill_mat(ctx, L.o, fmt, host_data, bytes, host_scale, rows, cols, none)) != MIE_OK) return s;
+    L.loaded[T_O] = true;
+  } else if (p == "gate" || p == "up") {
+    if ((s = want(c.ffn, d)) != MIE_OK) return s;
+    std::vector<int> map((size_t)c.ffn);
+    const int which = p == "up" ? 1 : 0;
+    for (int r = 0; r < c.ffn; ++r) map[(size_t)r] = 2 * r + which;
+    if (!L.gu.w && (s = alloc_mat(ctx, L.gu, c.wfmt, 2 * c.ffn, d)) != MIE_OK) return s;
+    if ((s = fill_mat(ctx, L.gu, fmt, host_data, bytes, host_scale, rows, cols, map)) != MIE_OK) return s;
+    L.loaded[which ? T_UP : T_GATE] = true;
+  } else if (p == "down") {
+    if ((s = want(d, c.ffn)) != MIE_OK) return s;
+    if (!L.down.w && (s = alloc_mat(ctx, L.down, c.wfmt, d, c.ffn)) != MIE_OK) return s;
+    if ((s = fill_mat(ctx, L.down, fmt, host_data, bytes, host_scale, rows, cols, none)) != MIE_OK) return s;
+    L.loaded[T_DOWN] = true;
+  } else {
+    return fail(MIE_E_ARG, "mie_load_weights: unknown tensor name '%s'", name);
+  }
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  return MIE_OK;
+}
+
+extern "C" mie_pool *mie_ctx_pool(mie_ctx *ctx) { return ctx ? ctx->pool : nullptr; }
+extern "C" uint16_t *mie_kv_pool(mie_ctx *ctx) { return ctx ? ctx->kv : nullptr; }
+extern "C" int64_t mie_kv_block_elems(const mie_ctx *ctx) { return ctx ? ctx->block_elems : 0; }
+
+extern "C" mie_status mie_kv_copy_block(mie_ctx *ctx, int32_t src, int32_t dst) {
+  if (!ctx) return fail(MIE_E_ARG, "mie_kv_copy_block: null context");
+  if (src < 0 || dst < 0 || src >= ctx->cfg.n_kv_blocks || dst >= ctx->cfg.n_kv_blocks)
+    return fail(MIE_E_ARG, "mie_kv_copy_block: block %d -> %d out of range", src, dst);
+  const size_t bytes = (size_t)ctx->block_elems * 2;
+  MIE_CUDA(cudaMemcpyAsync(ctx->kv + (int64_t)dst * ctx->block_elems, ctx->kv + (int64_t)src * ctx->block_elems, bytes,
+                           cudaMemcpyDeviceToDevice, ctx->stream));
+  return MIE_OK;
+}
+
+// ------------------------------------------------------------------ the step
+
+static bool all_loaded(const mie_ctx *ctx) {
+  if (!ctx->head_loaded || !ctx->embed_loaded) return false;
+  for (const auto &L : ctx->layers)
+    for (bool b : L.loaded)
+      if (!b) return false;
+  return true;
+}
+
+// Enqueues one decode step for slot 0 (the graph body).
+static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
+  const mie_config &c = ctx->cfg;
+  cudaStream_t st = ctx->stream;
+  int n = 0;
+  mie_status s;
+  const int64_t half = (int64_t)c.n_kv_heads * c.block_size * c.head_dim;
+  for (int l = 0; l < c.n_layers; ++l) {
+    Layer &L = ctx->layers[(size_t)l];
+    uint16_t *kv_layer = ctx->kv + (int64_t)l * 2 * half;
+    {  // qkv + RoPE + K/V write
+      GemvArgs a;
+      a.m = L.qkv;
+      a.x = ctx->x;
+      a.gain = L.attn_norm;
+      a.eps = c.rms_eps;
+      a.act_bf16 = c.act_bf16;
+      a.embed = ctx->embed;
+      a.x_store = ctx->x;
+      a.vocab = c.vocab;
+      a.q_out = ctx->q;
+      a.kv_layer = kv_layer;
+      a.block_stride = ctx->block_elems;
+      a.n_kv_blocks = c.n_kv_blocks;
+      a.rope_cos = ctx->rope_cos;
+      a.rope_sin = ctx->rope_sin;
+      a.max_pos = c.max_pos;
+      a.Hq = c.n_heads;
+      a.Hkv = c.n_kv_heads;
+      a.hd = c.head_dim;
+      a.bs = c.block_size;
+      a.sp = ctx->sp;
+      a.err = ctx->err;
+      if ((s = launch_gemv(l == 0 ? PRO_EMBED_NORM : PRO_NORM, EPI_QKV, a, gemv_default_grid(a.m, EPI_QKV), st,
+                           true)) != MIE_OK)
+        return s;
+      ++n;
+    }
+    {  // attention
+      AttnArgs a;
+      a.q = ctx->q;
+      a.k = kv_layer;
+      a.v = kv_layer + half;
+      a.block_stride = ctx->block_elems;
+      a.n_pool_blocks = c.n_kv_blocks;
+      a.sp = ctx->sp;
+      a.Hq = c.n_heads;
+      a.Hkv = c.n_kv_heads;
+      a.hd = c.head_dim;
+      a.bs = c.block_size;
+      a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+      a.out = ctx->att;
+      a.ws_part = ctx->attn_part;
+      a.ws_count = ctx->attn_count;
+      a.n_splits = ctx->attn_splits;
+      a.err = ctx->err;
+      if ((s = launch_attn(a, st, true)) != MIE_OK) return s;
+      ++n;
+    }
+    {  // x += Wo att
+      GemvArgs a;
+      a.m = L.o;
+      a.x = ctx->att;
+      a.act_bf16 = c.act_bf16;
+      a.y = ctx->x;
+      if ((s = launch_gemv(PRO_PLAIN, EPI_RESID, a, gemv_default_grid(a.m, EPI_RESID), st, true)) != MIE_OK) return s;
+      ++n;
+    }
+    {  // act = silu(Wg n(x)) * (Wu n(x))
+      GemvArgs a;
+      a.m = L.gu;
+      a.x = ctx->x;
+      a.gain = L.mlp_norm;
+      a.eps = c.rms_eps;
+      a.act_bf16 = c.act_bf16;
+      a.y = ctx->act;
+      if ((s = launch_gemv(PRO_NORM, EPI_SWIGLU, a, gemv_default_grid(a.m, EPI_SWIGLU), st, true)) != MIE_OK) return s;
+      ++n;
+    }
+    {  // x += Wd act
+      GemvArgs a;
+      a.m = L.down;
+      a.x = ctx->act;
+      a.act_bf16 = c.act_bf16;
+      a.y = ctx->x;
+      if ((s = launch_gemv(PRO_PLAIN, EPI_RESID, a, gemv_default_grid(a.m, EPI_RESID), st, true)) != MIE_OK) return s;
+      ++n;
+    }
+  }
+  {  // logits = Whead n(x); argmax
+    GemvArgs a;
+    a.m = ctx->head;
+    a.x = ctx->x;
+    a.gain = ctx->final_norm;
+    a.eps = c.rms_eps;
+    a.act_bf16 = c.act_bf16;
+    a.y = nullptr;
+    a.am_part = ctx->am_part;
+    a.am_count = ctx->am_count;
+    a.sp = ctx->sp;
+    a.err = ctx->err;
+    if ((s = launch_gemv(PRO_NORM, EPI_ARGMAX, a, gemv_default_grid(a.m, EPI_ARGMAX), st, true)) != MIE_OK) return s;
+    ++n;
+  }
+  *launches = n;
+  return MIE_OK;
+}
+
+static mie_status capture(mie_ctx *ctx) {
+  if (ctx->graph) {
+    cudaGraphExecDestroy(ctx->graph);
+    ctx->graph = nullptr;
+  }
+  cudaGraph_t g = nullptr;
+  MIE_CUDA(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
+  int n = 0;
+  mie_status s = enqueue_step(ctx, &n);
+  cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
+  if (s != MIE_OK) {
+    if (g) cudaGraphDestroy(g);
+    return s;
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "decode step: cudaStreamEndCapture");
+  e = cudaGraphInstantiate(&ctx->graph, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) return cuda_fail(e, "decode step: cudaGraphInstantiate");
+  ctx->launches = n;
+  ctx->primed = true;
+  return MIE_OK;
+}
+
+extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, const int32_t *block_table,
+                                      int n_blocks, float *logits_out, int32_t *argmax_out) {
+  if (!ctx || !block_table) return fail(MIE_E_ARG, "mie_decode_step: null pointer");
+  const mie_config &c = ctx->cfg;
+  if (!all_loaded(ctx)) return fail(MIE_E_STATE, "mie_decode_step: not every weight is loaded");
+  if (token < 0 || token >= c.vocab) return fail(MIE_E_ARG, "mie_decode_step: token %d outside [0, %d)", token, c.vocab);
+  if (pos < 0 || pos >= c.max_pos) return fail(MIE_E_ARG, "mie_decode_step: pos %d outside [0, %d)", pos, c.max_pos);
+  if (n_blocks < 1 || pos / c.block_size >= n_blocks)
+    return fail(MIE_E_ARG, "mie_decode_step: pos %d needs more than %d blocks", pos, n_blocks);
+  StepParams &p = ctx->sp_host;
+  memset(&p, 0, sizeof p);
+  p.token[0] = token;
+  p.pos[0] = pos;
+  p.block_table = block_table;
+  p.max_blocks = n_blocks;
+  p.n_slots = 1;
+  p.logits_out = logits_out;
+  p.argmax_out = argmax_out;
+  p.advance = 1;
+  MIE_CUDA(cudaMemcpyAsync(ctx->sp, &p, sizeof p, cudaMemcpyHostToDevice, ctx->stream));
+  if (!ctx->primed) {
+    mie_status s = capture(ctx);
+    if (s != MIE_OK) return s;
+  }
+  MIE_CUDA(cudaGraphLaunch(ctx->graph, ctx->stream));
+  return MIE_OK;
+}
+
+extern "C" mie_status mie_decode_continue(mie_ctx *ctx, int n_steps) {
+  if (!ctx) return fail(MIE_E_ARG, "mie_decode_continue: null context");
+  if (!ctx->primed || !ctx->graph) return fail(MIE_E_STATE, "mie_decode_continue: call mie_decode_step first");
+  if (n_steps < 0) return fail(MIE_E_ARG, "mie_decode_continue: n_steps %d", n_steps);
+  for (int i = 0; i < n_steps; ++i) MIE_CUDA(cudaGraphLaunch(ctx->graph, ctx->stream));
+  return MIE_OK;
+}
+
+extern "C" mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int32_t *tokens, const int32_t *pos,
+                                            const int32_t *block_tables, int max_blocks, float *logits_out,
+                                            int32_t *argmax_out) {
+  (void)tokens; (void)pos; (void)block_tables; (void)max_blocks; (void)logits_out; (void)argmax_out;
+  if (!ctx) return fail(MIE_E_ARG, "mie_decode_step_slots: null context");
+  if (n_slots < 1 || n_slots > ctx->cfg.max_slots) return fail(MIE_E_ARG, "mie_decode_step_slots: n_slots %d", n_slots);
+  return fail(MIE_E_STATE, "mie_decode_step_slots: the batched step is not built yet");
+}
+
+extern "C" mie_status mie_sync(mie_ctx *ctx) {
+  if (!ctx) return fail(MIE_E_ARG, "mie_sync: null context");
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  int v = 0;
+  MIE_CUDA(cudaMemcpy(&v, ctx->err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (v) {
+    MIE_CUDA(cudaMemset(ctx->err, 0, sizeof(int)));
+    return fail(MIE_E_DEVICE, "decode step: device bounds check fired (code %d)", v);
+  }
+  return MIE_OK;
+}
+
+extern "C" int mie_step_launches(const mie_ctx *ctx) { return ctx ? ctx->launches : 0; }

@@ -13,12 +13,13 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SO = os.path.join(_HERE, "libmie_oracle.so")
+_SO = os.path.join(_HERE, f"libmie_oracle.{platform.machine()}.so")
 _lib = None
 
 FMT = {"bf16": 0, "i8": 1, "q4_0": 2, "f32": 3}

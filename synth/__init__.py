@@ -19,13 +19,14 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 from dataclasses import dataclass, field, replace
 
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SO = os.path.join(_HERE, "libsynth.so")
+_SO = os.path.join(_HERE, f"libsynth.{platform.machine()}.so")
 _lib = None
 
 

@@ -1,0 +1,142 @@
+"""The decode step on the GPU against the oracle (teacher-forced with the oracle's tokens).
+
+Tolerances: max |dlogit| <= 2e-2 * std(logits) per step, argmax identical wherever the
+oracle's top-2 margin exceeds 1e-2; K/V cache entries within one bf16 rounding step.
+"""
+import numpy as np
+import pytest
+
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+mie = pytest.importorskip("memory_bound_decode_dequant_gb300")
+from memory_bound_decode_dequant_gb300.workload import build_gpu_model, prompt_tokens  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    torch.cuda.set_device(0)
+    mie.lib()
+
+
+def check_logits(got, ref, pos):
+    tol = 2e-2 * float(np.std(ref))
+    err = float(np.max(np.abs(got.astype(np.float64) - ref)))
+    assert err <= tol, f"pos {pos}: max |dlogit| {err:.3e} > {tol:.3e}"
+
+
+def check_argmax(got_best, ref, pos):
+    top = np.sort(ref)[-2:]
+    if top[1] - top[0] > 1e-2:
+        assert got_best == int(np.argmax(ref)), f"pos {pos}: argmax {got_best} vs {int(np.argmax(ref))}"
+
+
+def run_parity(orc, shape, layers, n_prompt, n_gen, perm_seed=5, compare_kv=True):
+    bs = shape.block_size
+    n_tok = n_prompt + n_gen
+    n_blocks = (n_tok + bs - 1) // bs + 3
+    max_pos = n_blocks * bs
+    om = orc.Model(shape, n_kv_blocks=n_blocks, max_pos=max_pos, layers=layers)
+    gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos, layers=layers)
+    bt = synth.permutation(perm_seed, n_blocks).astype(np.int32)
+    btd = torch.from_numpy(bt).cuda()
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    toks = list(prompt_tokens(shape, n_prompt))
+    for pos in range(n_tok):
+        ref, best = om.decode_step(int(toks[pos]), pos, bt)
+        gm.decode_step(int(toks[pos]), pos, btd, logits, am)
+        gm.sync()
+        check_logits(logits.cpu().numpy(), ref, pos)
+        check_argmax(int(am.item()), ref, pos)
+        if pos + 1 >= len(toks):
+            toks.append(best)  # teacher forcing with the oracle's greedy token
+    if compare_kv:
+        used = bt[: (n_tok + bs - 1) // bs]
+        g = gm.kv().cpu().numpy().view(np.uint16)[used]
+        r = om.kv()[used]
+        gf = orc.from_bf16(g).astype(np.float64)
+        rf = orc.from_bf16(r).astype(np.float64)
+        # entries past n_tok are untouched zeros on both sides
+        assert np.all(np.abs(gf - rf) <= np.abs(rf) * 2.0 ** -7 + 1e-6)
+        exact = float(np.mean(g == r))
+        assert exact > 0.97, f"only {exact:.3f} of the K/V bf16 values are identical"
+    return gm, om
+
+
+def test_tiny_q4_0_prompt_and_greedy(orc):
+    """64 prompt tokens + 16 greedy steps of the tiny Q4_0 decoder (K = 688 ragged)."""
+    run_parity(orc, synth.TINY, None, 64, 16)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0"])
+def test_llama32_shape_two_layers(orc, fmt):
+    """Llama-3.2-1B shapes (every GEMV and the LM head at full size), 2 of 16 layers."""
+    run_parity(orc, synth.llama32_1b(fmt), 2, 5, 2)
+
+
+def test_tinyllama_shape_bf16_activations(orc):
+    """TinyLlama shapes, Q4_0, bf16 GEMV inputs, 2 of 22 layers."""
+    run_parity(orc, synth.TINYLLAMA, 2, 4, 2)
+
+
+def test_llama32_full_depth_bf16(orc):
+    """All 16 layers of the bf16 Llama-3.2-1B shape, the bench's configuration."""
+    run_parity(orc, synth.LLAMA32_1B, None, 2, 1, compare_kv=False)
+
+
+def test_device_continuation_matches_host_steps(orc):
+    """mie_decode_continue (token and position advanced on the device) gives the same
+    bits as host-driven steps fed the previous argmax."""
+    shape = synth.TINY
+    n_blocks, max_pos = 8, 128
+    bt = torch.from_numpy(synth.permutation(9, n_blocks).astype(np.int32)).cuda()
+    outs = []
+    for mode in ("host", "device"):
+        gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+        logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+        am = torch.empty(1, dtype=torch.int32, device="cuda")
+        toks = prompt_tokens(shape, 10)
+        for pos, t in enumerate(toks):
+            gm.decode_step(int(t), pos, bt, logits, am)
+        if mode == "host":
+            pos = len(toks)
+            for _ in range(12):
+                gm.sync()
+                gm.decode_step(int(am.item()), pos, bt, logits, am)
+                pos += 1
+        else:
+            gm.decode_continue(12)
+        gm.sync()
+        outs.append((logits.cpu().numpy(), int(am.item())))
+        gm.close()
+    assert np.array_equal(outs[0][0].view(np.uint32), outs[1][0].view(np.uint32))
+    assert outs[0][1] == outs[1][1]
+
+
+def test_step_rejects_bad_inputs():
+    shape = synth.TINY
+    gm = build_gpu_model(shape, n_kv_blocks=4, max_pos=64)
+    bt = torch.tensor([3, 1, 99, 0], dtype=torch.int32, device="cuda")
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    with pytest.raises(mie.MieError) as e:
+        gm.decode_step(shape.vocab, 0, bt, logits)
+    assert e.value.status == 1
+    with pytest.raises(mie.MieError) as e:
+        gm.decode_step(1, 64, bt, logits)
+    assert e.value.status == 1
+    gm.decode_step(1, 3, bt, logits)
+    gm.sync()
+    gm.decode_step(1, 35, bt, logits)  # block 99 is outside the 4-block pool
+    with pytest.raises(mie.MieError) as e:
+        gm.sync()
+    assert e.value.status == 7
+    gm.sync()  # the flag was cleared
+    empty = mie.Model(gm.cfg)
+    with pytest.raises(mie.MieError) as e:
+        empty.decode_step(1, 0, bt, logits)
+    assert e.value.status == 6
