@@ -81,7 +81,8 @@ mie_status mie_quantize_i8(const float *w, int M, int K, int8_t *q, float *scale
 mie_status mie_quantize_q4_0(const float *w, int M, int K, uint8_t *blocks, void *stream);
 
 /* Size of the GPU layout of an M x K Q4_0 matrix: a nibble plane [M][nb][16] followed,
- * at the next 256-byte boundary, by a scale plane [M][nb] of f16 (nb = ceil(K/32)). */
+ * at the next 256-byte boundary, by a scale plane [M][nbp] of f16, nb = ceil(K/32),
+ * nbp = nb rounded up to a multiple of 8 (the extra scales are zero). */
 size_t mie_q4_0_packed_bytes(int M, int K);
 
 /* Canonical blocks (device) -> GPU layout (device, mie_q4_0_packed_bytes(M, K) bytes). */

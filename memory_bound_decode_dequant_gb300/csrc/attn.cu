@@ -6,30 +6,35 @@
 // the partial softmaxes are merged; "Writing an LLM inference engine from scratch in
 // Rust", Lesson 4: an online softmax with a running maximum and sum).
 //
-// Grid (splits, KV heads), 128 threads.  A CTA walks its share of the context in
-// steps of 32/LPT tokens (LPT = head_dim/32 lanes per token): each lane loads 32
-// dims (64 bytes) of one key, dots it with every query head of the group, and the
-// lanes of a token combine with one shuffle.  Each warp keeps an online softmax per
-// head; values are accumulated with each lane owning head_dim/32 dims, loading them
-// coalesced across the warp.  Warps merge in shared memory, CTAs write (m, l, o)
-// partials, and the last CTA of each KV head to finish (an atomic counter, no
-// waiting) merges the splits and resets the counter for the next launch.
+// Grid (splits, KV heads), 128 threads; the number of splits in use follows the
+// context (at least 4 blocks each).  A CTA stages the block ids of its split in shared
+// memory, then each warp takes groups of 32/LPT tokens (LPT = head_dim/32 lanes per
+// token) and issues all of a group's loads before any math: 64 bytes of one key per
+// lane, plus the lane's head_dim/32 value dims of every token in the group.  Each
+// key is dotted with every query head of the group (one K/V read serves them all),
+// the LPT lanes of a token combine with a shuffle, and each warp keeps an online
+// softmax per head.  Warps merge in shared memory; with one split the CTA writes the
+// result, otherwise CTAs write (m, l, o) partials and the last CTA of each KV head to
+// finish (an atomic counter, no waiting) merges them and resets the counter.
 #include "internal.h"
 
 namespace mie {
 
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = kAttnThreads / 32;
+constexpr int kAttnMaxBlocks = 256;     // block ids staged in shared memory at a time
+constexpr int kAttnBlocksPerSplit = 4;  // one block per warp per split, at least
 
 __device__ int g_device_error;  // latched by the stateless kernels of this device
 
 template <int G, int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
-  constexpr int LPT = HD / 32;          // lanes per token
+  constexpr int LPT = HD / 32;          // lanes per token (each lane dots 32 dims)
   constexpr int TPI = 32 / LPT;         // tokens per warp iteration
   constexpr int DPL = HD / 32;          // value dims per lane
   constexpr int PART = G * (2 + HD);    // floats of one (head group, split) partial
   __shared__ __align__(16) float q_s[G * HD];
+  __shared__ int s_blk[kAttnMaxBlocks];
   __shared__ float w_m[kAttnWarps][G], w_l[kAttnWarps][G];
   __shared__ float w_o[kAttnWarps][G][HD];
   __shared__ unsigned s_last;
@@ -58,14 +63,13 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   }
   if (ctx < 0) ctx = 0;
   const int nblk = (ctx + a.bs - 1) / a.bs;
-  const int nsplit = max(1, min(a.n_splits, nblk));
+  // at least kAttnBlocksPerSplit blocks per split, so every warp has a block to read
+  const int nsplit = max(1, min(a.n_splits, (nblk + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit));
   if (s >= nsplit) return;
-  // this split's positions: whole blocks [b0, b1)
   const int b0 = (int)((int64_t)s * nblk / nsplit), b1 = (int)((int64_t)(s + 1) * nblk / nsplit);
-  const int t0 = b0 * a.bs, t1 = min(b1 * a.bs, ctx);
+  const int t_end = min(b1 * a.bs, ctx);
 
   for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) q_s[i] = a.q[(g * G) * HD + i];
-  __syncthreads();
 
   float m[G], l[G], o[G][DPL];
 #pragma unroll
@@ -78,21 +82,59 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
   const int tok_in = lane / LPT, part_in = lane % LPT;
   const int64_t head_off = (int64_t)g * a.bs * HD;
 
-  for (int tb = t0 + warp * TPI; tb < t1; tb += kAttnWarps * TPI) {
-    const int t = tb + tok_in;
-    const bool valid = t < t1;
-    float sc[G];
-    if (valid) {
-      int blk = bt[t / a.bs];
+  // the split's blocks, staged kAttnMaxBlocks at a time (one coalesced load each)
+  for (int cb = b0; cb < b1; cb += kAttnMaxBlocks) {
+    const int ce = min(b1, cb + kAttnMaxBlocks);
+    __syncthreads();
+    for (int i = threadIdx.x; i < ce - cb; i += kAttnThreads) {
+      int blk = bt[cb + i];
       if (blk < 0 || blk >= a.n_pool_blocks) {
         latch_error(a.err, ERR_BLOCK_ID);
         blk = -1;
       }
-      if (blk >= 0) {
-        const uint16_t *kp = a.k + (int64_t)blk * a.block_stride + head_off + (int64_t)(t % a.bs) * HD + part_in * 32;
-        uint4 kv[4];
+      s_blk[i] = blk;
+    }
+    __syncthreads();
+    const int t0 = cb * a.bs, t1 = min(ce * a.bs, t_end);
+    for (int tb = t0 + warp * TPI; tb < t1; tb += kAttnWarps * TPI) {
+      const int nt = min(TPI, t1 - tb);
+      // issue every load of this token group first: my key slice, then my value dims
+      const int t = tb + tok_in;
+      const int kblk = (t < t1) ? s_blk[t / a.bs - cb] : -1;
+      uint4 kv[4];
+      if (kblk >= 0) {
+        const uint16_t *kp = a.k + (int64_t)kblk * a.block_stride + head_off + (int64_t)(t % a.bs) * HD + part_in * 32;
 #pragma unroll
         for (int i = 0; i < 4; ++i) kv[i] = *reinterpret_cast<const uint4 *>(kp + 8 * i);
+      }
+      float vf[TPI][DPL];
+#pragma unroll
+      for (int i = 0; i < TPI; ++i) {
+        const int t2 = tb + i;
+        const int vblk = (i < nt) ? s_blk[t2 / a.bs - cb] : -1;
+        if (vblk >= 0) {
+          const uint16_t *vp = a.v + (int64_t)vblk * a.block_stride + head_off + (int64_t)(t2 % a.bs) * HD + lane * DPL;
+          if constexpr (DPL == 1) {
+            vf[i][0] = bf16_bits_to_f32(*vp);
+          } else if constexpr (DPL == 2) {
+            const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
+            vf[i][0] = __uint_as_float(w << 16);
+            vf[i][1] = __uint_as_float(w & 0xffff0000u);
+          } else {
+            const uint2 w = *reinterpret_cast<const uint2 *>(vp);
+            vf[i][0] = __uint_as_float(w.x << 16);
+            vf[i][1] = __uint_as_float(w.x & 0xffff0000u);
+            vf[i][2] = __uint_as_float(w.y << 16);
+            vf[i][3] = __uint_as_float(w.y & 0xffff0000u);
+          }
+        } else {
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) vf[i][d] = 0.f;
+        }
+      }
+      // scores of my token for every query head of the group
+      float sc[G];
+      if (kblk >= 0) {
         float kf[32];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -116,64 +158,39 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
         }
       } else {
 #pragma unroll
-        for (int h = 0; h < G; ++h) sc[h] = -INFINITY;
-      }
-    } else {
-#pragma unroll
-      for (int h = 0; h < G; ++h) sc[h] = -INFINITY;
-    }
-    // combine the LPT lanes of a token
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-#pragma unroll
-      for (int off = 1; off < LPT; off <<= 1) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
-      sc[h] = (sc[h] == -INFINITY) ? -INFINITY : sc[h] * a.scale;
-    }
-    // online softmax update per head
-    float p[G];
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float bm = warp_max(sc[h]);
-      const float mn = fmaxf(m[h], bm);
-      if (mn == -INFINITY) {
-        p[h] = 0.f;
-        continue;
-      }
-      const float corr = expf(m[h] - mn);  // 0 when m was -inf
-      p[h] = (sc[h] == -INFINITY) ? 0.f : expf(sc[h] - mn);
-      // every token's score is held by LPT lanes: count it once
-      const float ps = warp_sum(part_in == 0 ? p[h] : 0.f);
-      l[h] = l[h] * corr + ps;
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) o[h][d] *= corr;
-      m[h] = mn;
-    }
-    // values: lane owns dims lane*DPL .. +DPL of every token in the group
-    const int nt = min(TPI, t1 - tb);
-    for (int i = 0; i < nt; ++i) {
-      const int t2 = tb + i;
-      const int blk = bt[t2 / a.bs];
-      if (blk < 0 || blk >= a.n_pool_blocks) continue;
-      const uint16_t *vp = a.v + (int64_t)blk * a.block_stride + head_off + (int64_t)(t2 % a.bs) * HD + lane * DPL;
-      float vf[DPL];
-      if constexpr (DPL == 1) {
-        vf[0] = bf16_bits_to_f32(*vp);
-      } else if constexpr (DPL == 2) {
-        const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
-        vf[0] = __uint_as_float(w << 16);
-        vf[1] = __uint_as_float(w & 0xffff0000u);
-      } else {
-        const uint2 w = *reinterpret_cast<const uint2 *>(vp);
-        vf[0] = __uint_as_float(w.x << 16);
-        vf[1] = __uint_as_float(w.x & 0xffff0000u);
-        vf[2] = __uint_as_float(w.y << 16);
-        vf[3] = __uint_as_float(w.y & 0xffff0000u);
+        for (int h = 0; h < G; ++h) sc[h] = 0.f;
       }
 #pragma unroll
       for (int h = 0; h < G; ++h) {
-        const float ph = __shfl_sync(0xffffffffu, p[h], i * LPT);
 #pragma unroll
-        for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(ph, vf[d], o[h][d]);
+        for (int off = 1; off < LPT; off <<= 1) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+        sc[h] = (kblk >= 0) ? sc[h] * a.scale : -INFINITY;
+      }
+      // online softmax: rescale the running sums to the new maximum
+      float p[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mn = fmaxf(m[h], warp_max(sc[h]));
+        if (mn == -INFINITY) {
+          p[h] = 0.f;
+          continue;
+        }
+        const float corr = expf(m[h] - mn);  // 0 while m was -inf
+        p[h] = (sc[h] == -INFINITY) ? 0.f : expf(sc[h] - mn);
+        const float ps = warp_sum(part_in == 0 ? p[h] : 0.f);  // each token counted once
+        l[h] = l[h] * corr + ps;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[h][d] *= corr;
+        m[h] = mn;
+      }
+#pragma unroll
+      for (int i = 0; i < TPI; ++i) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float ph = __shfl_sync(0xffffffffu, p[h], i * LPT);
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(ph, vf[i][d], o[h][d]);
+        }
       }
     }
   }
@@ -188,6 +205,21 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
 #pragma unroll
     for (int d = 0; d < DPL; ++d) w_o[warp][h][lane * DPL + d] = o[h][d];
   __syncthreads();
+  if (nsplit == 1) {  // the only split: write the result directly
+    for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
+      const int h = i / HD, d = i % HD;
+      float M = -INFINITY;
+      for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, w_m[w][h]);
+      float O = 0.f, L = 0.f;
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float f = (w_m[w][h] == -INFINITY) ? 0.f : expf(w_m[w][h] - M);
+        O = fmaf(w_o[w][h][d], f, O);
+        L = fmaf(w_l[w][h], f, L);
+      }
+      a.out[(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
+    }
+    return;
+  }
   float *part = a.ws_part + ((int64_t)g * a.n_splits + s) * PART;
   for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
     const int h = i / HD, d = i % HD;

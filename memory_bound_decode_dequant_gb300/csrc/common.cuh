@@ -70,7 +70,7 @@ __device__ __forceinline__ void latch_error(int *flag, int code) {
 }
 
 // Device error codes latched by bounds checks.
-enum : int { ERR_BLOCK_ID = 1, ERR_POS = 2, ERR_TOKEN = 4 };
+enum : int { ERR_BLOCK_ID = 1, ERR_POS = 2, ERR_TOKEN = 4, ERR_TIMEOUT = 8 };
 
 // ----------------------------------------------------------------- step parameters
 

@@ -6,12 +6,17 @@
 // dequant in registers; "Writing an LLM inference engine from scratch in Rust",
 // Lesson 1: decode speed is set by how fast the weights stream from memory).
 //
-// Design (GB300): the weights are read exactly once, so the kernel is a stream of
-// 16-byte non-caching loads spread over all SMs.
-//  * A CTA owns a contiguous range of rows; each warp owns one 2048-column slice of
-//    K and walks its rows.  The warp's slice of the (normalised) input vector sits in
-//    64 registers per lane for the whole kernel, so the inner loop reads no shared
-//    memory: per 16-byte chunk it is loads, in-register unpack and packed fp32x2 FMAs.
+// Design (GB300): the weights are read exactly once, so the kernel is a stream.
+//  * One CTA per SM owns a contiguous range of rows.  A producer warp streams that
+//    range through a ring of shared-memory stages with TMA bulk copies
+//    (cp.async.bulk, completion on mbarriers, L2 evict-first), so tens of KB per SM
+//    are in flight without holding registers.  It issues the first ring-full before
+//    griddepcontrol.wait: inside the step graph the weights of kernel N+1 stream in
+//    while kernel N finishes.
+//  * Each consumer warp owns one 2048-column slice of K; its slice of the normalised
+//    input vector sits in 64 registers per lane for the whole kernel, so per 16-byte
+//    chunk the inner loop is one shared-memory load, an in-register unpack and packed
+//    fp32x2 FMAs.
 //  * Unpack without int->float conversions: a code is moved into the mantissa of
 //    2^23 by one LOP3 (Q4_0) or PRMT (int8), and one packed fp32x2 add removes both
 //    the 2^23 and the stored bias (+8 for Q4_0, +128 after flipping the int8 sign
@@ -20,8 +25,8 @@
 //  * Rows of a CTA are reduced across lanes with shuffles and across K slices through
 //    shared memory in a fixed order, then an epilogue applies the row scale and the
 //    fused operation (residual add, SwiGLU, RoPE + paged K/V write, argmax).
-//  * The first rows' weight loads are issued before griddepcontrol.wait, so inside
-//    the step graph they overlap the previous kernel's tail.
+//  * Every mbarrier wait is bounded; a wait that gives up latches an error, drains
+//    the copies still in flight and leaves the kernel.
 #include <cstdarg>
 #include <cstdio>
 
@@ -29,16 +34,19 @@
 
 namespace mie {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kCWarps = 8;                    // consumer warps
+constexpr int kThreads = 32 * (kCWarps + 1);  // + one producer warp
+constexpr int kMaxStages = 16;
+constexpr size_t kSmemBudget = 110 * 1024;    // two such CTAs fit on one SM
+constexpr size_t kSmemMax = 200 * 1024;
 
 template <int F> struct FmtT;
-// EPC: elements per 16-byte chunk; CPL: chunks per lane per slice; U: rows in flight.
-template <> struct FmtT<MIE_FMT_BF16> { static constexpr int EPC = 8, CPL = 8, U = 1; };
-template <> struct FmtT<MIE_FMT_I8> { static constexpr int EPC = 16, CPL = 4, U = 2; };
-template <> struct FmtT<MIE_FMT_Q4_0> { static constexpr int EPC = 32, CPL = 2, U = 3; };
+// EPC: elements per 16-byte chunk; CPL: chunks per lane per 2048-column slice.
+template <> struct FmtT<MIE_FMT_BF16> { static constexpr int EPC = 8, CPL = 8; };
+template <> struct FmtT<MIE_FMT_I8> { static constexpr int EPC = 16, CPL = 4; };
+template <> struct FmtT<MIE_FMT_Q4_0> { static constexpr int EPC = 32, CPL = 2; };
 constexpr int kSlice = 2048;  // = 32 * EPC * CPL for every format
-constexpr int kMaxK = kSlice * kWarps;
+constexpr int kMaxK = kSlice * kCWarps;
 
 int gemv_chunk_elems(int fmt) {
   return fmt == MIE_FMT_BF16 ? 8 : fmt == MIE_FMT_I8 ? 16 : fmt == MIE_FMT_Q4_0 ? 32 : 0;
@@ -66,10 +74,9 @@ __device__ __forceinline__ float embed_at(const DevMat &m, int row, int k) {
     const int8_t q = reinterpret_cast<const int8_t *>(m.w + (int64_t)row * m.row_bytes)[k];
     return reinterpret_cast<const float *>(m.s)[row] * (float)q;
   } else {
-    const int nb = m.kp / 32;
     const uint8_t byte = m.w[(int64_t)row * m.row_bytes + (k >> 5) * 16 + (k & 15)];
     const int code = ((k & 31) < 16) ? (byte & 0xF) : (byte >> 4);
-    const float h = __half2float(reinterpret_cast<const __half *>(m.s)[(int64_t)row * nb + (k >> 5)]);
+    const float h = __half2float(reinterpret_cast<const __half *>(m.s)[(int64_t)row * m.s_stride + (k >> 5)]);
     return h * (float)(code - 8);
   }
 }
@@ -156,117 +163,197 @@ __device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr) {
   }
 }
 
+// --------------------------------------------------------------- mbarrier / bulk copy
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Waits for the phase of the given parity to complete; gives up after a bounded number
+// of polls (each poll may suspend the thread for a hardware-defined time) and returns
+// false, so a lost transfer can never hang the GPU.
+constexpr long kWaitPolls = 1L << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  for (long it = 0; it < kWaitPolls; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// One bulk (TMA 1-D) copy global -> shared, completing on an mbarrier; weights are
+// streamed once, so they are marked evict-first in L2.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Barrier over the consumer warps only (the producer warp never joins it).
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory"); }
+
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
 // --------------------------------------------------------------- the kernel
+//
+// One CTA per SM: warp kCWarps is the producer, warps 0..kCWarps-1 consume.  A stage
+// is RPS whole rows of the CTA's (contiguous) row range, RPS = kCWarps / KS, so each
+// consumer warp reduces one 2048-column slice of one row per stage.  The producer
+// issues the first ring-full of stages before any dependency wait.
 
 template <int F, int PRO, int EPI>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
   using T = FmtT<F>;
-  constexpr int EPC = T::EPC, CPL = T::CPL, U = T::U;
+  constexpr int EPC = T::EPC, CPL = T::CPL;
   constexpr int RU = (EPI == EPI_SWIGLU || EPI == EPI_QKV) ? 2 : 1;
-  extern __shared__ __align__(16) float smem[];
-  __shared__ float red[kWarps];
+  constexpr int kBitsPerElem = (F == MIE_FMT_BF16) ? 16 : (F == MIE_FMT_I8 ? 8 : 4);
+  constexpr int kSliceBytes = kSlice * kBitsPerElem / 8;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
+  __shared__ float red[kCWarps];
   __shared__ float s_scale;
-  __shared__ float s_bv[kWarps];
-  __shared__ int s_bi[kWarps];
+  __shared__ float s_bv[kCWarps];
+  __shared__ int s_bi[kCWarps];
   __shared__ unsigned s_last;
+  __shared__ volatile int s_abort, s_issued, s_prod_done;
+  __shared__ int s_abort_final;
 
   pdl_trigger();
 
   const DevMat &m = a.m;
   const int Kp = m.kp, K = m.cols, M = m.rows;
   const int KS = (Kp + kSlice - 1) / kSlice;
-  float *xs = smem;       // [Kp] staged input vector
-  float *part = smem + Kp; // [rows of this CTA][KS]
+  const int RPS = KS >= kCWarps ? 1 : kCWarps / KS;
+  const int NST = a.n_stages;
+  const uint32_t stage_bytes = a.stage_bytes, sc_bytes = a.sc_stage_bytes;
+  uint8_t *ring = smem_raw;
+  uint8_t *sring = ring + (size_t)NST * stage_bytes;
+  float *xs = reinterpret_cast<float *>(sring + (size_t)NST * sc_bytes);  // [Kp]
+  float *part = xs + Kp;                                                   // [rows][KS]
 
   const int n_units = (M + RU - 1) / RU;
   const int u0 = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
   const int u1 = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
   const int row0 = u0 * RU, row1 = min(u1 * RU, M);
+  const int n_stages = (row1 - row0 + RPS - 1) / RPS;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ks = warp % KS, rw = warp / KS, nrw = kWarps / KS;
-  const int nrows_w = (row1 - row0 > rw) ? (row1 - row0 - rw + nrw - 1) / nrw : 0;
-
-  // element offset of this lane's chunk c within a row
-  const int e0 = ks * kSlice + lane * EPC;
-  constexpr int kChunkStride = 32 * EPC;
-  constexpr int kBitsPerElem = (F == MIE_FMT_BF16) ? 16 : (F == MIE_FMT_I8 ? 8 : 4);
-
-  uint4 wbuf[U][CPL];
-  float hbuf[U][CPL];
-  auto issue = [&](int j, int slot) {
-    if (j < nrows_w) {
-      const int r = row0 + rw + j * nrw;
-      const uint8_t *row = m.w + (int64_t)r * m.row_bytes;
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        const int e = e0 + c * kChunkStride;
-        if (e < Kp) {
-          wbuf[slot][c] = ldg_stream(row + (int64_t)e * kBitsPerElem / 8);
-          if constexpr (F == MIE_FMT_Q4_0)
-            hbuf[slot][c] = __half2float(__ushort_as_half(
-                ldg_u16(reinterpret_cast<const __half *>(m.s) + (int64_t)r * (Kp / 32) + (e >> 5))));
-        } else {
-          wbuf[slot][c] = make_uint4(0, 0, 0, 0);
-          hbuf[slot][c] = 0.f;
-        }
-      }
-    }
-  };
-#pragma unroll
-  for (int u = 0; u < U; ++u) issue(u, u);
-
-  pdl_wait();
-
-  // ---------------------------------------------------------------- prologue
   const int tid = threadIdx.x;
+
+  if (tid == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kCWarps);
+    }
+    s_abort = 0;
+    s_issued = 0;
+    s_prod_done = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  // ---------------------------------------------------------------- producer
+  if (warp == kCWarps) {
+    if (lane == 0) {
+      const uint64_t pol = evict_first_policy();
+      for (int s = 0; s < n_stages; ++s) {
+        const int slot = s % NST, k = s / NST;
+        if (k > 0 && !mbar_wait(&empty_bar[slot], (k - 1) & 1)) {
+          s_abort = 1;
+          latch_error(a.err, ERR_TIMEOUT);
+          break;
+        }
+        if (s_abort) break;
+        const int r = row0 + s * RPS;
+        const int nr = min(RPS, row1 - r);
+        const uint32_t wb = (uint32_t)(nr * m.row_bytes);
+        const uint32_t sb = (F == MIE_FMT_Q4_0) ? (uint32_t)(nr * m.s_stride * 2) : 0u;
+        mbar_expect_tx(&full_bar[slot], wb + sb);
+        bulk_load(ring + (size_t)slot * stage_bytes, m.w + (int64_t)r * m.row_bytes, wb, &full_bar[slot], pol);
+        if constexpr (F == MIE_FMT_Q4_0)
+          bulk_load(sring + (size_t)slot * sc_bytes,
+                    reinterpret_cast<const uint8_t *>(m.s) + (int64_t)r * m.s_stride * 2, sb, &full_bar[slot], pol);
+        s_issued = s + 1;
+      }
+      s_prod_done = 1;
+    }
+    return;
+  }
+
+  // ---------------------------------------------------------------- consumers
+  pdl_wait();
   if constexpr (PRO == PRO_EMBED_NORM) {
     int tok = a.sp ? a.sp->token[a.slot] : 0;
     if (tok < 0 || tok >= a.vocab) {
       if (tid == 0 && blockIdx.x == 0) latch_error(a.err, ERR_TOKEN);
       tok = 0;
     }
-    for (int k = tid; k < Kp; k += kThreads) {
+    for (int k = tid; k < Kp; k += kCWarps * 32) {
       const float v = (k < K) ? embed_at(a.embed, tok, k) : 0.f;
       xs[k] = v;
       if (blockIdx.x == 0 && k < K) a.x_store[k] = v;
     }
   } else {
-    for (int k = tid; k < Kp; k += kThreads) xs[k] = (k < K) ? a.x[k] : 0.f;
+    for (int k = tid; k < Kp; k += kCWarps * 32) xs[k] = (k < K) ? a.x[k] : 0.f;
   }
   if constexpr (PRO != PRO_PLAIN) {
     float ss = 0.f;
-    for (int k = tid; k < K; k += kThreads) ss += xs[k] * xs[k];
+    for (int k = tid; k < K; k += kCWarps * 32) ss += xs[k] * xs[k];
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
-    __syncthreads();
+    consumer_sync();
     if (tid == 0) {
       float t = 0.f;
-      for (int w = 0; w < kWarps; ++w) t += red[w];
+      for (int w = 0; w < kCWarps; ++w) t += red[w];
       s_scale = 1.0f / sqrtf(t / (float)K + a.eps);
     }
-    __syncthreads();
+    consumer_sync();
     const float r = s_scale;
-    for (int k = tid; k < K; k += kThreads) {
+    for (int k = tid; k < K; k += kCWarps * 32) {
       float v = xs[k] * r * a.gain[k];
       if (a.act_bf16) v = round_bf16(v);
       xs[k] = v;
     }
   } else {
     if (a.act_bf16)
-      for (int k = tid; k < K; k += kThreads) xs[k] = round_bf16(xs[k]);
+      for (int k = tid; k < K; k += kCWarps * 32) xs[k] = round_bf16(xs[k]);
   }
-  __syncthreads();
+  consumer_sync();
 
-  // ---------------------------------------------------------------- main loop
+  const int ri = warp / KS, ks = warp % KS;
+  const bool has_slice = warp < RPS * KS;
+  const int e0 = ks * kSlice + lane * EPC;
+  constexpr int kChunkStride = 32 * EPC;
   float2 xr[CPL * EPC / 2];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {
     const int e = e0 + c * kChunkStride;
-    if (e < Kp) {
+    if (has_slice && e < Kp) {
       load_xr<F>(xs, e, xr + c * (EPC / 2));
     } else {
 #pragma unroll
@@ -274,54 +361,82 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     }
   }
 
-  for (int j0 = 0; j0 < nrows_w; j0 += U) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
-      const int j = j0 + u;
-      if (j < nrows_w) {
-        float sum = 0.f;
-        if constexpr (F == MIE_FMT_Q4_0) {
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) {
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            chunk_fma<F>(wbuf[u][c], xr + c * (EPC / 2), acc);
-            const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-            sum = fmaf(hbuf[u][c], cs, sum);
-          }
-        } else {
-          float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) chunk_fma<F>(wbuf[u][c], xr + c * (EPC / 2), acc);
-          sum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-        }
-        issue(j + U, u);
-        sum = warp_sum(sum);
-        if (lane == 0) part[(rw + j * nrw) * KS + ks] = sum;
-      }
+  int consumed = 0;
+  for (int s = 0; s < n_stages; ++s) {
+    const int slot = s % NST, k = s / NST;
+    if (!mbar_wait(&full_bar[slot], k & 1)) {
+      s_abort = 1;
+      latch_error(a.err, ERR_TIMEOUT);
+      break;
     }
+    consumed = s + 1;
+    const int r = row0 + s * RPS + ri;
+    if (has_slice && r < row1) {
+      const uint8_t *rowp = ring + (size_t)slot * stage_bytes + (size_t)ri * m.row_bytes + (size_t)ks * kSliceBytes;
+      float sum = 0.f;
+      if constexpr (F == MIE_FMT_Q4_0) {
+        const __half *hs = reinterpret_cast<const __half *>(sring + (size_t)slot * sc_bytes) + (size_t)ri * m.s_stride +
+                           ks * (kSlice / 32);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          if (e0 + c * kChunkStride < Kp) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(rowp + (size_t)(c * 32 + lane) * 16);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            chunk_fma<F>(w, xr + c * (EPC / 2), acc);
+            const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+            sum = fmaf(__half2float(hs[c * 32 + lane]), cs, sum);
+          }
+        }
+      } else {
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          if (e0 + c * kChunkStride < Kp) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(rowp + (size_t)(c * 32 + lane) * 16);
+            chunk_fma<F>(w, xr + c * (EPC / 2), acc);
+          }
+        }
+        sum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) part[(r - row0) * KS + ks] = sum;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty_bar[slot]);
   }
-  __syncthreads();
+  consumer_sync();
+  if (tid == 0) s_abort_final = s_abort;
+  consumer_sync();
+  if (s_abort_final) {
+    // a wait gave up: make sure no bulk copy is still writing into shared memory
+    if (tid == 0) {
+      for (long it = 0; it < kWaitPolls && !s_prod_done; ++it) __nanosleep(64);
+      const int issued = s_issued;
+      for (int s = max(consumed, issued - NST); s < issued; ++s) mbar_wait(&full_bar[s % NST], (s / NST) & 1);
+    }
+    return;
+  }
 
   // ---------------------------------------------------------------- epilogue
   auto row_value = [&](int r) {
     float v = 0.f;
-    for (int s = 0; s < KS; ++s) v += part[(r - row0) * KS + s];
+    for (int q = 0; q < KS; ++q) v += part[(r - row0) * KS + q];
     if constexpr (F == MIE_FMT_I8) v *= reinterpret_cast<const float *>(m.s)[r];
     return v;
   };
+  constexpr int kCT = kCWarps * 32;
 
   if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
-    for (int r = row0 + tid; r < row1; r += kThreads) {
+    for (int r = row0 + tid; r < row1; r += kCT) {
       const float v = row_value(r);
       if constexpr (EPI == EPI_STORE) a.y[r] = v;
       else a.y[r] = a.y[r] + v;
     }
   } else if constexpr (EPI == EPI_SWIGLU) {
     // packed rows 2i = gate_i, 2i+1 = up_i -> y_i = silu(gate_i) * up_i
-    for (int u = u0 + tid; u < u1; u += kThreads) {
+    for (int u = u0 + tid; u < u1; u += kCT) {
       const float g = row_value(2 * u), up = row_value(2 * u + 1);
-      float v = g / (1.0f + expf(-g)) * up;
-      a.y[u] = v;
+      a.y[u] = g / (1.0f + expf(-g)) * up;
     }
   } else if constexpr (EPI == EPI_QKV) {
     // packed rows 2p, 2p+1 = rows i and i + hd/2 of head h (p = h * hd/2 + i)
@@ -333,12 +448,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     if (pos_ok) blk = bt[pos / a.bs];
     const bool blk_ok = pos_ok && blk >= 0 && blk < a.n_kv_blocks;
     if (tid == 0 && blockIdx.x == 0 && !blk_ok) latch_error(a.err, pos_ok ? ERR_BLOCK_ID : ERR_POS);
-    for (int u = u0 + tid; u < u1; u += kThreads) {
+    for (int u = u0 + tid; u < u1; u += kCT) {
       const int h = u / h2, i = u % h2;
       float x0 = row_value(2 * u), x1 = row_value(2 * u + 1);
       if (h < a.Hq + a.Hkv && pos_ok) {
-        const float c = a.rope_cos[(int64_t)pos * h2 + i], s = a.rope_sin[(int64_t)pos * h2 + i];
-        const float r0 = x0 * c - x1 * s, r1 = x1 * c + x0 * s;
+        const float c = a.rope_cos[(int64_t)pos * h2 + i], sn = a.rope_sin[(int64_t)pos * h2 + i];
+        const float r0 = x0 * c - x1 * sn, r1 = x1 * c + x0 * sn;
         x0 = r0;
         x1 = r1;
       }
@@ -359,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     if (logits && a.sp && !a.y) logits += (int64_t)a.slot * M;
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    for (int r = row0 + tid; r < row1; r += kThreads) {
+    for (int r = row0 + tid; r < row1; r += kCT) {
       const float v = row_value(r);
       if (logits) logits[r] = v;
       if (better(v, r, bv, bi)) { bv = v; bi = r; }
@@ -371,20 +486,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
       if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
     if (lane == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
-    __syncthreads();
+    consumer_sync();
     if (tid == 0) {
-      for (int w = 1; w < kWarps; ++w)
+      for (int w = 1; w < kCWarps; ++w)
         if (better(s_bv[w], s_bi[w], bv, bi)) { bv = s_bv[w]; bi = s_bi[w]; }
       a.am_part[blockIdx.x] = make_float2(bv, __int_as_float(bi));
       __threadfence();
       s_last = (atomicAdd(a.am_count, 1u) == gridDim.x - 1);
     }
-    __syncthreads();
+    consumer_sync();
     if (s_last) {
       __threadfence();
       float fv = -INFINITY;
       int fi = 0x7fffffff;
-      for (int b = tid; b < (int)gridDim.x; b += kThreads) {
+      for (int b = tid; b < (int)gridDim.x; b += kCT) {
         const float2 p = __ldcg(a.am_part + b);
         if (better(p.x, __float_as_int(p.y), fv, fi)) { fv = p.x; fi = __float_as_int(p.y); }
       }
@@ -394,11 +509,11 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
         const int oi = __shfl_xor_sync(0xffffffffu, fi, o);
         if (better(ov, oi, fv, fi)) { fv = ov; fi = oi; }
       }
-      __syncthreads();
+      consumer_sync();
       if (lane == 0) { s_bv[warp] = fv; s_bi[warp] = fi; }
-      __syncthreads();
+      consumer_sync();
       if (tid == 0) {
-        for (int w = 1; w < kWarps; ++w)
+        for (int w = 1; w < kCWarps; ++w)
           if (better(s_bv[w], s_bi[w], fv, fi)) { fv = s_bv[w]; fi = s_bi[w]; }
         if (fi == 0x7fffffff) fi = 0;  // all values NaN: fall back to index 0
         if (a.am_out) a.am_out[a.slot] = fi;
@@ -417,28 +532,57 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 
 // --------------------------------------------------------------- launching
 
-template <int F, int PRO, int EPI>
-static mie_status launch_t(const GemvArgs &a, int grid, cudaStream_t st, bool pdl) {
-  const int RU = (EPI == EPI_SWIGLU || EPI == EPI_QKV) ? 2 : 1;
-  const int n_units = (a.m.rows + RU - 1) / RU;
-  const int KS = (a.m.kp + kSlice - 1) / kSlice;
+// Shared-memory plan of one launch: ring of n_stages stages plus the staged input and
+// the per-row partial sums, kept under kSmemBudget when possible so that a kernel and
+// its successor (prefetching under programmatic dependent launch) fit on one SM.
+struct Plan {
+  int grid, n_stages;
+  uint32_t stage_bytes, sc_bytes;
+  size_t smem;
+};
+
+static Plan make_plan(const DevMat &m, int epi, int grid) {
+  const int RU = (epi == EPI_SWIGLU || epi == EPI_QKV) ? 2 : 1;
+  const int n_units = (m.rows + RU - 1) / RU;
+  const int KS = (m.kp + kSlice - 1) / kSlice;
+  const int RPS = KS >= kCWarps ? 1 : kCWarps / KS;
   const int rows_max = ((n_units + grid - 1) / grid) * RU;
-  const size_t smem = sizeof(float) * ((size_t)a.m.kp + (size_t)rows_max * KS);
+  Plan p;
+  p.grid = grid;
+  p.stage_bytes = (uint32_t)((RPS * m.row_bytes + 127) / 128 * 128);
+  p.sc_bytes = m.fmt == MIE_FMT_Q4_0 ? (uint32_t)((RPS * m.s_stride * 2 + 127) / 128 * 128) : 0u;
+  const size_t fixed = sizeof(float) * ((size_t)m.kp + (size_t)rows_max * KS);
+  const int need = (rows_max + RPS - 1) / RPS;  // stages one CTA streams
+  long avail = (long)kSmemBudget - (long)fixed;
+  int ns = (int)(avail > 0 ? avail / (long)(p.stage_bytes + p.sc_bytes) : 0);
+  if (ns > kMaxStages) ns = kMaxStages;
+  if (ns > need) ns = need;
+  if (ns < 2) ns = 2;
+  p.n_stages = ns;
+  p.smem = fixed + (size_t)ns * (p.stage_bytes + p.sc_bytes);
+  return p;
+}
+
+template <int F, int PRO, int EPI>
+static mie_status launch_t(const GemvArgs &a0, int grid, cudaStream_t st, bool pdl) {
+  const Plan p = make_plan(a0.m, EPI, grid);
+  if (p.smem > kSmemMax) return fail(MIE_E_SHAPE, "gemv: %zu bytes of shared memory needed", p.smem);
+  GemvArgs a = a0;
+  a.n_stages = p.n_stages;
+  a.stage_bytes = p.stage_bytes;
+  a.sc_stage_bytes = p.sc_bytes;
   auto kern = gemv_kernel<F, PRO, EPI>;
   static bool configured[64] = {false};
-  static size_t configured_bytes[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && (!configured[dev] || configured_bytes[dev] < smem) && smem > 48 * 1024) {
-    MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024));
+  if (dev >= 0 && dev < 64 && !configured[dev]) {
+    MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemMax));
     configured[dev] = true;
-    configured_bytes[dev] = 200 * 1024;
   }
-  if (smem > 200 * 1024) return fail(MIE_E_SHAPE, "gemv: %zu bytes of shared memory needed", smem);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
+  cfg.gridDim = dim3(p.grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -459,8 +603,6 @@ static mie_status launch_f(int pro, int epi, const GemvArgs &a, int grid, cudaSt
   MIE_CASE(PRO_NORM, EPI_QKV)
   MIE_CASE(PRO_EMBED_NORM, EPI_QKV)
   MIE_CASE(PRO_NORM, EPI_ARGMAX)
-  MIE_CASE(PRO_PLAIN, EPI_ARGMAX)
-  MIE_CASE(PRO_NORM, EPI_STORE)
 #undef MIE_CASE
   return fail(MIE_E_ARG, "gemv: unsupported prologue/epilogue %d/%d", pro, epi);
 }
@@ -468,12 +610,16 @@ static mie_status launch_f(int pro, int epi, const GemvArgs &a, int grid, cudaSt
 int gemv_default_grid(const DevMat &m, int epi) {
   const int RU = (epi == EPI_SWIGLU || epi == EPI_QKV) ? 2 : 1;
   const int n_units = (m.rows + RU - 1) / RU;
-  const int target = 2 * sm_count();
+  const int target = sm_count();
   return n_units < target ? n_units : target;
 }
 
 mie_status launch_gemv(int pro, int epi, const GemvArgs &a, int grid, cudaStream_t st, bool pdl) {
   if (a.m.kp > kMaxK) return fail(MIE_E_SHAPE, "gemv: K = %d exceeds %d", a.m.kp, kMaxK);
+  if (((uintptr_t)a.m.w & 15) || (a.m.row_bytes & 15))
+    return fail(MIE_E_SHAPE, "gemv: weight rows must start on 16-byte boundaries");
+  if (a.m.fmt == MIE_FMT_Q4_0 && (((uintptr_t)a.m.s & 15) || (a.m.s_stride & 7)))
+    return fail(MIE_E_SHAPE, "gemv: Q4_0 scale rows must start on 16-byte boundaries");
   if (grid < 1) grid = 1;
   switch (a.m.fmt) {
     case MIE_FMT_BF16: return launch_f<MIE_FMT_BF16>(pro, epi, a, grid, st, pdl);
@@ -532,7 +678,7 @@ extern "C" size_t mie_q4_0_packed_bytes(int M, int K) {
   if (M < 1 || K < 1) return 0;
   const size_t nb = (size_t)(K + 31) / 32;
   const size_t nib = ((size_t)M * nb * 16 + 255) & ~(size_t)255;
-  return nib + (size_t)M * nb * 2;
+  return nib + (size_t)M * q4_scale_stride((int)nb) * 2;
 }
 
 extern "C" mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y, int M, int K, void *stream) {
@@ -547,5 +693,6 @@ extern "C" mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y
   m.row_bytes = (int64_t)nb * 16;
   const size_t nib = ((size_t)M * nb * 16 + 255) & ~(size_t)255;
   m.s = reinterpret_cast<const uint8_t *>(packed) + nib;
+  m.s_stride = q4_scale_stride(nb);
   return gemv_entry(m, x, y, stream);
 }

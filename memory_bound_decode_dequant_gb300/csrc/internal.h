@@ -14,9 +14,14 @@ struct DevMat {
   int rows = 0, cols = 0;  // logical shape
   int kp = 0;              // padded columns (multiple of the format's chunk)
   const uint8_t *w = nullptr;  // bf16/i8 row-major [rows][kp]; Q4_0 nibble plane [rows][kp/32][16]
-  const void *s = nullptr;     // i8: float[rows]; Q4_0: half[rows][kp/32]
+  const void *s = nullptr;     // i8: float[rows]; Q4_0: half[rows][s_stride]
   int64_t row_bytes = 0;
+  int s_stride = 0;            // Q4_0: scales per row, kp/32 rounded up to a multiple of 8
 };
+
+// Q4_0 scale-plane row stride: whole 16-byte groups, so a bulk copy of whole rows of
+// scales starts and ends on 16-byte boundaries.
+inline int q4_scale_stride(int nb) { return (nb + 7) / 8 * 8; }
 
 // Arguments of one GEMV launch (plain or fused).
 struct GemvArgs {
@@ -44,6 +49,9 @@ struct GemvArgs {
   StepParams *sp = nullptr;
   int slot = 0;
   int *err = nullptr;
+  // filled in by launch_gemv: the shared-memory ring of weight stages
+  int n_stages = 0;
+  uint32_t stage_bytes = 0, sc_stage_bytes = 0;
 };
 
 int gemv_chunk_elems(int fmt);  // elements per 16-byte chunk: 8 / 16 / 32
@@ -80,7 +88,7 @@ mie_status launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl);
 mie_status launch_convert_bf16(const float *w, int64_t n, uint16_t *out, cudaStream_t st);
 mie_status launch_quantize_i8(const float *w, int M, int K, int8_t *q, float *s, cudaStream_t st);
 mie_status launch_quantize_q4_0(const float *w, int M, int K, uint8_t *blocks, cudaStream_t st);
-mie_status launch_q4_0_pack(const uint8_t *blocks, int M, int K, uint8_t *nib, __half *scales,
+mie_status launch_q4_0_pack(const uint8_t *blocks, int M, int K, uint8_t *nib, __half *scales, int s_stride,
                             const int *row_map, cudaStream_t st);
 mie_status launch_row_permute(const uint8_t *src, uint8_t *dst, int64_t row_bytes, int M,
                               const int *row_map, cudaStream_t st);

@@ -250,7 +250,8 @@ mie_status alloc_mat(mie_ctx *ctx, DevMat &m, int fmt, int rows, int cols) {
   } else {
     m.kp = pad_to(cols, 32);
     m.row_bytes = (int64_t)(m.kp / 32) * 16;
-    sbytes = sizeof(__half) * (size_t)rows * (m.kp / 32);
+    m.s_stride = q4_scale_stride(m.kp / 32);
+    sbytes = sizeof(__half) * (size_t)rows * m.s_stride;
   }
   wbytes = (size_t)rows * m.row_bytes;
   uint8_t *w = (uint8_t *)ctx->dalloc(wbytes);
@@ -337,7 +338,7 @@ mie_status fill_mat_body(mie_ctx *ctx, Temp &tmp, DevMat &m, int fmt, const void
   }
   if (m.kp / 32 != nb) return fail(MIE_E_SHAPE, "weights: Q4_0 block count mismatch");
   return launch_q4_0_pack((const uint8_t *)canon, rows, cols, const_cast<uint8_t *>(m.w),
-                          (__half *)const_cast<void *>(m.s), dmap, st);
+                          (__half *)const_cast<void *>(m.s), m.s_stride, dmap, st);
 }
 
 mie_status fill_mat(mie_ctx *ctx, DevMat &m, int fmt, const void *host, size_t bytes, const float *host_scale, int rows,

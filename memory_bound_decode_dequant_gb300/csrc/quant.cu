@@ -69,7 +69,7 @@ __global__ void quantize_q4_0_kernel(const float *w, int M, int K, uint8_t *out)
 
 // Canonical blocks -> nibble plane + scale plane; source row r goes to row map[r].
 __global__ void q4_0_pack_kernel(const uint8_t *blocks, int M, int nb, uint8_t *nib, __half *scales,
-                                 const int *map) {
+                                 int s_stride, const int *map) {
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)M * nb) return;
   const int r = (int)(idx / nb), b = (int)(idx % nb);
@@ -78,7 +78,7 @@ __global__ void q4_0_pack_kernel(const uint8_t *blocks, int M, int nb, uint8_t *
   uint8_t *dst = nib + ((int64_t)dr * nb + b) * 16;
 #pragma unroll
   for (int j = 0; j < 16; ++j) dst[j] = src[2 + j];
-  scales[(int64_t)dr * nb + b] = __ushort_as_half((uint16_t)(src[0] | (src[1] << 8)));
+  scales[(int64_t)dr * s_stride + b] = __ushort_as_half((uint16_t)(src[0] | (src[1] << 8)));
 }
 
 // Row copy with optional scatter (source row r -> destination row map[r]) and zero
@@ -126,10 +126,10 @@ mie_status launch_quantize_q4_0(const float *w, int M, int K, uint8_t *blocks, c
   return MIE_OK;
 }
 
-mie_status launch_q4_0_pack(const uint8_t *blocks, int M, int K, uint8_t *nib, __half *scales, const int *row_map,
-                            cudaStream_t st) {
+mie_status launch_q4_0_pack(const uint8_t *blocks, int M, int K, uint8_t *nib, __half *scales, int s_stride,
+                            const int *row_map, cudaStream_t st) {
   const int nb = (K + 31) / 32;
-  q4_0_pack_kernel<<<blocks_for((int64_t)M * nb, 256), 256, 0, st>>>(blocks, M, nb, nib, scales, row_map);
+  q4_0_pack_kernel<<<blocks_for((int64_t)M * nb, 256), 256, 0, st>>>(blocks, M, nb, nib, scales, s_stride, row_map);
   MIE_CUDA(cudaGetLastError());
   return MIE_OK;
 }
@@ -184,7 +184,8 @@ extern "C" mie_status mie_q4_0_pack(const uint8_t *blocks, int M, int K, void *p
   if ((uintptr_t)packed & 255) return fail(MIE_E_SHAPE, "mie_q4_0_pack: output not 256-byte aligned");
   const int nb = (K + 31) / 32;
   const size_t nib = ((size_t)M * nb * 16 + 255) & ~(size_t)255;
-  return launch_q4_0_pack(blocks, M, K, reinterpret_cast<uint8_t *>(packed),
-                          reinterpret_cast<__half *>(reinterpret_cast<uint8_t *>(packed) + nib), nullptr,
-                          (cudaStream_t)stream);
+  uint8_t *sc = reinterpret_cast<uint8_t *>(packed) + nib;
+  MIE_CUDA(cudaMemsetAsync(sc, 0, (size_t)M * q4_scale_stride(nb) * 2, (cudaStream_t)stream));
+  return launch_q4_0_pack(blocks, M, K, reinterpret_cast<uint8_t *>(packed), reinterpret_cast<__half *>(sc),
+                          q4_scale_stride(nb), nullptr, (cudaStream_t)stream);
 }

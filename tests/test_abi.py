@@ -104,9 +104,10 @@ def test_host_side_argument_checks(L):
 
 
 def test_q4_0_packed_bytes(L):
-    assert mie.mie_q4_0_packed_bytes(1, 1) == 256 + 2
+    # nibble plane, then at a 256-byte boundary the scale plane with rows padded to 8 scales
+    assert mie.mie_q4_0_packed_bytes(1, 1) == 256 + 16
     assert mie.mie_q4_0_packed_bytes(3072, 2048) == 3072 * 64 * 16 + 3072 * 64 * 2
-    assert mie.mie_q4_0_packed_bytes(256, 688) == ((256 * 22 * 16 + 255) // 256) * 256 + 256 * 22 * 2
+    assert mie.mie_q4_0_packed_bytes(256, 688) == ((256 * 22 * 16 + 255) // 256) * 256 + 256 * 24 * 2
 
 
 def test_config_checks_need_no_gpu(L):

@@ -68,12 +68,13 @@ def test_q4_0_pack_layout(orc):
     w = synth.normal(77, M * K, std=0.02).reshape(M, K)
     blocks = orc.q4_0_quantize(w)
     packed = mie.mie_q4_0_pack(torch.from_numpy(blocks).cuda(), M, K).cpu().numpy()
-    nb = 3
+    nb, nbp = 3, 8  # scale rows padded to a multiple of 8
     nib = packed[: M * nb * 16].reshape(M, nb, 16)
     off = ((M * nb * 16 + 255) // 256) * 256
-    sc = packed[off: off + M * nb * 2].view(np.uint16).reshape(M, nb)
+    sc = packed[off: off + M * nbp * 2].view(np.uint16).reshape(M, nbp)
     assert np.array_equal(nib, blocks[:, :, 2:])
-    assert np.array_equal(sc, blocks[:, :, 0].astype(np.uint16) | (blocks[:, :, 1].astype(np.uint16) << 8))
+    assert np.array_equal(sc[:, :nb], blocks[:, :, 0].astype(np.uint16) | (blocks[:, :, 1].astype(np.uint16) << 8))
+    assert np.all(sc[:, nb:] == 0)
 
 
 # ------------------------------------------------------------------ GEMV

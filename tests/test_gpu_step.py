@@ -64,14 +64,19 @@ def run_parity(orc, shape, layers, n_prompt, n_gen, perm_seed=5, compare_kv=True
         rf = orc.from_bf16(r).astype(np.float64)
         # one bf16 step of the value plus the GEMV tolerance at the tensor's scale: an
         # element near zero can round to different bf16 neighbours when the fp32 GEMV
-        # outputs differ by ~1e-6 of the row scale (entries past n_tok are zero on both)
+        # outputs differ by ~1e-6 of the row scale (entries past n_tok are zero on both).
+        # With bf16 activations every GEMV input is rounded too: a ~1e-4 relative
+        # difference in the residual flips a few percent of the rounded inputs by one
+        # bf16 step (2^-8 relative), which moves later K/V values by ~1e-3 of their RMS
+        # with tails several times that, hence the wider term there.
         rms = float(np.sqrt(np.mean(rf[rf != 0] ** 2)))
         err = np.abs(gf - rf)
-        bound = np.abs(rf) * 2.0 ** -7 + 1e-3 * rms
+        c, min_exact = (1e-2, 0.85) if shape.act_bf16 else (1e-3, 0.97)
+        bound = np.abs(rf) * 2.0 ** -7 + c * rms
         worst = np.unravel_index(np.argmax(err / bound), err.shape)
         assert np.all(err <= bound), f"K/V {worst}: gpu {gf[worst]} oracle {rf[worst]} (rms {rms:.3g})"
         exact = float(np.mean(g == r))
-        assert exact > 0.97, f"only {exact:.3f} of the K/V bf16 values are identical"
+        assert exact > min_exact, f"only {exact:.3f} of the K/V bf16 values are identical"
     return gm, om
 
 
