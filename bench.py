@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--oracle-steps", type=int, default=3)
+    ap.add_argument("--chain", action="store_true", help="one kernel per phase instead of the persistent step")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the dominant kernel (the profiling command)")
     return ap.parse_args()
@@ -224,6 +225,8 @@ def run_mie(args, shape):
     max_pos = n_blocks * bs
     stream = torch.cuda.Stream()  # the context's stream: events are recorded on it
     gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos, stream=stream)
+    if args.chain:
+        gm.set_step_mode(gm.CHAIN)
     bt_host = synth.permutation(0x4254, n_blocks).astype(np.int32)
     bt = torch.from_numpy(bt_host).cuda()
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
@@ -320,6 +323,7 @@ def run_mie(args, shape):
                     "d2h_bytes_per_step": 4},
             "gpu_launches": launches * args.steps,
             "launches_per_step": launches,
+            "step_mode": "persistent" if gm.step_mode == 0 else "chain",
             "clocks": clk.summary(),
             "wall_s_timed": t_wall,
             "cpu_baseline": cpu,

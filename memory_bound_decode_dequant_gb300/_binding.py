@@ -77,6 +77,9 @@ _SIGS = {
     "mie_decode_step_slots": (I, [P, I, P, P, P, I, P, P]),
     "mie_sync": (I, [P]),
     "mie_step_launches": (I, [P]),
+    "mie_set_step_mode": (I, [P, I]),
+    "mie_step_mode": (I, [P]),
+    "mie_set_trace": (I, [P, P, SZ, ctypes.POINTER(I), ctypes.POINTER(I)]),
 }
 
 _lib = None
@@ -393,3 +396,27 @@ class Model:
     @property
     def launches(self) -> int:
         return int(lib().mie_step_launches(self.h))
+
+    PERSISTENT, CHAIN = 0, 1
+
+    def set_step_mode(self, mode: int):
+        _check(lib().mie_set_step_mode(self.h, mode), "mie_set_step_mode")
+
+    @property
+    def step_mode(self) -> int:
+        return int(lib().mie_step_mode(self.h))
+
+    def set_trace(self, enable: bool = True):
+        """Records the persistent step's timeline into a device tensor
+        [n_phases, n_ctas, 5] of int64 nanoseconds (returned), or switches it off."""
+        torch = _torch()
+        npz, nct = I(0), I(0)
+        if not enable:
+            _check(lib().mie_set_trace(self.h, None, 0, ctypes.byref(npz), ctypes.byref(nct)), "mie_set_trace")
+            self._trace = None
+            return None
+        _check(lib().mie_set_trace(self.h, None, 0, ctypes.byref(npz), ctypes.byref(nct)), "mie_set_trace")
+        buf = torch.zeros((npz.value, nct.value, 5), dtype=torch.int64, device="cuda")
+        _check(lib().mie_set_trace(self.h, buf.data_ptr(), buf.numel() * 8, None, None), "mie_set_trace")
+        self._trace = buf
+        return buf

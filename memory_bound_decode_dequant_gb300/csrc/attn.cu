@@ -7,44 +7,27 @@
 // Rust", Lesson 4: an online softmax with a running maximum and sum).
 //
 // Grid (splits, KV heads), 128 threads; the number of splits in use follows the
-// context (at least 4 blocks each).  A CTA stages the block ids of its split in shared
-// memory, then each warp takes groups of 32/LPT tokens (LPT = head_dim/32 lanes per
-// token) and issues all of a group's loads before any math: 64 bytes of one key per
-// lane, plus the lane's head_dim/32 value dims of every token in the group.  Each
-// key is dotted with every query head of the group (one K/V read serves them all),
-// the LPT lanes of a token combine with a shuffle, and each warp keeps an online
-// softmax per head.  Warps merge in shared memory; with one split the CTA writes the
-// result, otherwise CTAs write (m, l, o) partials and the last CTA of each KV head to
-// finish (an atomic counter, no waiting) merges them and resets the counter.
-#include "internal.h"
+// context (at least four blocks each); the per-split work is attn_split in
+// attn_core.cuh.
+#include "attn_core.cuh"
 
 namespace mie {
 
 constexpr int kAttnThreads = 128;
 constexpr int kAttnWarps = kAttnThreads / 32;
-constexpr int kAttnMaxBlocks = 256;     // block ids staged in shared memory at a time
-constexpr int kAttnBlocksPerSplit = 4;  // one block per warp per split, at least
 
 __device__ int g_device_error;  // latched by the stateless kernels of this device
 
+struct CtaSync {
+  __device__ static void sync() { __syncthreads(); }
+};
+
 template <int G, int HD>
 __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
-  constexpr int LPT = HD / 32;          // lanes per token (each lane dots 32 dims)
-  constexpr int TPI = 32 / LPT;         // tokens per warp iteration
-  constexpr int DPL = HD / 32;          // value dims per lane
-  constexpr int PART = G * (2 + HD);    // floats of one (head group, split) partial
-  __shared__ __align__(16) float q_s[G * HD];
-  __shared__ int s_blk[kAttnMaxBlocks];
-  __shared__ float w_m[kAttnWarps][G], w_l[kAttnWarps][G];
-  __shared__ float w_o[kAttnWarps][G][HD];
-  __shared__ unsigned s_last;
-  __shared__ int s_nsplit;
-
+  __shared__ AttnSmem<G, HD, kAttnWarps> sm;
   pdl_trigger();
   pdl_wait();
-
   const int g = blockIdx.y, s = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int ctx;
   const int32_t *bt;
   int n_table;
@@ -62,206 +45,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
     ctx = n_table * a.bs;
   }
   if (ctx < 0) ctx = 0;
-  const int nblk = (ctx + a.bs - 1) / a.bs;
-  // at least kAttnBlocksPerSplit blocks per split, so every warp has a block to read
-  const int nsplit = max(1, min(a.n_splits, (nblk + kAttnBlocksPerSplit - 1) / kAttnBlocksPerSplit));
+  const int nsplit = attn_nsplit((ctx + a.bs - 1) / a.bs, a.n_splits, attn_blocks_per_split<HD, kAttnWarps>(a.bs));
   if (s >= nsplit) return;
-  const int b0 = (int)((int64_t)s * nblk / nsplit), b1 = (int)((int64_t)(s + 1) * nblk / nsplit);
-  const int t_end = min(b1 * a.bs, ctx);
-
-  for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) q_s[i] = a.q[(g * G) * HD + i];
-
-  float m[G], l[G], o[G][DPL];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
-  }
-  const int tok_in = lane / LPT, part_in = lane % LPT;
-  const int64_t head_off = (int64_t)g * a.bs * HD;
-
-  // the split's blocks, staged kAttnMaxBlocks at a time (one coalesced load each)
-  for (int cb = b0; cb < b1; cb += kAttnMaxBlocks) {
-    const int ce = min(b1, cb + kAttnMaxBlocks);
-    __syncthreads();
-    for (int i = threadIdx.x; i < ce - cb; i += kAttnThreads) {
-      int blk = bt[cb + i];
-      if (blk < 0 || blk >= a.n_pool_blocks) {
-        latch_error(a.err, ERR_BLOCK_ID);
-        blk = -1;
-      }
-      s_blk[i] = blk;
-    }
-    __syncthreads();
-    const int t0 = cb * a.bs, t1 = min(ce * a.bs, t_end);
-    for (int tb = t0 + warp * TPI; tb < t1; tb += kAttnWarps * TPI) {
-      const int nt = min(TPI, t1 - tb);
-      // issue every load of this token group first: my key slice, then my value dims
-      const int t = tb + tok_in;
-      const int kblk = (t < t1) ? s_blk[t / a.bs - cb] : -1;
-      uint4 kv[4];
-      if (kblk >= 0) {
-        const uint16_t *kp = a.k + (int64_t)kblk * a.block_stride + head_off + (int64_t)(t % a.bs) * HD + part_in * 32;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) kv[i] = *reinterpret_cast<const uint4 *>(kp + 8 * i);
-      }
-      float vf[TPI][DPL];
-#pragma unroll
-      for (int i = 0; i < TPI; ++i) {
-        const int t2 = tb + i;
-        const int vblk = (i < nt) ? s_blk[t2 / a.bs - cb] : -1;
-        if (vblk >= 0) {
-          const uint16_t *vp = a.v + (int64_t)vblk * a.block_stride + head_off + (int64_t)(t2 % a.bs) * HD + lane * DPL;
-          if constexpr (DPL == 1) {
-            vf[i][0] = bf16_bits_to_f32(*vp);
-          } else if constexpr (DPL == 2) {
-            const uint32_t w = *reinterpret_cast<const uint32_t *>(vp);
-            vf[i][0] = __uint_as_float(w << 16);
-            vf[i][1] = __uint_as_float(w & 0xffff0000u);
-          } else {
-            const uint2 w = *reinterpret_cast<const uint2 *>(vp);
-            vf[i][0] = __uint_as_float(w.x << 16);
-            vf[i][1] = __uint_as_float(w.x & 0xffff0000u);
-            vf[i][2] = __uint_as_float(w.y << 16);
-            vf[i][3] = __uint_as_float(w.y & 0xffff0000u);
-          }
-        } else {
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) vf[i][d] = 0.f;
-        }
-      }
-      // scores of my token for every query head of the group
-      float sc[G];
-      if (kblk >= 0) {
-        float kf[32];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w[4] = {kv[i].x, kv[i].y, kv[i].z, kv[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            kf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-            kf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float *qh = q_s + h * HD + part_in * 32;
-          float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            d0 = fmaf(qh[i], kf[i], d0);
-            d1 = fmaf(qh[i + 1], kf[i + 1], d1);
-          }
-          sc[h] = d0 + d1;
-        }
-      } else {
-#pragma unroll
-        for (int h = 0; h < G; ++h) sc[h] = 0.f;
-      }
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int off = 1; off < LPT; off <<= 1) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
-        sc[h] = (kblk >= 0) ? sc[h] * a.scale : -INFINITY;
-      }
-      // online softmax: rescale the running sums to the new maximum
-      float p[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mn = fmaxf(m[h], warp_max(sc[h]));
-        if (mn == -INFINITY) {
-          p[h] = 0.f;
-          continue;
-        }
-        const float corr = expf(m[h] - mn);  // 0 while m was -inf
-        p[h] = (sc[h] == -INFINITY) ? 0.f : expf(sc[h] - mn);
-        const float ps = warp_sum(part_in == 0 ? p[h] : 0.f);  // each token counted once
-        l[h] = l[h] * corr + ps;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) o[h][d] *= corr;
-        m[h] = mn;
-      }
-#pragma unroll
-      for (int i = 0; i < TPI; ++i) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float ph = __shfl_sync(0xffffffffu, p[h], i * LPT);
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(ph, vf[i][d], o[h][d]);
-        }
-      }
-    }
-  }
-
-  // merge the warps of this CTA
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) { w_m[warp][h] = m[h]; w_l[warp][h] = l[h]; }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) w_o[warp][h][lane * DPL + d] = o[h][d];
-  __syncthreads();
-  if (nsplit == 1) {  // the only split: write the result directly
-    for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
-      const int h = i / HD, d = i % HD;
-      float M = -INFINITY;
-      for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, w_m[w][h]);
-      float O = 0.f, L = 0.f;
-      for (int w = 0; w < kAttnWarps; ++w) {
-        const float f = (w_m[w][h] == -INFINITY) ? 0.f : expf(w_m[w][h] - M);
-        O = fmaf(w_o[w][h][d], f, O);
-        L = fmaf(w_l[w][h], f, L);
-      }
-      a.out[(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
-    }
-    return;
-  }
-  float *part = a.ws_part + ((int64_t)g * a.n_splits + s) * PART;
-  for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
-    const int h = i / HD, d = i % HD;
-    float M = -INFINITY;
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, w_m[w][h]);
-    float O = 0.f, L = 0.f;
-    for (int w = 0; w < kAttnWarps; ++w) {
-      const float f = (w_m[w][h] == -INFINITY) ? 0.f : expf(w_m[w][h] - M);
-      O = fmaf(w_o[w][h][d], f, O);
-      L = fmaf(w_l[w][h], f, L);
-    }
-    part[2 * G + i] = O;
-    if (d == 0) { part[h] = M; part[G + h] = L; }
-  }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    s_last = (atomicAdd(a.ws_count + g, 1u) == (unsigned)nsplit - 1);
-    s_nsplit = nsplit;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // last CTA of this KV head: merge the splits
-  const float *base = a.ws_part + (int64_t)g * a.n_splits * PART;
-  for (int i = threadIdx.x; i < G * HD; i += kAttnThreads) {
-    const int h = i / HD;
-    float M = -INFINITY;
-    for (int sp = 0; sp < s_nsplit; ++sp) M = fmaxf(M, __ldcg(base + (int64_t)sp * PART + h));
-    float O = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-      for (int sp = 0; sp < s_nsplit; ++sp) {
-        const float *p = base + (int64_t)sp * PART;
-        const float ms = __ldcg(p + h);
-        const float f = (ms == -INFINITY) ? 0.f : expf(ms - M);
-        O = fmaf(__ldcg(p + 2 * G + i), f, O);
-        L = fmaf(__ldcg(p + G + h), f, L);
-      }
-    }
-    a.out[(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
-  }
-  if (threadIdx.x == 0) a.ws_count[g] = 0u;
+  attn_split<G, HD, kAttnWarps, CtaSync>(a, g, s, nsplit, ctx, bt, nullptr, sm);
 }
 
 // Empty context: the output is zero (no split has a position).

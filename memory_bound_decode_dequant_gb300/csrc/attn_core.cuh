@@ -1,0 +1,309 @@
+// attn_core.cuh -- one (KV head, context split) of paged GQA decode attention, shared
+// by the standalone attention kernel and the persistent step kernel.
+//
+// "Mini Inference Engine", "The KV cache, paged like virtual memory": K/V are read
+// through a block table; "infer" page, "GQA-aware split-KV attention": the query heads
+// of one KV head share every K/V load, the context is split and partial softmaxes are
+// merged; "Writing an LLM inference engine from scratch in Rust", Lesson 4: an online
+// softmax with a running maximum and sum.
+//
+// NW warps take groups of 32/LPT tokens (LPT = head_dim/32 lanes per token) and issue
+// all loads of a group before any math: 64 bytes of one key per lane, then the lane's
+// head_dim/32 value dims of every token of the group.  K/V are loaded with ld.global.cg
+// so that values written earlier in the same launch (by another SM) are read from L2.
+#pragma once
+
+#include "device.cuh"
+
+namespace mie {
+
+constexpr int kAttnMaxBlocks = 256;  // block ids staged in shared memory at a time
+
+// Splits in use for a context of nblk blocks: every split gets at least per_split
+// blocks (so its warps have work), at most max_splits splits.
+__host__ __device__ inline int attn_nsplit(int nblk, int max_splits, int per_split) {
+  int s = (nblk + per_split - 1) / per_split;
+  if (s > max_splits) s = max_splits;
+  return s < 1 ? 1 : s;
+}
+
+// Blocks per split: two token groups per warp, so each warp overlaps the loads of its
+// second group with the math of its first.
+template <int HD, int NW>
+__host__ __device__ inline int attn_blocks_per_split(int bs) {
+  const int tokens = 2 * NW * (32 / (HD / 32));
+  const int b = tokens / bs;
+  return b < 1 ? 1 : b;
+}
+
+// Shared-memory scratch of one attention CTA.
+template <int G, int HD, int NW>
+struct AttnSmem {
+  float q[G * HD];
+  int blk[kAttnMaxBlocks];
+  float m[NW][G], l[NW][G];
+  float o[NW][G][HD];
+  unsigned last;
+};
+
+// The loads of one group of tokens for one lane: 64 bytes of its key, and its value
+// dims of every token of the group.  Masked tokens read the pool base (always valid)
+// and are zeroed later, so the loads carry no branches and issue back to back.
+template <int HD>
+struct KvGroup {
+  static constexpr int LPT = HD / 32, TPI = 32 / LPT, DPL = HD / 32, VW = DPL == 4 ? 2 : 1;
+  uint4 kv[4];
+  uint32_t vraw[TPI][VW];
+  unsigned vmask;  // bit i: token i of the group is valid
+  int kblk;
+
+  __device__ __forceinline__ void load(const AttnArgs &a, const int *ids, int id0, int tb, int t1, int64_t head_off,
+                                       int lane) {
+    const int tok_in = lane / LPT, part_in = lane % LPT;
+    const int t = tb + tok_in;
+    kblk = (t < t1) ? ids[t / a.bs - id0] : -1;
+    const uint16_t *kp =
+        (kblk >= 0) ? a.k + (int64_t)kblk * a.block_stride + head_off + (int64_t)(t % a.bs) * HD + part_in * 32 : a.k;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) kv[i] = __ldcg(reinterpret_cast<const uint4 *>(kp + 8 * i));
+    vmask = 0u;
+#pragma unroll
+    for (int i = 0; i < TPI; ++i) {
+      const int t2 = tb + i;
+      const int vblk = (t2 < t1) ? ids[t2 / a.bs - id0] : -1;
+      if (vblk >= 0) vmask |= 1u << i;
+      const uint16_t *vp =
+          vblk >= 0 ? a.v + (int64_t)vblk * a.block_stride + head_off + (int64_t)(t2 % a.bs) * HD + lane * DPL : a.v;
+      if constexpr (DPL == 1) {
+        vraw[i][0] = __ldcg(reinterpret_cast<const unsigned short *>(vp));
+      } else if constexpr (DPL == 2) {
+        vraw[i][0] = __ldcg(reinterpret_cast<const unsigned int *>(vp));
+      } else {
+        const uint2 w = __ldcg(reinterpret_cast<const uint2 *>(vp));
+        vraw[i][0] = w.x;
+        vraw[i][1] = w.y;
+      }
+    }
+  }
+};
+
+// Computes split s of nsplit for KV head g.  With one split the result goes straight
+// to a.out; otherwise the split's (m, l, o) partial goes to the workspace and the last
+// split of the head to finish (atomic counter, no waiting) merges all partials and
+// resets the counter.  blk_pre, when not null, holds the block ids of blocks
+// [0, nblk) already staged in shared memory; otherwise they are read from bt in
+// chunks.  Sync::sync() is a barrier over the NW participating warps, whose threads
+// are numbered 0 .. NW*32-1.
+template <int G, int HD, int NW, class Sync>
+__device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx, const int32_t *bt, const int *blk_pre,
+                           AttnSmem<G, HD, NW> &sm) {
+  using KG = KvGroup<HD>;
+  constexpr int LPT = KG::LPT, TPI = KG::TPI, DPL = KG::DPL, VW = KG::VW;
+  constexpr int PART = G * (2 + HD);
+  constexpr int NT = NW * 32;
+  constexpr int QB = (G * HD + NT - 1) / NT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nblk = (ctx + a.bs - 1) / a.bs;
+  const int b0 = (int)((int64_t)s * nblk / nsplit), b1 = (int)((int64_t)(s + 1) * nblk / nsplit);
+  const int t_end = min(b1 * a.bs, ctx);
+  const int part_in = lane % LPT;
+  const int64_t head_off = (int64_t)g * a.bs * HD;
+
+  // the queries of the group: loads issued now, stored once the first K/V loads are out
+  float qv[QB];
+#pragma unroll
+  for (int j = 0; j < QB; ++j) qv[j] = __ldcg(a.q + (g * G) * HD + min(tid + j * NT, G * HD - 1));
+  bool q_stored = false;
+
+  float m[G], l[G], o[G][DPL];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) o[h][d] = 0.f;
+  }
+
+  for (int cb = b0; cb < b1; cb += kAttnMaxBlocks) {
+    const int ce = blk_pre ? b1 : min(b1, cb + kAttnMaxBlocks);
+    const int *ids = blk_pre;
+    int id0 = 0;
+    if (!blk_pre) {
+      Sync::sync();
+      for (int i = tid; i < ce - cb; i += NT) {
+        int blk = bt[cb + i];
+        if (blk < 0 || blk >= a.n_pool_blocks) {
+          latch_error(a.err, ERR_BLOCK_ID);
+          blk = -1;
+        }
+        sm.blk[i] = blk;
+      }
+      Sync::sync();
+      ids = sm.blk;
+      id0 = cb;
+    }
+    const int t0 = cb * a.bs, t1 = min(ce * a.bs, t_end);
+    int tb = t0 + warp * TPI;
+    KG cur;
+    cur.load(a, ids, id0, tb, t1, head_off, lane);
+    if (!q_stored) {
+#pragma unroll
+      for (int j = 0; j < QB; ++j)
+        if (tid + j * NT < G * HD) sm.q[tid + j * NT] = qv[j];
+      Sync::sync();
+      q_stored = true;
+    }
+    for (; tb < t1; tb += NW * TPI) {
+      const int kblk = cur.kblk;
+      float vf[TPI][DPL];
+#pragma unroll
+      for (int i = 0; i < TPI; ++i) {
+        const bool ok = (cur.vmask >> i) & 1u;
+        if constexpr (DPL == 1) {
+          vf[i][0] = ok ? __uint_as_float(cur.vraw[i][0] << 16) : 0.f;
+        } else {
+#pragma unroll
+          for (int w = 0; w < VW; ++w) {
+            vf[i][2 * w] = ok ? __uint_as_float(cur.vraw[i][w] << 16) : 0.f;
+            vf[i][2 * w + 1] = ok ? __uint_as_float(cur.vraw[i][w] & 0xffff0000u) : 0.f;
+          }
+        }
+      }
+      float sc[G];
+      {
+        float kf[32];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t w[4] = {cur.kv[i].x, cur.kv[i].y, cur.kv[i].z, cur.kv[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            kf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+            kf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+          }
+        }
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float *qh = sm.q + h * HD + part_in * 32;
+          float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            d0 = fmaf(qh[i], kf[i], d0);
+            d1 = fmaf(qh[i + 1], kf[i + 1], d1);
+          }
+          sc[h] = d0 + d1;
+        }
+      }
+      // the next group's loads go out before this group's softmax
+      if (tb + NW * TPI < t1) cur.load(a, ids, id0, tb + NW * TPI, t1, head_off, lane);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+#pragma unroll
+        for (int off = 1; off < LPT; off <<= 1) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+        sc[h] = (kblk >= 0) ? sc[h] * a.scale : -INFINITY;
+      }
+      float p[G];
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mn = fmaxf(m[h], warp_max(sc[h]));
+        if (mn == -INFINITY) {
+          p[h] = 0.f;
+          continue;
+        }
+        const float corr = expf(m[h] - mn);  // 0 while m was -inf
+        p[h] = (sc[h] == -INFINITY) ? 0.f : expf(sc[h] - mn);
+        const float ps = warp_sum(part_in == 0 ? p[h] : 0.f);  // each token counted once
+        l[h] = l[h] * corr + ps;
+#pragma unroll
+        for (int d = 0; d < DPL; ++d) o[h][d] *= corr;
+        m[h] = mn;
+      }
+#pragma unroll
+      for (int i = 0; i < TPI; ++i) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+          const float ph = __shfl_sync(0xffffffffu, p[h], i * LPT);
+#pragma unroll
+          for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(ph, vf[i][d], o[h][d]);
+        }
+      }
+    }
+  }
+  if (!q_stored) Sync::sync();  // empty split: keep the barrier count of the other paths
+
+  // merge the warps
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) { sm.m[warp][h] = m[h]; sm.l[warp][h] = l[h]; }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) sm.o[warp][h][lane * DPL + d] = o[h][d];
+  Sync::sync();
+  float *part = a.ws_part + ((int64_t)g * a.n_splits + s) * PART;
+  for (int i = tid; i < G * HD; i += NT) {
+    const int h = i / HD, d = i % HD;
+    float M = -INFINITY;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.m[w][h]);
+    float O = 0.f, L = 0.f;
+    for (int w = 0; w < NW; ++w) {
+      const float f = (sm.m[w][h] == -INFINITY) ? 0.f : expf(sm.m[w][h] - M);
+      O = fmaf(sm.o[w][h][d], f, O);
+      L = fmaf(sm.l[w][h], f, L);
+    }
+    if (nsplit == 1) {
+      a.out[(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
+    } else {
+      part[2 * G + i] = O;
+      if (d == 0) { part[h] = M; part[G + h] = L; }
+    }
+  }
+  if (nsplit == 1) {
+    Sync::sync();  // the scratch is reused by the caller's next item
+    return;
+  }
+  __threadfence();
+  Sync::sync();
+  if (tid == 0) sm.last = (atomicAdd(a.ws_count + g, 1u) == (unsigned)nsplit - 1);
+  Sync::sync();
+  if (!sm.last) return;
+  __threadfence();
+  const float *base = a.ws_part + (int64_t)g * a.n_splits * PART;
+  for (int i = tid; i < G * HD; i += NT) {
+    const int h = i / HD;
+    // one pass with online rescaling, eight splits' partials loaded per round trip
+    float M = -INFINITY, O = 0.f, L = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += 8) {
+      float ms[8], os[8], ls[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float *p = base + (int64_t)min(s0 + j, nsplit - 1) * PART;
+        ms[j] = __ldcg(p + h);
+        ls[j] = __ldcg(p + G + h);
+        os[j] = __ldcg(p + 2 * G + i);
+      }
+      float mb = M;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < nsplit) mb = fmaxf(mb, ms[j]);
+      if (mb == -INFINITY) continue;
+      const float c = (M == -INFINITY) ? 0.f : expf(M - mb);
+      O *= c;
+      L *= c;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j < nsplit && ms[j] != -INFINITY) {
+          const float f = expf(ms[j] - mb);
+          O = fmaf(os[j], f, O);
+          L = fmaf(ls[j], f, L);
+        }
+      }
+      M = mb;
+    }
+    a.out[(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
+  }
+  if (tid == 0) a.ws_count[g] = 0u;
+  Sync::sync();
+}
+
+}  // namespace mie

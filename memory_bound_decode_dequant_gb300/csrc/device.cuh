@@ -1,0 +1,312 @@
+// device.cuh -- device code shared by the GEMV kernels and the persistent step kernel:
+// weight-format traits, in-register dequantisation, mbarrier and bulk-copy helpers.
+#pragma once
+
+#include "internal.h"
+
+namespace mie {
+
+template <int F> struct FmtT;
+// EPC: elements per 16-byte chunk; CPL: chunks per lane per 2048-column slice.
+template <> struct FmtT<MIE_FMT_BF16> { static constexpr int EPC = 8, CPL = 8; };
+template <> struct FmtT<MIE_FMT_I8> { static constexpr int EPC = 16, CPL = 4; };
+template <> struct FmtT<MIE_FMT_Q4_0> { static constexpr int EPC = 32, CPL = 2; };
+constexpr int kSlice = 2048;  // = 32 * EPC * CPL for every format
+constexpr int kMaxK = 16384;  // eight 2048-column slices
+
+// --------------------------------------------------------------- element decoding
+
+__device__ __forceinline__ float embed_at(const DevMat &m, int row, int k) {
+  if (m.fmt == MIE_FMT_BF16) {
+    return bf16_bits_to_f32(reinterpret_cast<const uint16_t *>(m.w + (int64_t)row * m.row_bytes)[k]);
+  } else if (m.fmt == MIE_FMT_I8) {
+    const int8_t q = reinterpret_cast<const int8_t *>(m.w + (int64_t)row * m.row_bytes)[k];
+    return reinterpret_cast<const float *>(m.s)[row] * (float)q;
+  } else {
+    const uint8_t byte = m.w[(int64_t)row * m.row_bytes + (k >> 5) * 16 + (k & 15)];
+    const int code = ((k & 31) < 16) ? (byte & 0xF) : (byte >> 4);
+    const float h = __half2float(reinterpret_cast<const __half *>(m.s)[(int64_t)row * m.s_stride + (k >> 5)]);
+    return h * (float)(code - 8);
+  }
+}
+
+// Dot product of one 16-byte chunk with the lane's input registers.
+template <int F>
+__device__ __forceinline__ void chunk_fma(const uint4 &w, const float2 *xr, float2 *acc);
+
+template <>
+__device__ __forceinline__ void chunk_fma<MIE_FMT_BF16>(const uint4 &w, const float2 *xr, float2 *acc) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const float2 wf = make_float2(__uint_as_float(v[t] << 16), __uint_as_float(v[t] & 0xffff0000u));
+    acc[t] = __ffma2_rn(wf, xr[t], acc[t]);
+  }
+}
+
+template <>
+__device__ __forceinline__ void chunk_fma<MIE_FMT_I8>(const uint4 &w, const float2 *xr, float2 *acc) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+  const float2 bias = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t u = v[t] ^ 0x80808080u;  // int8 b -> b + 128 in 0..255
+    const float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
+    const float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
+                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
+    acc[t] = __ffma2_rn(__fadd2_rn(a, bias), xr[2 * t], acc[t]);
+    acc[t] = __ffma2_rn(__fadd2_rn(b, bias), xr[2 * t + 1], acc[t]);
+  }
+}
+
+// Q4_0 chunk = one block: word t holds bytes 4t..4t+3; byte j carries element j (low
+// nibble) and element j+16 (high nibble).  Unpack order per word, with the bit offset
+// p the code sits at: 4t(p0) 4t+16(p4) 4t+1(p8) 4t+17(p12) 4t+2(p16), then from
+// w >> 12: 4t+18(p8) 4t+3(p12) 4t+19(p16).  The input registers hold x * 2^-p in
+// that order, so (2^23 + n 2^p) - (2^23 + 8 2^p) = (n - 8) 2^p times them is
+// (n - 8) x.
+template <>
+__device__ __forceinline__ void chunk_fma<MIE_FMT_Q4_0>(const uint4 &w, const float2 *xr, float2 *acc) {
+  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
+  const uint32_t M = 0x4B000000u;
+  const float2 b01 = make_float2(-8388616.f, -8388736.f);  // -(2^23 + 8 * {1, 16})
+  const float2 b23 = make_float2(-8390656.f, -8421376.f);  // -(2^23 + 8 * {256, 4096})
+  const float2 b45 = make_float2(-8912896.f, -8390656.f);  // -(2^23 + 8 * {65536, 256})
+  const float2 b67 = make_float2(-8421376.f, -8912896.f);  // -(2^23 + 8 * {4096, 65536})
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t a = v[t], s = v[t] >> 12;
+    const float2 d01 = __fadd2_rn(make_float2(__uint_as_float((a & 0xFu) | M), __uint_as_float((a & 0xF0u) | M)), b01);
+    const float2 d23 = __fadd2_rn(make_float2(__uint_as_float((a & 0xF00u) | M), __uint_as_float((a & 0xF000u) | M)), b23);
+    const float2 d45 = __fadd2_rn(make_float2(__uint_as_float((a & 0xF0000u) | M), __uint_as_float((s & 0xF00u) | M)), b45);
+    const float2 d67 = __fadd2_rn(make_float2(__uint_as_float((s & 0xF000u) | M), __uint_as_float((s & 0xF0000u) | M)), b67);
+    acc[t] = __ffma2_rn(d01, xr[4 * t + 0], acc[t]);
+    acc[t] = __ffma2_rn(d23, xr[4 * t + 1], acc[t]);
+    acc[t] = __ffma2_rn(d45, xr[4 * t + 2], acc[t]);
+    acc[t] = __ffma2_rn(d67, xr[4 * t + 3], acc[t]);
+  }
+}
+
+// Input registers of one chunk from the staged vector xs (natural order).
+template <int F>
+__device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr) {
+  if constexpr (F == MIE_FMT_Q4_0) {
+    const float sc[8] = {1.f, 0.0625f, 0.00390625f, 0.000244140625f, 1.52587890625e-05f,
+                         0.00390625f, 0.000244140625f, 1.52587890625e-05f};
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int src[8] = {4 * t, 4 * t + 16, 4 * t + 1, 4 * t + 17, 4 * t + 2, 4 * t + 18, 4 * t + 3, 4 * t + 19};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        xr[4 * t + i] = make_float2(xs[e + src[2 * i]] * sc[2 * i], xs[e + src[2 * i + 1]] * sc[2 * i + 1]);
+    }
+  } else {
+    constexpr int EPC = FmtT<F>::EPC;
+#pragma unroll
+    for (int i = 0; i < EPC / 4; ++i) {
+      const float4 q = *reinterpret_cast<const float4 *>(xs + e + 4 * i);
+      xr[2 * i] = make_float2(q.x, q.y);
+      xr[2 * i + 1] = make_float2(q.z, q.w);
+    }
+  }
+}
+
+// --------------------------------------------------------------- mbarrier / bulk copy
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Waits for the phase of the given parity to complete; gives up after a bounded number
+// of polls (each poll may suspend the thread for a hardware-defined time) and returns
+// false, so a lost transfer can never hang the GPU.
+constexpr long kWaitPolls = 1L << 22;
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+  const uint32_t addr = smem_u32(bar);
+  for (long it = 0; it < kWaitPolls; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (ok) return true;
+  }
+  return false;
+}
+
+// One bulk (TMA 1-D) copy global -> shared, completing on an mbarrier; weights are
+// streamed once, so they are marked evict-first in L2.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bulk prefetch of global memory into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint64_t evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
+  return v > bv || (v == bv && i < bi);
+}
+
+// Stages a GEMV input vector into shared memory xs[0..Kp) (zeros past K), applying the
+// prologue: PRO_PLAIN copies x; PRO_NORM applies RMSNorm with the gain; PRO_EMBED_NORM
+// gathers row sp->token of the embedding first (CTA 0 also stores it as the residual).
+// With act_bf16 the staged values are rounded to bf16.  Each thread issues a batch of
+// independent loads (addresses clamped into range, values masked afterwards) before
+// its first shared-memory store, so the staging costs one round trip per batch instead
+// of one per element.  NT threads take part; Sync is a barrier over them.
+template <int NT, class Sync>
+__device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp, float *red, float *scale_slot,
+                            int *err) {
+  constexpr int B = 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // a vector that one batch covers gets its gains loaded together with its values
+  const bool one_batch = pro != PRO_PLAIN && K <= NT * B;
+  float g0[B];
+  if (one_batch) {
+#pragma unroll
+    for (int j = 0; j < B; ++j) g0[j] = __ldg(a.gain + min(tid + j * NT, K - 1));
+  }
+  if (pro == PRO_EMBED_NORM) {
+    int tok = a.sp ? a.sp->token[a.slot] : 0;
+    if (tok < 0 || tok >= a.vocab) {
+      if (tid == 0 && blockIdx.x == 0) latch_error(err, ERR_TOKEN);
+      tok = 0;
+    }
+    for (int k0 = tid; k0 < Kp; k0 += NT * B) {
+      float v[B];
+#pragma unroll
+      for (int j = 0; j < B; ++j) v[j] = embed_at(a.embed, tok, min(k0 + j * NT, K - 1));
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        const int k = k0 + j * NT;
+        if (k < Kp) xs[k] = (k < K) ? v[j] : 0.f;
+        if (blockIdx.x == 0 && k < K) a.x_store[k] = v[j];
+      }
+    }
+  } else {
+    for (int k0 = tid; k0 < Kp; k0 += NT * B) {
+      float v[B];
+#pragma unroll
+      for (int j = 0; j < B; ++j) v[j] = __ldcg(a.x + min(k0 + j * NT, K - 1));
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        const int k = k0 + j * NT;
+        if (k < Kp) xs[k] = (k < K) ? v[j] : 0.f;
+      }
+    }
+  }
+  if (pro != PRO_PLAIN) {
+    float ss = 0.f;
+    for (int k = tid; k < K; k += NT) ss += xs[k] * xs[k];
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    Sync::sync();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < NT / 32; ++w) t += red[w];
+      *scale_slot = 1.0f / sqrtf(t / (float)K + a.eps);
+    }
+    Sync::sync();
+    const float r = *scale_slot;
+    for (int k0 = tid; k0 < K; k0 += NT * B) {
+      float g[B];
+#pragma unroll
+      for (int j = 0; j < B; ++j) g[j] = one_batch ? g0[j] : __ldg(a.gain + min(k0 + j * NT, K - 1));
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        const int k = k0 + j * NT;
+        if (k < K) {
+          float v = xs[k] * r * g[j];
+          if (a.act_bf16) v = round_bf16(v);
+          xs[k] = v;
+        }
+      }
+    }
+  } else if (a.act_bf16) {
+    for (int k = tid; k < K; k += NT) xs[k] = round_bf16(xs[k]);
+  }
+  Sync::sync();
+}
+
+// What the QKV epilogue needs besides the GEMV results, read before the weights are
+// streamed so that the epilogue issues no dependent loads: the position, its KV
+// block, and the rows of RoPE angles for that position.
+struct QkvPrefetch {
+  int pos = 0, blk = -1;
+  bool pos_ok = false, blk_ok = false;
+  const float *crow = nullptr, *srow = nullptr;
+};
+
+__device__ __forceinline__ QkvPrefetch qkv_prefetch(const GemvArgs &a) {
+  QkvPrefetch q;
+  q.pos = a.sp->pos[a.slot];
+  const int h2 = a.hd / 2;
+  q.pos_ok = q.pos >= 0 && q.pos < a.max_pos && q.pos / a.bs < a.sp->max_blocks;
+  const int pos_c = q.pos_ok ? q.pos : 0;
+  q.blk = a.sp->block_table[(int64_t)a.slot * a.sp->max_blocks + pos_c / a.bs];
+  q.blk_ok = q.pos_ok && q.blk >= 0 && q.blk < a.n_kv_blocks;
+  q.crow = a.rope_cos + (int64_t)pos_c * h2;
+  q.srow = a.rope_sin + (int64_t)pos_c * h2;
+  return q;
+}
+
+// The QKV epilogue for pair unit u: RoPE on q and k rows, q to q_out, bf16 k/v into
+// the paged cache.  x0, x1 are the GEMV results of rows i and i + hd/2 of head h.
+__device__ __forceinline__ void qkv_store(const GemvArgs &a, const QkvPrefetch &q, int u, float x0, float x1) {
+  const int h2 = a.hd / 2;
+  const int h = u / h2, i = u % h2;
+  if (h < a.Hq + a.Hkv && q.pos_ok) {
+    const float c = q.crow[i], sn = q.srow[i];
+    const float r0 = x0 * c - x1 * sn, r1 = x1 * c + x0 * sn;
+    x0 = r0;
+    x1 = r1;
+  }
+  if (h < a.Hq) {
+    a.q_out[h * a.hd + i] = x0;
+    a.q_out[h * a.hd + i + h2] = x1;
+  } else if (q.blk_ok) {
+    const int isv = h >= a.Hq + a.Hkv;
+    const int g = h - a.Hq - (isv ? a.Hkv : 0);
+    uint16_t *dst = a.kv_layer + (int64_t)q.blk * a.block_stride + (int64_t)isv * a.Hkv * a.bs * a.hd +
+                    ((int64_t)g * a.bs + q.pos % a.bs) * a.hd;
+    dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
+    dst[i + h2] = __bfloat16_as_ushort(__float2bfloat16_rn(x1));
+  }
+}
+
+}  // namespace mie

@@ -30,7 +30,7 @@
 #include <cstdarg>
 #include <cstdio>
 
-#include "internal.h"
+#include "device.cuh"
 
 namespace mie {
 
@@ -39,14 +39,6 @@ constexpr int kThreads = 32 * (kCWarps + 1);  // + one producer warp
 constexpr int kMaxStages = 16;
 constexpr size_t kSmemBudget = 110 * 1024;    // two such CTAs fit on one SM
 constexpr size_t kSmemMax = 200 * 1024;
-
-template <int F> struct FmtT;
-// EPC: elements per 16-byte chunk; CPL: chunks per lane per 2048-column slice.
-template <> struct FmtT<MIE_FMT_BF16> { static constexpr int EPC = 8, CPL = 8; };
-template <> struct FmtT<MIE_FMT_I8> { static constexpr int EPC = 16, CPL = 4; };
-template <> struct FmtT<MIE_FMT_Q4_0> { static constexpr int EPC = 32, CPL = 2; };
-constexpr int kSlice = 2048;  // = 32 * EPC * CPL for every format
-constexpr int kMaxK = kSlice * kCWarps;
 
 int gemv_chunk_elems(int fmt) {
   return fmt == MIE_FMT_BF16 ? 8 : fmt == MIE_FMT_I8 ? 16 : fmt == MIE_FMT_Q4_0 ? 32 : 0;
@@ -65,160 +57,12 @@ int sm_count() {
   return cached[dev];
 }
 
-// --------------------------------------------------------------- element decoding
-
-__device__ __forceinline__ float embed_at(const DevMat &m, int row, int k) {
-  if (m.fmt == MIE_FMT_BF16) {
-    return bf16_bits_to_f32(reinterpret_cast<const uint16_t *>(m.w + (int64_t)row * m.row_bytes)[k]);
-  } else if (m.fmt == MIE_FMT_I8) {
-    const int8_t q = reinterpret_cast<const int8_t *>(m.w + (int64_t)row * m.row_bytes)[k];
-    return reinterpret_cast<const float *>(m.s)[row] * (float)q;
-  } else {
-    const uint8_t byte = m.w[(int64_t)row * m.row_bytes + (k >> 5) * 16 + (k & 15)];
-    const int code = ((k & 31) < 16) ? (byte & 0xF) : (byte >> 4);
-    const float h = __half2float(reinterpret_cast<const __half *>(m.s)[(int64_t)row * m.s_stride + (k >> 5)]);
-    return h * (float)(code - 8);
-  }
-}
-
-// Dot product of one 16-byte chunk with the lane's input registers.
-template <int F>
-__device__ __forceinline__ void chunk_fma(const uint4 &w, const float2 *xr, float2 *acc);
-
-template <>
-__device__ __forceinline__ void chunk_fma<MIE_FMT_BF16>(const uint4 &w, const float2 *xr, float2 *acc) {
-  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const float2 wf = make_float2(__uint_as_float(v[t] << 16), __uint_as_float(v[t] & 0xffff0000u));
-    acc[t] = __ffma2_rn(wf, xr[t], acc[t]);
-  }
-}
-
-template <>
-__device__ __forceinline__ void chunk_fma<MIE_FMT_I8>(const uint4 &w, const float2 *xr, float2 *acc) {
-  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-  const float2 bias = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint32_t u = v[t] ^ 0x80808080u;  // int8 b -> b + 128 in 0..255
-    const float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
-    const float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
-    acc[t] = __ffma2_rn(__fadd2_rn(a, bias), xr[2 * t], acc[t]);
-    acc[t] = __ffma2_rn(__fadd2_rn(b, bias), xr[2 * t + 1], acc[t]);
-  }
-}
-
-// Q4_0 chunk = one block: word t holds bytes 4t..4t+3; byte j carries element j (low
-// nibble) and element j+16 (high nibble).  Unpack order per word, with the bit offset
-// p the code sits at: 4t(p0) 4t+16(p4) 4t+1(p8) 4t+17(p12) 4t+2(p16), then from
-// w >> 12: 4t+18(p8) 4t+3(p12) 4t+19(p16).  The input registers hold x * 2^-p in
-// that order, so (2^23 + n 2^p) - (2^23 + 8 2^p) = (n - 8) 2^p times them is
-// (n - 8) x.
-template <>
-__device__ __forceinline__ void chunk_fma<MIE_FMT_Q4_0>(const uint4 &w, const float2 *xr, float2 *acc) {
-  const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-  const uint32_t M = 0x4B000000u;
-  const float2 b01 = make_float2(-8388616.f, -8388736.f);  // -(2^23 + 8 * {1, 16})
-  const float2 b23 = make_float2(-8390656.f, -8421376.f);  // -(2^23 + 8 * {256, 4096})
-  const float2 b45 = make_float2(-8912896.f, -8390656.f);  // -(2^23 + 8 * {65536, 256})
-  const float2 b67 = make_float2(-8421376.f, -8912896.f);  // -(2^23 + 8 * {4096, 65536})
-#pragma unroll
-  for (int t = 0; t < 4; ++t) {
-    const uint32_t a = v[t], s = v[t] >> 12;
-    const float2 d01 = __fadd2_rn(make_float2(__uint_as_float((a & 0xFu) | M), __uint_as_float((a & 0xF0u) | M)), b01);
-    const float2 d23 = __fadd2_rn(make_float2(__uint_as_float((a & 0xF00u) | M), __uint_as_float((a & 0xF000u) | M)), b23);
-    const float2 d45 = __fadd2_rn(make_float2(__uint_as_float((a & 0xF0000u) | M), __uint_as_float((s & 0xF00u) | M)), b45);
-    const float2 d67 = __fadd2_rn(make_float2(__uint_as_float((s & 0xF000u) | M), __uint_as_float((s & 0xF0000u) | M)), b67);
-    acc[t] = __ffma2_rn(d01, xr[4 * t + 0], acc[t]);
-    acc[t] = __ffma2_rn(d23, xr[4 * t + 1], acc[t]);
-    acc[t] = __ffma2_rn(d45, xr[4 * t + 2], acc[t]);
-    acc[t] = __ffma2_rn(d67, xr[4 * t + 3], acc[t]);
-  }
-}
-
-// Input registers of one chunk from the staged vector xs (natural order).
-template <int F>
-__device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr) {
-  if constexpr (F == MIE_FMT_Q4_0) {
-    const float sc[8] = {1.f, 0.0625f, 0.00390625f, 0.000244140625f, 1.52587890625e-05f,
-                         0.00390625f, 0.000244140625f, 1.52587890625e-05f};
-#pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const int src[8] = {4 * t, 4 * t + 16, 4 * t + 1, 4 * t + 17, 4 * t + 2, 4 * t + 18, 4 * t + 3, 4 * t + 19};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        xr[4 * t + i] = make_float2(xs[e + src[2 * i]] * sc[2 * i], xs[e + src[2 * i + 1]] * sc[2 * i + 1]);
-    }
-  } else {
-    constexpr int EPC = FmtT<F>::EPC;
-#pragma unroll
-    for (int i = 0; i < EPC / 4; ++i) {
-      const float4 q = *reinterpret_cast<const float4 *>(xs + e + 4 * i);
-      xr[2 * i] = make_float2(q.x, q.y);
-      xr[2 * i + 1] = make_float2(q.z, q.w);
-    }
-  }
-}
-
-// --------------------------------------------------------------- mbarrier / bulk copy
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Waits for the phase of the given parity to complete; gives up after a bounded number
-// of polls (each poll may suspend the thread for a hardware-defined time) and returns
-// false, so a lost transfer can never hang the GPU.
-constexpr long kWaitPolls = 1L << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
-  const uint32_t addr = smem_u32(bar);
-  for (long it = 0; it < kWaitPolls; ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (ok) return true;
-  }
-  return false;
-}
-
-// One bulk (TMA 1-D) copy global -> shared, completing on an mbarrier; weights are
-// streamed once, so they are marked evict-first in L2.
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
-      : "memory");
-}
-
-__device__ __forceinline__ uint64_t evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-
 // Barrier over the consumer warps only (the producer warp never joins it).
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory"); }
+struct CSync {
+  __device__ static void sync() { consumer_sync(); }
+};
 
-__device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
-  return v > bv || (v == bv && i < bi);
-}
 
 // --------------------------------------------------------------- the kernel
 //
@@ -307,43 +151,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 
   // ---------------------------------------------------------------- consumers
   pdl_wait();
-  if constexpr (PRO == PRO_EMBED_NORM) {
-    int tok = a.sp ? a.sp->token[a.slot] : 0;
-    if (tok < 0 || tok >= a.vocab) {
-      if (tid == 0 && blockIdx.x == 0) latch_error(a.err, ERR_TOKEN);
-      tok = 0;
-    }
-    for (int k = tid; k < Kp; k += kCWarps * 32) {
-      const float v = (k < K) ? embed_at(a.embed, tok, k) : 0.f;
-      xs[k] = v;
-      if (blockIdx.x == 0 && k < K) a.x_store[k] = v;
-    }
-  } else {
-    for (int k = tid; k < Kp; k += kCWarps * 32) xs[k] = (k < K) ? a.x[k] : 0.f;
-  }
-  if constexpr (PRO != PRO_PLAIN) {
-    float ss = 0.f;
-    for (int k = tid; k < K; k += kCWarps * 32) ss += xs[k] * xs[k];
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    consumer_sync();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < kCWarps; ++w) t += red[w];
-      s_scale = 1.0f / sqrtf(t / (float)K + a.eps);
-    }
-    consumer_sync();
-    const float r = s_scale;
-    for (int k = tid; k < K; k += kCWarps * 32) {
-      float v = xs[k] * r * a.gain[k];
-      if (a.act_bf16) v = round_bf16(v);
-      xs[k] = v;
-    }
-  } else {
-    if (a.act_bf16)
-      for (int k = tid; k < K; k += kCWarps * 32) xs[k] = round_bf16(xs[k]);
-  }
-  consumer_sync();
+  stage_input<kCWarps * 32, CSync>(a, PRO, xs, K, Kp, red, &s_scale, a.err);
+  QkvPrefetch qp;
+  if constexpr (EPI == EPI_QKV) qp = qkv_prefetch(a);
 
   const int ri = warp / KS, ks = warp % KS;
   const bool has_slice = warp < RPS * KS;
@@ -439,36 +249,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
       a.y[u] = g / (1.0f + expf(-g)) * up;
     }
   } else if constexpr (EPI == EPI_QKV) {
-    // packed rows 2p, 2p+1 = rows i and i + hd/2 of head h (p = h * hd/2 + i)
-    const int pos = a.sp->pos[a.slot];
-    const int h2 = a.hd / 2;
-    const int32_t *bt = a.sp->block_table + (int64_t)a.slot * a.sp->max_blocks;
-    const bool pos_ok = pos >= 0 && pos < a.max_pos && pos / a.bs < a.sp->max_blocks;
-    int blk = -1;
-    if (pos_ok) blk = bt[pos / a.bs];
-    const bool blk_ok = pos_ok && blk >= 0 && blk < a.n_kv_blocks;
-    if (tid == 0 && blockIdx.x == 0 && !blk_ok) latch_error(a.err, pos_ok ? ERR_BLOCK_ID : ERR_POS);
-    for (int u = u0 + tid; u < u1; u += kCT) {
-      const int h = u / h2, i = u % h2;
-      float x0 = row_value(2 * u), x1 = row_value(2 * u + 1);
-      if (h < a.Hq + a.Hkv && pos_ok) {
-        const float c = a.rope_cos[(int64_t)pos * h2 + i], sn = a.rope_sin[(int64_t)pos * h2 + i];
-        const float r0 = x0 * c - x1 * sn, r1 = x1 * c + x0 * sn;
-        x0 = r0;
-        x1 = r1;
-      }
-      if (h < a.Hq) {
-        a.q_out[h * a.hd + i] = x0;
-        a.q_out[h * a.hd + i + h2] = x1;
-      } else if (blk_ok) {
-        const int isv = h >= a.Hq + a.Hkv;
-        const int g = h - a.Hq - (isv ? a.Hkv : 0);
-        uint16_t *dst = a.kv_layer + (int64_t)blk * a.block_stride + (int64_t)isv * a.Hkv * a.bs * a.hd +
-                        ((int64_t)g * a.bs + pos % a.bs) * a.hd;
-        dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
-        dst[i + h2] = __bfloat16_as_ushort(__float2bfloat16_rn(x1));
-      }
-    }
+    if (tid == 0 && blockIdx.x == 0 && !qp.blk_ok) latch_error(a.err, qp.pos_ok ? ERR_BLOCK_ID : ERR_POS);
+    for (int u = u0 + tid; u < u1; u += kCT) qkv_store(a, qp, u, row_value(2 * u), row_value(2 * u + 1));
   } else if constexpr (EPI == EPI_ARGMAX) {
     float *logits = a.y ? a.y : (a.sp ? a.sp->logits_out : nullptr);
     if (logits && a.sp && !a.y) logits += (int64_t)a.slot * M;

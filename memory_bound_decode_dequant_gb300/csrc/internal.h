@@ -84,6 +84,34 @@ size_t attn_workspace_bytes(int Hq, int Hkv, int hd, int n_splits);
 int attn_splits_for(int Hkv, int max_ctx, int bs);
 mie_status launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl);
 
+// The whole step as one persistent cooperative kernel (step.cu).
+enum { PH_GEMV = 0, PH_ATTN = 1 };
+struct Phase {
+  int kind = PH_GEMV, pro = PRO_PLAIN, epi = EPI_STORE;
+  GemvArgs g;
+  AttnArgs at;
+};
+struct PersistArgs {
+  const Phase *ph = nullptr;  // device array of n_phases descriptors
+  int n_phases = 0;
+  unsigned *done = nullptr;   // [n_phases] grid-barrier counters, zero between launches
+  unsigned *reset_flag = nullptr;
+  int *abort = nullptr;       // nonzero once a bounded wait gave up
+  int n_slots = 0;
+  uint32_t slot_bytes = 0, slot_sc_bytes = 0;
+  int *err = nullptr;
+  unsigned long long *trace = nullptr;  // [n_phases][grid][kTracePoints] globaltimer ns, or null
+};
+constexpr int kTracePoints = 5;  // phase entry, barrier passed, input staged, stages consumed, outputs written
+struct PersistPlan {
+  const void *kernel = nullptr;
+  int grid = 0, threads = 0, n_slots = 0;
+  uint32_t slot_bytes = 0, slot_sc_bytes = 0;
+  size_t smem = 0;
+};
+mie_status persist_plan(const Phase *host_phases, int n, int G, int HD, PersistPlan *plan);
+mie_status persist_launch(const PersistPlan &plan, const PersistArgs &args, cudaStream_t st);
+
 // Load-time kernels.
 mie_status launch_convert_bf16(const float *w, int64_t n, uint16_t *out, cudaStream_t st);
 mie_status launch_quantize_i8(const float *w, int M, int K, int8_t *q, float *s, cudaStream_t st);

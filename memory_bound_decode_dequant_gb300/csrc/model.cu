@@ -107,9 +107,20 @@ struct mie_ctx {
   StepParams sp_host{};
   int *err = nullptr;
   cudaGraphExec_t graph = nullptr;
+  bool graph_ok = true;  // false: the step is launched directly (capture unsupported)
   int launches = 0;
   bool primed = false;
   mie_pool *pool = nullptr;
+  // persistent step
+  int mode = MIE_STEP_CHAIN;
+  std::vector<Phase> phases;
+  Phase *d_phases = nullptr;
+  size_t d_phases_cap = 0;
+  unsigned *done = nullptr;  // [n_phases + 1]: grid-barrier counters, then the reset flag
+  int *abort = nullptr;
+  PersistPlan plan;
+  unsigned long long *trace = nullptr;
+  size_t trace_bytes = 0;
 
   void *dalloc(size_t bytes) {
     void *p = nullptr;
@@ -188,6 +199,9 @@ extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **
   ctx->am_count = (unsigned *)ctx->dalloc(sizeof(unsigned) * 64);
   ctx->sp = (StepParams *)ctx->dalloc(sizeof(StepParams));
   ctx->err = (int *)ctx->dalloc(sizeof(int) * 4);
+  const int max_phases = 5 * c.n_layers + 1;
+  ctx->done = (unsigned *)ctx->dalloc(sizeof(unsigned) * (max_phases + 1));
+  ctx->abort = (int *)ctx->dalloc(sizeof(int));
   std::vector<float> ones((size_t)c.d_model, 1.0f);
   for (auto &L : ctx->layers) {
     L.attn_norm = (float *)ctx->dalloc(sizeof(float) * c.d_model);
@@ -195,7 +209,7 @@ extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **
   }
   ctx->final_norm = (float *)ctx->dalloc(sizeof(float) * c.d_model);
   bool ok = ctx->kv && ctx->x && ctx->q && ctx->att && ctx->act && ctx->rope_cos && ctx->rope_sin && ws &&
-            ctx->am_part && ctx->am_count && ctx->sp && ctx->err && ctx->final_norm;
+            ctx->am_part && ctx->am_count && ctx->sp && ctx->err && ctx->final_norm && ctx->done && ctx->abort;
   for (auto &L : ctx->layers) ok = ok && L.attn_norm && L.mlp_norm;
   if (!ok) {
     mie_destroy(ctx);
@@ -210,6 +224,8 @@ extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **
   chk(cudaMemsetAsync(ctx->am_count, 0, sizeof(unsigned) * 64, ctx->stream));
   chk(cudaMemsetAsync(ctx->err, 0, sizeof(int) * 4, ctx->stream));
   chk(cudaMemsetAsync(ctx->sp, 0, sizeof(StepParams), ctx->stream));
+  chk(cudaMemsetAsync(ctx->done, 0, sizeof(unsigned) * (max_phases + 1), ctx->stream));
+  chk(cudaMemsetAsync(ctx->abort, 0, sizeof(int), ctx->stream));
   for (auto &L : ctx->layers) {
     chk(cudaMemcpyAsync(L.attn_norm, ones.data(), sizeof(float) * c.d_model, cudaMemcpyHostToDevice, ctx->stream));
     chk(cudaMemcpyAsync(L.mlp_norm, ones.data(), sizeof(float) * c.d_model, cudaMemcpyHostToDevice, ctx->stream));
@@ -463,111 +479,165 @@ static bool all_loaded(const mie_ctx *ctx) {
   return true;
 }
 
-// Enqueues one decode step for slot 0 (the graph body).
-static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
+// The step's phases for slot 0, in execution order.
+static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
   const mie_config &c = ctx->cfg;
-  cudaStream_t st = ctx->stream;
-  int n = 0;
-  mie_status s;
+  out.clear();
   const int64_t half = (int64_t)c.n_kv_heads * c.block_size * c.head_dim;
   for (int l = 0; l < c.n_layers; ++l) {
     Layer &L = ctx->layers[(size_t)l];
     uint16_t *kv_layer = ctx->kv + (int64_t)l * 2 * half;
-    {  // qkv + RoPE + K/V write
-      GemvArgs a;
-      a.m = L.qkv;
-      a.x = ctx->x;
-      a.gain = L.attn_norm;
-      a.eps = c.rms_eps;
-      a.act_bf16 = c.act_bf16;
-      a.embed = ctx->embed;
-      a.x_store = ctx->x;
-      a.vocab = c.vocab;
-      a.q_out = ctx->q;
-      a.kv_layer = kv_layer;
-      a.block_stride = ctx->block_elems;
-      a.n_kv_blocks = c.n_kv_blocks;
-      a.rope_cos = ctx->rope_cos;
-      a.rope_sin = ctx->rope_sin;
-      a.max_pos = c.max_pos;
-      a.Hq = c.n_heads;
-      a.Hkv = c.n_kv_heads;
-      a.hd = c.head_dim;
-      a.bs = c.block_size;
-      a.sp = ctx->sp;
-      a.err = ctx->err;
-      if ((s = launch_gemv(l == 0 ? PRO_EMBED_NORM : PRO_NORM, EPI_QKV, a, gemv_default_grid(a.m, EPI_QKV), st,
-                           true)) != MIE_OK)
-        return s;
-      ++n;
-    }
-    {  // attention
-      AttnArgs a;
-      a.q = ctx->q;
-      a.k = kv_layer;
-      a.v = kv_layer + half;
-      a.block_stride = ctx->block_elems;
-      a.n_pool_blocks = c.n_kv_blocks;
-      a.sp = ctx->sp;
-      a.Hq = c.n_heads;
-      a.Hkv = c.n_kv_heads;
-      a.hd = c.head_dim;
-      a.bs = c.block_size;
-      a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
-      a.out = ctx->att;
-      a.ws_part = ctx->attn_part;
-      a.ws_count = ctx->attn_count;
-      a.n_splits = ctx->attn_splits;
-      a.err = ctx->err;
-      if ((s = launch_attn(a, st, true)) != MIE_OK) return s;
-      ++n;
-    }
-    {  // x += Wo att
-      GemvArgs a;
-      a.m = L.o;
-      a.x = ctx->att;
-      a.act_bf16 = c.act_bf16;
-      a.y = ctx->x;
-      if ((s = launch_gemv(PRO_PLAIN, EPI_RESID, a, gemv_default_grid(a.m, EPI_RESID), st, true)) != MIE_OK) return s;
-      ++n;
-    }
-    {  // act = silu(Wg n(x)) * (Wu n(x))
-      GemvArgs a;
-      a.m = L.gu;
-      a.x = ctx->x;
-      a.gain = L.mlp_norm;
-      a.eps = c.rms_eps;
-      a.act_bf16 = c.act_bf16;
-      a.y = ctx->act;
-      if ((s = launch_gemv(PRO_NORM, EPI_SWIGLU, a, gemv_default_grid(a.m, EPI_SWIGLU), st, true)) != MIE_OK) return s;
-      ++n;
-    }
-    {  // x += Wd act
-      GemvArgs a;
-      a.m = L.down;
-      a.x = ctx->act;
-      a.act_bf16 = c.act_bf16;
-      a.y = ctx->x;
-      if ((s = launch_gemv(PRO_PLAIN, EPI_RESID, a, gemv_default_grid(a.m, EPI_RESID), st, true)) != MIE_OK) return s;
-      ++n;
-    }
-  }
-  {  // logits = Whead n(x); argmax
-    GemvArgs a;
-    a.m = ctx->head;
+    Phase qkv;  // qkv + RoPE + K/V write (layer 0 gathers the embedding first)
+    qkv.kind = PH_GEMV;
+    qkv.pro = l == 0 ? PRO_EMBED_NORM : PRO_NORM;
+    qkv.epi = EPI_QKV;
+    GemvArgs &a = qkv.g;
+    a.m = L.qkv;
     a.x = ctx->x;
-    a.gain = ctx->final_norm;
+    a.gain = L.attn_norm;
     a.eps = c.rms_eps;
     a.act_bf16 = c.act_bf16;
-    a.y = nullptr;
-    a.am_part = ctx->am_part;
-    a.am_count = ctx->am_count;
+    a.embed = ctx->embed;
+    a.x_store = ctx->x;
+    a.vocab = c.vocab;
+    a.q_out = ctx->q;
+    a.kv_layer = kv_layer;
+    a.block_stride = ctx->block_elems;
+    a.n_kv_blocks = c.n_kv_blocks;
+    a.rope_cos = ctx->rope_cos;
+    a.rope_sin = ctx->rope_sin;
+    a.max_pos = c.max_pos;
+    a.Hq = c.n_heads;
+    a.Hkv = c.n_kv_heads;
+    a.hd = c.head_dim;
+    a.bs = c.block_size;
     a.sp = ctx->sp;
     a.err = ctx->err;
-    if ((s = launch_gemv(PRO_NORM, EPI_ARGMAX, a, gemv_default_grid(a.m, EPI_ARGMAX), st, true)) != MIE_OK) return s;
+    out.push_back(qkv);
+
+    Phase at;
+    at.kind = PH_ATTN;
+    AttnArgs &t = at.at;
+    t.q = ctx->q;
+    t.k = kv_layer;
+    t.v = kv_layer + half;
+    t.block_stride = ctx->block_elems;
+    t.n_pool_blocks = c.n_kv_blocks;
+    t.sp = ctx->sp;
+    t.Hq = c.n_heads;
+    t.Hkv = c.n_kv_heads;
+    t.hd = c.head_dim;
+    t.bs = c.block_size;
+    t.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+    t.out = ctx->att;
+    t.ws_part = ctx->attn_part;
+    t.ws_count = ctx->attn_count;
+    t.n_splits = ctx->attn_splits;
+    t.err = ctx->err;
+    out.push_back(at);
+
+    Phase o;  // x += Wo att
+    o.kind = PH_GEMV;
+    o.pro = PRO_PLAIN;
+    o.epi = EPI_RESID;
+    o.g.m = L.o;
+    o.g.x = ctx->att;
+    o.g.act_bf16 = c.act_bf16;
+    o.g.y = ctx->x;
+    o.g.err = ctx->err;
+    out.push_back(o);
+
+    Phase gu;  // act = silu(Wg n(x)) * (Wu n(x))
+    gu.kind = PH_GEMV;
+    gu.pro = PRO_NORM;
+    gu.epi = EPI_SWIGLU;
+    gu.g.m = L.gu;
+    gu.g.x = ctx->x;
+    gu.g.gain = L.mlp_norm;
+    gu.g.eps = c.rms_eps;
+    gu.g.act_bf16 = c.act_bf16;
+    gu.g.y = ctx->act;
+    gu.g.err = ctx->err;
+    out.push_back(gu);
+
+    Phase dn;  // x += Wd act
+    dn.kind = PH_GEMV;
+    dn.pro = PRO_PLAIN;
+    dn.epi = EPI_RESID;
+    dn.g.m = L.down;
+    dn.g.x = ctx->act;
+    dn.g.act_bf16 = c.act_bf16;
+    dn.g.y = ctx->x;
+    dn.g.err = ctx->err;
+    out.push_back(dn);
+  }
+  Phase hd;  // logits = Whead n(x); argmax
+  hd.kind = PH_GEMV;
+  hd.pro = PRO_NORM;
+  hd.epi = EPI_ARGMAX;
+  hd.g.m = ctx->head;
+  hd.g.x = ctx->x;
+  hd.g.gain = ctx->final_norm;
+  hd.g.eps = c.rms_eps;
+  hd.g.act_bf16 = c.act_bf16;
+  hd.g.am_part = ctx->am_part;
+  hd.g.am_count = ctx->am_count;
+  hd.g.sp = ctx->sp;
+  hd.g.err = ctx->err;
+  out.push_back(hd);
+}
+
+// Enqueues one decode step (the graph body) and counts its kernel launches.
+static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
+  cudaStream_t st = ctx->stream;
+  mie_status s;
+  if (ctx->mode == MIE_STEP_PERSISTENT) {
+    PersistArgs pa;
+    pa.ph = ctx->d_phases;
+    pa.n_phases = (int)ctx->phases.size();
+    pa.done = ctx->done;
+    pa.reset_flag = ctx->done + ctx->phases.size();
+    pa.abort = ctx->abort;
+    pa.n_slots = ctx->plan.n_slots;
+    pa.slot_bytes = ctx->plan.slot_bytes;
+    pa.slot_sc_bytes = ctx->plan.slot_sc_bytes;
+    pa.err = ctx->err;
+    const size_t need = sizeof(unsigned long long) * ctx->phases.size() * ctx->plan.grid * kTracePoints;
+    pa.trace = (ctx->trace && ctx->trace_bytes >= need) ? ctx->trace : nullptr;
+    if ((s = persist_launch(ctx->plan, pa, st)) != MIE_OK) return s;
+    *launches = 1;
+    return MIE_OK;
+  }
+  int n = 0;
+  for (const Phase &ph : ctx->phases) {
+    if (ph.kind == PH_GEMV) s = launch_gemv(ph.pro, ph.epi, ph.g, gemv_default_grid(ph.g.m, ph.epi), st, true);
+    else s = launch_attn(ph.at, st, true);
+    if (s != MIE_OK) return s;
     ++n;
   }
   *launches = n;
+  return MIE_OK;
+}
+
+// Builds the phase list, uploads it and plans the persistent kernel; a shape the
+// persistent kernel does not cover falls back to the kernel chain.
+static mie_status prepare_step(mie_ctx *ctx) {
+  build_phases(ctx, ctx->phases);
+  const size_t bytes = sizeof(Phase) * ctx->phases.size();
+  if (ctx->d_phases_cap < bytes) {
+    Phase *p = (Phase *)ctx->dalloc(bytes);
+    if (!p) return fail(MIE_E_OOM, "decode step: phase table");
+    ctx->d_phases = p;
+    ctx->d_phases_cap = bytes;
+  }
+  MIE_CUDA(cudaMemcpyAsync(ctx->d_phases, ctx->phases.data(), bytes, cudaMemcpyHostToDevice, ctx->stream));
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  if (ctx->mode == MIE_STEP_PERSISTENT &&
+      persist_plan(ctx->phases.data(), (int)ctx->phases.size(), ctx->cfg.n_heads / ctx->cfg.n_kv_heads,
+                   ctx->cfg.head_dim, &ctx->plan) != MIE_OK) {
+    cudaGetLastError();
+    ctx->mode = MIE_STEP_CHAIN;  // a shape the persistent kernel does not cover
+  }
   return MIE_OK;
 }
 
@@ -576,22 +646,34 @@ static mie_status capture(mie_ctx *ctx) {
     cudaGraphExecDestroy(ctx->graph);
     ctx->graph = nullptr;
   }
+  mie_status s = prepare_step(ctx);
+  if (s != MIE_OK) return s;
+  ctx->graph_ok = true;
   cudaGraph_t g = nullptr;
   MIE_CUDA(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
   int n = 0;
-  mie_status s = enqueue_step(ctx, &n);
+  s = enqueue_step(ctx, &n);
   cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
-  if (s != MIE_OK) {
-    if (g) cudaGraphDestroy(g);
-    return s;
+  if (s == MIE_OK && e == cudaSuccess) e = cudaGraphInstantiate(&ctx->graph, g, 0);
+  if (g) cudaGraphDestroy(g);
+  if (s != MIE_OK || e != cudaSuccess) {
+    // the launch is not capturable here: run the step without a graph
+    cudaGetLastError();
+    ctx->graph = nullptr;
+    ctx->graph_ok = false;
   }
-  if (e != cudaSuccess) return cuda_fail(e, "decode step: cudaStreamEndCapture");
-  e = cudaGraphInstantiate(&ctx->graph, g, 0);
-  cudaGraphDestroy(g);
-  if (e != cudaSuccess) return cuda_fail(e, "decode step: cudaGraphInstantiate");
   ctx->launches = n;
   ctx->primed = true;
   return MIE_OK;
+}
+
+static mie_status run_step(mie_ctx *ctx) {
+  if (ctx->graph_ok && ctx->graph) {
+    MIE_CUDA(cudaGraphLaunch(ctx->graph, ctx->stream));
+    return MIE_OK;
+  }
+  int n = 0;
+  return enqueue_step(ctx, &n);
 }
 
 extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, const int32_t *block_table,
@@ -618,15 +700,17 @@ extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, 
     mie_status s = capture(ctx);
     if (s != MIE_OK) return s;
   }
-  MIE_CUDA(cudaGraphLaunch(ctx->graph, ctx->stream));
-  return MIE_OK;
+  return run_step(ctx);
 }
 
 extern "C" mie_status mie_decode_continue(mie_ctx *ctx, int n_steps) {
   if (!ctx) return fail(MIE_E_ARG, "mie_decode_continue: null context");
-  if (!ctx->primed || !ctx->graph) return fail(MIE_E_STATE, "mie_decode_continue: call mie_decode_step first");
+  if (!ctx->primed) return fail(MIE_E_STATE, "mie_decode_continue: call mie_decode_step first");
   if (n_steps < 0) return fail(MIE_E_ARG, "mie_decode_continue: n_steps %d", n_steps);
-  for (int i = 0; i < n_steps; ++i) MIE_CUDA(cudaGraphLaunch(ctx->graph, ctx->stream));
+  for (int i = 0; i < n_steps; ++i) {
+    const mie_status s = run_step(ctx);
+    if (s != MIE_OK) return s;
+  }
   return MIE_OK;
 }
 
@@ -642,12 +726,55 @@ extern "C" mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int
 extern "C" mie_status mie_sync(mie_ctx *ctx) {
   if (!ctx) return fail(MIE_E_ARG, "mie_sync: null context");
   MIE_CUDA(cudaStreamSynchronize(ctx->stream));
-  int v = 0;
+  int v = 0, ab = 0;
   MIE_CUDA(cudaMemcpy(&v, ctx->err, sizeof(int), cudaMemcpyDeviceToHost));
+  MIE_CUDA(cudaMemcpy(&ab, ctx->abort, sizeof(int), cudaMemcpyDeviceToHost));
+  if (ab) {
+    // a bounded wait gave up: the step's counters are in an unknown state, reset them
+    const int max_phases = 5 * ctx->cfg.n_layers + 1;
+    MIE_CUDA(cudaMemset(ctx->done, 0, sizeof(unsigned) * (max_phases + 1)));
+    MIE_CUDA(cudaMemset(ctx->abort, 0, sizeof(int)));
+    MIE_CUDA(cudaMemset(ctx->am_count, 0, sizeof(unsigned) * 64));
+    MIE_CUDA(cudaMemset(ctx->attn_count, 0, sizeof(unsigned) * ctx->cfg.n_kv_heads));
+    MIE_CUDA(cudaMemset(ctx->err, 0, sizeof(int)));
+    return fail(MIE_E_TIMEOUT, "decode step: a bounded device wait gave up (code %d)", v);
+  }
   if (v) {
     MIE_CUDA(cudaMemset(ctx->err, 0, sizeof(int)));
     return fail(MIE_E_DEVICE, "decode step: device bounds check fired (code %d)", v);
   }
+  return MIE_OK;
+}
+
+extern "C" mie_status mie_set_step_mode(mie_ctx *ctx, int mode) {
+  if (!ctx) return fail(MIE_E_ARG, "mie_set_step_mode: null context");
+  if (mode != MIE_STEP_PERSISTENT && mode != MIE_STEP_CHAIN) return fail(MIE_E_ARG, "mie_set_step_mode: mode %d", mode);
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  const int old = ctx->mode;
+  ctx->mode = mode;
+  ctx->primed = false;
+  if (mode == MIE_STEP_PERSISTENT && all_loaded(ctx)) {
+    build_phases(ctx, ctx->phases);
+    const mie_status s = persist_plan(ctx->phases.data(), (int)ctx->phases.size(),
+                                      ctx->cfg.n_heads / ctx->cfg.n_kv_heads, ctx->cfg.head_dim, &ctx->plan);
+    if (s != MIE_OK) {
+      ctx->mode = old;
+      return s;
+    }
+  }
+  return MIE_OK;
+}
+
+extern "C" int mie_step_mode(const mie_ctx *ctx) { return ctx ? ctx->mode : -1; }
+
+extern "C" mie_status mie_set_trace(mie_ctx *ctx, void *device_buffer, size_t bytes, int *n_phases, int *n_ctas) {
+  if (!ctx) return fail(MIE_E_ARG, "mie_set_trace: null context");
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  ctx->trace = static_cast<unsigned long long *>(device_buffer);
+  ctx->trace_bytes = device_buffer ? bytes : 0;
+  ctx->primed = false;  // the next step re-captures with (or without) the trace
+  if (n_phases) *n_phases = 5 * ctx->cfg.n_layers + 1;
+  if (n_ctas) *n_ctas = sm_count();
   return MIE_OK;
 }
 

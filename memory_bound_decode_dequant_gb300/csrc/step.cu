@@ -1,0 +1,646 @@
+// step.cu -- the whole decode step as one persistent kernel.
+//
+// The step ("infer" page, data-flow figure) is a chain of phases -- per layer: QKV
+// GEMV with RMSNorm prologue and RoPE + paged K/V write; attention; O-proj + residual;
+// gate/up + SwiGLU with RMSNorm prologue; down + residual; then the LM head with
+// argmax.  Launched as separate kernels every phase pays launch, ramp-up and tail
+// (about 7 us measured on GB300).  Here one cooperative grid of one CTA per SM runs
+// them all:
+//  * The weights of every GEMV phase are known before the step starts, so the
+//    producer warp of each CTA streams its share of all of them, phase after phase,
+//    through a ring of shared-memory stages (TMA bulk copies, mbarrier handoff) and
+//    never waits for activations -- only for a free slot.  HBM stays busy across phase
+//    boundaries; the ring absorbs the synchronisation latency.
+//  * Consumer warps run the phases in order.  Between phases they meet at a grid
+//    barrier: each CTA adds one to the phase's counter (release) and the next phase
+//    polls it (acquire) with a bounded loop.  The last CTA of the LM-head phase resets
+//    every counter for the next launch.
+//  * A wait that gives up sets a global abort flag (every CTA then leaves), latches an
+//    error the host reads back, and drains this CTA's copies still in flight.
+#include "attn_core.cuh"
+
+namespace mie {
+
+constexpr int kPW = 8;                     // consumer warps
+constexpr int kPThreads = 32 * (kPW + 1);  // + one producer warp
+constexpr int kPCT = kPW * 32;             // consumer threads
+constexpr int kPRingMax = 32;              // ring slots (static mbarriers)
+constexpr long kGridPolls = 1L << 25;      // bounded grid-barrier polling (~1 s)
+
+struct ConsSync {
+  __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(kPCT) : "memory"); }
+};
+
+__device__ __forceinline__ int ld_volatile(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Optional timeline: thread 0 of each CTA stamps kTracePoints moments of each phase.
+__device__ __forceinline__ void stamp(unsigned long long *trace, int phase, int point) {
+  if (trace && threadIdx.x == 0) trace[((size_t)phase * gridDim.x + blockIdx.x) * kTracePoints + point] = globaltimer();
+}
+
+__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Values fixed for the whole step, read once per launch: the position, the block ids
+// of the context (when it has at most kStepMaxBlocks blocks) and the RoPE angles of
+// the position.  Later phases read them from shared memory instead of chasing
+// pointers in global memory.
+constexpr int kStepMaxBlocks = 512;
+struct StepConst {
+  int pos, ctx, nblk_staged;
+  int blk[kStepMaxBlocks];
+  float rc[64], rs[64];
+};
+
+struct PersistShared {
+  float red[kPW];
+  float scale;
+  float bv[kPW];
+  int bi[kPW];
+  unsigned last;
+  int ok;
+};
+
+// Waits until *ctr >= target (every CTA finished the previous phase).
+__device__ bool grid_wait(const unsigned *ctr, unsigned target, int *abort, int *err, PersistShared &ps) {
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    for (long it = 0;; ++it) {
+      if (ld_acquire(ctr) >= target) break;
+      if (ld_volatile(abort)) { ok = 0; break; }
+      if (it > kGridPolls) {
+        ok = 0;
+        atomicExch(abort, 1);
+        latch_error(err, ERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(20);
+    }
+    __threadfence();
+    ps.ok = ok;
+  }
+  ConsSync::sync();
+  return ps.ok != 0;
+}
+
+__device__ void grid_signal(unsigned *ctr) {
+  __threadfence();
+  ConsSync::sync();
+  if (threadIdx.x == 0) atomicAdd(ctr, 1u);
+}
+
+// Row range of this CTA for a GEMV phase (units of RU rows, balanced over the grid).
+struct RowRange {
+  int u0, u1, row0, row1, KS, RPS, n_stages;
+};
+
+__device__ __forceinline__ RowRange row_range(const DevMat &m, int epi) {
+  RowRange r;
+  const int RU = (epi == EPI_SWIGLU || epi == EPI_QKV) ? 2 : 1;
+  const int n_units = (m.rows + RU - 1) / RU;
+  r.u0 = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
+  r.u1 = (int)((int64_t)(blockIdx.x + 1) * n_units / gridDim.x);
+  r.row0 = r.u0 * RU;
+  r.row1 = min(r.u1 * RU, m.rows);
+  r.KS = (m.kp + kSlice - 1) / kSlice;
+  r.RPS = r.KS >= kPW ? 1 : kPW / r.KS;
+  r.n_stages = r.row1 > r.row0 ? (r.row1 - r.row0 + r.RPS - 1) / r.RPS : 0;
+  return r;
+}
+
+struct Ring {
+  uint8_t *w, *sc;
+  uint32_t slot_bytes, slot_sc_bytes;
+  int nst;
+  uint64_t *full, *empty;
+};
+
+// ---------------------------------------------------------------------- GEMV phase
+
+template <int F>
+__device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, float *scratch, PersistShared &ps,
+                           const StepConst &sc, int *abort, int *err, unsigned long long *trace, int pidx) {
+  using T = FmtT<F>;
+  constexpr int EPC = T::EPC, CPL = T::CPL;
+  constexpr int kBitsPerElem = (F == MIE_FMT_BF16) ? 16 : (F == MIE_FMT_I8 ? 8 : 4);
+  constexpr int kSliceBytes = kSlice * kBitsPerElem / 8;
+  constexpr int kChunkStride = 32 * EPC;
+  const GemvArgs &a = ph.g;
+  const DevMat &m = a.m;
+  const int Kp = m.kp, K = m.cols, M = m.rows;
+  const RowRange rr = row_range(m, ph.epi);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  float *xs = scratch;       // [Kp]
+  float *part = xs + Kp;     // [rows of this CTA][KS]
+
+  QkvPrefetch qp;
+  if (ph.epi == EPI_QKV) {
+    qp.pos = sc.pos;
+    qp.pos_ok = sc.pos >= 0 && sc.pos < a.max_pos && sc.pos / a.bs < a.sp->max_blocks;
+    const int b = qp.pos_ok ? sc.pos / a.bs : 0;
+    qp.blk = (b < sc.nblk_staged) ? sc.blk[b] : a.sp->block_table[(int64_t)a.slot * a.sp->max_blocks + b];
+    qp.blk_ok = qp.pos_ok && qp.blk >= 0 && qp.blk < a.n_kv_blocks;
+    qp.crow = sc.rc;
+    qp.srow = sc.rs;
+  }
+  stage_input<kPCT, ConsSync>(a, ph.pro, xs, K, Kp, ps.red, &ps.scale, err);
+  stamp(trace, pidx, 2);
+
+  const int ri = warp / rr.KS, ks = warp % rr.KS;
+  const bool has_slice = warp < rr.RPS * rr.KS;
+  const int e0 = ks * kSlice + lane * EPC;
+  float2 xr[CPL * EPC / 2];
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const int e = e0 + c * kChunkStride;
+    if (has_slice && e < Kp) {
+      load_xr<F>(xs, e, xr + c * (EPC / 2));
+    } else {
+#pragma unroll
+      for (int i = 0; i < EPC / 2; ++i) xr[c * (EPC / 2) + i] = make_float2(0.f, 0.f);
+    }
+  }
+
+  // stream this CTA's stages of the phase
+  for (int st = 0; st < rr.n_stages; ++st, ++s_global) {
+    const int slot = s_global % ring.nst, k = s_global / ring.nst;
+    if (!mbar_wait(&ring.full[slot], k & 1)) {
+      atomicExch(abort, 1);
+      latch_error(err, ERR_TIMEOUT);
+      return false;
+    }
+    const int r = rr.row0 + st * rr.RPS + ri;
+    if (has_slice && r < rr.row1) {
+      const uint8_t *rowp =
+          ring.w + (size_t)slot * ring.slot_bytes + (size_t)ri * m.row_bytes + (size_t)ks * kSliceBytes;
+      float sum = 0.f;
+      if constexpr (F == MIE_FMT_Q4_0) {
+        const __half *hs = reinterpret_cast<const __half *>(ring.sc + (size_t)slot * ring.slot_sc_bytes) +
+                           (size_t)ri * m.s_stride + ks * (kSlice / 32);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          if (e0 + c * kChunkStride < Kp) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(rowp + (size_t)(c * 32 + lane) * 16);
+            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            chunk_fma<F>(w, xr + c * (EPC / 2), acc);
+            const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+            sum = fmaf(__half2float(hs[c * 32 + lane]), cs, sum);
+          }
+        }
+      } else {
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) {
+          if (e0 + c * kChunkStride < Kp) {
+            const uint4 w = *reinterpret_cast<const uint4 *>(rowp + (size_t)(c * 32 + lane) * 16);
+            chunk_fma<F>(w, xr + c * (EPC / 2), acc);
+          }
+        }
+        sum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+      }
+      sum = warp_sum(sum);
+      if (lane == 0) part[(r - rr.row0) * rr.KS + ks] = sum;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[slot]);
+  }
+  ConsSync::sync();
+  stamp(trace, pidx, 3);
+
+  // epilogue
+  auto row_value = [&](int r) {
+    float v = 0.f;
+    for (int q = 0; q < rr.KS; ++q) v += part[(r - rr.row0) * rr.KS + q];
+    if constexpr (F == MIE_FMT_I8) v *= reinterpret_cast<const float *>(m.s)[r];
+    return v;
+  };
+  if (ph.epi == EPI_STORE || ph.epi == EPI_RESID) {
+    for (int r = rr.row0 + tid; r < rr.row1; r += kPCT) {
+      const float v = row_value(r);
+      a.y[r] = (ph.epi == EPI_RESID) ? __ldcg(a.y + r) + v : v;
+    }
+  } else if (ph.epi == EPI_SWIGLU) {
+    for (int u = rr.u0 + tid; u < rr.u1; u += kPCT) {
+      const float g = row_value(2 * u), up = row_value(2 * u + 1);
+      a.y[u] = g / (1.0f + expf(-g)) * up;
+    }
+  } else if (ph.epi == EPI_QKV) {
+    if (tid == 0 && blockIdx.x == 0 && !qp.blk_ok) latch_error(err, qp.pos_ok ? ERR_BLOCK_ID : ERR_POS);
+    for (int u = rr.u0 + tid; u < rr.u1; u += kPCT)
+      qkv_store(a, qp, u, row_value(2 * u), row_value(2 * u + 1));
+  } else if (ph.epi == EPI_ARGMAX) {
+    float *logits = a.sp ? a.sp->logits_out : nullptr;
+    if (logits) logits += (int64_t)a.slot * M;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int r = rr.row0 + tid; r < rr.row1; r += kPCT) {
+      const float v = row_value(r);
+      if (logits) logits[r] = v;
+      if (better(v, r, bv, bi)) { bv = v; bi = r; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (lane == 0) { ps.bv[warp] = bv; ps.bi[warp] = bi; }
+    ConsSync::sync();
+    if (tid == 0) {
+      for (int w = 1; w < kPW; ++w)
+        if (better(ps.bv[w], ps.bi[w], bv, bi)) { bv = ps.bv[w]; bi = ps.bi[w]; }
+      a.am_part[blockIdx.x] = make_float2(bv, __int_as_float(bi));
+      __threadfence();
+      ps.last = (atomicAdd(a.am_count, 1u) == gridDim.x - 1);
+    }
+    ConsSync::sync();
+    if (ps.last) {
+      __threadfence();
+      float fv = -INFINITY;
+      int fi = 0x7fffffff;
+      for (int b = tid; b < (int)gridDim.x; b += kPCT) {
+        const float2 p = __ldcg(a.am_part + b);
+        if (better(p.x, __float_as_int(p.y), fv, fi)) { fv = p.x; fi = __float_as_int(p.y); }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, fv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, fi, o);
+        if (better(ov, oi, fv, fi)) { fv = ov; fi = oi; }
+      }
+      ConsSync::sync();
+      if (lane == 0) { ps.bv[warp] = fv; ps.bi[warp] = fi; }
+      ConsSync::sync();
+      if (tid == 0) {
+        for (int w = 1; w < kPW; ++w)
+          if (better(ps.bv[w], ps.bi[w], fv, fi)) { fv = ps.bv[w]; fi = ps.bi[w]; }
+        if (fi == 0x7fffffff) fi = 0;
+        if (a.sp) {
+          if (a.sp->argmax_out) a.sp->argmax_out[a.slot] = fi;
+          if (a.sp->advance) {
+            a.sp->token[a.slot] = fi;
+            a.sp->pos[a.slot] += 1;
+          }
+        }
+        *a.am_count = 0u;
+      }
+    }
+  }
+  return true;
+}
+
+// ---------------------------------------------------------------------- attention phase
+
+template <int G, int HD>
+__device__ void attn_phase(const AttnArgs &at, float *scratch, const StepConst &sc) {
+  auto &sm = *reinterpret_cast<AttnSmem<G, HD, kPW> *>(scratch);
+  int ctx = sc.ctx;
+  const int32_t *bt = at.sp->block_table + (int64_t)at.slot * at.sp->max_blocks;
+  const int n_table = at.sp->max_blocks;
+  if (ctx > n_table * at.bs) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) latch_error(at.err, ERR_POS);
+    ctx = n_table * at.bs;
+  }
+  if (ctx < 0) ctx = 0;
+  const int nblk = (ctx + at.bs - 1) / at.bs;
+  const int *pre = (nblk <= sc.nblk_staged) ? sc.blk : nullptr;
+  const int nsplit = attn_nsplit(nblk, at.n_splits, attn_blocks_per_split<HD, kPW>(at.bs));
+  const int items = at.Hkv * nsplit;
+  for (int it = blockIdx.x; it < items; it += gridDim.x)
+    attn_split<G, HD, kPW, ConsSync>(at, it / nsplit, it % nsplit, nsplit, ctx, bt, pre, sm);
+}
+
+// ---------------------------------------------------------------------- producer
+//
+// Walks the stages of every GEMV phase in order and copies each into the next free
+// ring slot; entering a layer's QKV phase it also prefetches that layer's K/V blocks
+// (this CTA's share) into L2 for the attention phase.  Measured on GB300 and not kept:
+// prefetching weights into L2 ahead of the ring halved the streaming rate, and capping
+// the bytes in flight per CTA slowed streaming without shortening the consumers'
+// load latencies.
+
+
+struct StageCursor {
+  const PersistArgs *a;
+  int p = 0, st = 0;  // phase, stage within the phase
+  RowRange rr;
+  bool done = false;
+
+  __device__ void settle() {  // move to the next existing stage
+    while (p < a->n_phases) {
+      const Phase &ph = a->ph[p];
+      if (ph.kind == PH_GEMV) {
+        rr = row_range(ph.g.m, ph.epi);
+        if (st < rr.n_stages) return;
+      }
+      ++p;
+      st = 0;
+    }
+    done = true;
+  }
+  __device__ void next() {
+    ++st;
+    settle();
+  }
+  __device__ const DevMat &mat() const { return a->ph[p].g.m; }
+  __device__ int first_row() const { return rr.row0 + st * rr.RPS; }
+  __device__ int rows() const { return min(rr.RPS, rr.row1 - first_row()); }
+  __device__ uint32_t w_bytes() const { return (uint32_t)(rows() * mat().row_bytes); }
+  __device__ uint32_t s_bytes() const {
+    return mat().fmt == MIE_FMT_Q4_0 ? (uint32_t)(rows() * mat().s_stride * 2) : 0u;
+  }
+};
+
+// L2 prefetch of this CTA's share of the K/V blocks a layer's attention will read.
+__device__ void prefetch_layer_kv(const Phase &qkv_phase) {
+  const GemvArgs &g = qkv_phase.g;
+  const StepParams *sp = g.sp;
+  const int ctx = sp->pos[g.slot] + 1;
+  const int nblk = min((max(ctx, 0) + g.bs - 1) / g.bs, sp->max_blocks);
+  const uint32_t half = (uint32_t)g.Hkv * g.bs * g.hd * 2;  // bytes of K (or V) of one layer in a block
+  for (int i = blockIdx.x; i < nblk; i += gridDim.x) {
+    const int b = sp->block_table[(int64_t)g.slot * sp->max_blocks + i];
+    if (b < 0 || b >= g.n_kv_blocks) continue;
+    prefetch_l2(g.kv_layer + (int64_t)b * g.block_stride, 2 * half);  // K then V, contiguous
+  }
+}
+
+__device__ void produce(const PersistArgs &a, const Ring &ring, volatile int &s_issued, volatile int &s_prod_done) {
+  const uint64_t pol = evict_first_policy();
+  StageCursor ld;
+  ld.a = &a;
+  ld.settle();
+  int s_global = 0;
+  int last_kv_phase = -1;
+  while (!ld.done) {
+    // a layer's K/V blocks go to L2 when the ring reaches its QKV phase
+    if (ld.p != last_kv_phase && ld.st == 0 && a.ph[ld.p].epi == EPI_QKV) {
+      prefetch_layer_kv(a.ph[ld.p]);
+      last_kv_phase = ld.p;
+    }
+    const int slot = s_global % a.n_slots, k = s_global / a.n_slots;
+    if (k > 0 && !mbar_wait(&ring.empty[slot], (k - 1) & 1)) {
+      atomicExch(a.abort, 1);
+      latch_error(a.err, ERR_TIMEOUT);
+      break;
+    }
+    if (ld_volatile(a.abort)) break;
+    const DevMat &m = ld.mat();
+    const int r = ld.first_row();
+    const uint32_t wb = ld.w_bytes(), sb = ld.s_bytes();
+    mbar_expect_tx(&ring.full[slot], wb + sb);
+    bulk_load(ring.w + (size_t)slot * a.slot_bytes, m.w + (int64_t)r * m.row_bytes, wb, &ring.full[slot], pol);
+    if (sb)
+      bulk_load(ring.sc + (size_t)slot * a.slot_sc_bytes, reinterpret_cast<const uint8_t *>(m.s) + (int64_t)r * m.s_stride * 2,
+                sb, &ring.full[slot], pol);
+    ++s_global;
+    s_issued = s_global;
+    ld.next();
+  }
+  s_prod_done = 1;
+}
+
+// ---------------------------------------------------------------------- the kernel
+
+template <int FL, int FH, int G, int HD>
+__global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kPRingMax], empty_bar[kPRingMax];
+  __shared__ PersistShared ps;
+  __shared__ StepConst sc;
+  // descriptors of the current and the next phase: read from shared memory, not through
+  // global loads that every barrier's acquire would send back to L2
+  __shared__ __align__(16) Phase s_ph[2];
+  __shared__ volatile int s_issued, s_prod_done;
+
+  Ring ring;
+  ring.nst = a.n_slots;
+  ring.slot_bytes = a.slot_bytes;
+  ring.slot_sc_bytes = a.slot_sc_bytes;
+  ring.w = smem;
+  ring.sc = smem + (size_t)a.n_slots * a.slot_bytes;
+  ring.full = full_bar;
+  ring.empty = empty_bar;
+  float *scratch = reinterpret_cast<float *>(ring.sc + (size_t)a.n_slots * a.slot_sc_bytes);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int i = 0; i < a.n_slots; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kPW);
+    }
+    s_issued = 0;
+    s_prod_done = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (warp == kPW) {
+    if (lane == 0) produce(a, ring, s_issued, s_prod_done);
+    return;
+  }
+
+  // consumers: the step's constants first
+  {
+    const GemvArgs &g0 = a.ph[0].g;  // layer 0's QKV phase carries the step's tables
+    const StepParams *sp = g0.sp;
+    const int pos = sp->pos[g0.slot];
+    const int ctx = pos + 1;
+    const int n_table = sp->max_blocks;
+    const int nblk = min((max(ctx, 0) + g0.bs - 1) / g0.bs, n_table);
+    const int staged = nblk <= kStepMaxBlocks ? nblk : 0;
+    const int32_t *bt = sp->block_table + (int64_t)g0.slot * n_table;
+    int ids[kStepMaxBlocks / kPCT];
+#pragma unroll
+    for (int j = 0; j < kStepMaxBlocks / kPCT; ++j) ids[j] = bt[min(tid + j * kPCT, max(staged - 1, 0))];
+#pragma unroll
+    for (int j = 0; j < kStepMaxBlocks / kPCT; ++j) {
+      const int i = tid + j * kPCT;
+      if (i < staged) {
+        int b = ids[j];
+        if (b < 0 || b >= g0.n_kv_blocks) {
+          latch_error(a.err, ERR_BLOCK_ID);
+          b = -1;
+        }
+        sc.blk[i] = b;
+      }
+    }
+    const int h2 = g0.hd / 2;
+    const int pos_c = (pos >= 0 && pos < g0.max_pos) ? pos : 0;
+    if (tid < h2) {
+      sc.rc[tid] = g0.rope_cos[(int64_t)pos_c * h2 + tid];
+      sc.rs[tid] = g0.rope_sin[(int64_t)pos_c * h2 + tid];
+    }
+    if (tid == 0) {
+      sc.pos = pos;
+      sc.ctx = ctx;
+      sc.nblk_staged = staged;
+    }
+    ConsSync::sync();
+  }
+  auto copy_phase = [&](int p) {
+    if (p >= a.n_phases) return;
+    constexpr int W = sizeof(Phase) / 4;
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(a.ph + p);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(&s_ph[p & 1]);
+    for (int i = tid; i < W; i += kPCT) dst[i] = __ldcg(src + i);
+  };
+  copy_phase(0);
+  copy_phase(1);
+  ConsSync::sync();
+  int s_global = 0;
+  bool ok = true;
+  for (int p = 0; p < a.n_phases && ok; ++p) {
+    const Phase &ph = s_ph[p & 1];
+    stamp(a.trace, p, 0);
+    if (p > 0 && !grid_wait(&a.done[p - 1], gridDim.x, a.abort, a.err, ps)) {
+      ok = false;
+      break;
+    }
+    stamp(a.trace, p, 1);
+    if (ph.kind == PH_GEMV) {
+      if (ph.g.m.fmt == FL) ok = gemv_phase<FL>(ph, ring, s_global, scratch, ps, sc, a.abort, a.err, a.trace, p);
+      else ok = gemv_phase<FH>(ph, ring, s_global, scratch, ps, sc, a.abort, a.err, a.trace, p);
+    } else {
+      stamp(a.trace, p, 2);
+      attn_phase<G, HD>(ph.at, scratch, sc);
+      stamp(a.trace, p, 3);
+    }
+    ConsSync::sync();
+    stamp(a.trace, p, 4);
+    copy_phase(p + 2);  // into the slot phase p used; visible after the next barrier
+    if (ok && p + 1 < a.n_phases) grid_signal(&a.done[p]);
+  }
+  if (ok) {
+    // the last CTA of the final phase (it reset the argmax counter) resets the rest:
+    // every CTA has passed every grid wait of this launch by then
+    if (tid == 0 && a.reset_flag && atomicAdd(a.reset_flag, 1u) == gridDim.x - 1) {
+      for (int p = 0; p < a.n_phases; ++p) a.done[p] = 0u;
+      __threadfence();
+      *a.reset_flag = 0u;
+    }
+    return;
+  }
+  // a wait gave up: no copy may still be writing into shared memory when we leave
+  if (tid == 0) {
+    for (long it = 0; it < kWaitPolls && !s_prod_done; ++it) __nanosleep(64);
+    const int issued = s_issued;
+    for (int s = max(0, issued - a.n_slots); s < issued; ++s) mbar_wait(&full_bar[s % a.n_slots], (s / a.n_slots) & 1);
+  }
+}
+
+// ---------------------------------------------------------------------- host side
+
+template <int FL, int FH, int G, int HD>
+static const void *kernel_ptr() {
+  return reinterpret_cast<const void *>(&persistent_step<FL, FH, G, HD>);
+}
+
+static const void *pick_kernel(int fl, int fh, int G, int HD) {
+#define MIE_K(A, B, C, D) \
+  if (fl == A && fh == B && G == C && HD == D) return kernel_ptr<A, B, C, D>();
+#define MIE_K_SHAPES(A, B) MIE_K(A, B, 4, 32) MIE_K(A, B, 8, 64) MIE_K(A, B, 4, 64)
+  MIE_K_SHAPES(MIE_FMT_BF16, MIE_FMT_BF16)
+  MIE_K_SHAPES(MIE_FMT_I8, MIE_FMT_I8)
+  MIE_K_SHAPES(MIE_FMT_Q4_0, MIE_FMT_Q4_0)
+  MIE_K_SHAPES(MIE_FMT_Q4_0, MIE_FMT_I8)
+#undef MIE_K_SHAPES
+#undef MIE_K
+  return nullptr;
+}
+
+size_t persist_attn_smem(int G, int HD) {
+  switch (G * 1000 + HD) {
+    case 4032: return sizeof(AttnSmem<4, 32, kPW>);
+    case 8064: return sizeof(AttnSmem<8, 64, kPW>);
+    case 4064: return sizeof(AttnSmem<4, 64, kPW>);
+  }
+  return 0;
+}
+
+mie_status persist_plan(const Phase *host_phases, int n, int G, int HD, PersistPlan *plan) {
+  const int grid = sm_count();
+  uint32_t slot = 0, slot_sc = 0;
+  size_t scratch = persist_attn_smem(G, HD);
+  int fl = -1, fh = -1;
+  for (int p = 0; p < n; ++p) {
+    const Phase &ph = host_phases[p];
+    if (ph.kind != PH_GEMV) continue;
+    const DevMat &m = ph.g.m;
+    if (fl < 0) fl = m.fmt;
+    else if (m.fmt != fl && fh < 0) fh = m.fmt;
+    const int RU = (ph.epi == EPI_SWIGLU || ph.epi == EPI_QKV) ? 2 : 1;
+    const int n_units = (m.rows + RU - 1) / RU;
+    const int KS = (m.kp + kSlice - 1) / kSlice;
+    const int RPS = KS >= kPW ? 1 : kPW / KS;
+    const int rows_max = ((n_units + grid - 1) / grid) * RU;
+    const uint32_t sb = (uint32_t)((RPS * m.row_bytes + 127) / 128 * 128);
+    const uint32_t scb = m.fmt == MIE_FMT_Q4_0 ? (uint32_t)((RPS * m.s_stride * 2 + 127) / 128 * 128) : 0u;
+    if (sb > slot) slot = sb;
+    if (scb > slot_sc) slot_sc = scb;
+    const size_t need = sizeof(float) * ((size_t)m.kp + (size_t)rows_max * KS);
+    if (need > scratch) scratch = need;
+    if (((uintptr_t)m.w & 15) || (m.row_bytes & 15)) return fail(MIE_E_SHAPE, "persistent step: unaligned rows");
+  }
+  if (fh < 0) fh = fl;
+  if (!pick_kernel(fl, fh, G, HD)) return fail(MIE_E_SHAPE, "persistent step: no kernel for this shape");
+  scratch = (scratch + 127) / 128 * 128;
+  const void *kern = pick_kernel(fl, fh, G, HD);
+  int dev = 0, max_smem = 0;
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "persistent step: kernel attributes");
+  }
+  // dynamic + static shared memory must fit the per-block opt-in limit
+  const long avail = (long)max_smem - (long)fa.sharedSizeBytes - (long)scratch - 256;
+  int nst = (int)(avail / (long)(slot + slot_sc));
+  if (nst > kPRingMax) nst = kPRingMax;
+  if (nst < 2) return fail(MIE_E_SHAPE, "persistent step: shared memory too small for the ring");
+  plan->kernel = kern;
+  plan->grid = grid;
+  plan->threads = kPThreads;
+  plan->n_slots = nst;
+  plan->slot_bytes = slot;
+  plan->slot_sc_bytes = slot_sc;
+  plan->smem = (size_t)nst * (slot + slot_sc) + scratch;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)plan->smem);
+  int blocks = 0;
+  if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, kPThreads, plan->smem);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return cuda_fail(e, "persistent step: shared-memory plan");
+  }
+  if (blocks < 1) return fail(MIE_E_SHAPE, "persistent step: one CTA per SM does not fit");
+  return MIE_OK;
+}
+
+mie_status persist_launch(const PersistPlan &plan, const PersistArgs &args, cudaStream_t st) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid);
+  cfg.blockDim = dim3(plan.threads);
+  cfg.dynamicSmemBytes = plan.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void *params[] = {const_cast<PersistArgs *>(&args)};
+  MIE_CUDA(cudaLaunchKernelExC(&cfg, plan.kernel, params));
+  return MIE_OK;
+}
+
+}  // namespace mie

@@ -36,13 +36,17 @@ def check_argmax(got_best, ref, pos):
         assert got_best == int(np.argmax(ref)), f"pos {pos}: argmax {got_best} vs {int(np.argmax(ref))}"
 
 
-def run_parity(orc, shape, layers, n_prompt, n_gen, perm_seed=5, compare_kv=True):
+PERSISTENT, CHAIN = 0, 1
+
+
+def run_parity(orc, shape, layers, n_prompt, n_gen, perm_seed=5, compare_kv=True, mode=PERSISTENT):
     bs = shape.block_size
     n_tok = n_prompt + n_gen
     n_blocks = (n_tok + bs - 1) // bs + 3
     max_pos = n_blocks * bs
     om = orc.Model(shape, n_kv_blocks=n_blocks, max_pos=max_pos, layers=layers)
     gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos, layers=layers)
+    gm.set_step_mode(mode)
     bt = synth.permutation(perm_seed, n_blocks).astype(np.int32)
     btd = torch.from_numpy(bt).cuda()
     logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
@@ -52,6 +56,7 @@ def run_parity(orc, shape, layers, n_prompt, n_gen, perm_seed=5, compare_kv=True
         ref, best = om.decode_step(int(toks[pos]), pos, bt)
         gm.decode_step(int(toks[pos]), pos, btd, logits, am)
         gm.sync()
+        assert gm.step_mode == mode
         check_logits(logits.cpu().numpy(), ref, pos)
         check_argmax(int(am.item()), ref, pos)
         if pos + 1 >= len(toks):
@@ -80,25 +85,49 @@ def run_parity(orc, shape, layers, n_prompt, n_gen, perm_seed=5, compare_kv=True
     return gm, om
 
 
-def test_tiny_q4_0_prompt_and_greedy(orc):
+@pytest.mark.parametrize("mode", [PERSISTENT, CHAIN])
+def test_tiny_q4_0_prompt_and_greedy(orc, mode):
     """64 prompt tokens + 16 greedy steps of the tiny Q4_0 decoder (K = 688 ragged)."""
-    run_parity(orc, synth.TINY, None, 64, 16)
+    run_parity(orc, synth.TINY, None, 64, 16, mode=mode)
 
 
+@pytest.mark.parametrize("mode", [PERSISTENT, CHAIN])
 @pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0"])
-def test_llama32_shape_two_layers(orc, fmt):
+def test_llama32_shape_two_layers(orc, fmt, mode):
     """Llama-3.2-1B shapes (every GEMV and the LM head at full size), 2 of 16 layers."""
-    run_parity(orc, synth.llama32_1b(fmt), 2, 5, 2)
+    run_parity(orc, synth.llama32_1b(fmt), 2, 5, 2, mode=mode)
 
 
-def test_tinyllama_shape_bf16_activations(orc):
+@pytest.mark.parametrize("mode", [PERSISTENT, CHAIN])
+def test_tinyllama_shape_bf16_activations(orc, mode):
     """TinyLlama shapes, Q4_0, bf16 GEMV inputs, 2 of 22 layers."""
-    run_parity(orc, synth.TINYLLAMA, 2, 4, 2)
+    run_parity(orc, synth.TINYLLAMA, 2, 4, 2, mode=mode)
 
 
 def test_llama32_full_depth_bf16(orc):
     """All 16 layers of the bf16 Llama-3.2-1B shape, the bench's configuration."""
     run_parity(orc, synth.LLAMA32_1B, None, 2, 1, compare_kv=False)
+
+
+def test_persistent_and_chain_agree_over_long_context(orc):
+    """The two step implementations compute the same arithmetic in the same order per
+    row, so over 300 greedy steps their logits stay within rounding of each other
+    and their tokens agree wherever the margin is clear."""
+    shape = synth.TINY
+    n_blocks, max_pos = 24, 24 * 16
+    bt = torch.from_numpy(synth.permutation(11, n_blocks).astype(np.int32)).cuda()
+    res = []
+    for mode in (PERSISTENT, CHAIN):
+        gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+        gm.set_step_mode(mode)
+        logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+        am = torch.empty(1, dtype=torch.int32, device="cuda")
+        gm.decode_step(3, 0, bt, logits, am)
+        gm.decode_continue(299)
+        gm.sync()
+        res.append(logits.cpu().numpy())
+        gm.close()
+    assert np.max(np.abs(res[0] - res[1])) <= 1e-3 * float(np.std(res[1]))
 
 
 def test_device_continuation_matches_host_steps(orc):
@@ -110,6 +139,7 @@ def test_device_continuation_matches_host_steps(orc):
     outs = []
     for mode in ("host", "device"):
         gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+        assert gm.step_mode == CHAIN
         logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
         am = torch.empty(1, dtype=torch.int32, device="cuda")
         toks = prompt_tokens(shape, 10)
