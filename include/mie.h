@@ -132,6 +132,28 @@ mie_status mie_paged_attn_decode(const float *q, const uint16_t *k_pool, const u
                                  float scale, float *out, void *workspace,
                                  size_t workspace_bytes, void *stream);
 
+/* Allocation-free variant of mie_paged_attn_decode.  The pages have no counterpart:
+ * they never consider callers that cannot allocate.  Some callers cannot call
+ * cudaMalloc at the moment they run attention -- a loop that must never enter the
+ * device allocator, or code whose device memory is owned entirely by another
+ * allocator -- so they cannot provide a workspace.  This entry point takes none and
+ * allocates nothing: its partial results live in a 1 MiB array compiled into the
+ * library, which every GPU that loads the library holds until the process exits.
+ * Arguments, results and errors are those of mie_paged_attn_decode, except that sizes
+ * needing more scratch than the array holds (mie_paged_attn_workspace_bytes(...) >
+ * 1048576) are rejected with MIE_E_SHAPE.  The first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress); make that first call before any stream
+ * capture.  Each call clears the counters it needs before its kernel runs.  All calls
+ * on one device share the array and it keeps the last call's partial results, so
+ * calls that overlap on the GPU (other streams, other host threads) race: the caller
+ * must serialise them. */
+mie_status mie_paged_attn_decode_noalloc(const float *q, const uint16_t *k_pool,
+                                         const uint16_t *v_pool, int64_t block_stride,
+                                         int n_pool_blocks, const int32_t *block_table,
+                                         int n_table, int ctx_len, int n_q_heads, int n_kv_heads,
+                                         int head_dim, int block_size, float scale, float *out,
+                                         void *stream);
+
 /* ========================================================================== argmax */
 
 size_t mie_argmax_workspace_bytes(int n);

@@ -18,7 +18,8 @@ STATUS = {0: "MIE_OK", 1: "MIE_E_ARG", 2: "MIE_E_SHAPE", 3: "MIE_E_OOM", 4: "MIE
 __all__ = ["lib", "MieError", "FMT", "LIB_PATH", "exported_names", "header_functions",
            "mie_convert_bf16", "mie_quantize_i8", "mie_quantize_q4_0", "mie_q4_0_pack",
            "mie_q4_0_packed_bytes", "mie_gemv_bf16", "mie_gemv_i8", "mie_gemv_q4_0",
-           "mie_paged_attn_decode", "mie_paged_attn_workspace_bytes", "mie_argmax",
+           "mie_paged_attn_decode", "mie_paged_attn_workspace_bytes", "mie_paged_attn_decode_noalloc",
+           "mie_argmax",
            "mie_argmax_workspace_bytes", "mie_check", "Pool", "Config", "Model", "DeviceArray"]
 
 
@@ -53,6 +54,7 @@ _SIGS = {
     "mie_gemv_q4_0": (I, [P, P, P, I, I, P]),
     "mie_paged_attn_workspace_bytes": (SZ, [I, I, I, I, I]),
     "mie_paged_attn_decode": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, F, P, P, SZ, P]),
+    "mie_paged_attn_decode_noalloc": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, F, P, P]),
     "mie_argmax_workspace_bytes": (SZ, [I]),
     "mie_argmax": (I, [P, I, P, P, SZ, P]),
     "mie_check": (I, [P]),
@@ -234,6 +236,22 @@ def mie_paged_attn_decode(q, k_pool, v_pool, block_stride: int, n_pool_blocks: i
         block_stride, n_pool_blocks, _dev(block_table, torch.int32, "block_table"), block_table.numel(),
         ctx_len, Hq, Hkv, hd, bs, scale, _dev(out, torch.float32, "out"), workspace.data_ptr(),
         workspace.numel() * workspace.element_size(), _stream(stream)), "mie_paged_attn_decode")
+    return out
+
+
+def mie_paged_attn_decode_noalloc(q, k_pool, v_pool, block_stride: int, n_pool_blocks: int, block_table,
+                                  ctx_len: int, Hq: int, Hkv: int, hd: int, bs: int, scale: float,
+                                  out=None, stream=None):
+    """mie_paged_attn_decode without a workspace: for callers that cannot allocate
+    device memory; its scratch is the library's built-in 1 MiB array (see mie.h)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(Hq * hd, dtype=torch.float32, device=q.device)
+    _check(lib().mie_paged_attn_decode_noalloc(
+        _dev(q, torch.float32, "q"), _dev(k_pool, None, "k_pool"), _dev(v_pool, None, "v_pool"),
+        block_stride, n_pool_blocks, _dev(block_table, torch.int32, "block_table"), block_table.numel(),
+        ctx_len, Hq, Hkv, hd, bs, scale, _dev(out, torch.float32, "out"), _stream(stream)),
+        "mie_paged_attn_decode_noalloc")
     return out
 
 

@@ -9,6 +9,8 @@
 // Grid (splits, KV heads), 128 threads; the number of splits in use follows the
 // context (at least four blocks each); the per-split work is attn_split in
 // attn_core.cuh.
+#include <mutex>
+
 #include "attn_core.cuh"
 
 namespace mie {
@@ -290,4 +292,64 @@ extern "C" mie_status mie_check(void *stream) {
     return fail(MIE_E_DEVICE, "device bounds check fired (code %d)", v);
   }
   return MIE_OK;
+}
+
+// --------------------------------------------------------------- C ABI: allocation-free attention
+//
+// Some callers cannot allocate device memory at the moment they need attention: code
+// running where cudaMalloc is not allowed or not wanted (inside a real-time loop that
+// must never hit the allocator, or while a custom allocator owns all device memory).
+// mie_paged_attn_decode_noalloc serves them: it needs no caller workspace and allocates
+// nothing, because its partial results live in one fixed array that is part of the
+// library's device image.  Every GPU that loads the library holds that array until the
+// process exits.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 1u << 20;  // 1 MiB: the largest workspace served
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+unsigned char *g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device, looked up once per device.
+mie_status noalloc_scratch(unsigned char **out) {
+  int dev = 0;
+  MIE_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(MIE_E_ARG, "mie_paged_attn_decode_noalloc: device %d", dev);
+  std::lock_guard<std::mutex> g(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "mie_paged_attn_decode_noalloc: cudaGetSymbolAddress");
+    g_noalloc_ptr[dev] = static_cast<unsigned char *>(p);
+  }
+  *out = g_noalloc_ptr[dev];
+  return MIE_OK;
+}
+
+}  // namespace
+
+extern "C" mie_status mie_paged_attn_decode_noalloc(const float *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                                                    int64_t block_stride, int n_pool_blocks, const int32_t *block_table,
+                                                    int n_table, int ctx_len, int n_q_heads, int n_kv_heads,
+                                                    int head_dim, int block_size, float scale, float *out,
+                                                    void *stream) {
+  if (!q || !k_pool || !v_pool || !block_table || !out)
+    return fail(MIE_E_ARG, "mie_paged_attn_decode_noalloc: null pointer");
+  if (n_kv_heads < 1 || n_q_heads < n_kv_heads || head_dim < 1 || block_size < 1 || ctx_len < 0)
+    return fail(MIE_E_SHAPE, "mie_paged_attn_decode_noalloc: bad sizes");
+  const size_t need = mie_paged_attn_workspace_bytes(n_q_heads, n_kv_heads, head_dim, ctx_len, block_size);
+  if (need > kNoAllocScratchBytes)
+    return fail(MIE_E_SHAPE,
+                "mie_paged_attn_decode_noalloc: these sizes need %zu bytes of scratch, more than the %zu-byte "
+                "built-in array; use mie_paged_attn_decode with a workspace",
+                need, kNoAllocScratchBytes);
+  unsigned char *scratch = nullptr;
+  const mie_status s = noalloc_scratch(&scratch);
+  if (s != MIE_OK) return s;
+  // the same checks, counter clearing and launch as the workspace entry point
+  return mie_paged_attn_decode(q, k_pool, v_pool, block_stride, n_pool_blocks, block_table, n_table, ctx_len,
+                               n_q_heads, n_kv_heads, head_dim, block_size, scale, out, scratch,
+                               kNoAllocScratchBytes, stream);
 }
