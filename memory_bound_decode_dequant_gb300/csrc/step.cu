@@ -334,13 +334,29 @@ struct StageCursor {
   int p = 0, st = 0;  // phase, stage within the phase
   RowRange rr;
   bool done = false;
+  // fields of the current phase, held in registers: the issue loop touches no memory
+  const uint8_t *w = nullptr, *sc = nullptr;
+  int64_t row_bytes = 0;
+  int s_stride = 0;
+  bool q4 = false, qkv = false;
+  uint16_t *kv_layer = nullptr;
 
   __device__ void settle() {  // move to the next existing stage
     while (p < a->n_phases) {
       const Phase &ph = a->ph[p];
       if (ph.kind == PH_GEMV) {
-        rr = row_range(ph.g.m, ph.epi);
-        if (st < rr.n_stages) return;
+        const DevMat m = ph.g.m;
+        rr = row_range(m, ph.epi);
+        if (st < rr.n_stages) {
+          w = m.w;
+          sc = reinterpret_cast<const uint8_t *>(m.s);
+          row_bytes = m.row_bytes;
+          s_stride = m.s_stride;
+          q4 = m.fmt == MIE_FMT_Q4_0;
+          qkv = ph.epi == EPI_QKV;
+          kv_layer = ph.g.kv_layer;
+          return;
+        }
       }
       ++p;
       st = 0;
@@ -348,34 +364,47 @@ struct StageCursor {
     done = true;
   }
   __device__ void next() {
-    ++st;
-    settle();
+    if (++st >= rr.n_stages) {
+      ++p;
+      st = 0;
+      settle();
+    }
   }
-  __device__ const DevMat &mat() const { return a->ph[p].g.m; }
   __device__ int first_row() const { return rr.row0 + st * rr.RPS; }
   __device__ int rows() const { return min(rr.RPS, rr.row1 - first_row()); }
-  __device__ uint32_t w_bytes() const { return (uint32_t)(rows() * mat().row_bytes); }
-  __device__ uint32_t s_bytes() const {
-    return mat().fmt == MIE_FMT_Q4_0 ? (uint32_t)(rows() * mat().s_stride * 2) : 0u;
+  __device__ uint32_t w_bytes() const { return (uint32_t)(rows() * row_bytes); }
+  __device__ uint32_t s_bytes() const { return q4 ? (uint32_t)(rows() * s_stride * 2) : 0u; }
+};
+
+// The K/V blocks of this CTA's share of the context, read once at kernel start so that
+// the per-layer L2 prefetch issues no dependent loads.
+constexpr int kKvPrefetchMax = 8;
+struct KvShare {
+  int n = 0;
+  int blk[kKvPrefetchMax];
+  int64_t block_stride = 0;
+  uint32_t bytes = 0;  // K and V of one layer in one block
+
+  __device__ void load(const GemvArgs &g) {
+    const StepParams *sp = g.sp;
+    const int ctx = sp->pos[g.slot] + 1;
+    const int nblk = min((max(ctx, 0) + g.bs - 1) / g.bs, sp->max_blocks);
+    block_stride = g.block_stride;
+    bytes = 2u * (uint32_t)g.Hkv * g.bs * g.hd * 2;
+    for (int i = blockIdx.x; i < nblk && n < kKvPrefetchMax; i += gridDim.x) {
+      const int b = sp->block_table[(int64_t)g.slot * sp->max_blocks + i];
+      if (b >= 0 && b < g.n_kv_blocks) blk[n++] = b;
+    }
+  }
+  __device__ void prefetch(const uint16_t *kv_layer) const {
+    for (int j = 0; j < n; ++j) prefetch_l2(kv_layer + (int64_t)blk[j] * block_stride, bytes);
   }
 };
 
-// L2 prefetch of this CTA's share of the K/V blocks a layer's attention will read.
-__device__ void prefetch_layer_kv(const Phase &qkv_phase) {
-  const GemvArgs &g = qkv_phase.g;
-  const StepParams *sp = g.sp;
-  const int ctx = sp->pos[g.slot] + 1;
-  const int nblk = min((max(ctx, 0) + g.bs - 1) / g.bs, sp->max_blocks);
-  const uint32_t half = (uint32_t)g.Hkv * g.bs * g.hd * 2;  // bytes of K (or V) of one layer in a block
-  for (int i = blockIdx.x; i < nblk; i += gridDim.x) {
-    const int b = sp->block_table[(int64_t)g.slot * sp->max_blocks + i];
-    if (b < 0 || b >= g.n_kv_blocks) continue;
-    prefetch_l2(g.kv_layer + (int64_t)b * g.block_stride, 2 * half);  // K then V, contiguous
-  }
-}
-
 __device__ void produce(const PersistArgs &a, const Ring &ring, volatile int &s_issued, volatile int &s_prod_done) {
   const uint64_t pol = evict_first_policy();
+  KvShare kv;
+  kv.load(a.ph[0].g);
   StageCursor ld;
   ld.a = &a;
   ld.settle();
@@ -383,8 +412,8 @@ __device__ void produce(const PersistArgs &a, const Ring &ring, volatile int &s_
   int last_kv_phase = -1;
   while (!ld.done) {
     // a layer's K/V blocks go to L2 when the ring reaches its QKV phase
-    if (ld.p != last_kv_phase && ld.st == 0 && a.ph[ld.p].epi == EPI_QKV) {
-      prefetch_layer_kv(a.ph[ld.p]);
+    if (ld.qkv && ld.p != last_kv_phase) {
+      kv.prefetch(ld.kv_layer);
       last_kv_phase = ld.p;
     }
     const int slot = s_global % a.n_slots, k = s_global / a.n_slots;
@@ -394,14 +423,13 @@ __device__ void produce(const PersistArgs &a, const Ring &ring, volatile int &s_
       break;
     }
     if (ld_volatile(a.abort)) break;
-    const DevMat &m = ld.mat();
     const int r = ld.first_row();
     const uint32_t wb = ld.w_bytes(), sb = ld.s_bytes();
     mbar_expect_tx(&ring.full[slot], wb + sb);
-    bulk_load(ring.w + (size_t)slot * a.slot_bytes, m.w + (int64_t)r * m.row_bytes, wb, &ring.full[slot], pol);
+    bulk_load(ring.w + (size_t)slot * a.slot_bytes, ld.w + (int64_t)r * ld.row_bytes, wb, &ring.full[slot], pol);
     if (sb)
-      bulk_load(ring.sc + (size_t)slot * a.slot_sc_bytes, reinterpret_cast<const uint8_t *>(m.s) + (int64_t)r * m.s_stride * 2,
-                sb, &ring.full[slot], pol);
+      bulk_load(ring.sc + (size_t)slot * a.slot_sc_bytes, ld.sc + (int64_t)r * ld.s_stride * 2, sb, &ring.full[slot],
+                pol);
     ++s_global;
     s_issued = s_global;
     ld.next();
