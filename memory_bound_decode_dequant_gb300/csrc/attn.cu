@@ -22,6 +22,7 @@ __device__ int g_device_error;  // latched by the stateless kernels of this devi
 
 struct CtaSync {
   __device__ static void sync() { __syncthreads(); }
+  __device__ static bool all(bool v) { return __syncthreads_and(v) != 0; }
 };
 
 template <int G, int HD>
@@ -59,10 +60,11 @@ __global__ void zero_kernel(float *out, int n) {
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) out[i] = 0.f;
 }
 
+size_t attn_counter_bytes(int Hkv) { return 256 + ((size_t)Hkv * 4 + 255) / 256 * 256; }
+
 size_t attn_workspace_bytes(int Hq, int Hkv, int hd, int n_splits) {
   const int G = Hq / Hkv;
-  const size_t counters = 256 + ((size_t)Hkv * 4 + 255) / 256 * 256;
-  return counters + (size_t)Hkv * n_splits * G * (2 + hd) * sizeof(float);
+  return attn_counter_bytes(Hkv) + (size_t)Hkv * n_splits * G * (2 + hd) * sizeof(float);
 }
 
 int attn_splits_for(int Hkv, int max_ctx, int bs) {

@@ -40,6 +40,7 @@ __host__ __device__ inline int attn_blocks_per_split(int bs) {
 template <int G, int HD, int NW>
 struct AttnSmem {
   float q[G * HD];
+  float kn[HD], vn[HD];  // tagged variant: the current token's k and v
   int blk[kAttnMaxBlocks];
   float m[NW][G], l[NW][G];
   float o[NW][G][HD];
@@ -87,6 +88,37 @@ struct KvGroup {
   }
 };
 
+// Tagged variant: polls the group's queries into sm.q and, when has_pos, the current
+// token's k and v of KV head g into sm.kn / sm.vn, all in one batch of round trips.
+template <int G, int HD, int NT, class Sync>
+__device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, AttnSmem<G, HD, NT / 32> &sm, uint32_t tag,
+                              const int *abort) {
+  constexpr int NQ = G * HD / 2, NK = HD / 2;
+  const uint64_t *qs = a.qkv_t + (int64_t)(g * G) * HD;
+  const uint64_t *ks = a.qkv_t + (int64_t)(a.Hq + g) * HD;
+  const uint64_t *vs = a.qkv_t + (int64_t)(a.Hq + a.Hkv + g) * HD;
+  const int n = NQ + (has_pos ? 2 * NK : 0);
+  bool ok = poll_pairs<NT, 4>(n, tag, abort, [&](int j, const uint64_t *&src, float *&dst, int &c) {
+    c = 2;
+    if (j < NQ) {
+      src = qs + 2 * j;
+      dst = sm.q + 2 * j;
+    } else if (j < NQ + NK) {
+      src = ks + 2 * (j - NQ);
+      dst = sm.kn + 2 * (j - NQ);
+    } else {
+      src = vs + 2 * (j - NQ - NK);
+      dst = sm.vn + 2 * (j - NQ - NK);
+    }
+  });
+  return Sync::all(ok);
+}
+
+// bf16 bits of two values that are already bf16-exact, packed as the cache holds them.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+}
+
 // Computes split s of nsplit for KV head g.  With one split the result goes straight
 // to a.out; otherwise the split's (m, l, o) partial goes to the workspace and the last
 // split of the head to finish (atomic counter, no waiting) merges all partials and
@@ -94,9 +126,15 @@ struct KvGroup {
 // [0, nblk) already staged in shared memory; otherwise they are read from bt in
 // chunks.  Sync::sync() is a barrier over the NW participating warps, whose threads
 // are numbered 0 .. NW*32-1.
-template <int G, int HD, int NW, class Sync>
-__device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx, const int32_t *bt, const int *blk_pre,
-                           AttnSmem<G, HD, NW> &sm) {
+//
+// Tagged (the persistent step): q and the current token's k and v (position ctx-1)
+// are polled as tagged words from a.qkv_t, whose k and v values are already rounded
+// to bf16; the token's K/V then replace whatever the cache held at its slot (its
+// write into the cache by another SM may not be visible yet), and the output is
+// written as tagged words to a.out_t.  Returns false if a poll gave up.
+template <int G, int HD, int NW, class Sync, bool Tagged = false>
+__device__ bool attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx, const int32_t *bt, const int *blk_pre,
+                           AttnSmem<G, HD, NW> &sm, uint32_t tag = 0, const int *abort = nullptr) {
   using KG = KvGroup<HD>;
   constexpr int LPT = KG::LPT, TPI = KG::TPI, DPL = KG::DPL, VW = KG::VW;
   constexpr int PART = G * (2 + HD);
@@ -111,9 +149,13 @@ __device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
 
   // the queries of the group: loads issued now, stored once the first K/V loads are out
   float qv[QB];
+  if constexpr (!Tagged) {
 #pragma unroll
-  for (int j = 0; j < QB; ++j) qv[j] = __ldcg(a.q + (g * G) * HD + min(tid + j * NT, G * HD - 1));
+    for (int j = 0; j < QB; ++j) qv[j] = __ldcg(a.q + (g * G) * HD + min(tid + j * NT, G * HD - 1));
+  }
   bool q_stored = false;
+  const int pos = ctx - 1;
+  const bool has_pos = Tagged && t_end == ctx && ctx > 0;  // this split holds the current token
 
   float m[G], l[G], o[G][DPL];
 #pragma unroll
@@ -147,13 +189,40 @@ __device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
     KG cur;
     cur.load(a, ids, id0, tb, t1, head_off, lane);
     if (!q_stored) {
+      if constexpr (Tagged) {
+        if (!tagged_inputs<G, HD, NT, Sync>(a, g, has_pos, sm, tag, abort)) return false;
+      } else {
 #pragma unroll
-      for (int j = 0; j < QB; ++j)
-        if (tid + j * NT < G * HD) sm.q[tid + j * NT] = qv[j];
-      Sync::sync();
+        for (int j = 0; j < QB; ++j)
+          if (tid + j * NT < G * HD) sm.q[tid + j * NT] = qv[j];
+        Sync::sync();
+      }
       q_stored = true;
     }
     for (; tb < t1; tb += NW * TPI) {
+      if constexpr (Tagged) {
+        const int pi = pos - tb;  // the current token's place in this warp's group
+        if (has_pos && pi >= 0 && pi < TPI) {
+          if (lane / LPT == pi) {
+            const float *kn = sm.kn + part_in * 32;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              cur.kv[i] = make_uint4(pack_bf16x2(kn[8 * i], kn[8 * i + 1]), pack_bf16x2(kn[8 * i + 2], kn[8 * i + 3]),
+                                     pack_bf16x2(kn[8 * i + 4], kn[8 * i + 5]), pack_bf16x2(kn[8 * i + 6], kn[8 * i + 7]));
+          }
+#pragma unroll
+          for (int i = 0; i < TPI; ++i) {
+            if (i != pi) continue;
+            if constexpr (DPL == 1) {
+              cur.vraw[i][0] = __float_as_uint(sm.vn[lane]) >> 16;
+            } else {
+#pragma unroll
+              for (int w = 0; w < VW; ++w)
+                cur.vraw[i][w] = pack_bf16x2(sm.vn[lane * DPL + 2 * w], sm.vn[lane * DPL + 2 * w + 1]);
+            }
+          }
+        }
+      }
       const int kblk = cur.kblk;
       float vf[TPI][DPL];
 #pragma unroll
@@ -228,7 +297,13 @@ __device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
       }
     }
   }
-  if (!q_stored) Sync::sync();  // empty split: keep the barrier count of the other paths
+  if (!q_stored) {  // empty split: keep the barrier count of the other paths
+    if constexpr (Tagged) {
+      if (!tagged_inputs<G, HD, NT, Sync>(a, g, false, sm, tag, abort)) return false;
+    } else {
+      Sync::sync();
+    }
+  }
 
   // merge the warps
   if (lane == 0) {
@@ -252,7 +327,9 @@ __device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
       L = fmaf(sm.l[w][h], f, L);
     }
     if (nsplit == 1) {
-      a.out[(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
+      const float r = (L > 0.f) ? O / L : 0.f;
+      if constexpr (Tagged) st_tagged(a.out_t + (g * G) * HD + i, r, tag);
+      else a.out[(g * G) * HD + i] = r;
     } else {
       part[2 * G + i] = O;
       if (d == 0) { part[h] = M; part[G + h] = L; }
@@ -260,13 +337,13 @@ __device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
   }
   if (nsplit == 1) {
     Sync::sync();  // the scratch is reused by the caller's next item
-    return;
+    return true;
   }
   __threadfence();
   Sync::sync();
   if (tid == 0) sm.last = (atomicAdd(a.ws_count + g, 1u) == (unsigned)nsplit - 1);
   Sync::sync();
-  if (!sm.last) return;
+  if (!sm.last) return true;
   __threadfence();
   const float *base = a.ws_part + (int64_t)g * a.n_splits * PART;
   for (int i = tid; i < G * HD; i += NT) {
@@ -300,10 +377,13 @@ __device__ void attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
       }
       M = mb;
     }
-    a.out[(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
+    const float r = (L > 0.f) ? O / L : 0.f;
+    if constexpr (Tagged) st_tagged(a.out_t + (g * G) * HD + i, r, tag);
+    else a.out[(g * G) * HD + i] = r;
   }
   if (tid == 0) a.ws_count[g] = 0u;
   Sync::sync();
+  return true;
 }
 
 }  // namespace mie

@@ -182,6 +182,47 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
+// RMSNorm of the staged vector xs[0..K) in place (PRO_NORM, PRO_EMBED_NORM), or only
+// the bf16 rounding of PRO_PLAIN inputs when act_bf16 is set.  g0, when not null,
+// holds the gains of elements tid + j*NT (j < 8), loaded by the caller ahead of time
+// (K <= 8*NT).  NT threads take part; Sync is a barrier over them.
+template <int NT, class Sync>
+__device__ void normalize_staged(const GemvArgs &a, int pro, float *xs, int K, float *red, float *scale_slot,
+                                 const float *g0) {
+  constexpr int B = 8;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (pro != PRO_PLAIN) {
+    float ss = 0.f;
+    for (int k = tid; k < K; k += NT) ss += xs[k] * xs[k];
+    ss = warp_sum(ss);
+    if (lane == 0) red[warp] = ss;
+    Sync::sync();
+    if (tid == 0) {
+      float t = 0.f;
+      for (int w = 0; w < NT / 32; ++w) t += red[w];
+      *scale_slot = 1.0f / sqrtf(t / (float)K + a.eps);
+    }
+    Sync::sync();
+    const float r = *scale_slot;
+    for (int k0 = tid; k0 < K; k0 += NT * B) {
+      float g[B];
+#pragma unroll
+      for (int j = 0; j < B; ++j) g[j] = g0 ? g0[j] : __ldg(a.gain + min(k0 + j * NT, K - 1));
+#pragma unroll
+      for (int j = 0; j < B; ++j) {
+        const int k = k0 + j * NT;
+        if (k < K) {
+          float v = xs[k] * r * g[j];
+          if (a.act_bf16) v = round_bf16(v);
+          xs[k] = v;
+        }
+      }
+    }
+  } else if (a.act_bf16) {
+    for (int k = tid; k < K; k += NT) xs[k] = round_bf16(xs[k]);
+  }
+}
+
 // Stages a GEMV input vector into shared memory xs[0..Kp) (zeros past K), applying the
 // prologue: PRO_PLAIN copies x; PRO_NORM applies RMSNorm with the gain; PRO_EMBED_NORM
 // gathers row sp->token of the embedding first (CTA 0 also stores it as the residual).
@@ -193,7 +234,7 @@ template <int NT, class Sync>
 __device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp, float *red, float *scale_slot,
                             int *err) {
   constexpr int B = 8;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x;
   // a vector that one batch covers gets its gains loaded together with its values
   const bool one_batch = pro != PRO_PLAIN && K <= NT * B;
   float g0[B];
@@ -230,37 +271,112 @@ __device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp
       }
     }
   }
-  if (pro != PRO_PLAIN) {
-    float ss = 0.f;
-    for (int k = tid; k < K; k += NT) ss += xs[k] * xs[k];
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    Sync::sync();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < NT / 32; ++w) t += red[w];
-      *scale_slot = 1.0f / sqrtf(t / (float)K + a.eps);
-    }
-    Sync::sync();
-    const float r = *scale_slot;
-    for (int k0 = tid; k0 < K; k0 += NT * B) {
-      float g[B];
+  normalize_staged<NT, Sync>(a, pro, xs, K, red, scale_slot, one_batch ? g0 : nullptr);
+  Sync::sync();
+}
+
+// --------------------------------------------------------------- tagged words
+//
+// Between the phases of the persistent step every value travels as one 64-bit word:
+// the fp32 bits in the low half and the launch's tag in the high half.  A 64-bit
+// aligned access is single-copy atomic, so a reader that sees the current tag also
+// sees the value written with it; it polls the words themselves instead of meeting the
+// writers at a barrier first.  Words left by an earlier launch carry an older tag.
+
+__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
+  const uint64_t w = ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ void ld_tagged2(const uint64_t *p, uint64_t &w0, uint64_t &w1) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(w0), "=l"(w1) : "l"(p) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_tagged(const uint64_t *p) {
+  uint64_t w;
+  asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+
+__device__ __forceinline__ bool tag_ok(uint64_t w, uint32_t tag) { return (uint32_t)(w >> 32) == tag; }
+__device__ __forceinline__ float tag_val(uint64_t w) { return __uint_as_float((uint32_t)w); }
+
+constexpr long kTagPolls = 1L << 22;  // bounded polling of tagged words (seconds)
+
+// Polls n pairs of tagged words until all carry `tag`.  map(j, src, dst, n) names pair
+// j: its source (16-byte aligned when both words are wanted), its destination in
+// shared memory, and how many words it has (1 or 2).  Each thread polls its own pairs, B per round trip, and
+// gives up after kTagPolls rounds or once *abort is set; returns false then.
+template <int NT, int B, class Map>
+__device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map) {
+  const int tid = threadIdx.x;
+  for (int j0 = tid; j0 < n; j0 += NT * B) {
+    uint32_t pending = 0;
 #pragma unroll
-      for (int j = 0; j < B; ++j) g[j] = one_batch ? g0[j] : __ldg(a.gain + min(k0 + j * NT, K - 1));
+    for (int i = 0; i < B; ++i)
+      if (j0 + i * NT < n) pending |= 1u << i;
+    for (long it = 0; pending; ++it) {
+      uint64_t w0[B], w1[B];
 #pragma unroll
-      for (int j = 0; j < B; ++j) {
-        const int k = k0 + j * NT;
-        if (k < K) {
-          float v = xs[k] * r * g[j];
-          if (a.act_bf16) v = round_bf16(v);
-          xs[k] = v;
+      for (int i = 0; i < B; ++i) {
+        w0[i] = w1[i] = 0;
+        if ((pending >> i) & 1u) {
+          const uint64_t *src;
+          float *dst;
+          int cnt;
+          map(j0 + i * NT, src, dst, cnt);
+          if (cnt == 2) ld_tagged2(src, w0[i], w1[i]);
+          else w0[i] = ld_tagged(src);
         }
       }
+#pragma unroll
+      for (int i = 0; i < B; ++i) {
+        if (!((pending >> i) & 1u)) continue;
+        const uint64_t *src;
+        float *dst;
+        int cnt;
+        map(j0 + i * NT, src, dst, cnt);
+        if (tag_ok(w0[i], tag) && (cnt < 2 || tag_ok(w1[i], tag))) {
+          dst[0] = tag_val(w0[i]);
+          if (cnt == 2) dst[1] = tag_val(w1[i]);
+          pending &= ~(1u << i);
+        }
+      }
+      if (pending) {
+        if (it >= kTagPolls) return false;
+        if ((it & 63) == 63 && *reinterpret_cast<const volatile int *>(abort)) return false;
+        __nanosleep(32);
+      }
     }
-  } else if (a.act_bf16) {
-    for (int k = tid; k < K; k += NT) xs[k] = round_bf16(xs[k]);
   }
-  Sync::sync();
+  return true;
+}
+
+// Copies tagged words [0, K) of src into xs once all carry `tag`; xs[K..Kp) = 0.  src
+// is 16-byte aligned.
+template <int NT>
+__device__ bool poll_vector(const uint64_t *src, int K, int Kp, uint32_t tag, float *xs, const int *abort) {
+  const bool ok = poll_pairs<NT, 8>((K + 1) / 2, tag, abort, [&](int j, const uint64_t *&s, float *&d, int &c) {
+    s = src + 2 * j;
+    d = xs + 2 * j;
+    c = (2 * j + 1 < K) ? 2 : 1;
+  });
+  for (int k = K + threadIdx.x; k < Kp; k += NT) xs[k] = 0.f;
+  return ok;
+}
+
+// One tagged word, polled the same way.
+__device__ __forceinline__ bool poll_word(const uint64_t *src, uint32_t tag, float &v, const int *abort) {
+  for (long it = 0;; ++it) {
+    const uint64_t w = ld_tagged(src);
+    if (tag_ok(w, tag)) {
+      v = tag_val(w);
+      return true;
+    }
+    if (it >= kTagPolls) return false;
+    if ((it & 63) == 63 && *reinterpret_cast<const volatile int *>(abort)) return false;
+    __nanosleep(32);
+  }
 }
 
 // What the QKV epilogue needs besides the GEMV results, read before the weights are

@@ -49,6 +49,10 @@ struct GemvArgs {
   StepParams *sp = nullptr;
   int slot = 0;
   int *err = nullptr;
+  // persistent step: vectors as tagged words (fp32 bits | tag << 32) instead of x / y
+  const uint64_t *x_t = nullptr;  // input (PRO_PLAIN, PRO_NORM)
+  const uint64_t *res_t = nullptr;  // EPI_RESID residual; null: the token's embedding row
+  uint64_t *y_t = nullptr;        // RESID / SWIGLU output; QKV: q | k | v after RoPE
   // filled in by launch_gemv: the shared-memory ring of weight stages
   int n_stages = 0;
   uint32_t stage_bytes = 0, sc_stage_bytes = 0;
@@ -79,8 +83,12 @@ struct AttnArgs {
   unsigned *ws_count = nullptr;
   int n_splits = 1;
   int *err = nullptr;
+  // persistent step: the current token's q | k | v and the output as tagged words
+  const uint64_t *qkv_t = nullptr;
+  uint64_t *out_t = nullptr;
 };
 size_t attn_workspace_bytes(int Hq, int Hkv, int hd, int n_splits);
+size_t attn_counter_bytes(int Hkv);  // the counters at the start of a workspace
 int attn_splits_for(int Hkv, int max_ctx, int bs);
 mie_status launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl);
 
@@ -94,15 +102,15 @@ struct Phase {
 struct PersistArgs {
   const Phase *ph = nullptr;  // device array of n_phases descriptors
   int n_phases = 0;
-  unsigned *done = nullptr;   // [n_phases] grid-barrier counters, zero between launches
-  unsigned *reset_flag = nullptr;
+  unsigned *epoch = nullptr;  // tag of this launch's words (never 0); advanced by the last CTA
+  unsigned *fin = nullptr;    // CTAs done with the launch, zero between launches
   int *abort = nullptr;       // nonzero once a bounded wait gave up
   int n_slots = 0;
   uint32_t slot_bytes = 0, slot_sc_bytes = 0;
   int *err = nullptr;
   unsigned long long *trace = nullptr;  // [n_phases][grid][kTracePoints] globaltimer ns, or null
 };
-constexpr int kTracePoints = 5;  // phase entry, barrier passed, input staged, stages consumed, outputs written
+constexpr int kTracePoints = 5;  // phase entry, inputs arrived, input staged, stages consumed, outputs written
 struct PersistPlan {
   const void *kernel = nullptr;
   int grid = 0, threads = 0, n_slots = 0;

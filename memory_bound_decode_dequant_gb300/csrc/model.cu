@@ -98,8 +98,8 @@ struct mie_ctx {
   int64_t block_elems = 0;
   float *x = nullptr, *q = nullptr, *att = nullptr, *act = nullptr;
   float *rope_cos = nullptr, *rope_sin = nullptr;
-  float *attn_part = nullptr;
-  unsigned *attn_count = nullptr;
+  uint8_t *attn_ws = nullptr;  // per layer: split counters, then split partials
+  size_t attn_ws_bytes = 0;    // one layer's share
   int attn_splits = 1;
   float2 *am_part = nullptr;
   unsigned *am_count = nullptr;
@@ -116,7 +116,9 @@ struct mie_ctx {
   std::vector<Phase> phases;
   Phase *d_phases = nullptr;
   size_t d_phases_cap = 0;
-  unsigned *done = nullptr;  // [n_phases + 1]: grid-barrier counters, then the reset flag
+  uint64_t *tagged = nullptr;  // per layer: q|k|v, attention out, x after o, act, x after down
+  size_t tagged_words = 0;
+  unsigned *epoch = nullptr;   // [0]: the next launch's tag; [1]: CTAs finished
   int *abort = nullptr;
   PersistPlan plan;
   unsigned long long *trace = nullptr;
@@ -129,6 +131,23 @@ struct mie_ctx {
     return p;
   }
 };
+
+// Tagged words of one layer's phase outputs (each vector rounded up to whole 16-byte
+// pairs): q|k|v, attention output, x after O-proj, SwiGLU activation, x after down.
+static int64_t even_words(int64_t n) { return (n + 1) / 2 * 2; }
+static int64_t tagged_layer_words(const mie_config &c) {
+  return even_words((int64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim) +
+         even_words((int64_t)c.n_heads * c.head_dim) + 2 * even_words(c.d_model) + even_words(c.ffn);
+}
+
+// Every tagged word back to tag 0 (no launch writes it) and the next tag to 1.
+static cudaError_t reset_tags(mie_ctx *ctx) {
+  static const unsigned init[2] = {1u, 0u};
+  cudaError_t e = cudaMemsetAsync(ctx->tagged, 0, sizeof(uint64_t) * ctx->tagged_words, ctx->stream);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->epoch, init, sizeof init, cudaMemcpyHostToDevice, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  return e;
+}
 
 static mie_status check_config(const mie_config &c) {
   if (c.n_layers < 1 || c.d_model < 1 || c.n_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 1 || c.ffn < 1 ||
@@ -193,14 +212,16 @@ extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **
   ctx->rope_cos = (float *)ctx->dalloc(sizeof(float) * (size_t)c.max_pos * (c.head_dim / 2));
   ctx->rope_sin = (float *)ctx->dalloc(sizeof(float) * (size_t)c.max_pos * (c.head_dim / 2));
   ctx->attn_splits = attn_splits_for(c.n_kv_heads, c.max_pos, c.block_size);
-  const size_t aws = attn_workspace_bytes(c.n_heads, c.n_kv_heads, c.head_dim, ctx->attn_splits);
-  uint8_t *ws = (uint8_t *)ctx->dalloc(aws * S);
+  ctx->attn_ws_bytes = attn_workspace_bytes(c.n_heads, c.n_kv_heads, c.head_dim, ctx->attn_splits);
+  const size_t aws_total = ctx->attn_ws_bytes * c.n_layers * S;
+  uint8_t *ws = (uint8_t *)ctx->dalloc(aws_total);
+  ctx->tagged_words = tagged_layer_words(c) * c.n_layers;
+  ctx->tagged = (uint64_t *)ctx->dalloc(sizeof(uint64_t) * ctx->tagged_words);
   ctx->am_part = (float2 *)ctx->dalloc(sizeof(float2) * 4 * sm_count() * S);
   ctx->am_count = (unsigned *)ctx->dalloc(sizeof(unsigned) * 64);
   ctx->sp = (StepParams *)ctx->dalloc(sizeof(StepParams));
   ctx->err = (int *)ctx->dalloc(sizeof(int) * 4);
-  const int max_phases = 5 * c.n_layers + 1;
-  ctx->done = (unsigned *)ctx->dalloc(sizeof(unsigned) * (max_phases + 1));
+  ctx->epoch = (unsigned *)ctx->dalloc(sizeof(unsigned) * 2);
   ctx->abort = (int *)ctx->dalloc(sizeof(int));
   std::vector<float> ones((size_t)c.d_model, 1.0f);
   for (auto &L : ctx->layers) {
@@ -209,22 +230,22 @@ extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **
   }
   ctx->final_norm = (float *)ctx->dalloc(sizeof(float) * c.d_model);
   bool ok = ctx->kv && ctx->x && ctx->q && ctx->att && ctx->act && ctx->rope_cos && ctx->rope_sin && ws &&
-            ctx->am_part && ctx->am_count && ctx->sp && ctx->err && ctx->final_norm && ctx->done && ctx->abort;
+            ctx->am_part && ctx->am_count && ctx->sp && ctx->err && ctx->final_norm && ctx->tagged && ctx->epoch &&
+            ctx->abort;
   for (auto &L : ctx->layers) ok = ok && L.attn_norm && L.mlp_norm;
   if (!ok) {
     mie_destroy(ctx);
     return fail(MIE_E_OOM, "mie_create: device allocation of %zu KV bytes failed", kv_bytes);
   }
-  ctx->attn_count = (unsigned *)ws;
-  ctx->attn_part = (float *)(ws + 256 + ((size_t)c.n_kv_heads * 4 + 255) / 256 * 256);
+  ctx->attn_ws = ws;
   cudaError_t e = cudaSuccess;
   auto chk = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
   chk(cudaMemsetAsync(ctx->kv, 0, kv_bytes, ctx->stream));
-  chk(cudaMemsetAsync(ws, 0, aws * S, ctx->stream));
+  chk(cudaMemsetAsync(ws, 0, aws_total, ctx->stream));
+  chk(reset_tags(ctx));
   chk(cudaMemsetAsync(ctx->am_count, 0, sizeof(unsigned) * 64, ctx->stream));
   chk(cudaMemsetAsync(ctx->err, 0, sizeof(int) * 4, ctx->stream));
   chk(cudaMemsetAsync(ctx->sp, 0, sizeof(StepParams), ctx->stream));
-  chk(cudaMemsetAsync(ctx->done, 0, sizeof(unsigned) * (max_phases + 1), ctx->stream));
   chk(cudaMemsetAsync(ctx->abort, 0, sizeof(int), ctx->stream));
   for (auto &L : ctx->layers) {
     chk(cudaMemcpyAsync(L.attn_norm, ones.data(), sizeof(float) * c.d_model, cudaMemcpyHostToDevice, ctx->stream));
@@ -484,9 +505,16 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
   const mie_config &c = ctx->cfg;
   out.clear();
   const int64_t half = (int64_t)c.n_kv_heads * c.block_size * c.head_dim;
+  // the persistent step's tagged vectors of each layer, and the previous layer's x
+  const int64_t w_qkv = even_words((int64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim);
+  const int64_t w_att = even_words((int64_t)c.n_heads * c.head_dim), w_d = even_words(c.d_model);
+  const uint64_t *x_prev = nullptr;  // layer 0 reads the embedding instead
   for (int l = 0; l < c.n_layers; ++l) {
     Layer &L = ctx->layers[(size_t)l];
     uint16_t *kv_layer = ctx->kv + (int64_t)l * 2 * half;
+    uint64_t *t_qkv = ctx->tagged + (int64_t)l * tagged_layer_words(c);
+    uint64_t *t_att = t_qkv + w_qkv, *t_x1 = t_att + w_att, *t_act = t_x1 + w_d, *t_x2 = t_act + even_words(c.ffn);
+    uint8_t *ws = ctx->attn_ws + (size_t)l * ctx->attn_ws_bytes;
     Phase qkv;  // qkv + RoPE + K/V write (layer 0 gathers the embedding first)
     qkv.kind = PH_GEMV;
     qkv.pro = l == 0 ? PRO_EMBED_NORM : PRO_NORM;
@@ -513,6 +541,8 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
     a.bs = c.block_size;
     a.sp = ctx->sp;
     a.err = ctx->err;
+    a.x_t = x_prev;
+    a.y_t = t_qkv;
     out.push_back(qkv);
 
     Phase at;
@@ -530,10 +560,12 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
     t.bs = c.block_size;
     t.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
     t.out = ctx->att;
-    t.ws_part = ctx->attn_part;
-    t.ws_count = ctx->attn_count;
+    t.ws_count = reinterpret_cast<unsigned *>(ws);
+    t.ws_part = reinterpret_cast<float *>(ws + attn_counter_bytes(c.n_kv_heads));
     t.n_splits = ctx->attn_splits;
     t.err = ctx->err;
+    t.qkv_t = t_qkv;
+    t.out_t = t_att;
     out.push_back(at);
 
     Phase o;  // x += Wo att
@@ -545,6 +577,10 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
     o.g.act_bf16 = c.act_bf16;
     o.g.y = ctx->x;
     o.g.err = ctx->err;
+    o.g.x_t = t_att;
+    o.g.res_t = x_prev;
+    o.g.embed = ctx->embed;
+    o.g.y_t = t_x1;
     out.push_back(o);
 
     Phase gu;  // act = silu(Wg n(x)) * (Wu n(x))
@@ -558,6 +594,8 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
     gu.g.act_bf16 = c.act_bf16;
     gu.g.y = ctx->act;
     gu.g.err = ctx->err;
+    gu.g.x_t = t_x1;
+    gu.g.y_t = t_act;
     out.push_back(gu);
 
     Phase dn;  // x += Wd act
@@ -569,7 +607,11 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
     dn.g.act_bf16 = c.act_bf16;
     dn.g.y = ctx->x;
     dn.g.err = ctx->err;
+    dn.g.x_t = t_act;
+    dn.g.res_t = t_x1;
+    dn.g.y_t = t_x2;
     out.push_back(dn);
+    x_prev = t_x2;
   }
   Phase hd;  // logits = Whead n(x); argmax
   hd.kind = PH_GEMV;
@@ -584,6 +626,7 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
   hd.g.am_count = ctx->am_count;
   hd.g.sp = ctx->sp;
   hd.g.err = ctx->err;
+  hd.g.x_t = x_prev;
   out.push_back(hd);
 }
 
@@ -595,8 +638,8 @@ static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
     PersistArgs pa;
     pa.ph = ctx->d_phases;
     pa.n_phases = (int)ctx->phases.size();
-    pa.done = ctx->done;
-    pa.reset_flag = ctx->done + ctx->phases.size();
+    pa.epoch = ctx->epoch;
+    pa.fin = ctx->epoch + 1;
     pa.abort = ctx->abort;
     pa.n_slots = ctx->plan.n_slots;
     pa.slot_bytes = ctx->plan.slot_bytes;
@@ -730,12 +773,12 @@ extern "C" mie_status mie_sync(mie_ctx *ctx) {
   MIE_CUDA(cudaMemcpy(&v, ctx->err, sizeof(int), cudaMemcpyDeviceToHost));
   MIE_CUDA(cudaMemcpy(&ab, ctx->abort, sizeof(int), cudaMemcpyDeviceToHost));
   if (ab) {
-    // a bounded wait gave up: the step's counters are in an unknown state, reset them
-    const int max_phases = 5 * ctx->cfg.n_layers + 1;
-    MIE_CUDA(cudaMemset(ctx->done, 0, sizeof(unsigned) * (max_phases + 1)));
+    // a bounded wait gave up: the step's counters and tags are in an unknown state
+    const mie_config &c = ctx->cfg;
     MIE_CUDA(cudaMemset(ctx->abort, 0, sizeof(int)));
     MIE_CUDA(cudaMemset(ctx->am_count, 0, sizeof(unsigned) * 64));
-    MIE_CUDA(cudaMemset(ctx->attn_count, 0, sizeof(unsigned) * ctx->cfg.n_kv_heads));
+    MIE_CUDA(cudaMemset(ctx->attn_ws, 0, ctx->attn_ws_bytes * c.n_layers * c.max_slots));
+    MIE_CUDA(reset_tags(ctx));
     MIE_CUDA(cudaMemset(ctx->err, 0, sizeof(int)));
     return fail(MIE_E_TIMEOUT, "decode step: a bounded device wait gave up (code %d)", v);
   }

@@ -11,10 +11,12 @@
 //    through a ring of shared-memory stages (TMA bulk copies, mbarrier handoff) and
 //    never waits for activations -- only for a free slot.  HBM stays busy across phase
 //    boundaries; the ring absorbs the synchronisation latency.
-//  * Consumer warps run the phases in order.  Between phases they meet at a grid
-//    barrier: each CTA adds one to the phase's counter (release) and the next phase
-//    polls it (acquire) with a bounded loop.  The last CTA of the LM-head phase resets
-//    every counter for the next launch.
+//  * Consumer warps run the phases in order.  There is no grid barrier: every phase
+//    writes its output vector as tagged 64-bit words (value | launch tag), each in its
+//    own buffer, and the next phase polls the words it needs until they carry this
+//    launch's tag.  A phase boundary so costs one round trip to L2 instead of a barrier
+//    (atomic, then polling a counter) followed by the loads of the vector.  The last CTA
+//    to finish advances the tag for the next launch.
 //  * A wait that gives up sets a global abort flag (every CTA then leaves), latches an
 //    error the host reads back, and drains this CTA's copies still in flight.
 #include "attn_core.cuh"
@@ -29,6 +31,16 @@ constexpr long kGridPolls = 1L << 25;      // bounded grid-barrier polling (~1 s
 
 struct ConsSync {
   __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(kPCT) : "memory"); }
+  // barrier that also returns whether v holds on every consumer thread
+  __device__ static bool all(bool v) {
+    int r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.and.pred q, 1, %2, p;\n selp.s32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((int)v), "n"(kPCT)
+        : "memory");
+    return r != 0;
+  }
 };
 
 __device__ __forceinline__ int ld_volatile(const int *p) { return *reinterpret_cast<const volatile int *>(p); }
@@ -44,19 +56,14 @@ __device__ __forceinline__ void stamp(unsigned long long *trace, int phase, int 
   if (trace && threadIdx.x == 0) trace[((size_t)phase * gridDim.x + blockIdx.x) * kTracePoints + point] = globaltimer();
 }
 
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Values fixed for the whole step, read once per launch: the position, the block ids
-// of the context (when it has at most kStepMaxBlocks blocks) and the RoPE angles of
-// the position.  Later phases read them from shared memory instead of chasing
-// pointers in global memory.
+// Values fixed for the whole step, read once per launch: the launch's tag, the token
+// and position, the block ids of the context (when it has at most kStepMaxBlocks
+// blocks) and the RoPE angles of the position.  Later phases read them from shared
+// memory instead of chasing pointers in global memory.
 constexpr int kStepMaxBlocks = 512;
 struct StepConst {
-  int pos, ctx, nblk_staged;
+  uint32_t tag;
+  int tok, pos, ctx, nblk_staged;
   int blk[kStepMaxBlocks];
   float rc[64], rs[64];
 };
@@ -69,34 +76,6 @@ struct PersistShared {
   unsigned last;
   int ok;
 };
-
-// Waits until *ctr >= target (every CTA finished the previous phase).
-__device__ bool grid_wait(const unsigned *ctr, unsigned target, int *abort, int *err, PersistShared &ps) {
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    for (long it = 0;; ++it) {
-      if (ld_acquire(ctr) >= target) break;
-      if (ld_volatile(abort)) { ok = 0; break; }
-      if (it > kGridPolls) {
-        ok = 0;
-        atomicExch(abort, 1);
-        latch_error(err, ERR_TIMEOUT);
-        break;
-      }
-      __nanosleep(20);
-    }
-    __threadfence();
-    ps.ok = ok;
-  }
-  ConsSync::sync();
-  return ps.ok != 0;
-}
-
-__device__ void grid_signal(unsigned *ctr) {
-  __threadfence();
-  ConsSync::sync();
-  if (threadIdx.x == 0) atomicAdd(ctr, 1u);
-}
 
 // Row range of this CTA for a GEMV phase (units of RU rows, balanced over the grid).
 struct RowRange {
@@ -126,9 +105,45 @@ struct Ring {
 
 // ---------------------------------------------------------------------- GEMV phase
 
+// The QKV epilogue for pair unit u, tagged variant: RoPE on q and k rows; k and v
+// rounded to bf16 go into the paged cache; q | k | v go out as tagged words for the
+// attention phase.  x0, x1 are the GEMV results of rows i and i + hd/2 of head h.
+__device__ __forceinline__ void qkv_store_tagged(const GemvArgs &a, const QkvPrefetch &q, int u, float x0, float x1,
+                                                 uint32_t tag) {
+  const int h2 = a.hd / 2;
+  const int h = u / h2, i = u % h2;
+  if (h < a.Hq + a.Hkv && q.pos_ok) {
+    const float c = q.crow[i], sn = q.srow[i];
+    const float r0 = x0 * c - x1 * sn, r1 = x1 * c + x0 * sn;
+    x0 = r0;
+    x1 = r1;
+  }
+  if (h >= a.Hq) {
+    x0 = round_bf16(x0);
+    x1 = round_bf16(x1);
+    if (q.blk_ok) {
+      const int isv = h >= a.Hq + a.Hkv;
+      const int g = h - a.Hq - (isv ? a.Hkv : 0);
+      uint16_t *dst = a.kv_layer + (int64_t)q.blk * a.block_stride + (int64_t)isv * a.Hkv * a.bs * a.hd +
+                      ((int64_t)g * a.bs + q.pos % a.bs) * a.hd;
+      dst[i] = (uint16_t)(__float_as_uint(x0) >> 16);
+      dst[i + h2] = (uint16_t)(__float_as_uint(x1) >> 16);
+    }
+  }
+  st_tagged(a.y_t + (int64_t)h * a.hd + i, x0, tag);
+  st_tagged(a.y_t + (int64_t)h * a.hd + i + h2, x1, tag);
+}
+
+__device__ __forceinline__ void give_up(const PersistArgs &pa) {
+  if (threadIdx.x == 0) {
+    atomicExch(pa.abort, 1);
+    latch_error(pa.err, ERR_TIMEOUT);
+  }
+}
+
 template <int F>
 __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, float *scratch, PersistShared &ps,
-                           const StepConst &sc, int *abort, int *err, unsigned long long *trace, int pidx) {
+                           const StepConst &sc, const PersistArgs &pa, int pidx) {
   using T = FmtT<F>;
   constexpr int EPC = T::EPC, CPL = T::CPL;
   constexpr int kBitsPerElem = (F == MIE_FMT_BF16) ? 16 : (F == MIE_FMT_I8 ? 8 : 4);
@@ -139,8 +154,11 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   const int Kp = m.kp, K = m.cols, M = m.rows;
   const RowRange rr = row_range(m, ph.epi);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  float *xs = scratch;       // [Kp]
-  float *part = xs + Kp;     // [rows of this CTA][KS]
+  const uint32_t tag = sc.tag;
+  const bool has_rows = rr.row1 > rr.row0;
+  float *xs = scratch;                            // [Kp]
+  float *part = xs + Kp;                          // [rows of this CTA][KS]
+  float *resv = part + (rr.row1 - rr.row0) * rr.KS;  // EPI_RESID: residual of this CTA's rows
 
   QkvPrefetch qp;
   if (ph.epi == EPI_QKV) {
@@ -152,8 +170,55 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     qp.crow = sc.rc;
     qp.srow = sc.rs;
   }
-  stage_input<kPCT, ConsSync>(a, ph.pro, xs, K, Kp, ps.red, &ps.scale, err);
-  stamp(trace, pidx, 2);
+
+  // input: the gains and the embedding are constants, loaded before the tagged words
+  // of the previous phases are polled; the residual rows are polled with the input
+  if (has_rows) {
+    constexpr int B = 8;
+    const bool one_batch = ph.pro != PRO_PLAIN && K <= kPCT * B;
+    float g0[B];
+    if (one_batch) {
+#pragma unroll
+      for (int j = 0; j < B; ++j) g0[j] = __ldg(a.gain + min(tid + j * kPCT, K - 1));
+    }
+    if (ph.epi == EPI_RESID && !a.res_t)
+      for (int r = rr.row0 + tid; r < rr.row1; r += kPCT) resv[r - rr.row0] = embed_at(a.embed, sc.tok, r);
+    if (ph.pro == PRO_EMBED_NORM) {
+      for (int k0 = tid; k0 < Kp; k0 += kPCT * B) {
+        float v[B];
+#pragma unroll
+        for (int j = 0; j < B; ++j) v[j] = embed_at(a.embed, sc.tok, min(k0 + j * kPCT, K - 1));
+#pragma unroll
+        for (int j = 0; j < B; ++j) {
+          const int k = k0 + j * kPCT;
+          if (k < Kp) xs[k] = (k < K) ? v[j] : 0.f;
+        }
+      }
+    }
+    const int n_in = (ph.pro == PRO_EMBED_NORM) ? 0 : (K + 1) / 2;
+    const int n_res = (ph.epi == EPI_RESID && a.res_t) ? rr.row1 - rr.row0 : 0;
+    bool ok = poll_pairs<kPCT, B>(n_in + n_res, tag, pa.abort, [&](int j, const uint64_t *&src, float *&dst, int &c) {
+      if (j < n_in) {
+        src = a.x_t + 2 * j;
+        dst = xs + 2 * j;
+        c = (2 * j + 1 < K) ? 2 : 1;
+      } else {
+        src = a.res_t + rr.row0 + (j - n_in);
+        dst = resv + (j - n_in);
+        c = 1;
+      }
+    });
+    if (ph.pro != PRO_EMBED_NORM)
+      for (int k = K + tid; k < Kp; k += kPCT) xs[k] = 0.f;
+    if (!ConsSync::all(ok)) {
+      give_up(pa);
+      return false;
+    }
+    stamp(pa.trace, pidx, 1);
+    normalize_staged<kPCT, ConsSync>(a, ph.pro, xs, K, ps.red, &ps.scale, one_batch ? g0 : nullptr);
+    ConsSync::sync();
+  }
+  stamp(pa.trace, pidx, 2);
 
   const int ri = warp / rr.KS, ks = warp % rr.KS;
   const bool has_slice = warp < rr.RPS * rr.KS;
@@ -170,16 +235,18 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     }
   }
 
-  // stream this CTA's stages of the phase
+  // stream this CTA's stages of the phase; a wait that gives up stops the math but
+  // keeps every warp on the same barriers
+  bool ok = true;
   for (int st = 0; st < rr.n_stages; ++st, ++s_global) {
     const int slot = s_global % ring.nst, k = s_global / ring.nst;
-    if (!mbar_wait(&ring.full[slot], k & 1)) {
-      atomicExch(abort, 1);
-      latch_error(err, ERR_TIMEOUT);
-      return false;
+    if (ok && !mbar_wait(&ring.full[slot], k & 1)) {
+      ok = false;
+      atomicExch(pa.abort, 1);
+      latch_error(pa.err, ERR_TIMEOUT);
     }
     const int r = rr.row0 + st * rr.RPS + ri;
-    if (has_slice && r < rr.row1) {
+    if (ok && has_slice && r < rr.row1) {
       const uint8_t *rowp =
           ring.w + (size_t)slot * ring.slot_bytes + (size_t)ri * m.row_bytes + (size_t)ks * kSliceBytes;
       float sum = 0.f;
@@ -213,8 +280,8 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     __syncwarp();
     if (lane == 0) mbar_arrive(&ring.empty[slot]);
   }
-  ConsSync::sync();
-  stamp(trace, pidx, 3);
+  if (!ConsSync::all(ok)) return false;
+  stamp(pa.trace, pidx, 3);
 
   // epilogue
   auto row_value = [&](int r) {
@@ -226,17 +293,17 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   if (ph.epi == EPI_STORE || ph.epi == EPI_RESID) {
     for (int r = rr.row0 + tid; r < rr.row1; r += kPCT) {
       const float v = row_value(r);
-      a.y[r] = (ph.epi == EPI_RESID) ? __ldcg(a.y + r) + v : v;
+      st_tagged(a.y_t + r, (ph.epi == EPI_RESID) ? resv[r - rr.row0] + v : v, tag);
     }
   } else if (ph.epi == EPI_SWIGLU) {
     for (int u = rr.u0 + tid; u < rr.u1; u += kPCT) {
       const float g = row_value(2 * u), up = row_value(2 * u + 1);
-      a.y[u] = g / (1.0f + expf(-g)) * up;
+      st_tagged(a.y_t + u, g / (1.0f + expf(-g)) * up, tag);
     }
   } else if (ph.epi == EPI_QKV) {
-    if (tid == 0 && blockIdx.x == 0 && !qp.blk_ok) latch_error(err, qp.pos_ok ? ERR_BLOCK_ID : ERR_POS);
+    if (tid == 0 && blockIdx.x == 0 && !qp.blk_ok) latch_error(pa.err, qp.pos_ok ? ERR_BLOCK_ID : ERR_POS);
     for (int u = rr.u0 + tid; u < rr.u1; u += kPCT)
-      qkv_store(a, qp, u, row_value(2 * u), row_value(2 * u + 1));
+      qkv_store_tagged(a, qp, u, row_value(2 * u), row_value(2 * u + 1), tag);
   } else if (ph.epi == EPI_ARGMAX) {
     float *logits = a.sp ? a.sp->logits_out : nullptr;
     if (logits) logits += (int64_t)a.slot * M;
@@ -301,7 +368,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
 // ---------------------------------------------------------------------- attention phase
 
 template <int G, int HD>
-__device__ void attn_phase(const AttnArgs &at, float *scratch, const StepConst &sc) {
+__device__ bool attn_phase(const AttnArgs &at, float *scratch, const StepConst &sc, const PersistArgs &pa) {
   auto &sm = *reinterpret_cast<AttnSmem<G, HD, kPW> *>(scratch);
   int ctx = sc.ctx;
   const int32_t *bt = at.sp->block_table + (int64_t)at.slot * at.sp->max_blocks;
@@ -315,8 +382,14 @@ __device__ void attn_phase(const AttnArgs &at, float *scratch, const StepConst &
   const int *pre = (nblk <= sc.nblk_staged) ? sc.blk : nullptr;
   const int nsplit = attn_nsplit(nblk, at.n_splits, attn_blocks_per_split<HD, kPW>(at.bs));
   const int items = at.Hkv * nsplit;
-  for (int it = blockIdx.x; it < items; it += gridDim.x)
-    attn_split<G, HD, kPW, ConsSync>(at, it / nsplit, it % nsplit, nsplit, ctx, bt, pre, sm);
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
+    if (!attn_split<G, HD, kPW, ConsSync, true>(at, it / nsplit, it % nsplit, nsplit, ctx, bt, pre, sm, sc.tag,
+                                                pa.abort)) {
+      give_up(pa);
+      return false;
+    }
+  }
+  return true;
 }
 
 // ---------------------------------------------------------------------- producer
@@ -445,10 +518,12 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
   __shared__ __align__(8) uint64_t full_bar[kPRingMax], empty_bar[kPRingMax];
   __shared__ PersistShared ps;
   __shared__ StepConst sc;
-  // descriptors of the current and the next phase: read from shared memory, not through
-  // global loads that every barrier's acquire would send back to L2
+  // descriptors of the current and the next phase, in shared memory; the one after
+  // is loaded into registers while the current phase runs
   __shared__ __align__(16) Phase s_ph[2];
   __shared__ volatile int s_issued, s_prod_done;
+  constexpr int kPhWords = sizeof(Phase) / 4;
+  static_assert(sizeof(Phase) % 4 == 0 && kPhWords <= kPCT, "one descriptor word per consumer thread");
 
   Ring ring;
   ring.nst = a.n_slots;
@@ -482,6 +557,7 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
     const GemvArgs &g0 = a.ph[0].g;  // layer 0's QKV phase carries the step's tables
     const StepParams *sp = g0.sp;
     const int pos = sp->pos[g0.slot];
+    int tok = sp->token[g0.slot];
     const int ctx = pos + 1;
     const int n_table = sp->max_blocks;
     const int nblk = min((max(ctx, 0) + g0.bs - 1) / g0.bs, n_table);
@@ -509,52 +585,53 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
       sc.rs[tid] = g0.rope_sin[(int64_t)pos_c * h2 + tid];
     }
     if (tid == 0) {
+      if (tok < 0 || tok >= g0.vocab) {
+        latch_error(a.err, ERR_TOKEN);
+        tok = 0;
+      }
+      sc.tag = __ldcg(a.epoch);
+      sc.tok = tok;
       sc.pos = pos;
       sc.ctx = ctx;
       sc.nblk_staged = staged;
     }
-    ConsSync::sync();
   }
-  auto copy_phase = [&](int p) {
-    if (p >= a.n_phases) return;
-    constexpr int W = sizeof(Phase) / 4;
-    const uint32_t *src = reinterpret_cast<const uint32_t *>(a.ph + p);
-    uint32_t *dst = reinterpret_cast<uint32_t *>(&s_ph[p & 1]);
-    for (int i = tid; i < W; i += kPCT) dst[i] = __ldcg(src + i);
-  };
-  copy_phase(0);
-  copy_phase(1);
+  const uint32_t *ph_words = reinterpret_cast<const uint32_t *>(a.ph);
+  for (int p = 0; p < 2 && p < a.n_phases; ++p)
+    if (tid < kPhWords) reinterpret_cast<uint32_t *>(&s_ph[p])[tid] = __ldcg(ph_words + (size_t)p * kPhWords + tid);
   ConsSync::sync();
   int s_global = 0;
   bool ok = true;
-  for (int p = 0; p < a.n_phases && ok; ++p) {
+  for (int p = 0; p < a.n_phases; ++p) {
+    const uint32_t next_word =
+        (p + 2 < a.n_phases && tid < kPhWords) ? __ldcg(ph_words + (size_t)(p + 2) * kPhWords + tid) : 0u;
     const Phase &ph = s_ph[p & 1];
     stamp(a.trace, p, 0);
-    if (p > 0 && !grid_wait(&a.done[p - 1], gridDim.x, a.abort, a.err, ps)) {
-      ok = false;
-      break;
-    }
-    stamp(a.trace, p, 1);
     if (ph.kind == PH_GEMV) {
-      if (ph.g.m.fmt == FL) ok = gemv_phase<FL>(ph, ring, s_global, scratch, ps, sc, a.abort, a.err, a.trace, p);
-      else ok = gemv_phase<FH>(ph, ring, s_global, scratch, ps, sc, a.abort, a.err, a.trace, p);
+      if (ph.g.m.fmt == FL) ok = gemv_phase<FL>(ph, ring, s_global, scratch, ps, sc, a, p);
+      else ok = gemv_phase<FH>(ph, ring, s_global, scratch, ps, sc, a, p);
     } else {
+      stamp(a.trace, p, 1);
       stamp(a.trace, p, 2);
-      attn_phase<G, HD>(ph.at, scratch, sc);
+      ok = attn_phase<G, HD>(ph.at, scratch, sc, a);
       stamp(a.trace, p, 3);
     }
     ConsSync::sync();
     stamp(a.trace, p, 4);
-    copy_phase(p + 2);  // into the slot phase p used; visible after the next barrier
-    if (ok && p + 1 < a.n_phases) grid_signal(&a.done[p]);
+    if (!ok) break;
+    if (p + 2 < a.n_phases && tid < kPhWords) reinterpret_cast<uint32_t *>(&s_ph[p & 1])[tid] = next_word;
   }
   if (ok) {
-    // the last CTA of the final phase (it reset the argmax counter) resets the rest:
-    // every CTA has passed every grid wait of this launch by then
-    if (tid == 0 && a.reset_flag && atomicAdd(a.reset_flag, 1u) == gridDim.x - 1) {
-      for (int p = 0; p < a.n_phases; ++p) a.done[p] = 0u;
+    // the last CTA to finish advances the tag for the next launch (never 0, the tag of
+    // words no launch has written)
+    if (tid == 0) {
       __threadfence();
-      *a.reset_flag = 0u;
+      if (atomicAdd(a.fin, 1u) == gridDim.x - 1) {
+        const unsigned next = sc.tag + 1u;
+        *a.epoch = next ? next : 1u;
+        *a.fin = 0u;
+        __threadfence();
+      }
     }
     return;
   }
@@ -615,7 +692,7 @@ mie_status persist_plan(const Phase *host_phases, int n, int G, int HD, PersistP
     const uint32_t scb = m.fmt == MIE_FMT_Q4_0 ? (uint32_t)((RPS * m.s_stride * 2 + 127) / 128 * 128) : 0u;
     if (sb > slot) slot = sb;
     if (scb > slot_sc) slot_sc = scb;
-    const size_t need = sizeof(float) * ((size_t)m.kp + (size_t)rows_max * KS);
+    const size_t need = sizeof(float) * ((size_t)m.kp + (size_t)rows_max * (KS + 1));
     if (need > scratch) scratch = need;
     if (((uintptr_t)m.w & 15) || (m.row_bytes & 15)) return fail(MIE_E_SHAPE, "persistent step: unaligned rows");
   }
