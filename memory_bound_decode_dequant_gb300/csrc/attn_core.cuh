@@ -48,16 +48,17 @@ struct AttnSmem {
 };
 
 // The loads of one group of tokens for one lane: 64 bytes of its key, and its value
-// dims of every token of the group.  Masked tokens read the pool base (always valid)
-// and are zeroed later, so the loads carry no branches and issue back to back.
+// dims of every token of the group.  Masked tokens read a valid address and are
+// zeroed later, so the loads carry no branches and issue back to back.
 template <int HD>
 struct KvGroup {
   static constexpr int LPT = HD / 32, TPI = 32 / LPT, DPL = HD / 32, VW = DPL == 4 ? 2 : 1;
   uint4 kv[4];
   uint32_t vraw[TPI][VW];
   unsigned vmask;  // bit i: token i of the group is valid
-  int kblk;
+  int kblk;        // >= 0: this lane's key token is valid
 
+  // From the paged pool in global memory, through the block ids ids[.. - id0].
   __device__ __forceinline__ void load(const AttnArgs &a, const int *ids, int id0, int tb, int t1, int64_t head_off,
                                        int lane) {
     const int tok_in = lane / LPT, part_in = lane % LPT;
@@ -88,11 +89,132 @@ struct KvGroup {
   }
 };
 
+// bf16 bits of two values that are already bf16-exact, packed as the cache holds them.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+}
+
+// Puts the current token's k and v (bf16-exact floats kn[HD], vn[HD]) in place of
+// what the group loaded for it; pi = its index in the group (warp-uniform).
+template <int HD>
+__device__ __forceinline__ void patch_current(KvGroup<HD> &cur, int pi, const float *kn, const float *vn, int lane) {
+  using KG = KvGroup<HD>;
+  constexpr int LPT = KG::LPT, TPI = KG::TPI, DPL = KG::DPL, VW = KG::VW;
+  if (pi < 0 || pi >= TPI) return;
+  if (lane / LPT == pi) {
+    const float *k = kn + (lane % LPT) * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      cur.kv[i] = make_uint4(pack_bf16x2(k[8 * i], k[8 * i + 1]), pack_bf16x2(k[8 * i + 2], k[8 * i + 3]),
+                             pack_bf16x2(k[8 * i + 4], k[8 * i + 5]), pack_bf16x2(k[8 * i + 6], k[8 * i + 7]));
+  }
+#pragma unroll
+  for (int i = 0; i < TPI; ++i) {
+    if (i != pi) continue;
+    if constexpr (DPL == 1) {
+      cur.vraw[i][0] = __float_as_uint(vn[lane]) >> 16;
+    } else {
+#pragma unroll
+      for (int w = 0; w < VW; ++w) cur.vraw[i][w] = pack_bf16x2(vn[lane * DPL + 2 * w], vn[lane * DPL + 2 * w + 1]);
+    }
+  }
+}
+
+// The group's values as fp32 (zero for masked tokens).
+template <int HD>
+__device__ __forceinline__ void group_values(const KvGroup<HD> &cur, float (&vf)[KvGroup<HD>::TPI][KvGroup<HD>::DPL]) {
+  using KG = KvGroup<HD>;
+  constexpr int TPI = KG::TPI, DPL = KG::DPL, VW = KG::VW;
+#pragma unroll
+  for (int i = 0; i < TPI; ++i) {
+    const bool ok = (cur.vmask >> i) & 1u;
+    if constexpr (DPL == 1) {
+      vf[i][0] = ok ? __uint_as_float(cur.vraw[i][0] << 16) : 0.f;
+    } else {
+#pragma unroll
+      for (int w = 0; w < VW; ++w) {
+        vf[i][2 * w] = ok ? __uint_as_float(cur.vraw[i][w] << 16) : 0.f;
+        vf[i][2 * w + 1] = ok ? __uint_as_float(cur.vraw[i][w] & 0xffff0000u) : 0.f;
+      }
+    }
+  }
+}
+
+// Partial dot products of this lane's 32 key dims with the G queries at shared
+// address q (fp32, 16-byte aligned), read as float4 into four accumulators.
+template <int G, int HD>
+__device__ __forceinline__ void group_scores(const KvGroup<HD> &cur, uint32_t q, int part_in, float (&sc)[G]) {
+  float kf[32];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {cur.kv[i].x, cur.kv[i].y, cur.kv[i].z, cur.kv[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      kf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      kf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const uint32_t qh = q + (uint32_t)(h * HD + part_in * 32) * 4;
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 qq = lds128f(qh + 16 * i);
+      d[0] = fmaf(qq.x, kf[4 * i], d[0]);
+      d[1] = fmaf(qq.y, kf[4 * i + 1], d[1]);
+      d[2] = fmaf(qq.z, kf[4 * i + 2], d[2]);
+      d[3] = fmaf(qq.w, kf[4 * i + 3], d[3]);
+    }
+    sc[h] = (d[0] + d[1]) + (d[2] + d[3]);
+  }
+}
+
+// Online-softmax update of (m, l, o) with one group: scores summed over the lanes of a
+// token, masked, scaled; then the values weighted by the new probabilities.
+template <int G, int HD>
+__device__ __forceinline__ void group_update(float (&sc)[G], const float (&vf)[KvGroup<HD>::TPI][KvGroup<HD>::DPL],
+                                             int kblk, float scale, int part_in, float (&m)[G], float (&l)[G],
+                                             float (&o)[G][KvGroup<HD>::DPL]) {
+  using KG = KvGroup<HD>;
+  constexpr int LPT = KG::LPT, TPI = KG::TPI, DPL = KG::DPL;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int off = 1; off < LPT; off <<= 1) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
+    sc[h] = (kblk >= 0) ? sc[h] * scale : -INFINITY;
+  }
+  float p[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    const float mn = fmaxf(m[h], warp_max(sc[h]));
+    if (mn == -INFINITY) {
+      p[h] = 0.f;
+      continue;
+    }
+    const float corr = expf(m[h] - mn);  // 0 while m was -inf
+    p[h] = (sc[h] == -INFINITY) ? 0.f : expf(sc[h] - mn);
+    const float ps = warp_sum(part_in == 0 ? p[h] : 0.f);  // each token counted once
+    l[h] = l[h] * corr + ps;
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) o[h][d] *= corr;
+    m[h] = mn;
+  }
+#pragma unroll
+  for (int i = 0; i < TPI; ++i) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float ph = __shfl_sync(0xffffffffu, p[h], i * LPT);
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(ph, vf[i][d], o[h][d]);
+    }
+  }
+}
+
 // Tagged variant: polls the group's queries into sm.q and, when has_pos, the current
 // token's k and v of KV head g into sm.kn / sm.vn, all in one batch of round trips.
-template <int G, int HD, int NT, class Sync>
-__device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, AttnSmem<G, HD, NT / 32> &sm, uint32_t tag,
-                              const int *abort) {
+template <int G, int HD, int NT, class Sync, class SM>
+__device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, SM &sm, uint32_t tag, const int *abort) {
   constexpr int NQ = G * HD / 2, NK = HD / 2;
   const uint64_t *qs = a.qkv_t + (int64_t)(g * G) * HD;
   const uint64_t *ks = a.qkv_t + (int64_t)(a.Hq + g) * HD;
@@ -114,18 +236,114 @@ __device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, AttnSmem<G
   return Sync::all(ok);
 }
 
-// bf16 bits of two values that are already bf16-exact, packed as the cache holds them.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  return (__float_as_uint(lo) >> 16) | (__float_as_uint(hi) & 0xffff0000u);
+// After a split of KV head g wrote its partial (m, l, o) to the workspace: the last
+// split of the head to arrive (atomic counter, no waiting) merges all nsplit partials
+// into the output and resets the counter.  `last` is a shared-memory flag.
+template <int G, int HD, int NT, class Sync, bool Tagged>
+__device__ void attn_merge_splits(const AttnArgs &a, int g, int nsplit, unsigned &last, uint32_t tag) {
+  constexpr int PART = G * (2 + HD);
+  const int tid = threadIdx.x;
+  __threadfence();
+  Sync::sync();
+  if (tid == 0) last = (atomicAdd(a.ws_count + g, 1u) == (unsigned)nsplit - 1);
+  Sync::sync();
+  if (!last) return;
+  __threadfence();
+  const float *base = a.ws_part + (int64_t)g * a.n_splits * PART;
+  for (int i = tid; i < G * HD; i += NT) {
+    const int h = i / HD;
+    // one pass with online rescaling, eight splits' partials loaded per round trip
+    float M = -INFINITY, O = 0.f, L = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += 8) {
+      float ms[8], os[8], ls[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float *p = base + (int64_t)min(s0 + j, nsplit - 1) * PART;
+        ms[j] = __ldcg(p + h);
+        ls[j] = __ldcg(p + G + h);
+        os[j] = __ldcg(p + 2 * G + i);
+      }
+      float mb = M;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (s0 + j < nsplit) mb = fmaxf(mb, ms[j]);
+      if (mb == -INFINITY) continue;
+      const float c = (M == -INFINITY) ? 0.f : expf(M - mb);
+      O *= c;
+      L *= c;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (s0 + j < nsplit && ms[j] != -INFINITY) {
+          const float f = expf(ms[j] - mb);
+          O = fmaf(os[j], f, O);
+          L = fmaf(ls[j], f, L);
+        }
+      }
+      M = mb;
+    }
+    const float r = (L > 0.f) ? O / L : 0.f;
+    if constexpr (Tagged) st_tagged(a.out_t + (g * G) * HD + i, r, tag);
+    else a.out[(g * G) * HD + i] = r;
+  }
+  if (tid == 0) a.ws_count[g] = 0u;
+  Sync::sync();
 }
 
-// Computes split s of nsplit for KV head g.  With one split the result goes straight
-// to a.out; otherwise the split's (m, l, o) partial goes to the workspace and the last
-// split of the head to finish (atomic counter, no waiting) merges all partials and
-// resets the counter.  blk_pre, when not null, holds the block ids of blocks
-// [0, nblk) already staged in shared memory; otherwise they are read from bt in
-// chunks.  Sync::sync() is a barrier over the NW participating warps, whose threads
-// are numbered 0 .. NW*32-1.
+// Finishes split s of nsplit for KV head g from every warp's (m, l, o): with one split
+// the result goes straight to the output; otherwise the split's partial goes to the
+// workspace and the last split of the head to finish (atomic counter, no waiting)
+// merges all partials and resets the counter.  Tagged: the output is written as
+// tagged words to a.out_t, else as floats to a.out.
+template <int G, int HD, int NW, class Sync, bool Tagged>
+__device__ void attn_store(const AttnArgs &a, int g, int s, int nsplit, const float (&m)[G], const float (&l)[G],
+                           const float (&o)[G][KvGroup<HD>::DPL], AttnSmem<G, HD, NW> &sm, uint32_t tag) {
+  constexpr int DPL = KvGroup<HD>::DPL;
+  constexpr int PART = G * (2 + HD);
+  constexpr int NT = NW * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  auto put = [&](int i, float r) {
+    if constexpr (Tagged) st_tagged(a.out_t + (g * G) * HD + i, r, tag);
+    else a.out[(g * G) * HD + i] = r;
+  };
+  // merge the warps
+  if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < G; ++h) { sm.m[warp][h] = m[h]; sm.l[warp][h] = l[h]; }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h)
+#pragma unroll
+    for (int d = 0; d < DPL; ++d) sm.o[warp][h][lane * DPL + d] = o[h][d];
+  Sync::sync();
+  float *part = a.ws_part + ((int64_t)g * a.n_splits + s) * PART;
+  for (int i = tid; i < G * HD; i += NT) {
+    const int h = i / HD, d = i % HD;
+    float M = -INFINITY;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.m[w][h]);
+    float O = 0.f, L = 0.f;
+    for (int w = 0; w < NW; ++w) {
+      const float f = (sm.m[w][h] == -INFINITY) ? 0.f : expf(sm.m[w][h] - M);
+      O = fmaf(sm.o[w][h][d], f, O);
+      L = fmaf(sm.l[w][h], f, L);
+    }
+    if (nsplit == 1) {
+      put(i, (L > 0.f) ? O / L : 0.f);
+    } else {
+      part[2 * G + i] = O;
+      if (d == 0) { part[h] = M; part[G + h] = L; }
+    }
+  }
+  if (nsplit == 1) {
+    Sync::sync();  // the scratch is reused by the caller's next item
+    return;
+  }
+  attn_merge_splits<G, HD, NT, Sync, Tagged>(a, g, nsplit, sm.last, tag);
+}
+
+// Computes split s of nsplit for KV head g, reading K/V from the paged pool.
+// blk_pre, when not null, holds the block ids of blocks [0, nblk) already staged in
+// shared memory; otherwise they are read from bt in chunks.  Sync::sync() is a barrier
+// over the NW participating warps, whose threads are numbered 0 .. NW*32-1.
 //
 // Tagged (the persistent step): q and the current token's k and v (position ctx-1)
 // are polled as tagged words from a.qkv_t, whose k and v values are already rounded
@@ -136,8 +354,7 @@ template <int G, int HD, int NW, class Sync, bool Tagged = false>
 __device__ bool attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx, const int32_t *bt, const int *blk_pre,
                            AttnSmem<G, HD, NW> &sm, uint32_t tag = 0, const int *abort = nullptr) {
   using KG = KvGroup<HD>;
-  constexpr int LPT = KG::LPT, TPI = KG::TPI, DPL = KG::DPL, VW = KG::VW;
-  constexpr int PART = G * (2 + HD);
+  constexpr int TPI = KG::TPI, DPL = KG::DPL, LPT = KG::LPT;
   constexpr int NT = NW * 32;
   constexpr int QB = (G * HD + NT - 1) / NT;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -200,101 +417,15 @@ __device__ bool attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
       q_stored = true;
     }
     for (; tb < t1; tb += NW * TPI) {
-      if constexpr (Tagged) {
-        const int pi = pos - tb;  // the current token's place in this warp's group
-        if (has_pos && pi >= 0 && pi < TPI) {
-          if (lane / LPT == pi) {
-            const float *kn = sm.kn + part_in * 32;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              cur.kv[i] = make_uint4(pack_bf16x2(kn[8 * i], kn[8 * i + 1]), pack_bf16x2(kn[8 * i + 2], kn[8 * i + 3]),
-                                     pack_bf16x2(kn[8 * i + 4], kn[8 * i + 5]), pack_bf16x2(kn[8 * i + 6], kn[8 * i + 7]));
-          }
-#pragma unroll
-          for (int i = 0; i < TPI; ++i) {
-            if (i != pi) continue;
-            if constexpr (DPL == 1) {
-              cur.vraw[i][0] = __float_as_uint(sm.vn[lane]) >> 16;
-            } else {
-#pragma unroll
-              for (int w = 0; w < VW; ++w)
-                cur.vraw[i][w] = pack_bf16x2(sm.vn[lane * DPL + 2 * w], sm.vn[lane * DPL + 2 * w + 1]);
-            }
-          }
-        }
-      }
+      if (has_pos) patch_current<HD>(cur, pos - tb, sm.kn, sm.vn, lane);
       const int kblk = cur.kblk;
       float vf[TPI][DPL];
-#pragma unroll
-      for (int i = 0; i < TPI; ++i) {
-        const bool ok = (cur.vmask >> i) & 1u;
-        if constexpr (DPL == 1) {
-          vf[i][0] = ok ? __uint_as_float(cur.vraw[i][0] << 16) : 0.f;
-        } else {
-#pragma unroll
-          for (int w = 0; w < VW; ++w) {
-            vf[i][2 * w] = ok ? __uint_as_float(cur.vraw[i][w] << 16) : 0.f;
-            vf[i][2 * w + 1] = ok ? __uint_as_float(cur.vraw[i][w] & 0xffff0000u) : 0.f;
-          }
-        }
-      }
+      group_values<HD>(cur, vf);
       float sc[G];
-      {
-        float kf[32];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t w[4] = {cur.kv[i].x, cur.kv[i].y, cur.kv[i].z, cur.kv[i].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            kf[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
-            kf[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float *qh = sm.q + h * HD + part_in * 32;
-          float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            d0 = fmaf(qh[i], kf[i], d0);
-            d1 = fmaf(qh[i + 1], kf[i + 1], d1);
-          }
-          sc[h] = d0 + d1;
-        }
-      }
+      group_scores<G, HD>(cur, smem_u32(sm.q), part_in, sc);
       // the next group's loads go out before this group's softmax
       if (tb + NW * TPI < t1) cur.load(a, ids, id0, tb + NW * TPI, t1, head_off, lane);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-#pragma unroll
-        for (int off = 1; off < LPT; off <<= 1) sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], off);
-        sc[h] = (kblk >= 0) ? sc[h] * a.scale : -INFINITY;
-      }
-      float p[G];
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float mn = fmaxf(m[h], warp_max(sc[h]));
-        if (mn == -INFINITY) {
-          p[h] = 0.f;
-          continue;
-        }
-        const float corr = expf(m[h] - mn);  // 0 while m was -inf
-        p[h] = (sc[h] == -INFINITY) ? 0.f : expf(sc[h] - mn);
-        const float ps = warp_sum(part_in == 0 ? p[h] : 0.f);  // each token counted once
-        l[h] = l[h] * corr + ps;
-#pragma unroll
-        for (int d = 0; d < DPL; ++d) o[h][d] *= corr;
-        m[h] = mn;
-      }
-#pragma unroll
-      for (int i = 0; i < TPI; ++i) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-          const float ph = __shfl_sync(0xffffffffu, p[h], i * LPT);
-#pragma unroll
-          for (int d = 0; d < DPL; ++d) o[h][d] = fmaf(ph, vf[i][d], o[h][d]);
-        }
-      }
+      group_update<G, HD>(sc, vf, kblk, a.scale, part_in, m, l, o);
     }
   }
   if (!q_stored) {  // empty split: keep the barrier count of the other paths
@@ -304,85 +435,7 @@ __device__ bool attn_split(const AttnArgs &a, int g, int s, int nsplit, int ctx,
       Sync::sync();
     }
   }
-
-  // merge the warps
-  if (lane == 0) {
-#pragma unroll
-    for (int h = 0; h < G; ++h) { sm.m[warp][h] = m[h]; sm.l[warp][h] = l[h]; }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h)
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) sm.o[warp][h][lane * DPL + d] = o[h][d];
-  Sync::sync();
-  float *part = a.ws_part + ((int64_t)g * a.n_splits + s) * PART;
-  for (int i = tid; i < G * HD; i += NT) {
-    const int h = i / HD, d = i % HD;
-    float M = -INFINITY;
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm.m[w][h]);
-    float O = 0.f, L = 0.f;
-    for (int w = 0; w < NW; ++w) {
-      const float f = (sm.m[w][h] == -INFINITY) ? 0.f : expf(sm.m[w][h] - M);
-      O = fmaf(sm.o[w][h][d], f, O);
-      L = fmaf(sm.l[w][h], f, L);
-    }
-    if (nsplit == 1) {
-      const float r = (L > 0.f) ? O / L : 0.f;
-      if constexpr (Tagged) st_tagged(a.out_t + (g * G) * HD + i, r, tag);
-      else a.out[(g * G) * HD + i] = r;
-    } else {
-      part[2 * G + i] = O;
-      if (d == 0) { part[h] = M; part[G + h] = L; }
-    }
-  }
-  if (nsplit == 1) {
-    Sync::sync();  // the scratch is reused by the caller's next item
-    return true;
-  }
-  __threadfence();
-  Sync::sync();
-  if (tid == 0) sm.last = (atomicAdd(a.ws_count + g, 1u) == (unsigned)nsplit - 1);
-  Sync::sync();
-  if (!sm.last) return true;
-  __threadfence();
-  const float *base = a.ws_part + (int64_t)g * a.n_splits * PART;
-  for (int i = tid; i < G * HD; i += NT) {
-    const int h = i / HD;
-    // one pass with online rescaling, eight splits' partials loaded per round trip
-    float M = -INFINITY, O = 0.f, L = 0.f;
-    for (int s0 = 0; s0 < nsplit; s0 += 8) {
-      float ms[8], os[8], ls[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float *p = base + (int64_t)min(s0 + j, nsplit - 1) * PART;
-        ms[j] = __ldcg(p + h);
-        ls[j] = __ldcg(p + G + h);
-        os[j] = __ldcg(p + 2 * G + i);
-      }
-      float mb = M;
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (s0 + j < nsplit) mb = fmaxf(mb, ms[j]);
-      if (mb == -INFINITY) continue;
-      const float c = (M == -INFINITY) ? 0.f : expf(M - mb);
-      O *= c;
-      L *= c;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (s0 + j < nsplit && ms[j] != -INFINITY) {
-          const float f = expf(ms[j] - mb);
-          O = fmaf(os[j], f, O);
-          L = fmaf(ls[j], f, L);
-        }
-      }
-      M = mb;
-    }
-    const float r = (L > 0.f) ? O / L : 0.f;
-    if constexpr (Tagged) st_tagged(a.out_t + (g * G) * HD + i, r, tag);
-    else a.out[(g * G) * HD + i] = r;
-  }
-  if (tid == 0) a.ws_count[g] = 0u;
-  Sync::sync();
+  attn_store<G, HD, NW, Sync, Tagged>(a, g, s, nsplit, m, l, o, sm, tag);
   return true;
 }
 

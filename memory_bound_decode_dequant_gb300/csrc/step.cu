@@ -27,7 +27,6 @@ constexpr int kPW = 8;                     // consumer warps
 constexpr int kPThreads = 32 * (kPW + 1);  // + one producer warp
 constexpr int kPCT = kPW * 32;             // consumer threads
 constexpr int kPRingMax = 32;              // ring slots (static mbarriers)
-constexpr long kGridPolls = 1L << 25;      // bounded grid-barrier polling (~1 s)
 
 struct ConsSync {
   __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(kPCT) : "memory"); }
@@ -63,10 +62,22 @@ __device__ __forceinline__ void stamp(unsigned long long *trace, int phase, int 
 constexpr int kStepMaxBlocks = 512;
 struct StepConst {
   uint32_t tag;
-  int tok, pos, ctx, nblk_staged;
+  int tok, pos;
+  int ctx;           // attention context: pos + 1, clamped to the block table
+  int n_table;       // block-table entries of the slot
+  const int32_t *bt; // the slot's block table
+  int nblk_staged;
   int blk[kStepMaxBlocks];
   float rc[64], rs[64];
 };
+
+// The attention context of the step: positions 0..pos, clamped to the n_table blocks
+// the table holds (the clamp is reported as a position error).
+__device__ __forceinline__ int attn_ctx(int pos, int n_table, int bs) {
+  int ctx = pos + 1;
+  if (ctx > n_table * bs) ctx = n_table * bs;
+  return ctx < 0 ? 0 : ctx;
+}
 
 struct PersistShared {
   float red[kPW];
@@ -163,9 +174,9 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   QkvPrefetch qp;
   if (ph.epi == EPI_QKV) {
     qp.pos = sc.pos;
-    qp.pos_ok = sc.pos >= 0 && sc.pos < a.max_pos && sc.pos / a.bs < a.sp->max_blocks;
+    qp.pos_ok = sc.pos >= 0 && sc.pos < a.max_pos && sc.pos / a.bs < sc.n_table;
     const int b = qp.pos_ok ? sc.pos / a.bs : 0;
-    qp.blk = (b < sc.nblk_staged) ? sc.blk[b] : a.sp->block_table[(int64_t)a.slot * a.sp->max_blocks + b];
+    qp.blk = (b < sc.nblk_staged) ? sc.blk[b] : sc.bt[b];
     qp.blk_ok = qp.pos_ok && qp.blk >= 0 && qp.blk < a.n_kv_blocks;
     qp.crow = sc.rc;
     qp.srow = sc.rs;
@@ -366,25 +377,189 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
 }
 
 // ---------------------------------------------------------------------- attention phase
+//
+// One attention item = (KV head g, split sp of nsplit).  Its K/V arrive as ring
+// stages of up to `cap` whole blocks, K of the stage's token t at byte t*hd*2 and V at
+// cap*kb + t*hd*2 (kb = bs*hd*2 bytes per block).  With a whole chunk in shared
+// memory the item runs three CTA-wide passes per stage instead of the per-warp online
+// softmax of the standalone kernel, whose shuffle chains cost about 5000 cycles per
+// 16 tokens at one CTA per SM (measured): (1) a score for every (head, token) pair,
+// lanes starting at different 16-byte chunks of their key rows so that the reads
+// avoid bank conflicts; (2) one warp per head takes max, exp and sum and rescales
+// the running (m, l); (3) every thread accumulates its (head, dim) outputs over the
+// chunk.  The softmax is the same two-pass definition, evaluated per stage with the
+// running maximum carried across stages.
+
+constexpr int kChunkTok = 256;  // tokens of one attention stage at most
 
 template <int G, int HD>
-__device__ bool attn_phase(const AttnArgs &at, float *scratch, const StepConst &sc, const PersistArgs &pa) {
-  auto &sm = *reinterpret_cast<AttnSmem<G, HD, kPW> *>(scratch);
-  int ctx = sc.ctx;
-  const int32_t *bt = at.sp->block_table + (int64_t)at.slot * at.sp->max_blocks;
-  const int n_table = at.sp->max_blocks;
-  if (ctx > n_table * at.bs) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) latch_error(at.err, ERR_POS);
-    ctx = n_table * at.bs;
-  }
-  if (ctx < 0) ctx = 0;
+struct RingAttnSmem {
+  float q[G * HD];
+  float kn[HD], vn[HD];   // the current token's k and v (bf16-exact)
+  float s[G][kChunkTok];  // scores, then probabilities (zero past the chunk up to a multiple of 4)
+  float m[G], l[G], corr[G];
+  unsigned last;
+};
+
+// Blocks per attention stage: as many as a ring slot holds, at most kChunkTok tokens.
+__host__ __device__ inline int attn_stage_blocks(uint32_t slot_bytes, int bs, int hd) {
+  const int cap = (int)(slot_bytes / (2u * (uint32_t)bs * hd * 2));
+  const int lim = kChunkTok / bs;
+  return cap < lim ? cap : lim;
+}
+
+template <int G, int HD>
+__device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, int ctx, const Ring &ring,
+                               int &s_global, RingAttnSmem<G, HD> &sm, const StepConst &sc, const PersistArgs &pa) {
+  constexpr int NO = (G * HD + kPCT - 1) / kPCT;  // outputs per thread
+  constexpr int NCH = HD / 8;                      // 16-byte chunks of a key row
+  static_assert(2 * HD <= kPCT, "one thread per element of the current token's k and v");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nblk = (ctx + at.bs - 1) / at.bs;
-  const int *pre = (nblk <= sc.nblk_staged) ? sc.blk : nullptr;
+  const int b0 = (int)((int64_t)sp * nblk / nsplit), b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
+  const int t_end = min(b1 * at.bs, ctx);
+  const int pos = ctx - 1;
+  const bool has_pos = t_end == ctx && ctx > 0;
+  const int kb = at.bs * HD * 2, cap = attn_stage_blocks(ring.slot_bytes, at.bs, HD);
+  if (tid < G) {
+    sm.m[tid] = -INFINITY;
+    sm.l[tid] = 0.f;
+  }
+  if (!tagged_inputs<G, HD, kPCT, ConsSync>(at, g, has_pos, sm, sc.tag, pa.abort)) return false;
+  float o[NO];
+#pragma unroll
+  for (int j = 0; j < NO; ++j) o[j] = 0.f;
+  const uint32_t qa = smem_u32(sm.q), sa = smem_u32(&sm.s[0][0]);
+  bool ok = true;
+  for (int cb = b0; cb < b1; cb += cap, ++s_global) {
+    const int slot = s_global % ring.nst, k = s_global / ring.nst;
+    if (ok && !mbar_wait(&ring.full[slot], k & 1)) {
+      ok = false;
+      atomicExch(pa.abort, 1);
+      latch_error(pa.err, ERR_TIMEOUT);
+    }
+    const uint32_t kbase = smem_u32(ring.w) + (uint32_t)slot * ring.slot_bytes;
+    const uint32_t vbase = kbase + (uint32_t)(cap * kb);
+    const int t0 = cb * at.bs, ntok = min(min(cb + cap, b1) * at.bs, t_end) - t0;
+    if (ok) {
+      // the current token's k and v replace what the stage holds at its slot
+      if (has_pos && pos >= t0 && pos < t0 + ntok) {
+        const uint32_t off = (uint32_t)(pos - t0) * (HD * 2);
+        if (tid < HD) sts16(kbase + off + tid * 2, (uint16_t)(__float_as_uint(sm.kn[tid]) >> 16));
+        else if (tid < 2 * HD) sts16(vbase + off + (tid - HD) * 2, (uint16_t)(__float_as_uint(sm.vn[tid - HD]) >> 16));
+        ConsSync::sync();
+      }
+      // (1) scores
+      for (int p = tid; p < G * ntok; p += kPCT) {
+        const int h = p / ntok, t = p - h * ntok;
+        const uint32_t krow = kbase + (uint32_t)t * (HD * 2), qrow = qa + (uint32_t)h * (HD * 4);
+        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+        for (int c0 = 0; c0 < NCH; ++c0) {
+          const int c = (c0 + lane) % NCH;
+          const uint4 kw = lds128(krow + c * 16);
+          const float4 qa0 = lds128f(qrow + c * 32), qa1 = lds128f(qrow + c * 32 + 16);
+          d0 = fmaf(qa0.x, __uint_as_float(kw.x << 16), d0);
+          d1 = fmaf(qa0.y, __uint_as_float(kw.x & 0xffff0000u), d1);
+          d2 = fmaf(qa0.z, __uint_as_float(kw.y << 16), d2);
+          d3 = fmaf(qa0.w, __uint_as_float(kw.y & 0xffff0000u), d3);
+          d0 = fmaf(qa1.x, __uint_as_float(kw.z << 16), d0);
+          d1 = fmaf(qa1.y, __uint_as_float(kw.z & 0xffff0000u), d1);
+          d2 = fmaf(qa1.z, __uint_as_float(kw.w << 16), d2);
+          d3 = fmaf(qa1.w, __uint_as_float(kw.w & 0xffff0000u), d3);
+        }
+        sm.s[h][t] = ((d0 + d1) + (d2 + d3)) * at.scale;
+      }
+      ConsSync::sync();
+      // (2) softmax statistics, one warp per head
+      if (warp < G) {
+        const int h = warp;
+        float mx = -INFINITY;
+        for (int t = lane; t < ntok; t += 32) mx = fmaxf(mx, sm.s[h][t]);
+        mx = warp_max(mx);
+        const float m_old = sm.m[h], m_new = fmaxf(m_old, mx);
+        float sum = 0.f;
+        const int npad = (ntok + 3) & ~3;
+        for (int t = lane; t < npad; t += 32) {
+          const float pr = (t < ntok) ? expf(sm.s[h][t] - m_new) : 0.f;
+          sm.s[h][t] = pr;
+          sum += pr;
+        }
+        sum = warp_sum(sum);
+        if (lane == 0) {
+          const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+          sm.corr[h] = c;
+          sm.l[h] = sm.l[h] * c + sum;
+          sm.m[h] = m_new;
+        }
+      }
+      ConsSync::sync();
+      // (3) outputs
+#pragma unroll
+      for (int j = 0; j < NO; ++j) {
+        const int i = tid + j * kPCT;
+        if (i < G * HD) {
+          const int h = i / HD, d = i % HD;
+          float acc = o[j] * sm.corr[h];
+          const uint32_t prow = sa + (uint32_t)h * (kChunkTok * 4), vcol = vbase + d * 2;
+          for (int t = 0; t < ntok; t += 4) {
+            const float4 p4 = lds128f(prow + t * 4);
+            const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int tt = min(t + u, ntok - 1);  // past the chunk the probability is 0
+              acc = fmaf(pv[u], __uint_as_float(lds16(vcol + (uint32_t)tt * (HD * 2)) << 16), acc);
+            }
+          }
+          o[j] = acc;
+        }
+      }
+    }
+    fence_proxy_async_smem();  // the patch above was a generic write into a bulk-copy slot
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ring.empty[slot]);
+    ConsSync::sync();  // the next stage rewrites sm.s
+  }
+  if (!ConsSync::all(ok)) return false;
+  if (nsplit == 1) {
+#pragma unroll
+    for (int j = 0; j < NO; ++j) {
+      const int i = tid + j * kPCT;
+      if (i < G * HD) {
+        const float L = sm.l[i / HD];
+        st_tagged(at.out_t + (int64_t)(g * G) * HD + i, (L > 0.f) ? o[j] / L : 0.f, sc.tag);
+      }
+    }
+    ConsSync::sync();  // the scratch is reused by the next item
+    return true;
+  }
+  float *part = at.ws_part + ((int64_t)g * at.n_splits + sp) * (G * (2 + HD));
+#pragma unroll
+  for (int j = 0; j < NO; ++j) {
+    const int i = tid + j * kPCT;
+    if (i < G * HD) {
+      const int h = i / HD;
+      part[2 * G + i] = o[j];
+      if (i % HD == 0) {
+        part[h] = sm.m[h];
+        part[G + h] = sm.l[h];
+      }
+    }
+  }
+  attn_merge_splits<G, HD, kPCT, ConsSync, true>(at, g, nsplit, sm.last, sc.tag);
+  return true;
+}
+
+template <int G, int HD>
+__device__ bool attn_phase(const AttnArgs &at, const Ring &ring, int &s_global, float *scratch, const StepConst &sc,
+                           const PersistArgs &pa) {
+  auto &sm = *reinterpret_cast<RingAttnSmem<G, HD> *>(scratch);
+  const int ctx = sc.ctx;
+  const int nblk = (ctx + at.bs - 1) / at.bs;
   const int nsplit = attn_nsplit(nblk, at.n_splits, attn_blocks_per_split<HD, kPW>(at.bs));
   const int items = at.Hkv * nsplit;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    if (!attn_split<G, HD, kPW, ConsSync, true>(at, it / nsplit, it % nsplit, nsplit, ctx, bt, pre, sm, sc.tag,
-                                                pa.abort)) {
+    if (!attn_ring_item<G, HD>(at, it / nsplit, it % nsplit, nsplit, ctx, ring, s_global, sm, sc, pa)) {
       give_up(pa);
       return false;
     }
@@ -394,101 +569,112 @@ __device__ bool attn_phase(const AttnArgs &at, float *scratch, const StepConst &
 
 // ---------------------------------------------------------------------- producer
 //
-// Walks the stages of every GEMV phase in order and copies each into the next free
-// ring slot; entering a layer's QKV phase it also prefetches that layer's K/V blocks
-// (this CTA's share) into L2 for the attention phase.  Measured on GB300 and not kept:
-// prefetching weights into L2 ahead of the ring halved the streaming rate, and capping
-// the bytes in flight per CTA slowed streaming without shortening the consumers'
-// load latencies.
+// Walks the stages of every phase in order and copies each into the next free ring
+// slot: a GEMV stage is RPS whole weight rows (plus their Q4_0 scales); an attention
+// stage is the K and V of up to `cap` consecutive context blocks of one KV head, for
+// the attention items this CTA runs.  Neither depends on the step's activations, so
+// the K/V of old positions are in shared memory before the attention phase starts;
+// only the current token's k/v (and q) arrive as tagged words.  Measured on GB300 and
+// not kept: prefetching weights into L2 ahead of the ring halved the streaming rate,
+// and capping the bytes in flight per CTA slowed streaming without shortening the
+// consumers' load latencies.
 
-
+template <int HD>
 struct StageCursor {
   const PersistArgs *a;
-  int p = 0, st = 0;  // phase, stage within the phase
-  RowRange rr;
+  const StepConst *sc;
+  int ctx = 0;  // the step's attention context, clamped like the consumers clamp it
+  int p = -1, kind = PH_GEMV;
   bool done = false;
-  // fields of the current phase, held in registers: the issue loop touches no memory
-  const uint8_t *w = nullptr, *sc = nullptr;
+  // GEMV phase, held in registers: the issue loop touches no memory
+  RowRange rr;
+  int st = 0;
+  const uint8_t *w = nullptr, *s = nullptr;
   int64_t row_bytes = 0;
   int s_stride = 0;
-  bool q4 = false, qkv = false;
-  uint16_t *kv_layer = nullptr;
+  bool q4 = false;
+  // attention phase
+  const uint8_t *kbase = nullptr, *vbase = nullptr;
+  int64_t blk_bytes = 0;  // bytes between consecutive pool blocks
+  const int32_t *bt = nullptr;
+  int n_pool = 0, bs = 0, kb = 0, cap = 0, nblk = 0, nsplit = 1, items = 0, it = 0, cb = 0, b1 = 0;
+  int64_t hoff = 0;
 
-  __device__ void settle() {  // move to the next existing stage
-    while (p < a->n_phases) {
-      const Phase &ph = a->ph[p];
-      if (ph.kind == PH_GEMV) {
-        const DevMat m = ph.g.m;
-        rr = row_range(m, ph.epi);
-        if (st < rr.n_stages) {
-          w = m.w;
-          sc = reinterpret_cast<const uint8_t *>(m.s);
-          row_bytes = m.row_bytes;
-          s_stride = m.s_stride;
-          q4 = m.fmt == MIE_FMT_Q4_0;
-          qkv = ph.epi == EPI_QKV;
-          kv_layer = ph.g.kv_layer;
-          return;
-        }
+  __device__ bool next_item() {  // this CTA's next attention item with blocks
+    for (it += gridDim.x; it < items; it += gridDim.x) {
+      const int g = it / nsplit, sp = it % nsplit;
+      const int b0 = (int)((int64_t)sp * nblk / nsplit);
+      b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
+      if (b0 < b1) {
+        cb = b0;
+        hoff = (int64_t)g * bs * HD * 2;
+        return true;
       }
-      ++p;
-      st = 0;
     }
+    return false;
+  }
+  __device__ bool enter(int q) {  // phase q has stages for this CTA
+    const Phase &ph = a->ph[q];
+    kind = ph.kind;
+    if (ph.kind == PH_GEMV) {
+      const DevMat m = ph.g.m;
+      rr = row_range(m, ph.epi);
+      st = 0;
+      w = m.w;
+      s = reinterpret_cast<const uint8_t *>(m.s);
+      row_bytes = m.row_bytes;
+      s_stride = m.s_stride;
+      q4 = m.fmt == MIE_FMT_Q4_0;
+      return rr.n_stages > 0;
+    }
+    const AttnArgs &at = ph.at;
+    kbase = reinterpret_cast<const uint8_t *>(at.k);
+    vbase = reinterpret_cast<const uint8_t *>(at.v);
+    blk_bytes = at.block_stride * 2;
+    n_pool = at.n_pool_blocks;
+    bs = at.bs;
+    kb = bs * HD * 2;
+    cap = attn_stage_blocks(a->slot_bytes, bs, HD);
+    nblk = (ctx + bs - 1) / bs;
+    nsplit = attn_nsplit(nblk, at.n_splits, attn_blocks_per_split<HD, kPW>(bs));
+    items = at.Hkv * nsplit;
+    it = (int)blockIdx.x - (int)gridDim.x;
+    return next_item();
+  }
+  __device__ void advance() {
+    while (++p < a->n_phases)
+      if (enter(p)) return;
     done = true;
   }
   __device__ void next() {
-    if (++st >= rr.n_stages) {
-      ++p;
-      st = 0;
-      settle();
+    if (kind == PH_GEMV) {
+      if (++st >= rr.n_stages) advance();
+    } else {
+      cb += cap;
+      if (cb >= b1 && !next_item()) advance();
     }
   }
   __device__ int first_row() const { return rr.row0 + st * rr.RPS; }
   __device__ int rows() const { return min(rr.RPS, rr.row1 - first_row()); }
-  __device__ uint32_t w_bytes() const { return (uint32_t)(rows() * row_bytes); }
-  __device__ uint32_t s_bytes() const { return q4 ? (uint32_t)(rows() * s_stride * 2) : 0u; }
 };
 
-// The K/V blocks of this CTA's share of the context, read once at kernel start so that
-// the per-layer L2 prefetch issues no dependent loads.
-constexpr int kKvPrefetchMax = 8;
-struct KvShare {
-  int n = 0;
-  int blk[kKvPrefetchMax];
-  int64_t block_stride = 0;
-  uint32_t bytes = 0;  // K and V of one layer in one block
-
-  __device__ void load(const GemvArgs &g) {
-    const StepParams *sp = g.sp;
-    const int ctx = sp->pos[g.slot] + 1;
-    const int nblk = min((max(ctx, 0) + g.bs - 1) / g.bs, sp->max_blocks);
-    block_stride = g.block_stride;
-    bytes = 2u * (uint32_t)g.Hkv * g.bs * g.hd * 2;
-    for (int i = blockIdx.x; i < nblk && n < kKvPrefetchMax; i += gridDim.x) {
-      const int b = sp->block_table[(int64_t)g.slot * sp->max_blocks + i];
-      if (b >= 0 && b < g.n_kv_blocks) blk[n++] = b;
-    }
-  }
-  __device__ void prefetch(const uint16_t *kv_layer) const {
-    for (int j = 0; j < n; ++j) prefetch_l2(kv_layer + (int64_t)blk[j] * block_stride, bytes);
-  }
-};
-
-__device__ void produce(const PersistArgs &a, const Ring &ring, volatile int &s_issued, volatile int &s_prod_done) {
+template <int HD>
+__device__ void produce(const PersistArgs &a, const Ring &ring, const StepConst &sc, volatile int &s_sc_ready,
+                        volatile int &s_issued, volatile int &s_prod_done) {
   const uint64_t pol = evict_first_policy();
-  KvShare kv;
-  kv.load(a.ph[0].g);
-  StageCursor ld;
+  StageCursor<HD> ld;
   ld.a = &a;
-  ld.settle();
+  ld.sc = &sc;
+  {
+    const GemvArgs &g0 = a.ph[0].g;
+    const StepParams *sp = g0.sp;
+    ld.ctx = attn_ctx(sp->pos[g0.slot], sp->max_blocks, g0.bs);
+    ld.bt = sp->block_table + (int64_t)g0.slot * sp->max_blocks;
+  }
+  ld.advance();
   int s_global = 0;
-  int last_kv_phase = -1;
+  bool sc_ready = false;
   while (!ld.done) {
-    // a layer's K/V blocks go to L2 when the ring reaches its QKV phase
-    if (ld.qkv && ld.p != last_kv_phase) {
-      kv.prefetch(ld.kv_layer);
-      last_kv_phase = ld.p;
-    }
     const int slot = s_global % a.n_slots, k = s_global / a.n_slots;
     if (k > 0 && !mbar_wait(&ring.empty[slot], (k - 1) & 1)) {
       atomicExch(a.abort, 1);
@@ -496,13 +682,36 @@ __device__ void produce(const PersistArgs &a, const Ring &ring, volatile int &s_
       break;
     }
     if (ld_volatile(a.abort)) break;
-    const int r = ld.first_row();
-    const uint32_t wb = ld.w_bytes(), sb = ld.s_bytes();
-    mbar_expect_tx(&ring.full[slot], wb + sb);
-    bulk_load(ring.w + (size_t)slot * a.slot_bytes, ld.w + (int64_t)r * ld.row_bytes, wb, &ring.full[slot], pol);
-    if (sb)
-      bulk_load(ring.sc + (size_t)slot * a.slot_sc_bytes, ld.sc + (int64_t)r * ld.s_stride * 2, sb, &ring.full[slot],
-                pol);
+    uint8_t *dst = ring.w + (size_t)slot * a.slot_bytes;
+    if (ld.kind == PH_GEMV) {
+      const int r = ld.first_row();
+      const uint32_t wb = (uint32_t)(ld.rows() * ld.row_bytes);
+      const uint32_t sb = ld.q4 ? (uint32_t)(ld.rows() * ld.s_stride * 2) : 0u;
+      mbar_expect_tx(&ring.full[slot], wb + sb);
+      bulk_load(dst, ld.w + (int64_t)r * ld.row_bytes, wb, &ring.full[slot], pol);
+      if (sb)
+        bulk_load(ring.sc + (size_t)slot * a.slot_sc_bytes, ld.s + (int64_t)r * ld.s_stride * 2, sb, &ring.full[slot],
+                  pol);
+    } else {
+      if (!sc_ready) {  // the block ids are staged in shared memory by the consumers
+        for (long it = 0; it < kWaitPolls && !s_sc_ready; ++it) __nanosleep(64);
+        __threadfence_block();
+        sc_ready = true;
+      }
+      const int nb = min(ld.cap, ld.b1 - ld.cb);
+      mbar_expect_tx(&ring.full[slot], 2u * nb * ld.kb);
+      for (int j = 0; j < nb; ++j) {
+        const int b = ld.cb + j;
+        int blk = (b < sc.nblk_staged && s_sc_ready) ? sc.blk[b] : ld.bt[b];
+        if (blk < 0 || blk >= ld.n_pool) {
+          latch_error(a.err, ERR_BLOCK_ID);
+          blk = 0;
+        }
+        const int64_t off = (int64_t)blk * ld.blk_bytes + ld.hoff;
+        bulk_load(dst + (size_t)j * ld.kb, ld.kbase + off, ld.kb, &ring.full[slot], pol);
+        bulk_load(dst + (size_t)(ld.cap + j) * ld.kb, ld.vbase + off, ld.kb, &ring.full[slot], pol);
+      }
+    }
     ++s_global;
     s_issued = s_global;
     ld.next();
@@ -521,7 +730,7 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
   // descriptors of the current and the next phase, in shared memory; the one after
   // is loaded into registers while the current phase runs
   __shared__ __align__(16) Phase s_ph[2];
-  __shared__ volatile int s_issued, s_prod_done;
+  __shared__ volatile int s_issued, s_prod_done, s_sc_ready;
   constexpr int kPhWords = sizeof(Phase) / 4;
   static_assert(sizeof(Phase) % 4 == 0 && kPhWords <= kPCT, "one descriptor word per consumer thread");
 
@@ -543,12 +752,13 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
     }
     s_issued = 0;
     s_prod_done = 0;
+    s_sc_ready = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
   if (warp == kPW) {
-    if (lane == 0) produce(a, ring, s_issued, s_prod_done);
+    if (lane == 0) produce<HD>(a, ring, sc, s_sc_ready, s_issued, s_prod_done);
     return;
   }
 
@@ -558,9 +768,9 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
     const StepParams *sp = g0.sp;
     const int pos = sp->pos[g0.slot];
     int tok = sp->token[g0.slot];
-    const int ctx = pos + 1;
     const int n_table = sp->max_blocks;
-    const int nblk = min((max(ctx, 0) + g0.bs - 1) / g0.bs, n_table);
+    const int ctx = attn_ctx(pos, n_table, g0.bs);
+    const int nblk = (ctx + g0.bs - 1) / g0.bs;
     const int staged = nblk <= kStepMaxBlocks ? nblk : 0;
     const int32_t *bt = sp->block_table + (int64_t)g0.slot * n_table;
     int ids[kStepMaxBlocks / kPCT];
@@ -589,10 +799,13 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
         latch_error(a.err, ERR_TOKEN);
         tok = 0;
       }
+      if (ctx != pos + 1) latch_error(a.err, ERR_POS);
       sc.tag = __ldcg(a.epoch);
       sc.tok = tok;
       sc.pos = pos;
       sc.ctx = ctx;
+      sc.n_table = n_table;
+      sc.bt = bt;
       sc.nblk_staged = staged;
     }
   }
@@ -600,6 +813,10 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
   for (int p = 0; p < 2 && p < a.n_phases; ++p)
     if (tid < kPhWords) reinterpret_cast<uint32_t *>(&s_ph[p])[tid] = __ldcg(ph_words + (size_t)p * kPhWords + tid);
   ConsSync::sync();
+  if (tid == 0) {  // the step constants are complete: the producer may read the block ids
+    __threadfence_block();
+    s_sc_ready = 1;
+  }
   int s_global = 0;
   bool ok = true;
   for (int p = 0; p < a.n_phases; ++p) {
@@ -613,7 +830,7 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
     } else {
       stamp(a.trace, p, 1);
       stamp(a.trace, p, 2);
-      ok = attn_phase<G, HD>(ph.at, scratch, sc, a);
+      ok = attn_phase<G, HD>(ph.at, ring, s_global, scratch, sc, a);
       stamp(a.trace, p, 3);
     }
     ConsSync::sync();
@@ -665,9 +882,9 @@ static const void *pick_kernel(int fl, int fh, int G, int HD) {
 
 size_t persist_attn_smem(int G, int HD) {
   switch (G * 1000 + HD) {
-    case 4032: return sizeof(AttnSmem<4, 32, kPW>);
-    case 8064: return sizeof(AttnSmem<8, 64, kPW>);
-    case 4064: return sizeof(AttnSmem<4, 64, kPW>);
+    case 4032: return sizeof(RingAttnSmem<4, 32>);
+    case 8064: return sizeof(RingAttnSmem<8, 64>);
+    case 4064: return sizeof(RingAttnSmem<4, 64>);
   }
   return 0;
 }
@@ -679,7 +896,11 @@ mie_status persist_plan(const Phase *host_phases, int n, int G, int HD, PersistP
   int fl = -1, fh = -1;
   for (int p = 0; p < n; ++p) {
     const Phase &ph = host_phases[p];
-    if (ph.kind != PH_GEMV) continue;
+    if (ph.kind != PH_GEMV) {  // an attention stage holds the K and V of at least one block
+      const uint32_t kv = (uint32_t)(2 * ph.at.bs * HD * 2 + 127) / 128 * 128;
+      if (kv > slot) slot = kv;
+      continue;
+    }
     const DevMat &m = ph.g.m;
     if (fl < 0) fl = m.fmt;
     else if (m.fmt != fl && fh < 0) fh = m.fmt;
