@@ -267,14 +267,16 @@ mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int32_t *token
                                  const int32_t *pos, const int32_t *block_tables, int max_blocks,
                                  float *logits_out, int32_t *argmax_out);
 
-/* How mie_decode_step runs the step.  MIE_STEP_CHAIN (the default): one kernel per
- * phase with programmatic dependent launch.  MIE_STEP_PERSISTENT: one cooperative
- * kernel of one CTA per SM runs every phase; its producer warps stream all weights
- * through shared-memory rings while consumer warps meet at bounded grid barriers
- * between phases.  Either is captured in a CUDA graph.  The persistent kernel covers
- * group/head-dim shapes (4, 32), (8, 64), (4, 64) and the format pairs (layers, head)
- * bf16/bf16, i8/i8, q4_0/q4_0, q4_0/i8; selecting it for another shape returns
- * MIE_E_SHAPE and keeps the chain. */
+/* How mie_decode_step runs the step.  MIE_STEP_PERSISTENT (the default where the shape
+ * is covered): one cooperative kernel of one CTA per SM runs every phase; its producer
+ * warps stream all weights and the K/V of old positions through shared-memory rings,
+ * and consumer warps pass each phase's output vector to the next as tagged words
+ * (value + launch tag), polled with bounded waits instead of grid barriers.
+ * MIE_STEP_CHAIN: one kernel per phase with programmatic dependent launch.  Either is
+ * captured in a CUDA graph.  The persistent kernel covers group/head-dim shapes
+ * (4, 32), (8, 64), (4, 64) and the format pairs (layers, head) bf16/bf16, i8/i8,
+ * q4_0/q4_0, q4_0/i8; selecting it for another shape returns MIE_E_SHAPE and keeps the
+ * chain, and a context created for such a shape runs the chain from its first step. */
 enum { MIE_STEP_PERSISTENT = 0, MIE_STEP_CHAIN = 1 };
 mie_status mie_set_step_mode(mie_ctx *ctx, int mode);
 int mie_step_mode(const mie_ctx *ctx);
@@ -282,14 +284,15 @@ int mie_step_mode(const mie_ctx *ctx);
 /* Timeline of the persistent step (tracing).  device_buffer: device memory of at least
  * n_phases * n_ctas * 5 * 8 bytes (NULL switches tracing off); every later step
  * overwrites it.  Entry [phase][cta][point] is the GPU's global timer in ns when CTA
- * `cta` reached point 0 = phase entry, 1 = grid barrier passed, 2 = input vector
- * staged, 3 = weight stages consumed, 4 = outputs written.  *n_phases and *n_ctas
+ * `cta` reached point 0 = phase entry, 1 = input words arrived, 2 = input vector
+ * staged (normalised), 3 = ring stages consumed, 4 = outputs written.  *n_phases and *n_ctas
  * (nullable) receive the dimensions.  Takes effect at the next mie_decode_step. */
 mie_status mie_set_trace(mie_ctx *ctx, void *device_buffer, size_t bytes, int *n_phases, int *n_ctas);
 
 /* Synchronises the context's stream, then reads and clears its device error flags:
  * MIE_E_DEVICE when a bounds check fired, MIE_E_TIMEOUT when a bounded device wait of
- * the persistent step gave up (its barrier counters are reset for the next step). */
+ * the persistent step gave up (its counters and tagged words are reset for the next
+ * step). */
 mie_status mie_sync(mie_ctx *ctx);
 
 /* Kernel launches one mie_decode_step replay performs (for launch accounting). */

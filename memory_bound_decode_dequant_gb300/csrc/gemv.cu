@@ -182,32 +182,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
     consumed = s + 1;
     const int r = row0 + s * RPS + ri;
     if (has_slice && r < row1) {
-      const uint8_t *rowp = ring + (size_t)slot * stage_bytes + (size_t)ri * m.row_bytes + (size_t)ks * kSliceBytes;
-      float sum = 0.f;
-      if constexpr (F == MIE_FMT_Q4_0) {
-        const __half *hs = reinterpret_cast<const __half *>(sring + (size_t)slot * sc_bytes) + (size_t)ri * m.s_stride +
-                           ks * (kSlice / 32);
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          if (e0 + c * kChunkStride < Kp) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(rowp + (size_t)(c * 32 + lane) * 16);
-            float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            chunk_fma<F>(w, xr + c * (EPC / 2), acc);
-            const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-            sum = fmaf(__half2float(hs[c * 32 + lane]), cs, sum);
-          }
-        }
-      } else {
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) {
-          if (e0 + c * kChunkStride < Kp) {
-            const uint4 w = *reinterpret_cast<const uint4 *>(rowp + (size_t)(c * 32 + lane) * 16);
-            chunk_fma<F>(w, xr + c * (EPC / 2), acc);
-          }
-        }
-        sum = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-      }
+      const uint32_t rowa = smem_u32(ring) + (uint32_t)slot * stage_bytes + (uint32_t)(ri * m.row_bytes) +
+                            (uint32_t)ks * kSliceBytes;
+      const uint32_t sca = smem_u32(sring) + (uint32_t)slot * sc_bytes + (uint32_t)(ri * m.s_stride + ks * (kSlice / 32)) * 2;
+      float sum = stage_row_dot<F>(rowa, sca, xr, e0, Kp, lane);
       sum = warp_sum(sum);
       if (lane == 0) part[(r - row0) * KS + ks] = sum;
     }

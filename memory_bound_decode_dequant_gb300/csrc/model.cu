@@ -112,7 +112,7 @@ struct mie_ctx {
   bool primed = false;
   mie_pool *pool = nullptr;
   // persistent step
-  int mode = MIE_STEP_CHAIN;
+  int mode = MIE_STEP_PERSISTENT;  // prepare_step falls back to the chain for other shapes
   std::vector<Phase> phases;
   Phase *d_phases = nullptr;
   size_t d_phases_cap = 0;

@@ -130,7 +130,8 @@ def test_persistent_and_chain_agree_over_long_context(orc):
     assert np.max(np.abs(res[0] - res[1])) <= 1e-3 * float(np.std(res[1]))
 
 
-def test_device_continuation_matches_host_steps(orc):
+@pytest.mark.parametrize("step_mode", [PERSISTENT, CHAIN])
+def test_device_continuation_matches_host_steps(orc, step_mode):
     """mie_decode_continue (token and position advanced on the device) gives the same
     bits as host-driven steps fed the previous argmax."""
     shape = synth.TINY
@@ -139,7 +140,8 @@ def test_device_continuation_matches_host_steps(orc):
     outs = []
     for mode in ("host", "device"):
         gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
-        assert gm.step_mode == CHAIN
+        assert gm.step_mode == PERSISTENT  # the default where the shape is covered
+        gm.set_step_mode(step_mode)
         logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
         am = torch.empty(1, dtype=torch.int32, device="cuda")
         toks = prompt_tokens(shape, 10)
