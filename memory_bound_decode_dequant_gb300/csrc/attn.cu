@@ -26,10 +26,20 @@ struct CtaSync {
 };
 
 template <int G, int HD>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a) {
+__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a_in) {
   __shared__ AttnSmem<G, HD, kAttnWarps> sm;
   pdl_trigger();
   pdl_wait();
+  AttnArgs a = a_in;
+  if (a_in.slot_z) {  // one grid layer per slot of the few-slot step
+    const int z = blockIdx.z;
+    if (z >= a_in.sp->n_slots) return;
+    a.slot = z;
+    a.q += (int64_t)z * a.Hq * a.hd;
+    a.out += (int64_t)z * a.Hq * a.hd;
+    a.ws_count = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(a.ws_count) + z * a.ws_slot_bytes);
+    a.ws_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.ws_part) + z * a.ws_slot_bytes);
+  }
   const int g = blockIdx.y, s = blockIdx.x;
   int ctx;
   const int32_t *bt;
@@ -77,7 +87,7 @@ int attn_splits_for(int Hkv, int max_ctx, int bs) {
 template <int G, int HD>
 static mie_status launch_attn_t(const AttnArgs &a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(a.n_splits, a.Hkv);
+  cfg.gridDim = dim3(a.n_splits, a.Hkv, a.slot_z ? a.max_slots : 1);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

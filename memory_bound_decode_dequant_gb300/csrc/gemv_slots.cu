@@ -1,0 +1,470 @@
+// gemv_slots.cu -- the weight GEMVs of the few-slot step ("Mini Inference Engine",
+// "Continuous batching": several sequences advance one token per step and share one
+// pass over the weights).
+//
+// Every weight row is read from HBM once per step and multiplied with the input
+// vectors of all n_slots (<= 8) slots on the tensor cores, with mma.sync m16n8k16
+// (bf16 operands, fp32 accumulators) in transposed form:
+//   Y^T[slot][row] = X^T[slot][k] * W^T[k][row]
+//   A = X^T: 16 x 16, rows = slots 0..7 (rows 8..15 are zero), held in registers;
+//   B = W^T: 16 k x 8 weight rows -- the staged rows read as they lie in memory;
+//   C = Y^T: thread (g = lane/4, t = lane%4) holds Y[row 2t, 2t+1][slot g].
+// x is fp32 in the method, so each x value is split into x_hi = bf16(x) and
+// x_lo = bf16(x - x_hi) and every tile takes two MMAs: the products are exact in
+// fp32 and x keeps about 16 significant bits (int8 weights become bf16 exactly).
+//
+// A producer warp streams stages of 8 weight rows x one 2048-column slice through a
+// ring in shared memory (one bulk copy per row into rows padded by 16 bytes, so the
+// B-fragment loads hit 32 distinct banks); the 8 consumer warps each own 16 of the
+// slice's 128 k-steps and keep their x fragments in registers for the whole slice.
+// Warp partials are summed in a fixed order, so results do not depend on timing.
+#include "device.cuh"
+
+namespace mie {
+
+constexpr int kSW = 8;               // consumer warps
+constexpr int kSCT = 32 * kSW;       // consumer threads
+constexpr int kST = kSCT + 32;       // + one producer warp
+constexpr int kSRows = 8;            // weight rows per stage (the MMA's N)
+constexpr int kSSlice = 2048;        // columns per stage
+constexpr int kSKSteps = kSSlice / 16 / kSW;  // k-steps per warp per slice (16)
+constexpr int kSMaxNst = 8;
+constexpr int kSMaxAccTiles = 64;    // tiles per CTA whose partial sums persist across slices
+
+struct SSync {
+  __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSCT) : "memory"); }
+  // barrier that also returns whether v holds on any consumer thread
+  __device__ static bool any(bool v) {
+    int r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.s32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n selp.s32 %0, 1, 0, q;\n}"
+        : "=r"(r)
+        : "r"((int)v), "n"(kSCT)
+        : "memory");
+    return r != 0;
+  }
+};
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+  return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+         ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+}
+
+// hi / lo bf16 pairs of two fp32 values
+__device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_t &lo) {
+  const float h0 = __bfloat162float(__float2bfloat16_rn(v0)), h1 = __bfloat162float(__float2bfloat16_rn(v1));
+  hi = bf16x2_bits(h0, h1);
+  lo = bf16x2_bits(v0 - h0, v1 - h1);
+}
+
+// B fragment word: weights (row, k) and (row, k + 1) of a staged row as a bf16 pair.
+template <int F>
+__device__ __forceinline__ uint32_t b_word(uint32_t addr);
+template <>
+__device__ __forceinline__ uint32_t b_word<MIE_FMT_BF16>(uint32_t addr) {
+  return lds32(addr);
+}
+template <>
+__device__ __forceinline__ uint32_t b_word<MIE_FMT_I8>(uint32_t addr) {
+  const uint32_t v = lds16(addr);
+  const int q0 = (int)(int8_t)(v & 0xffu), q1 = (int)(int8_t)(v >> 8);
+  return bf16x2_bits((float)q0, (float)q1);  // exact: |q| <= 127
+}
+
+// Shared state of one CTA.
+struct SlotShared {
+  float ss[kSW][kMaxSlots];            // per-warp sums of squares (RMSNorm)
+  float rs[kMaxSlots];                 // RMSNorm scale per slot
+  float red[2][kSW][kMaxSlots][kSRows];  // warp partials of a stage (double-buffered)
+  float acc[kSMaxAccTiles][kMaxSlots][kSRows];  // partial sums across slices
+  int pos[kMaxSlots], blk[kMaxSlots], tok[kMaxSlots];
+  bool pos_ok[kMaxSlots], blk_ok[kMaxSlots];
+  float bv[2][kMaxSlots];
+  int bi[2][kMaxSlots];
+  unsigned last;
+};
+
+struct SlotPlan {
+  int nst = 0;
+  uint32_t pitch = 0, stage_bytes = 0;  // padded row bytes in shared memory, bytes per slot
+  int n_tiles = 0, KS = 1;
+  size_t smem = 0;
+};
+
+template <int F, int PRO, int EPI>
+__global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, const SlotPlan pl) {
+  constexpr int ES = (F == MIE_FMT_BF16) ? 2 : 1;  // bytes per weight
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kSMaxNst], empty_bar[kSMaxNst];
+  __shared__ SlotShared sh;
+  __shared__ volatile int s_issued, s_prod_done, s_abort;
+
+  const DevMat &m = a.m;
+  const int M = m.rows, K = m.cols, Kp = m.kp;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tt0 = (int)((int64_t)blockIdx.x * pl.n_tiles / gridDim.x);
+  const int tt1 = (int)((int64_t)(blockIdx.x + 1) * pl.n_tiles / gridDim.x);
+  const int n_my = tt1 - tt0;
+  const int n_stages = n_my * pl.KS;
+  const int S = a.sp->n_slots;
+
+  if (tid == 0) {
+    for (int i = 0; i < pl.nst; ++i) {
+      mbar_init(&full_bar[i], 1);
+      mbar_init(&empty_bar[i], kSW);
+    }
+    s_issued = 0;
+    s_prod_done = 0;
+    s_abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_trigger();
+
+  if (warp == kSW) {  // producer: weights do not depend on earlier kernels
+    if (lane == 0) {
+      const uint64_t pol = evict_first_policy();
+      for (int s = 0; s < n_stages; ++s) {
+        const int slot = s % pl.nst, k = s / pl.nst;
+        if (k > 0 && !mbar_wait(&empty_bar[slot], (k - 1) & 1)) {
+          s_abort = 1;
+          latch_error(a.err, ERR_TIMEOUT);
+          break;
+        }
+        if (s_abort) break;
+        const int q = s / n_my, r0 = (tt0 + s % n_my) * kSRows;
+        const int rows = min(kSRows, M - r0);
+        const uint32_t cb = (uint32_t)(min(kSSlice, Kp - q * kSSlice) * ES);
+        mbar_expect_tx(&full_bar[slot], rows * cb);
+        uint8_t *dst = smem + (size_t)slot * pl.stage_bytes;
+        for (int j = 0; j < rows; ++j)
+          bulk_load(dst + (size_t)j * pl.pitch, m.w + (int64_t)(r0 + j) * m.row_bytes + (int64_t)q * kSSlice * ES, cb,
+                    &full_bar[slot], pol);
+        s_issued = s + 1;
+      }
+      s_prod_done = 1;
+    }
+    return;
+  }
+
+  pdl_wait();
+  const int g = lane >> 2, t = lane & 3;
+
+  // per-slot constants of the epilogue
+  if (tid < kMaxSlots) {
+    const int s = tid;
+    int tok = 0, pos = 0, blk = -1;
+    bool pos_ok = false, blk_ok = false;
+    if (s < S) {
+      tok = a.sp->token[s];
+      if (tok < 0 || tok >= a.vocab) {
+        if (PRO == PRO_EMBED_NORM) latch_error(a.err, ERR_TOKEN);
+        tok = 0;
+      }
+      if constexpr (EPI == EPI_QKV) {
+        pos = a.sp->pos[s];
+        pos_ok = pos >= 0 && pos < a.max_pos && pos / a.bs < a.sp->max_blocks;
+        blk = a.sp->block_table[(int64_t)s * a.sp->max_blocks + (pos_ok ? pos / a.bs : 0)];
+        blk_ok = pos_ok && blk >= 0 && blk < a.n_kv_blocks;
+        if (!blk_ok) latch_error(a.err, pos_ok ? ERR_BLOCK_ID : ERR_POS);
+      }
+    }
+    sh.tok[s] = tok;
+    sh.pos[s] = pos;
+    sh.blk[s] = blk;
+    sh.pos_ok[s] = pos_ok;
+    sh.blk_ok[s] = blk_ok;
+  }
+  SSync::sync();
+
+  // A fragments of slice q: x of slot g at columns kk + 2t (+1) and kk + 2t + 8 (+9)
+  // of this warp's k-steps, as hi / lo bf16 pairs.
+  uint32_t ah0[kSKSteps], ah2[kSKSteps], al0[kSKSteps], al2[kSKSteps];
+  auto x_at = [&](int e) -> float {
+    if (g >= S || e >= K) return 0.f;
+    if (PRO == PRO_EMBED_NORM) return embed_at(a.embed, sh.tok[g], e);
+    return __ldcg(a.x + (int64_t)g * K + e);
+  };
+  auto load_slice = [&](int q) {
+    // RMSNorm over the whole vector: the prologues that normalise have K <= kSSlice
+    float rn = 1.f;
+    if (PRO != PRO_PLAIN) {
+      float ss = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < kSKSteps; ++j) {
+        const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
+        const float v[4] = {x_at(kk), x_at(kk + 1), x_at(kk + 8), x_at(kk + 9)};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) ss += v[u] * v[u];
+      }
+      ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+      ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+      if (t == 0) sh.ss[warp][g] = ss;
+      SSync::sync();
+      if (tid < kMaxSlots) {
+        float tot = 0.f;
+        for (int w = 0; w < kSW; ++w) tot += sh.ss[w][tid];
+        sh.rs[tid] = 1.0f / sqrtf(tot / (float)K + a.eps);
+      }
+      SSync::sync();
+      rn = sh.rs[g];
+    }
+#pragma unroll
+    for (int j = 0; j < kSKSteps; ++j) {
+      const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
+      float v[4] = {x_at(kk), x_at(kk + 1), x_at(kk + 8), x_at(kk + 9)};
+      if (PRO == PRO_EMBED_NORM && blockIdx.x == 0 && g < S) {
+        const int ee[4] = {kk, kk + 1, kk + 8, kk + 9};
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (ee[u] < K) a.x_store[(int64_t)g * K + ee[u]] = v[u];
+      }
+      if (PRO != PRO_PLAIN) {
+        const int ee[4] = {kk, kk + 1, kk + 8, kk + 9};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = (ee[u] < K) ? v[u] * rn * __ldg(a.gain + ee[u]) : 0.f;
+      }
+      if (a.act_bf16) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = round_bf16(v[u]);
+      }
+      split2(v[0], v[1], ah0[j], al0[j]);
+      split2(v[2], v[3], ah2[j], al2[j]);
+    }
+  };
+
+  // epilogue state: thread i < 64 owns (slot i / 8, row i % 8) of every tile
+  const int es = tid >> 3, er = tid & 7;
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  auto epilogue = [&](int r0, float v) {  // v = Y[r0 + er][es] (tid < 64)
+    const int r = r0 + er;
+    if (F == MIE_FMT_I8 && r < M) v *= reinterpret_cast<const float *>(m.s)[r];
+    if constexpr (EPI == EPI_STORE) {
+      if (es < S && r < M) a.y[(int64_t)es * M + r] = v;
+    } else if constexpr (EPI == EPI_RESID) {
+      if (es < S && r < M) a.y[(int64_t)es * M + r] += v;
+    } else if constexpr (EPI == EPI_SWIGLU) {
+      const float up = __shfl_down_sync(0xffffffffu, v, 1);  // row r + 1 of the same slot
+      if (es < S && (er & 1) == 0 && r + 1 < M) a.y[(int64_t)es * (M / 2) + r / 2] = v / (1.0f + expf(-v)) * up;
+    } else if constexpr (EPI == EPI_QKV) {
+      const float x1 = __shfl_down_sync(0xffffffffu, v, 1);
+      if (es < S && (er & 1) == 0 && r + 1 < M) {
+        const int h2 = a.hd / 2, u = r / 2;
+        const int h = u / h2, i = u % h2;
+        float x0 = v, y1 = x1;
+        if (h < a.Hq + a.Hkv && sh.pos_ok[es]) {
+          const float c = a.rope_cos[(int64_t)sh.pos[es] * h2 + i], sn = a.rope_sin[(int64_t)sh.pos[es] * h2 + i];
+          const float r0v = x0 * c - y1 * sn, r1v = y1 * c + x0 * sn;
+          x0 = r0v;
+          y1 = r1v;
+        }
+        if (h < a.Hq) {
+          float *qo = a.q_out + (int64_t)es * a.Hq * a.hd + h * a.hd;
+          qo[i] = x0;
+          qo[i + h2] = y1;
+        } else if (sh.blk_ok[es]) {
+          const int isv = h >= a.Hq + a.Hkv;
+          const int gh = h - a.Hq - (isv ? a.Hkv : 0);
+          uint16_t *dst = a.kv_layer + (int64_t)sh.blk[es] * a.block_stride + (int64_t)isv * a.Hkv * a.bs * a.hd +
+                          ((int64_t)gh * a.bs + sh.pos[es] % a.bs) * a.hd;
+          dst[i] = __bfloat16_as_ushort(__float2bfloat16_rn(x0));
+          dst[i + h2] = __bfloat16_as_ushort(__float2bfloat16_rn(y1));
+        }
+      }
+    } else if constexpr (EPI == EPI_ARGMAX) {
+      if (es < S && r < M) {
+        if (a.sp->logits_out) a.sp->logits_out[(int64_t)es * M + r] = v;
+        if (better(v, r, bv, bi)) { bv = v; bi = r; }
+      }
+    }
+  };
+
+  bool ok = true;
+  int s = 0;
+  const uint32_t ring = smem_u32(smem);
+  for (int q = 0; q < pl.KS; ++q) {
+    load_slice(q);
+    const int nk = min(kSSlice, Kp - q * kSSlice) / 16;  // k-steps of this slice
+    for (int tl = 0; tl < n_my; ++tl, ++s) {
+      const int slot = s % pl.nst, k = s / pl.nst;
+      if (ok && !mbar_wait(&full_bar[slot], k & 1)) {
+        ok = false;
+        s_abort = 1;
+        latch_error(a.err, ERR_TIMEOUT);
+      }
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      if (ok) {
+        const uint32_t base = ring + (uint32_t)slot * pl.stage_bytes + (uint32_t)g * pl.pitch + (uint32_t)(2 * t) * ES;
+#pragma unroll
+        for (int j = 0; j < kSKSteps; ++j) {
+          const int ks = warp + kSW * j;
+          if (ks < nk) {
+            const uint32_t ad = base + (uint32_t)(ks * 16) * ES;
+            const uint32_t b0 = b_word<F>(ad), b1 = b_word<F>(ad + 8 * ES);
+            mma_bf16_16816(c, ah0[j], ah2[j], b0, b1);
+            mma_bf16_16816(c, al0[j], al2[j], b0, b1);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
+      // c[0], c[1] = Y[row 2t, 2t+1][slot g] of this warp's k-steps
+      float (*red)[kMaxSlots][kSRows] = sh.red[s & 1];
+      red[warp][g][2 * t] = c[0];
+      red[warp][g][2 * t + 1] = c[1];
+      SSync::sync();
+      if (tid < kMaxSlots * kSRows) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kSW; ++w) v += red[w][es][er];
+        const bool multi = pl.KS > 1;
+        if (multi && q > 0) v += sh.acc[tl][es][er];
+        if (q + 1 < pl.KS) sh.acc[tl][es][er] = v;
+        else epilogue((tt0 + tl) * kSRows, v);  // warps 0 and 1 whole: the pair shuffles see every lane
+      }
+    }
+  }
+  if (SSync::any(!ok || s_abort)) {
+    if (tid == 0) {
+      for (long it = 0; it < kWaitPolls && !s_prod_done; ++it) __nanosleep(64);
+      const int issued = s_issued;
+      for (int x = max(s, issued - pl.nst); x < issued; ++x) mbar_wait(&full_bar[x % pl.nst], (x / pl.nst) & 1);
+    }
+    return;
+  }
+  if constexpr (EPI == EPI_ARGMAX) {
+    // per slot: best of this CTA over its 8 row lanes, then the last CTA over all CTAs
+    if (tid < kMaxSlots * kSRows) {
+#pragma unroll
+      for (int o = 1; o < kSRows; o <<= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+      }
+      if (er == 0) a.am_part[(int64_t)es * gridDim.x + blockIdx.x] = make_float2(bv, __int_as_float(bi));
+    }
+    __threadfence();
+    SSync::sync();
+    if (tid == 0) sh.last = (atomicAdd(a.am_count, 1u) == gridDim.x - 1);
+    SSync::sync();
+    if (sh.last) {
+      __threadfence();
+      // warp w reduces slot w
+      const int sl = warp;
+      if (sl < S) {
+        float fv = -INFINITY;
+        int fi = 0x7fffffff;
+        for (int b = lane; b < (int)gridDim.x; b += 32) {
+          const float2 p = __ldcg(a.am_part + (int64_t)sl * gridDim.x + b);
+          if (better(p.x, __float_as_int(p.y), fv, fi)) { fv = p.x; fi = __float_as_int(p.y); }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, fv, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, fi, o);
+          if (better(ov, oi, fv, fi)) { fv = ov; fi = oi; }
+        }
+        if (lane == 0) {
+          if (fi == 0x7fffffff) fi = 0;
+          if (a.sp->argmax_out) a.sp->argmax_out[sl] = fi;
+          if (a.sp->advance) {
+            a.sp->token[sl] = fi;
+            a.sp->pos[sl] += 1;
+          }
+        }
+      }
+      SSync::sync();
+      if (tid == 0) *a.am_count = 0u;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------- host side
+
+static SlotPlan slot_plan(const DevMat &m, int grid) {
+  SlotPlan p;
+  const int ES = (m.fmt == MIE_FMT_BF16) ? 2 : 1;
+  p.KS = (m.kp + kSSlice - 1) / kSSlice;
+  const int slice = min(kSSlice, m.kp);
+  p.pitch = (uint32_t)(slice * ES + 16);
+  p.stage_bytes = (uint32_t)((kSRows * p.pitch + 127) / 128 * 128);
+  p.n_tiles = (m.rows + kSRows - 1) / kSRows;
+  int dev = 0, max_smem = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  const long avail = (long)max_smem - (long)sizeof(SlotShared) - 1024;
+  int nst = (int)(avail / (long)p.stage_bytes);
+  p.nst = nst > kSMaxNst ? kSMaxNst : nst;
+  p.smem = (size_t)p.nst * p.stage_bytes;
+  (void)grid;
+  return p;
+}
+
+template <int F, int PRO, int EPI>
+static mie_status launch_slots_t(const GemvArgs &a, const SlotPlan &p, int grid, cudaStream_t st, bool pdl) {
+  auto kern = gemv_slots_kernel<F, PRO, EPI>;
+  MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)p.smem));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kST);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  MIE_CUDA(cudaLaunchKernelEx(&cfg, kern, a, p));
+  return MIE_OK;
+}
+
+template <int F>
+static mie_status launch_slots_f(int pro, int epi, const GemvArgs &a, const SlotPlan &p, int grid, cudaStream_t st,
+                                 bool pdl) {
+#define MIE_S(P, E) \
+  if (pro == P && epi == E) return launch_slots_t<F, P, E>(a, p, grid, st, pdl);
+  MIE_S(PRO_EMBED_NORM, EPI_QKV)
+  MIE_S(PRO_NORM, EPI_QKV)
+  MIE_S(PRO_PLAIN, EPI_RESID)
+  MIE_S(PRO_NORM, EPI_SWIGLU)
+  MIE_S(PRO_NORM, EPI_ARGMAX)
+  MIE_S(PRO_PLAIN, EPI_STORE)
+#undef MIE_S
+  return fail(MIE_E_SHAPE, "slot GEMV: prologue %d / epilogue %d not built", pro, epi);
+}
+
+// Checks that the batched GEMV covers matrix m with prologue pro.
+mie_status slots_gemv_supported(const DevMat &m, int pro) {
+  if (m.fmt != MIE_FMT_BF16 && m.fmt != MIE_FMT_I8)
+    return fail(MIE_E_SHAPE, "few-slot step: weight format %d (bf16 and int8 are built)", m.fmt);
+  if (m.kp % 16) return fail(MIE_E_SHAPE, "few-slot step: padded width %d is not a multiple of 16", m.kp);
+  if (pro != PRO_PLAIN && m.cols > kSSlice)
+    return fail(MIE_E_SHAPE, "few-slot step: RMSNorm over %d > %d columns", m.cols, kSSlice);
+  if (((uintptr_t)m.w & 15) || (m.row_bytes & 15)) return fail(MIE_E_SHAPE, "few-slot step: unaligned rows");
+  const SlotPlan p = slot_plan(m, 1);
+  if (p.nst < 2) return fail(MIE_E_SHAPE, "few-slot step: shared memory too small for the ring");
+  const int grid = sm_count();
+  if (p.KS > 1 && (p.n_tiles + grid - 1) / grid > kSMaxAccTiles)
+    return fail(MIE_E_SHAPE, "few-slot step: %d rows are too many for a %d-column input", m.rows, m.cols);
+  return MIE_OK;
+}
+
+mie_status launch_gemv_slots(int pro, int epi, const GemvArgs &a, cudaStream_t st, bool pdl) {
+  if (!a.sp) return fail(MIE_E_ARG, "slot GEMV: no step parameters");  // the kernel reads the slot count there
+  const int grid = sm_count();
+  const SlotPlan p = slot_plan(a.m, grid);
+  if (a.m.fmt == MIE_FMT_BF16) return launch_slots_f<MIE_FMT_BF16>(pro, epi, a, p, grid, st, pdl);
+  if (a.m.fmt == MIE_FMT_I8) return launch_slots_f<MIE_FMT_I8>(pro, epi, a, p, grid, st, pdl);
+  return fail(MIE_E_SHAPE, "few-slot step: weight format %d", a.m.fmt);
+}
+
+}  // namespace mie

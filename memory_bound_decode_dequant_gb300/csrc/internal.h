@@ -86,6 +86,11 @@ struct AttnArgs {
   // persistent step: the current token's q | k | v and the output as tagged words
   const uint64_t *qkv_t = nullptr;
   uint64_t *out_t = nullptr;
+  // few-slot step: grid layer z is slot z (z >= sp->n_slots exits); q, out and the
+  // workspace of slot z are offset by z * (Hq * hd) floats and z * ws_slot_bytes
+  int slot_z = 0;
+  int max_slots = 1;
+  size_t ws_slot_bytes = 0;
 };
 size_t attn_workspace_bytes(int Hq, int Hkv, int hd, int n_splits);
 size_t attn_counter_bytes(int Hkv);  // the counters at the start of a workspace
@@ -119,6 +124,11 @@ struct PersistPlan {
 };
 mie_status persist_plan(const Phase *host_phases, int n, int G, int HD, PersistPlan *plan);
 mie_status persist_launch(const PersistPlan &plan, const PersistArgs &args, cudaStream_t st);
+
+// The few-slot step's GEMVs (gemv_slots.cu): every vector argument is slot 0's of
+// [n_slots][length] arrays; sp->n_slots slots are computed.
+mie_status slots_gemv_supported(const DevMat &m, int pro);
+mie_status launch_gemv_slots(int pro, int epi, const GemvArgs &a, cudaStream_t st, bool pdl);
 
 // Load-time kernels.
 mie_status launch_convert_bf16(const float *w, int64_t n, uint16_t *out, cudaStream_t st);

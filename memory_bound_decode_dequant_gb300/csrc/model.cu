@@ -123,6 +123,11 @@ struct mie_ctx {
   PersistPlan plan;
   unsigned long long *trace = nullptr;
   size_t trace_bytes = 0;
+  // few-slot step: its own phase list and graph (always the kernel chain)
+  std::vector<Phase> slot_phases;
+  cudaGraphExec_t slot_graph = nullptr;
+  bool slot_graph_ok = true, slot_primed = false;
+  int slot_launches = 0;
 
   void *dalloc(size_t bytes) {
     void *p = nullptr;
@@ -176,6 +181,7 @@ extern "C" void mie_destroy(mie_ctx *ctx) {
   if (!ctx) return;
   if (ctx->stream) cudaStreamSynchronize(ctx->stream);
   if (ctx->graph) cudaGraphExecDestroy(ctx->graph);
+  if (ctx->slot_graph) cudaGraphExecDestroy(ctx->slot_graph);
   for (void *p : ctx->allocs) cudaFree(p);
   if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
   mie_pool_destroy(ctx->pool);
@@ -415,6 +421,7 @@ extern "C" mie_status mie_load_weights(mie_ctx *ctx, const char *name, int fmt, 
   mie_status s;
   std::vector<int> none;
   ctx->primed = false;  // weights changed: the next step re-captures
+  ctx->slot_primed = false;
   if (n == "head" || n == "embed") {
     const bool is_head = n == "head";
     if (!is_head && c.tied) return fail(MIE_E_ARG, "mie_load_weights: tied model has no separate embedding");
@@ -757,13 +764,101 @@ extern "C" mie_status mie_decode_continue(mie_ctx *ctx, int n_steps) {
   return MIE_OK;
 }
 
+// The few-slot step's phases: those of the single-slot step, with attention launched
+// as one grid layer per slot (each slot's workspace follows the previous slot's).
+static mie_status build_slot_phases(mie_ctx *ctx) {
+  build_phases(ctx, ctx->slot_phases);
+  for (Phase &ph : ctx->slot_phases) {
+    if (ph.kind == PH_ATTN) {
+      ph.at.slot_z = 1;
+      ph.at.max_slots = ctx->cfg.max_slots;
+      ph.at.ws_slot_bytes = ctx->attn_ws_bytes * ctx->cfg.n_layers;
+    } else {
+      ph.g.sp = ctx->sp;  // every batched GEMV reads the slot count from the step parameters
+      const mie_status s = slots_gemv_supported(ph.g.m, ph.pro);
+      if (s != MIE_OK) return s;
+    }
+  }
+  return MIE_OK;
+}
+
+static mie_status enqueue_slots(mie_ctx *ctx, int *launches) {
+  int n = 0;
+  for (const Phase &ph : ctx->slot_phases) {
+    const mie_status s =
+        ph.kind == PH_GEMV ? launch_gemv_slots(ph.pro, ph.epi, ph.g, ctx->stream, true) : launch_attn(ph.at, ctx->stream, true);
+    if (s != MIE_OK) return s;
+    ++n;
+  }
+  *launches = n;
+  return MIE_OK;
+}
+
+static mie_status capture_slots(mie_ctx *ctx) {
+  if (ctx->slot_graph) {
+    cudaGraphExecDestroy(ctx->slot_graph);
+    ctx->slot_graph = nullptr;
+  }
+  mie_status s = build_slot_phases(ctx);
+  if (s != MIE_OK) return s;
+  ctx->slot_graph_ok = true;
+  cudaGraph_t g = nullptr;
+  MIE_CUDA(cudaStreamBeginCapture(ctx->stream, cudaStreamCaptureModeThreadLocal));
+  int n = 0;
+  s = enqueue_slots(ctx, &n);
+  cudaError_t e = cudaStreamEndCapture(ctx->stream, &g);
+  if (s == MIE_OK && e == cudaSuccess) e = cudaGraphInstantiate(&ctx->slot_graph, g, 0);
+  if (g) cudaGraphDestroy(g);
+  if (s != MIE_OK || e != cudaSuccess) {
+    cudaGetLastError();
+    ctx->slot_graph = nullptr;
+    ctx->slot_graph_ok = false;
+  }
+  ctx->slot_launches = n;
+  ctx->slot_primed = true;
+  return MIE_OK;
+}
+
 extern "C" mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int32_t *tokens, const int32_t *pos,
                                             const int32_t *block_tables, int max_blocks, float *logits_out,
                                             int32_t *argmax_out) {
-  (void)tokens; (void)pos; (void)block_tables; (void)max_blocks; (void)logits_out; (void)argmax_out;
-  if (!ctx) return fail(MIE_E_ARG, "mie_decode_step_slots: null context");
-  if (n_slots < 1 || n_slots > ctx->cfg.max_slots) return fail(MIE_E_ARG, "mie_decode_step_slots: n_slots %d", n_slots);
-  return fail(MIE_E_STATE, "mie_decode_step_slots: the batched step is not built yet");
+  if (!ctx || !tokens || !pos || !block_tables) return fail(MIE_E_ARG, "mie_decode_step_slots: null pointer");
+  const mie_config &c = ctx->cfg;
+  if (n_slots < 1 || n_slots > c.max_slots)
+    return fail(MIE_E_ARG, "mie_decode_step_slots: n_slots %d outside [1, %d]", n_slots, c.max_slots);
+  if (max_blocks < 1) return fail(MIE_E_ARG, "mie_decode_step_slots: max_blocks %d", max_blocks);
+  if (!all_loaded(ctx)) return fail(MIE_E_STATE, "mie_decode_step_slots: not every weight is loaded");
+  for (int s = 0; s < n_slots; ++s) {
+    if (tokens[s] < 0 || tokens[s] >= c.vocab)
+      return fail(MIE_E_ARG, "mie_decode_step_slots: slot %d token %d outside [0, %d)", s, tokens[s], c.vocab);
+    if (pos[s] < 0 || pos[s] >= c.max_pos)
+      return fail(MIE_E_ARG, "mie_decode_step_slots: slot %d pos %d outside [0, %d)", s, pos[s], c.max_pos);
+    if (pos[s] / c.block_size >= max_blocks)
+      return fail(MIE_E_ARG, "mie_decode_step_slots: slot %d pos %d needs more than %d blocks", s, pos[s], max_blocks);
+  }
+  StepParams &p = ctx->sp_host;
+  memset(&p, 0, sizeof p);
+  for (int s = 0; s < n_slots; ++s) {
+    p.token[s] = tokens[s];
+    p.pos[s] = pos[s];
+  }
+  p.block_table = block_tables;
+  p.max_blocks = max_blocks;
+  p.n_slots = n_slots;
+  p.logits_out = logits_out;
+  p.argmax_out = argmax_out;
+  p.advance = 0;
+  MIE_CUDA(cudaMemcpyAsync(ctx->sp, &p, sizeof p, cudaMemcpyHostToDevice, ctx->stream));
+  if (!ctx->slot_primed) {
+    const mie_status s = capture_slots(ctx);
+    if (s != MIE_OK) return s;
+  }
+  if (ctx->slot_graph_ok && ctx->slot_graph) {
+    MIE_CUDA(cudaGraphLaunch(ctx->slot_graph, ctx->stream));
+    return MIE_OK;
+  }
+  int n = 0;
+  return enqueue_slots(ctx, &n);
 }
 
 extern "C" mie_status mie_sync(mie_ctx *ctx) {
