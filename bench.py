@@ -2,12 +2,17 @@
 shape (bf16 weights, fp32 activations, bf16 paged KV cache), seeded synthetic weights.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mie|reference] [--fmt bf16|i8|q4_0]
-                [--ctx 128] [--no-cpu-baseline]
+                [--ctx 128] [--no-cpu-baseline] [--workload step|slots]
 
 One step = one full decode step (embedding gather, 16 layers of fused GEMVs + paged
 attention, LM head + argmax) replayed from the captured CUDA graph, token and position
 advanced on the device.  The weights (2.47 GB bf16) are far larger than the 129 MB L2,
 so nothing is served from L2 between steps.  Rank 0 prints one JSON line.
+
+--workload slots: the continuous-batching step instead -- 8 slots with contexts drawn
+from U[128, 4096], slots 0-3 sharing a refcounted 512-token prefix, block tables in
+random physical order from the host block pool, 256 steps with one slot retired and a
+256-token request admitted every 32 steps; aggregate tok/s = 8 * steps / time.
 """
 from __future__ import annotations
 
@@ -42,6 +47,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--oracle-steps", type=int, default=3)
     ap.add_argument("--chain", action="store_true", help="one kernel per phase instead of the persistent step")
+    ap.add_argument("--workload", default="step", choices=["step", "slots"],
+                    help="step: batch-1 decode (the headline); slots: 8-slot continuous batching")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the dominant kernel (the profiling command)")
     return ap.parse_args()
@@ -181,7 +188,33 @@ def run_reference(args, shape):
     print(json.dumps(line), flush=True)
 
 
+def run_reference_slots(args):
+    rank, world, local, pg = dist_init(args)
+    if rank != 0:
+        return
+    shape = synth.llama32_1b("bf16")
+    wl = synth.SlotWorkload()
+    cpu = time_oracle_slots(shape, wl)
+    v = cpu["value"]
+    line = {"impl": "reference", "metric": "continuous-batching decode tok/s (8 slots, Llama-3.2-1B shape bf16)",
+            "value": v, "unit": "tok/s", "n_gpus": 1, "steps": 1, "warmup": 0, "ms_per_step": 8e3 / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": "llama-3.2-1b bf16 8-slot continuous-batching step"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- GPU arm
+
+def read_traffic(name: str):
+    """DRAM bytes per launch of a kernel from its ncu summary under profiles/, or None."""
+    tp = os.path.join(ROOT, "profiles", f"{name}.traffic.json")
+    if os.path.exists(tp):
+        with open(tp) as f:
+            return json.load(f).get("bytes_per_launch")
+    return None
+
 
 def gemv_roofline(torch, mie, n_iter: int = 40):
     """The dominant kernel of the step -- the bf16 GEMV at the gate/up shape
@@ -267,7 +300,8 @@ def run_mie(args, shape):
     t0 = time.perf_counter()
     for _ in range(args.e2e_steps):
         gm.decode_step(tok, pos, bt, logits, am)
-        tok = int(am.item())  # device -> host read of the step's result (synchronises)
+        with torch.cuda.stream(stream):  # the read is ordered after the step on its stream
+            tok = int(am.item())  # device -> host read of the step's result (synchronises)
         pos += 1
     gm.sync()
     e2e_dt = max_over_ranks(pg, (time.perf_counter() - t0) / args.e2e_steps)
@@ -283,11 +317,20 @@ def run_mie(args, shape):
     if rank == 0:
         algo, kdt, n_iter = gemv_roofline(torch, mie)
         achieved = algo / kdt / 1e9
-        traffic = None
-        tp = os.path.join(ROOT, "profiles", "gemv_bf16_16384x2048.traffic.json")
-        if os.path.exists(tp):
-            with open(tp) as f:
-                traffic = json.load(f).get("bytes_per_launch")
+        gemv_roof = {"bound": "hbm", "kernel": "gemv bf16 16384x2048 (gate/up shape), standalone",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": read_traffic("gemv_bf16_16384x2048"),
+                     "algorithmic_bytes": algo, "launches_timed": n_iter, "us_per_launch": kdt * 1e6}
+        if gm.step_mode == 0:
+            # the persistent step is the step's only launch: its duration is the step time
+            # measured above with events on its stream
+            ach = step_bytes / dt / 1e9
+            roof = {"bound": "hbm", "kernel": "persistent_step (one launch = one decode step)",
+                    "achieved": ach, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / peak,
+                    "traffic": read_traffic(f"persistent_step_llama32_{args.fmt}"),
+                    "algorithmic_bytes": step_bytes, "launches_timed": args.steps, "us_per_launch": dt * 1e6}
+        else:
+            roof = gemv_roof
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             n = max(1, args.oracle_steps)
@@ -315,10 +358,8 @@ def run_mie(args, shape):
                        "l2": "weights 2.47 GB per step >> 129 MB L2: inputs larger than L2",
                        "step_bytes": step_bytes, "step_hbm_gbs": step_bytes / dt / 1e9,
                        "step_frac_of_peak": step_bytes / dt / 1e9 / peak},
-            "roofline": {"bound": "hbm", "kernel": "gemv bf16 16384x2048 (gate/up shape)",
-                         "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": traffic, "algorithmic_bytes": algo,
-                         "launches_timed": n_iter, "us_per_launch": kdt * 1e6},
+            "roofline": roof,
+            "gemv_roofline": gemv_roof,
             "e2e": {"value": world / e2e_dt, "unit": "tok/s", "h2d_bytes_per_step": STEP_PARAMS_BYTES,
                     "d2h_bytes_per_step": 4},
             "gpu_launches": launches * args.steps,
@@ -335,8 +376,178 @@ def run_mie(args, shape):
     return result
 
 
+# ----------------------------------------------------------------------------- few-slot step
+
+def slot_tables(pool, wl, n_blocks: int, bs: int, max_blocks: int, seed: int):
+    """The context's host block pool with its free list shuffled (tables in random
+    physical order), the shared prefix of slots 0..shared_slots-1 (refcount
+    shared_slots) and each slot's blocks for its context plus the steps it runs."""
+    ids = [pool.alloc() for _ in range(n_blocks)]
+    for i in synth.permutation(seed, n_blocks):
+        pool.decref(ids[int(i)])
+    tables = np.zeros((wl.n_slots, max_blocks), np.int32)
+    n_prefix = wl.shared_prefix // bs
+    prefix = [pool.alloc() for _ in range(n_prefix)]
+    for s in range(wl.n_slots):
+        nb = (int(wl.ctx[s]) + wl.steps + bs - 1) // bs
+        for b in range(nb):
+            if s < wl.shared_slots and b < n_prefix:
+                tables[s, b] = prefix[b]
+                if s > 0:
+                    pool.incref(prefix[b])
+            else:
+                tables[s, b] = pool.alloc()
+    assert all(pool.refcount(b) == wl.shared_slots for b in prefix)
+    return pool, tables, prefix
+
+
+def run_slots(args):
+    import torch
+
+    rank, world, local, pg = dist_init(args)
+    torch.cuda.set_device(local)
+    import memory_bound_decode_dequant_gb300 as mie
+    from memory_bound_decode_dequant_gb300.workload import build_gpu_model
+
+    shape = synth.llama32_1b("bf16")
+    wl = synth.SlotWorkload()
+    bs = shape.block_size
+    S = wl.n_slots
+    max_ctx = int(wl.ctx.max()) + wl.steps + args.warmup + 1
+    max_blocks = (max_ctx + bs - 1) // bs + 1
+    n_blocks = S * max_blocks + 64
+    stream = torch.cuda.Stream()
+    gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_blocks * bs, max_slots=S, stream=stream)
+    # synthetic prefilled cache: every block holds seeded N(0,1) bf16 values
+    kv = gm.kv()
+    gen = torch.Generator(device="cuda").manual_seed(0x4B56)
+    flat = kv.view(-1)
+    for i in range(0, flat.numel(), 1 << 26):
+        n = min(1 << 26, flat.numel() - i)
+        flat[i:i + n].copy_(torch.randn(n, generator=gen, device="cuda").to(torch.bfloat16).view(torch.int16))
+    pool, tables, prefix = slot_tables(gm.pool, wl, n_blocks, bs, max_blocks, seed=0x534C)
+    tdev = torch.from_numpy(tables).cuda()
+    logits = None
+    am = torch.empty(S, dtype=torch.int32, device="cuda")
+    toks = shape.tokens(S * (wl.steps + args.warmup + 64), stream=7).astype(np.int32).reshape(-1, S)
+    pos = wl.ctx.astype(np.int32).copy()
+    for i in range(args.warmup):
+        gm.decode_step_slots(toks[i], pos, tdev, logits, am)
+        pos += 1
+    gm.sync()
+    torch.cuda.synchronize()
+
+    # timed: wl.steps batched steps through the public call; every admit_every steps the
+    # host retires one slot (round robin), releases its blocks to the pool and admits a
+    # new admit_len-token request into fresh blocks (its K/V already holds seeded values)
+    kv_tokens = 0
+    retired = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with Clocks(local) as clk:
+        t_wall = time.perf_counter()
+        e0.record(stream)
+        for i in range(wl.steps):
+            if i > 0 and i % wl.admit_every == 0:
+                s = retired % S
+                retired += 1
+                nb = (int(pos[s]) + bs) // bs
+                for b in tables[s, :nb]:
+                    pool.decref(int(b))
+                new_len = wl.admit_len
+                need = (new_len + wl.steps + bs - 1) // bs
+                row = np.zeros(max_blocks, np.int32)
+                for b in range(need):
+                    row[b] = pool.alloc()
+                tables[s] = row
+                tdev[s].copy_(torch.from_numpy(row), non_blocking=True)
+                pos[s] = new_len
+            gm.decode_step_slots(toks[args.warmup + i], pos, tdev, logits, am)
+            kv_tokens += int(pos.sum()) + S
+            pos += 1
+        e1.record(stream)
+        e1.synchronize()
+        t_wall = time.perf_counter() - t_wall
+    gm.sync()
+    dt = e0.elapsed_time(e1) / 1e3 / wl.steps
+    # end to end: the same call with the argmax read back every step
+    e2e_steps = 16
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        gm.decode_step_slots(toks[args.warmup + wl.steps + i], pos, tdev, logits, am)
+        with torch.cuda.stream(stream):  # the read is ordered after the step on its stream
+            _ = am.cpu()  # device -> host read of the step's results (synchronises)
+        pos += 1
+    e2e_dt = (time.perf_counter() - t0) / e2e_steps
+    gm.sync()
+    w_bytes = shape.weight_bytes()
+    kv_bytes = shape.kv_bytes_per_token() * kv_tokens / wl.steps
+    step_bytes = w_bytes + kv_bytes
+    peak, peak_kind = measured_peaks()
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and world == 1:
+        cpu = time_oracle_slots(shape, wl)
+    if rank == 0:
+        ach = step_bytes / dt / 1e9
+        line = {
+            "metric": "continuous-batching decode tok/s (8 slots, Llama-3.2-1B shape bf16)",
+            "value": world * S / dt, "unit": "tok/s", "n_gpus": world, "steps": wl.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16 weights, bf16 hi+lo inputs on tensor cores with f32 accumulation, bf16 KV",
+            "data": "synthetic (seeded N(0,0.02) weights, seeded N(0,1) K/V cache, uniform tokens)",
+            "config": {"workload": "llama-3.2-1b bf16 8-slot continuous-batching step", "global_batch": S * world,
+                       "ctx_initial": [int(c) for c in wl.ctx], "shared_prefix": wl.shared_prefix,
+                       "shared_slots": wl.shared_slots, "admit_every": wl.admit_every, "admit_len": wl.admit_len,
+                       "parallelism": "replicas" if world > 1 else "single",
+                       "l2": "weights 2.47 GB per step >> 129 MB L2: inputs larger than L2",
+                       "step_bytes": step_bytes, "kv_bytes_per_step": kv_bytes},
+            "roofline": {"bound": "hbm", "kernel": "whole few-slot step (kernel chain in one graph)",
+                         "achieved": ach, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": ach / peak, "traffic": None, "algorithmic_bytes": step_bytes,
+                         "us_per_step": dt * 1e6},
+            "e2e": {"value": world * S / e2e_dt, "unit": "tok/s", "h2d_bytes_per_step": STEP_PARAMS_BYTES,
+                    "d2h_bytes_per_step": 4 * S},
+            "gpu_launches": gm.slot_launches * wl.steps, "launches_per_step": gm.slot_launches,
+            "clocks": clk.summary(), "wall_s_timed": t_wall, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    gm.close()
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def time_oracle_slots(shape, wl):
+    """The oracle's batched step (independent single-slot steps) on a bounded sample:
+    two of the eight slots, at their contexts, K/V prefilled with seeded values."""
+    import oracle
+    bs = shape.block_size
+    sample = [0, S_last] if (S_last := wl.n_slots - 1) else [0]
+    ctxs = [int(wl.ctx[s]) for s in sample]
+    need = sum((c + 1 + bs - 1) // bs for c in ctxs) + 1
+    om = oracle.Model(shape, n_kv_blocks=need, max_pos=(max(ctxs) + bs) // bs * bs + bs)
+    kv = om.kv()
+    kv[...] = oracle.to_bf16(synth.normal(0x4B56, kv.size)).reshape(kv.shape)
+    toks = shape.tokens(len(sample), stream=9)
+    t0 = time.perf_counter()
+    off = 0
+    for j, c in enumerate(ctxs):
+        nb = (c + 1 + bs - 1) // bs
+        bt = np.arange(off, off + nb, dtype=np.int32)
+        off += nb
+        om.decode_step(int(toks[j]), c, bt)
+    sec_per_slot = (time.perf_counter() - t0) / len(sample)
+    return {"value": 1.0 / sec_per_slot, "unit": "tok/s", "cores": 1, "kind": "oracle",
+            "sample": f"slots {sample} of the 8 (contexts {ctxs}) through the oracle's single-slot step, "
+                      f"which defines its batched step; plain single-threaded C, K/V seeded"}
+
+
 def main():
     args = parse()
+    if args.workload == "slots":
+        if args.impl == "reference":
+            run_reference_slots(args)
+        else:
+            run_slots(args)
+        return
     shape = synth.llama32_1b(args.fmt)
     if args.kernel_only:
         import torch

@@ -298,6 +298,9 @@ mie_status mie_sync(mie_ctx *ctx);
 /* Kernel launches one mie_decode_step replay performs (for launch accounting). */
 int mie_step_launches(const mie_ctx *ctx);
 
+/* Kernel launches one mie_decode_step_slots replay performs (0 before its first call). */
+int mie_slot_step_launches(const mie_ctx *ctx);
+
 #ifdef __cplusplus
 }
 #endif

@@ -81,6 +81,7 @@ _SIGS = {
     "mie_step_launches": (I, [P]),
     "mie_set_step_mode": (I, [P, I]),
     "mie_step_mode": (I, [P]),
+    "mie_slot_step_launches": (I, [P]),
     "mie_set_trace": (I, [P, P, SZ, ctypes.POINTER(I), ctypes.POINTER(I)]),
 }
 
@@ -414,6 +415,10 @@ class Model:
     @property
     def launches(self) -> int:
         return int(lib().mie_step_launches(self.h))
+
+    @property
+    def slot_launches(self) -> int:
+        return int(lib().mie_slot_step_launches(self.h))
 
     PERSISTENT, CHAIN = 0, 1
 

@@ -917,3 +917,5 @@ extern "C" mie_status mie_set_trace(mie_ctx *ctx, void *device_buffer, size_t by
 }
 
 extern "C" int mie_step_launches(const mie_ctx *ctx) { return ctx ? ctx->launches : 0; }
+
+extern "C" int mie_slot_step_launches(const mie_ctx *ctx) { return ctx ? ctx->slot_launches : 0; }
