@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--oracle-steps", type=int, default=3)
     ap.add_argument("--chain", action="store_true", help="one kernel per phase instead of the persistent step")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="truncate the model to this many layers (a small case for profiling; 0 = all)")
     ap.add_argument("--workload", default="step", choices=["step", "slots"],
                     help="step: batch-1 decode (the headline); slots: 8-slot continuous batching")
     ap.add_argument("--kernel-only", action="store_true",
@@ -352,7 +354,8 @@ def run_mie(args, shape):
             "vs_baseline": None,
             "dtype": "bf16 weights, f32 activations/accumulation, bf16 KV",
             "data": "synthetic (seeded N(0,0.02) weights, uniform tokens, prefilled by real decode steps)",
-            "config": {"workload": f"{shape.name} {args.fmt} batch-1 decode step",
+            "config": {"workload": f"{shape.name} {args.fmt} batch-1 decode step"
+                                   + (f" ({shape.n_layers} layers, profiling case)" if args.layers else ""),
                        "model": shape.name, "weights": args.fmt, "global_batch": world, "seq_len": args.ctx,
                        "ctx_range": [args.ctx, ctx_end], "parallelism": "replicas" if world > 1 else "single",
                        "l2": "weights 2.47 GB per step >> 129 MB L2: inputs larger than L2",
@@ -542,13 +545,18 @@ def time_oracle_slots(shape, wl):
 
 def main():
     args = parse()
+    if args.layers:
+        from dataclasses import replace as _replace  # a truncated model for profiling captures
+        synth_shape = _replace(synth.llama32_1b(args.fmt), n_layers=args.layers)
+    else:
+        synth_shape = None
     if args.workload == "slots":
         if args.impl == "reference":
             run_reference_slots(args)
         else:
             run_slots(args)
         return
-    shape = synth.llama32_1b(args.fmt)
+    shape = synth_shape or synth.llama32_1b(args.fmt)
     if args.kernel_only:
         import torch
         import memory_bound_decode_dequant_gb300 as mie
