@@ -379,6 +379,12 @@ struct RingAttnSmem {
   unsigned last;
 };
 
+// Blocks per attention split of the persistent step: 32 tokens, so that the context of
+// one KV head spreads over several CTAs (the passes over one 128-token chunk cost about
+// 6,300 cycles on one CTA; a 32-token split about a quarter of that), merged by the last
+// split of the head.
+__host__ __device__ inline int ring_attn_blocks_per_split(int bs) { return bs >= 32 ? 1 : 32 / bs; }
+
 // Blocks per attention stage: as many as a ring slot holds, at most kChunkTok tokens.
 __host__ __device__ inline int attn_stage_blocks(uint32_t slot_bytes, int bs, int hd) {
   const int cap = (int)(slot_bytes / (2u * (uint32_t)bs * hd * 2));
@@ -534,7 +540,7 @@ __device__ bool attn_phase(const AttnArgs &at, const Ring &ring, int &s_global, 
   auto &sm = *reinterpret_cast<RingAttnSmem<G, HD> *>(scratch);
   const int ctx = sc.ctx;
   const int nblk = (ctx + at.bs - 1) / at.bs;
-  const int nsplit = attn_nsplit(nblk, at.n_splits, attn_blocks_per_split<HD, kPW>(at.bs));
+  const int nsplit = attn_nsplit(nblk, at.n_splits, ring_attn_blocks_per_split(at.bs));
   const int items = at.Hkv * nsplit;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
     if (!attn_ring_item<G, HD>(at, it / nsplit, it % nsplit, nsplit, ctx, ring, s_global, sm, sc, pa)) {
@@ -614,7 +620,7 @@ struct StageCursor {
     kb = bs * HD * 2;
     cap = attn_stage_blocks(a->slot_bytes, bs, HD);
     nblk = (ctx + bs - 1) / bs;
-    nsplit = attn_nsplit(nblk, at.n_splits, attn_blocks_per_split<HD, kPW>(bs));
+    nsplit = attn_nsplit(nblk, at.n_splits, ring_attn_blocks_per_split(bs));
     items = at.Hkv * nsplit;
     it = (int)blockIdx.x - (int)gridDim.x;
     return next_item();
@@ -803,7 +809,10 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
     const Phase &ph = s_ph[p & 1];
     stamp(a.trace, p, 0);
     if (ph.kind == PH_GEMV) {
-      if (ph.g.m.fmt == FL) ok = gemv_phase<FL>(ph, ring, s_global, scratch, ps, sc, a, p);
+      // one inlined copy per distinct format: the kernel's code is kept small so that the
+      // phases run once per layer (attention, epilogues) hit the instruction cache
+      if constexpr (FL == FH) ok = gemv_phase<FL>(ph, ring, s_global, scratch, ps, sc, a, p);
+      else if (ph.g.m.fmt == FL) ok = gemv_phase<FL>(ph, ring, s_global, scratch, ps, sc, a, p);
       else ok = gemv_phase<FH>(ph, ring, s_global, scratch, ps, sc, a, p);
     } else {
       stamp(a.trace, p, 1);
