@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--oracle-steps", type=int, default=3)
     ap.add_argument("--chain", action="store_true", help="one kernel per phase instead of the persistent step")
+    ap.add_argument("--slot-steps", type=int, default=256,
+                    help="timed steps of --workload slots (the workload's 256; fewer for profiling)")
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (a small case for profiling; 0 = all)")
     ap.add_argument("--workload", default="step", choices=["step", "slots"],
@@ -413,7 +415,7 @@ def run_slots(args):
     from memory_bound_decode_dequant_gb300.workload import build_gpu_model
 
     shape = synth.llama32_1b("bf16")
-    wl = synth.SlotWorkload()
+    wl = synth.SlotWorkload(steps=args.slot_steps)
     bs = shape.block_size
     S = wl.n_slots
     max_ctx = int(wl.ctx.max()) + wl.steps + args.warmup + 1

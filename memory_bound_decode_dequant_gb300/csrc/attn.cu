@@ -63,6 +63,151 @@ __global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a_in)
   attn_split<G, HD, kAttnWarps, CtaSync>(a, g, s, nsplit, ctx, bt, nullptr, sm);
 }
 
+// Chunked variant: 8 warps per (split, KV head[, slot]); the split's K/V blocks are
+// brought into shared memory by bulk copies (one per block for K and one for V, 128
+// tokens per chunk, two chunks in flight) and each chunk is reduced by the three
+// CTA-wide passes of chunk_passes.  Splits of 256 tokens; merged by the last split.
+constexpr int kCThreads = 256;
+constexpr int kCTok = 128;       // tokens per chunk
+constexpr int kCSplitTok = 256;  // tokens per split
+
+struct CSync {
+  __device__ static void sync() { __syncthreads(); }
+  __device__ static bool all(bool v) { return __syncthreads_and(v) != 0; }
+};
+
+template <int G, int HD>
+__global__ void __launch_bounds__(kCThreads) attn_chunk_kernel(const AttnArgs a_in) {
+  constexpr int NO = (G * HD + kCThreads - 1) / kCThreads;
+  extern __shared__ __align__(128) uint8_t cbuf[];  // 2 x [K: kCTok*HD*2 bytes][V: same]
+  __shared__ ChunkSmem<G, HD> sm;
+  __shared__ __align__(8) uint64_t bar[2];
+  __shared__ int ids[kCSplitTok / 8];
+  pdl_trigger();
+  AttnArgs a = a_in;
+  if (a_in.slot_z) {  // one grid layer per slot of the few-slot step
+    const int z = blockIdx.z;
+    if (z >= a_in.sp->n_slots) return;
+    a.slot = z;
+    a.q += (int64_t)z * a.Hq * a.hd;
+    a.out += (int64_t)z * a.Hq * a.hd;
+    a.ws_count = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(a.ws_count) + z * a.ws_slot_bytes);
+    a.ws_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.ws_part) + z * a.ws_slot_bytes);
+  }
+  pdl_wait();
+  const int tid = threadIdx.x, g = blockIdx.y, sp = blockIdx.x;
+  int ctx;
+  const int32_t *bt;
+  int n_table;
+  if (a.sp) {
+    ctx = a.sp->pos[a.slot] + 1;
+    bt = a.sp->block_table + (int64_t)a.slot * a.sp->max_blocks;
+    n_table = a.sp->max_blocks;
+  } else {
+    ctx = a.ctx;
+    bt = a.block_table;
+    n_table = a.n_table;
+  }
+  if (ctx > n_table * a.bs) {
+    if (tid == 0 && sp == 0 && g == 0) latch_error(a.err, ERR_POS);
+    ctx = n_table * a.bs;
+  }
+  if (ctx < 0) ctx = 0;
+  const int nblk = (ctx + a.bs - 1) / a.bs;
+  const int nsplit = attn_nsplit(nblk, a.n_splits, kCSplitTok / a.bs);
+  if (sp >= nsplit) return;
+  const int b0 = (int)((int64_t)sp * nblk / nsplit), b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
+  const int t_end = min(b1 * a.bs, ctx);
+  const int kb = a.bs * HD * 2;           // bytes of one block of one head
+  const int cb = kCTok / a.bs;            // blocks per chunk
+  const int nch = (b1 - b0 + cb - 1) / cb;
+  const uint32_t buf_bytes = 2u * kCTok * HD * 2;
+
+  if (tid < b1 - b0) {
+    int blk = bt[b0 + tid];
+    if (blk < 0 || blk >= a.n_pool_blocks) {
+      latch_error(a.err, ERR_BLOCK_ID);
+      blk = 0;  // a valid block: the result is wrong but the error is reported
+    }
+    ids[tid] = blk;
+  }
+  for (int i = tid; i < G * HD; i += kCThreads) sm.q[i] = __ldcg(a.q + (int64_t)(g * G) * HD + i);
+  if (tid < G) {
+    sm.m[tid] = -INFINITY;
+    sm.l[tid] = 0.f;
+  }
+  if (tid == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const int64_t head_off = (int64_t)g * a.bs * HD;  // elements
+  auto issue = [&](int ci) {  // thread 0: the bulk copies of chunk ci into buffer ci & 1
+    const int first = ci * cb, nb = min(cb, b1 - b0 - first);
+    uint8_t *kd = cbuf + (size_t)(ci & 1) * buf_bytes, *vd = kd + (size_t)kCTok * HD * 2;
+    mbar_expect_tx(&bar[ci & 1], 2u * nb * kb);
+    for (int j = 0; j < nb; ++j) {
+      const int64_t off = (int64_t)ids[first + j] * a.block_stride + head_off;
+      bulk_load(kd + (size_t)j * kb, a.k + off, kb, &bar[ci & 1], 0ull);
+      bulk_load(vd + (size_t)j * kb, a.v + off, kb, &bar[ci & 1], 0ull);
+    }
+  };
+  if (tid == 0) {
+    issue(0);
+    if (nch > 1) issue(1);
+  }
+  float o[NO];
+#pragma unroll
+  for (int j = 0; j < NO; ++j) o[j] = 0.f;
+  bool ok = true;
+  for (int ci = 0; ci < nch; ++ci) {
+    ok = CSync::all(ok && mbar_wait(&bar[ci & 1], (ci >> 1) & 1));
+    if (!ok) break;
+    const uint32_t kbase = smem_u32(cbuf) + (uint32_t)(ci & 1) * buf_bytes, vbase = kbase + (uint32_t)kCTok * HD * 2;
+    const int t0 = (b0 + ci * cb) * a.bs;
+    const int ntok = min((b0 + min((ci + 1) * cb, b1 - b0)) * a.bs, t_end) - t0;
+    chunk_passes<G, HD, kCThreads, CSync>(kbase, vbase, ntok, a.scale, sm, o);
+    __syncthreads();  // every thread is done with the buffer
+    if (tid == 0 && ci + 2 < nch) {
+      fence_proxy_async_smem();
+      issue(ci + 2);
+    }
+  }
+  if (!ok) {  // a copy never completed: report, and leave no copy writing into shared memory
+    if (tid == 0) {
+      latch_error(a.err, ERR_TIMEOUT);
+      for (int ci = 0; ci < nch && ci < 2; ++ci) mbar_wait(&bar[ci & 1], 0);
+    }
+    return;
+  }
+  if (nsplit == 1) {
+#pragma unroll
+    for (int j = 0; j < NO; ++j) {
+      const int i = tid + j * kCThreads;
+      if (i < G * HD) {
+        const float L = sm.l[i / HD];
+        a.out[(int64_t)(g * G) * HD + i] = (L > 0.f) ? o[j] / L : 0.f;
+      }
+    }
+    return;
+  }
+  float *part = a.ws_part + ((int64_t)g * a.n_splits + sp) * (G * (2 + HD));
+#pragma unroll
+  for (int j = 0; j < NO; ++j) {
+    const int i = tid + j * kCThreads;
+    if (i < G * HD) {
+      const int h = i / HD;
+      part[2 * G + i] = o[j];
+      if (i % HD == 0) {
+        part[h] = sm.m[h];
+        part[G + h] = sm.l[h];
+      }
+    }
+  }
+  attn_merge_splits<G, HD, kCThreads, CSync, false>(a, g, nsplit, sm.last, 0u);
+}
+
 // Empty context: the output is zero (no split has a position).
 __global__ void zero_kernel(float *out, int n) {
   pdl_trigger();
@@ -77,25 +222,35 @@ size_t attn_workspace_bytes(int Hq, int Hkv, int hd, int n_splits) {
   return attn_counter_bytes(Hkv) + (size_t)Hkv * n_splits * G * (2 + hd) * sizeof(float);
 }
 
+// Splits a workspace is sized for: two CTAs per SM over the KV heads, and at least
+// enough that no split of the chunked kernel exceeds kCSplitTok tokens (the block ids
+// of a split are cached in shared memory).
 int attn_splits_for(int Hkv, int max_ctx, int bs) {
   const int nblk = (max_ctx + bs - 1) / bs;
   int s = (2 * sm_count() + Hkv - 1) / Hkv;
   if (s > nblk) s = nblk;
+  const int per = kCSplitTok / bs;
+  const int need = (nblk + per - 1) / per;
+  if (s < need) s = need;
   return s < 1 ? 1 : s;
 }
 
 template <int G, int HD>
 static mie_status launch_attn_t(const AttnArgs &a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
+  const size_t smem = 2u * 2u * kCTok * HD * 2;
+  auto kern = attn_chunk_kernel<G, HD>;
+  MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   cfg.gridDim = dim3(a.n_splits, a.Hkv, a.slot_z ? a.max_slots : 1);
-  cfg.blockDim = dim3(kAttnThreads);
+  cfg.blockDim = dim3(kCThreads);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
-  MIE_CUDA(cudaLaunchKernelEx(&cfg, attn_kernel<G, HD>, a));
+  MIE_CUDA(cudaLaunchKernelEx(&cfg, kern, a));
   return MIE_OK;
 }
 

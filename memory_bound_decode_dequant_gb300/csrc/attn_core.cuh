@@ -340,6 +340,109 @@ __device__ void attn_store(const AttnArgs &a, int g, int s, int nsplit, const fl
   attn_merge_splits<G, HD, NT, Sync, Tagged>(a, g, nsplit, sm.last, tag);
 }
 
+// ------------------------------------------------------------------ chunk passes
+//
+// Attention over a chunk of K/V held in shared memory -- token t's key at byte t*hd*2
+// from kbase, its value likewise from vbase (a run of whole blocks: kb = bs*hd*2 bytes
+// per block makes the block arithmetic vanish) -- in three passes over the whole CTA
+// instead of the per-warp online softmax above, whose shuffle chains cost ~5000 cycles
+// per 16 tokens when few warps share an SM (measured on GB300): (1) a score for every
+// (head, token) pair, lanes starting at different 16-byte chunks of their key rows so
+// that the reads avoid bank conflicts; (2) one warp per head takes max, exp and sum and
+// rescales the running (m, l); (3) every thread accumulates its (head, dim) outputs
+// over the chunk.  The softmax is the two-pass definition evaluated per chunk with the
+// running maximum carried across chunks.
+
+constexpr int kChunkTok = 256;  // tokens of one chunk at most
+
+template <int G, int HD>
+struct ChunkSmem {
+  float q[G * HD];
+  float kn[HD], vn[HD];   // persistent step: the current token's k and v (bf16-exact)
+  float s[G][kChunkTok];  // scores, then probabilities (zero past the chunk up to a multiple of 4)
+  float m[G], l[G], corr[G];
+  unsigned last;
+};
+
+// One chunk of ntok (1..kChunkTok) tokens.  sm.q holds the queries, sm.m / sm.l the
+// running statistics (-inf / 0 before the first chunk); o[j] is this thread's output
+// i = tid + j*NT of the G*HD outputs, rescaled and accumulated.  NT threads (warps
+// 0..NT/32-1, at least G of them) take part; Sync is a barrier over them.
+template <int G, int HD, int NT, class Sync>
+__device__ __forceinline__ void chunk_passes(uint32_t kbase, uint32_t vbase, int ntok, float scale,
+                                             ChunkSmem<G, HD> &sm, float (&o)[(G * HD + NT - 1) / NT]) {
+  constexpr int NO = (G * HD + NT - 1) / NT;
+  constexpr int NCH = HD / 8;  // 16-byte chunks of a key row
+  static_assert(NT / 32 >= G, "one warp per head in the statistics pass");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t qa = smem_u32(sm.q), sa = smem_u32(&sm.s[0][0]);
+  // (1) scores
+  for (int p = tid; p < G * ntok; p += NT) {
+    const int h = p / ntok, t = p - h * ntok;
+    const uint32_t krow = kbase + (uint32_t)t * (HD * 2), qrow = qa + (uint32_t)h * (HD * 4);
+    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+#pragma unroll
+    for (int c0 = 0; c0 < NCH; ++c0) {
+      const int c = (c0 + lane) % NCH;
+      const uint4 kw = lds128(krow + c * 16);
+      const float4 qa0 = lds128f(qrow + c * 32), qa1 = lds128f(qrow + c * 32 + 16);
+      d0 = fmaf(qa0.x, __uint_as_float(kw.x << 16), d0);
+      d1 = fmaf(qa0.y, __uint_as_float(kw.x & 0xffff0000u), d1);
+      d2 = fmaf(qa0.z, __uint_as_float(kw.y << 16), d2);
+      d3 = fmaf(qa0.w, __uint_as_float(kw.y & 0xffff0000u), d3);
+      d0 = fmaf(qa1.x, __uint_as_float(kw.z << 16), d0);
+      d1 = fmaf(qa1.y, __uint_as_float(kw.z & 0xffff0000u), d1);
+      d2 = fmaf(qa1.z, __uint_as_float(kw.w << 16), d2);
+      d3 = fmaf(qa1.w, __uint_as_float(kw.w & 0xffff0000u), d3);
+    }
+    sm.s[h][t] = ((d0 + d1) + (d2 + d3)) * scale;
+  }
+  Sync::sync();
+  // (2) softmax statistics, one warp per head
+  if (warp < G) {
+    const int h = warp;
+    float mx = -INFINITY;
+    for (int t = lane; t < ntok; t += 32) mx = fmaxf(mx, sm.s[h][t]);
+    mx = warp_max(mx);
+    const float m_old = sm.m[h], m_new = fmaxf(m_old, mx);
+    float sum = 0.f;
+    const int npad = (ntok + 3) & ~3;
+    for (int t = lane; t < npad; t += 32) {
+      const float pr = (t < ntok) ? expf(sm.s[h][t] - m_new) : 0.f;
+      sm.s[h][t] = pr;
+      sum += pr;
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) {
+      const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
+      sm.corr[h] = c;
+      sm.l[h] = sm.l[h] * c + sum;
+      sm.m[h] = m_new;
+    }
+  }
+  Sync::sync();
+  // (3) outputs
+#pragma unroll
+  for (int j = 0; j < NO; ++j) {
+    const int i = tid + j * NT;
+    if (i < G * HD) {
+      const int h = i / HD, d = i % HD;
+      float acc = o[j] * sm.corr[h];
+      const uint32_t prow = sa + (uint32_t)h * (kChunkTok * 4), vcol = vbase + d * 2;
+      for (int t = 0; t < ntok; t += 4) {
+        const float4 p4 = lds128f(prow + t * 4);
+        const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int tt = min(t + u, ntok - 1);  // past the chunk the probability is 0
+          acc = fmaf(pv[u], __uint_as_float(lds16(vcol + (uint32_t)tt * (HD * 2)) << 16), acc);
+        }
+      }
+      o[j] = acc;
+    }
+  }
+}
+
 // Computes split s of nsplit for KV head g, reading K/V from the paged pool.
 // blk_pre, when not null, holds the block ids of blocks [0, nblk) already staged in
 // shared memory; otherwise they are read from bt in chunks.  Sync::sync() is a barrier

@@ -29,7 +29,8 @@ constexpr int kSRows = 8;            // weight rows per stage (the MMA's N)
 constexpr int kSSlice = 2048;        // columns per stage
 constexpr int kSKSteps = kSSlice / 16 / kSW;  // k-steps per warp per slice (16)
 constexpr int kSMaxNst = 8;
-constexpr int kSMaxAccTiles = 64;    // tiles per CTA whose partial sums persist across slices
+constexpr int kSMaxAccTiles = 16;    // tiles per CTA whose partial sums persist across slices
+constexpr int kSBurst = 2;           // stages issued before the consumers have their first input
 
 struct SSync {
   __device__ static void sync() { asm volatile("bar.sync 1, %0;" ::"n"(kSCT) : "memory"); }
@@ -81,16 +82,35 @@ __device__ __forceinline__ uint32_t b_word<MIE_FMT_I8>(uint32_t addr) {
 
 // Shared state of one CTA.
 struct SlotShared {
-  float ss[kSW][kMaxSlots];            // per-warp sums of squares (RMSNorm)
-  float rs[kMaxSlots];                 // RMSNorm scale per slot
-  float red[2][kSW][kMaxSlots][kSRows];  // warp partials of a stage (double-buffered)
+  float ss[kSW][kMaxSlots];                    // per-warp sums of squares (RMSNorm)
+  float rs[kMaxSlots];                         // RMSNorm scale per slot
+  float red[kSMaxNst][kSW][kMaxSlots][kSRows];  // warp partials of the stage in each ring slot
+  unsigned cnt[kSMaxNst];                      // warps done with the stage in each ring slot
   float acc[kSMaxAccTiles][kMaxSlots][kSRows];  // partial sums across slices
+  unsigned long long best[kMaxSlots];          // argmax per slot: orderable value << 32 | ~row
   int pos[kMaxSlots], blk[kMaxSlots], tok[kMaxSlots];
   bool pos_ok[kMaxSlots], blk_ok[kMaxSlots];
-  float bv[2][kMaxSlots];
-  int bi[2][kMaxSlots];
+  float rc[kMaxSlots][64], rsn[kMaxSlots][64];  // RoPE cos / sin of each slot's position (hd <= 128)
+  float gain[kSSlice];                           // RMSNorm gains (the normalising prologues have K <= kSSlice)
   unsigned last;
 };
+
+// Orderable key of (value, row): larger value first, then lower row; 0 = no row yet.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int row) {
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t o = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)o << 32) | (unsigned long long)(0xffffffffu - (uint32_t)row);
+}
+__device__ __forceinline__ void argmax_unkey(unsigned long long k, float &v, int &row) {
+  if (k == 0ull) {
+    v = -INFINITY;
+    row = 0x7fffffff;
+    return;
+  }
+  const uint32_t o = (uint32_t)(k >> 32);
+  v = __uint_as_float((o & 0x80000000u) ? (o & 0x7fffffffu) : ~o);
+  row = (int)(0xffffffffu - (uint32_t)k);
+}
 
 struct SlotPlan {
   int nst = 0;
@@ -105,7 +125,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kSMaxNst], empty_bar[kSMaxNst];
   __shared__ SlotShared sh;
-  __shared__ volatile int s_issued, s_prod_done, s_abort;
+  __shared__ volatile int s_issued, s_prod_done, s_abort, s_x_ready;
 
   const DevMat &m = a.m;
   const int M = m.rows, K = m.cols, Kp = m.kp;
@@ -124,6 +144,9 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     s_issued = 0;
     s_prod_done = 0;
     s_abort = 0;
+    s_x_ready = 0;
+    for (int i = 0; i < kSMaxNst; ++i) sh.cnt[i] = 0u;
+    for (int i = 0; i < kMaxSlots; ++i) sh.best[i] = 0ull;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -134,6 +157,11 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       const uint64_t pol = evict_first_policy();
       for (int s = 0; s < n_stages; ++s) {
         const int slot = s % pl.nst, k = s / pl.nst;
+        if (s == kSBurst) {
+          // the consumers' input loads go out before the rest of the ring's copies: L2 and
+          // HBM requests queue behind bulk copies in flight (measured 5-10 us otherwise)
+          for (long it = 0; it < kWaitPolls && !s_x_ready && !s_abort; ++it) __nanosleep(128);
+        }
         if (k > 0 && !mbar_wait(&empty_bar[slot], (k - 1) & 1)) {
           s_abort = 1;
           latch_error(a.err, ERR_TIMEOUT);
@@ -155,6 +183,8 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     return;
   }
 
+  if (PRO != PRO_PLAIN)  // gains are weights: loaded before waiting for the previous kernel
+    for (int i = tid; i < K && i < kSSlice; i += kSCT) sh.gain[i] = __ldg(a.gain + i);
   pdl_wait();
   const int g = lane >> 2, t = lane & 3;
 
@@ -183,28 +213,66 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     sh.pos_ok[s] = pos_ok;
     sh.blk_ok[s] = blk_ok;
   }
+  if constexpr (EPI == EPI_QKV) {  // each slot's RoPE row, so the epilogue issues no dependent loads
+    const int h2 = a.hd / 2;
+    for (int i = tid; i < kMaxSlots * h2; i += kSCT) {
+      const int s = i / h2, j = i % h2;
+      int pos = (s < S) ? a.sp->pos[s] : 0;
+      if (pos < 0 || pos >= a.max_pos) pos = 0;
+      sh.rc[s][j] = a.rope_cos[(int64_t)pos * h2 + j];
+      sh.rsn[s][j] = a.rope_sin[(int64_t)pos * h2 + j];
+    }
+  }
   SSync::sync();
 
   // A fragments of slice q: x of slot g at columns kk + 2t (+1) and kk + 2t + 8 (+9)
-  // of this warp's k-steps, as hi / lo bf16 pairs.
+  // of this warp's k-steps, as hi / lo bf16 pairs.  Every load of the slice (x pairs
+  // and gain pairs, 8 bytes each) is issued before the first use, so staging costs one
+  // round trip; the values stay in registers through the RMSNorm.
   uint32_t ah0[kSKSteps], ah2[kSKSteps], al0[kSKSteps], al2[kSKSteps];
-  auto x_at = [&](int e) -> float {
-    if (g >= S || e >= K) return 0.f;
-    if (PRO == PRO_EMBED_NORM) return embed_at(a.embed, sh.tok[g], e);
-    return __ldcg(a.x + (int64_t)g * K + e);
+  auto load_pair = [&](int e) -> float2 {  // x of slot g at columns e, e + 1 (e even)
+    if (g >= S || e >= K) return make_float2(0.f, 0.f);
+    if (PRO == PRO_EMBED_NORM) {
+      if (a.embed.fmt == MIE_FMT_BF16 && e + 1 < K) {
+        const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(a.embed.w + (int64_t)sh.tok[g] * a.embed.row_bytes) + e / 2);
+        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+      }
+      return make_float2(embed_at(a.embed, sh.tok[g], e), e + 1 < K ? embed_at(a.embed, sh.tok[g], e + 1) : 0.f);
+    }
+    if (e + 1 < K) return __ldcg(reinterpret_cast<const float2 *>(a.x + (int64_t)g * K + e));
+    return make_float2(__ldcg(a.x + (int64_t)g * K + e), 0.f);
+  };
+  auto gain_pair = [&](int e) -> float2 {  // staged in shared memory before the kernel waited
+    if (e >= K) return make_float2(0.f, 0.f);
+    return make_float2(sh.gain[e], e + 1 < K ? sh.gain[e + 1] : 0.f);
   };
   auto load_slice = [&](int q) {
-    // RMSNorm over the whole vector: the prologues that normalise have K <= kSSlice
-    float rn = 1.f;
-    if (PRO != PRO_PLAIN) {
-      float ss = 0.f;
-#pragma unroll 4
+    float2 xv[kSKSteps][2];
+#pragma unroll
+    for (int j = 0; j < kSKSteps; ++j) {
+      const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
+      xv[j][0] = load_pair(kk);
+      xv[j][1] = load_pair(kk + 8);
+    }
+    if (PRO == PRO_EMBED_NORM && blockIdx.x == 0 && g < S) {  // the residual stream starts as x
+#pragma unroll
       for (int j = 0; j < kSKSteps; ++j) {
         const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
-        const float v[4] = {x_at(kk), x_at(kk + 1), x_at(kk + 8), x_at(kk + 9)};
 #pragma unroll
-        for (int u = 0; u < 4; ++u) ss += v[u] * v[u];
+        for (int h = 0; h < 2; ++h) {
+          const int e = kk + 8 * h;
+          if (e < K) a.x_store[(int64_t)g * K + e] = xv[j][h].x;
+          if (e + 1 < K) a.x_store[(int64_t)g * K + e + 1] = xv[j][h].y;
+        }
       }
+    }
+    if (PRO != PRO_PLAIN) {
+      // RMSNorm over the whole vector: the prologues that normalise have K <= kSSlice
+      float ss = 0.f;
+#pragma unroll
+      for (int j = 0; j < kSKSteps; ++j)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) ss += xv[j][h].x * xv[j][h].x + xv[j][h].y * xv[j][h].y;
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
       if (t == 0) sh.ss[warp][g] = ss;
@@ -215,23 +283,21 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
         sh.rs[tid] = 1.0f / sqrtf(tot / (float)K + a.eps);
       }
       SSync::sync();
-      rn = sh.rs[g];
+      const float rn = sh.rs[g];
+#pragma unroll
+      for (int j = 0; j < kSKSteps; ++j) {
+        const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float2 gg = gain_pair(kk + 8 * h);
+          xv[j][h].x = xv[j][h].x * rn * gg.x;
+          xv[j][h].y = xv[j][h].y * rn * gg.y;
+        }
+      }
     }
 #pragma unroll
     for (int j = 0; j < kSKSteps; ++j) {
-      const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
-      float v[4] = {x_at(kk), x_at(kk + 1), x_at(kk + 8), x_at(kk + 9)};
-      if (PRO == PRO_EMBED_NORM && blockIdx.x == 0 && g < S) {
-        const int ee[4] = {kk, kk + 1, kk + 8, kk + 9};
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (ee[u] < K) a.x_store[(int64_t)g * K + ee[u]] = v[u];
-      }
-      if (PRO != PRO_PLAIN) {
-        const int ee[4] = {kk, kk + 1, kk + 8, kk + 9};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v[u] = (ee[u] < K) ? v[u] * rn * __ldg(a.gain + ee[u]) : 0.f;
-      }
+      float v[4] = {xv[j][0].x, xv[j][0].y, xv[j][1].x, xv[j][1].y};
       if (a.act_bf16) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) v[u] = round_bf16(v[u]);
@@ -241,11 +307,9 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     }
   };
 
-  // epilogue state: thread i < 64 owns (slot i / 8, row i % 8) of every tile
-  const int es = tid >> 3, er = tid & 7;
-  float bv = -INFINITY;
-  int bi = 0x7fffffff;
-  auto epilogue = [&](int r0, float v) {  // v = Y[r0 + er][es] (tid < 64)
+  // epilogue of one tile: the warp that completes it calls this twice, lane l holding
+  // output i = l + 32h = (slot i / 8, row r0 + i % 8); all 32 lanes call it together
+  auto epilogue = [&](int r0, int es, int er, float v) {
     const int r = r0 + er;
     if (F == MIE_FMT_I8 && r < M) v *= reinterpret_cast<const float *>(m.s)[r];
     if constexpr (EPI == EPI_STORE) {
@@ -262,7 +326,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
         const int h = u / h2, i = u % h2;
         float x0 = v, y1 = x1;
         if (h < a.Hq + a.Hkv && sh.pos_ok[es]) {
-          const float c = a.rope_cos[(int64_t)sh.pos[es] * h2 + i], sn = a.rope_sin[(int64_t)sh.pos[es] * h2 + i];
+          const float c = sh.rc[es][i], sn = sh.rsn[es][i];
           const float r0v = x0 * c - y1 * sn, r1v = y1 * c + x0 * sn;
           x0 = r0v;
           y1 = r1v;
@@ -281,18 +345,33 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
         }
       }
     } else if constexpr (EPI == EPI_ARGMAX) {
+      unsigned long long key = 0ull;
       if (es < S && r < M) {
         if (a.sp->logits_out) a.sp->logits_out[(int64_t)es * M + r] = v;
-        if (better(v, r, bv, bi)) { bv = v; bi = r; }
+        key = argmax_key(v, r);
       }
+#pragma unroll
+      for (int o = 1; o < kSRows; o <<= 1) {  // the 8 lanes of one slot
+        const unsigned long long ok2 = __shfl_xor_sync(0xffffffffu, key, o);
+        key = ok2 > key ? ok2 : key;
+      }
+      if (er == 0 && es < S && key) atomicMax(&sh.best[es], key);
     }
   };
 
+  // Stage loop without CTA barriers: each warp posts its partial of the stage's tile and
+  // counts itself done in shared memory; the last warp of the stage sums the eight
+  // partials in a fixed order and finishes the tile.  Every warp releases the ring slot
+  // after that, so a slot's partials are read before its next stage can be written.
   bool ok = true;
   int s = 0;
   const uint32_t ring = smem_u32(smem);
   for (int q = 0; q < pl.KS; ++q) {
     load_slice(q);
+    if (q == 0) {
+      SSync::sync();
+      if (tid == 0) s_x_ready = 1;  // the producer may fill the rest of the ring
+    }
     const int nk = min(kSSlice, Kp - q * kSSlice) / 16;  // k-steps of this slice
     for (int tl = 0; tl < n_my; ++tl, ++s) {
       const int slot = s % pl.nst, k = s / pl.nst;
@@ -301,36 +380,54 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
         s_abort = 1;
         latch_error(a.err, ERR_TIMEOUT);
       }
-      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      // four independent accumulators: even / odd k-steps x hi / lo
+      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+      float c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok) {
         const uint32_t base = ring + (uint32_t)slot * pl.stage_bytes + (uint32_t)g * pl.pitch + (uint32_t)(2 * t) * ES;
 #pragma unroll
-        for (int j = 0; j < kSKSteps; ++j) {
-          const int ks = warp + kSW * j;
-          if (ks < nk) {
-            const uint32_t ad = base + (uint32_t)(ks * 16) * ES;
+        for (int j = 0; j < kSKSteps; j += 2) {
+          const int ks0 = warp + kSW * j, ks1 = ks0 + kSW;
+          if (ks0 < nk) {
+            const uint32_t ad = base + (uint32_t)(ks0 * 16) * ES;
             const uint32_t b0 = b_word<F>(ad), b1 = b_word<F>(ad + 8 * ES);
-            mma_bf16_16816(c, ah0[j], ah2[j], b0, b1);
-            mma_bf16_16816(c, al0[j], al2[j], b0, b1);
+            mma_bf16_16816(c0, ah0[j], ah2[j], b0, b1);
+            mma_bf16_16816(c1, al0[j], al2[j], b0, b1);
+          }
+          if (ks1 < nk) {
+            const uint32_t ad = base + (uint32_t)(ks1 * 16) * ES;
+            const uint32_t b0 = b_word<F>(ad), b1 = b_word<F>(ad + 8 * ES);
+            mma_bf16_16816(c2, ah0[j + 1], ah2[j + 1], b0, b1);
+            mma_bf16_16816(c3, al0[j + 1], al2[j + 1], b0, b1);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty_bar[slot]);
       // c[0], c[1] = Y[row 2t, 2t+1][slot g] of this warp's k-steps
-      float (*red)[kMaxSlots][kSRows] = sh.red[s & 1];
-      red[warp][g][2 * t] = c[0];
-      red[warp][g][2 * t + 1] = c[1];
-      SSync::sync();
-      if (tid < kMaxSlots * kSRows) {
-        float v = 0.f;
+      sh.red[slot][warp][g][2 * t] = (c0[0] + c2[0]) + (c1[0] + c3[0]);
+      sh.red[slot][warp][g][2 * t + 1] = (c0[1] + c2[1]) + (c1[1] + c3[1]);
+      __threadfence_block();
+      __syncwarp();
+      unsigned prev = 0u;
+      if (lane == 0) prev = atomicAdd(&sh.cnt[slot], 1u);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == kSW - 1) {  // the last warp of this stage
+        __threadfence_block();
+        const int r0 = (tt0 + tl) * kSRows;
 #pragma unroll
-        for (int w = 0; w < kSW; ++w) v += red[w][es][er];
-        const bool multi = pl.KS > 1;
-        if (multi && q > 0) v += sh.acc[tl][es][er];
-        if (q + 1 < pl.KS) sh.acc[tl][es][er] = v;
-        else epilogue((tt0 + tl) * kSRows, v);  // warps 0 and 1 whole: the pair shuffles see every lane
+        for (int h = 0; h < 2; ++h) {
+          const int i = lane + 32 * h, es = i >> 3, er = i & 7;
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < kSW; ++w) v += sh.red[slot][w][es][er];
+          if (q > 0) v += sh.acc[tl][es][er];
+          if (q + 1 < pl.KS) sh.acc[tl][es][er] = v;
+          else epilogue(r0, es, er, v);
+        }
+        if (lane == 0) sh.cnt[slot] = 0u;
+        __threadfence_block();
+        __syncwarp();
       }
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
     }
   }
   if (SSync::any(!ok || s_abort)) {
@@ -342,15 +439,12 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     return;
   }
   if constexpr (EPI == EPI_ARGMAX) {
-    // per slot: best of this CTA over its 8 row lanes, then the last CTA over all CTAs
-    if (tid < kMaxSlots * kSRows) {
-#pragma unroll
-      for (int o = 1; o < kSRows; o <<= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-      }
-      if (er == 0) a.am_part[(int64_t)es * gridDim.x + blockIdx.x] = make_float2(bv, __int_as_float(bi));
+    // per slot: this CTA's best (shared-memory key), then the last CTA over all CTAs
+    if (tid < kMaxSlots) {
+      float bv;
+      int bi;
+      argmax_unkey(sh.best[tid], bv, bi);
+      a.am_part[(int64_t)tid * gridDim.x + blockIdx.x] = make_float2(bv, __int_as_float(bi));
     }
     __threadfence();
     SSync::sync();
@@ -447,6 +541,7 @@ mie_status slots_gemv_supported(const DevMat &m, int pro) {
   if (m.fmt != MIE_FMT_BF16 && m.fmt != MIE_FMT_I8)
     return fail(MIE_E_SHAPE, "few-slot step: weight format %d (bf16 and int8 are built)", m.fmt);
   if (m.kp % 16) return fail(MIE_E_SHAPE, "few-slot step: padded width %d is not a multiple of 16", m.kp);
+  if (m.cols % 2) return fail(MIE_E_SHAPE, "few-slot step: odd input length %d (inputs are read in pairs)", m.cols);
   if (pro != PRO_PLAIN && m.cols > kSSlice)
     return fail(MIE_E_SHAPE, "few-slot step: RMSNorm over %d > %d columns", m.cols, kSSlice);
   if (((uintptr_t)m.w & 15) || (m.row_bytes & 15)) return fail(MIE_E_SHAPE, "few-slot step: unaligned rows");

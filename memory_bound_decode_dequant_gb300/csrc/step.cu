@@ -368,17 +368,6 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
 // chunk.  The softmax is the same two-pass definition, evaluated per stage with the
 // running maximum carried across stages.
 
-constexpr int kChunkTok = 256;  // tokens of one attention stage at most
-
-template <int G, int HD>
-struct RingAttnSmem {
-  float q[G * HD];
-  float kn[HD], vn[HD];   // the current token's k and v (bf16-exact)
-  float s[G][kChunkTok];  // scores, then probabilities (zero past the chunk up to a multiple of 4)
-  float m[G], l[G], corr[G];
-  unsigned last;
-};
-
 // Blocks per attention split of the persistent step: 32 tokens, so that the context of
 // one KV head spreads over several CTAs (the passes over one 128-token chunk cost about
 // 6,300 cycles on one CTA; a 32-token split about a quarter of that), merged by the last
@@ -394,9 +383,8 @@ __host__ __device__ inline int attn_stage_blocks(uint32_t slot_bytes, int bs, in
 
 template <int G, int HD>
 __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, int ctx, const Ring &ring,
-                               int &s_global, RingAttnSmem<G, HD> &sm, const StepConst &sc, const PersistArgs &pa) {
+                               int &s_global, ChunkSmem<G, HD> &sm, const StepConst &sc, const PersistArgs &pa) {
   constexpr int NO = (G * HD + kPCT - 1) / kPCT;  // outputs per thread
-  constexpr int NCH = HD / 8;                      // 16-byte chunks of a key row
   static_assert(2 * HD <= kPCT, "one thread per element of the current token's k and v");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nblk = (ctx + at.bs - 1) / at.bs;
@@ -413,7 +401,6 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
   float o[NO];
 #pragma unroll
   for (int j = 0; j < NO; ++j) o[j] = 0.f;
-  const uint32_t qa = smem_u32(sm.q), sa = smem_u32(&sm.s[0][0]);
   bool ok = true;
   for (int cb = b0; cb < b1; cb += cap, ++s_global) {
     const int slot = s_global % ring.nst, k = s_global / ring.nst;
@@ -433,71 +420,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
         else if (tid < 2 * HD) sts16(vbase + off + (tid - HD) * 2, (uint16_t)(__float_as_uint(sm.vn[tid - HD]) >> 16));
         ConsSync::sync();
       }
-      // (1) scores
-      for (int p = tid; p < G * ntok; p += kPCT) {
-        const int h = p / ntok, t = p - h * ntok;
-        const uint32_t krow = kbase + (uint32_t)t * (HD * 2), qrow = qa + (uint32_t)h * (HD * 4);
-        float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
-#pragma unroll
-        for (int c0 = 0; c0 < NCH; ++c0) {
-          const int c = (c0 + lane) % NCH;
-          const uint4 kw = lds128(krow + c * 16);
-          const float4 qa0 = lds128f(qrow + c * 32), qa1 = lds128f(qrow + c * 32 + 16);
-          d0 = fmaf(qa0.x, __uint_as_float(kw.x << 16), d0);
-          d1 = fmaf(qa0.y, __uint_as_float(kw.x & 0xffff0000u), d1);
-          d2 = fmaf(qa0.z, __uint_as_float(kw.y << 16), d2);
-          d3 = fmaf(qa0.w, __uint_as_float(kw.y & 0xffff0000u), d3);
-          d0 = fmaf(qa1.x, __uint_as_float(kw.z << 16), d0);
-          d1 = fmaf(qa1.y, __uint_as_float(kw.z & 0xffff0000u), d1);
-          d2 = fmaf(qa1.z, __uint_as_float(kw.w << 16), d2);
-          d3 = fmaf(qa1.w, __uint_as_float(kw.w & 0xffff0000u), d3);
-        }
-        sm.s[h][t] = ((d0 + d1) + (d2 + d3)) * at.scale;
-      }
-      ConsSync::sync();
-      // (2) softmax statistics, one warp per head
-      if (warp < G) {
-        const int h = warp;
-        float mx = -INFINITY;
-        for (int t = lane; t < ntok; t += 32) mx = fmaxf(mx, sm.s[h][t]);
-        mx = warp_max(mx);
-        const float m_old = sm.m[h], m_new = fmaxf(m_old, mx);
-        float sum = 0.f;
-        const int npad = (ntok + 3) & ~3;
-        for (int t = lane; t < npad; t += 32) {
-          const float pr = (t < ntok) ? expf(sm.s[h][t] - m_new) : 0.f;
-          sm.s[h][t] = pr;
-          sum += pr;
-        }
-        sum = warp_sum(sum);
-        if (lane == 0) {
-          const float c = (m_old == -INFINITY) ? 0.f : expf(m_old - m_new);
-          sm.corr[h] = c;
-          sm.l[h] = sm.l[h] * c + sum;
-          sm.m[h] = m_new;
-        }
-      }
-      ConsSync::sync();
-      // (3) outputs
-#pragma unroll
-      for (int j = 0; j < NO; ++j) {
-        const int i = tid + j * kPCT;
-        if (i < G * HD) {
-          const int h = i / HD, d = i % HD;
-          float acc = o[j] * sm.corr[h];
-          const uint32_t prow = sa + (uint32_t)h * (kChunkTok * 4), vcol = vbase + d * 2;
-          for (int t = 0; t < ntok; t += 4) {
-            const float4 p4 = lds128f(prow + t * 4);
-            const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int tt = min(t + u, ntok - 1);  // past the chunk the probability is 0
-              acc = fmaf(pv[u], __uint_as_float(lds16(vcol + (uint32_t)tt * (HD * 2)) << 16), acc);
-            }
-          }
-          o[j] = acc;
-        }
-      }
+      chunk_passes<G, HD, kPCT, ConsSync>(kbase, vbase, ntok, at.scale, sm, o);
     }
     fence_proxy_async_smem();  // the patch above was a generic write into a bulk-copy slot
     __syncwarp();
@@ -537,7 +460,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
 template <int G, int HD>
 __device__ bool attn_phase(const AttnArgs &at, const Ring &ring, int &s_global, float *scratch, const StepConst &sc,
                            const PersistArgs &pa) {
-  auto &sm = *reinterpret_cast<RingAttnSmem<G, HD> *>(scratch);
+  auto &sm = *reinterpret_cast<ChunkSmem<G, HD> *>(scratch);
   const int ctx = sc.ctx;
   const int nblk = (ctx + at.bs - 1) / at.bs;
   const int nsplit = attn_nsplit(nblk, at.n_splits, ring_attn_blocks_per_split(at.bs));
@@ -869,9 +792,9 @@ static const void *pick_kernel(int fl, int fh, int G, int HD) {
 
 size_t persist_attn_smem(int G, int HD) {
   switch (G * 1000 + HD) {
-    case 4032: return sizeof(RingAttnSmem<4, 32>);
-    case 8064: return sizeof(RingAttnSmem<8, 64>);
-    case 4064: return sizeof(RingAttnSmem<4, 64>);
+    case 4032: return sizeof(ChunkSmem<4, 32>);
+    case 8064: return sizeof(ChunkSmem<8, 64>);
+    case 4064: return sizeof(ChunkSmem<4, 64>);
   }
   return 0;
 }
