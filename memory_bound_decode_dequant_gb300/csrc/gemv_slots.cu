@@ -46,8 +46,9 @@ struct SSync {
   }
 };
 
+// Not volatile: a pure function of its registers, so the compiler may schedule it.
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -385,20 +386,25 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       float c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok) {
         const uint32_t base = ring + (uint32_t)slot * pl.stage_bytes + (uint32_t)g * pl.pitch + (uint32_t)(2 * t) * ES;
+        // B words of eight k-steps are loaded in one batch (k-steps past the slice read
+        // its first k-step: their A fragments are zero), then the MMAs run
+        constexpr int H = kSKSteps / 2;
 #pragma unroll
-        for (int j = 0; j < kSKSteps; j += 2) {
-          const int ks0 = warp + kSW * j, ks1 = ks0 + kSW;
-          if (ks0 < nk) {
-            const uint32_t ad = base + (uint32_t)(ks0 * 16) * ES;
-            const uint32_t b0 = b_word<F>(ad), b1 = b_word<F>(ad + 8 * ES);
-            mma_bf16_16816(c0, ah0[j], ah2[j], b0, b1);
-            mma_bf16_16816(c1, al0[j], al2[j], b0, b1);
+        for (int h0 = 0; h0 < kSKSteps; h0 += H) {
+          uint32_t b0[H], b1[H];
+#pragma unroll
+          for (int j = 0; j < H; ++j) {
+            const int ks = warp + kSW * (h0 + j);
+            const uint32_t ad = base + (uint32_t)((ks < nk ? ks : 0) * 16) * ES;
+            b0[j] = b_word<F>(ad);
+            b1[j] = b_word<F>(ad + 8 * ES);
           }
-          if (ks1 < nk) {
-            const uint32_t ad = base + (uint32_t)(ks1 * 16) * ES;
-            const uint32_t b0 = b_word<F>(ad), b1 = b_word<F>(ad + 8 * ES);
-            mma_bf16_16816(c2, ah0[j + 1], ah2[j + 1], b0, b1);
-            mma_bf16_16816(c3, al0[j + 1], al2[j + 1], b0, b1);
+#pragma unroll
+          for (int j = 0; j < H; j += 2) {
+            mma_bf16_16816(c0, ah0[h0 + j], ah2[h0 + j], b0[j], b1[j]);
+            mma_bf16_16816(c1, al0[h0 + j], al2[h0 + j], b0[j], b1[j]);
+            mma_bf16_16816(c2, ah0[h0 + j + 1], ah2[h0 + j + 1], b0[j + 1], b1[j + 1]);
+            mma_bf16_16816(c3, al0[h0 + j + 1], al2[h0 + j + 1], b0[j + 1], b1[j + 1]);
           }
         }
       }
