@@ -373,7 +373,7 @@ __device__ __forceinline__ void chunk_passes(uint32_t kbase, uint32_t vbase, int
                                              ChunkSmem<G, HD> &sm, float (&o)[(G * HD + NT - 1) / NT]) {
   constexpr int NO = (G * HD + NT - 1) / NT;
   constexpr int NCH = HD / 8;  // 16-byte chunks of a key row
-  static_assert(NT / 32 >= G, "one warp per head in the statistics pass");
+
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t qa = smem_u32(sm.q), sa = smem_u32(&sm.s[0][0]);
   // (1) scores
@@ -399,8 +399,7 @@ __device__ __forceinline__ void chunk_passes(uint32_t kbase, uint32_t vbase, int
   }
   Sync::sync();
   // (2) softmax statistics, one warp per head
-  if (warp < G) {
-    const int h = warp;
+  for (int h = warp; h < G; h += NT / 32) {
     float mx = -INFINITY;
     for (int t = lane; t < ntok; t += 32) mx = fmaxf(mx, sm.s[h][t]);
     mx = warp_max(mx);
