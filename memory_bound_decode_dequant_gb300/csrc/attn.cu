@@ -77,7 +77,7 @@ struct CSync {
 };
 
 template <int G, int HD>
-__global__ void __launch_bounds__(kCThreads) attn_chunk_kernel(const AttnArgs a_in) {
+__global__ void __launch_bounds__(kCThreads, 2) attn_chunk_kernel(const AttnArgs a_in) {
   constexpr int NO = (G * HD + kCThreads - 1) / kCThreads;
   extern __shared__ __align__(128) uint8_t cbuf[];  // 2 x [K: kCTok*HD*2 bytes][V: same]
   __shared__ ChunkSmem<G, HD> sm;

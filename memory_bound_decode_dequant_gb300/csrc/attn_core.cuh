@@ -355,60 +355,82 @@ __device__ void attn_store(const AttnArgs &a, int g, int s, int nsplit, const fl
 
 constexpr int kChunkTok = 256;  // tokens of one chunk at most
 
+// Shared scratch of the chunk passes.  buf holds the per-part scores in pass 1 and the
+// per-token-group partial outputs in pass 3 (sized for up to 256 threads).
 template <int G, int HD>
 struct ChunkSmem {
+  static constexpr int kParts = HD / 32;                       // 32-dim parts of a key row
+  static constexpr int kGroupsMax = 512 / HD;                  // token groups of pass 3 at 256 threads
+  static constexpr int kBuf = (kParts * kChunkTok > kGroupsMax * HD ? kParts * kChunkTok : kGroupsMax * HD) * G;
   float q[G * HD];
-  float kn[HD], vn[HD];   // persistent step: the current token's k and v (bf16-exact)
-  float s[G][kChunkTok];  // scores, then probabilities (zero past the chunk up to a multiple of 4)
+  float kn[HD], vn[HD];          // persistent step: the current token's k and v (bf16-exact)
+  float pt[kChunkTok][G];        // probabilities, [token][head]
+  float buf[kBuf];
   float m[G], l[G], corr[G];
   unsigned last;
 };
 
 // One chunk of ntok (1..kChunkTok) tokens.  sm.q holds the queries, sm.m / sm.l the
 // running statistics (-inf / 0 before the first chunk); o[j] is this thread's output
-// i = tid + j*NT of the G*HD outputs, rescaled and accumulated.  NT threads (warps
-// 0..NT/32-1, at least G of them) take part; Sync is a barrier over them.
+// i = tid + j*NT of the G*HD outputs, rescaled and accumulated.  NT threads take part;
+// Sync is a barrier over them.  The caller synchronises before the next chunk.
 template <int G, int HD, int NT, class Sync>
 __device__ __forceinline__ void chunk_passes(uint32_t kbase, uint32_t vbase, int ntok, float scale,
                                              ChunkSmem<G, HD> &sm, float (&o)[(G * HD + NT - 1) / NT]) {
   constexpr int NO = (G * HD + NT - 1) / NT;
-  constexpr int NCH = HD / 8;  // 16-byte chunks of a key row
-
+  constexpr int P = ChunkSmem<G, HD>::kParts;
+  constexpr int DP = HD / 2;        // dim pairs
+  constexpr int TG = NT / DP;       // token groups of pass 3
+  constexpr int NW = NT / 32;
+  static_assert(TG <= ChunkSmem<G, HD>::kGroupsMax && TG >= 1, "pass-3 groups fit the buffer");
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const uint32_t qa = smem_u32(sm.q), sa = smem_u32(&sm.s[0][0]);
-  // (1) scores
-  for (int p = tid; p < G * ntok; p += NT) {
-    const int h = p / ntok, t = p - h * ntok;
-    const uint32_t krow = kbase + (uint32_t)t * (HD * 2), qrow = qa + (uint32_t)h * (HD * 4);
-    float d0 = 0.f, d1 = 0.f, d2 = 0.f, d3 = 0.f;
+  const uint32_t qa = smem_u32(sm.q);
+  // (1) scores: one (token, 32-dim part) per item, all heads at once
+  for (int it = tid; it < ntok * P; it += NT) {
+    const int t = it / P, part = it % P;
+    const uint32_t krow = kbase + (uint32_t)t * (HD * 2) + part * 64;
+    uint4 kw[4];
 #pragma unroll
-    for (int c0 = 0; c0 < NCH; ++c0) {
-      const int c = (c0 + lane) % NCH;
-      const uint4 kw = lds128(krow + c * 16);
-      const float4 qa0 = lds128f(qrow + c * 32), qa1 = lds128f(qrow + c * 32 + 16);
-      d0 = fmaf(qa0.x, __uint_as_float(kw.x << 16), d0);
-      d1 = fmaf(qa0.y, __uint_as_float(kw.x & 0xffff0000u), d1);
-      d2 = fmaf(qa0.z, __uint_as_float(kw.y << 16), d2);
-      d3 = fmaf(qa0.w, __uint_as_float(kw.y & 0xffff0000u), d3);
-      d0 = fmaf(qa1.x, __uint_as_float(kw.z << 16), d0);
-      d1 = fmaf(qa1.y, __uint_as_float(kw.z & 0xffff0000u), d1);
-      d2 = fmaf(qa1.z, __uint_as_float(kw.w << 16), d2);
-      d3 = fmaf(qa1.w, __uint_as_float(kw.w & 0xffff0000u), d3);
+    for (int c = 0; c < 4; ++c) kw[c] = lds128(krow + ((c + lane) & 3) * 16);
+    float acc[G][2];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      acc[h][0] = acc[h][1] = 0.f;
+      const uint32_t qrow = qa + (uint32_t)(h * HD + part * 32) * 4;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const uint32_t qo = qrow + ((c + lane) & 3) * 32;
+        const float4 q0 = lds128f(qo), q1 = lds128f(qo + 16);
+        acc[h][0] = fmaf(q0.x, __uint_as_float(kw[c].x << 16), acc[h][0]);
+        acc[h][1] = fmaf(q0.y, __uint_as_float(kw[c].x & 0xffff0000u), acc[h][1]);
+        acc[h][0] = fmaf(q0.z, __uint_as_float(kw[c].y << 16), acc[h][0]);
+        acc[h][1] = fmaf(q0.w, __uint_as_float(kw[c].y & 0xffff0000u), acc[h][1]);
+        acc[h][0] = fmaf(q1.x, __uint_as_float(kw[c].z << 16), acc[h][0]);
+        acc[h][1] = fmaf(q1.y, __uint_as_float(kw[c].z & 0xffff0000u), acc[h][1]);
+        acc[h][0] = fmaf(q1.z, __uint_as_float(kw[c].w << 16), acc[h][0]);
+        acc[h][1] = fmaf(q1.w, __uint_as_float(kw[c].w & 0xffff0000u), acc[h][1]);
+      }
     }
-    sm.s[h][t] = ((d0 + d1) + (d2 + d3)) * scale;
+#pragma unroll
+    for (int h = 0; h < G; ++h) sm.buf[(part * G + h) * kChunkTok + t] = acc[h][0] + acc[h][1];
   }
   Sync::sync();
-  // (2) softmax statistics, one warp per head
-  for (int h = warp; h < G; h += NT / 32) {
+  // (2) softmax statistics, one warp per head; probabilities to pt[token][head]
+  for (int h = warp; h < G; h += NW) {
+    auto score = [&](int t) {
+      float v = 0.f;
+#pragma unroll
+      for (int part = 0; part < P; ++part) v += sm.buf[(part * G + h) * kChunkTok + t];
+      return v * scale;
+    };
     float mx = -INFINITY;
-    for (int t = lane; t < ntok; t += 32) mx = fmaxf(mx, sm.s[h][t]);
+    for (int t = lane; t < ntok; t += 32) mx = fmaxf(mx, score(t));
     mx = warp_max(mx);
     const float m_old = sm.m[h], m_new = fmaxf(m_old, mx);
     float sum = 0.f;
-    const int npad = (ntok + 3) & ~3;
-    for (int t = lane; t < npad; t += 32) {
-      const float pr = (t < ntok) ? expf(sm.s[h][t] - m_new) : 0.f;
-      sm.s[h][t] = pr;
+    for (int t = lane; t < ntok; t += 32) {
+      const float pr = expf(score(t) - m_new);
+      sm.pt[t][h] = pr;
       sum += pr;
     }
     sum = warp_sum(sum);
@@ -420,23 +442,51 @@ __device__ __forceinline__ void chunk_passes(uint32_t kbase, uint32_t vbase, int
     }
   }
   Sync::sync();
-  // (3) outputs
+  // (3) outputs: thread (dim pair dp, token group tg) over tokens tg, tg + TG, ...
+  if (tid < TG * DP) {
+    const int dp = tid % DP, tg = tid / DP;
+    float a[G][2];
+#pragma unroll
+    for (int h = 0; h < G; ++h) a[h][0] = a[h][1] = 0.f;
+    const uint32_t vcol = vbase + dp * 4, pa = smem_u32(&sm.pt[0][0]);
+    for (int t = tg; t < ntok; t += TG) {
+      const uint32_t vw = lds32(vcol + (uint32_t)t * (HD * 2));
+      const float v0 = __uint_as_float(vw << 16), v1 = __uint_as_float(vw & 0xffff0000u);
+      float pv[G];
+      if constexpr (G % 4 == 0) {
+#pragma unroll
+        for (int h = 0; h < G; h += 4) {
+          const float4 p4 = lds128f(pa + (uint32_t)(t * G + h) * 4);
+          pv[h] = p4.x;
+          pv[h + 1] = p4.y;
+          pv[h + 2] = p4.z;
+          pv[h + 3] = p4.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < G; ++h) pv[h] = sm.pt[t][h];
+      }
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        a[h][0] = fmaf(pv[h], v0, a[h][0]);
+        a[h][1] = fmaf(pv[h], v1, a[h][1]);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      sm.buf[(tg * G + h) * HD + 2 * dp] = a[h][0];
+      sm.buf[(tg * G + h) * HD + 2 * dp + 1] = a[h][1];
+    }
+  }
+  Sync::sync();
 #pragma unroll
   for (int j = 0; j < NO; ++j) {
     const int i = tid + j * NT;
     if (i < G * HD) {
       const int h = i / HD, d = i % HD;
       float acc = o[j] * sm.corr[h];
-      const uint32_t prow = sa + (uint32_t)h * (kChunkTok * 4), vcol = vbase + d * 2;
-      for (int t = 0; t < ntok; t += 4) {
-        const float4 p4 = lds128f(prow + t * 4);
-        const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int tt = min(t + u, ntok - 1);  // past the chunk the probability is 0
-          acc = fmaf(pv[u], __uint_as_float(lds16(vcol + (uint32_t)tt * (HD * 2)) << 16), acc);
-        }
-      }
+#pragma unroll 4
+      for (int tg = 0; tg < TG; ++tg) acc += sm.buf[(tg * G + h) * HD + d];
       o[j] = acc;
     }
   }

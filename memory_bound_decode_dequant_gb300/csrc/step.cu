@@ -371,11 +371,11 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
 // chunk.  The softmax is the same two-pass definition, evaluated per stage with the
 // running maximum carried across stages.
 
-// Blocks per attention split of the persistent step: 32 tokens, so that the context of
-// one KV head spreads over several CTAs (the passes over one 128-token chunk cost about
-// 6,300 cycles on one CTA; a 32-token split about a quarter of that), merged by the last
-// split of the head.
-__host__ __device__ inline int ring_attn_blocks_per_split(int bs) { return bs >= 32 ? 1 : 32 / bs; }
+// Blocks per attention split of the persistent step: 256 tokens (two 128-token ring
+// stages at hd 64), so up to that context one CTA per KV head finishes attention
+// without a merge (a merge costs a fence, an atomic and a round trip, ~2.5 us); longer
+// contexts spread over more CTAs and the last split of each head merges.
+__host__ __device__ inline int ring_attn_blocks_per_split(int bs) { return bs >= 256 ? 1 : 256 / bs; }
 
 // Blocks per attention stage: as many as a ring slot holds, at most kChunkTok tokens.
 __host__ __device__ inline int attn_stage_blocks(uint32_t slot_bytes, int bs, int hd) {
