@@ -261,8 +261,12 @@ mie_status mie_decode_continue(mie_ctx *ctx, int n_steps);
 
 /* Few-slot step ([MIE] "Continuous batching"): every slot s advances one token,
  * tokens[s] at pos[s] (host arrays), through row s of block_tables (device int32
- * [n_slots][max_blocks]).  The weights are read once for all slots.  logits_out:
- * device [n_slots][vocab] or NULL; argmax_out: device [n_slots] or NULL. */
+ * [n_slots][max_blocks]).  The weights are read once for all slots (tensor-core MMAs
+ * over the slots' input vectors, split into bf16 hi + lo).  logits_out: device
+ * [n_slots][vocab] or NULL; argmax_out: device [n_slots] or NULL.  Layers and head in
+ * bf16, int8 or Q4_0 with even input lengths; otherwise MIE_E_SHAPE.  The first call
+ * captures the few-slot step into its own CUDA graph.  Slots never write into a block
+ * another slot's table shares (block-aligned prefixes; see mie_pool_writable). */
 mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int32_t *tokens,
                                  const int32_t *pos, const int32_t *block_tables, int max_blocks,
                                  float *logits_out, int32_t *argmax_out);

@@ -12,6 +12,9 @@
 // x is fp32 in the method, so each x value is split into x_hi = bf16(x) and
 // x_lo = bf16(x - x_hi) and every tile takes two MMAs: the products are exact in
 // fp32 and x keeps about 16 significant bits (int8 weights become bf16 exactly).
+// Q4_0: the B values are the codes minus 8 (exact in bf16); each warp owns whole
+// 32-column blocks, accumulates a block's MMAs apart and adds them times the f16 block
+// scale of each output row.
 //
 // A producer warp streams stages of 8 weight rows x one 2048-column slice through a
 // ring in shared memory (one bulk copy per row into rows padded by 16 bytes, so the
@@ -71,6 +74,10 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_
 template <int F>
 __device__ __forceinline__ uint32_t b_word(uint32_t addr);
 template <>
+__device__ __forceinline__ uint32_t b_word<MIE_FMT_Q4_0>(uint32_t) {  // not used: Q4_0 has its own loop
+  return 0u;
+}
+template <>
 __device__ __forceinline__ uint32_t b_word<MIE_FMT_BF16>(uint32_t addr) {
   return lds32(addr);
 }
@@ -79,6 +86,19 @@ __device__ __forceinline__ uint32_t b_word<MIE_FMT_I8>(uint32_t addr) {
   const uint32_t v = lds16(addr);
   const int q0 = (int)(int8_t)(v & 0xffu), q1 = (int)(int8_t)(v >> 8);
   return bf16x2_bits((float)q0, (float)q1);  // exact: |q| <= 127
+}
+
+// The k-step of a slice that warp `warp` handles as its j-th (0..kSKSteps-1): the slice's
+// 128 k-steps are dealt round robin, or, for Q4_0, as whole blocks (two k-steps each).
+template <int F>
+__device__ __forceinline__ int kstep_of(int warp, int j) {
+  if constexpr (F == MIE_FMT_Q4_0) return 2 * (warp + kSW * (j >> 1)) + (j & 1);
+  return warp + kSW * j;
+}
+
+// bf16 bits of a Q4_0 code minus 8 (exact), two codes packed
+__device__ __forceinline__ uint32_t q4_pair(uint32_t n0, uint32_t n1) {
+  return bf16x2_bits((float)(int)n0 - 8.f, (float)(int)n1 - 8.f);
 }
 
 // Shared state of one CTA.
@@ -116,13 +136,15 @@ __device__ __forceinline__ void argmax_unkey(unsigned long long k, float &v, int
 struct SlotPlan {
   int nst = 0;
   uint32_t pitch = 0, stage_bytes = 0;  // padded row bytes in shared memory, bytes per slot
+  uint32_t sc_off = 0;                  // Q4_0: offset of the stage's scale rows (128 bytes each)
   int n_tiles = 0, KS = 1;
   size_t smem = 0;
 };
 
 template <int F, int PRO, int EPI>
 __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, const SlotPlan pl) {
-  constexpr int ES = (F == MIE_FMT_BF16) ? 2 : 1;  // bytes per weight
+  constexpr int ES = (F == MIE_FMT_BF16) ? 2 : 1;  // bytes per weight (bf16, int8)
+  constexpr bool Q4 = F == MIE_FMT_Q4_0;
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kSMaxNst], empty_bar[kSMaxNst];
   __shared__ SlotShared sh;
@@ -171,12 +193,25 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
         if (s_abort) break;
         const int q = s / n_my, r0 = (tt0 + s % n_my) * kSRows;
         const int rows = min(kSRows, M - r0);
-        const uint32_t cb = (uint32_t)(min(kSSlice, Kp - q * kSSlice) * ES);
-        mbar_expect_tx(&full_bar[slot], rows * cb);
         uint8_t *dst = smem + (size_t)slot * pl.stage_bytes;
-        for (int j = 0; j < rows; ++j)
-          bulk_load(dst + (size_t)j * pl.pitch, m.w + (int64_t)(r0 + j) * m.row_bytes + (int64_t)q * kSSlice * ES, cb,
-                    &full_bar[slot], pol);
+        if constexpr (Q4) {
+          const int nb = min(kSSlice, Kp - q * kSSlice) / 32;  // blocks of this slice
+          const uint32_t cb = (uint32_t)nb * 16, sb = (uint32_t)((nb + 7) / 8 * 8) * 2;  // scales: whole 16 B
+          mbar_expect_tx(&full_bar[slot], rows * (cb + sb));
+          for (int j = 0; j < rows; ++j) {
+            bulk_load(dst + (size_t)j * pl.pitch, m.w + (int64_t)(r0 + j) * m.row_bytes + (int64_t)q * (kSSlice / 32) * 16,
+                      cb, &full_bar[slot], pol);
+            bulk_load(dst + pl.sc_off + (size_t)j * 128,
+                      reinterpret_cast<const uint8_t *>(m.s) + ((int64_t)(r0 + j) * m.s_stride + q * (kSSlice / 32)) * 2,
+                      sb, &full_bar[slot], pol);
+          }
+        } else {
+          const uint32_t cb = (uint32_t)(min(kSSlice, Kp - q * kSSlice) * ES);
+          mbar_expect_tx(&full_bar[slot], rows * cb);
+          for (int j = 0; j < rows; ++j)
+            bulk_load(dst + (size_t)j * pl.pitch, m.w + (int64_t)(r0 + j) * m.row_bytes + (int64_t)q * kSSlice * ES, cb,
+                      &full_bar[slot], pol);
+        }
         s_issued = s + 1;
       }
       s_prod_done = 1;
@@ -251,14 +286,14 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     float2 xv[kSKSteps][2];
 #pragma unroll
     for (int j = 0; j < kSKSteps; ++j) {
-      const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
+      const int kk = q * kSSlice + kstep_of<F>(warp, j) * 16 + 2 * t;
       xv[j][0] = load_pair(kk);
       xv[j][1] = load_pair(kk + 8);
     }
     if (PRO == PRO_EMBED_NORM && blockIdx.x == 0 && g < S) {  // the residual stream starts as x
 #pragma unroll
       for (int j = 0; j < kSKSteps; ++j) {
-        const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
+        const int kk = q * kSSlice + kstep_of<F>(warp, j) * 16 + 2 * t;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int e = kk + 8 * h;
@@ -287,7 +322,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       const float rn = sh.rs[g];
 #pragma unroll
       for (int j = 0; j < kSKSteps; ++j) {
-        const int kk = q * kSSlice + (warp + kSW * j) * 16 + 2 * t;
+        const int kk = q * kSSlice + kstep_of<F>(warp, j) * 16 + 2 * t;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const float2 gg = gain_pair(kk + 8 * h);
@@ -384,7 +419,31 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       // four independent accumulators: even / odd k-steps x hi / lo
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       float c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
-      if (ok) {
+      if (ok && Q4) {
+        // whole blocks: b = warp + kSW * i, k-steps 2b (low nibbles) and 2b + 1 (high)
+        const uint32_t sbase = ring + (uint32_t)slot * pl.stage_bytes;
+        const uint32_t nrow = sbase + (uint32_t)g * pl.pitch + 2 * t;  // row g's bytes 2t, 2t + 1 of a block
+        const uint32_t srow = sbase + pl.sc_off + (uint32_t)(2 * t) * 128;  // scales of output rows 2t, 2t + 1
+#pragma unroll
+        for (int i = 0; i < kSKSteps / 2; ++i) {
+          const int b = warp + kSW * i;
+          if (2 * b < nk) {
+            const uint32_t w01 = lds16(nrow + b * 16), w89 = lds16(nrow + b * 16 + 8);
+            const float d0 = __half2float(__ushort_as_half((unsigned short)lds16(srow + b * 2)));
+            const float d1 = __half2float(__ushort_as_half((unsigned short)lds16(srow + 128 + b * 2)));
+            float ct[4] = {0.f, 0.f, 0.f, 0.f};
+            const uint32_t lb0 = q4_pair(w01 & 0xFu, (w01 >> 8) & 0xFu), lb1 = q4_pair(w89 & 0xFu, (w89 >> 8) & 0xFu);
+            const uint32_t hb0 = q4_pair((w01 >> 4) & 0xFu, (w01 >> 12) & 0xFu);
+            const uint32_t hb1 = q4_pair((w89 >> 4) & 0xFu, (w89 >> 12) & 0xFu);
+            mma_bf16_16816(ct, ah0[2 * i], ah2[2 * i], lb0, lb1);
+            mma_bf16_16816(ct, al0[2 * i], al2[2 * i], lb0, lb1);
+            mma_bf16_16816(ct, ah0[2 * i + 1], ah2[2 * i + 1], hb0, hb1);
+            mma_bf16_16816(ct, al0[2 * i + 1], al2[2 * i + 1], hb0, hb1);
+            c0[0] = fmaf(d0, ct[0], c0[0]);
+            c0[1] = fmaf(d1, ct[1], c0[1]);
+          }
+        }
+      } else if (ok) {
         const uint32_t base = ring + (uint32_t)slot * pl.stage_bytes + (uint32_t)g * pl.pitch + (uint32_t)(2 * t) * ES;
         // B words of eight k-steps are loaded in one batch (k-steps past the slice read
         // its first k-step: their A fragments are zero), then the MMAs run
@@ -492,11 +551,17 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
 
 static SlotPlan slot_plan(const DevMat &m, int grid) {
   SlotPlan p;
-  const int ES = (m.fmt == MIE_FMT_BF16) ? 2 : 1;
   p.KS = (m.kp + kSSlice - 1) / kSSlice;
   const int slice = min(kSSlice, m.kp);
-  p.pitch = (uint32_t)(slice * ES + 16);
-  p.stage_bytes = (uint32_t)((kSRows * p.pitch + 127) / 128 * 128);
+  if (m.fmt == MIE_FMT_Q4_0) {
+    p.pitch = (uint32_t)(slice / 32 * 16 + 16);
+    p.sc_off = (uint32_t)((kSRows * p.pitch + 15) / 16 * 16);
+    p.stage_bytes = (uint32_t)((p.sc_off + kSRows * 128 + 127) / 128 * 128);
+  } else {
+    const int ES = (m.fmt == MIE_FMT_BF16) ? 2 : 1;
+    p.pitch = (uint32_t)(slice * ES + 16);
+    p.stage_bytes = (uint32_t)((kSRows * p.pitch + 127) / 128 * 128);
+  }
   p.n_tiles = (m.rows + kSRows - 1) / kSRows;
   int dev = 0, max_smem = 0;
   cudaGetDevice(&dev);
@@ -544,8 +609,8 @@ static mie_status launch_slots_f(int pro, int epi, const GemvArgs &a, const Slot
 
 // Checks that the batched GEMV covers matrix m with prologue pro.
 mie_status slots_gemv_supported(const DevMat &m, int pro) {
-  if (m.fmt != MIE_FMT_BF16 && m.fmt != MIE_FMT_I8)
-    return fail(MIE_E_SHAPE, "few-slot step: weight format %d (bf16 and int8 are built)", m.fmt);
+  if (m.fmt != MIE_FMT_BF16 && m.fmt != MIE_FMT_I8 && m.fmt != MIE_FMT_Q4_0)
+    return fail(MIE_E_SHAPE, "few-slot step: weight format %d", m.fmt);
   if (m.kp % 16) return fail(MIE_E_SHAPE, "few-slot step: padded width %d is not a multiple of 16", m.kp);
   if (m.cols % 2) return fail(MIE_E_SHAPE, "few-slot step: odd input length %d (inputs are read in pairs)", m.cols);
   if (pro != PRO_PLAIN && m.cols > kSSlice)
@@ -565,6 +630,7 @@ mie_status launch_gemv_slots(int pro, int epi, const GemvArgs &a, cudaStream_t s
   const SlotPlan p = slot_plan(a.m, grid);
   if (a.m.fmt == MIE_FMT_BF16) return launch_slots_f<MIE_FMT_BF16>(pro, epi, a, p, grid, st, pdl);
   if (a.m.fmt == MIE_FMT_I8) return launch_slots_f<MIE_FMT_I8>(pro, epi, a, p, grid, st, pdl);
+  if (a.m.fmt == MIE_FMT_Q4_0) return launch_slots_f<MIE_FMT_Q4_0>(pro, epi, a, p, grid, st, pdl);
   return fail(MIE_E_SHAPE, "few-slot step: weight format %d", a.m.fmt);
 }
 

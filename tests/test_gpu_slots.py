@@ -2,7 +2,7 @@
 
 The oracle defines the batched step as independent single-slot steps, one per slot,
 each through its own block table of the shared pool.  Here four slots of a
-tiny-shaped decoder (bf16 or int8 weights) are prefilled by single-slot steps, slots 0
+tiny-shaped decoder (bf16, int8 or Q4_0 weights) are prefilled by single-slot steps, slots 0
 and 1 sharing a two-block prefix (refcount 2 in the host pool), then advanced together
 by batched steps, teacher-forced with the oracle's greedy tokens.  Tolerances as for
 the single-slot step: max |dlogit| <= 2e-2 * std(logits), argmax identical where the
@@ -115,7 +115,7 @@ def run_slots(orc, shape, n_slots, max_slots, prompts, n_gen, compare_kv=True):
     return gm
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "i8"])
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0"])
 def test_slots_match_single_slot_oracle(orc, fmt):
     shape = replace(synth.TINY, wfmt=fmt, head_fmt=fmt)
     run_slots(orc, shape, n_slots=4, max_slots=4, prompts=[40, 37, 21, 50], n_gen=6)
@@ -142,7 +142,7 @@ def test_slots_reject_bad_inputs_and_unbuilt_formats():
     with pytest.raises(mie.MieError) as e:  # position beyond the table
         gm.decode_step_slots(np.array([1, 2], np.int32), np.array([0, 4 * 16], np.int32), tdev, logits)
     assert e.value.status == 1
-    gq = build_gpu_model(synth.TINY, n_kv_blocks=8, max_pos=64, max_slots=2)
-    with pytest.raises(mie.MieError) as e:  # Q4_0 layers: the batched step is built for bf16 / int8
-        gq.decode_step_slots(np.array([1, 2], np.int32), np.array([0, 0], np.int32), tdev, logits)
-    assert e.value.status == 2
+    gq = build_gpu_model(synth.TINY, n_kv_blocks=8, max_pos=64, max_slots=2)  # Q4_0 layers
+    tq = torch.tensor([[0, 1, 2, 3], [4, 5, 6, 7]], dtype=torch.int32, device="cuda")
+    gq.decode_step_slots(np.array([1, 2], np.int32), np.array([0, 0], np.int32), tq, logits)
+    gq.sync()
