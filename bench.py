@@ -9,6 +9,11 @@ attention, LM head + argmax) replayed from the captured CUDA graph, token and po
 advanced on the device.  The weights (2.47 GB bf16) are far larger than the 129 MB L2,
 so nothing is served from L2 between steps.  Rank 0 prints one JSON line.
 
+--workload sweep: the stateless kernels alone -- GEMVs 3072x2048, 2048x2048, 16384x2048,
+2048x8192, 128256x2048 in bf16 / int8 / Q4_0, paged attention (32 q / 8 KV heads, hd 64)
+at ctx 512 / 2048 / 8192 over randomly permuted blocks, argmax over 128256 -- each
+replayed back to back from a CUDA graph over more than 1 GB of distinct inputs.
+
 --workload slots: the continuous-batching step instead -- 8 slots with contexts drawn
 from U[128, 4096], slots 0-3 sharing a refcounted 512-token prefix, block tables in
 random physical order from the host block pool, 256 steps with one slot retired and a
@@ -51,8 +56,15 @@ def parse():
                     help="timed steps of --workload slots (the workload's 256; fewer for profiling)")
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (a small case for profiling; 0 = all)")
-    ap.add_argument("--workload", default="step", choices=["step", "slots"],
-                    help="step: batch-1 decode (the headline); slots: 8-slot continuous batching")
+    ap.add_argument("--workload", default="step", choices=["step", "slots", "sweep"],
+                    help="step: batch-1 decode (the headline); slots: 8-slot continuous batching; "
+                         "sweep: the per-kernel sweep at the Llama-3.2-1B shapes")
+    ap.add_argument("--only", default="",
+                    help="sweep: run only the cases whose 'kind:name:fmt' label contains this text "
+                         "(e.g. gemv:lm_head:q4_0, attn:512, argmax)")
+    ap.add_argument("--sweep-bytes", type=float, default=1.1e9,
+                    help="sweep: bytes of distinct inputs each case rotates through")
+    ap.add_argument("--sweep-min", type=int, default=20, help="sweep: least number of input copies per case")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the dominant kernel (the profiling command)")
     return ap.parse_args()
@@ -545,8 +557,117 @@ def time_oracle_slots(shape, wl):
                       f"which defines its batched step; plain single-threaded C, K/V seeded"}
 
 
+# ----------------------------------------------------------------------------- per-kernel sweep
+
+def graph_time(torch, launches, reps: int = 5):
+    """Seconds per launch of a list of closures replayed from one CUDA graph (median)."""
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        for f in launches[:3]:
+            f(st)
+    st.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for f in launches:
+            f(st)
+    g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        with torch.cuda.stream(st):
+            g.replay()
+        e1.record(st)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3 / len(launches))
+    return statistics.median(times)
+
+
+def run_sweep(args):
+    import torch
+    import memory_bound_decode_dequant_gb300 as mie
+
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    peak, peak_kind = measured_peaks()
+    gen = torch.Generator(device="cuda").manual_seed(synth.SWEEP_SEED)
+    total, least = args.sweep_bytes, args.sweep_min
+    want = lambda label: args.only in label
+    out = {"metric": "per-kernel sweep (Llama-3.2-1B decode shapes)", "unit": "us / GB/s per launch",
+           "peak_gbs": peak, "peak_kind": peak_kind, "gemv": [], "attention": [], "argmax": None,
+           "method": "graph of back-to-back launches over > 1 GB of distinct inputs; median of 5 replays"}
+    with Clocks(int(os.environ.get("LOCAL_RANK", 0))) as clk:
+        for name, M, K in synth.SWEEP_GEMV:
+            if not any(want(f"gemv:{name}:{f}") for f in ("bf16", "i8", "q4_0")):
+                continue
+            w = torch.randn((M, K), generator=gen, device="cuda") * 0.02
+            x = torch.randn(K, generator=gen, device="cuda").to(torch.bfloat16).float()
+            y = torch.empty(M, dtype=torch.float32, device="cuda")
+            for fmt in ("bf16", "i8", "q4_0"):
+                if not want(f"gemv:{name}:{fmt}"):
+                    continue
+                if fmt == "bf16":
+                    one = (mie.mie_convert_bf16(w),)
+                    nbytes = M * K * 2
+                    call = lambda a, st: mie.mie_gemv_bf16(a[0], x, y, stream=st)
+                elif fmt == "i8":
+                    one = mie.mie_quantize_i8(w)
+                    nbytes = M * K + 4 * M
+                    call = lambda a, st: mie.mie_gemv_i8(a[0], a[1], x, y, stream=st)
+                else:
+                    one = (mie.mie_q4_0_pack(mie.mie_quantize_q4_0(w), M, K),)
+                    nbytes = M * ((K + 31) // 32) * 18
+                    call = lambda a, st: mie.mie_gemv_q4_0(a[0], x, M, K, y, stream=st)
+                n = max(least, int(total // nbytes) + 1)
+                copies = [one] + [tuple(t.clone() for t in one) for _ in range(n - 1)]
+                dt = graph_time(torch, [(lambda st, a=a: call(a, st)) for a in copies])
+                algo = nbytes + K * 4 + M * 4
+                out["gemv"].append({"shape": [M, K], "name": name, "fmt": fmt, "us": dt * 1e6,
+                                    "gbs": algo / dt / 1e9, "frac": algo / dt / 1e9 / peak, "launches": n})
+                del copies, one
+                torch.cuda.empty_cache()
+            del w
+        Hq, Hkv, hd, bs = 32, 8, 64, 16
+        for ctx in synth.SWEEP_ATTN_CTX:
+            if not want(f"attn:{ctx}"):
+                continue
+            nblk = (ctx + bs - 1) // bs
+            per_call = ctx * Hkv * hd * 2 * 2
+            n = max(least, int(total // per_call) + 1)
+            pool_blocks = nblk * n
+            k_pool = torch.randn((pool_blocks, Hkv, bs, hd), generator=gen, device="cuda").to(torch.bfloat16)
+            v_pool = torch.randn((pool_blocks, Hkv, bs, hd), generator=gen, device="cuda").to(torch.bfloat16)
+            perm = torch.from_numpy(synth.permutation(synth.SWEEP_SEED + ctx, pool_blocks).astype(np.int32)).cuda()
+            tables = [perm[i * nblk:(i + 1) * nblk].contiguous() for i in range(n)]
+            q = torch.randn(Hq * hd, generator=gen, device="cuda")
+            o = torch.empty(Hq * hd, dtype=torch.float32, device="cuda")
+            ws = torch.empty(max(mie.mie_paged_attn_workspace_bytes(Hq, Hkv, hd, ctx, bs), 256), dtype=torch.uint8,
+                             device="cuda")
+            stride = Hkv * bs * hd
+            dt = graph_time(torch, [(lambda st, t=t: mie.mie_paged_attn_decode(
+                q, k_pool, v_pool, stride, pool_blocks, t, ctx, Hq, Hkv, hd, bs, hd ** -0.5, o, ws, stream=st))
+                for t in tables])
+            out["attention"].append({"ctx": ctx, "us": dt * 1e6, "gbs": per_call / dt / 1e9,
+                                     "frac": per_call / dt / 1e9 / peak, "launches": n})
+            del k_pool, v_pool, tables
+            torch.cuda.empty_cache()
+        V = 128256
+        if want("argmax"):
+            n = max(least, int(total // (V * 4)) + 1)
+            vs = [torch.randn(V, generator=gen, device="cuda") for _ in range(n)]
+            am = torch.empty(1, dtype=torch.int32, device="cuda")
+            wsa = torch.empty(mie.mie_argmax_workspace_bytes(V), dtype=torch.uint8, device="cuda")
+            dt = graph_time(torch, [(lambda st, v=v: mie.mie_argmax(v, am, wsa, stream=st)) for v in vs])
+            out["argmax"] = {"n": V, "us": dt * 1e6, "gbs": V * 4 / dt / 1e9, "launches": n}
+    out["clocks"] = clk.summary()
+    print(json.dumps(out), flush=True)
+
+
 def main():
     args = parse()
+    if args.workload == "sweep":
+        run_sweep(args)
+        return
     if args.layers:
         from dataclasses import replace as _replace  # a truncated model for profiling captures
         synth_shape = _replace(synth.llama32_1b(args.fmt), n_layers=args.layers)

@@ -7,10 +7,15 @@
 namespace mie {
 
 template <int F> struct FmtT;
-// EPC: elements per 16-byte chunk; CPL: chunks per lane per 2048-column slice.
-template <> struct FmtT<MIE_FMT_BF16> { static constexpr int EPC = 8, CPL = 8; };
-template <> struct FmtT<MIE_FMT_I8> { static constexpr int EPC = 16, CPL = 4; };
-template <> struct FmtT<MIE_FMT_Q4_0> { static constexpr int EPC = 32, CPL = 2; };
+// EPC: elements per 16-byte chunk; CPL: chunks per lane per 2048-column slice; RPW:
+// rows a warp reduces per stage, so that every format moves 8 x 16 bytes per lane per
+// stage (a stage of one row per warp would be 8 KB for Q4_0, and the per-stage handoff
+// would then cost more than the bytes: measured 27 % of HBM on the Q4_0 LM head).
+template <> struct FmtT<MIE_FMT_BF16> { static constexpr int EPC = 8, CPL = 8, RPW = 1; };
+template <> struct FmtT<MIE_FMT_I8> { static constexpr int EPC = 16, CPL = 4, RPW = 2; };
+template <> struct FmtT<MIE_FMT_Q4_0> { static constexpr int EPC = 32, CPL = 2, RPW = 4; };
+
+__host__ __device__ inline int fmt_rows_per_warp(int fmt) { return fmt == MIE_FMT_Q4_0 ? 4 : (fmt == MIE_FMT_I8 ? 2 : 1); }
 constexpr int kSlice = 2048;  // = 32 * EPC * CPL for every format
 constexpr int kMaxK = 16384;  // eight 2048-column slices
 
@@ -88,24 +93,34 @@ __device__ __forceinline__ void chunk_fma<MIE_FMT_Q4_0>(const uint4 &w, const fl
   }
 }
 
-// Input registers of one chunk from the staged vector xs (natural order).
+// Staged input vectors keep four spare floats after every 32 elements: element k sits
+// at xs_at(k).  A lane's chunk (8, 16 or 32 consecutive elements) then starts 36, 18
+// or 9 float4 slots after its neighbour's, so the float4 reads of a warp fill the 32
+// banks evenly (unpadded, the 32 lanes of a Q4_0 warp all start on the same bank).
+__host__ __device__ constexpr int xs_at(int k) { return k + ((k >> 5) << 2); }
+__host__ __device__ constexpr int xs_floats(int Kp) { return Kp + ((Kp + 31) >> 5) * 4; }
+
+// Input registers of one chunk (elements e .. e+EPC-1, e a multiple of EPC) from the
+// staged vector xs.
 template <int F>
 __device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr) {
+  constexpr int EPC = FmtT<F>::EPC;
+  const float4 *q4 = reinterpret_cast<const float4 *>(xs + xs_at(e));
   if constexpr (F == MIE_FMT_Q4_0) {
-    const float sc[8] = {1.f, 0.0625f, 0.00390625f, 0.000244140625f, 1.52587890625e-05f,
-                         0.00390625f, 0.000244140625f, 1.52587890625e-05f};
+    // the unpack order of chunk_fma and the powers of two that undo each code's bit
+    // offset are fixed per register
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const int src[8] = {4 * t, 4 * t + 16, 4 * t + 1, 4 * t + 17, 4 * t + 2, 4 * t + 18, 4 * t + 3, 4 * t + 19};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        xr[4 * t + i] = make_float2(xs[e + src[2 * i]] * sc[2 * i], xs[e + src[2 * i + 1]] * sc[2 * i + 1]);
+      const float4 a = q4[t], b = q4[t + 4];  // elements 4t.. and 4t+16..
+      xr[4 * t + 0] = make_float2(a.x, b.x * 0.0625f);
+      xr[4 * t + 1] = make_float2(a.y * 0.00390625f, b.y * 0.000244140625f);
+      xr[4 * t + 2] = make_float2(a.z * 1.52587890625e-05f, b.z * 0.00390625f);
+      xr[4 * t + 3] = make_float2(a.w * 0.000244140625f, b.w * 1.52587890625e-05f);
     }
   } else {
-    constexpr int EPC = FmtT<F>::EPC;
 #pragma unroll
     for (int i = 0; i < EPC / 4; ++i) {
-      const float4 q = *reinterpret_cast<const float4 *>(xs + e + 4 * i);
+      const float4 q = q4[i];
       xr[2 * i] = make_float2(q.x, q.y);
       xr[2 * i + 1] = make_float2(q.z, q.w);
     }
@@ -247,12 +262,59 @@ __device__ __forceinline__ float stage_row_dot(uint32_t row, uint32_t sc, const 
   }
 }
 
+// stage_row_dot over the RPW consecutive staged rows of this warp (row addresses
+// row + i*row_bytes, scale rows sc + i*s_bytes): every chunk and scale of all rows is
+// loaded before any math.  nrows (<= RPW) rows are valid; the others read row 0.
+template <int F>
+__device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes, uint32_t sc, uint32_t s_bytes,
+                                               int nrows, const float2 *xr, int e0, int Kp, int lane,
+                                               float (&sum)[FmtT<F>::RPW]) {
+  using T = FmtT<F>;
+  constexpr int EPC = T::EPC, CPL = T::CPL, R = T::RPW, kChunkStride = 32 * EPC;
+  uint4 w[R][CPL];
+#pragma unroll
+  for (int i = 0; i < R; ++i) {
+    const uint32_t ra = row + (uint32_t)(i < nrows ? i : 0) * row_bytes;
+#pragma unroll
+    for (int c = 0; c < CPL; ++c) w[i][c] = lds128(e0 + c * kChunkStride < Kp ? ra + (uint32_t)(c * 32 + lane) * 16 : ra);
+  }
+  if constexpr (F == MIE_FMT_Q4_0) {
+    uint32_t hb[R][CPL];
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      const uint32_t sa = sc + (uint32_t)(i < nrows ? i : 0) * s_bytes;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) hb[i][c] = lds16(e0 + c * kChunkStride < Kp ? sa + (uint32_t)(c * 32 + lane) * 2 : sa);
+    }
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      float acc_s = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        chunk_fma<F>(w[i][c], xr + c * (EPC / 2), acc);
+        const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+        acc_s = fmaf(__half2float(__ushort_as_half((unsigned short)hb[i][c])), cs, acc_s);
+      }
+      sum[i] = acc_s;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < R; ++i) {
+      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) chunk_fma<F>(w[i][c], xr + c * (EPC / 2), acc);
+      sum[i] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+    }
+  }
+}
+
 __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
   return v > bv || (v == bv && i < bi);
 }
 
-// RMSNorm of the staged vector xs[0..K) in place (PRO_NORM, PRO_EMBED_NORM), or only
-// the bf16 rounding of PRO_PLAIN inputs when act_bf16 is set.  g0, when not null,
+// RMSNorm of the staged vector xs (element k at xs_at(k), k < K) in place (PRO_NORM,
+// PRO_EMBED_NORM), or only the bf16 rounding of PRO_PLAIN inputs when act_bf16 is set.  g0, when not null,
 // holds the gains of elements tid + j*NT (j < 8), loaded by the caller ahead of time
 // (K <= 8*NT).  NT threads take part; Sync is a barrier over them.
 template <int NT, class Sync>
@@ -262,7 +324,7 @@ __device__ void normalize_staged(const GemvArgs &a, int pro, float *xs, int K, f
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (pro != PRO_PLAIN) {
     float ss = 0.f;
-    for (int k = tid; k < K; k += NT) ss += xs[k] * xs[k];
+    for (int k = tid; k < K; k += NT) ss += xs[xs_at(k)] * xs[xs_at(k)];
     ss = warp_sum(ss);
     if (lane == 0) red[warp] = ss;
     Sync::sync();
@@ -281,18 +343,19 @@ __device__ void normalize_staged(const GemvArgs &a, int pro, float *xs, int K, f
       for (int j = 0; j < B; ++j) {
         const int k = k0 + j * NT;
         if (k < K) {
-          float v = xs[k] * r * g[j];
+          float v = xs[xs_at(k)] * r * g[j];
           if (a.act_bf16) v = round_bf16(v);
-          xs[k] = v;
+          xs[xs_at(k)] = v;
         }
       }
     }
   } else if (a.act_bf16) {
-    for (int k = tid; k < K; k += NT) xs[k] = round_bf16(xs[k]);
+    for (int k = tid; k < K; k += NT) xs[xs_at(k)] = round_bf16(xs[xs_at(k)]);
   }
 }
 
-// Stages a GEMV input vector into shared memory xs[0..Kp) (zeros past K), applying the
+// Stages a GEMV input vector into shared memory xs (element k at xs_at(k), zeros from K
+// to Kp), applying the
 // prologue: PRO_PLAIN copies x; PRO_NORM applies RMSNorm with the gain; PRO_EMBED_NORM
 // gathers row sp->token of the embedding first (CTA 0 also stores it as the residual).
 // With act_bf16 the staged values are rounded to bf16.  Each thread issues a batch of
@@ -324,7 +387,7 @@ __device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp
 #pragma unroll
       for (int j = 0; j < B; ++j) {
         const int k = k0 + j * NT;
-        if (k < Kp) xs[k] = (k < K) ? v[j] : 0.f;
+        if (k < Kp) xs[xs_at(k)] = (k < K) ? v[j] : 0.f;
         if (blockIdx.x == 0 && k < K) a.x_store[k] = v[j];
       }
     }
@@ -336,7 +399,7 @@ __device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp
 #pragma unroll
       for (int j = 0; j < B; ++j) {
         const int k = k0 + j * NT;
-        if (k < Kp) xs[k] = (k < K) ? v[j] : 0.f;
+        if (k < Kp) xs[xs_at(k)] = (k < K) ? v[j] : 0.f;
       }
     }
   }
@@ -421,16 +484,16 @@ __device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map) {
   return true;
 }
 
-// Copies tagged words [0, K) of src into xs once all carry `tag`; xs[K..Kp) = 0.  src
-// is 16-byte aligned.
+// Copies tagged words [0, K) of src into the staged vector xs (element k at xs_at(k))
+// once all carry `tag`, zeros from K to Kp.  src is 16-byte aligned.
 template <int NT>
 __device__ bool poll_vector(const uint64_t *src, int K, int Kp, uint32_t tag, float *xs, const int *abort) {
   const bool ok = poll_pairs<NT, 8>((K + 1) / 2, tag, abort, [&](int j, const uint64_t *&s, float *&d, int &c) {
     s = src + 2 * j;
-    d = xs + 2 * j;
+    d = xs + xs_at(2 * j);  // a pair never straddles a padding gap
     c = (2 * j + 1 < K) ? 2 : 1;
   });
-  for (int k = K + threadIdx.x; k < Kp; k += NT) xs[k] = 0.f;
+  for (int k = K + threadIdx.x; k < Kp; k += NT) xs[xs_at(k)] = 0.f;
   return ok;
 }
 

@@ -93,13 +93,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
   const DevMat &m = a.m;
   const int Kp = m.kp, K = m.cols, M = m.rows;
   const int KS = (Kp + kSlice - 1) / kSlice;
-  const int RPS = KS >= kCWarps ? 1 : kCWarps / KS;
+  constexpr int RPW = T::RPW;
+  const int WR = KS >= kCWarps ? 1 : kCWarps / KS;  // warps per slice column
+  const int RPS = WR * RPW;                          // rows per stage
   const int NST = a.n_stages;
   const uint32_t stage_bytes = a.stage_bytes, sc_bytes = a.sc_stage_bytes;
   uint8_t *ring = smem_raw;
   uint8_t *sring = ring + (size_t)NST * stage_bytes;
-  float *xs = reinterpret_cast<float *>(sring + (size_t)NST * sc_bytes);  // [Kp]
-  float *part = xs + Kp;                                                   // [rows][KS]
+  float *xs = reinterpret_cast<float *>(sring + (size_t)NST * sc_bytes);  // element k at xs_at(k)
+  float *part = xs + xs_floats(Kp);                                        // [rows][KS]
 
   const int n_units = (M + RU - 1) / RU;
   const int u0 = (int)((int64_t)blockIdx.x * n_units / gridDim.x);
@@ -156,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
   if constexpr (EPI == EPI_QKV) qp = qkv_prefetch(a);
 
   const int ri = warp / KS, ks = warp % KS;
-  const bool has_slice = warp < RPS * KS;
+  const bool has_slice = warp < WR * KS;
   const int e0 = ks * kSlice + lane * EPC;
   constexpr int kChunkStride = 32 * EPC;
   float2 xr[CPL * EPC / 2];
@@ -180,14 +182,20 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
       break;
     }
     consumed = s + 1;
-    const int r = row0 + s * RPS + ri;
+    const int r = row0 + s * RPS + ri * RPW;  // this warp's first row of the stage
     if (has_slice && r < row1) {
-      const uint32_t rowa = smem_u32(ring) + (uint32_t)slot * stage_bytes + (uint32_t)(ri * m.row_bytes) +
+      const int nr = min(RPW, row1 - r);
+      const uint32_t rowa = smem_u32(ring) + (uint32_t)slot * stage_bytes + (uint32_t)(ri * RPW * m.row_bytes) +
                             (uint32_t)ks * kSliceBytes;
-      const uint32_t sca = smem_u32(sring) + (uint32_t)slot * sc_bytes + (uint32_t)(ri * m.s_stride + ks * (kSlice / 32)) * 2;
-      float sum = stage_row_dot<F>(rowa, sca, xr, e0, Kp, lane);
-      sum = warp_sum(sum);
-      if (lane == 0) part[(r - row0) * KS + ks] = sum;
+      const uint32_t sca = smem_u32(sring) + (uint32_t)slot * sc_bytes +
+                           (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice / 32)) * 2;
+      float sum[RPW];
+      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, e0, Kp, lane, sum);
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        const float v = warp_sum(sum[i]);
+        if (lane == 0 && i < nr) part[(r + i - row0) * KS + ks] = v;
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);
@@ -305,13 +313,13 @@ static Plan make_plan(const DevMat &m, int epi, int grid) {
   const int RU = (epi == EPI_SWIGLU || epi == EPI_QKV) ? 2 : 1;
   const int n_units = (m.rows + RU - 1) / RU;
   const int KS = (m.kp + kSlice - 1) / kSlice;
-  const int RPS = KS >= kCWarps ? 1 : kCWarps / KS;
+  const int RPS = (KS >= kCWarps ? 1 : kCWarps / KS) * fmt_rows_per_warp(m.fmt);
   const int rows_max = ((n_units + grid - 1) / grid) * RU;
   Plan p;
   p.grid = grid;
   p.stage_bytes = (uint32_t)((RPS * m.row_bytes + 127) / 128 * 128);
   p.sc_bytes = m.fmt == MIE_FMT_Q4_0 ? (uint32_t)((RPS * m.s_stride * 2 + 127) / 128 * 128) : 0u;
-  const size_t fixed = sizeof(float) * ((size_t)m.kp + (size_t)rows_max * KS);
+  const size_t fixed = sizeof(float) * ((size_t)xs_floats(m.kp) + (size_t)rows_max * KS);
   const int need = (rows_max + RPS - 1) / RPS;  // stages one CTA streams
   long avail = (long)kSmemBudget - (long)fixed;
   int ns = (int)(avail > 0 ? avail / (long)(p.stage_bytes + p.sc_bytes) : 0);

@@ -93,7 +93,7 @@ struct PersistShared {
 
 // Row range of this CTA for a GEMV phase (units of RU rows, balanced over the grid).
 struct RowRange {
-  int u0, u1, row0, row1, KS, RPS, n_stages;
+  int u0, u1, row0, row1, KS, WR, RPS, n_stages;  // WR: warps per slice column; RPS = WR * rows per warp
 };
 
 __device__ __forceinline__ RowRange row_range(const DevMat &m, int epi) {
@@ -105,7 +105,8 @@ __device__ __forceinline__ RowRange row_range(const DevMat &m, int epi) {
   r.row0 = r.u0 * RU;
   r.row1 = min(r.u1 * RU, m.rows);
   r.KS = (m.kp + kSlice - 1) / kSlice;
-  r.RPS = r.KS >= kPW ? 1 : kPW / r.KS;
+  r.WR = r.KS >= kPW ? 1 : kPW / r.KS;
+  r.RPS = r.WR * fmt_rows_per_warp(m.fmt);
   r.n_stages = r.row1 > r.row0 ? (r.row1 - r.row0 + r.RPS - 1) / r.RPS : 0;
   return r;
 }
@@ -170,8 +171,8 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const uint32_t tag = sc.tag;
   const bool has_rows = rr.row1 > rr.row0;
-  float *xs = scratch;                            // [Kp]
-  float *part = xs + Kp;                          // [rows of this CTA][KS]
+  float *xs = scratch;                            // [xs_floats(Kp)], element k at xs_at(k)
+  float *part = xs + xs_floats(Kp);               // [rows of this CTA][KS]
   float *resv = part + (rr.row1 - rr.row0) * rr.KS;  // EPI_RESID: residual of this CTA's rows
 
   QkvPrefetch qp;
@@ -205,7 +206,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
 #pragma unroll
         for (int j = 0; j < B; ++j) {
           const int k = k0 + j * kPCT;
-          if (k < Kp) xs[k] = (k < K) ? v[j] : 0.f;
+          if (k < Kp) xs[xs_at(k)] = (k < K) ? v[j] : 0.f;
         }
       }
     }
@@ -214,7 +215,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     bool ok = poll_pairs<kPCT, B>(n_in + n_res, tag, pa.abort, [&](int j, const uint64_t *&src, float *&dst, int &c) {
       if (j < n_in) {
         src = a.x_t + 2 * j;
-        dst = xs + 2 * j;
+        dst = xs + xs_at(2 * j);  // a pair never straddles a padding gap
         c = (2 * j + 1 < K) ? 2 : 1;
       } else {
         src = a.res_t + rr.row0 + (j - n_in);
@@ -223,7 +224,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
       }
     });
     if (ph.pro != PRO_EMBED_NORM)
-      for (int k = K + tid; k < Kp; k += kPCT) xs[k] = 0.f;
+      for (int k = K + tid; k < Kp; k += kPCT) xs[xs_at(k)] = 0.f;
     if (!ConsSync::all(ok)) {
       give_up(pa);
       return false;
@@ -234,8 +235,9 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   }
   stamp(pa.trace, pidx, 2);
 
+  constexpr int RPW = FmtT<F>::RPW;
   const int ri = warp / rr.KS, ks = warp % rr.KS;
-  const bool has_slice = warp < rr.RPS * rr.KS;
+  const bool has_slice = warp < rr.WR * rr.KS;
   const int e0 = ks * kSlice + lane * EPC;
   float2 xr[CPL * EPC / 2];
 #pragma unroll
@@ -259,15 +261,20 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
       atomicExch(pa.abort, 1);
       latch_error(pa.err, ERR_TIMEOUT);
     }
-    const int r = rr.row0 + st * rr.RPS + ri;
+    const int r = rr.row0 + st * rr.RPS + ri * RPW;  // this warp's first row of the stage
     if (ok && has_slice && r < rr.row1) {
-      const uint32_t rowa = smem_u32(ring.w) + (uint32_t)slot * ring.slot_bytes + (uint32_t)(ri * m.row_bytes) +
+      const int nr = min(RPW, rr.row1 - r);
+      const uint32_t rowa = smem_u32(ring.w) + (uint32_t)slot * ring.slot_bytes + (uint32_t)(ri * RPW * m.row_bytes) +
                             (uint32_t)ks * kSliceBytes;
       const uint32_t sca = smem_u32(ring.sc) + (uint32_t)slot * ring.slot_sc_bytes +
-                           (uint32_t)(ri * m.s_stride + ks * (kSlice / 32)) * 2;
-      float sum = stage_row_dot<F>(rowa, sca, xr, e0, Kp, lane);
-      sum = warp_sum(sum);
-      if (lane == 0) part[(r - rr.row0) * rr.KS + ks] = sum;
+                           (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice / 32)) * 2;
+      float sum[RPW];
+      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, e0, Kp, lane, sum);
+#pragma unroll
+      for (int i = 0; i < RPW; ++i) {
+        const float v = warp_sum(sum[i]);
+        if (lane == 0 && i < nr) part[(r + i - rr.row0) * rr.KS + ks] = v;
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&ring.empty[slot]);
@@ -821,13 +828,13 @@ mie_status persist_plan(const Phase *host_phases, int n, int G, int HD, PersistP
     const int RU = (ph.epi == EPI_SWIGLU || ph.epi == EPI_QKV) ? 2 : 1;
     const int n_units = (m.rows + RU - 1) / RU;
     const int KS = (m.kp + kSlice - 1) / kSlice;
-    const int RPS = KS >= kPW ? 1 : kPW / KS;
+    const int RPS = (KS >= kPW ? 1 : kPW / KS) * fmt_rows_per_warp(m.fmt);
     const int rows_max = ((n_units + grid - 1) / grid) * RU;
     const uint32_t sb = (uint32_t)((RPS * m.row_bytes + 127) / 128 * 128);
     const uint32_t scb = m.fmt == MIE_FMT_Q4_0 ? (uint32_t)((RPS * m.s_stride * 2 + 127) / 128 * 128) : 0u;
     if (sb > slot) slot = sb;
     if (scb > slot_sc) slot_sc = scb;
-    const size_t need = sizeof(float) * ((size_t)m.kp + (size_t)rows_max * (KS + 1));
+    const size_t need = sizeof(float) * ((size_t)xs_floats(m.kp) + (size_t)rows_max * (KS + 1));
     if (need > scratch) scratch = need;
     if (((uintptr_t)m.w & 15) || (m.row_bytes & 15)) return fail(MIE_E_SHAPE, "persistent step: unaligned rows");
   }
