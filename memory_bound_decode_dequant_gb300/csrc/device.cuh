@@ -314,27 +314,29 @@ __device__ __forceinline__ bool better(float v, int i, float bv, int bi) {
 }
 
 // RMSNorm of the staged vector xs (element k at xs_at(k), k < K) in place (PRO_NORM,
-// PRO_EMBED_NORM), or only the bf16 rounding of PRO_PLAIN inputs when act_bf16 is set.  g0, when not null,
+// PRO_EMBED_NORM), or only the bf16 rounding of PRO_PLAIN inputs when act_bf16 is set.
+// sq is this thread's share of the sum of squares of the staged values, taken while
+// they were staged; with `published` the warps' sums already sit in red[] behind a
+// barrier, otherwise they are reduced here.  Every thread then forms the same scale
+// from red[] (same order), so no thread waits on another for it.  g0, when not null,
 // holds the gains of elements tid + j*NT (j < 8), loaded by the caller ahead of time
-// (K <= 8*NT).  NT threads take part; Sync is a barrier over them.
+// (K <= 8*NT).  NT threads take part; Sync is a barrier over them.  The caller
+// synchronises before xs is read.
 template <int NT, class Sync>
-__device__ void normalize_staged(const GemvArgs &a, int pro, float *xs, int K, float *red, float *scale_slot,
-                                 const float *g0) {
+__device__ void normalize_staged(const GemvArgs &a, int pro, float *xs, int K, float *red, const float *g0, float sq,
+                                 bool published) {
   constexpr int B = 8;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (pro != PRO_PLAIN) {
-    float ss = 0.f;
-    for (int k = tid; k < K; k += NT) ss += xs[xs_at(k)] * xs[xs_at(k)];
-    ss = warp_sum(ss);
-    if (lane == 0) red[warp] = ss;
-    Sync::sync();
-    if (tid == 0) {
-      float t = 0.f;
-      for (int w = 0; w < NT / 32; ++w) t += red[w];
-      *scale_slot = 1.0f / sqrtf(t / (float)K + a.eps);
+    if (!published) {
+      sq = warp_sum(sq);
+      if (lane == 0) red[warp] = sq;
+      Sync::sync();
     }
-    Sync::sync();
-    const float r = *scale_slot;
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < NT / 32; ++w) t += red[w];
+    const float r = 1.0f / sqrtf(t / (float)K + a.eps);
     for (int k0 = tid; k0 < K; k0 += NT * B) {
       float g[B];
 #pragma unroll
@@ -363,13 +365,12 @@ __device__ void normalize_staged(const GemvArgs &a, int pro, float *xs, int K, f
 // its first shared-memory store, so the staging costs one round trip per batch instead
 // of one per element.  NT threads take part; Sync is a barrier over them.
 template <int NT, class Sync>
-__device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp, float *red, float *scale_slot,
-                            int *err) {
+__device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp, float *red, int *err) {
   constexpr int B = 8;
   const int tid = threadIdx.x;
   // a vector that one batch covers gets its gains loaded together with its values
   const bool one_batch = pro != PRO_PLAIN && K <= NT * B;
-  float g0[B];
+  float g0[B], sq = 0.f;
   if (one_batch) {
 #pragma unroll
     for (int j = 0; j < B; ++j) g0[j] = __ldg(a.gain + min(tid + j * NT, K - 1));
@@ -388,6 +389,7 @@ __device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp
       for (int j = 0; j < B; ++j) {
         const int k = k0 + j * NT;
         if (k < Kp) xs[xs_at(k)] = (k < K) ? v[j] : 0.f;
+        if (k < K) sq = fmaf(v[j], v[j], sq);
         if (blockIdx.x == 0 && k < K) a.x_store[k] = v[j];
       }
     }
@@ -400,10 +402,11 @@ __device__ void stage_input(const GemvArgs &a, int pro, float *xs, int K, int Kp
       for (int j = 0; j < B; ++j) {
         const int k = k0 + j * NT;
         if (k < Kp) xs[xs_at(k)] = (k < K) ? v[j] : 0.f;
+        if (k < K) sq = fmaf(v[j], v[j], sq);
       }
     }
   }
-  normalize_staged<NT, Sync>(a, pro, xs, K, red, scale_slot, one_batch ? g0 : nullptr);
+  normalize_staged<NT, Sync>(a, pro, xs, K, red, one_batch ? g0 : nullptr, sq, false);
   Sync::sync();
 }
 
@@ -437,10 +440,11 @@ constexpr long kTagPolls = 1L << 22;  // bounded polling of tagged words (second
 
 // Polls n pairs of tagged words until all carry `tag`.  map(j, src, dst, n) names pair
 // j: its source (16-byte aligned when both words are wanted), its destination in
-// shared memory, and how many words it has (1 or 2).  Each thread polls its own pairs, B per round trip, and
-// gives up after kTagPolls rounds or once *abort is set; returns false then.
+// shared memory, and how many words it has (1 or 2).  The squares of the values of
+// pairs j < n_sq are added to *sq.  Each thread polls its own pairs, B per round trip,
+// and gives up after kTagPolls rounds or once *abort is set; returns false then.
 template <int NT, int B, class Map>
-__device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map) {
+__device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map, int n_sq = 0, float *sq = nullptr) {
   const int tid = threadIdx.x;
   for (int j0 = tid; j0 < n; j0 += NT * B) {
     uint32_t pending = 0;
@@ -469,8 +473,10 @@ __device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map) {
         int cnt;
         map(j0 + i * NT, src, dst, cnt);
         if (tag_ok(w0[i], tag) && (cnt < 2 || tag_ok(w1[i], tag))) {
-          dst[0] = tag_val(w0[i]);
-          if (cnt == 2) dst[1] = tag_val(w1[i]);
+          const float v0 = tag_val(w0[i]), v1 = cnt == 2 ? tag_val(w1[i]) : 0.f;
+          dst[0] = v0;
+          if (cnt == 2) dst[1] = v1;
+          if (j0 + i * NT < n_sq) *sq = fmaf(v1, v1, fmaf(v0, v0, *sq));
           pending &= ~(1u << i);
         }
       }

@@ -81,7 +81,6 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ float red[kCWarps];
-  __shared__ float s_scale;
   __shared__ float s_bv[kCWarps];
   __shared__ int s_bi[kCWarps];
   __shared__ unsigned s_last;
@@ -153,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 
   // ---------------------------------------------------------------- consumers
   pdl_wait();
-  stage_input<kCWarps * 32, CSync>(a, PRO, xs, K, Kp, red, &s_scale, a.err);
+  stage_input<kCWarps * 32, CSync>(a, PRO, xs, K, Kp, red, a.err);
   QkvPrefetch qp;
   if constexpr (EPI == EPI_QKV) qp = qkv_prefetch(a);
 

@@ -84,7 +84,6 @@ __device__ __forceinline__ int attn_ctx(int pos, int n_table, int bs) {
 
 struct PersistShared {
   float red[kPW];
-  float scale;
   float bv[kPW];
   int bi[kPW];
   unsigned last;
@@ -191,7 +190,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   if (has_rows) {
     constexpr int B = 8;
     const bool one_batch = ph.pro != PRO_PLAIN && K <= kPCT * B;
-    float g0[B];
+    float g0[B], sq = 0.f;
     if (one_batch) {
 #pragma unroll
       for (int j = 0; j < B; ++j) g0[j] = __ldg(a.gain + min(tid + j * kPCT, K - 1));
@@ -207,6 +206,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
         for (int j = 0; j < B; ++j) {
           const int k = k0 + j * kPCT;
           if (k < Kp) xs[xs_at(k)] = (k < K) ? v[j] : 0.f;
+          if (k < K) sq = fmaf(v[j], v[j], sq);
         }
       }
     }
@@ -222,15 +222,19 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
         dst = resv + (j - n_in);
         c = 1;
       }
-    });
+    }, ph.pro == PRO_NORM ? n_in : 0, &sq);
     if (ph.pro != PRO_EMBED_NORM)
       for (int k = K + tid; k < Kp; k += kPCT) xs[xs_at(k)] = 0.f;
+    if (ph.pro != PRO_PLAIN) {  // the warps' sums of squares ride on the poll's barrier
+      sq = warp_sum(sq);
+      if (lane == 0) ps.red[warp] = sq;
+    }
     if (!ConsSync::all(ok)) {
       give_up(pa);
       return false;
     }
     stamp(pa.trace, pidx, 1);
-    normalize_staged<kPCT, ConsSync>(a, ph.pro, xs, K, ps.red, &ps.scale, one_batch ? g0 : nullptr);
+    normalize_staged<kPCT, ConsSync>(a, ph.pro, xs, K, ps.red, one_batch ? g0 : nullptr, 0.f, true);
     ConsSync::sync();
   }
   stamp(pa.trace, pidx, 2);
@@ -396,7 +400,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
                                int &s_global, ChunkSmem<G, HD> &sm, const StepConst &sc, const PersistArgs &pa) {
   constexpr int NO = (G * HD + kPCT - 1) / kPCT;  // outputs per thread
   static_assert(2 * HD <= kPCT, "one thread per element of the current token's k and v");
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int nblk = (ctx + at.bs - 1) / at.bs;
   const int b0 = (int)((int64_t)sp * nblk / nsplit), b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
   const int t_end = min(b1 * at.bs, ctx);
