@@ -37,8 +37,14 @@ namespace mie {
 constexpr int kCWarps = 8;                    // consumer warps
 constexpr int kThreads = 32 * (kCWarps + 1);  // + one producer warp
 constexpr int kMaxStages = 16;
-constexpr size_t kSmemBudget = 110 * 1024;    // two such CTAs fit on one SM
 constexpr size_t kSmemMax = 200 * 1024;
+// bf16 rows need little arithmetic per byte: two CTAs per SM (a kernel and its
+// successor prefetching under programmatic dependent launch), each under 110 KB of
+// shared memory.  int8 and Q4_0 rows are unpacked in registers and the arithmetic per
+// byte sets the pace: one CTA per SM with the whole register file and ring (measured
+// on the 128256 x 2048 int8 GEMV: 69 -> 80 % of HBM).
+template <int F> constexpr int kMinBlocks = F == MIE_FMT_BF16 ? 2 : 1;
+constexpr size_t smem_budget(int fmt) { return fmt == MIE_FMT_BF16 ? 110 * 1024 : kSmemMax; }
 
 int gemv_chunk_elems(int fmt) {
   return fmt == MIE_FMT_BF16 ? 8 : fmt == MIE_FMT_I8 ? 16 : fmt == MIE_FMT_Q4_0 ? 32 : 0;
@@ -72,7 +78,7 @@ struct CSync {
 // issues the first ring-full of stages before any dependency wait.
 
 template <int F, int PRO, int EPI>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
+__global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const GemvArgs a) {
   using T = FmtT<F>;
   constexpr int EPC = T::EPC, CPL = T::CPL;
   constexpr int RU = (EPI == EPI_SWIGLU || EPI == EPI_QKV) ? 2 : 1;
@@ -300,8 +306,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const GemvArgs a) {
 // --------------------------------------------------------------- launching
 
 // Shared-memory plan of one launch: ring of n_stages stages plus the staged input and
-// the per-row partial sums, kept under kSmemBudget when possible so that a kernel and
-// its successor (prefetching under programmatic dependent launch) fit on one SM.
+// the per-row partial sums, kept under smem_budget(fmt) when possible (for bf16, so
+// that a kernel and its successor prefetching under programmatic dependent launch fit
+// on one SM).
 struct Plan {
   int grid, n_stages;
   uint32_t stage_bytes, sc_bytes;
@@ -320,7 +327,7 @@ static Plan make_plan(const DevMat &m, int epi, int grid) {
   p.sc_bytes = m.fmt == MIE_FMT_Q4_0 ? (uint32_t)((RPS * m.s_stride * 2 + 127) / 128 * 128) : 0u;
   const size_t fixed = sizeof(float) * ((size_t)xs_floats(m.kp) + (size_t)rows_max * KS);
   const int need = (rows_max + RPS - 1) / RPS;  // stages one CTA streams
-  long avail = (long)kSmemBudget - (long)fixed;
+  long avail = (long)smem_budget(m.fmt) - (long)fixed;
   int ns = (int)(avail > 0 ? avail / (long)(p.stage_bytes + p.sc_bytes) : 0);
   if (ns > kMaxStages) ns = kMaxStages;
   if (ns > need) ns = need;
