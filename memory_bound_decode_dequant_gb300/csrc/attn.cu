@@ -6,64 +6,18 @@
 // the partial softmaxes are merged; "Writing an LLM inference engine from scratch in
 // Rust", Lesson 4: an online softmax with a running maximum and sum).
 //
-// Grid (splits, KV heads), 128 threads; the number of splits in use follows the
-// context (at least four blocks each); the per-split work is attn_split in
-// attn_core.cuh.
+// Grid (splits, KV heads[, slots]), 256 threads; splits of 256 tokens; each split's
+// K/V blocks come into shared memory by bulk copies and are reduced by the chunk
+// passes of attn_core.cuh.
 #include <mutex>
 
 #include "attn_core.cuh"
 
 namespace mie {
 
-constexpr int kAttnThreads = 128;
-constexpr int kAttnWarps = kAttnThreads / 32;
-
 __device__ int g_device_error;  // latched by the stateless kernels of this device
 
-struct CtaSync {
-  __device__ static void sync() { __syncthreads(); }
-  __device__ static bool all(bool v) { return __syncthreads_and(v) != 0; }
-};
-
-template <int G, int HD>
-__global__ void __launch_bounds__(kAttnThreads) attn_kernel(const AttnArgs a_in) {
-  __shared__ AttnSmem<G, HD, kAttnWarps> sm;
-  pdl_trigger();
-  pdl_wait();
-  AttnArgs a = a_in;
-  if (a_in.slot_z) {  // one grid layer per slot of the few-slot step
-    const int z = blockIdx.z;
-    if (z >= a_in.sp->n_slots) return;
-    a.slot = z;
-    a.q += (int64_t)z * a.Hq * a.hd;
-    a.out += (int64_t)z * a.Hq * a.hd;
-    a.ws_count = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(a.ws_count) + z * a.ws_slot_bytes);
-    a.ws_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.ws_part) + z * a.ws_slot_bytes);
-  }
-  const int g = blockIdx.y, s = blockIdx.x;
-  int ctx;
-  const int32_t *bt;
-  int n_table;
-  if (a.sp) {
-    ctx = a.sp->pos[a.slot] + 1;
-    bt = a.sp->block_table + (int64_t)a.slot * a.sp->max_blocks;
-    n_table = a.sp->max_blocks;
-  } else {
-    ctx = a.ctx;
-    bt = a.block_table;
-    n_table = a.n_table;
-  }
-  if (ctx > n_table * a.bs) {
-    if (threadIdx.x == 0 && s == 0 && g == 0) latch_error(a.err, ERR_POS);
-    ctx = n_table * a.bs;
-  }
-  if (ctx < 0) ctx = 0;
-  const int nsplit = attn_nsplit((ctx + a.bs - 1) / a.bs, a.n_splits, attn_blocks_per_split<HD, kAttnWarps>(a.bs));
-  if (s >= nsplit) return;
-  attn_split<G, HD, kAttnWarps, CtaSync>(a, g, s, nsplit, ctx, bt, nullptr, sm);
-}
-
-// Chunked variant: 8 warps per (split, KV head[, slot]); the split's K/V blocks are
+// The kernel: 8 warps per (split, KV head[, slot]); the split's K/V blocks are
 // brought into shared memory by bulk copies (one per block for K and one for V, 128
 // tokens per chunk, two chunks in flight) and each chunk is reduced by the three
 // CTA-wide passes of chunk_passes.  Splits of 256 tokens; merged by the last split.
