@@ -427,6 +427,9 @@ def run_slots(args):
     from memory_bound_decode_dequant_gb300.workload import build_gpu_model
 
     shape = synth.llama32_1b("bf16")
+    if args.layers:  # a truncated model for profiling captures
+        from dataclasses import replace as _replace
+        shape = _replace(shape, n_layers=args.layers)
     wl = synth.SlotWorkload(steps=args.slot_steps)
     bs = shape.block_size
     S = wl.n_slots
