@@ -264,7 +264,7 @@ mie_status mie_decode_continue(mie_ctx *ctx, int n_steps);
  * [n_slots][max_blocks]).  The weights are read once for all slots (tensor-core MMAs
  * over the slots' input vectors, split into bf16 hi + lo).  logits_out: device
  * [n_slots][vocab] or NULL; argmax_out: device [n_slots] or NULL.  Layers and head in
- * bf16, int8 or Q4_0 with even input lengths; otherwise MIE_E_SHAPE.  The first call
+ * bf16, int8 or Q4_0 with input lengths a multiple of 4; otherwise MIE_E_SHAPE.  The first call
  * captures the few-slot step into its own CUDA graph.  Slots never write into a block
  * another slot's table shares (block-aligned prefixes; see mie_pool_writable). */
 mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int32_t *tokens,

@@ -12,6 +12,10 @@
 // x is fp32 in the method, so each x value is split into x_hi = bf16(x) and
 // x_lo = bf16(x - x_hi) and every tile takes two MMAs: the products are exact in
 // fp32 and x keeps about 16 significant bits (int8 weights become bf16 exactly).
+// Within each 16-column k-step the fragment positions 2t, 2t+1, 2t+8, 2t+9 of lane
+// (g, t) are mapped to columns 4t .. 4t+3 for both A and B (a sum over k does not depend
+// on its order), so a lane's x is one float4 and its weights one 8-byte (bf16) or
+// 4-byte (int8, Q4_0: both nibbles of four bytes) shared load per k-step.
 // Q4_0: the B values are the codes minus 8 (exact in bf16); each warp owns whole
 // 32-column blocks, accumulates a block's MMAs apart and adds them times the f16 block
 // scale of each output row.
@@ -70,22 +74,23 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_
   lo = bf16x2_bits(v0 - h0, v1 - h1);
 }
 
-// B fragment word: weights (row, k) and (row, k + 1) of a staged row as a bf16 pair.
+// B fragment words of one k-step: the lane's four consecutive weights of a staged row
+// (columns 4t .. 4t+3) as bf16 pairs b0 = (4t, 4t+1), b1 = (4t+2, 4t+3).
 template <int F>
-__device__ __forceinline__ uint32_t b_word(uint32_t addr);
+__device__ __forceinline__ void b_words(uint32_t addr, uint32_t &b0, uint32_t &b1);
 template <>
-__device__ __forceinline__ uint32_t b_word<MIE_FMT_Q4_0>(uint32_t) {  // not used: Q4_0 has its own loop
-  return 0u;
+__device__ __forceinline__ void b_words<MIE_FMT_Q4_0>(uint32_t, uint32_t &b0, uint32_t &b1) {  // own loop
+  b0 = b1 = 0u;
 }
 template <>
-__device__ __forceinline__ uint32_t b_word<MIE_FMT_BF16>(uint32_t addr) {
-  return lds32(addr);
+__device__ __forceinline__ void b_words<MIE_FMT_BF16>(uint32_t addr, uint32_t &b0, uint32_t &b1) {
+  asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(b0), "=r"(b1) : "r"(addr));
 }
 template <>
-__device__ __forceinline__ uint32_t b_word<MIE_FMT_I8>(uint32_t addr) {
-  const uint32_t v = lds16(addr);
-  const int q0 = (int)(int8_t)(v & 0xffu), q1 = (int)(int8_t)(v >> 8);
-  return bf16x2_bits((float)q0, (float)q1);  // exact: |q| <= 127
+__device__ __forceinline__ void b_words<MIE_FMT_I8>(uint32_t addr, uint32_t &b0, uint32_t &b1) {
+  const uint32_t v = lds32(addr);
+  b0 = bf16x2_bits((float)(int8_t)(v & 0xffu), (float)(int8_t)((v >> 8) & 0xffu));  // exact: |q| <= 127
+  b1 = bf16x2_bits((float)(int8_t)((v >> 16) & 0xffu), (float)(int8_t)(v >> 24));
 }
 
 // The k-step of a slice that warp `warp` handles as its j-th (0..kSKSteps-1): the slice's
@@ -261,54 +266,55 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   }
   SSync::sync();
 
-  // A fragments of slice q: x of slot g at columns kk + 2t (+1) and kk + 2t + 8 (+9)
-  // of this warp's k-steps, as hi / lo bf16 pairs.  Every load of the slice (x pairs
-  // and gain pairs, 8 bytes each) is issued before the first use, so staging costs one
-  // round trip; the values stay in registers through the RMSNorm.
+  // A fragments of slice q: x of slot g at columns kk + 4t .. kk + 4t + 3 of this warp's
+  // k-steps, as hi / lo bf16 pairs.  Every load of the slice (x and gains, 16 bytes each)
+  // is issued before the first use, so staging costs one round trip; the values stay in
+  // registers through the RMSNorm.
   uint32_t ah0[kSKSteps], ah2[kSKSteps], al0[kSKSteps], al2[kSKSteps];
-  auto load_pair = [&](int e) -> float2 {  // x of slot g at columns e, e + 1 (e even)
-    if (g >= S || e >= K) return make_float2(0.f, 0.f);
+  auto load_quad = [&](int e) -> float4 {  // x of slot g at columns e .. e + 3 (e % 4 == 0)
+    if (g >= S || e >= K) return make_float4(0.f, 0.f, 0.f, 0.f);
     if (PRO == PRO_EMBED_NORM) {
-      if (a.embed.fmt == MIE_FMT_BF16 && e + 1 < K) {
-        const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(a.embed.w + (int64_t)sh.tok[g] * a.embed.row_bytes) + e / 2);
-        return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+      if (a.embed.fmt == MIE_FMT_BF16 && e + 3 < K) {
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(a.embed.w + (int64_t)sh.tok[g] * a.embed.row_bytes) + e / 4);
+        return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u), __uint_as_float(w.y << 16),
+                           __uint_as_float(w.y & 0xffff0000u));
       }
-      return make_float2(embed_at(a.embed, sh.tok[g], e), e + 1 < K ? embed_at(a.embed, sh.tok[g], e + 1) : 0.f);
+      float v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = e + u < K ? embed_at(a.embed, sh.tok[g], e + u) : 0.f;
+      return make_float4(v[0], v[1], v[2], v[3]);
     }
-    if (e + 1 < K) return __ldcg(reinterpret_cast<const float2 *>(a.x + (int64_t)g * K + e));
-    return make_float2(__ldcg(a.x + (int64_t)g * K + e), 0.f);
+    if (e + 3 < K) return __ldcg(reinterpret_cast<const float4 *>(a.x + (int64_t)g * K + e));  // K % 4 == 0
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = e + u < K ? __ldcg(a.x + (int64_t)g * K + e + u) : 0.f;
+    return make_float4(v[0], v[1], v[2], v[3]);
   };
-  auto gain_pair = [&](int e) -> float2 {  // staged in shared memory before the kernel waited
-    if (e >= K) return make_float2(0.f, 0.f);
-    return make_float2(sh.gain[e], e + 1 < K ? sh.gain[e + 1] : 0.f);
+  auto gain_quad = [&](int e) -> float4 {  // staged in shared memory before the kernel waited
+    float v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = e + u < K ? sh.gain[e + u] : 0.f;
+    return make_float4(v[0], v[1], v[2], v[3]);
   };
   auto load_slice = [&](int q) {
-    float2 xv[kSKSteps][2];
+    float4 xv[kSKSteps];
 #pragma unroll
-    for (int j = 0; j < kSKSteps; ++j) {
-      const int kk = q * kSSlice + kstep_of<F>(warp, j) * 16 + 2 * t;
-      xv[j][0] = load_pair(kk);
-      xv[j][1] = load_pair(kk + 8);
-    }
+    for (int j = 0; j < kSKSteps; ++j) xv[j] = load_quad(q * kSSlice + kstep_of<F>(warp, j) * 16 + 4 * t);
     if (PRO == PRO_EMBED_NORM && blockIdx.x == 0 && g < S) {  // the residual stream starts as x
 #pragma unroll
       for (int j = 0; j < kSKSteps; ++j) {
-        const int kk = q * kSSlice + kstep_of<F>(warp, j) * 16 + 2 * t;
+        const int e = q * kSSlice + kstep_of<F>(warp, j) * 16 + 4 * t;
+        const float v[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int e = kk + 8 * h;
-          if (e < K) a.x_store[(int64_t)g * K + e] = xv[j][h].x;
-          if (e + 1 < K) a.x_store[(int64_t)g * K + e + 1] = xv[j][h].y;
-        }
+        for (int u = 0; u < 4; ++u)
+          if (e + u < K) a.x_store[(int64_t)g * K + e + u] = v[u];
       }
     }
     if (PRO != PRO_PLAIN) {
       // RMSNorm over the whole vector: the prologues that normalise have K <= kSSlice
       float ss = 0.f;
 #pragma unroll
-      for (int j = 0; j < kSKSteps; ++j)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) ss += xv[j][h].x * xv[j][h].x + xv[j][h].y * xv[j][h].y;
+      for (int j = 0; j < kSKSteps; ++j) ss += xv[j].x * xv[j].x + xv[j].y * xv[j].y + xv[j].z * xv[j].z + xv[j].w * xv[j].w;
       ss += __shfl_xor_sync(0xffffffffu, ss, 1);
       ss += __shfl_xor_sync(0xffffffffu, ss, 2);
       if (t == 0) sh.ss[warp][g] = ss;
@@ -322,18 +328,16 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       const float rn = sh.rs[g];
 #pragma unroll
       for (int j = 0; j < kSKSteps; ++j) {
-        const int kk = q * kSSlice + kstep_of<F>(warp, j) * 16 + 2 * t;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float2 gg = gain_pair(kk + 8 * h);
-          xv[j][h].x = xv[j][h].x * rn * gg.x;
-          xv[j][h].y = xv[j][h].y * rn * gg.y;
-        }
+        const float4 gg = gain_quad(q * kSSlice + kstep_of<F>(warp, j) * 16 + 4 * t);
+        xv[j].x = xv[j].x * rn * gg.x;
+        xv[j].y = xv[j].y * rn * gg.y;
+        xv[j].z = xv[j].z * rn * gg.z;
+        xv[j].w = xv[j].w * rn * gg.w;
       }
     }
 #pragma unroll
     for (int j = 0; j < kSKSteps; ++j) {
-      float v[4] = {xv[j][0].x, xv[j][0].y, xv[j][1].x, xv[j][1].y};
+      float v[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
       if (a.act_bf16) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) v[u] = round_bf16(v[u]);
@@ -422,19 +426,19 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       if (ok && Q4) {
         // whole blocks: b = warp + kSW * i, k-steps 2b (low nibbles) and 2b + 1 (high)
         const uint32_t sbase = ring + (uint32_t)slot * pl.stage_bytes;
-        const uint32_t nrow = sbase + (uint32_t)g * pl.pitch + 2 * t;  // row g's bytes 2t, 2t + 1 of a block
+        const uint32_t nrow = sbase + (uint32_t)g * pl.pitch + 4 * t;  // row g's bytes 4t .. 4t + 3 of a block
         const uint32_t srow = sbase + pl.sc_off + (uint32_t)(2 * t) * 128;  // scales of output rows 2t, 2t + 1
 #pragma unroll
         for (int i = 0; i < kSKSteps / 2; ++i) {
           const int b = warp + kSW * i;
           if (2 * b < nk) {
-            const uint32_t w01 = lds16(nrow + b * 16), w89 = lds16(nrow + b * 16 + 8);
+            const uint32_t w = lds32(nrow + b * 16);  // codes 4t.. (low nibbles) and 4t+16.. (high)
             const float d0 = __half2float(__ushort_as_half((unsigned short)lds16(srow + b * 2)));
             const float d1 = __half2float(__ushort_as_half((unsigned short)lds16(srow + 128 + b * 2)));
             float ct[4] = {0.f, 0.f, 0.f, 0.f};
-            const uint32_t lb0 = q4_pair(w01 & 0xFu, (w01 >> 8) & 0xFu), lb1 = q4_pair(w89 & 0xFu, (w89 >> 8) & 0xFu);
-            const uint32_t hb0 = q4_pair((w01 >> 4) & 0xFu, (w01 >> 12) & 0xFu);
-            const uint32_t hb1 = q4_pair((w89 >> 4) & 0xFu, (w89 >> 12) & 0xFu);
+            const uint32_t lb0 = q4_pair(w & 0xFu, (w >> 8) & 0xFu), lb1 = q4_pair((w >> 16) & 0xFu, (w >> 24) & 0xFu);
+            const uint32_t hb0 = q4_pair((w >> 4) & 0xFu, (w >> 12) & 0xFu);
+            const uint32_t hb1 = q4_pair((w >> 20) & 0xFu, (w >> 28) & 0xFu);
             mma_bf16_16816(ct, ah0[2 * i], ah2[2 * i], lb0, lb1);
             mma_bf16_16816(ct, al0[2 * i], al2[2 * i], lb0, lb1);
             mma_bf16_16816(ct, ah0[2 * i + 1], ah2[2 * i + 1], hb0, hb1);
@@ -444,7 +448,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
           }
         }
       } else if (ok) {
-        const uint32_t base = ring + (uint32_t)slot * pl.stage_bytes + (uint32_t)g * pl.pitch + (uint32_t)(2 * t) * ES;
+        const uint32_t base = ring + (uint32_t)slot * pl.stage_bytes + (uint32_t)g * pl.pitch + (uint32_t)(4 * t) * ES;
         // B words of eight k-steps are loaded in one batch (k-steps past the slice read
         // its first k-step: their A fragments are zero), then the MMAs run
         constexpr int H = kSKSteps / 2;
@@ -454,9 +458,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
 #pragma unroll
           for (int j = 0; j < H; ++j) {
             const int ks = warp + kSW * (h0 + j);
-            const uint32_t ad = base + (uint32_t)((ks < nk ? ks : 0) * 16) * ES;
-            b0[j] = b_word<F>(ad);
-            b1[j] = b_word<F>(ad + 8 * ES);
+            b_words<F>(base + (uint32_t)((ks < nk ? ks : 0) * 16) * ES, b0[j], b1[j]);
           }
 #pragma unroll
           for (int j = 0; j < H; j += 2) {
@@ -612,7 +614,8 @@ mie_status slots_gemv_supported(const DevMat &m, int pro) {
   if (m.fmt != MIE_FMT_BF16 && m.fmt != MIE_FMT_I8 && m.fmt != MIE_FMT_Q4_0)
     return fail(MIE_E_SHAPE, "few-slot step: weight format %d", m.fmt);
   if (m.kp % 16) return fail(MIE_E_SHAPE, "few-slot step: padded width %d is not a multiple of 16", m.kp);
-  if (m.cols % 2) return fail(MIE_E_SHAPE, "few-slot step: odd input length %d (inputs are read in pairs)", m.cols);
+  if (m.cols % 4)
+    return fail(MIE_E_SHAPE, "few-slot step: input length %d is not a multiple of 4 (inputs are read in fours)", m.cols);
   if (pro != PRO_PLAIN && m.cols > kSSlice)
     return fail(MIE_E_SHAPE, "few-slot step: RMSNorm over %d > %d columns", m.cols, kSSlice);
   if (((uintptr_t)m.w & 15) || (m.row_bytes & 15)) return fail(MIE_E_SHAPE, "few-slot step: unaligned rows");
