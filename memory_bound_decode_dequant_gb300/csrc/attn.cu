@@ -18,12 +18,15 @@ namespace mie {
 __device__ int g_device_error;  // latched by the stateless kernels of this device
 
 // The kernel: 8 warps per (split, KV head[, slot]); the split's K/V blocks are
-// brought into shared memory by bulk copies (one per block for K and one for V, 128
-// tokens per chunk, two chunks in flight) and each chunk is reduced by the three
-// CTA-wide passes of chunk_passes.  Splits of 256 tokens; merged by the last split.
+// brought into shared memory by bulk copies (one per block for K and one for V) and
+// reduced by the three CTA-wide passes of chunk_passes.  Splits of 256 tokens, merged by
+// the last split.  A split is one chunk: the passes cost ~1 us whatever the chunk's
+// length, and the second CTA on the SM overlaps one CTA's copies with the other's math
+// (two 128-token chunks in flight per CTA measured slower).
 constexpr int kCThreads = 256;
-constexpr int kCTok = 128;       // tokens per chunk
+constexpr int kCTok = 256;       // tokens per chunk
 constexpr int kCSplitTok = 256;  // tokens per split
+constexpr int kCBufs = kCSplitTok / kCTok >= 2 ? 2 : 1;  // chunks in flight per CTA
 
 struct CSync {
   __device__ static void sync() { __syncthreads(); }
@@ -97,41 +100,40 @@ __global__ void __launch_bounds__(kCThreads, 2) attn_chunk_kernel(const AttnArgs
   }
   __syncthreads();
   const int64_t head_off = (int64_t)g * a.bs * HD;  // elements
-  auto issue = [&](int ci) {  // thread 0: the bulk copies of chunk ci into buffer ci & 1
-    const int first = ci * cb, nb = min(cb, b1 - b0 - first);
-    uint8_t *kd = cbuf + (size_t)(ci & 1) * buf_bytes, *vd = kd + (size_t)kCTok * HD * 2;
-    mbar_expect_tx(&bar[ci & 1], 2u * nb * kb);
+  auto issue = [&](int ci) {  // thread 0: the bulk copies of chunk ci into buffer ci % kCBufs
+    const int first = ci * cb, nb = min(cb, b1 - b0 - first), bi = ci % kCBufs;
+    uint8_t *kd = cbuf + (size_t)bi * buf_bytes, *vd = kd + (size_t)kCTok * HD * 2;
+    mbar_expect_tx(&bar[bi], 2u * nb * kb);
     for (int j = 0; j < nb; ++j) {
       const int64_t off = (int64_t)ids[first + j] * a.block_stride + head_off;
-      bulk_load(kd + (size_t)j * kb, a.k + off, kb, &bar[ci & 1], 0ull);
-      bulk_load(vd + (size_t)j * kb, a.v + off, kb, &bar[ci & 1], 0ull);
+      bulk_load(kd + (size_t)j * kb, a.k + off, kb, &bar[bi], 0ull);
+      bulk_load(vd + (size_t)j * kb, a.v + off, kb, &bar[bi], 0ull);
     }
   };
-  if (tid == 0) {
-    issue(0);
-    if (nch > 1) issue(1);
-  }
+  if (tid == 0)
+    for (int ci = 0; ci < kCBufs && ci < nch; ++ci) issue(ci);
   float o[NO];
 #pragma unroll
   for (int j = 0; j < NO; ++j) o[j] = 0.f;
   bool ok = true;
   for (int ci = 0; ci < nch; ++ci) {
-    ok = CSync::all(ok && mbar_wait(&bar[ci & 1], (ci >> 1) & 1));
+    ok = CSync::all(ok && mbar_wait(&bar[ci % kCBufs], (ci / kCBufs) & 1));
     if (!ok) break;
-    const uint32_t kbase = smem_u32(cbuf) + (uint32_t)(ci & 1) * buf_bytes, vbase = kbase + (uint32_t)kCTok * HD * 2;
+    const uint32_t kbase = smem_u32(cbuf) + (uint32_t)(ci % kCBufs) * buf_bytes,
+                   vbase = kbase + (uint32_t)kCTok * HD * 2;
     const int t0 = (b0 + ci * cb) * a.bs;
     const int ntok = min((b0 + min((ci + 1) * cb, b1 - b0)) * a.bs, t_end) - t0;
     chunk_passes<G, HD, kCThreads, CSync>(kbase, vbase, ntok, a.scale, sm, o);
     __syncthreads();  // every thread is done with the buffer
-    if (tid == 0 && ci + 2 < nch) {
+    if (tid == 0 && ci + kCBufs < nch) {
       fence_proxy_async_smem();
-      issue(ci + 2);
+      issue(ci + kCBufs);
     }
   }
   if (!ok) {  // a copy never completed: report, and leave no copy writing into shared memory
     if (tid == 0) {
       latch_error(a.err, ERR_TIMEOUT);
-      for (int ci = 0; ci < nch && ci < 2; ++ci) mbar_wait(&bar[ci & 1], 0);
+      for (int ci = 0; ci < nch && ci < kCBufs; ++ci) mbar_wait(&bar[ci], 0);
     }
     return;
   }
@@ -192,7 +194,7 @@ int attn_splits_for(int Hkv, int max_ctx, int bs) {
 template <int G, int HD>
 static mie_status launch_attn_t(const AttnArgs &a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  const size_t smem = 2u * 2u * kCTok * HD * 2;
+  const size_t smem = (size_t)kCBufs * 2u * kCTok * HD * 2;
   auto kern = attn_chunk_kernel<G, HD>;
   MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   cfg.gridDim = dim3(a.n_splits, a.Hkv, a.slot_z ? a.max_slots : 1);
