@@ -6,12 +6,15 @@
 // vectors of all n_slots (<= 8) slots on the tensor cores, with mma.sync m16n8k16
 // (bf16 operands, fp32 accumulators) in transposed form:
 //   Y^T[slot][row] = X^T[slot][k] * W^T[k][row]
-//   A = X^T: 16 x 16, rows = slots 0..7 (rows 8..15 are zero), held in registers;
+//   A = X^T: 16 x 16, rows 0..7 = the slots' x_hi, rows 8..15 = their x_lo (below),
+//       held in registers;
 //   B = W^T: 16 k x 8 weight rows -- the staged rows read as they lie in memory;
-//   C = Y^T: thread (g = lane/4, t = lane%4) holds Y[row 2t, 2t+1][slot g].
+//   C = Y^T: thread (g = lane/4, t = lane%4) holds the x_hi and x_lo parts of
+//       Y[row 2t, 2t+1][slot g], added at the end.
 // x is fp32 in the method, so each x value is split into x_hi = bf16(x) and
-// x_lo = bf16(x - x_hi) and every tile takes two MMAs: the products are exact in
-// fp32 and x keeps about 16 significant bits (int8 weights become bf16 exactly).
+// x_lo = bf16(x - x_hi), which fill the sixteen rows of one MMA: the products are
+// exact in fp32 and x keeps about 16 significant bits (int8 weights become bf16
+// exactly).
 // Within each 16-column k-step the fragment positions 2t, 2t+1, 2t+8, 2t+9 of lane
 // (g, t) are mapped to columns 4t .. 4t+3 for both A and B (a sum over k does not depend
 // on its order), so a lane's x is one float4 and its weights one 8-byte (bf16) or
@@ -53,15 +56,6 @@ struct SSync {
   }
 };
 
-// Not volatile: a pure function of its registers, so the compiler may schedule it.
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-}
-
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
   return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
@@ -72,6 +66,17 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_
   const float h0 = __bfloat162float(__float2bfloat16_rn(v0)), h1 = __bfloat162float(__float2bfloat16_rn(v1));
   hi = bf16x2_bits(h0, h1);
   lo = bf16x2_bits(v0 - h0, v1 - h1);
+}
+
+// One m16n8k16 bf16 MMA with all four A registers (not volatile: a pure function of its
+// registers, so the compiler may schedule it): a0 / a2 rows g (x_hi of slot g),
+// a1 / a3 rows g + 8 (x_lo of slot g); c[0], c[1] and c[2], c[3] come back as the hi and
+// lo products of rows 2t, 2t + 1.
+__device__ __forceinline__ void mma_hl(float (&c)[4], uint32_t ah0, uint32_t al0, uint32_t ah2, uint32_t al2,
+                                       uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(ah0), "r"(al0), "r"(ah2), "r"(al2), "r"(b0), "r"(b1));
 }
 
 // B fragment words of one k-step: the lane's four consecutive weights of a staged row
@@ -420,7 +425,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
         s_abort = 1;
         latch_error(a.err, ERR_TIMEOUT);
       }
-      // four independent accumulators: even / odd k-steps x hi / lo
+      // four independent accumulator chains over the warp's k-steps
       float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
       float c2[4] = {0.f, 0.f, 0.f, 0.f}, c3[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok && Q4) {
@@ -439,12 +444,10 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
             const uint32_t lb0 = q4_pair(w & 0xFu, (w >> 8) & 0xFu), lb1 = q4_pair((w >> 16) & 0xFu, (w >> 24) & 0xFu);
             const uint32_t hb0 = q4_pair((w >> 4) & 0xFu, (w >> 12) & 0xFu);
             const uint32_t hb1 = q4_pair((w >> 20) & 0xFu, (w >> 28) & 0xFu);
-            mma_bf16_16816(ct, ah0[2 * i], ah2[2 * i], lb0, lb1);
-            mma_bf16_16816(ct, al0[2 * i], al2[2 * i], lb0, lb1);
-            mma_bf16_16816(ct, ah0[2 * i + 1], ah2[2 * i + 1], hb0, hb1);
-            mma_bf16_16816(ct, al0[2 * i + 1], al2[2 * i + 1], hb0, hb1);
-            c0[0] = fmaf(d0, ct[0], c0[0]);
-            c0[1] = fmaf(d1, ct[1], c0[1]);
+            mma_hl(ct, ah0[2 * i], al0[2 * i], ah2[2 * i], al2[2 * i], lb0, lb1);
+            mma_hl(ct, ah0[2 * i + 1], al0[2 * i + 1], ah2[2 * i + 1], al2[2 * i + 1], hb0, hb1);
+            c0[0] = fmaf(d0, ct[0] + ct[2], c0[0]);
+            c0[1] = fmaf(d1, ct[1] + ct[3], c0[1]);
           }
         }
       } else if (ok) {
@@ -461,17 +464,18 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
             b_words<F>(base + (uint32_t)((ks < nk ? ks : 0) * 16) * ES, b0[j], b1[j]);
           }
 #pragma unroll
-          for (int j = 0; j < H; j += 2) {
-            mma_bf16_16816(c0, ah0[h0 + j], ah2[h0 + j], b0[j], b1[j]);
-            mma_bf16_16816(c1, al0[h0 + j], al2[h0 + j], b0[j], b1[j]);
-            mma_bf16_16816(c2, ah0[h0 + j + 1], ah2[h0 + j + 1], b0[j + 1], b1[j + 1]);
-            mma_bf16_16816(c3, al0[h0 + j + 1], al2[h0 + j + 1], b0[j + 1], b1[j + 1]);
+          for (int j = 0; j < H; j += 4) {  // four independent accumulator chains
+            mma_hl(c0, ah0[h0 + j], al0[h0 + j], ah2[h0 + j], al2[h0 + j], b0[j], b1[j]);
+            mma_hl(c1, ah0[h0 + j + 1], al0[h0 + j + 1], ah2[h0 + j + 1], al2[h0 + j + 1], b0[j + 1], b1[j + 1]);
+            mma_hl(c2, ah0[h0 + j + 2], al0[h0 + j + 2], ah2[h0 + j + 2], al2[h0 + j + 2], b0[j + 2], b1[j + 2]);
+            mma_hl(c3, ah0[h0 + j + 3], al0[h0 + j + 3], ah2[h0 + j + 3], al2[h0 + j + 3], b0[j + 3], b1[j + 3]);
           }
         }
       }
       // c[0], c[1] = Y[row 2t, 2t+1][slot g] of this warp's k-steps
-      sh.red[slot][warp][g][2 * t] = (c0[0] + c2[0]) + (c1[0] + c3[0]);
-      sh.red[slot][warp][g][2 * t + 1] = (c0[1] + c2[1]) + (c1[1] + c3[1]);
+      // hi + lo parts (Q4_0 carries them summed in c0[0], c0[1])
+      sh.red[slot][warp][g][2 * t] = ((c0[0] + c0[2]) + (c1[0] + c1[2])) + ((c2[0] + c2[2]) + (c3[0] + c3[2]));
+      sh.red[slot][warp][g][2 * t + 1] = ((c0[1] + c0[3]) + (c1[1] + c1[3])) + ((c2[1] + c2[3]) + (c3[1] + c3[3]));
       __threadfence_block();
       __syncwarp();
       unsigned prev = 0u;
