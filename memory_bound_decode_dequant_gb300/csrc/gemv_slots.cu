@@ -145,6 +145,7 @@ __device__ __forceinline__ void argmax_unkey(unsigned long long k, float &v, int
 
 struct SlotPlan {
   int nst = 0;
+  uint32_t x_off = 0, x_pitch = 0;      // the slots' input slice after the ring: [kMaxSlots][x_pitch]
   uint32_t pitch = 0, stage_bytes = 0;  // padded row bytes in shared memory, bytes per slot
   uint32_t sc_off = 0;                  // Q4_0: offset of the stage's scale rows (128 bytes each)
   int n_tiles = 0, KS = 1;
@@ -156,7 +157,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   constexpr int ES = (F == MIE_FMT_BF16) ? 2 : 1;  // bytes per weight (bf16, int8)
   constexpr bool Q4 = F == MIE_FMT_Q4_0;
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full_bar[kSMaxNst], empty_bar[kSMaxNst];
+  __shared__ __align__(8) uint64_t full_bar[kSMaxNst], empty_bar[kSMaxNst], x_bar;
   __shared__ SlotShared sh;
   __shared__ volatile int s_issued, s_prod_done, s_abort, s_x_ready;
 
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       mbar_init(&full_bar[i], 1);
       mbar_init(&empty_bar[i], kSW);
     }
+    mbar_init(&x_bar, 1);
     s_issued = 0;
     s_prod_done = 0;
     s_abort = 0;
@@ -276,6 +278,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   // is issued before the first use, so staging costs one round trip; the values stay in
   // registers through the RMSNorm.
   uint32_t ah0[kSKSteps], ah2[kSKSteps], al0[kSKSteps], al2[kSKSteps];
+  const uint32_t xsm = smem_u32(smem) + pl.x_off;
   auto load_quad = [&](int e) -> float4 {  // x of slot g at columns e .. e + 3 (e % 4 == 0)
     if (g >= S || e >= K) return make_float4(0.f, 0.f, 0.f, 0.f);
     if (PRO == PRO_EMBED_NORM) {
@@ -289,11 +292,26 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       for (int u = 0; u < 4; ++u) v[u] = e + u < K ? embed_at(a.embed, sh.tok[g], e + u) : 0.f;
       return make_float4(v[0], v[1], v[2], v[3]);
     }
-    if (e + 3 < K) return __ldcg(reinterpret_cast<const float4 *>(a.x + (int64_t)g * K + e));  // K % 4 == 0
-    float v[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) v[u] = e + u < K ? __ldcg(a.x + (int64_t)g * K + e + u) : 0.f;
-    return make_float4(v[0], v[1], v[2], v[3]);
+    // the slice staged in shared memory (K % 4 == 0: a quad is all in or all out)
+    return lds128f(xsm + (uint32_t)g * pl.x_pitch + (uint32_t)(e % kSSlice) * 4);
+  };
+  // the slots' x of slice q into shared memory by bulk copies (one per slot row): one
+  // request per row instead of a load per lane; every warp is done with slice q - 1
+  auto stage_x = [&](int q) {
+    if (PRO == PRO_EMBED_NORM) return;
+    if (q > 0) SSync::sync();
+    const int cols = min(kSSlice, K - q * kSSlice);
+    if (tid == 0 && cols > 0) {
+      fence_proxy_async_smem();  // generic reads of the previous slice before the async writes
+      mbar_expect_tx(&x_bar, (uint32_t)(S * cols * 4));
+      for (int sl = 0; sl < S; ++sl)
+        bulk_load(smem + pl.x_off + (size_t)sl * pl.x_pitch, a.x + (int64_t)sl * K + (int64_t)q * kSSlice,
+                  (uint32_t)cols * 4, &x_bar, 0ull);
+    }
+    if (cols > 0 && !mbar_wait(&x_bar, q & 1)) {
+      s_abort = 1;
+      latch_error(a.err, ERR_TIMEOUT);
+    }
   };
   auto gain_quad = [&](int e) -> float4 {  // staged in shared memory before the kernel waited
     float v[4];
@@ -302,6 +320,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     return make_float4(v[0], v[1], v[2], v[3]);
   };
   auto load_slice = [&](int q) {
+    stage_x(q);
     float4 xv[kSKSteps];
 #pragma unroll
     for (int j = 0; j < kSKSteps; ++j) xv[j] = load_quad(q * kSSlice + kstep_of<F>(warp, j) * 16 + 4 * t);
@@ -503,6 +522,8 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   }
   if (SSync::any(!ok || s_abort)) {
     if (tid == 0) {
+      if (PRO != PRO_EMBED_NORM && min(kSSlice, K - (pl.KS - 1) * kSSlice) > 0)
+        mbar_wait(&x_bar, (pl.KS - 1) & 1);  // the last input copy (bounded)
       for (long it = 0; it < kWaitPolls && !s_prod_done; ++it) __nanosleep(64);
       const int issued = s_issued;
       for (int x = max(s, issued - pl.nst); x < issued; ++x) mbar_wait(&full_bar[x % pl.nst], (x / pl.nst) & 1);
@@ -572,10 +593,13 @@ static SlotPlan slot_plan(const DevMat &m, int grid) {
   int dev = 0, max_smem = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  const long avail = (long)max_smem - (long)sizeof(SlotShared) - 1024;
+  p.x_pitch = (uint32_t)(slice * 4 + 16);  // 16 spare bytes: the slots' rows start on different banks
+  const long x_bytes = (long)kMaxSlots * p.x_pitch;
+  const long avail = (long)max_smem - (long)sizeof(SlotShared) - 1024 - x_bytes;
   int nst = (int)(avail / (long)p.stage_bytes);
   p.nst = nst > kSMaxNst ? kSMaxNst : nst;
-  p.smem = (size_t)p.nst * p.stage_bytes;
+  p.x_off = (uint32_t)p.nst * p.stage_bytes;
+  p.smem = (size_t)p.x_off + (size_t)x_bytes;
   (void)grid;
   return p;
 }
