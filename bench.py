@@ -191,12 +191,12 @@ def run_reference(args, shape):
         om.decode_step(int(toks[args.warmup + i]), args.ctx + args.warmup + i, bt)
     dt = (time.perf_counter() - t0) / steps
     v = 1.0 / dt
-    line = {"impl": "reference", "metric": "batch-1 decode tok/s", "value": v, "unit": "tok/s",
+    line = {"impl": "reference", "metric": "batch-1 decode tok/s (Llama-3.2-1B shape)", "value": v, "unit": "tok/s",
             "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate/f32",
             "data": "synthetic (seeded N(0,0.02) weights, uniform tokens)",
-            "config": {"workload": f"{shape.name} {args.fmt} decode step, ctx {args.ctx}",
-                       "global_batch": 1, "seq_len": args.ctx},
+            "config": {"workload": f"{shape.name} {args.fmt} batch-1 decode step", "model": shape.name,
+                       "weights": args.fmt, "global_batch": 1, "seq_len": args.ctx},
             "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v, "unit": "tok/s",
                              "sample": f"{steps} full decode steps of the oracle (single-threaded C) at ctx "
                                        f"{args.ctx}+, K/V cache prefilled with seeded values"},
