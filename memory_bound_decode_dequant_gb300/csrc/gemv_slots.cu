@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kSMaxNst], empty_bar[kSMaxNst], x_bar;
   __shared__ SlotShared sh;
-  __shared__ volatile int s_issued, s_prod_done, s_abort, s_x_ready;
+  __shared__ volatile int s_issued, s_prod_done, s_abort, s_x_ready, s_x_last;
 
   const DevMat &m = a.m;
   const int M = m.rows, K = m.cols, Kp = m.kp;
@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     s_prod_done = 0;
     s_abort = 0;
     s_x_ready = 0;
+    s_x_last = -1;
     for (int i = 0; i < kSMaxNst; ++i) sh.cnt[i] = 0u;
     for (int i = 0; i < kMaxSlots; ++i) sh.best[i] = 0ull;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -296,19 +297,23 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     return lds128f(xsm + (uint32_t)g * pl.x_pitch + (uint32_t)(e % kSSlice) * 4);
   };
   // the slots' x of slice q into shared memory by bulk copies (one per slot row): one
-  // request per row instead of a load per lane; every warp is done with slice q - 1
-  auto stage_x = [&](int q) {
-    if (PRO == PRO_EMBED_NORM) return;
-    if (q > 0) SSync::sync();
+  // request per row instead of a load per lane.  Thread 0 issues slice 0 here and slice
+  // q + 1 once every warp holds its fragments of slice q, so the copy overlaps slice q's
+  // stages.
+  auto issue_x = [&](int q) {
     const int cols = min(kSSlice, K - q * kSSlice);
-    if (tid == 0 && cols > 0) {
-      fence_proxy_async_smem();  // generic reads of the previous slice before the async writes
-      mbar_expect_tx(&x_bar, (uint32_t)(S * cols * 4));
-      for (int sl = 0; sl < S; ++sl)
-        bulk_load(smem + pl.x_off + (size_t)sl * pl.x_pitch, a.x + (int64_t)sl * K + (int64_t)q * kSSlice,
-                  (uint32_t)cols * 4, &x_bar, 0ull);
-    }
-    if (cols > 0 && !mbar_wait(&x_bar, q & 1)) {
+    if (PRO == PRO_EMBED_NORM || cols <= 0) return;
+    fence_proxy_async_smem();  // generic reads of the previous slice before the async writes
+    mbar_expect_tx(&x_bar, (uint32_t)(S * cols * 4));
+    for (int sl = 0; sl < S; ++sl)
+      bulk_load(smem + pl.x_off + (size_t)sl * pl.x_pitch, a.x + (int64_t)sl * K + (int64_t)q * kSSlice,
+                (uint32_t)cols * 4, &x_bar, 0ull);
+    s_x_last = q;
+  };
+  auto stage_x = [&](int q) {
+    if (PRO == PRO_EMBED_NORM || min(kSSlice, K - q * kSSlice) <= 0) return;
+    if (q == 0 && tid == 0) issue_x(0);
+    if (!mbar_wait(&x_bar, q & 1)) {
       s_abort = 1;
       latch_error(a.err, ERR_TIMEOUT);
     }
@@ -432,9 +437,10 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   const uint32_t ring = smem_u32(smem);
   for (int q = 0; q < pl.KS; ++q) {
     load_slice(q);
-    if (q == 0) {
-      SSync::sync();
-      if (tid == 0) s_x_ready = 1;  // the producer may fill the rest of the ring
+    SSync::sync();  // every warp holds its fragments of slice q: the input buffer is free
+    if (tid == 0) {
+      if (q == 0) s_x_ready = 1;  // the producer may fill the rest of the ring
+      if (q + 1 < pl.KS) issue_x(q + 1);
     }
     const int nk = min(kSSlice, Kp - q * kSSlice) / 16;  // k-steps of this slice
     for (int tl = 0; tl < n_my; ++tl, ++s) {
@@ -522,8 +528,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
   }
   if (SSync::any(!ok || s_abort)) {
     if (tid == 0) {
-      if (PRO != PRO_EMBED_NORM && min(kSSlice, K - (pl.KS - 1) * kSSlice) > 0)
-        mbar_wait(&x_bar, (pl.KS - 1) & 1);  // the last input copy (bounded)
+      if (s_x_last >= 0) mbar_wait(&x_bar, s_x_last & 1);  // the last input copy (bounded)
       for (long it = 0; it < kWaitPolls && !s_prod_done; ++it) __nanosleep(64);
       const int issued = s_issued;
       for (int x = max(s, issued - pl.nst); x < issued; ++x) mbar_wait(&full_bar[x % pl.nst], (x / pl.nst) & 1);
