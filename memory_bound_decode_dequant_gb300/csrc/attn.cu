@@ -27,6 +27,7 @@ constexpr int kCThreads = 256;
 constexpr int kCTok = 256;       // tokens per chunk
 constexpr int kCSplitTok = 256;  // tokens per split
 constexpr int kCBufs = kCSplitTok / kCTok >= 2 ? 2 : 1;  // chunks in flight per CTA
+constexpr int kCSlotGrid = 16;   // few-slot step: CTAs per (KV head, slot)
 
 struct CSync {
   __device__ static void sync() { __syncthreads(); }
@@ -52,7 +53,7 @@ __global__ void __launch_bounds__(kCThreads, 2) attn_chunk_kernel(const AttnArgs
     a.ws_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a.ws_part) + z * a.ws_slot_bytes);
   }
   pdl_wait();
-  const int tid = threadIdx.x, g = blockIdx.y, sp = blockIdx.x;
+  const int tid = threadIdx.x, g = blockIdx.y;
   int ctx;
   const int32_t *bt;
   int n_table;
@@ -66,102 +67,109 @@ __global__ void __launch_bounds__(kCThreads, 2) attn_chunk_kernel(const AttnArgs
     n_table = a.n_table;
   }
   if (ctx > n_table * a.bs) {
-    if (tid == 0 && sp == 0 && g == 0) latch_error(a.err, ERR_POS);
+    if (tid == 0 && blockIdx.x == 0 && g == 0) latch_error(a.err, ERR_POS);
     ctx = n_table * a.bs;
   }
   if (ctx < 0) ctx = 0;
   const int nblk = (ctx + a.bs - 1) / a.bs;
   const int nsplit = attn_nsplit(nblk, a.n_splits, kCSplitTok / a.bs);
-  if (sp >= nsplit) return;
-  const int b0 = (int)((int64_t)sp * nblk / nsplit), b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
-  const int t_end = min(b1 * a.bs, ctx);
+  if ((int)blockIdx.x >= nsplit) return;
   const int kb = a.bs * HD * 2;           // bytes of one block of one head
   const int cb = kCTok / a.bs;            // blocks per chunk
-  const int nch = (b1 - b0 + cb - 1) / cb;
   const uint32_t buf_bytes = 2u * kCTok * HD * 2;
+  const int64_t head_off = (int64_t)g * a.bs * HD;  // elements
 
-  if (tid < b1 - b0) {
-    int blk = bt[b0 + tid];
-    if (blk < 0 || blk >= a.n_pool_blocks) {
-      latch_error(a.err, ERR_BLOCK_ID);
-      blk = 0;  // a valid block: the result is wrong but the error is reported
-    }
-    ids[tid] = blk;
-  }
   for (int i = tid; i < G * HD; i += kCThreads) sm.q[i] = __ldcg(a.q + (int64_t)(g * G) * HD + i);
-  if (tid < G) {
-    sm.m[tid] = -INFINITY;
-    sm.l[tid] = 0.f;
-  }
   if (tid == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
-  const int64_t head_off = (int64_t)g * a.bs * HD;  // elements
-  auto issue = [&](int ci) {  // thread 0: the bulk copies of chunk ci into buffer ci % kCBufs
-    const int first = ci * cb, nb = min(cb, b1 - b0 - first), bi = ci % kCBufs;
-    uint8_t *kd = cbuf + (size_t)bi * buf_bytes, *vd = kd + (size_t)kCTok * HD * 2;
-    mbar_expect_tx(&bar[bi], 2u * nb * kb);
-    for (int j = 0; j < nb; ++j) {
-      const int64_t off = (int64_t)ids[first + j] * a.block_stride + head_off;
-      bulk_load(kd + (size_t)j * kb, a.k + off, kb, &bar[bi], 0ull);
-      bulk_load(vd + (size_t)j * kb, a.v + off, kb, &bar[bi], 0ull);
+  // splits blockIdx.x, + gridDim.x, ... (the few-slot grid has fewer CTAs than splits a
+  // long context needs); chunk c of this CTA uses buffer c % kCBufs, phase c / kCBufs
+  int done = 0, issued = 0;
+  for (int sp = blockIdx.x; sp < nsplit; sp += gridDim.x) {
+    const int b0 = (int)((int64_t)sp * nblk / nsplit), b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
+    const int t_end = min(b1 * a.bs, ctx);
+    const int nch = (b1 - b0 + cb - 1) / cb;
+    if (tid < b1 - b0) {
+      int blk = bt[b0 + tid];
+      if (blk < 0 || blk >= a.n_pool_blocks) {
+        latch_error(a.err, ERR_BLOCK_ID);
+        blk = 0;  // a valid block: the result is wrong but the error is reported
+      }
+      ids[tid] = blk;
     }
-  };
-  if (tid == 0)
-    for (int ci = 0; ci < kCBufs && ci < nch; ++ci) issue(ci);
-  float o[NO];
+    if (tid < G) {
+      sm.m[tid] = -INFINITY;
+      sm.l[tid] = 0.f;
+    }
+    __syncthreads();  // block ids, statistics; the previous split is done with everything
+    auto issue = [&](int ci) {  // thread 0: the bulk copies of chunk ci of this split
+      const int first = ci * cb, nb = min(cb, b1 - b0 - first), c = done + ci, bi = c % kCBufs;
+      uint8_t *kd = cbuf + (size_t)bi * buf_bytes, *vd = kd + (size_t)kCTok * HD * 2;
+      fence_proxy_async_smem();  // earlier generic reads of the buffer before the async writes
+      mbar_expect_tx(&bar[bi], 2u * nb * kb);
+      for (int j = 0; j < nb; ++j) {
+        const int64_t off = (int64_t)ids[first + j] * a.block_stride + head_off;
+        bulk_load(kd + (size_t)j * kb, a.k + off, kb, &bar[bi], 0ull);
+        bulk_load(vd + (size_t)j * kb, a.v + off, kb, &bar[bi], 0ull);
+      }
+      issued = c + 1;
+    };
+    if (tid == 0)
+      for (int ci = 0; ci < kCBufs && ci < nch; ++ci) issue(ci);
+    float o[NO];
 #pragma unroll
-  for (int j = 0; j < NO; ++j) o[j] = 0.f;
-  bool ok = true;
-  for (int ci = 0; ci < nch; ++ci) {
-    ok = CSync::all(ok && mbar_wait(&bar[ci % kCBufs], (ci / kCBufs) & 1));
-    if (!ok) break;
-    const uint32_t kbase = smem_u32(cbuf) + (uint32_t)(ci % kCBufs) * buf_bytes,
-                   vbase = kbase + (uint32_t)kCTok * HD * 2;
-    const int t0 = (b0 + ci * cb) * a.bs;
-    const int ntok = min((b0 + min((ci + 1) * cb, b1 - b0)) * a.bs, t_end) - t0;
-    chunk_passes<G, HD, kCThreads, CSync>(kbase, vbase, ntok, a.scale, sm, o);
-    __syncthreads();  // every thread is done with the buffer
-    if (tid == 0 && ci + kCBufs < nch) {
-      fence_proxy_async_smem();
-      issue(ci + kCBufs);
+    for (int j = 0; j < NO; ++j) o[j] = 0.f;
+    bool ok = true;
+    int ci = 0;
+    for (; ci < nch; ++ci) {
+      const int c = done + ci;
+      ok = CSync::all(ok && mbar_wait(&bar[c % kCBufs], (c / kCBufs) & 1));
+      if (!ok) break;
+      const uint32_t kbase = smem_u32(cbuf) + (uint32_t)(c % kCBufs) * buf_bytes,
+                     vbase = kbase + (uint32_t)kCTok * HD * 2;
+      const int t0 = (b0 + ci * cb) * a.bs;
+      const int ntok = min((b0 + min((ci + 1) * cb, b1 - b0)) * a.bs, t_end) - t0;
+      chunk_passes<G, HD, kCThreads, CSync>(kbase, vbase, ntok, a.scale, sm, o);
+      __syncthreads();  // every thread is done with the buffer
+      if (tid == 0 && ci + kCBufs < nch) issue(ci + kCBufs);
     }
-  }
-  if (!ok) {  // a copy never completed: report, and leave no copy writing into shared memory
-    if (tid == 0) {
-      latch_error(a.err, ERR_TIMEOUT);
-      for (int ci = 0; ci < nch && ci < kCBufs; ++ci) mbar_wait(&bar[ci], 0);
+    if (!ok) {  // a copy never completed: report, and leave no copy writing into shared memory
+      if (tid == 0) {
+        latch_error(a.err, ERR_TIMEOUT);
+        for (int c = done + ci; c < issued; ++c) mbar_wait(&bar[c % kCBufs], (c / kCBufs) & 1);
+      }
+      return;
     }
-    return;
-  }
-  if (nsplit == 1) {
+    done += nch;
+    if (nsplit == 1) {
+#pragma unroll
+      for (int j = 0; j < NO; ++j) {
+        const int i = tid + j * kCThreads;
+        if (i < G * HD) {
+          const float L = sm.l[i / HD];
+          a.out[(int64_t)(g * G) * HD + i] = (L > 0.f) ? o[j] / L : 0.f;
+        }
+      }
+      return;
+    }
+    float *part = a.ws_part + ((int64_t)g * a.n_splits + sp) * (G * (2 + HD));
 #pragma unroll
     for (int j = 0; j < NO; ++j) {
       const int i = tid + j * kCThreads;
       if (i < G * HD) {
-        const float L = sm.l[i / HD];
-        a.out[(int64_t)(g * G) * HD + i] = (L > 0.f) ? o[j] / L : 0.f;
+        const int h = i / HD;
+        part[2 * G + i] = o[j];
+        if (i % HD == 0) {
+          part[h] = sm.m[h];
+          part[G + h] = sm.l[h];
+        }
       }
     }
-    return;
+    attn_merge_splits<G, HD, kCThreads, CSync, false>(a, g, nsplit, sm.last, 0u);
   }
-  float *part = a.ws_part + ((int64_t)g * a.n_splits + sp) * (G * (2 + HD));
-#pragma unroll
-  for (int j = 0; j < NO; ++j) {
-    const int i = tid + j * kCThreads;
-    if (i < G * HD) {
-      const int h = i / HD;
-      part[2 * G + i] = o[j];
-      if (i % HD == 0) {
-        part[h] = sm.m[h];
-        part[G + h] = sm.l[h];
-      }
-    }
-  }
-  attn_merge_splits<G, HD, kCThreads, CSync, false>(a, g, nsplit, sm.last, 0u);
 }
 
 // Empty context: the output is zero (no split has a position).
@@ -197,7 +205,10 @@ static mie_status launch_attn_t(const AttnArgs &a, cudaStream_t st, bool pdl) {
   const size_t smem = (size_t)kCBufs * 2u * kCTok * HD * 2;
   auto kern = attn_chunk_kernel<G, HD>;
   MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-  cfg.gridDim = dim3(a.n_splits, a.Hkv, a.slot_z ? a.max_slots : 1);
+  // few-slot step: the grid is captured once for any context, so it holds at most
+  // kCSlotGrid CTAs per (KV head, slot) and each loops over its splits; CTAs past a slot's
+  // splits only read its position and leave (a grid of n_splits left ~3/4 of them idle)
+  cfg.gridDim = dim3(a.slot_z ? min(a.n_splits, kCSlotGrid) : a.n_splits, a.Hkv, a.slot_z ? a.max_slots : 1);
   cfg.blockDim = dim3(kCThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

@@ -53,10 +53,8 @@ def tables_with_prefix(pool, lengths, bs, max_blocks, shared=2, prefix_blocks=2)
     return tables, prefix
 
 
-def run_slots(orc, shape, n_slots, max_slots, prompts, n_gen, compare_kv=True):
+def run_slots(orc, shape, n_slots, max_slots, prompts, n_gen, compare_kv=True, n_blocks=64, max_pos=128):
     bs = shape.block_size
-    n_blocks = 64
-    max_pos = 128
     lengths = [p + n_gen for p in prompts]
     max_blocks = max((n + bs - 1) // bs for n in lengths) + 1
     pool = mie.Pool(n_blocks)
@@ -119,6 +117,14 @@ def run_slots(orc, shape, n_slots, max_slots, prompts, n_gen, compare_kv=True):
 def test_slots_match_single_slot_oracle(orc, fmt):
     shape = replace(synth.TINY, wfmt=fmt, head_fmt=fmt)
     run_slots(orc, shape, n_slots=4, max_slots=4, prompts=[40, 37, 21, 50], n_gen=6)
+
+
+def test_slots_long_context_loops_over_splits(orc):
+    """A slot whose context needs more 256-token splits than the few-slot attention grid
+    has CTAs per (KV head, slot) (16): each CTA then loops over several splits."""
+    shape = replace(synth.TINY, wfmt="bf16", head_fmt="bf16")
+    run_slots(orc, shape, n_slots=2, max_slots=2, prompts=[4200, 300], n_gen=2, compare_kv=False,
+              n_blocks=300, max_pos=4224)
 
 
 def test_fewer_slots_than_the_context_holds(orc):
