@@ -24,8 +24,8 @@
 // scale of each output row.
 //
 // A producer warp streams stages of 8 weight rows x one 2048-column slice through a
-// ring in shared memory (one bulk copy per row into rows padded by 16 bytes, so the
-// B-fragment loads hit 32 distinct banks); the 8 consumer warps each own 16 of the
+// ring in shared memory (one bulk copy per row into rows padded so that the B-fragment
+// loads hit distinct banks); the 8 consumer warps each own 16 of the
 // slice's 128 k-steps and keep their x fragments in registers for the whole slice.
 // Warp partials are summed in a fixed order, so results do not depend on timing.
 #include "device.cuh"
@@ -590,15 +590,17 @@ static SlotPlan slot_plan(const DevMat &m, int grid) {
     p.sc_off = (uint32_t)((kSRows * p.pitch + 15) / 16 * 16);
     p.stage_bytes = (uint32_t)((p.sc_off + kSRows * 128 + 127) / 128 * 128);
   } else {
+    // rows padded so the 8 rows of a B fragment start 8 (bf16: 8-byte loads, served per
+    // half warp) or 4 (int8: 4-byte loads) banks apart: no bank conflicts
     const int ES = (m.fmt == MIE_FMT_BF16) ? 2 : 1;
-    p.pitch = (uint32_t)(slice * ES + 16);
+    p.pitch = (uint32_t)(slice * ES + (ES == 2 ? 32 : 16));
     p.stage_bytes = (uint32_t)((kSRows * p.pitch + 127) / 128 * 128);
   }
   p.n_tiles = (m.rows + kSRows - 1) / kSRows;
   int dev = 0, max_smem = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  p.x_pitch = (uint32_t)(slice * 4 + 16);  // 16 spare bytes: the slots' rows start on different banks
+  p.x_pitch = (uint32_t)(slice * 4 + 64);  // slot rows 16 banks apart: a quarter warp's 16-byte reads cover 2 rows
   const long x_bytes = (long)kMaxSlots * p.x_pitch;
   const long avail = (long)max_smem - (long)sizeof(SlotShared) - 1024 - x_bytes;
   int nst = (int)(avail / (long)p.stage_bytes);
