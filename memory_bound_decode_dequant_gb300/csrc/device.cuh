@@ -195,17 +195,6 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
       : "memory");
 }
 
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
 // Orders this thread's generic-proxy accesses to shared memory before later async-proxy
 // (bulk copy) accesses, e.g. before a ring slot written by threads goes back to TMA.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -214,11 +203,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 
 __device__ __forceinline__ void sts16(uint32_t a, uint16_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(a), "h"(v) : "memory");
-}
-
-// Bulk prefetch of global memory into L2 (no shared memory, no completion to wait for).
-__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ uint64_t evict_first_policy() {
@@ -488,33 +472,6 @@ __device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map, int n
     }
   }
   return true;
-}
-
-// Copies tagged words [0, K) of src into the staged vector xs (element k at xs_at(k))
-// once all carry `tag`, zeros from K to Kp.  src is 16-byte aligned.
-template <int NT>
-__device__ bool poll_vector(const uint64_t *src, int K, int Kp, uint32_t tag, float *xs, const int *abort) {
-  const bool ok = poll_pairs<NT, 8>((K + 1) / 2, tag, abort, [&](int j, const uint64_t *&s, float *&d, int &c) {
-    s = src + 2 * j;
-    d = xs + xs_at(2 * j);  // a pair never straddles a padding gap
-    c = (2 * j + 1 < K) ? 2 : 1;
-  });
-  for (int k = K + threadIdx.x; k < Kp; k += NT) xs[xs_at(k)] = 0.f;
-  return ok;
-}
-
-// One tagged word, polled the same way.
-__device__ __forceinline__ bool poll_word(const uint64_t *src, uint32_t tag, float &v, const int *abort) {
-  for (long it = 0;; ++it) {
-    const uint64_t w = ld_tagged(src);
-    if (tag_ok(w, tag)) {
-      v = tag_val(w);
-      return true;
-    }
-    if (it >= kTagPolls) return false;
-    if ((it & 63) == 63 && *reinterpret_cast<const volatile int *>(abort)) return false;
-    __nanosleep(32);
-  }
 }
 
 // What the QKV epilogue needs besides the GEMV results, read before the weights are
