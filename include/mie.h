@@ -97,7 +97,12 @@ mie_status mie_q4_0_pack(const uint8_t *blocks, int M, int K, void *packed, void
  *                  y_i = s_i * sum_k q_ik x_k.
  *   mie_gemv_q4_0: packed: device GPU layout from mie_q4_0_pack; any K >= 1.
  * x: device [K] fp32; y: device [M] fp32 (must not alias x).  1 <= K <= 16384,
- * M >= 1.  MIE_E_SHAPE for other sizes or misaligned pointers. */
+ * M >= 1.  MIE_E_SHAPE for other sizes or misaligned pointers.
+ * Launched with programmatic dependent launch: when the previous kernel on the stream is
+ * one of this library's GEMV, attention or argmax kernels, W starts streaming while that
+ * kernel finishes; x is read and y written only after it has completed.  (None of those
+ * kernels writes weights; the quantise / convert / pack kernels do not release their
+ * successor early.) */
 mie_status mie_gemv_bf16(const uint16_t *W, const float *x, float *y, int M, int K, void *stream);
 mie_status mie_gemv_i8(const int8_t *W, const float *row_scale, const float *x, float *y, int M,
                        int K, void *stream);

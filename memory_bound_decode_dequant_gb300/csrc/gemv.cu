@@ -418,7 +418,9 @@ static mie_status gemv_entry(DevMat m, const float *x, float *y, void *stream) {
   a.m = m;
   a.x = x;
   a.y = y;
-  return launch_gemv(PRO_PLAIN, EPI_STORE, a, gemv_default_grid(m, EPI_STORE), (cudaStream_t)stream, false);
+  // programmatic dependent launch: the weight stream may start during the previous
+  // kernel's tail; x and y are touched only after its completion (see mie.h)
+  return launch_gemv(PRO_PLAIN, EPI_STORE, a, gemv_default_grid(m, EPI_STORE), (cudaStream_t)stream, true);
 }
 
 extern "C" mie_status mie_gemv_bf16(const uint16_t *W, const float *x, float *y, int M, int K, void *stream) {
