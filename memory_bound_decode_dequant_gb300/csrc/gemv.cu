@@ -34,8 +34,9 @@
 
 namespace mie {
 
-constexpr int kCWarps = 8;                    // consumer warps
-constexpr int kThreads = 32 * (kCWarps + 1);  // + one producer warp
+constexpr int kCWarps = 8;                    // consumer warps (12 for large int8 GEMVs, below)
+constexpr int kCWarpsWide = 12;
+constexpr int kWideRows = 32768;
 constexpr int kMaxStages = 16;
 constexpr size_t kSmemMax = 200 * 1024;
 // bf16 rows need little arithmetic per byte: two CTAs per SM (a kernel and its
@@ -64,21 +65,23 @@ int sm_count() {
 }
 
 // Barrier over the consumer warps only (the producer warp never joins it).
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kCWarps * 32) : "memory"); }
+template <int NW>
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(NW * 32) : "memory"); }
+template <int NW>
 struct CSync {
-  __device__ static void sync() { consumer_sync(); }
+  __device__ static void sync() { consumer_sync<NW>(); }
 };
 
 
 // --------------------------------------------------------------- the kernel
 //
-// One CTA per SM: warp kCWarps is the producer, warps 0..kCWarps-1 consume.  A stage
-// is RPS whole rows of the CTA's (contiguous) row range, RPS = kCWarps / KS, so each
+// One CTA per SM: warp NW is the producer, warps 0..NW-1 consume.  A stage
+// is RPS whole rows of the CTA's (contiguous) row range, RPS = NW / KS, so each
 // consumer warp reduces one 2048-column slice of one row per stage.  The producer
 // issues the first ring-full of stages before any dependency wait.
 
-template <int F, int PRO, int EPI>
-__global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const GemvArgs a) {
+template <int F, int PRO, int EPI, int NW>
+__global__ void __launch_bounds__(32 * (NW + 1), kMinBlocks<F>) gemv_kernel(const GemvArgs a) {
   using T = FmtT<F>;
   constexpr int EPC = T::EPC, CPL = T::CPL;
   constexpr int RU = (EPI == EPI_SWIGLU || EPI == EPI_QKV) ? 2 : 1;
@@ -86,9 +89,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
   constexpr int kSliceBytes = kSlice * kBitsPerElem / 8;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
-  __shared__ float red[kCWarps];
-  __shared__ float s_bv[kCWarps];
-  __shared__ int s_bi[kCWarps];
+  __shared__ float red[NW];
+  __shared__ float s_bv[NW];
+  __shared__ int s_bi[NW];
   __shared__ unsigned s_last;
   __shared__ volatile int s_abort, s_issued, s_prod_done;
   __shared__ int s_abort_final;
@@ -99,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
   const int Kp = m.kp, K = m.cols, M = m.rows;
   const int KS = (Kp + kSlice - 1) / kSlice;
   constexpr int RPW = T::RPW;
-  const int WR = KS >= kCWarps ? 1 : kCWarps / KS;  // warps per slice column
+  const int WR = KS >= NW ? 1 : NW / KS;  // warps per slice column
   const int RPS = WR * RPW;                          // rows per stage
   const int NST = a.n_stages;
   const uint32_t stage_bytes = a.stage_bytes, sc_bytes = a.sc_stage_bytes;
@@ -119,7 +122,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&full_bar[i], 1);
-      mbar_init(&empty_bar[i], kCWarps);
+      mbar_init(&empty_bar[i], NW);
     }
     s_abort = 0;
     s_issued = 0;
@@ -129,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
   __syncthreads();
 
   // ---------------------------------------------------------------- producer
-  if (warp == kCWarps) {
+  if (warp == NW) {
     if (lane == 0) {
       const uint64_t pol = evict_first_policy();
       for (int s = 0; s < n_stages; ++s) {
@@ -158,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
 
   // ---------------------------------------------------------------- consumers
   pdl_wait();
-  stage_input<kCWarps * 32, CSync>(a, PRO, xs, K, Kp, red, a.err);
+  stage_input<NW * 32, CSync<NW>>(a, PRO, xs, K, Kp, red, a.err);
   QkvPrefetch qp;
   if constexpr (EPI == EPI_QKV) qp = qkv_prefetch(a);
 
@@ -205,9 +208,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty_bar[slot]);
   }
-  consumer_sync();
+  consumer_sync<NW>();
   if (tid == 0) s_abort_final = s_abort;
-  consumer_sync();
+  consumer_sync<NW>();
   if (s_abort_final) {
     // a wait gave up: make sure no bulk copy is still writing into shared memory
     if (tid == 0) {
@@ -225,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
     if constexpr (F == MIE_FMT_I8) v *= reinterpret_cast<const float *>(m.s)[r];
     return v;
   };
-  constexpr int kCT = kCWarps * 32;
+  constexpr int kCT = NW * 32;
 
   if constexpr (EPI == EPI_STORE || EPI == EPI_RESID) {
     for (int r = row0 + tid; r < row1; r += kCT) {
@@ -259,15 +262,15 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
       if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
     if (lane == 0) { s_bv[warp] = bv; s_bi[warp] = bi; }
-    consumer_sync();
+    consumer_sync<NW>();
     if (tid == 0) {
-      for (int w = 1; w < kCWarps; ++w)
+      for (int w = 1; w < NW; ++w)
         if (better(s_bv[w], s_bi[w], bv, bi)) { bv = s_bv[w]; bi = s_bi[w]; }
       a.am_part[blockIdx.x] = make_float2(bv, __int_as_float(bi));
       __threadfence();
       s_last = (atomicAdd(a.am_count, 1u) == gridDim.x - 1);
     }
-    consumer_sync();
+    consumer_sync<NW>();
     if (s_last) {
       __threadfence();
       float fv = -INFINITY;
@@ -282,11 +285,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks<F>) gemv_kernel(const Gem
         const int oi = __shfl_xor_sync(0xffffffffu, fi, o);
         if (better(ov, oi, fv, fi)) { fv = ov; fi = oi; }
       }
-      consumer_sync();
+      consumer_sync<NW>();
       if (lane == 0) { s_bv[warp] = fv; s_bi[warp] = fi; }
-      consumer_sync();
+      consumer_sync<NW>();
       if (tid == 0) {
-        for (int w = 1; w < kCWarps; ++w)
+        for (int w = 1; w < NW; ++w)
           if (better(s_bv[w], s_bi[w], fv, fi)) { fv = s_bv[w]; fi = s_bi[w]; }
         if (fi == 0x7fffffff) fi = 0;  // all values NaN: fall back to index 0
         if (a.am_out) a.am_out[a.slot] = fi;
@@ -315,11 +318,11 @@ struct Plan {
   size_t smem;
 };
 
-static Plan make_plan(const DevMat &m, int epi, int grid) {
+static Plan make_plan(const DevMat &m, int epi, int grid, int nw) {
   const int RU = (epi == EPI_SWIGLU || epi == EPI_QKV) ? 2 : 1;
   const int n_units = (m.rows + RU - 1) / RU;
   const int KS = (m.kp + kSlice - 1) / kSlice;
-  const int RPS = (KS >= kCWarps ? 1 : kCWarps / KS) * fmt_rows_per_warp(m.fmt);
+  const int RPS = (KS >= nw ? 1 : nw / KS) * fmt_rows_per_warp(m.fmt);
   const int rows_max = ((n_units + grid - 1) / grid) * RU;
   Plan p;
   p.grid = grid;
@@ -337,15 +340,15 @@ static Plan make_plan(const DevMat &m, int epi, int grid) {
   return p;
 }
 
-template <int F, int PRO, int EPI>
+template <int F, int PRO, int EPI, int NW = kCWarps>
 static mie_status launch_t(const GemvArgs &a0, int grid, cudaStream_t st, bool pdl) {
-  const Plan p = make_plan(a0.m, EPI, grid);
+  const Plan p = make_plan(a0.m, EPI, grid, NW);
   if (p.smem > kSmemMax) return fail(MIE_E_SHAPE, "gemv: %zu bytes of shared memory needed", p.smem);
   GemvArgs a = a0;
   a.n_stages = p.n_stages;
   a.stage_bytes = p.stage_bytes;
   a.sc_stage_bytes = p.sc_bytes;
-  auto kern = gemv_kernel<F, PRO, EPI>;
+  auto kern = gemv_kernel<F, PRO, EPI, NW>;
   static bool configured[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -355,7 +358,7 @@ static mie_status launch_t(const GemvArgs &a0, int grid, cudaStream_t st, bool p
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(32 * (NW + 1));
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -369,6 +372,11 @@ static mie_status launch_t(const GemvArgs &a0, int grid, cudaStream_t st, bool p
 
 template <int F>
 static mie_status launch_f(int pro, int epi, const GemvArgs &a, int grid, cudaStream_t st, bool pdl) {
+  // a long int8 stream hides its unpack latency better with 12 consumer warps (128256 x
+  // 2048: 82 -> 87 % of HBM); smaller int8 matrices measured slower with them
+  if constexpr (F == MIE_FMT_I8)
+    if (pro == PRO_PLAIN && epi == EPI_STORE && a.m.rows >= kWideRows)
+      return launch_t<F, PRO_PLAIN, EPI_STORE, kCWarpsWide>(a, grid, st, pdl);
 #define MIE_CASE(P, E) \
   if (pro == P && epi == E) return launch_t<F, P, E>(a, grid, st, pdl);
   MIE_CASE(PRO_PLAIN, EPI_STORE)
