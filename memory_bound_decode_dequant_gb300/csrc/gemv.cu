@@ -372,9 +372,10 @@ static mie_status launch_t(const GemvArgs &a0, int grid, cudaStream_t st, bool p
 
 template <int F>
 static mie_status launch_f(int pro, int epi, const GemvArgs &a, int grid, cudaStream_t st, bool pdl) {
-  // a long int8 stream hides its unpack latency better with 12 consumer warps (128256 x
-  // 2048: 82 -> 87 % of HBM); smaller int8 matrices measured slower with them
-  if constexpr (F == MIE_FMT_I8)
+  // a long int8 or Q4_0 stream hides its unpack latency better with 12 consumer warps
+  // (128256 x 2048: int8 82 -> 91 %, Q4_0 46 -> 49 % of HBM); smaller matrices measured
+  // slower with them
+  if constexpr (F == MIE_FMT_I8 || F == MIE_FMT_Q4_0)
     if (pro == PRO_PLAIN && epi == EPI_STORE && a.m.rows >= kWideRows)
       return launch_t<F, PRO_PLAIN, EPI_STORE, kCWarpsWide>(a, grid, st, pdl);
 #define MIE_CASE(P, E) \
