@@ -211,44 +211,14 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   return pol;
 }
 
-// Dot product of this lane's part of one weight row staged in shared memory with its
-// input registers xr: row = shared address of the row's 2048-column slice, sc = shared
-// address of the slice's Q4_0 scales.  All CPL chunks (and scales) are loaded before
-// any math, so the loads cost one shared-memory latency instead of CPL of them.
-// Chunks at or past Kp are read from the slice start instead (always staged) and meet
-// zero input registers, so they add exact zeros.
-template <int F>
-__device__ __forceinline__ float stage_row_dot(uint32_t row, uint32_t sc, const float2 *xr, int e0, int Kp, int lane) {
-  using T = FmtT<F>;
-  constexpr int EPC = T::EPC, CPL = T::CPL, kChunkStride = 32 * EPC;
-  uint4 w[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c)
-    w[c] = lds128(e0 + c * kChunkStride < Kp ? row + (uint32_t)(c * 32 + lane) * 16 : row);
-  if constexpr (F == MIE_FMT_Q4_0) {
-    uint32_t hb[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) hb[c] = lds16(e0 + c * kChunkStride < Kp ? sc + (uint32_t)(c * 32 + lane) * 2 : sc);
-    float sum = 0.f;
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) {
-      float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-      chunk_fma<F>(w[c], xr + c * (EPC / 2), acc);
-      const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-      sum = fmaf(__half2float(__ushort_as_half((unsigned short)hb[c])), cs, sum);
-    }
-    return sum;
-  } else {
-    float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) chunk_fma<F>(w[c], xr + c * (EPC / 2), acc);
-    return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-  }
-}
-
-// stage_row_dot over the RPW consecutive staged rows of this warp (row addresses
-// row + i*row_bytes, scale rows sc + i*s_bytes): every chunk and scale of all rows is
-// loaded before any math.  nrows (<= RPW) rows are valid; the others read row 0.
+// Dot products of this lane's part of the RPW consecutive weight rows of this warp,
+// staged in shared memory, with its input registers xr: row = shared address of the
+// first row's 2048-column slice (the others at row + i*row_bytes), sc = shared address
+// of its Q4_0 scales (the others at sc + i*s_bytes).  Every chunk and scale of all rows
+// is loaded before any math, so the loads cost one shared-memory latency.  Chunks at or
+// past Kp are read from the slice start instead (always staged) and meet zero input
+// registers, so they add exact zeros.  nrows (<= RPW) rows are valid; the others read
+// the first row.
 template <int F>
 __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes, uint32_t sc, uint32_t s_bytes,
                                                int nrows, const float2 *xr, int e0, int Kp, int lane,
