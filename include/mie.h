@@ -64,8 +64,8 @@ const char *mie_status_string(mie_status s);
 /* fp32 -> bf16, round to nearest even.  w, out: device, n elements. */
 mie_status mie_convert_bf16(const float *w, int64_t n, uint16_t *out, void *stream);
 
-/* int8 with one scale per row ([INFER] design notes: weight-only quantization, "int8
- * per row").  Per row: s = max|w| / 127 (fp32), q = round-half-away(w / s) clamped to
+/* int8 with one scale per row ([INFER] design notes, weight-only quantization: each
+ * row has its own scale).  Per row: s = max|w| / 127 (fp32), q = round-half-away(w / s) clamped to
  * [-127, 127]; a zero row gives s = 0, q = 0.  w: device [M][K] fp32 row-major;
  * q: device [M][K]; scale: device [M]. */
 mie_status mie_quantize_i8(const float *w, int M, int K, int8_t *q, float *scale, void *stream);
@@ -115,8 +115,8 @@ size_t mie_paged_attn_workspace_bytes(int n_q_heads, int n_kv_heads, int head_di
                                       int block_size);
 
 /* Paged GQA decode attention, split over the context with an online softmax and a
- * merge ([MIE] "The KV cache, paged like virtual memory"; [INFER] "GQA-aware split-KV
- * attention"; [RUST] "Lesson 4": running maximum and sum, query heads sharing a KV
+ * merge ([MIE] "The KV cache, paged like virtual memory"; [INFER] design notes, the
+ * split-KV attention item; [RUST] "Lesson 4": running maximum and sum, query heads sharing a KV
  * head read it together).
  *   out[h][d] = sum_{t < ctx_len} softmax_t(scale * q_h . k_{g,t}) v_{g,t}[d],
  *   g = h / (n_q_heads / n_kv_heads).

@@ -1,7 +1,7 @@
 // attn.cu -- paged GQA decode attention and argmax on sm_103a.
 //
 // Attention ("Mini Inference Engine", "The KV cache, paged like virtual memory": the
-// kernel reads K/V through a block table; "infer" page, "GQA-aware split-KV attention":
+// kernel reads K/V through a block table; "infer" page, design notes, the split-KV attention item:
 // one CTA per KV head serves the query heads of its group, the context is split and
 // the partial softmaxes are merged; "Writing an LLM inference engine from scratch in
 // Rust", Lesson 4: an online softmax with a running maximum and sum).

@@ -2,7 +2,7 @@
 // by the standalone attention kernel and the persistent step kernel.
 //
 // "Mini Inference Engine", "The KV cache, paged like virtual memory": K/V are read
-// through a block table; "infer" page, "GQA-aware split-KV attention": the query heads
+// through a block table; "infer" page, design notes, the split-KV attention item: the query heads
 // of one KV head share every K/V load, the context is split and partial softmaxes are
 // merged; "Writing an LLM inference engine from scratch in Rust", Lesson 4: an online
 // softmax with a running maximum and sum.

@@ -9,9 +9,9 @@
  * What it is: a plain, slow, single-threaded CPU implementation of what the decode
  * step computes, written for a reader to check against the pages by eye.  Tensors
  * are stored at the precision the pages fix -- fp32 activations and residual stream,
- * bf16 K/V cache, quantised weights ("infer" page: "bf16 weights, fp32 activations and
- * accumulation, bf16 KV cache"; the reference there rounds K and V to bf16 as the cache
- * does).  Inside one operation every sum is taken in fp64 and the result rounded once
+ * bf16 K/V cache, quantised weights (the "infer" page, design notes: weights in bf16,
+ * activations and sums in fp32, the cache in bf16; its reference rounds K and V to bf16
+ * when they enter the cache).  Inside one operation every sum is taken in fp64 and the result rounded once
  * to fp32, so each function returns its plain definition rounded to the storage type.
  * Compile with -ffp-contract=off so that no multiply-add is fused behind the reader's
  * back (the quantisers' rounding decisions depend on it).
@@ -108,8 +108,9 @@ enum { OR_BF16 = 0, OR_I8 = 1, OR_Q4_0 = 2, OR_F32 = 3 };
 
 /* Q4_0 ([RUST] "Lesson 1" and "Is the 4-bit model still good?"; [INFER] design notes,
  * weight-only quantization): blocks of 32 weights, one 2-byte scale, 4-bit values
- * stored as w + 8 in 0..15.  The scale comes from the value of largest magnitude,
- * sign kept, divided by -8, so that value maps exactly to -8.
+ * stored as w + 8 in 0..15.  The scale is the block's signed extreme (the element
+ * whose magnitude is largest) over -8: that element's code is then exactly -8, the
+ * end of the 4-bit range that has no positive twin.
  * READING: first such element on ties; d = m / -8 in fp32 (exact); stored h = f16(d)
  * rounded to nearest even; codes use the stored scale: id = 1/h (0 when h == 0),
  * q = clamp(floor(w*id + 8.5), 0, 15) with the product and the sum each rounded in
@@ -163,7 +164,8 @@ void or_q4_0_dequantize(const uint8_t *wq, int M, int K, float *w) {
     for (int k = 0; k < K; ++k) w[(int64_t)r * K + k] = q4_0_at(wq, nb, r, k);
 }
 
-/* int8 with one scale per row ([INFER]: "int8 per row", "one scale per row").
+/* int8 with one scale per row ([INFER] design notes, weight-only quantization: each
+ * output row carries its own scale).
  * READING: s = max|w| / 127 in fp32; q = round-half-away(w / s) clamped to
  * [-127, 127]; a zero row has s = 0 and all q = 0. */
 void or_i8_quantize(const float *w, int M, int K, int8_t *q, float *s) {
@@ -220,7 +222,7 @@ void or_gemv(int fmt, const void *W, const float *s, const float *x, int M, int 
 }
 
 /* One row of the embedding table as fp32 (the gather at the start of the step,
- * [INFER] data-flow figure: "token -> Embedding -> x (fp32 residual stream)"). */
+ * [INFER] data-flow figure: the token's embedding row starts the fp32 residual). */
 void or_embed_row(int fmt, const void *E, const float *s, int V, int d, int token, float *x) {
   (void)V;
   const int nb = (d + Q4_BLOCK - 1) / Q4_BLOCK;
@@ -236,8 +238,8 @@ void or_embed_row(int fmt, const void *E, const float *s, int V, int d, int toke
 
 /* ------------------------------------------------------------------ elementwise ops */
 
-/* RMSNorm ([RUST] "How a Llama model generates text"; [INFER] "RMSNorm is applied while
- * the GEMV stages its input"): out_i = x_i / sqrt(mean(x^2) + eps) * g_i. */
+/* RMSNorm ([RUST] "How a Llama model generates text"; [INFER] design notes, fusion:
+ * the norm is folded into the input staging of the next GEMV): out_i = x_i / sqrt(mean(x^2) + eps) * g_i. */
 void or_rmsnorm(const float *x, const float *g, int n, float eps, float *out) {
   double ss = 0.0;
   for (int i = 0; i < n; ++i) ss += (double)x[i] * (double)x[i];
@@ -272,8 +274,8 @@ void or_rope_apply(float *v, int n_heads, int hd, const float *c, const float *s
     }
 }
 
-/* SwiGLU ([RUST] "How a Llama model generates text"; [INFER] "SwiGLU is computed from
- * paired gate/up rows"): a_i = silu(g_i) * u_i, silu(z) = z / (1 + e^-z). */
+/* SwiGLU ([RUST] "How a Llama model generates text"; [INFER] design notes, fusion: the
+ * gate and up rows are read as pairs): a_i = silu(g_i) * u_i, silu(z) = z / (1 + e^-z). */
 void or_swiglu(const float *g, const float *u, int n, float *a) {
   for (int i = 0; i < n; ++i) {
     const double z = g[i];
@@ -333,8 +335,8 @@ static const uint16_t *paged_look(const void *c, int which, int g, int t) {
 }
 
 /* Paged GQA decode attention ([MIE] "The KV cache, paged like virtual memory": a block
- * table maps logical positions to physical 16-token blocks; [INFER] "GQA-aware split-KV
- * attention"; [RUST] "Lesson 4": query heads sharing a KV head).  Query head h reads KV
+ * table maps logical positions to physical 16-token blocks; [INFER] design notes, the
+ * split-KV attention item; [RUST] "Lesson 4": query heads sharing a KV head).  Query head h reads KV
  * head h / (Hq/Hkv).  Key t of KV head g lives in physical block bt[t / bs], slot t % bs:
  * element d at k_pool[blk * block_stride + (g * bs + t % bs) * hd + d] (bf16); the same
  * for v_pool.  out[h][d] = sum_t softmax_t(scale * q_h . k_t) v_t[d]. */
