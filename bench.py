@@ -254,7 +254,7 @@ def gemv_roofline(torch, mie, n_iter: int = 40):
     e1.record(st)
     e1.synchronize()
     dt = e0.elapsed_time(e1) / 1e3 / n_iter
-    algo = M * K * 2 + K * 4 + M * 4
+    algo = synth.gemv_bytes("bf16", M, K)
     del w
     torch.cuda.empty_cache()
     return algo, dt, n_iter
@@ -323,10 +323,7 @@ def run_mie(args, shape):
     e2e_dt = max_over_ranks(pg, (time.perf_counter() - t0) / args.e2e_steps)
 
     # algorithmic bytes of one step: all weights once + the K/V of every position read
-    w_bytes = shape.weight_bytes()
-    mid_ctx = (args.ctx + 1 + ctx_end) / 2
-    kv_bytes = shape.kv_bytes_per_token() * mid_ctx
-    step_bytes = w_bytes + kv_bytes
+    step_bytes = shape.decode_bytes(args.ctx + args.warmup, args.steps)  # the timed steps
     peak, peak_kind = measured_peaks()
 
     result = None
@@ -611,20 +608,20 @@ def run_sweep(args):
                     continue
                 if fmt == "bf16":
                     one = (mie.mie_convert_bf16(w),)
-                    nbytes = M * K * 2
+                    nbytes = synth.matrix_bytes("bf16", M, K)
                     call = lambda a, st: mie.mie_gemv_bf16(a[0], x, y, stream=st)
                 elif fmt == "i8":
                     one = mie.mie_quantize_i8(w)
-                    nbytes = M * K + 4 * M
+                    nbytes = synth.matrix_bytes("i8", M, K)
                     call = lambda a, st: mie.mie_gemv_i8(a[0], a[1], x, y, stream=st)
                 else:
                     one = (mie.mie_q4_0_pack(mie.mie_quantize_q4_0(w), M, K),)
-                    nbytes = M * ((K + 31) // 32) * 18
+                    nbytes = synth.matrix_bytes("q4_0", M, K)
                     call = lambda a, st: mie.mie_gemv_q4_0(a[0], x, M, K, y, stream=st)
                 n = max(least, int(total // nbytes) + 1)
                 copies = [one] + [tuple(t.clone() for t in one) for _ in range(n - 1)]
                 dt = graph_time(torch, [(lambda st, a=a: call(a, st)) for a in copies])
-                algo = nbytes + K * 4 + M * 4
+                algo = synth.gemv_bytes(fmt, M, K)
                 out["gemv"].append({"shape": [M, K], "name": name, "fmt": fmt, "us": dt * 1e6,
                                     "gbs": algo / dt / 1e9, "frac": algo / dt / 1e9 / peak, "launches": n})
                 del copies, one

@@ -177,7 +177,15 @@ class ModelShape:
         return total
 
     def kv_bytes_per_token(self) -> int:
+        """bf16 K and V of one position, every layer."""
         return self.n_layers * 2 * self.n_kv_heads * self.head_dim * 2
+
+    def decode_bytes(self, first_pos: int, n_steps: int) -> float:
+        """Mean algorithmic bytes of one step over n_steps consecutive decode steps whose
+        first writes position first_pos: the weights once, plus the K/V of every position
+        the step attends to (p + 1 of them at position p)."""
+        mean_ctx = first_pos + (n_steps + 1) / 2
+        return self.weight_bytes() + self.kv_bytes_per_token() * mean_ctx
 
 
 def matrix_bytes(fmt: str, m: int, k: int) -> int:
@@ -191,6 +199,12 @@ def matrix_bytes(fmt: str, m: int, k: int) -> int:
     if fmt == "f32":
         return m * k * 4
     raise ValueError(fmt)
+
+
+def gemv_bytes(fmt: str, m: int, k: int) -> int:
+    """Algorithmic bytes of one y = W x launch: the weights once, an fp32 x in, an fp32
+    y out."""
+    return matrix_bytes(fmt, m, k) + 4 * k + 4 * m
 
 
 TINY = ModelShape("tiny", 0, n_layers=2, d_model=256, n_heads=8, n_kv_heads=2, head_dim=32,
