@@ -125,15 +125,25 @@ class Clocks:
                 "reasons": reasons, "samples": len(self.rows)}
 
 
-def dist_init(args):
-    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
-    local = int(os.environ.get("LOCAL_RANK", 0))
+def env_rank() -> tuple[int, int, int]:
+    """(RANK, WORLD_SIZE, LOCAL_RANK) as torchrun sets them; (0, 1, 0) when run alone."""
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def dist_init(args, backend: str = "nccl"):
+    """One process per GPU: each rank runs an independent replica of the step, so the
+    process group carries only the start/stop barriers and the max of the ranks' times."""
+    rank, world, local = env_rank()
     pg = None
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group(backend)
         pg = dist
     return rank, world, local, pg
 
@@ -147,7 +157,8 @@ def max_over_ranks(pg, v: float) -> float:
     if pg is None:
         return v
     import torch
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
 
@@ -178,8 +189,7 @@ def time_oracle(shape, ctx: int, steps: int):
 
 
 def run_reference(args, shape):
-    rank, world, local, pg = dist_init(args)
-    if rank != 0:
+    if env_rank()[0] != 0:  # under torchrun rank 0 alone times the oracle
         return
     steps = max(1, args.steps)
     om, bt = oracle_model(shape, args.ctx, args.warmup + steps)
@@ -205,8 +215,7 @@ def run_reference(args, shape):
 
 
 def run_reference_slots(args):
-    rank, world, local, pg = dist_init(args)
-    if rank != 0:
+    if env_rank()[0] != 0:
         return
     shape = synth.llama32_1b("bf16")
     wl = synth.SlotWorkload()
