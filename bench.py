@@ -232,13 +232,48 @@ def run_reference_slots(args):
 
 # ----------------------------------------------------------------------------- GPU arm
 
+CSRC = os.path.join(ROOT, "memory_bound_decode_dequant_gb300", "csrc")
+
+
+def source_digest(unit: str) -> str:
+    """Digest of a translation unit under csrc/ and every local header it includes, with
+    comments and layout removed: it changes when the compiled code can, not when a
+    comment does."""
+    import hashlib
+    import re
+    seen, order, todo = set(), [], [os.path.normpath(os.path.join(CSRC, unit))]
+    while todo:
+        path = todo.pop()
+        if path in seen:
+            continue
+        seen.add(path)
+        order.append(path)
+        with open(path) as f:
+            text = f.read()
+        for inc in re.findall(r'^\s*#include\s+"([^"]+)"', text, flags=re.M):
+            todo.append(os.path.normpath(os.path.join(os.path.dirname(path), inc)))
+    h = hashlib.sha256()
+    for path in sorted(order):
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(os.path.relpath(path, ROOT).encode() + b"\0" + " ".join(text.split()).encode() + b"\0")
+    return h.hexdigest()[:16]
+
+
 def read_traffic(name: str):
-    """DRAM bytes per launch of a kernel from its ncu summary under profiles/, or None."""
+    """DRAM bytes per launch of a kernel from its ncu record under profiles/, or None when
+    there is no record or the kernel's source has changed since the counters were taken."""
     tp = os.path.join(ROOT, "profiles", f"{name}.traffic.json")
-    if os.path.exists(tp):
-        with open(tp) as f:
-            return json.load(f).get("bytes_per_launch")
-    return None
+    if not os.path.exists(tp):
+        return None
+    with open(tp) as f:
+        rec = json.load(f)
+    unit, digest = rec.get("translation_unit"), rec.get("source_digest")
+    if not unit or not digest or source_digest(unit) != digest:
+        return None
+    return rec.get("bytes_per_launch")
 
 
 def gemv_roofline(torch, mie, n_iter: int = 40):
