@@ -392,6 +392,20 @@ class Model:
             raise ValueError("oracle decode step rejected its arguments")
         return logits, r
 
+    def decode_step_slots(self, tokens, pos, block_tables) -> tuple[np.ndarray, np.ndarray]:
+        """One step of every slot: tokens[s] at pos[s] through block_tables[s] (one row of
+        the [n_slots, max_blocks] table per slot); returns ([n_slots, vocab] logits, argmax)."""
+        t, p = _c(tokens, np.int32), _c(pos, np.int32)
+        bt = _c(block_tables, np.int32)
+        n = t.size
+        assert p.size == n and bt.ndim == 2 and bt.shape[0] == n
+        logits = np.empty((n, self.shape.vocab), np.float32)
+        best = np.empty(n, np.int32)
+        r = lib().or_decode_step_slots(self.h, n, _p(t), _p(p), _p(bt), bt.shape[1], _p(logits), _p(best))
+        if r < 0:
+            raise ValueError("oracle slot step rejected its arguments")
+        return logits, best
+
     def forward_nocache(self, tokens) -> tuple[np.ndarray, int]:
         t = _c(tokens, np.int32)
         logits = np.empty(self.shape.vocab, np.float32)

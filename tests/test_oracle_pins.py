@@ -493,3 +493,70 @@ def test_step_rejects_bad_arguments(orc):
     bad[0] = 99
     with pytest.raises(ValueError):
         m.decode_step(1, 0, bad)
+
+
+def test_slots_sharing_a_prefix_equal_independent_sequences(orc):
+    """Few-slot step: three slots that borrow one 40-token prefix (two whole blocks shared,
+    the half-filled third copied on write by the two borrowers) and then continue with
+    their own tokens give, bit for bit, the logits of each sequence decoded alone in a
+    fresh cache with its own blocks ("Mini Inference Engine", "Prefix sharing and
+    copy-on-write", "Continuous batching")."""
+    shape, bs = synth.TINY, synth.TINY.block_size
+    n_pre, n_gen, S, max_blocks = 40, 6, 3, 8
+    prefix = shape.tokens(n_pre, stream=11)
+    cont = [shape.tokens(n_gen, stream=12 + s) for s in range(S)]
+
+    m = _tiny_model(orc, n_blocks=24)
+    kv = m.kv()
+    tables = np.full((S, max_blocks), -1, np.int32)
+    tables[0, :3] = [5, 9, 2]
+    for pos, t in enumerate(prefix):
+        m.decode_step(int(t), pos, tables[0])
+    spare = [11, 3, 17, 20, 7, 13, 0, 22, 15]
+    for s in (1, 2):
+        tables[s, :3] = tables[0, :3]
+        # the first write of slot s lands in the shared, half-filled block: copy, then swap
+        nb = spare.pop()
+        kv[nb] = kv[tables[s, 2]]
+        tables[s, 2] = nb
+    for s in range(S):
+        tables[s, 3:5] = [spare.pop(), spare.pop()] if s else [1, 4]
+    got = []
+    for i in range(n_gen):
+        logits, best = m.decode_step_slots([int(c[i]) for c in cont], [n_pre + i] * S, tables)
+        got.append((logits.copy(), best.copy()))
+
+    for s in range(S):
+        alone = _tiny_model(orc, n_blocks=24)
+        bt = np.arange(24, dtype=np.int32)
+        for pos, t in enumerate(prefix):
+            alone.decode_step(int(t), pos, bt)
+        for i in range(n_gen):
+            ref, rbest = alone.decode_step(int(cont[s][i]), n_pre + i, bt)
+            assert np.array_equal(got[i][0][s], ref), (s, i)
+            assert got[i][1][s] == rbest
+
+
+def test_slots_sharing_without_copy_on_write_diverge(orc):
+    """The copy above is needed: if a borrower writes into the shared half-filled block
+    in place, the owner's later logits change (the pin would catch a missing copy)."""
+    shape = synth.TINY
+    n_pre = 40
+    prefix = shape.tokens(n_pre, stream=11)
+    m = _tiny_model(orc, n_blocks=24)
+    tables = np.full((2, 8), -1, np.int32)
+    tables[0, :4] = [5, 9, 2, 1]
+    tables[1, :4] = [5, 9, 2, 4]  # block 2 shared, no copy
+    for pos, t in enumerate(prefix):
+        m.decode_step(int(t), pos, tables[0])
+    a = shape.tokens(2, stream=21)
+    b = shape.tokens(2, stream=22)
+    m.decode_step_slots([int(a[0]), int(b[0])], [n_pre, n_pre], tables)  # both write position 40
+    logits, _ = m.decode_step_slots([int(a[1]), int(b[1])], [n_pre + 1, n_pre + 1], tables)
+
+    alone = _tiny_model(orc, n_blocks=24)
+    bt = np.arange(24, dtype=np.int32)
+    for pos, t in enumerate(list(prefix) + [int(a[0])]):
+        alone.decode_step(int(t), pos, bt)
+    ref, _ = alone.decode_step(int(a[1]), n_pre + 1, bt)
+    assert not np.array_equal(logits[0], ref)
