@@ -186,8 +186,11 @@ mie_status mie_pool_create(int n_blocks, mie_pool **out);
 void mie_pool_destroy(mie_pool *p);
 /* *id = a block with refcount 1, or -1 and MIE_E_OOM when the pool is exhausted. */
 mie_status mie_pool_alloc(mie_pool *p, int32_t *id);
+/* Adds a reference to a live block (a sequence borrowing it); MIE_E_ARG for an id out
+ * of range or not live. */
 mie_status mie_pool_incref(mie_pool *p, int32_t id);
-/* Drops one reference; a block reaching 0 returns to the free list. */
+/* Drops one reference; a block reaching 0 returns to the free list.  MIE_E_ARG for an
+ * id out of range or not live. */
 mie_status mie_pool_decref(mie_pool *p, int32_t id);
 int mie_pool_refcount(const mie_pool *p, int32_t id); /* -1 for an id out of range */
 int mie_pool_free_count(const mie_pool *p);
@@ -241,11 +244,15 @@ mie_status mie_load_weights(mie_ctx *ctx, const char *name, int fmt, const void 
                             size_t bytes, const int64_t *shape, int ndim,
                             const float *host_scale);
 
+/* The context's host block pool (n_kv_blocks blocks), owned by the context: valid until
+ * mie_destroy, never passed to mie_pool_destroy. */
 mie_pool *mie_ctx_pool(mie_ctx *ctx);
-/* Device pointer of the KV pool and the elements of one block (all layers, k and v). */
+/* Device pointer of the KV pool (owned by the context) and the elements of one block
+ * (all layers, k and v). */
 uint16_t *mie_kv_pool(mie_ctx *ctx);
 int64_t mie_kv_block_elems(const mie_ctx *ctx);
-/* Enqueues a device copy of block src into block dst (copy-on-write). */
+/* Enqueues a device copy of block src into block dst (copy-on-write) on the context's
+ * stream; MIE_E_ARG for a block id outside 0..n_kv_blocks-1. */
 mie_status mie_kv_copy_block(mie_ctx *ctx, int32_t src, int32_t dst);
 
 /* One decode step ([INFER] data-flow figure; [RUST] "How a Llama model generates
