@@ -104,7 +104,13 @@ struct mie_ctx {
   float2 *am_part = nullptr;
   unsigned *am_count = nullptr;
   StepParams *sp = nullptr;
-  StepParams sp_host{};
+  // Host side of the step parameters: a ring of pinned buffers, so each upload is a DMA
+  // that runs in stream order; a buffer is rewritten only after the event recorded
+  // behind its previous upload has fired.
+  static constexpr int kParamRing = 8;
+  StepParams *sp_pinned = nullptr;
+  cudaEvent_t sp_uploaded[kParamRing] = {};
+  int sp_next = 0;
   int *err = nullptr;
   cudaGraphExec_t graph = nullptr;
   bool graph_ok = true;  // false: the step is launched directly (capture unsupported)
@@ -183,6 +189,9 @@ extern "C" void mie_destroy(mie_ctx *ctx) {
   if (ctx->graph) cudaGraphExecDestroy(ctx->graph);
   if (ctx->slot_graph) cudaGraphExecDestroy(ctx->slot_graph);
   for (void *p : ctx->allocs) cudaFree(p);
+  for (cudaEvent_t ev : ctx->sp_uploaded)
+    if (ev) cudaEventDestroy(ev);
+  if (ctx->sp_pinned) cudaFreeHost(ctx->sp_pinned);
   if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
   mie_pool_destroy(ctx->pool);
   delete ctx;
@@ -242,6 +251,19 @@ extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **
   if (!ok) {
     mie_destroy(ctx);
     return fail(MIE_E_OOM, "mie_create: device allocation of %zu KV bytes failed", kv_bytes);
+  }
+  if (cudaMallocHost((void **)&ctx->sp_pinned, sizeof(StepParams) * mie_ctx::kParamRing) != cudaSuccess) {
+    ctx->sp_pinned = nullptr;
+    mie_destroy(ctx);
+    return fail(MIE_E_OOM, "mie_create: pinned host allocation of the step parameters");
+  }
+  for (cudaEvent_t &ev : ctx->sp_uploaded) {
+    const cudaError_t r = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (r != cudaSuccess) {
+      ev = nullptr;
+      mie_destroy(ctx);
+      return cuda_fail(r, "mie_create: cudaEventCreate");
+    }
   }
   ctx->attn_ws = ws;
   cudaError_t e = cudaSuccess;
@@ -726,6 +748,17 @@ static mie_status run_step(mie_ctx *ctx) {
   return enqueue_step(ctx, &n);
 }
 
+// Copies the step parameters to the device from the next pinned buffer of the ring.
+static mie_status upload_params(mie_ctx *ctx, const StepParams &p) {
+  const int i = ctx->sp_next;
+  ctx->sp_next = (i + 1) % mie_ctx::kParamRing;
+  MIE_CUDA(cudaEventSynchronize(ctx->sp_uploaded[i]));  // the buffer's previous upload has run
+  ctx->sp_pinned[i] = p;
+  MIE_CUDA(cudaMemcpyAsync(ctx->sp, ctx->sp_pinned + i, sizeof p, cudaMemcpyHostToDevice, ctx->stream));
+  MIE_CUDA(cudaEventRecord(ctx->sp_uploaded[i], ctx->stream));
+  return MIE_OK;
+}
+
 extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, const int32_t *block_table,
                                       int n_blocks, float *logits_out, int32_t *argmax_out) {
   if (!ctx || !block_table) return fail(MIE_E_ARG, "mie_decode_step: null pointer");
@@ -735,7 +768,7 @@ extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, 
   if (pos < 0 || pos >= c.max_pos) return fail(MIE_E_ARG, "mie_decode_step: pos %d outside [0, %d)", pos, c.max_pos);
   if (n_blocks < 1 || pos / c.block_size >= n_blocks)
     return fail(MIE_E_ARG, "mie_decode_step: pos %d needs more than %d blocks", pos, n_blocks);
-  StepParams &p = ctx->sp_host;
+  StepParams p;
   memset(&p, 0, sizeof p);
   p.token[0] = token;
   p.pos[0] = pos;
@@ -745,7 +778,8 @@ extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, 
   p.logits_out = logits_out;
   p.argmax_out = argmax_out;
   p.advance = 1;
-  MIE_CUDA(cudaMemcpyAsync(ctx->sp, &p, sizeof p, cudaMemcpyHostToDevice, ctx->stream));
+  const mie_status su = upload_params(ctx, p);
+  if (su != MIE_OK) return su;
   if (!ctx->primed) {
     mie_status s = capture(ctx);
     if (s != MIE_OK) return s;
@@ -836,7 +870,7 @@ extern "C" mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int
     if (pos[s] / c.block_size >= max_blocks)
       return fail(MIE_E_ARG, "mie_decode_step_slots: slot %d pos %d needs more than %d blocks", s, pos[s], max_blocks);
   }
-  StepParams &p = ctx->sp_host;
+  StepParams p;
   memset(&p, 0, sizeof p);
   for (int s = 0; s < n_slots; ++s) {
     p.token[s] = tokens[s];
@@ -848,7 +882,8 @@ extern "C" mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int
   p.logits_out = logits_out;
   p.argmax_out = argmax_out;
   p.advance = 0;
-  MIE_CUDA(cudaMemcpyAsync(ctx->sp, &p, sizeof p, cudaMemcpyHostToDevice, ctx->stream));
+  const mie_status su = upload_params(ctx, p);
+  if (su != MIE_OK) return su;
   if (!ctx->slot_primed) {
     const mie_status s = capture_slots(ctx);
     if (s != MIE_OK) return s;

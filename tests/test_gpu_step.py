@@ -162,6 +162,38 @@ def test_device_continuation_matches_host_steps(orc, step_mode):
     assert outs[0][1] == outs[1][1]
 
 
+@pytest.mark.parametrize("step_mode", [PERSISTENT, CHAIN])
+def test_back_to_back_host_steps_without_waiting(orc, step_mode):
+    """30 host-driven steps enqueued with no host wait between them (more than the ring
+    of 8 pinned parameter buffers) give the bits of the same steps each followed by a
+    sync, and the oracle's logits."""
+    shape = synth.TINY
+    n_blocks, max_pos, n = 8, 128, 30
+    bt_host = synth.permutation(4, n_blocks).astype(np.int32)
+    bt = torch.from_numpy(bt_host).cuda()
+    toks = prompt_tokens(shape, n)
+    outs = []
+    for wait in (False, True):
+        gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+        gm.set_step_mode(step_mode)
+        logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+        am = torch.empty(1, dtype=torch.int32, device="cuda")
+        for pos, t in enumerate(toks):
+            gm.decode_step(int(t), pos, bt, logits, am)
+            if wait:
+                gm.sync()
+        gm.sync()
+        outs.append((logits.cpu().numpy(), int(am.item())))
+        gm.close()
+    assert np.array_equal(outs[0][0].view(np.uint32), outs[1][0].view(np.uint32))
+    assert outs[0][1] == outs[1][1]
+    om = orc.Model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+    for pos, t in enumerate(toks):
+        ref, best = om.decode_step(int(t), pos, bt_host)
+    check_logits(outs[0][0], ref, n - 1)
+    check_argmax(outs[0][1], ref, n - 1)
+
+
 def test_step_rejects_bad_inputs():
     shape = synth.TINY
     gm = build_gpu_model(shape, n_kv_blocks=4, max_pos=64)
