@@ -10,9 +10,10 @@
 //  * One CTA per SM owns a contiguous range of rows.  A producer warp streams that
 //    range through a ring of shared-memory stages with TMA bulk copies
 //    (cp.async.bulk, completion on mbarriers, L2 evict-first), so tens of KB per SM
-//    are in flight without holding registers.  It issues the first ring-full before
-//    griddepcontrol.wait: inside the step graph the weights of kernel N+1 stream in
-//    while kernel N finishes.
+//    are in flight without holding registers.  The producer never waits on the
+//    previous kernel (weights do not depend on it); only the consumers execute
+//    griddepcontrol.wait before they read the input vector, so under programmatic
+//    dependent launch the weights of kernel N+1 stream in while kernel N finishes.
 //  * Each consumer warp owns one 2048-column slice of K; its slice of the normalised
 //    input vector sits in 64 registers per lane for the whole kernel, so per 16-byte
 //    chunk the inner loop is one shared-memory load, an in-register unpack and packed
