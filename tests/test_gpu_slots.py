@@ -127,6 +127,13 @@ def test_slots_long_context_loops_over_splits(orc):
               n_blocks=300, max_pos=4224)
 
 
+@pytest.mark.parametrize("fmt", ["bf16", "q4_0"])
+def test_eight_slots_the_maximum(orc, fmt):
+    """All eight slots (the largest batch a context takes) with uneven contexts."""
+    shape = replace(synth.TINY, wfmt=fmt, head_fmt=fmt)
+    run_slots(orc, shape, n_slots=8, max_slots=8, prompts=[40, 37, 21, 50, 18, 33, 45, 26], n_gen=3)
+
+
 def test_fewer_slots_than_the_context_holds(orc):
     """n_slots < max_slots: the unused slots' lanes of every tile carry zeros."""
     shape = replace(synth.TINY, wfmt="bf16", head_fmt="bf16")
