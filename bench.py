@@ -38,6 +38,7 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 STEP_PARAMS_BYTES = 112  # sizeof(StepParams): copied host -> device per host-driven step
+SPEC_HBM_GBS = 7900.0  # GB300 HBM3e, nominal; every fraction is also given against it
 
 
 def parse():
@@ -376,7 +377,8 @@ def run_mie(args, shape):
         achieved = algo / kdt / 1e9
         gemv_roof = {"bound": "hbm", "kernel": "gemv bf16 16384x2048 (gate/up shape), standalone",
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": read_traffic("gemv_bf16_16384x2048"),
+                     "frac": achieved / peak, "frac_of_spec": achieved / SPEC_HBM_GBS,
+                     "traffic": read_traffic("gemv_bf16_16384x2048"),
                      "algorithmic_bytes": algo, "launches_timed": n_iter, "us_per_launch": kdt * 1e6}
         if gm.step_mode == 0:
             # the persistent step is the step's only launch: its duration is the step time
@@ -384,6 +386,7 @@ def run_mie(args, shape):
             ach = step_bytes / dt / 1e9
             roof = {"bound": "hbm", "kernel": "persistent_step (one launch = one decode step)",
                     "achieved": ach, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": ach / peak,
+                    "frac_of_spec": ach / SPEC_HBM_GBS,
                     "traffic": read_traffic(f"persistent_step_llama32_{args.fmt}"),
                     "algorithmic_bytes": step_bytes, "launches_timed": args.steps, "us_per_launch": dt * 1e6}
         else:
@@ -415,7 +418,8 @@ def run_mie(args, shape):
                        "ctx_range": [args.ctx, ctx_end], "parallelism": "replicas" if world > 1 else "single",
                        "l2": "weights 2.47 GB per step >> 129 MB L2: inputs larger than L2",
                        "step_bytes": step_bytes, "step_hbm_gbs": step_bytes / dt / 1e9,
-                       "step_frac_of_peak": step_bytes / dt / 1e9 / peak},
+                       "step_frac_of_peak": step_bytes / dt / 1e9 / peak,
+                       "step_frac_of_spec": step_bytes / dt / 1e9 / SPEC_HBM_GBS},
             "roofline": roof,
             "gemv_roofline": gemv_roof,
             "e2e": {"value": world / e2e_dt, "unit": "tok/s", "h2d_bytes_per_step": STEP_PARAMS_BYTES,
@@ -563,7 +567,8 @@ def run_slots(args):
                        "step_bytes": step_bytes, "kv_bytes_per_step": kv_bytes},
             "roofline": {"bound": "hbm", "kernel": "whole few-slot step (kernel chain in one graph)",
                          "achieved": ach, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": ach / peak, "traffic": None, "algorithmic_bytes": step_bytes,
+                         "frac": ach / peak, "frac_of_spec": ach / SPEC_HBM_GBS, "traffic": None,
+                         "algorithmic_bytes": step_bytes,
                          "us_per_step": dt * 1e6},
             "e2e": {"value": world * S / e2e_dt, "unit": "tok/s", "h2d_bytes_per_step": STEP_PARAMS_BYTES,
                     "d2h_bytes_per_step": 4 * S},
