@@ -23,6 +23,10 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
  *    Kernel entry points only enqueue work: results are ready once the stream is
  *    synchronised.  Arguments are validated on the host before anything is enqueued.
+ *  - A model context (mie_ctx) may be used by one host thread at a time; distinct
+ *    contexts are independent.  A block pool serialises its calls internally (one
+ *    lock per pool).  Stateless entry points may be called from several threads; the
+ *    scratch of mie_paged_attn_decode_noalloc is the one shared resource (see there).
  *  - Storage formats: MIE_FMT_BF16 (uint16 bit patterns), MIE_FMT_I8 (int8 plus one
  *    fp32 scale per row), MIE_FMT_Q4_0 (blocks of 32 four-bit codes plus one f16
  *    scale), MIE_FMT_F32.
