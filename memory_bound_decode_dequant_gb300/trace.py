@@ -4,9 +4,9 @@ python -m memory_bound_decode_dequant_gb300.trace [--fmt bf16|i8|q4_0] [--ctx 12
 
 Builds the Llama-3.2-1B-shape model from the seeded synthetic weights, fills the
 context with real decode steps, switches the step to the persistent kernel, records one
-step and prints, per phase kind averaged over the layers: the spread of the grid
-barrier, the input staging, the weight streaming (mean and slowest CTA), the epilogue
-and the phase's span, in microseconds.
+step and prints, per phase kind averaged over the layers: the spread over CTAs of the
+moment the phase's input arrived, the input staging, the weight streaming (mean and
+slowest CTA), the epilogue and the phase's span, in microseconds.
 """
 from __future__ import annotations
 
@@ -17,12 +17,13 @@ import numpy as np
 
 
 def summarise(t: np.ndarray, n_layers: int) -> dict:
-    """t: [phases, ctas, 5] nanoseconds -> per-kind means in microseconds."""
+    """t: [phases, ctas, 5] nanoseconds (points: entry, input arrived, input staged,
+    stages consumed, outputs written) -> per-kind means over the layers, microseconds."""
     t = (t.astype(np.float64) - float(t[:, :, 0].min())) / 1e3
     names = ["qkv", "attn", "o", "gu", "down"] * n_layers + ["head"]
     agg: dict = {}
     for p, name in enumerate(names):
-        d = {"barrier_spread": t[p, :, 1].max() - t[p, :, 1].min(),
+        d = {"input_spread": t[p, :, 1].max() - t[p, :, 1].min(),
              "staging": float(np.mean(t[p, :, 2] - t[p, :, 1])),
              "stream_mean": float(np.mean(t[p, :, 3] - t[p, :, 2])),
              "stream_max": float(np.max(t[p, :, 3] - t[p, :, 2])),
