@@ -524,7 +524,8 @@ def run_slots(args):
                 for b in range(need):
                     row[b] = pool.alloc()
                 tables[s] = row
-                tdev[s].copy_(torch.from_numpy(row), non_blocking=True)
+                with torch.cuda.stream(stream):  # ordered before the next step on its stream
+                    tdev[s].copy_(torch.from_numpy(row))
                 pos[s] = new_len
             gm.decode_step_slots(toks[args.warmup + i], pos, tdev, logits, am)
             kv_tokens += int(pos.sum()) + S
