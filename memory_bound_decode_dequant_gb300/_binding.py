@@ -443,3 +443,128 @@ class Model:
         _check(lib().mie_set_trace(self.h, buf.data_ptr(), buf.numel() * 8, None, None), "mie_set_trace")
         self._trace = buf
         return buf
+
+
+# ------------------------------------------------ the context and pool calls by C name
+#
+# The same entry points as the methods above, under the names include/mie.h gives them:
+# `ctx` is a Model (mie_ctx), `pool` a Pool (mie_pool).
+
+def mie_last_error() -> str:
+    return lib().mie_last_error().decode(errors="replace")
+
+
+def mie_status_string(status: int) -> str:
+    return lib().mie_status_string(int(status)).decode(errors="replace")
+
+
+def mie_pool_create(n_blocks: int) -> Pool:
+    return Pool(n_blocks)
+
+
+def mie_pool_destroy(pool: Pool) -> None:
+    if pool._own and pool.h:
+        lib().mie_pool_destroy(pool.h)
+        pool.h = None
+
+
+def mie_pool_alloc(pool: Pool) -> int:
+    """A block id, or -1 when the pool is exhausted."""
+    return pool.alloc()
+
+
+def mie_pool_incref(pool: Pool, block: int) -> None:
+    _check(pool.incref(block), "mie_pool_incref")
+
+
+def mie_pool_decref(pool: Pool, block: int) -> None:
+    _check(pool.decref(block), "mie_pool_decref")
+
+
+def mie_pool_refcount(pool: Pool, block: int) -> int:
+    return pool.refcount(block)
+
+
+def mie_pool_free_count(pool: Pool) -> int:
+    return pool.free_count()
+
+
+def mie_pool_writable(pool: Pool, table: np.ndarray, pos: int, block_size: int):
+    """(block, copy_src, copy_dst) with the table updated in place; MieError (out of
+    memory) when no block is free."""
+    st, b, s, d = pool.writable(table, pos, block_size)
+    _check(st, "mie_pool_writable")
+    return b, s, d
+
+
+def mie_create(cfg: dict, stream=None) -> Model:
+    return Model(cfg, stream)
+
+
+def mie_destroy(ctx: Model) -> None:
+    ctx.close()
+
+
+def mie_load_weights(ctx: Model, name: str, data: np.ndarray, fmt: str = "f32",
+                     scale: np.ndarray | None = None, cols: int | None = None) -> None:
+    ctx.load_weights(name, data, fmt, scale, cols)
+
+
+def mie_ctx_pool(ctx: Model) -> Pool:
+    return ctx.pool
+
+
+def mie_kv_pool(ctx: Model):
+    return ctx.kv()
+
+
+def mie_kv_block_elems(ctx: Model) -> int:
+    return ctx.block_elems
+
+
+def mie_kv_copy_block(ctx: Model, src: int, dst: int) -> None:
+    ctx.kv_copy_block(src, dst)
+
+
+def mie_decode_step(ctx: Model, token: int, pos: int, block_table, logits_out=None, argmax_out=None) -> None:
+    ctx.decode_step(token, pos, block_table, logits_out, argmax_out)
+
+
+def mie_decode_continue(ctx: Model, n_steps: int) -> None:
+    ctx.decode_continue(n_steps)
+
+
+def mie_decode_step_slots(ctx: Model, tokens, pos, block_tables, logits_out=None, argmax_out=None) -> None:
+    ctx.decode_step_slots(tokens, pos, block_tables, logits_out, argmax_out)
+
+
+def mie_set_step_mode(ctx: Model, mode: int) -> None:
+    ctx.set_step_mode(mode)
+
+
+def mie_step_mode(ctx: Model) -> int:
+    return ctx.step_mode
+
+
+def mie_set_trace(ctx: Model, enable: bool = True):
+    return ctx.set_trace(enable)
+
+
+def mie_sync(ctx: Model) -> None:
+    ctx.sync()
+
+
+def mie_step_launches(ctx: Model) -> int:
+    return ctx.launches
+
+
+def mie_slot_step_launches(ctx: Model) -> int:
+    return ctx.slot_launches
+
+
+__all__ += ["mie_last_error", "mie_status_string", "mie_pool_create", "mie_pool_destroy", "mie_pool_alloc",
+            "mie_pool_incref", "mie_pool_decref", "mie_pool_refcount", "mie_pool_free_count",
+            "mie_pool_writable", "mie_create", "mie_destroy", "mie_load_weights", "mie_ctx_pool",
+            "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_decode_step",
+            "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
+            "mie_set_trace", "mie_sync", "mie_step_launches", "mie_slot_step_launches"]

@@ -123,3 +123,32 @@ def test_config_checks_need_no_gpu(L):
     with pytest.raises(mie.MieError) as e:
         mie.Model(dict(cfg, max_slots=9), stream=0)
     assert e.value.status == 2
+
+
+def test_binding_has_every_declared_name(L):
+    """The Python binding offers each entry point of the header under its C name."""
+    missing = [n for n in mie.header_functions() if not callable(getattr(mie, n, None))]
+    assert not missing, missing
+
+
+def test_pool_calls_by_c_name(L):
+    p = mie.mie_pool_create(3)
+    assert [mie.mie_pool_alloc(p) for _ in range(3)] == [0, 1, 2]
+    assert mie.mie_pool_alloc(p) == -1
+    mie.mie_pool_incref(p, 1)
+    assert mie.mie_pool_refcount(p, 1) == 2
+    table = np.array([1, -1], np.int32)
+    with pytest.raises(mie.MieError) as e:  # block 1 is shared and the pool is empty
+        mie.mie_pool_writable(p, table, 3, 16)
+    assert e.value.status == 3 and table[0] == 1
+    mie.mie_pool_decref(p, 2)
+    assert mie.mie_pool_free_count(p) == 1
+    blk, src, dst = mie.mie_pool_writable(p, table, 3, 16)  # copy-on-write into block 2
+    assert (blk, src, dst) == (2, 1, 2) and table[0] == 2 and mie.mie_pool_refcount(p, 1) == 1
+    with pytest.raises(mie.MieError) as e:
+        mie.mie_pool_decref(p, 7)
+    assert e.value.status == 1
+    assert mie.mie_status_string(3) == "out of memory"
+    assert "mie_pool_decref" in mie.mie_last_error() or "not live" in mie.mie_last_error()
+    mie.mie_pool_destroy(p)
+    assert p.h is None
