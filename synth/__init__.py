@@ -32,7 +32,7 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile synth.c into libsynth.<machine>.so next to it (gcc, no target-specific
-    flags; one file per host architecture, since the tree is shared with an Arm machine)."""
+    flags; one file per host architecture, so x86-64 and AArch64 builds sit side by side)."""
     src = os.path.join(_HERE, "synth.c")
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
         tmp = _SO + f".tmp{os.getpid()}"
