@@ -482,6 +482,58 @@ def test_step_composition_at_position_zero(orc):
     assert np.array_equal(logits, ref) and best == oracle.argmax(ref)
 
 
+def test_step_composition_at_a_later_position(orc):
+    """At position 20 (two blocks, a permuted table) one layer is the pinned parts
+    composed, bit for bit: per position the normed input, the QKV GEMV, RoPE on q and k
+    (not v) with that position's angles, K and V rounded to bf16 into the cache; then
+    attention of the last q over all 21 positions with scale fp32(1/sqrt(hd)), O-proj and
+    residual, the MLP and the head.  Unlike position 0 (where attention returns v), this
+    fixes the rotation, the scale, the GQA head mapping and the cache positions.  The
+    same composition with RoPE left out of k differs, so the check has teeth."""
+    import math
+
+    import oracle
+    shape = synth.TINY
+    m = _tiny_model(orc, layers=1)
+    d, hd, Hq, Hkv = shape.d_model, shape.head_dim, shape.n_heads, shape.n_kv_heads
+    gains = [synth.normal(200 + i, d) + 2 for i in range(3)]
+    lib = oracle.lib()
+    for which, g in zip((5, 6), gains[:2]):
+        lib.or_model_set(m.h, which, 0, 3, g.ctypes.data, None, 1, d)
+    lib.or_model_set(m.h, 102, 0, 3, gains[2].ctypes.data, None, 1, d)
+    m._keep += gains
+    toks = shape.tokens(21, stream=5)
+    bt = synth.permutation(8, 16).astype(np.int32)
+    for pos, t in enumerate(toks):
+        logits, best = m.decode_step(int(t), pos, bt)
+
+    M, eps = m.mats, shape.rms_eps
+    cos, sin = oracle.rope_table(128, hd, shape.rope_theta)
+    hq, hk = Hq * hd, Hkv * hd
+
+    def compose(rope_k: bool):
+        K, V = [], []
+        for pos, t in enumerate(toks):
+            x = oracle.embed_row(M["embed"], int(t))
+            qkv = oracle.gemv(M["l0.qkv"], oracle.rmsnorm(x, gains[0], eps))
+            q = oracle.rope_apply(qkv[:hq], Hq, hd, cos[pos], sin[pos])
+            k = qkv[hq:hq + hk]
+            if rope_k:
+                k = oracle.rope_apply(k, Hkv, hd, cos[pos], sin[pos])
+            K.append(oracle.to_bf16(k))
+            V.append(oracle.to_bf16(qkv[hq + hk:]))
+        att = oracle.attention_contig(q, np.stack(K), np.stack(V), len(toks), Hq, Hkv, hd, 1.0 / math.sqrt(hd))
+        x = x + oracle.gemv(M["l0.o"], att)
+        xn = oracle.rmsnorm(x, gains[1], eps)
+        a = oracle.swiglu(oracle.gemv(M["l0.gate"], xn), oracle.gemv(M["l0.up"], xn))
+        x = x + oracle.gemv(M["l0.down"], a)
+        return oracle.gemv(M["head"], oracle.rmsnorm(x, gains[2], eps))
+
+    ref = compose(True)
+    assert np.array_equal(logits, ref) and best == oracle.argmax(ref)
+    assert not np.array_equal(logits, compose(False))
+
+
 def test_step_rejects_bad_arguments(orc):
     m = _tiny_model(orc)
     bt = np.arange(16, dtype=np.int32)
