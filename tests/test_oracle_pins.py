@@ -534,6 +534,57 @@ def test_step_composition_at_a_later_position(orc):
     assert not np.array_equal(logits, compose(False))
 
 
+def test_two_layer_composition(orc):
+    """Two layers with distinct norm gains per layer, 18 positions: the step's logits
+    equal the parts composed layer by layer -- every position's output of layer 0 is the
+    input of layer 1, and each layer keeps its own K/V -- bit for bit.  A wrong layer
+    index for a weight, a gain or a cache slice would break it."""
+    import math
+
+    import oracle
+    shape = synth.TINY
+    m = _tiny_model(orc, layers=2)
+    d, hd, Hq, Hkv = shape.d_model, shape.head_dim, shape.n_heads, shape.n_kv_heads
+    lib = oracle.lib()
+    gains = {}
+    for layer in range(2):
+        for which in (5, 6):
+            g = synth.normal(300 + 10 * layer + which, d) + 2
+            lib.or_model_set(m.h, which, layer, 3, g.ctypes.data, None, 1, d)
+            gains[(layer, which)] = g
+    gf = synth.normal(399, d) + 2
+    lib.or_model_set(m.h, 102, 0, 3, gf.ctypes.data, None, 1, d)
+    m._keep += list(gains.values()) + [gf]
+    toks = shape.tokens(18, stream=6)
+    bt = synth.permutation(9, 16).astype(np.int32)
+    for pos, t in enumerate(toks):
+        logits, best = m.decode_step(int(t), pos, bt)
+
+    M, eps = m.mats, shape.rms_eps
+    cos, sin = oracle.rope_table(128, hd, shape.rope_theta)
+    hq, hk = Hq * hd, Hkv * hd
+    X = [oracle.embed_row(M["embed"], int(t)) for t in toks]
+    for layer in range(2):
+        W = {n: M[f"l{layer}.{n}"] for n in ("qkv", "o", "gate", "up", "down")}
+        K, V, Q = [], [], []
+        for pos, x in enumerate(X):
+            qkv = oracle.gemv(W["qkv"], oracle.rmsnorm(x, gains[(layer, 5)], eps))
+            Q.append(oracle.rope_apply(qkv[:hq], Hq, hd, cos[pos], sin[pos]))
+            K.append(oracle.to_bf16(oracle.rope_apply(qkv[hq:hq + hk], Hkv, hd, cos[pos], sin[pos])))
+            V.append(oracle.to_bf16(qkv[hq + hk:]))
+        out = []
+        for pos, x in enumerate(X):
+            att = oracle.attention_contig(Q[pos], np.stack(K[:pos + 1]), np.stack(V[:pos + 1]), pos + 1,
+                                          Hq, Hkv, hd, 1.0 / math.sqrt(hd))
+            x = x + oracle.gemv(W["o"], att)
+            xn = oracle.rmsnorm(x, gains[(layer, 6)], eps)
+            out.append(x + oracle.gemv(W["down"], oracle.swiglu(oracle.gemv(W["gate"], xn),
+                                                                 oracle.gemv(W["up"], xn))))
+        X = out
+    ref = oracle.gemv(M["head"], oracle.rmsnorm(X[-1], gf, eps))
+    assert np.array_equal(logits, ref) and best == oracle.argmax(ref)
+
+
 def test_step_rejects_bad_arguments(orc):
     m = _tiny_model(orc)
     bt = np.arange(16, dtype=np.int32)
