@@ -585,6 +585,51 @@ def test_two_layer_composition(orc):
     assert np.array_equal(logits, ref) and best == oracle.argmax(ref)
 
 
+def test_bf16_activation_points(orc):
+    """With bf16 activations (the TinyLlama workload) every GEMV input vector -- the two
+    normed inputs, the attention output, the SwiGLU output and the head's normed input --
+    is rounded to bf16 and nothing else is (the residual stays fp32): the step equals
+    that composition bit for bit at position 9, and leaving the SwiGLU output unrounded
+    differs."""
+    import math
+    from dataclasses import replace
+
+    import oracle
+    shape = replace(synth.TINY, act_bf16=True)
+    m = orc.Model(shape, n_kv_blocks=16, max_pos=128, layers=1)
+    d, hd, Hq, Hkv = shape.d_model, shape.head_dim, shape.n_heads, shape.n_kv_heads
+    toks = shape.tokens(10, stream=7)
+    bt = np.arange(16, dtype=np.int32)
+    for pos, t in enumerate(toks):
+        logits, best = m.decode_step(int(t), pos, bt)
+
+    M, eps, ones = m.mats, shape.rms_eps, np.ones(d, np.float32)
+    cos, sin = oracle.rope_table(128, hd, shape.rope_theta)
+    hq, hk = Hq * hd, Hkv * hd
+
+    def bf(v):
+        return oracle.from_bf16(oracle.to_bf16(v))
+
+    def compose(round_act: bool):
+        K, V = [], []
+        for pos, t in enumerate(toks):
+            x = oracle.embed_row(M["embed"], int(t))
+            qkv = oracle.gemv(M["l0.qkv"], bf(oracle.rmsnorm(x, ones, eps)))
+            q = oracle.rope_apply(qkv[:hq], Hq, hd, cos[pos], sin[pos])
+            K.append(oracle.to_bf16(oracle.rope_apply(qkv[hq:hq + hk], Hkv, hd, cos[pos], sin[pos])))
+            V.append(oracle.to_bf16(qkv[hq + hk:]))
+        att = oracle.attention_contig(q, np.stack(K), np.stack(V), len(toks), Hq, Hkv, hd, 1.0 / math.sqrt(hd))
+        x = x + oracle.gemv(M["l0.o"], bf(att))
+        xn = bf(oracle.rmsnorm(x, ones, eps))
+        a = oracle.swiglu(oracle.gemv(M["l0.gate"], xn), oracle.gemv(M["l0.up"], xn))
+        x = x + oracle.gemv(M["l0.down"], bf(a) if round_act else a)
+        return oracle.gemv(M["head"], bf(oracle.rmsnorm(x, ones, eps)))
+
+    ref = compose(True)
+    assert np.array_equal(logits, ref) and best == oracle.argmax(ref)
+    assert not np.array_equal(logits, compose(False))
+
+
 def test_step_rejects_bad_arguments(orc):
     m = _tiny_model(orc)
     bt = np.arange(16, dtype=np.int32)
