@@ -630,6 +630,33 @@ def test_bf16_activation_points(orc):
     assert not np.array_equal(logits, compose(False))
 
 
+@pytest.mark.parametrize("fmt", ["i8", "bf16"])
+def test_tied_embedding_is_the_head_matrix(orc, fmt):
+    """With tied weights (the Llama-3.2-1B shape) the token's input row is the head
+    matrix's row, dequantised (int8: times its row scale): a one-layer step at position 0
+    equals that composition bit for bit."""
+    from dataclasses import replace
+
+    import oracle
+    shape = replace(synth.TINY, tied=True, wfmt=fmt, head_fmt=fmt)
+    m = orc.Model(shape, n_kv_blocks=16, max_pos=128, layers=1)
+    assert "embed" not in m.mats
+    d, hd, Hq, Hkv = shape.d_model, shape.head_dim, shape.n_heads, shape.n_kv_heads
+    tok = 321
+    logits, best = m.decode_step(tok, 0, np.arange(16, dtype=np.int32))
+    M, eps, ones = m.mats, shape.rms_eps, np.ones(d, np.float32)
+    x = M["head"].dequantize()[tok].astype(np.float32)
+    assert np.array_equal(x, oracle.embed_row(M["head"], tok))
+    qkv = oracle.gemv(M["l0.qkv"], oracle.rmsnorm(x, ones, eps))
+    v = oracle.from_bf16(oracle.to_bf16(qkv[(Hq + Hkv) * hd:]))
+    att = np.repeat(v.reshape(Hkv, hd), Hq // Hkv, axis=0).ravel()
+    x = x + oracle.gemv(M["l0.o"], att)
+    xn = oracle.rmsnorm(x, ones, eps)
+    x = x + oracle.gemv(M["l0.down"], oracle.swiglu(oracle.gemv(M["l0.gate"], xn), oracle.gemv(M["l0.up"], xn)))
+    ref = oracle.gemv(M["head"], oracle.rmsnorm(x, ones, eps))
+    assert np.array_equal(logits, ref) and best == oracle.argmax(ref)
+
+
 def test_step_rejects_bad_arguments(orc):
     m = _tiny_model(orc)
     bt = np.arange(16, dtype=np.int32)
