@@ -198,14 +198,19 @@ mie_status mie_pool_incref(mie_pool *p, int32_t id);
 mie_status mie_pool_decref(mie_pool *p, int32_t id);
 int mie_pool_refcount(const mie_pool *p, int32_t id); /* -1 for an id out of range */
 int mie_pool_free_count(const mie_pool *p);
-/* Copy-on-write for a write at logical position pos of a sequence whose block table
- * (host int32, updated in place) is `table`: a private block is returned as is; a
- * shared block is split -- allocate, (caller copies contents src -> dst), drop one
- * reference to the old block, point the table at the new one.  *copy_src / *copy_dst
- * are the split's blocks, or -1 when no copy is needed.  MIE_E_OOM with the table and
- * counts untouched when no block is free.  The contents copy is the caller's
- * (mie_kv_copy_block does it for a model context's pool) and must be enqueued before
- * any write into the new block. */
+/* Copy-on-write ([MIE] "Prefix sharing and copy-on-write": a sequence writing into a
+ * block that others share first moves to a private copy, and the shared block must
+ * stay alive until the copy is made) for a write at logical position pos of a sequence
+ * whose block table (host int32, updated in place) is `table`.  A block this sequence
+ * holds alone is returned as is (*copy_src = *copy_dst = -1).  For a shared block a
+ * fresh block is allocated and the table entry points at it (*block = *copy_dst = the
+ * new id, *copy_src = the shared id), but the sequence KEEPS its reference on the
+ * shared block: the caller enqueues the contents copy src -> dst (mie_kv_copy_block for
+ * a model context's pool) and only then calls mie_pool_decref(p, *copy_src).  Until that
+ * decref no other thread can free the shared block and have it reused, so the copy
+ * never reads overwritten contents.  MIE_E_OOM (table and counts untouched, outputs -1)
+ * when no block is free; MIE_E_ARG when the table's block is not live.  A model
+ * context's mie_kv_writable does all three steps in order. */
 mie_status mie_pool_writable(mie_pool *p, int32_t *table, int pos, int block_size, int32_t *block,
                              int32_t *copy_src, int32_t *copy_dst);
 
@@ -258,6 +263,15 @@ int64_t mie_kv_block_elems(const mie_ctx *ctx);
 /* Enqueues a device copy of block src into block dst (copy-on-write) on the context's
  * stream; MIE_E_ARG for a block id outside 0..n_kv_blocks-1. */
 mie_status mie_kv_copy_block(mie_ctx *ctx, int32_t src, int32_t dst);
+/* Copy-on-write on the context's pool, in the safe order: mie_pool_writable (allocate,
+ * repoint the table entry), then the contents copy enqueued on the context's stream,
+ * then the sequence's reference on the shared block dropped.  Every later step of this
+ * context, and any reuse of the shared block by work on the same stream, is ordered
+ * after the copy.  table: host int32 block table of the sequence, updated in place;
+ * *block receives the block to write.  Errors as mie_pool_writable; a failed copy
+ * enqueue (MIE_E_CUDA) leaves the table pointing at the fresh block and keeps the
+ * reference on the shared one, for the caller to retry or release. */
+mie_status mie_kv_writable(mie_ctx *ctx, int32_t *table, int pos, int32_t *block);
 
 /* One decode step ([INFER] data-flow figure; [RUST] "How a Llama model generates
  * text"): the token at 0-based position pos writes its K/V into block

@@ -74,6 +74,7 @@ _SIGS = {
     "mie_kv_pool": (P, [P]),
     "mie_kv_block_elems": (I64, [P]),
     "mie_kv_copy_block": (I, [P, ctypes.c_int32, ctypes.c_int32]),
+    "mie_kv_writable": (I, [P, P, I, ctypes.POINTER(ctypes.c_int32)]),
     "mie_decode_step": (I, [P, ctypes.c_int32, ctypes.c_int32, P, I, P, P]),
     "mie_decode_continue": (I, [P, I]),
     "mie_decode_step_slots": (I, [P, I, P, P, P, I, P, P]),
@@ -313,7 +314,9 @@ class Pool:
         return lib().mie_pool_free_count(self.h)
 
     def writable(self, table: np.ndarray, pos: int, block_size: int):
-        """(status, block, copy_src, copy_dst); the table is updated in place."""
+        """(status, block, copy_src, copy_dst); the table is updated in place.  After a
+        split (copy_src >= 0) the sequence still holds copy_src: queue the copy, then
+        decref(copy_src)."""
         assert table.dtype == np.int32 and table.flags.c_contiguous
         b, s, d = ctypes.c_int32(-1), ctypes.c_int32(-1), ctypes.c_int32(-1)
         st = lib().mie_pool_writable(self.h, table.ctypes.data, pos, block_size, ctypes.byref(b),
@@ -386,6 +389,14 @@ class Model:
 
     def kv_copy_block(self, src: int, dst: int):
         _check(lib().mie_kv_copy_block(self.h, src, dst), "mie_kv_copy_block")
+
+    def kv_writable(self, table: np.ndarray, pos: int) -> int:
+        """Copy-on-write on the context's pool (split, copy queued, old reference
+        dropped); the host table is updated in place; returns the block to write."""
+        assert table.dtype == np.int32 and table.flags.c_contiguous
+        b = ctypes.c_int32(-1)
+        _check(lib().mie_kv_writable(self.h, table.ctypes.data, int(pos), ctypes.byref(b)), "mie_kv_writable")
+        return b.value
 
     def decode_step(self, token: int, pos: int, block_table, logits_out=None, argmax_out=None):
         torch = _torch()
@@ -491,7 +502,8 @@ def mie_pool_free_count(pool: Pool) -> int:
 
 def mie_pool_writable(pool: Pool, table: np.ndarray, pos: int, block_size: int):
     """(block, copy_src, copy_dst) with the table updated in place; MieError (out of
-    memory) when no block is free."""
+    memory) when no block is free.  After a split the caller still holds copy_src and
+    drops it with mie_pool_decref once the copy is queued."""
     st, b, s, d = pool.writable(table, pos, block_size)
     _check(st, "mie_pool_writable")
     return b, s, d
@@ -524,6 +536,10 @@ def mie_kv_block_elems(ctx: Model) -> int:
 
 def mie_kv_copy_block(ctx: Model, src: int, dst: int) -> None:
     ctx.kv_copy_block(src, dst)
+
+
+def mie_kv_writable(ctx: Model, table: np.ndarray, pos: int) -> int:
+    return ctx.kv_writable(table, pos)
 
 
 def mie_decode_step(ctx: Model, token: int, pos: int, block_table, logits_out=None, argmax_out=None) -> None:
@@ -565,6 +581,6 @@ def mie_slot_step_launches(ctx: Model) -> int:
 __all__ += ["mie_last_error", "mie_status_string", "mie_pool_create", "mie_pool_destroy", "mie_pool_alloc",
             "mie_pool_incref", "mie_pool_decref", "mie_pool_refcount", "mie_pool_free_count",
             "mie_pool_writable", "mie_create", "mie_destroy", "mie_load_weights", "mie_ctx_pool",
-            "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_decode_step",
+            "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_kv_writable", "mie_decode_step",
             "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
             "mie_set_trace", "mie_sync", "mie_step_launches", "mie_slot_step_launches"]

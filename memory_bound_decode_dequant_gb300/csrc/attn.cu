@@ -315,10 +315,14 @@ mie_status launch_argmax(const float *v, int n, int32_t *out, float2 *part, unsi
   return MIE_OK;
 }
 
+// Device address of the error flag on the current device, looked up once per device;
+// the lookup table is shared by every host thread, so it is filled under a lock.
 int *device_error_flag() {
+  static std::mutex mu;
   static int *cached[64] = {nullptr};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> g(mu);
   if (!cached[dev]) {
     void *p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;

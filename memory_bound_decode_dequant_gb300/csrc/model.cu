@@ -519,6 +519,17 @@ extern "C" mie_status mie_kv_copy_block(mie_ctx *ctx, int32_t src, int32_t dst) 
   return MIE_OK;
 }
 
+// Copy-on-write in the order that keeps the shared block alive until its copy is
+// queued: split (the sequence still holds the shared block), queue the copy, release.
+extern "C" mie_status mie_kv_writable(mie_ctx *ctx, int32_t *table, int pos, int32_t *block) {
+  if (!ctx || !table || !block) return fail(MIE_E_ARG, "mie_kv_writable: null pointer");
+  int32_t src = -1, dst = -1;
+  mie_status s = mie_pool_writable(ctx->pool, table, pos, ctx->cfg.block_size, block, &src, &dst);
+  if (s != MIE_OK || src < 0) return s;
+  if ((s = mie_kv_copy_block(ctx, src, dst)) != MIE_OK) return s;
+  return mie_pool_decref(ctx->pool, src);
+}
+
 // ------------------------------------------------------------------ the step
 
 static bool all_loaded(const mie_ctx *ctx) {

@@ -1,17 +1,16 @@
 // pool.cpp -- host bookkeeping of the paged KV cache.
 //
 // "Mini Inference Engine", "The KV cache, paged like virtual memory": the cache is cut
-// into fixed-size blocks handed out from a preallocated pool by integer id, with a
-// refcount per id and a LIFO free list; running out is a sentinel, not an exception.
-// "Prefix sharing and copy-on-write": a shared block is split on its first write by
-// allocate -> copy -> decref -> swap, so the source stays alive during the copy.
-// The block contents live on the GPU; this object only tracks ids and counts.
-#include <cstdarg>
-#include <cstdio>
-#include <cstring>
+// into fixed-size blocks handed out by integer id from a preallocated pool; each id
+// carries a count of the sequences holding it, and running out is reported as a
+// status, not thrown.  "Prefix sharing and copy-on-write": sequences may hold the same
+// block; before one of them writes into a block that others also hold, it moves to a
+// private copy, and the shared block must stay alive until that copy has been made.
+//
+// The block contents live on the GPU; this object only tracks ids and counts.  Every
+// public call takes the pool's lock, so the pool may be shared between host threads.
 #include <mutex>
 #include <new>
-#include <string>
 #include <vector>
 
 #include "../../include/mie.h"
@@ -21,105 +20,105 @@ mie_status fail(mie_status s, const char *fmt, ...);
 }
 
 struct mie_pool {
-  std::vector<int> refcount;
-  std::vector<int32_t> free_list;  // LIFO: back() is handed out next
+  // holders[id] = number of sequences holding block id (0: free)
+  std::vector<int> holders;
+  // ids with no holder; the most recently freed id is handed out first, and a fresh
+  // pool hands out 0, 1, 2, ...
+  std::vector<int32_t> spare;
   std::mutex mu;
+
+  explicit mie_pool(int n) : holders((size_t)n, 0) {
+    spare.reserve((size_t)n);
+    for (int id = n - 1; id >= 0; --id) spare.push_back(id);
+  }
+  int size() const { return (int)holders.size(); }
+  bool held(int32_t id) const { return id >= 0 && id < size() && holders[(size_t)id] > 0; }
+
+  // Hands out a block with one holder; false when none is spare.
+  bool take(int32_t *id) {
+    if (spare.empty()) return false;
+    *id = spare.back();
+    spare.pop_back();
+    holders[(size_t)*id] = 1;
+    return true;
+  }
+  // Drops one holder of a held block; the last one frees it.
+  void release(int32_t id) {
+    if (--holders[(size_t)id] == 0) spare.push_back(id);
+  }
 };
 
 extern "C" mie_status mie_pool_create(int n_blocks, mie_pool **out) {
   if (!out) return mie::fail(MIE_E_ARG, "mie_pool_create: null out");
   *out = nullptr;
   if (n_blocks < 1) return mie::fail(MIE_E_SHAPE, "mie_pool_create: n_blocks = %d", n_blocks);
-  mie_pool *p = new (std::nothrow) mie_pool;
+  mie_pool *p = new (std::nothrow) mie_pool(n_blocks);
   if (!p) return mie::fail(MIE_E_OOM, "mie_pool_create: out of host memory");
-  p->refcount.assign((size_t)n_blocks, 0);
-  p->free_list.reserve((size_t)n_blocks);
-  for (int i = n_blocks - 1; i >= 0; --i) p->free_list.push_back(i);  // hands out 0, 1, 2, ...
   *out = p;
   return MIE_OK;
 }
 
 extern "C" void mie_pool_destroy(mie_pool *p) { delete p; }
 
-static bool live(const mie_pool *p, int32_t id) {
-  return id >= 0 && (size_t)id < p->refcount.size() && p->refcount[(size_t)id] > 0;
-}
-
-static mie_status alloc_locked(mie_pool *p, int32_t *id) {
-  if (p->free_list.empty()) {
-    *id = -1;
-    return mie::fail(MIE_E_OOM, "KV block pool exhausted (%zu blocks)", p->refcount.size());
-  }
-  *id = p->free_list.back();
-  p->free_list.pop_back();
-  p->refcount[(size_t)*id] = 1;
-  return MIE_OK;
-}
-
-static mie_status decref_locked(mie_pool *p, int32_t id) {
-  if (!live(p, id)) return mie::fail(MIE_E_ARG, "mie_pool_decref: block %d is not live", id);
-  if (--p->refcount[(size_t)id] == 0) p->free_list.push_back(id);
-  return MIE_OK;
-}
-
 extern "C" mie_status mie_pool_alloc(mie_pool *p, int32_t *id) {
   if (!p || !id) return mie::fail(MIE_E_ARG, "mie_pool_alloc: null pointer");
   std::lock_guard<std::mutex> g(p->mu);
-  return alloc_locked(p, id);
+  if (!p->take(id)) {
+    *id = -1;
+    return mie::fail(MIE_E_OOM, "KV block pool exhausted (%d blocks)", p->size());
+  }
+  return MIE_OK;
 }
 
 extern "C" mie_status mie_pool_incref(mie_pool *p, int32_t id) {
   if (!p) return mie::fail(MIE_E_ARG, "mie_pool_incref: null pool");
   std::lock_guard<std::mutex> g(p->mu);
-  if (!live(p, id)) return mie::fail(MIE_E_ARG, "mie_pool_incref: block %d is not live", id);
-  ++p->refcount[(size_t)id];
+  if (!p->held(id)) return mie::fail(MIE_E_ARG, "mie_pool_incref: block %d is not live", id);
+  ++p->holders[(size_t)id];
   return MIE_OK;
 }
 
 extern "C" mie_status mie_pool_decref(mie_pool *p, int32_t id) {
   if (!p) return mie::fail(MIE_E_ARG, "mie_pool_decref: null pool");
   std::lock_guard<std::mutex> g(p->mu);
-  return decref_locked(p, id);
+  if (!p->held(id)) return mie::fail(MIE_E_ARG, "mie_pool_decref: block %d is not live", id);
+  p->release(id);
+  return MIE_OK;
 }
 
 extern "C" int mie_pool_refcount(const mie_pool *p, int32_t id) {
-  if (!p || id < 0 || (size_t)id >= p->refcount.size()) return -1;
+  if (!p || id < 0 || id >= p->size()) return -1;
   std::lock_guard<std::mutex> g(const_cast<mie_pool *>(p)->mu);
-  return p->refcount[(size_t)id];
+  return p->holders[(size_t)id];
 }
 
 extern "C" int mie_pool_free_count(const mie_pool *p) {
   if (!p) return -1;
   std::lock_guard<std::mutex> g(const_cast<mie_pool *>(p)->mu);
-  return (int)p->free_list.size();
+  return (int)p->spare.size();
 }
 
+// A write at logical position pos needs a block that the sequence holds alone.  When
+// the table's block has other holders too, the sequence moves to a fresh block: the
+// table entry changes now, but the sequence keeps its hold on the shared block, which
+// it gives up (mie_pool_decref(copy_src)) only after the copy of the contents is
+// queued.  Until then no other caller can free the shared block and hand it out again.
 extern "C" mie_status mie_pool_writable(mie_pool *p, int32_t *table, int pos, int block_size, int32_t *block,
                                         int32_t *copy_src, int32_t *copy_dst) {
   if (!p || !table || !block || !copy_src || !copy_dst) return mie::fail(MIE_E_ARG, "mie_pool_writable: null pointer");
   if (pos < 0 || block_size < 1) return mie::fail(MIE_E_ARG, "mie_pool_writable: pos %d, block size %d", pos, block_size);
+  *copy_src = *copy_dst = *block = -1;
+  int32_t &entry = table[pos / block_size];
   std::lock_guard<std::mutex> g(p->mu);
-  *copy_src = *copy_dst = -1;
-  const int32_t old = table[pos / block_size];
-  if (!live(p, old)) {
-    *block = -1;
-    return mie::fail(MIE_E_ARG, "mie_pool_writable: block %d is not live", old);
+  if (!p->held(entry)) return mie::fail(MIE_E_ARG, "mie_pool_writable: block %d is not live", entry);
+  if (p->holders[(size_t)entry] > 1) {
+    int32_t fresh = -1;
+    if (!p->take(&fresh))
+      return mie::fail(MIE_E_OOM, "KV block pool exhausted (%d blocks) on copy-on-write", p->size());
+    *copy_src = entry;
+    *copy_dst = fresh;
+    entry = fresh;
   }
-  if (p->refcount[(size_t)old] == 1) {
-    *block = old;
-    return MIE_OK;
-  }
-  int32_t nw = -1;
-  const mie_status s = alloc_locked(p, &nw);
-  if (s != MIE_OK) {
-    *block = -1;
-    return s;
-  }
-  // The caller copies old -> nw before writing; the source keeps its other holders.
-  *copy_src = old;
-  *copy_dst = nw;
-  decref_locked(p, old);
-  table[pos / block_size] = nw;
-  *block = nw;
+  *block = entry;
   return MIE_OK;
 }

@@ -62,16 +62,40 @@ def test_pool_matches_oracle_pool(L, orc):
             st, blk, src, dst = ours.writable(t, slot * 16 + 3, 16)
             rblk = ref.writable(t2, slot * 16 + 3, 16)
             if st == 0:
-                assert blk == rblk and np.array_equal(t, t2)
-                if dst >= 0:
+                if dst >= 0:  # the split keeps our hold on src until the copy is queued
+                    assert ours.refcount(src) >= 2
+                    assert ours.decref(src) == 0
                     live.remove(src)
                     live.append(dst)
+                assert blk == rblk and np.array_equal(t, t2)
             else:
                 assert st == 3 and rblk == -1
         assert ours.free_count() == ref.free_count()
     for i in range(n):
         assert ours.refcount(i) == ref.refcount(i)
     assert ours.refcount(n) == -1 and ours.refcount(-1) == -1
+
+
+def test_split_block_stays_held_until_released(L):
+    """Copy-on-write ordering: after a split the shared block keeps this sequence's
+    hold, so even when its other holder retires at once, the block is not free and
+    cannot be handed out again (and overwritten) before the caller has queued its
+    copy and released it."""
+    p = mie.Pool(4)
+    shared = p.alloc()
+    p.incref(shared)                      # two sequences hold it
+    table = np.array([shared], np.int32)
+    st, blk, src, dst = p.writable(table, 5, 16)
+    assert st == 0 and src == shared and dst == blk != shared and table[0] == blk
+    assert p.decref(shared) == 0          # the other holder retires meanwhile
+    assert p.refcount(shared) == 1        # ... the block is still held for the copy
+    taken = [p.alloc() for _ in range(2)]
+    assert shared not in taken and p.alloc() == -1
+    assert p.decref(src) == 0             # copy queued: the hold is dropped
+    assert p.refcount(shared) == 0 and p.alloc() == shared
+    # a private block needs no split
+    st, blk2, src2, dst2 = p.writable(np.array([blk], np.int32), 0, 16)
+    assert (st, blk2, src2, dst2) == (0, blk, -1, -1)
 
 
 def test_pool_exhaustion_is_a_status(L):
@@ -144,7 +168,10 @@ def test_pool_calls_by_c_name(L):
     mie.mie_pool_decref(p, 2)
     assert mie.mie_pool_free_count(p) == 1
     blk, src, dst = mie.mie_pool_writable(p, table, 3, 16)  # copy-on-write into block 2
-    assert (blk, src, dst) == (2, 1, 2) and table[0] == 2 and mie.mie_pool_refcount(p, 1) == 1
+    assert (blk, src, dst) == (2, 1, 2) and table[0] == 2
+    assert mie.mie_pool_refcount(p, 1) == 2  # still held by this sequence until the copy is queued
+    mie.mie_pool_decref(p, src)
+    assert mie.mie_pool_refcount(p, 1) == 1
     with pytest.raises(mie.MieError) as e:
         mie.mie_pool_decref(p, 7)
     assert e.value.status == 1

@@ -3,10 +3,12 @@
 mie_paged_attn_decode_noalloc is for callers that cannot allocate device memory when
 they run attention, so they cannot pass a workspace: it keeps its partial results in an
 array built into the library.  Here two calls in a row (the second reusing the array
-the first left behind, with a different context length and split count) are checked
-against the workspace entry point on the same inputs, with the attention tolerance
-used by the other kernel tests.  This file sorts last so a stopping run has already
-run every other test; it also passes on its own in a fresh process.
+the first left behind, with a different context length and split count) must give the
+same bits as the workspace entry point on the same inputs -- both run the same kernel
+with the same split count and merge order, so any difference would mean a corrupted
+read of the shared array -- and both must match the oracle within the attention
+tolerance of the other kernel tests.  This file sorts last so a stopping run has
+already run every other test; it also passes on its own in a fresh process.
 """
 import math
 
@@ -44,18 +46,28 @@ def _case(seed, ctx, Hq=32, Hkv=8, hd=64, bs=16):
 
 def _close(out, ref):
     out = out.cpu().numpy().astype(np.float64)
-    ref = ref.cpu().numpy().astype(np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
     rms = math.sqrt(float(np.mean(ref ** 2)))
     assert np.all(np.abs(out - ref) <= 1e-4 * np.maximum(np.abs(ref), rms) + 1e-6)
 
 
-def test_no_alloc_matches_workspace_entry_on_two_calls_in_a_row():
+def _oracle(orc, c):
+    return orc.attention_paged(c["q"].cpu().numpy(), c["k_pool"].cpu().numpy().view(np.uint16),
+                               c["v_pool"].cpu().numpy().view(np.uint16), c["block_stride"],
+                               c["block_table"].cpu().numpy(), c["ctx_len"], c["Hq"], c["Hkv"], c["hd"],
+                               c["bs"], c["scale"])
+
+
+def test_no_alloc_matches_workspace_entry_on_two_calls_in_a_row(orc):
     for seed, ctx in ((900, 2048), (910, 300)):
         c = _case(seed, ctx)
         ref = mie.mie_paged_attn_decode(**c)
         got = mie.mie_paged_attn_decode_noalloc(**c)
         torch.cuda.synchronize()
-        _close(got, ref)
+        assert torch.equal(got.view(torch.int32), ref.view(torch.int32)), f"ctx {ctx}: not bit-identical"
+        want = _oracle(orc, c)
+        _close(ref, want)
+        _close(got, want)
     mie.mie_check()
 
 
