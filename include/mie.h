@@ -173,6 +173,20 @@ size_t mie_argmax_workspace_bytes(int n);
 mie_status mie_argmax(const float *v, int n, int32_t *out, void *workspace, size_t workspace_bytes,
                       void *stream);
 
+/* ================================================================ bandwidth probe */
+
+/* Read-only streaming probe ([INFER]: every kernel's bandwidth is quoted as a fraction
+ * of a peak the page measured with its own read probe, not of the datasheet figure).
+ * Reads each of the `bytes` bytes of buf (device) exactly once, with load_bytes-wide
+ * loads (16 or 32) that bypass L1 and are marked evict-first in L2, from a grid of
+ * blocks_per_sm (1..4) CTAs of 512 threads per SM; *xor_out (device uint32, zeroed by
+ * the call) receives the XOR of all of the buffer's 32-bit words, so the result is
+ * exact and checkable.  To measure HBM rather than L2, pass a buffer many times the
+ * 129 MB L2.  bytes must be a nonzero multiple of load_bytes and buf load_bytes-aligned
+ * (MIE_E_SHAPE otherwise).  Asynchronous on `stream`. */
+mie_status mie_hbm_read_probe(const void *buf, size_t bytes, uint32_t *xor_out, int load_bytes,
+                              int blocks_per_sm, void *stream);
+
 /* Reads and clears the device error flag that kernels latch when a bounds check
  * fails (stateless kernels share one flag per device).  Synchronises `stream`.
  * MIE_E_DEVICE if a check fired since the last call. */
@@ -328,6 +342,19 @@ mie_status mie_set_trace(mie_ctx *ctx, void *device_buffer, size_t bytes, int *n
  * the persistent step gave up (its counters and tagged words are reset for the next
  * step). */
 mie_status mie_sync(mie_ctx *ctx);
+
+/* Testing aid for the bounded waits of the persistent step.  From the next
+ * mie_decode_step on, phase `phase` (0-based, five per layer -- QKV, attention, O-proj,
+ * gate/up, down -- then the LM head; 1 <= phase <= 5 * n_layers) reads its input vector
+ * from words that no phase ever writes, and every bounded wait of the step gives up
+ * after `wait_polls` rounds (one round: one L2 round trip or one mbarrier probe).  The
+ * step therefore ends early with its waits timed out; mie_sync then returns
+ * MIE_E_TIMEOUT and resets the step's counters and tagged words.  phase < 0 restores
+ * the normal phase table and the default limit (a few seconds), after which steps are
+ * correct again.  The chain mode has no tagged inputs and is not affected.  MIE_E_ARG
+ * for phase 0 (it has no input to withhold), a phase past the LM head, or
+ * wait_polls < 1. */
+mie_status mie_debug_stall(mie_ctx *ctx, int phase, long wait_polls);
 
 /* Kernel launches one mie_decode_step replay performs (for launch accounting). */
 int mie_step_launches(const mie_ctx *ctx);

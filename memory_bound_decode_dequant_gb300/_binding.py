@@ -20,7 +20,8 @@ __all__ = ["lib", "MieError", "FMT", "LIB_PATH", "exported_names", "header_funct
            "mie_q4_0_packed_bytes", "mie_gemv_bf16", "mie_gemv_i8", "mie_gemv_q4_0",
            "mie_paged_attn_decode", "mie_paged_attn_workspace_bytes", "mie_paged_attn_decode_noalloc",
            "mie_argmax",
-           "mie_argmax_workspace_bytes", "mie_check", "Pool", "Config", "Model", "DeviceArray"]
+           "mie_argmax_workspace_bytes", "mie_check", "mie_hbm_read_probe", "Pool", "Config", "Model",
+           "DeviceArray"]
 
 
 class MieError(RuntimeError):
@@ -58,6 +59,7 @@ _SIGS = {
     "mie_argmax_workspace_bytes": (SZ, [I]),
     "mie_argmax": (I, [P, I, P, P, SZ, P]),
     "mie_check": (I, [P]),
+    "mie_hbm_read_probe": (I, [P, SZ, P, I, I, P]),
     "mie_pool_create": (I, [I, ctypes.POINTER(P)]),
     "mie_pool_destroy": (None, [P]),
     "mie_pool_alloc": (I, [P, ctypes.POINTER(ctypes.c_int32)]),
@@ -84,6 +86,7 @@ _SIGS = {
     "mie_step_mode": (I, [P]),
     "mie_slot_step_launches": (I, [P]),
     "mie_set_trace": (I, [P, P, SZ, ctypes.POINTER(I), ctypes.POINTER(I)]),
+    "mie_debug_stall": (I, [P, I, ctypes.c_long]),
 }
 
 _lib = None
@@ -272,6 +275,18 @@ def mie_argmax(v, out=None, workspace=None, stream=None):
     return out
 
 
+def mie_hbm_read_probe(buf, xor_out=None, load_bytes: int = 32, blocks_per_sm: int = 2, stream=None):
+    """Reads every byte of the device tensor `buf` once; returns the int32 device tensor
+    that receives the XOR of its 32-bit words."""
+    torch = _torch()
+    if xor_out is None:
+        xor_out = torch.empty(1, dtype=torch.int32, device=buf.device)
+    _check(lib().mie_hbm_read_probe(_dev(buf, None, "buf"), buf.numel() * buf.element_size(),
+                                    _dev(xor_out, torch.int32, "xor_out"), load_bytes, blocks_per_sm,
+                                    _stream(stream)), "mie_hbm_read_probe")
+    return xor_out
+
+
 def mie_check(stream=None):
     _check(lib().mie_check(_stream(stream)), "mie_check")
 
@@ -440,6 +455,11 @@ class Model:
     def step_mode(self) -> int:
         return int(lib().mie_step_mode(self.h))
 
+    def debug_stall(self, phase: int, wait_polls: int = 0):
+        """Testing aid: phase `phase` of the persistent step waits for an input nobody
+        writes, and every wait gives up after wait_polls rounds (phase < 0 restores)."""
+        _check(lib().mie_debug_stall(self.h, int(phase), int(wait_polls)), "mie_debug_stall")
+
     def set_trace(self, enable: bool = True):
         """Records the persistent step's timeline into a device tensor
         [n_phases, n_ctas, 5] of int64 nanoseconds (returned), or switches it off."""
@@ -570,6 +590,10 @@ def mie_sync(ctx: Model) -> None:
     ctx.sync()
 
 
+def mie_debug_stall(ctx: Model, phase: int, wait_polls: int = 0) -> None:
+    ctx.debug_stall(phase, wait_polls)
+
+
 def mie_step_launches(ctx: Model) -> int:
     return ctx.launches
 
@@ -583,4 +607,4 @@ __all__ += ["mie_last_error", "mie_status_string", "mie_pool_create", "mie_pool_
             "mie_pool_writable", "mie_create", "mie_destroy", "mie_load_weights", "mie_ctx_pool",
             "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_kv_writable", "mie_decode_step",
             "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
-            "mie_set_trace", "mie_sync", "mie_step_launches", "mie_slot_step_launches"]
+            "mie_set_trace", "mie_debug_stall", "mie_sync", "mie_step_launches", "mie_slot_step_launches"]

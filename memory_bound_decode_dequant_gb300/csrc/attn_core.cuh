@@ -26,13 +26,14 @@ __host__ __device__ inline int attn_nsplit(int nblk, int max_splits, int per_spl
 // Tagged variant: polls the group's queries into sm.q and, when has_pos, the current
 // token's k and v of KV head g into sm.kn / sm.vn, all in one batch of round trips.
 template <int G, int HD, int NT, class Sync, class SM>
-__device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, SM &sm, uint32_t tag, const int *abort) {
+__device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, SM &sm, uint32_t tag, const int *abort,
+                              long limit) {
   constexpr int NQ = G * HD / 2, NK = HD / 2;
   const uint64_t *qs = a.qkv_t + (int64_t)(g * G) * HD;
   const uint64_t *ks = a.qkv_t + (int64_t)(a.Hq + g) * HD;
   const uint64_t *vs = a.qkv_t + (int64_t)(a.Hq + a.Hkv + g) * HD;
   const int n = NQ + (has_pos ? 2 * NK : 0);
-  bool ok = poll_pairs<NT, 4>(n, tag, abort, [&](int j, const uint64_t *&src, float *&dst, int &c) {
+  bool ok = poll_pairs<NT, 4>(n, tag, abort, limit, [&](int j, const uint64_t *&src, float *&dst, int &c) {
     c = 2;
     if (j < NQ) {
       src = qs + 2 * j;

@@ -170,17 +170,28 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
 // Waits for the phase of the given parity to complete; gives up after a bounded number
 // of polls (each poll may suspend the thread for a hardware-defined time) and returns
 // false, so a lost transfer can never hang the GPU.
-constexpr long kWaitPolls = 1L << 22;
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_try(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long limit = kWaitPolls) {
   const uint32_t addr = smem_u32(bar);
-  for (long it = 0; it < kWaitPolls; ++it) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(addr), "r"(parity)
-        : "memory");
-    if (ok) return true;
+  for (long it = 0; it < limit; ++it)
+    if (mbar_try(addr, parity)) return true;
+  return false;
+}
+// The same wait that also gives up once *abort is set (checked every 64 polls): a CTA
+// whose partner warps or other CTAs have left stops waiting for them at once.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, long limit, const int *abort) {
+  const uint32_t addr = smem_u32(bar);
+  for (long it = 0; it < limit; ++it) {
+    if (mbar_try(addr, parity)) return true;
+    if ((it & 63) == 63 && *reinterpret_cast<const volatile int *>(abort)) return false;
   }
   return false;
 }
@@ -396,9 +407,10 @@ constexpr long kTagPolls = 1L << 22;  // bounded polling of tagged words (second
 // j: its source (16-byte aligned when both words are wanted), its destination in
 // shared memory, and how many words it has (1 or 2).  The squares of the values of
 // pairs j < n_sq are added to *sq.  Each thread polls its own pairs, B per round trip,
-// and gives up after kTagPolls rounds or once *abort is set; returns false then.
+// and gives up after `limit` rounds or once *abort is set; returns false then.
 template <int NT, int B, class Map>
-__device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map, int n_sq = 0, float *sq = nullptr) {
+__device__ bool poll_pairs(int n, uint32_t tag, const int *abort, long limit, Map map, int n_sq = 0,
+                           float *sq = nullptr) {
   const int tid = threadIdx.x;
   for (int j0 = tid; j0 < n; j0 += NT * B) {
     uint32_t pending = 0;
@@ -435,7 +447,7 @@ __device__ bool poll_pairs(int n, uint32_t tag, const int *abort, Map map, int n
         }
       }
       if (pending) {
-        if (it >= kTagPolls) return false;
+        if (it >= limit) return false;
         if ((it & 63) == 63 && *reinterpret_cast<const volatile int *>(abort)) return false;
         __nanosleep(32);
       }

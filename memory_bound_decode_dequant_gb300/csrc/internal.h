@@ -97,6 +97,9 @@ size_t attn_counter_bytes(int Hkv);  // the counters at the start of a workspace
 int attn_splits_for(int Hkv, int max_ctx, int bs);
 mie_status launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl);
 
+// Rounds after which a bounded device-side wait gives up (a few seconds).
+constexpr long kWaitPolls = 1L << 22;
+
 // The whole step as one persistent cooperative kernel (step.cu).
 enum { PH_GEMV = 0, PH_ATTN = 1 };
 struct Phase {
@@ -114,6 +117,7 @@ struct PersistArgs {
   uint32_t slot_bytes = 0, slot_sc_bytes = 0;
   int *err = nullptr;
   unsigned long long *trace = nullptr;  // [n_phases][grid][kTracePoints] globaltimer ns, or null
+  long wait_polls = kWaitPolls;         // rounds after which a bounded wait of the step gives up
 };
 constexpr int kTracePoints = 5;  // phase entry, inputs arrived, input staged, stages consumed, outputs written
 struct PersistPlan {

@@ -14,6 +14,7 @@
 // launched with programmatic dependent launch, so inside the graph each one issues
 // its first weight loads while its predecessor drains.  Token, position and block
 // table are read from device memory (StepParams), so one graph serves every step.
+#include <algorithm>
 #include <cstdarg>
 #include <cstdio>
 #include <cmath>
@@ -129,6 +130,11 @@ struct mie_ctx {
   PersistPlan plan;
   unsigned long long *trace = nullptr;
   size_t trace_bytes = 0;
+  // testing aid for the bounded waits (mie_debug_stall): phase whose input is read from
+  // never-written words, and the rounds after which a wait gives up
+  int stall_phase = -1;
+  long wait_polls = kWaitPolls;
+  uint64_t *stall_words = nullptr;
   // few-slot step: its own phase list and graph (always the kernel chain)
   std::vector<Phase> slot_phases;
   cudaGraphExec_t slot_graph = nullptr;
@@ -687,6 +693,7 @@ static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
     pa.err = ctx->err;
     const size_t need = sizeof(unsigned long long) * ctx->phases.size() * ctx->plan.grid * kTracePoints;
     pa.trace = (ctx->trace && ctx->trace_bytes >= need) ? ctx->trace : nullptr;
+    pa.wait_polls = ctx->wait_polls;
     if ((s = persist_launch(ctx->plan, pa, st)) != MIE_OK) return s;
     *launches = 1;
     return MIE_OK;
@@ -706,6 +713,11 @@ static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
 // persistent kernel does not cover falls back to the kernel chain.
 static mie_status prepare_step(mie_ctx *ctx) {
   build_phases(ctx, ctx->phases);
+  if (ctx->stall_phase >= 0 && ctx->stall_phase < (int)ctx->phases.size()) {
+    Phase &ph = ctx->phases[(size_t)ctx->stall_phase];
+    if (ph.kind == PH_GEMV) ph.g.x_t = ctx->stall_words;
+    else ph.at.qkv_t = ctx->stall_words;
+  }
   const size_t bytes = sizeof(Phase) * ctx->phases.size();
   if (ctx->d_phases_cap < bytes) {
     Phase *p = (Phase *)ctx->dalloc(bytes);
@@ -959,6 +971,28 @@ extern "C" mie_status mie_set_trace(mie_ctx *ctx, void *device_buffer, size_t by
   ctx->primed = false;  // the next step re-captures with (or without) the trace
   if (n_phases) *n_phases = 5 * ctx->cfg.n_layers + 1;
   if (n_ctas) *n_ctas = sm_count();
+  return MIE_OK;
+}
+
+// Testing aid: phase `phase` of the persistent step reads its input from words that no
+// phase writes (tag 0, which no launch uses), so its wait can only run out.
+extern "C" mie_status mie_debug_stall(mie_ctx *ctx, int phase, long wait_polls) {
+  if (!ctx) return fail(MIE_E_ARG, "mie_debug_stall: null context");
+  const mie_config &c = ctx->cfg;
+  const int n_phases = 5 * c.n_layers + 1;
+  if (phase == 0 || phase >= n_phases || (phase > 0 && wait_polls < 1))
+    return fail(MIE_E_ARG, "mie_debug_stall: phase %d (1..%d), wait_polls %ld", phase, n_phases - 1, wait_polls);
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  if (phase > 0 && !ctx->stall_words) {
+    // the longest input vector of any phase, as tagged words
+    int64_t n = std::max<int64_t>({(int64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim, c.d_model, c.ffn});
+    ctx->stall_words = (uint64_t *)ctx->dalloc(sizeof(uint64_t) * (size_t)n);
+    if (!ctx->stall_words) return fail(MIE_E_OOM, "mie_debug_stall: word buffer");
+    MIE_CUDA(cudaMemset(ctx->stall_words, 0, sizeof(uint64_t) * (size_t)n));
+  }
+  ctx->stall_phase = phase < 0 ? -1 : phase;
+  ctx->wait_polls = phase < 0 ? kWaitPolls : wait_polls;
+  ctx->primed = false;  // the next step re-captures with the changed phase table and limit
   return MIE_OK;
 }
 

@@ -212,7 +212,8 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     }
     const int n_in = (ph.pro == PRO_EMBED_NORM) ? 0 : (K + 1) / 2;
     const int n_res = (ph.epi == EPI_RESID && a.res_t) ? rr.row1 - rr.row0 : 0;
-    bool ok = poll_pairs<kPCT, B>(n_in + n_res, tag, pa.abort, [&](int j, const uint64_t *&src, float *&dst, int &c) {
+    bool ok = poll_pairs<kPCT, B>(n_in + n_res, tag, pa.abort, pa.wait_polls,
+                                  [&](int j, const uint64_t *&src, float *&dst, int &c) {
       if (j < n_in) {
         src = a.x_t + 2 * j;
         dst = xs + xs_at(2 * j);  // a pair never straddles a padding gap
@@ -255,12 +256,13 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     }
   }
 
-  // stream this CTA's stages of the phase; a wait that gives up stops the math but
-  // keeps every warp on the same barriers
+  // stream this CTA's stages of the phase; a wait that gives up stops the math, and a
+  // warp hands a slot back only after it saw the slot's copy land, so after a failure
+  // the producer can never refill a slot whose copy is still in flight
   bool ok = true;
   for (int st = 0; st < rr.n_stages; ++st, ++s_global) {
     const int slot = s_global % ring.nst, k = s_global / ring.nst;
-    if (ok && !mbar_wait(&ring.full[slot], k & 1)) {
+    if (ok && !mbar_wait_or_abort(&ring.full[slot], k & 1, pa.wait_polls, pa.abort)) {
       ok = false;
       atomicExch(pa.abort, 1);
       latch_error(pa.err, ERR_TIMEOUT);
@@ -281,7 +283,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ring.empty[slot]);
+    if (lane == 0 && ok) mbar_arrive(&ring.empty[slot]);
   }
   if (!ConsSync::all(ok)) return false;
   stamp(pa.trace, pidx, 3);
@@ -411,14 +413,14 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
     sm.m[tid] = -INFINITY;
     sm.l[tid] = 0.f;
   }
-  if (!tagged_inputs<G, HD, kPCT, ConsSync>(at, g, has_pos, sm, sc.tag, pa.abort)) return false;
+  if (!tagged_inputs<G, HD, kPCT, ConsSync>(at, g, has_pos, sm, sc.tag, pa.abort, pa.wait_polls)) return false;
   float o[NO];
 #pragma unroll
   for (int j = 0; j < NO; ++j) o[j] = 0.f;
   bool ok = true;
   for (int cb = b0; cb < b1; cb += cap, ++s_global) {
     const int slot = s_global % ring.nst, k = s_global / ring.nst;
-    if (ok && !mbar_wait(&ring.full[slot], k & 1)) {
+    if (ok && !mbar_wait_or_abort(&ring.full[slot], k & 1, pa.wait_polls, pa.abort)) {
       ok = false;
       atomicExch(pa.abort, 1);
       latch_error(pa.err, ERR_TIMEOUT);
@@ -438,7 +440,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
     }
     fence_proxy_async_smem();  // the patch above was a generic write into a bulk-copy slot
     __syncwarp();
-    if (lane == 0) mbar_arrive(&ring.empty[slot]);
+    if (lane == 0 && ok) mbar_arrive(&ring.empty[slot]);  // only a slot whose copy landed
     ConsSync::sync();  // the next stage rewrites sm.s
   }
   if (!ConsSync::all(ok)) return false;
@@ -597,7 +599,7 @@ __device__ void produce(const PersistArgs &a, const Ring &ring, const StepConst 
   bool sc_ready = false;
   while (!ld.done) {
     const int slot = s_global % a.n_slots, k = s_global / a.n_slots;
-    if (k > 0 && !mbar_wait(&ring.empty[slot], (k - 1) & 1)) {
+    if (k > 0 && !mbar_wait_or_abort(&ring.empty[slot], (k - 1) & 1, a.wait_polls, a.abort)) {
       atomicExch(a.abort, 1);
       latch_error(a.err, ERR_TIMEOUT);
       break;
@@ -615,7 +617,7 @@ __device__ void produce(const PersistArgs &a, const Ring &ring, const StepConst 
                   pol);
     } else {
       if (!sc_ready) {  // the block ids are staged in shared memory by the consumers
-        for (long it = 0; it < kWaitPolls && !s_sc_ready; ++it) __nanosleep(64);
+        for (long it = 0; it < a.wait_polls && !s_sc_ready; ++it) __nanosleep(64);
         __threadfence_block();
         sc_ready = true;
       }

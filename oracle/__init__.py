@@ -2,7 +2,9 @@
 
 Only the tests, `__graft_entry__.smoke()` and the bench's CPU-baseline leg may import
 this package.  It is a thin ctypes layer: every number it returns is computed by the
-plain single-threaded C code in mie_oracle.c.  It shares no code with the CUDA library.
+plain C code in mie_oracle.c (serial by default; set_threads(n) spreads independent
+rows and heads over n host threads with bit-identical results).  It shares no code
+with the CUDA library.
 
 Parity pins: every function is pinned by a `-m "not gpu"` test.  The full-model logits
 are "parity unpinned" beyond the composition of pinned parts (the pages print no
@@ -32,8 +34,11 @@ def build(force: bool = False) -> str:
     src = os.path.join(_HERE, "mie_oracle.c")
     if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(src):
         tmp = _SO + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off",
-                               "-fno-fast-math", "-o", tmp, src, "-lm"])
+        base = ["gcc", "-O2", "-fPIC", "-shared", "-std=c11", "-ffp-contract=off", "-fno-fast-math"]
+        try:  # OpenMP for the optional multi-threaded runs; without it the oracle is serial
+            subprocess.check_call(base + ["-fopenmp", "-o", tmp, src, "-lm"], stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base + ["-o", tmp, src, "-lm"])
         os.replace(tmp, _SO)
     return _SO
 
@@ -53,6 +58,8 @@ def lib():
     L = ctypes.CDLL(_SO)
     i, i64, f, d = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double
     sig = {
+        "or_set_threads": (i, [i]),
+        "or_max_threads": (i, []),
         "or_f32_to_bf16": (ctypes.c_uint16, [f]),
         "or_bf16_to_f32": (f, [ctypes.c_uint16]),
         "or_f32_to_f16": (ctypes.c_uint16, [f]),
@@ -110,6 +117,16 @@ def _p(a):
 
 
 # --------------------------------------------------------------------- conversions
+
+def set_threads(n: int) -> int:
+    """Host threads for the oracle's independent rows and heads (1 = serial); returns
+    the count in effect (1 when built without OpenMP)."""
+    return int(lib().or_set_threads(int(n)))
+
+
+def max_threads() -> int:
+    return int(lib().or_max_threads())
+
 
 def to_bf16(x) -> np.ndarray:
     x = _c(x, np.float32)

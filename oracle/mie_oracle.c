@@ -6,13 +6,15 @@
  * or helper with the CUDA library; both sides draw their inputs from the separate
  * `synth` generator module.
  *
- * What it is: a plain, slow, single-threaded CPU implementation of what the decode
- * step computes, written for a reader to check against the pages by eye.  Tensors
- * are stored at the precision the pages fix -- fp32 activations and residual stream,
- * bf16 K/V cache, quantised weights (the "infer" page, design notes: weights in bf16,
- * activations and sums in fp32, the cache in bf16; its reference rounds K and V to bf16
- * when they enter the cache).  Inside one operation every sum is taken in fp64 and the result rounded once
- * to fp32, so each function returns its plain definition rounded to the storage type.
+ * What it is: a plain, slow CPU implementation of what the decode step computes,
+ * written for a reader to check against the pages by eye (single-threaded unless
+ * or_set_threads asks for more; the result is the same).  Tensors are stored at the
+ * precision the pages fix -- fp32 activations and residual stream, bf16 K/V cache,
+ * quantised weights (the "infer" page, design notes: weights in bf16, activations and
+ * sums in fp32, the cache in bf16; its reference rounds K and V to bf16 when they
+ * enter the cache).  Inside one operation every sum is taken in fp64 and the result
+ * rounded once to fp32, so each function returns its plain definition rounded to the
+ * storage type.
  * Compile with -ffp-contract=off so that no multiply-add is fused behind the reader's
  * back (the quantisers' rounding decisions depend on it).
  *
@@ -21,8 +23,8 @@
  *  [MIE]   "Mini Inference Engine"
  *  [INFER] "infer" -- an LLM inference engine in C++ and CUDA for Llama-3.2-1B
  *
- * Readings of points the pages leave open are marked READING below; each is also
- * listed in the design document.
+ * Readings of points the pages leave open are marked READING below, each with the
+ * reason it was taken.
  *
  * Parity pins: every function here is pinned by a `-m "not gpu"` test against
  * something other than itself (closed forms, invariants, brute force, numpy's IEEE
@@ -34,6 +36,36 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------ threads */
+
+/* Host threads used by the loops marked "parallel over independent ..." below (GEMV
+ * output rows, attention heads, quantiser rows, element conversions).  Each output
+ * keeps its own serial arithmetic, so the results are bit-identical for every thread
+ * count; 1 (the default) runs everything on the calling thread.  Built without
+ * OpenMP the pragmas are ignored and the count stays 1. */
+static int g_threads = 1;
+
+int or_set_threads(int n) {
+#ifdef _OPENMP
+  g_threads = n < 1 ? 1 : n;
+#else
+  (void)n;
+  g_threads = 1;
+#endif
+  return g_threads;
+}
+
+int or_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_num_procs();
+#else
+  return 1;
+#endif
+}
 
 /* ------------------------------------------------------------------ conversions */
 
@@ -88,6 +120,7 @@ float or_f16_to_f32(uint16_t h) {
 }
 
 void or_f32_to_bf16_n(const float *x, int64_t n, uint16_t *out) {
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1) /* independent elements */
   for (int64_t i = 0; i < n; ++i) out[i] = or_f32_to_bf16(x[i]);
 }
 void or_bf16_to_f32_n(const uint16_t *x, int64_t n, float *out) {
@@ -120,6 +153,7 @@ enum { OR_BF16 = 0, OR_I8 = 1, OR_Q4_0 = 2, OR_F32 = 3 };
  * Output: rows of ceil(K/32) blocks of 18 bytes, [M][nb][18]. */
 void or_q4_0_quantize(const float *w, int M, int K, uint8_t *out) {
   const int nb = (K + Q4_BLOCK - 1) / Q4_BLOCK;
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1) /* independent rows */
   for (int r = 0; r < M; ++r) {
     for (int b = 0; b < nb; ++b) {
       float v[Q4_BLOCK];
@@ -169,6 +203,7 @@ void or_q4_0_dequantize(const uint8_t *wq, int M, int K, float *w) {
  * READING: s = max|w| / 127 in fp32; q = round-half-away(w / s) clamped to
  * [-127, 127]; a zero row has s = 0 and all q = 0. */
 void or_i8_quantize(const float *w, int M, int K, int8_t *q, float *s) {
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1) /* independent rows */
   for (int r = 0; r < M; ++r) {
     const float *row = w + (int64_t)r * K;
     float amax = 0.0f;
@@ -202,6 +237,7 @@ void or_i8_dequantize(const int8_t *q, const float *s, int M, int K, float *w) {
  * f32 [M][K]. */
 void or_gemv(int fmt, const void *W, const float *s, const float *x, int M, int K, float *y) {
   const int nb = (K + Q4_BLOCK - 1) / Q4_BLOCK;
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1 && M >= 64) /* independent rows */
   for (int r = 0; r < M; ++r) {
     double acc = 0.0;
     if (fmt == OR_BF16) {
@@ -344,10 +380,13 @@ void or_attention_paged(const float *q, const uint16_t *k_pool, const uint16_t *
                         int64_t block_stride, const int32_t *block_table, int ctx, int Hq,
                         int Hkv, int hd, int bs, float scale, float *out) {
   paged_view pv = {k_pool, v_pool, block_stride, block_table, bs, hd};
-  double *score = (double *)malloc(sizeof(double) * (ctx > 0 ? ctx : 1));
+  const int64_t per_head = ctx > 0 ? ctx : 1;
+  double *score = (double *)malloc(sizeof(double) * (size_t)(per_head * Hq));
   const int group = Hq / Hkv;
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1) /* independent heads */
   for (int h = 0; h < Hq; ++h)
-    attend_head(q + h * hd, hd, ctx, h / group, (double)scale, paged_look, &pv, out + h * hd, score);
+    attend_head(q + h * hd, hd, ctx, h / group, (double)scale, paged_look, &pv, out + h * hd,
+                score + h * per_head);
   free(score);
 }
 

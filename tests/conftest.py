@@ -16,4 +16,7 @@ def pytest_configure(config):
 def orc():
     import oracle
     oracle.lib()
+    # all host cores: rows and heads are independent and each keeps its serial sum, so
+    # the oracle's results are the same bits as on one thread (pinned by a test)
+    oracle.set_threads(oracle.max_threads())
     return oracle

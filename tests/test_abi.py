@@ -125,6 +125,13 @@ def test_host_side_argument_checks(L):
     assert L.mie_paged_attn_decode(fake, fake, fake, 4096, 4, fake, 2, 33, 8, 2, 32, 16, 1.0, fake, fake,
                                    1 << 20, None) == 2
     assert L.mie_argmax(fake, 0, fake, fake, 1024, None) == 2
+    # the read probe: whole aligned words only, 16- or 32-byte loads, 1..4 CTAs per SM
+    assert L.mie_hbm_read_probe(None, 64, fake, 32, 2, None) == 1
+    assert L.mie_hbm_read_probe(fake, 64, fake, 8, 2, None) == 1
+    assert L.mie_hbm_read_probe(fake, 64, fake, 32, 5, None) == 1
+    assert L.mie_hbm_read_probe(fake, 48, fake, 32, 2, None) == 2
+    assert L.mie_hbm_read_probe(ctypes.c_void_p(272), 64, fake, 32, 2, None) == 2
+    assert L.mie_hbm_read_probe(fake, 0, fake, 16, 2, None) == 2
 
 
 def test_q4_0_packed_bytes(L):

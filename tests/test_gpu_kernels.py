@@ -1,6 +1,6 @@
 """Parity of the CUDA kernels with the oracle, through the C ABI (GPU only).
 
-Tolerances (the arithmetic fixes them; see the design document):
+Tolerances (the arithmetic fixes them):
   * quantisers, K/V gathers, argmax: bit-exact;
   * GEMV: |dy_i| <= 1e-3 * max(|y_ref_i|, rms(y_ref)) (fp32 accumulation in another
     order than the oracle's fp64 sum);
@@ -258,3 +258,17 @@ def test_argmax_ties_pick_lowest_index(orc):
     assert int(mie.mie_argmax(torch.from_numpy(v).cuda()).item()) == 7 == orc.argmax(v)
     v = np.zeros(50000, np.float32)
     assert int(mie.mie_argmax(torch.from_numpy(v).cuda()).item()) == 0
+
+
+@pytest.mark.parametrize("load_bytes", [16, 32])
+@pytest.mark.parametrize("blocks_per_sm", [1, 2, 4])
+def test_hbm_read_probe_reads_every_word_once(load_bytes, blocks_per_sm):
+    """The probe's XOR of all 32-bit words equals numpy's, on buffers that end in a
+    ragged part of the grid stride and on one single load."""
+    for n_words in ((1 << 22) + 8 * 37, load_bytes // 4):
+        words = synth.uniform_int(0x5052 + n_words, n_words, -(1 << 31), (1 << 31) - 1)
+        want = int(np.bitwise_xor.reduce(words.view(np.uint32)))
+        d = torch.from_numpy(words).cuda()
+        got = mie.mie_hbm_read_probe(d, load_bytes=load_bytes, blocks_per_sm=blocks_per_sm)
+        torch.cuda.synchronize()
+        assert (int(got.item()) & 0xFFFFFFFF) == want, (n_words, load_bytes, blocks_per_sm)

@@ -4,6 +4,8 @@ Tolerances: max |dlogit| <= 2e-2 * std(logits) per step, argmax identical wherev
 oracle's top-2 margin exceeds 1e-2; K/V cache entries within one bf16 step of the value
 plus 1e-3 of the tensor's RMS (the GEMV tolerance), with > 97% of them bit-identical.
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -216,3 +218,44 @@ def test_step_rejects_bad_inputs():
     with pytest.raises(mie.MieError) as e:
         empty.decode_step(1, 0, bt, logits)
     assert e.value.status == 6
+
+
+@pytest.mark.parametrize("phase", [1, 3, 10])
+def test_bounded_wait_runs_out_then_the_step_recovers(orc, phase):
+    """A phase whose input never arrives (attention, gate/up, the LM head of the tiny
+    two-layer model: its input words are redirected to a buffer no phase writes) makes
+    the persistent step's bounded waits give up: the step ends on its own, mie_sync
+    reports MIE_E_TIMEOUT, and once the phase table is restored the same position and
+    the next one match the oracle again."""
+    shape = synth.TINY
+    n_blocks, max_pos = 8, 128
+    bt_host = synth.permutation(6, n_blocks).astype(np.int32)
+    bt = torch.from_numpy(bt_host).cuda()
+    gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+    om = orc.Model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    toks = prompt_tokens(shape, 12)
+    for pos in range(10):
+        om.decode_step(int(toks[pos]), pos, bt_host)
+        gm.decode_step(int(toks[pos]), pos, bt, logits, am)
+    gm.sync()
+    assert gm.step_mode == PERSISTENT
+    gm.debug_stall(phase, 1 << 14)
+    t0 = time.perf_counter()
+    gm.decode_step(int(toks[10]), 10, bt, logits, am)
+    with pytest.raises(mie.MieError) as e:
+        gm.sync()
+    assert e.value.status == 5, e.value  # MIE_E_TIMEOUT
+    assert time.perf_counter() - t0 < 30
+    gm.debug_stall(-1)
+    for pos in (10, 11):
+        ref, _ = om.decode_step(int(toks[pos]), pos, bt_host)
+        gm.decode_step(int(toks[pos]), pos, bt, logits, am)
+        gm.sync()
+        check_logits(logits.cpu().numpy(), ref, pos)
+        check_argmax(int(am.item()), ref, pos)
+    with pytest.raises(mie.MieError) as e:  # phase 0 has no input to withhold
+        gm.debug_stall(0, 1 << 14)
+    assert e.value.status == 1
+    gm.close()

@@ -439,6 +439,29 @@ def test_incremental_equals_nocache(orc):
     assert np.array_equal(logits, ref) and best == rbest
 
 
+def test_threads_do_not_change_a_bit(orc):
+    """Spreading rows and heads over host threads keeps every output's serial sum:
+    the quantisers, a GEMV and 24 decode steps give the same bits on 1 and 4 threads."""
+    if orc.max_threads() < 2:
+        pytest.skip("oracle built without OpenMP")
+    w = synth.normal(0x7417, 300 * 688, std=0.02).reshape(300, 688)
+    x = synth.normal(0x7418, 688)
+    runs = []
+    for n in (1, 4):
+        assert orc.set_threads(n) == n
+        q4 = orc.q4_0_quantize(w)
+        q8, s8 = orc.i8_quantize(w)
+        y = orc.gemv(orc.Mat("q4_0", q4, 300, 688), x)
+        m = _tiny_model(orc)
+        bt = synth.permutation(8, 16).astype(np.int32)
+        for pos, t in enumerate(synth.TINY.tokens(24)):
+            logits, best = m.decode_step(int(t), pos, bt)
+        runs.append((q4, q8, s8, y, logits, best, m.kv().copy()))
+    orc.set_threads(orc.max_threads())
+    for a, b in zip(*runs):
+        assert np.array_equal(np.asarray(a), np.asarray(b))
+
+
 def test_paged_step_independent_of_physical_order(orc):
     toks = synth.TINY.tokens(18)
     outs = []
