@@ -68,6 +68,10 @@ def parse():
     ap.add_argument("--sweep-min", type=int, default=20, help="sweep: least number of input copies per case")
     ap.add_argument("--kernel-only", action="store_true",
                     help="time only the dominant kernel (the profiling command)")
+    ap.add_argument("--quick", action="store_true",
+                    help="the headline step only: skip the other workloads recorded in the default line")
+    ap.add_argument("--decode-steps", type=int, default=128,
+                    help="timed decode steps at each context of the per-context table")
     return ap.parse_args()
 
 
@@ -179,21 +183,60 @@ def oracle_model(shape, ctx: int, n_extra: int):
     return om, np.arange(n_blocks, dtype=np.int32)
 
 
-def time_oracle(shape, ctx: int, steps: int):
-    """Seconds per oracle decode step (single-threaded plain C), over `steps` steps."""
+def cpu_model() -> str:
+    """The host CPU's model string (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def time_oracle(shape, ctx: int, steps: int, threads: int = 1):
+    """Seconds per oracle decode step over `steps` steps, on `threads` host threads (the
+    oracle spreads GEMV rows and attention heads over them, bit-identically)."""
+    import oracle
     om, bt = oracle_model(shape, ctx, steps)
+    oracle.set_threads(threads)
     toks = shape.tokens(steps, stream=3)
-    t0 = time.perf_counter()
-    for i in range(steps):
-        om.decode_step(int(toks[i]), ctx + i, bt)
-    return (time.perf_counter() - t0) / steps
+    try:
+        t0 = time.perf_counter()
+        for i in range(steps):
+            om.decode_step(int(toks[i]), ctx + i, bt)
+        return (time.perf_counter() - t0) / steps
+    finally:
+        oracle.set_threads(1)
+
+
+def oracle_baseline(shape, ctx: int, steps: int) -> dict:
+    """The oracle on all host cores (the reported baseline) and on one core."""
+    import oracle
+    n = oracle.max_threads()
+    sec_all = time_oracle(shape, ctx, steps, threads=n)
+    sec_one = time_oracle(shape, ctx, steps, threads=1)
+    return {"value": 1.0 / sec_all, "unit": "tok/s", "cores": n, "kind": "oracle", "cpu": cpu_model(),
+            "sample": f"{steps} full decode steps of the oracle (plain C, fp64 sums; GEMV rows and attention "
+                      f"heads over {n} threads) at ctx {ctx}, K/V cache prefilled with seeded values",
+            "single_core": {"value": 1.0 / sec_one, "unit": "tok/s", "cores": 1}}
 
 
 def run_reference(args, shape):
     if env_rank()[0] != 0:  # under torchrun rank 0 alone times the oracle
         return
+    import oracle
     steps = max(1, args.steps)
     om, bt = oracle_model(shape, args.ctx, args.warmup + steps)
+    cores = oracle.set_threads(oracle.max_threads())
     toks = shape.tokens(args.warmup + steps, stream=3)
     for i in range(args.warmup):
         om.decode_step(int(toks[i]), args.ctx + i, bt)
@@ -206,11 +249,11 @@ def run_reference(args, shape):
             "n_gpus": 1, "steps": steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64-accumulate/f32",
             "data": "synthetic (seeded N(0,0.02) weights, uniform tokens)",
-            "config": {"workload": f"{shape.name} {args.fmt} batch-1 decode step", "model": shape.name,
-                       "weights": args.fmt, "global_batch": 1, "seq_len": args.ctx},
-            "cpu_baseline": {"kind": "oracle", "cores": 1, "value": v, "unit": "tok/s",
-                             "sample": f"{steps} full decode steps of the oracle (single-threaded C) at ctx "
-                                       f"{args.ctx}+, K/V cache prefilled with seeded values"},
+            "config": step_config(args, shape, 1),
+            "cpu_baseline": {"kind": "oracle", "cores": cores, "value": v, "unit": "tok/s", "cpu": cpu_model(),
+                             "sample": f"{steps} full decode steps of the oracle (plain C, fp64 sums, GEMV rows "
+                                       f"and attention heads over {cores} threads) at ctx {args.ctx}+, K/V cache "
+                                       f"prefilled with seeded values"},
             "e2e": {"value": v, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -280,7 +323,9 @@ def read_traffic(name: str):
 def gemv_roofline(torch, mie, n_iter: int = 40):
     """The dominant kernel of the step -- the bf16 GEMV at the gate/up shape
     (16384 x 2048, 42% of the step's weight bytes) -- timed alone with CUDA events on
-    its stream, rotating over enough weight copies (> 1 GB) that L2 serves nothing."""
+    its stream: n_iter back-to-back launches captured in one CUDA graph (so no host
+    launch gap sits between them), rotating over enough weight copies (> 1 GB) that L2
+    serves nothing; the median of 5 replays."""
     M, K = 16384, 2048
     copies = 20
     w = torch.empty((copies, M, K), dtype=torch.bfloat16, device="cuda")
@@ -288,21 +333,96 @@ def gemv_roofline(torch, mie, n_iter: int = 40):
         w[c].copy_(torch.from_numpy(synth.normal(0x525F + c, M * K, std=0.02).reshape(M, K)).to(torch.bfloat16))
     x = torch.from_numpy(synth.normal(0x5260, K)).to(torch.bfloat16).float().cuda()
     y = torch.empty(M, dtype=torch.float32, device="cuda")
-    st = torch.cuda.current_stream()
-    for i in range(6):
-        mie.mie_gemv_bf16(w[i % copies], x, y, stream=st)
-    st.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for i in range(n_iter):
-        mie.mie_gemv_bf16(w[i % copies], x, y, stream=st)
-    e1.record(st)
-    e1.synchronize()
-    dt = e0.elapsed_time(e1) / 1e3 / n_iter
+    dt = graph_time(torch, [(lambda st, i=i: mie.mie_gemv_bf16(w[i % copies], x, y, stream=st))
+                            for i in range(n_iter)])
     algo = synth.gemv_bytes("bf16", M, K)
     del w
     torch.cuda.empty_cache()
     return algo, dt, n_iter
+
+
+def read_probe(torch, mie, gib: int = 4) -> dict:
+    """The read-only streaming peak of this GPU: mie_hbm_read_probe over a `gib` GiB
+    buffer (31 x L2 at 4 GiB), 16- and 32-byte loads at 1, 2 and 4 CTAs per SM, the
+    best median of 10 back-to-back launches."""
+    buf = torch.empty((gib << 28,), dtype=torch.int32, device="cuda")
+    buf.fill_(0x5A5A5A5A)
+    nbytes = buf.numel() * 4
+    out = torch.empty(1, dtype=torch.int32, device="cuda")
+    st = torch.cuda.current_stream()
+    runs = []
+    for load in (16, 32):
+        for bps in (1, 2, 4):
+            for _ in range(3):
+                mie.mie_hbm_read_probe(buf, out, load, bps, stream=st)
+            times = []
+            for _ in range(3):  # 10 back-to-back launches between one pair of events
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                for _ in range(10):
+                    mie.mie_hbm_read_probe(buf, out, load, bps, stream=st)
+                e1.record(st)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) / 1e3 / 10)
+            runs.append({"load_bytes": load, "blocks_per_sm": bps, "gbs": nbytes / statistics.median(times) / 1e9})
+    del buf
+    torch.cuda.empty_cache()
+    best = max(runs, key=lambda r: r["gbs"])
+    return {"gbs": best["gbs"], "best": best, "bytes": nbytes, "runs": runs,
+            "method": f"mie_hbm_read_probe over {gib} GiB; per setting the median of 3 timings of 10 "
+                      f"back-to-back launches"}
+
+
+def contexts_table(torch, gm, stream, shape, bt, logits, am, pos: int, tok: int, ctxs, steps: int, peak: float,
+                   read_peak: float | None) -> tuple[list, int, int]:
+    """For each context in order: real greedy decode steps (untimed) bring the sequence
+    to that context, then `steps` steps replayed from the graph are timed with events on
+    the context's stream.  Returns the rows and the position and token reached."""
+    rows = []
+    for ctx in ctxs:
+        if ctx <= pos:
+            continue
+        gm.decode_step(tok, pos, bt, logits, am)  # the step at pos; the graph advances from there
+        gm.decode_continue(ctx - pos - 1)  # the next step writes position ctx
+        gm.sync()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gm.decode_continue(steps)
+        e1.record(stream)
+        e1.synchronize()
+        gm.sync()
+        dt = e0.elapsed_time(e1) / 1e3 / steps
+        b = shape.decode_bytes(ctx, steps)
+        row = {"ctx": ctx, "steps": steps, "tok_s": 1.0 / dt, "ms_per_step": dt * 1e3, "step_bytes": b,
+               "gbs": b / dt / 1e9, "frac_of_peak": b / dt / 1e9 / peak}
+        if read_peak:
+            row["frac_of_read_probe"] = b / dt / 1e9 / read_peak
+        rows.append(row)
+        pos = ctx + steps
+        with torch.cuda.stream(stream):
+            tok = int(am.item())
+    return rows, pos, tok
+
+
+def model_contexts(torch, shape, ctxs, steps: int, peak: float, read_peak: float | None, label: str) -> dict:
+    """A fresh context for `shape`, prefilled from position 0 by real decode steps,
+    timed at each context of ctxs (contexts_table)."""
+    from memory_bound_decode_dequant_gb300.workload import build_gpu_model
+    bs = shape.block_size
+    n_blocks = (max(ctxs) + steps + bs - 1) // bs + 2
+    stream = torch.cuda.Stream()
+    gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=n_blocks * bs, stream=stream)
+    bt = torch.from_numpy(synth.permutation(0x4254, n_blocks).astype(np.int32)).cuda()
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    rows, _, _ = contexts_table(torch, gm, stream, shape, bt, logits, am, 0, int(shape.tokens(1)[0]), ctxs, steps,
+                                peak, read_peak)
+    out = {"workload": label, "weights": shape.wfmt, "head": shape.head_fmt, "weight_bytes": shape.weight_bytes(),
+           "step_mode": "persistent" if gm.step_mode == 0 else "chain", "contexts": rows}
+    gm.close()
+    del gm
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_mie(args, shape):
@@ -314,7 +434,9 @@ def run_mie(args, shape):
     from memory_bound_decode_dequant_gb300.workload import build_gpu_model
 
     bs = shape.block_size
-    total = args.ctx + 2 * (args.warmup + args.steps) + args.e2e_steps + 2
+    ctxs = [c for c in CONTEXTS[shape.name] if c > args.ctx] if not args.quick else []
+    total = max([args.ctx + 2 * (args.warmup + args.steps) + args.e2e_steps + 2] +
+                [c + args.decode_steps + 2 for c in ctxs])
     n_blocks = (total + bs - 1) // bs + 1
     max_pos = n_blocks * bs
     stream = torch.cuda.Stream()  # the context's stream: events are recorded on it
@@ -351,11 +473,11 @@ def run_mie(args, shape):
     dt_local = e0.elapsed_time(e1) / 1e3 / args.steps
     barrier(pg)
     dt = max_over_ranks(pg, dt_local)
-    ctx_end = args.ctx + args.warmup + args.steps
 
     # end to end: host token and position in, argmax read back every step
     pos = args.ctx + args.warmup + args.steps
-    tok = int(am.item())
+    with torch.cuda.stream(stream):
+        tok = int(am.item())
     gm.sync()
     barrier(pg)
     t0 = time.perf_counter()
@@ -370,8 +492,21 @@ def run_mie(args, shape):
     # algorithmic bytes of one step: all weights once + the K/V of every position read
     step_bytes = shape.decode_bytes(args.ctx + args.warmup, args.steps)  # the timed steps
     peak, peak_kind = measured_peaks()
+    extras = {}
+    if rank == 0 and world == 1 and not args.quick:
+        extras["read_probe"] = guarded(lambda: read_probe(torch, mie))
+    read_peak = (extras.get("read_probe") or {}).get("gbs")
+    if ctxs:  # the longer contexts of the same sequence, on the same context
+        head = {"ctx": args.ctx, "steps": args.steps, "tok_s": 1.0 / dt, "ms_per_step": dt * 1e3,
+                "step_bytes": step_bytes, "gbs": step_bytes / dt / 1e9, "frac_of_peak": step_bytes / dt / 1e9 / peak}
+        if read_peak:
+            head["frac_of_read_probe"] = step_bytes / dt / 1e9 / read_peak
+        rows, pos, tok = contexts_table(torch, gm, stream, shape, bt, logits, am, pos, tok, ctxs, args.decode_steps,
+                                        peak, read_peak)
+        extras["contexts"] = [head] + rows
 
     result = None
+    step_mode = "persistent" if gm.step_mode == 0 else "chain"
     if rank == 0:
         algo, kdt, n_iter = gemv_roofline(torch, mie)
         achieved = algo / kdt / 1e9
@@ -379,7 +514,8 @@ def run_mie(args, shape):
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": achieved / peak, "frac_of_spec": achieved / SPEC_HBM_GBS,
                      "traffic": read_traffic("gemv_bf16_16384x2048"),
-                     "algorithmic_bytes": algo, "launches_timed": n_iter, "us_per_launch": kdt * 1e6}
+                     "algorithmic_bytes": algo, "launches_timed": n_iter, "us_per_launch": kdt * 1e6,
+                     "method": "40 back-to-back launches in one CUDA graph, median of 5 replays"}
         if gm.step_mode == 0:
             # the persistent step is the step's only launch: its duration is the step time
             # measured above with events on its stream
@@ -391,13 +527,29 @@ def run_mie(args, shape):
                     "algorithmic_bytes": step_bytes, "launches_timed": args.steps, "us_per_launch": dt * 1e6}
         else:
             roof = gemv_roof
+        for r in (roof, gemv_roof):
+            if read_peak:
+                r["read_probe_gbs"] = read_peak
+                r["frac_of_read_probe"] = r["achieved"] / read_peak
+    gm.close()
+    del gm
+    torch.cuda.empty_cache()
+    if rank == 0:
+        if world == 1 and not args.quick:
+            # the other workloads of the decode-step family, each recorded in this line
+            fmts = {"bf16": "i8 q4_0", "i8": "bf16 q4_0", "q4_0": "bf16 i8"}[args.fmt].split()
+            for f in fmts:
+                extras[f"contexts_{f}"] = guarded(lambda f=f: model_contexts(
+                    torch, synth.llama32_1b(f), CONTEXTS["llama-3.2-1b"], args.decode_steps, peak, read_peak,
+                    f"llama-3.2-1b {f} batch-1 decode"))
+            extras["tinyllama_q4_0"] = guarded(lambda: model_contexts(
+                torch, synth.TINYLLAMA, CONTEXTS["tinyllama-1.1b"], args.decode_steps, peak, read_peak,
+                "tinyllama-1.1b q4_0 (bf16 GEMV inputs) batch-1 decode"))
+            extras["slots"] = guarded(lambda: slots_summary(measure_slots(args, torch)))
+            extras["kernel_sweep"] = guarded(lambda: measure_sweep(args, clocks=False))
         cpu = None
         if not args.no_cpu_baseline and world == 1:
-            n = max(1, args.oracle_steps)
-            sec = time_oracle(shape, args.ctx, n)
-            cpu = {"value": 1.0 / sec, "unit": "tok/s", "cores": 1, "kind": "oracle",
-                   "sample": f"{n} full decode steps of the oracle (plain single-threaded C) at ctx {args.ctx}, "
-                             f"K/V cache prefilled with seeded values"}
+            cpu = oracle_baseline(shape, args.ctx, max(1, args.oracle_steps))
         value = world * 1.0 / dt
         result = {
             "metric": "batch-1 decode tok/s (Llama-3.2-1B shape)",
@@ -412,30 +564,53 @@ def run_mie(args, shape):
             "vs_baseline": None,
             "dtype": "bf16 weights, f32 activations/accumulation, bf16 KV",
             "data": "synthetic (seeded N(0,0.02) weights, uniform tokens, prefilled by real decode steps)",
-            "config": {"workload": f"{shape.name} {args.fmt} batch-1 decode step"
-                                   + (f" ({shape.n_layers} layers, profiling case)" if args.layers else ""),
-                       "model": shape.name, "weights": args.fmt, "global_batch": world, "seq_len": args.ctx,
-                       "ctx_range": [args.ctx, ctx_end], "parallelism": "replicas" if world > 1 else "single",
-                       "l2": "weights 2.47 GB per step >> 129 MB L2: inputs larger than L2",
-                       "step_bytes": step_bytes, "step_hbm_gbs": step_bytes / dt / 1e9,
-                       "step_frac_of_peak": step_bytes / dt / 1e9 / peak,
-                       "step_frac_of_spec": step_bytes / dt / 1e9 / SPEC_HBM_GBS},
+            "config": step_config(args, shape, world),
+            "step_hbm": {"step_bytes": step_bytes, "gbs": step_bytes / dt / 1e9,
+                         "frac_of_peak": step_bytes / dt / 1e9 / peak,
+                         "frac_of_spec": step_bytes / dt / 1e9 / SPEC_HBM_GBS,
+                         "frac_of_read_probe": (step_bytes / dt / 1e9 / read_peak) if read_peak else None},
             "roofline": roof,
             "gemv_roofline": gemv_roof,
             "e2e": {"value": world / e2e_dt, "unit": "tok/s", "h2d_bytes_per_step": STEP_PARAMS_BYTES,
                     "d2h_bytes_per_step": 4},
             "gpu_launches": launches * args.steps,
             "launches_per_step": launches,
-            "step_mode": "persistent" if gm.step_mode == 0 else "chain",
+            "step_mode": step_mode,
             "clocks": clk.summary(),
             "wall_s_timed": t_wall,
             "cpu_baseline": cpu,
         }
+        result.update(extras)
         print(json.dumps(result), flush=True)
-    gm.close()
     if pg is not None:
         pg.destroy_process_group()
     return result
+
+
+def step_config(args, shape, world: int) -> dict:
+    """The workload of the batch-1 line, the same dict in both arms."""
+    return {"workload": f"{shape.name} {args.fmt} batch-1 decode step"
+                        + (f" ({shape.n_layers} layers, profiling case)" if args.layers else ""),
+            "model": shape.name, "weights": args.fmt, "global_batch": world, "seq_len": args.ctx,
+            "ctx_range": [args.ctx, args.ctx + args.warmup + args.steps],
+            "parallelism": "replicas" if world > 1 else "single",
+            "l2": "weights 2.47 GB per step >> 129 MB L2: inputs larger than L2",
+            "step_bytes": shape.decode_bytes(args.ctx + args.warmup, args.steps)}
+
+
+def guarded(fn):
+    """Runs one of the extra workloads of the default line; a failure is reported in its
+    key instead of losing the headline."""
+    try:
+        return fn()
+    except Exception as e:  # noqa: BLE001 -- the line must still be printed
+        import traceback
+        return {"error": f"{type(e).__name__}: {e}", "where": traceback.format_exc().splitlines()[-3:]}
+
+
+# the contexts each workload is quoted at (the decode tables of the pages: Llama-3.2-1B at
+# 128 / 512 / 2048, TinyLlama at 50 / 500 / 1500)
+CONTEXTS = {"llama-3.2-1b": [128, 512, 2048], "tinyllama-1.1b": [50, 500, 1500]}
 
 
 # ----------------------------------------------------------------------------- few-slot step
@@ -468,8 +643,27 @@ def run_slots(args):
 
     rank, world, local, pg = dist_init(args)
     torch.cuda.set_device(local)
-    import memory_bound_decode_dequant_gb300 as mie
+    line = measure_slots(args, torch, rank=rank, world=world, local=local,
+                         with_cpu=rank == 0 and not args.no_cpu_baseline and world == 1)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+def slots_summary(line: dict) -> dict:
+    """The few-slot workload's figures as one key of the default line."""
+    keep = ("metric", "value", "unit", "ms_per_step", "steps", "dtype", "config", "roofline", "e2e",
+            "launches_per_step", "clocks")
+    return {k: line[k] for k in keep if k in line}
+
+
+def measure_slots(args, torch, rank: int = 0, world: int = 1, local: int | None = None,
+                  with_cpu: bool = False) -> dict:
+    """The 8-slot continuous-batching workload (--workload slots); returns its line."""
     from memory_bound_decode_dequant_gb300.workload import build_gpu_model
+    if local is None:
+        local = torch.cuda.current_device()
 
     shape = synth.llama32_1b("bf16")
     if args.layers:  # a truncated model for profiling captures
@@ -549,9 +743,8 @@ def run_slots(args):
     kv_bytes = shape.kv_bytes_per_token() * kv_tokens / wl.steps
     step_bytes = w_bytes + kv_bytes
     peak, peak_kind = measured_peaks()
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline and world == 1:
-        cpu = time_oracle_slots(shape, wl)
+    cpu = time_oracle_slots(shape, wl) if with_cpu else None
+    line = None
     if rank == 0:
         ach = step_bytes / dt / 1e9
         line = {
@@ -576,10 +769,10 @@ def run_slots(args):
             "gpu_launches": gm.slot_launches * wl.steps, "launches_per_step": gm.slot_launches,
             "clocks": clk.summary(), "wall_s_timed": t_wall, "cpu_baseline": cpu,
         }
-        print(json.dumps(line), flush=True)
     gm.close()
-    if pg is not None:
-        pg.destroy_process_group()
+    del gm
+    torch.cuda.empty_cache()
+    return line
 
 
 def time_oracle_slots(shape, wl):
@@ -636,9 +829,16 @@ def graph_time(torch, launches, reps: int = 5):
 
 def run_sweep(args):
     import torch
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+    print(json.dumps(measure_sweep(args)), flush=True)
+
+
+def measure_sweep(args, clocks: bool = True) -> dict:
+    """The per-kernel sweep (--workload sweep); returns its record."""
+    import contextlib
+    import torch
     import memory_bound_decode_dequant_gb300 as mie
 
-    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
     peak, peak_kind = measured_peaks()
     gen = torch.Generator(device="cuda").manual_seed(synth.SWEEP_SEED)
     total, least = args.sweep_bytes, args.sweep_min
@@ -646,7 +846,8 @@ def run_sweep(args):
     out = {"metric": "per-kernel sweep (Llama-3.2-1B decode shapes)", "unit": "us / GB/s per launch",
            "peak_gbs": peak, "peak_kind": peak_kind, "gemv": [], "attention": [], "argmax": None,
            "method": "graph of back-to-back launches over > 1 GB of distinct inputs; median of 5 replays"}
-    with Clocks(int(os.environ.get("LOCAL_RANK", 0))) as clk:
+    clk = Clocks(int(os.environ.get("LOCAL_RANK", 0))) if clocks else None
+    with clk or contextlib.nullcontext():
         for name, M, K in synth.SWEEP_GEMV:
             if not any(want(f"gemv:{name}:{f}") for f in ("bf16", "i8", "q4_0")):
                 continue
@@ -709,8 +910,11 @@ def run_sweep(args):
             wsa = torch.empty(mie.mie_argmax_workspace_bytes(V), dtype=torch.uint8, device="cuda")
             dt = graph_time(torch, [(lambda st, v=v: mie.mie_argmax(v, am, wsa, stream=st)) for v in vs])
             out["argmax"] = {"n": V, "us": dt * 1e6, "gbs": V * 4 / dt / 1e9, "launches": n}
-    out["clocks"] = clk.summary()
-    print(json.dumps(out), flush=True)
+            del vs
+            torch.cuda.empty_cache()
+    if clk:
+        out["clocks"] = clk.summary()
+    return out
 
 
 def main():
