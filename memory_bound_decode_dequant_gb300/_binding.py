@@ -460,9 +460,13 @@ class Model:
         writes, and every wait gives up after wait_polls rounds (phase < 0 restores)."""
         _check(lib().mie_debug_stall(self.h, int(phase), int(wait_polls)), "mie_debug_stall")
 
-    def set_trace(self, enable: bool = True):
+    STAGE_TRACE, STAGE_POINTS = 1024, 4
+
+    def set_trace(self, enable: bool = True, stages: bool = False):
         """Records the persistent step's timeline into a device tensor
-        [n_phases, n_ctas, 5] of int64 nanoseconds (returned), or switches it off."""
+        [n_phases, n_ctas, 5] of int64 nanoseconds (returned), or switches it off.  With
+        stages=True the tensor also carries the per-stage stamps and (phases, stages)
+        views of it are returned: stages [n_ctas, 1024, 4]."""
         torch = _torch()
         npz, nct = I(0), I(0)
         if not enable:
@@ -470,10 +474,15 @@ class Model:
             self._trace = None
             return None
         _check(lib().mie_set_trace(self.h, None, 0, ctypes.byref(npz), ctypes.byref(nct)), "mie_set_trace")
-        buf = torch.zeros((npz.value, nct.value, 5), dtype=torch.int64, device="cuda")
-        _check(lib().mie_set_trace(self.h, buf.data_ptr(), buf.numel() * 8, None, None), "mie_set_trace")
-        self._trace = buf
-        return buf
+        n_ph = npz.value * nct.value * 5
+        n_st = nct.value * self.STAGE_TRACE * self.STAGE_POINTS if stages else 0
+        flat = torch.zeros(n_ph + n_st, dtype=torch.int64, device="cuda")
+        _check(lib().mie_set_trace(self.h, flat.data_ptr(), flat.numel() * 8, None, None), "mie_set_trace")
+        self._trace = flat
+        ph = flat[:n_ph].view(npz.value, nct.value, 5)
+        if not stages:
+            return ph
+        return ph, flat[n_ph:].view(nct.value, self.STAGE_TRACE, self.STAGE_POINTS)
 
 
 # ------------------------------------------------ the context and pool calls by C name

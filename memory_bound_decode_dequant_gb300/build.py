@@ -20,6 +20,12 @@ STAMP = os.path.join(BUILD_DIR, "libmie.so.stamp")
 SOURCES = ["gemv.cu", "gemv_slots.cu", "attn.cu", "step.cu", "quant.cu", "model.cu", "probe.cu", "pool.cpp"]
 HEADERS = ["common.cuh", "internal.h", "device.cuh", "attn_core.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+# MIE_STAGE_TRACE=1 builds the instrumented library whose persistent step also stamps
+# every ring stage (mie_set_trace); its objects live in their own build folder.
+DEFINES = ["-DMIE_STAGE_TRACE"] if os.environ.get("MIE_STAGE_TRACE") == "1" else []
+if DEFINES:
+    BUILD_DIR = BUILD_DIR + "-stage-trace"
+    STAMP = os.path.join(BUILD_DIR, "libmie.so.stamp")
 
 
 def nvcc() -> str:
@@ -48,7 +54,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
         objs.append(obj)
         if force or _stale(obj, [sp] + header_paths):
             cmd = [cc, *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
-                   "-I", os.path.join(ROOT, "include"), "-c", sp, "-o", obj + ".tmp"]
+                   "-I", os.path.join(ROOT, "include"), *DEFINES, "-c", sp, "-o", obj + ".tmp"]
             if src.endswith(".cu"):
                 cmd[1:1] = ["-Xptxas", "-v"] if verbose else []
             jobs.append((cmd, obj))

@@ -23,13 +23,14 @@ __host__ __device__ inline int attn_nsplit(int nblk, int max_splits, int per_spl
   return s < 1 ? 1 : s;
 }
 
-// Tagged variant: polls the group's queries into sm.q and, when has_pos, the current
-// token's k and v of KV head g into sm.kn / sm.vn, all in one batch of round trips.
+// Tagged variant: polls the G queries from query head h0 on into sm.q and, when
+// has_pos, the current token's k and v of KV head g into sm.kn / sm.vn, all in one
+// batch of round trips.
 template <int G, int HD, int NT, class Sync, class SM>
-__device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, SM &sm, uint32_t tag, const int *abort,
-                              long limit) {
+__device__ bool tagged_inputs(const AttnArgs &a, int h0, int g, bool has_pos, SM &sm, uint32_t tag,
+                              const int *abort, long limit) {
   constexpr int NQ = G * HD / 2, NK = HD / 2;
-  const uint64_t *qs = a.qkv_t + (int64_t)(g * G) * HD;
+  const uint64_t *qs = a.qkv_t + (int64_t)h0 * HD;
   const uint64_t *ks = a.qkv_t + (int64_t)(a.Hq + g) * HD;
   const uint64_t *vs = a.qkv_t + (int64_t)(a.Hq + a.Hkv + g) * HD;
   const int n = NQ + (has_pos ? 2 * NK : 0);
@@ -49,9 +50,10 @@ __device__ bool tagged_inputs(const AttnArgs &a, int g, bool has_pos, SM &sm, ui
   return Sync::all(ok);
 }
 
-// After a split of KV head g wrote its partial (m, l, o) to the workspace: the last
-// split of the head to arrive (atomic counter, no waiting) merges all nsplit partials
-// into the output and resets the counter.  `last` is a shared-memory flag.
+// After a split of unit g (a KV head with its G query heads, or with G = 1 a single
+// query head) wrote its partial (m, l, o) to the workspace: the last split of the unit
+// to arrive (atomic counter, no waiting) merges all nsplit partials into the outputs of
+// query heads g*G .. g*G+G-1 and resets the counter.  `last` is a shared-memory flag.
 template <int G, int HD, int NT, class Sync, bool Tagged>
 __device__ void attn_merge_splits(const AttnArgs &a, int g, int nsplit, unsigned &last, uint32_t tag) {
   constexpr int PART = G * (2 + HD);

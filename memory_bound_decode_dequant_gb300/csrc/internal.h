@@ -117,9 +117,14 @@ struct PersistArgs {
   uint32_t slot_bytes = 0, slot_sc_bytes = 0;
   int *err = nullptr;
   unsigned long long *trace = nullptr;  // [n_phases][grid][kTracePoints] globaltimer ns, or null
+  unsigned long long *stage_trace = nullptr;  // [grid][kStageTrace][kStagePoints], or null
   long wait_polls = kWaitPolls;         // rounds after which a bounded wait of the step gives up
 };
 constexpr int kTracePoints = 5;  // phase entry, inputs arrived, input staged, stages consumed, outputs written
+// Optional per-stage stamps after the phase stamps: [grid][kStageTrace][kStagePoints] =
+// copy issued (producer), consumer warp 0 starts waiting for it, the wait returns, warp
+// 0 done with the stage; the first kStageTrace ring stages of each CTA.
+constexpr int kStageTrace = 1024, kStagePoints = 4;
 struct PersistPlan {
   const void *kernel = nullptr;
   int grid = 0, threads = 0, n_slots = 0;

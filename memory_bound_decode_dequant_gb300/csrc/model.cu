@@ -233,7 +233,10 @@ extern "C" mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **
   ctx->rope_cos = (float *)ctx->dalloc(sizeof(float) * (size_t)c.max_pos * (c.head_dim / 2));
   ctx->rope_sin = (float *)ctx->dalloc(sizeof(float) * (size_t)c.max_pos * (c.head_dim / 2));
   ctx->attn_splits = attn_splits_for(c.n_kv_heads, c.max_pos, c.block_size);
-  ctx->attn_ws_bytes = attn_workspace_bytes(c.n_heads, c.n_kv_heads, c.head_dim, ctx->attn_splits);
+  // per layer: split counters of the attention units (query heads or KV heads), then the
+  // split partials (m, l, o) of every query head
+  ctx->attn_ws_bytes = attn_counter_bytes(c.n_heads) +
+                       (size_t)c.n_heads * ctx->attn_splits * (2 + c.head_dim) * sizeof(float);
   const size_t aws_total = ctx->attn_ws_bytes * c.n_layers * S;
   uint8_t *ws = (uint8_t *)ctx->dalloc(aws_total);
   ctx->tagged_words = tagged_layer_words(c) * c.n_layers;
@@ -607,7 +610,7 @@ static void build_phases(mie_ctx *ctx, std::vector<Phase> &out) {
     t.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
     t.out = ctx->att;
     t.ws_count = reinterpret_cast<unsigned *>(ws);
-    t.ws_part = reinterpret_cast<float *>(ws + attn_counter_bytes(c.n_kv_heads));
+    t.ws_part = reinterpret_cast<float *>(ws + attn_counter_bytes(c.n_heads));
     t.n_splits = ctx->attn_splits;
     t.err = ctx->err;
     t.qkv_t = t_qkv;
@@ -692,7 +695,9 @@ static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
     pa.slot_sc_bytes = ctx->plan.slot_sc_bytes;
     pa.err = ctx->err;
     const size_t need = sizeof(unsigned long long) * ctx->phases.size() * ctx->plan.grid * kTracePoints;
+    const size_t need_st = sizeof(unsigned long long) * ctx->plan.grid * kStageTrace * kStagePoints;
     pa.trace = (ctx->trace && ctx->trace_bytes >= need) ? ctx->trace : nullptr;
+    pa.stage_trace = (pa.trace && ctx->trace_bytes >= need + need_st) ? ctx->trace + need / 8 : nullptr;
     pa.wait_polls = ctx->wait_polls;
     if ((s = persist_launch(ctx->plan, pa, st)) != MIE_OK) return s;
     *launches = 1;

@@ -58,6 +58,25 @@ __device__ __forceinline__ void stamp(unsigned long long *trace, int phase, int 
   if (trace && threadIdx.x == 0) trace[((size_t)phase * gridDim.x + blockIdx.x) * kTracePoints + point] = globaltimer();
 }
 
+// Optional per-stage stamps (the producer lane, or consumer thread 0), compiled only into
+// an instrumented build (MIE_STAGE_TRACE defined): in the stage loops they would cost
+// registers that the Q4_0 kernels do not have.
+#ifdef MIE_STAGE_TRACE
+__shared__ unsigned long long *s_stage_trace;
+__device__ __forceinline__ void stage_stamp(int s, int point) {
+  unsigned long long *tr = *reinterpret_cast<unsigned long long *volatile *>(&s_stage_trace);
+  if (tr && s < kStageTrace) tr[((size_t)blockIdx.x * kStageTrace + s) * kStagePoints + point] = globaltimer();
+}
+#define STAGE_STAMP(cond, s, point) \
+  do {                              \
+    if (cond) stage_stamp(s, point); \
+  } while (0)
+#else
+#define STAGE_STAMP(cond, s, point) \
+  do {                              \
+  } while (0)
+#endif
+
 // Values fixed for the whole step, read once per launch: the launch's tag, the token
 // and position, the block ids of the context (when it has at most kStepMaxBlocks
 // blocks) and the RoPE angles of the position.  Later phases read them from shared
@@ -262,11 +281,13 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   bool ok = true;
   for (int st = 0; st < rr.n_stages; ++st, ++s_global) {
     const int slot = s_global % ring.nst, k = s_global / ring.nst;
+    STAGE_STAMP(tid == 0, s_global, 1);
     if (ok && !mbar_wait_or_abort(&ring.full[slot], k & 1, pa.wait_polls, pa.abort)) {
       ok = false;
       atomicExch(pa.abort, 1);
       latch_error(pa.err, ERR_TIMEOUT);
     }
+    STAGE_STAMP(tid == 0, s_global, 2);
     const int r = rr.row0 + st * rr.RPS + ri * RPW;  // this warp's first row of the stage
     if (ok && has_slice && r < rr.row1) {
       const int nr = min(RPW, rr.row1 - r);
@@ -284,6 +305,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     }
     __syncwarp();
     if (lane == 0 && ok) mbar_arrive(&ring.empty[slot]);
+    STAGE_STAMP(tid == 0, s_global, 3);
   }
   if (!ConsSync::all(ok)) return false;
   stamp(pa.trace, pidx, 3);
@@ -397,9 +419,21 @@ __host__ __device__ inline int attn_stage_blocks(uint32_t slot_bytes, int bs, in
   return cap < lim ? cap : lim;
 }
 
-template <int G, int HD>
-__device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, int ctx, const Ring &ring,
-                               int &s_global, ChunkSmem<G, HD> &sm, const StepConst &sc, const PersistArgs &pa) {
+// Attention items.  While the context needs few splits, one item per (query head,
+// split) spreads the work over Hq * nsplit CTAs (each reads its KV head's K/V for
+// itself; the group's other query heads read the same bytes, mostly from L2); longer
+// contexts take one item per (KV head, split), whose CTA serves the group's G query
+// heads from one read.  The producer walks the items in the same order.
+__host__ __device__ inline bool attn_items_per_query_head(int Hq, int Hkv, int nsplit, int grid) {
+  return Hq > Hkv && Hq * nsplit <= grid;
+}
+
+// One item: unit u of GI query heads from query head h0 on, KV head g, split sp.
+template <int GI, int HD>
+__device__ bool attn_ring_item(const AttnArgs &at, int u, int g, int h0, int sp, int nsplit, int ctx,
+                               const Ring &ring, int &s_global, ChunkSmem<GI, HD> &sm, const StepConst &sc,
+                               const PersistArgs &pa) {
+  constexpr int G = GI;
   constexpr int NO = (G * HD + kPCT - 1) / kPCT;  // outputs per thread
   static_assert(2 * HD <= kPCT, "one thread per element of the current token's k and v");
   const int tid = threadIdx.x, lane = tid & 31;
@@ -413,18 +447,20 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
     sm.m[tid] = -INFINITY;
     sm.l[tid] = 0.f;
   }
-  if (!tagged_inputs<G, HD, kPCT, ConsSync>(at, g, has_pos, sm, sc.tag, pa.abort, pa.wait_polls)) return false;
+  if (!tagged_inputs<G, HD, kPCT, ConsSync>(at, h0, g, has_pos, sm, sc.tag, pa.abort, pa.wait_polls)) return false;
   float o[NO];
 #pragma unroll
   for (int j = 0; j < NO; ++j) o[j] = 0.f;
   bool ok = true;
   for (int cb = b0; cb < b1; cb += cap, ++s_global) {
     const int slot = s_global % ring.nst, k = s_global / ring.nst;
+    STAGE_STAMP(tid == 0, s_global, 1);
     if (ok && !mbar_wait_or_abort(&ring.full[slot], k & 1, pa.wait_polls, pa.abort)) {
       ok = false;
       atomicExch(pa.abort, 1);
       latch_error(pa.err, ERR_TIMEOUT);
     }
+    STAGE_STAMP(tid == 0, s_global, 2);
     const uint32_t kbase = smem_u32(ring.w) + (uint32_t)slot * ring.slot_bytes;
     const uint32_t vbase = kbase + (uint32_t)(cap * kb);
     const int t0 = cb * at.bs, ntok = min(min(cb + cap, b1) * at.bs, t_end) - t0;
@@ -441,6 +477,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
     fence_proxy_async_smem();  // the patch above was a generic write into a bulk-copy slot
     __syncwarp();
     if (lane == 0 && ok) mbar_arrive(&ring.empty[slot]);  // only a slot whose copy landed
+    STAGE_STAMP(tid == 0, s_global, 3);
     ConsSync::sync();  // the next stage rewrites sm.s
   }
   if (!ConsSync::all(ok)) return false;
@@ -450,13 +487,13 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
       const int i = tid + j * kPCT;
       if (i < G * HD) {
         const float L = sm.l[i / HD];
-        st_tagged(at.out_t + (int64_t)(g * G) * HD + i, (L > 0.f) ? o[j] / L : 0.f, sc.tag);
+        st_tagged(at.out_t + (int64_t)h0 * HD + i, (L > 0.f) ? o[j] / L : 0.f, sc.tag);
       }
     }
     ConsSync::sync();  // the scratch is reused by the next item
     return true;
   }
-  float *part = at.ws_part + ((int64_t)g * at.n_splits + sp) * (G * (2 + HD));
+  float *part = at.ws_part + ((int64_t)u * at.n_splits + sp) * (G * (2 + HD));
 #pragma unroll
   for (int j = 0; j < NO; ++j) {
     const int i = tid + j * kPCT;
@@ -469,20 +506,25 @@ __device__ bool attn_ring_item(const AttnArgs &at, int g, int sp, int nsplit, in
       }
     }
   }
-  attn_merge_splits<G, HD, kPCT, ConsSync, true>(at, g, nsplit, sm.last, sc.tag);
+  attn_merge_splits<G, HD, kPCT, ConsSync, true>(at, u, nsplit, sm.last, sc.tag);
   return true;
 }
 
 template <int G, int HD>
 __device__ bool attn_phase(const AttnArgs &at, const Ring &ring, int &s_global, float *scratch, const StepConst &sc,
                            const PersistArgs &pa) {
-  auto &sm = *reinterpret_cast<ChunkSmem<G, HD> *>(scratch);
   const int ctx = sc.ctx;
   const int nblk = (ctx + at.bs - 1) / at.bs;
   const int nsplit = attn_nsplit(nblk, at.n_splits, ring_attn_blocks_per_split(at.bs));
-  const int items = at.Hkv * nsplit;
+  const bool per_q = attn_items_per_query_head(at.Hq, at.Hkv, nsplit, gridDim.x);
+  const int items = (per_q ? at.Hq : at.Hkv) * nsplit;
   for (int it = blockIdx.x; it < items; it += gridDim.x) {
-    if (!attn_ring_item<G, HD>(at, it / nsplit, it % nsplit, nsplit, ctx, ring, s_global, sm, sc, pa)) {
+    const int u = it / nsplit, sp = it % nsplit;
+    const bool ok = per_q ? attn_ring_item<1, HD>(at, u, u / G, u, sp, nsplit, ctx, ring, s_global,
+                                                  *reinterpret_cast<ChunkSmem<1, HD> *>(scratch), sc, pa)
+                          : attn_ring_item<G, HD>(at, u, u, u * G, sp, nsplit, ctx, ring, s_global,
+                                                  *reinterpret_cast<ChunkSmem<G, HD> *>(scratch), sc, pa);
+    if (!ok) {
       give_up(pa);
       return false;
     }
@@ -521,11 +563,12 @@ struct StageCursor {
   int64_t blk_bytes = 0;  // bytes between consecutive pool blocks
   const int32_t *bt = nullptr;
   int n_pool = 0, bs = 0, kb = 0, cap = 0, nblk = 0, nsplit = 1, items = 0, it = 0, cb = 0, b1 = 0;
+  int group = 1;  // query heads per item unit's KV head: G for per-query-head items, else 1
   int64_t hoff = 0;
 
-  __device__ bool next_item() {  // this CTA's next attention item with blocks
+  __device__ bool next_item() {  // this CTA's next attention item with blocks (consumers' order)
     for (it += gridDim.x; it < items; it += gridDim.x) {
-      const int g = it / nsplit, sp = it % nsplit;
+      const int g = (it / nsplit) / group, sp = it % nsplit;
       const int b0 = (int)((int64_t)sp * nblk / nsplit);
       b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
       if (b0 < b1) {
@@ -560,7 +603,9 @@ struct StageCursor {
     cap = attn_stage_blocks(a->slot_bytes, bs, HD);
     nblk = (ctx + bs - 1) / bs;
     nsplit = attn_nsplit(nblk, at.n_splits, ring_attn_blocks_per_split(bs));
-    items = at.Hkv * nsplit;
+    const bool per_q = attn_items_per_query_head(at.Hq, at.Hkv, nsplit, gridDim.x);
+    group = per_q ? at.Hq / at.Hkv : 1;
+    items = (per_q ? at.Hq : at.Hkv) * nsplit;
     it = (int)blockIdx.x - (int)gridDim.x;
     return next_item();
   }
@@ -635,6 +680,7 @@ __device__ void produce(const PersistArgs &a, const Ring &ring, const StepConst 
         bulk_load(dst + (size_t)(ld.cap + j) * ld.kb, ld.vbase + off, ld.kb, &ring.full[slot], pol);
       }
     }
+    STAGE_STAMP(true, s_global, 0);
     ++s_global;
     s_issued = s_global;
     ld.next();
@@ -676,6 +722,9 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
     s_issued = 0;
     s_prod_done = 0;
     s_sc_ready = 0;
+#ifdef MIE_STAGE_TRACE
+    s_stage_trace = a.stage_trace;
+#endif
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();

@@ -1,6 +1,6 @@
 """Timeline of the persistent decode step (mie_set_trace), summarised per phase kind.
 
-python -m memory_bound_decode_dequant_gb300.trace [--fmt bf16|i8|q4_0] [--ctx 128]
+python -m memory_bound_decode_dequant_gb300.trace [--fmt bf16|i8|q4_0] [--ctx 128] [--stages]
 
 Builds the Llama-3.2-1B-shape model from the seeded synthetic weights, fills the
 context with real decode steps, switches the step to the persistent kernel, records one
@@ -36,6 +36,40 @@ def summarise(t: np.ndarray, n_layers: int) -> dict:
     return out
 
 
+def summarise_stages(t: np.ndarray, st: np.ndarray, n_layers: int) -> dict:
+    """Per-stage stamps st [ctas, stages, 4] (issued, consumer starts waiting, wait
+    returns, consumer done; 0 = not recorded) against the phase stamps t, per phase kind
+    averaged over layers and CTAs, microseconds: `lead` = wait start - issue (how early
+    the copy was issued), `wait` = wait return - wait start (time the consumer stalled),
+    `stalled` = fraction of stages whose wait lasted over 0.1 us, `latency` = wait return
+    - issue over the stalled stages (an upper bound on issue -> landing), `math` = done -
+    wait return."""
+    names = ["qkv", "attn", "o", "gu", "down"] * n_layers + ["head"]
+    t = t.astype(np.float64)
+    st = st.astype(np.float64)
+    agg: dict = {}
+    for c in range(st.shape[0]):
+        rec = st[c]
+        ok = rec[:, 1] > 0
+        for p, name in enumerate(names):
+            lo, hi = t[p, c, 2], t[p, c, 3]
+            sel = ok & (rec[:, 1] >= lo) & (rec[:, 1] <= hi)
+            if not np.any(sel):
+                continue
+            r = rec[sel] / 1e3
+            wait = r[:, 2] - r[:, 1]
+            stalled = wait > 0.1
+            a = agg.setdefault(name, {"lead": [], "wait": [], "stalled": [], "latency": [], "math": [], "n": []})
+            a["lead"].append(float(np.mean(r[:, 1] - r[:, 0])))
+            a["wait"].append(float(np.mean(wait)))
+            a["stalled"].append(float(np.mean(stalled)))
+            if np.any(stalled):
+                a["latency"].append(float(np.mean(r[stalled, 2] - r[stalled, 0])))
+            a["math"].append(float(np.mean(r[:, 3] - r[:, 2])))
+            a["n"].append(int(sel.sum()))
+    return {k: {kk: round(float(np.mean(v)), 3) if v else None for kk, v in a.items()} for k, a in agg.items()}
+
+
 def main():
     import torch
 
@@ -45,8 +79,14 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--fmt", default="bf16", choices=["bf16", "i8", "q4_0"])
     ap.add_argument("--ctx", type=int, default=128)
+    ap.add_argument("--stages", action="store_true",
+                    help="also summarise the per-stage stamps (library built with MIE_STAGE_TRACE=1)")
+    ap.add_argument("--layers", type=int, default=0, help="truncate the model (0 = all layers)")
     args = ap.parse_args()
     shape = synth.llama32_1b(args.fmt)
+    if args.layers:
+        from dataclasses import replace
+        shape = replace(shape, n_layers=args.layers)
     torch.cuda.set_device(0)
     n_blocks = (args.ctx + 8) // shape.block_size + 2
     gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=n_blocks * shape.block_size)
@@ -58,11 +98,15 @@ def main():
     for pos, tok in enumerate(toks):
         gm.decode_step(int(tok), pos, bt, logits, am)
     gm.sync()
-    buf = gm.set_trace(True)
+    got = gm.set_trace(True, stages=args.stages)
+    buf, stb = got if args.stages else (got, None)
     gm.decode_step(int(toks[-1]), args.ctx, bt, logits, am)
     gm.decode_continue(3)
     gm.sync()
-    print(json.dumps(summarise(buf.cpu().numpy(), shape.n_layers)))
+    out = summarise(buf.cpu().numpy(), shape.n_layers)
+    if args.stages:
+        out["stages"] = summarise_stages(buf.cpu().numpy(), stb.cpu().numpy(), shape.n_layers)
+    print(json.dumps(out))
 
 
 if __name__ == "__main__":

@@ -42,3 +42,32 @@ def test_layers_are_averaged_per_kind():
     s = summarise(t, n_layers)
     assert s["qkv"]["stream_mean"] == pytest.approx(2.0)
     assert s["head"]["stream_mean"] == pytest.approx(3.0)
+
+
+def test_stage_summary_of_a_hand_built_trace():
+    """Two phases' worth of stages on one CTA: the stages are assigned to the phase whose
+    streaming window holds their wait start; lead, wait, stall fraction, latency and
+    math come out as built."""
+    from memory_bound_decode_dequant_gb300.trace import summarise_stages
+    n_layers = 1
+    t = np.zeros((6, 1, 5), np.int64)
+    t[0, 0] = [0, 0, 10_000, 20_000, 20_000]      # qkv streams in [10, 20] us
+    t[3, 0] = [0, 0, 30_000, 40_000, 40_000]      # gate/up streams in [30, 40] us
+    st = np.zeros((1, 1024, 4), np.int64)
+    # qkv: two stages issued 5 us early, landed before they were wanted (no stall)
+    st[0, 0] = [5_000, 10_000, 10_050, 10_550]
+    st[0, 1] = [6_000, 11_000, 11_050, 11_550]
+    # gate/up: one stage waited 2 us (issued 1 us before the wait began), one did not
+    st[0, 2] = [29_000, 30_000, 32_000, 32_500]
+    st[0, 3] = [29_500, 33_000, 33_000, 33_500]
+    s = summarise_stages(t, st, n_layers)
+    assert set(s) == {"qkv", "gu"}
+    assert s["qkv"]["n"] == 2 and s["gu"]["n"] == 2
+    assert s["qkv"]["lead"] == pytest.approx(5.0)
+    assert s["qkv"]["wait"] == pytest.approx(0.05)
+    assert s["qkv"]["stalled"] == pytest.approx(0.0) and s["qkv"]["latency"] is None
+    assert s["qkv"]["math"] == pytest.approx(0.5)
+    assert s["gu"]["lead"] == pytest.approx((1.0 + 3.5) / 2)
+    assert s["gu"]["wait"] == pytest.approx(1.0)
+    assert s["gu"]["stalled"] == pytest.approx(0.5)
+    assert s["gu"]["latency"] == pytest.approx(3.0)
