@@ -335,11 +335,13 @@ int mie_step_mode(const mie_ctx *ctx);
  * `cta` reached point 0 = phase entry, 1 = input words arrived, 2 = input vector
  * staged (normalised), 3 = ring stages consumed, 4 = outputs written.  In a library built
  * with MIE_STAGE_TRACE defined, and when the buffer is at least
- * n_ctas * 1024 * 4 * 8 bytes larger, those bytes receive per-stage stamps
+ * n_ctas * (1024 * 4 + n_phases * 8) * 8 bytes larger, those bytes receive per-stage stamps
  * [cta][stage][point] for the first 1024 ring stages of each CTA: 0 = the stage's copy
  * issued, 1 = consumer warp 0 starts waiting for it, 2 = that wait returns (the copy
- * had landed), 3 = warp 0 done with the stage.  *n_phases and *n_ctas (nullable)
- * receive the dimensions.  Takes effect at the next mie_decode_step. */
+ * had landed), 3 = warp 0 done with the stage; then 8 points per [phase][cta] inside
+ * the phase (GEMV: input polled, normalised, in registers; attention: inputs polled,
+ * first K/V stage landed, first chunk reduced, outputs written).  *n_phases and *n_ctas
+ * (nullable) receive the dimensions.  Takes effect at the next mie_decode_step. */
 mie_status mie_set_trace(mie_ctx *ctx, void *device_buffer, size_t bytes, int *n_phases, int *n_ctas);
 
 /* Synchronises the context's stream, then reads and clears its device error flags:

@@ -465,8 +465,9 @@ class Model:
     def set_trace(self, enable: bool = True, stages: bool = False):
         """Records the persistent step's timeline into a device tensor
         [n_phases, n_ctas, 5] of int64 nanoseconds (returned), or switches it off.  With
-        stages=True the tensor also carries the per-stage stamps and (phases, stages)
-        views of it are returned: stages [n_ctas, 1024, 4]."""
+        stages=True the tensor also carries the per-stage stamps and points inside each
+        phase (instrumented build), and (phases, stages, points) views of it are
+        returned: stages [n_ctas, 1024, 4], points [n_phases, n_ctas, 8]."""
         torch = _torch()
         npz, nct = I(0), I(0)
         if not enable:
@@ -476,13 +477,15 @@ class Model:
         _check(lib().mie_set_trace(self.h, None, 0, ctypes.byref(npz), ctypes.byref(nct)), "mie_set_trace")
         n_ph = npz.value * nct.value * 5
         n_st = nct.value * self.STAGE_TRACE * self.STAGE_POINTS if stages else 0
-        flat = torch.zeros(n_ph + n_st, dtype=torch.int64, device="cuda")
+        n_sub = npz.value * nct.value * 8 if stages else 0
+        flat = torch.zeros(n_ph + n_st + n_sub, dtype=torch.int64, device="cuda")
         _check(lib().mie_set_trace(self.h, flat.data_ptr(), flat.numel() * 8, None, None), "mie_set_trace")
         self._trace = flat
         ph = flat[:n_ph].view(npz.value, nct.value, 5)
         if not stages:
             return ph
-        return ph, flat[n_ph:].view(nct.value, self.STAGE_TRACE, self.STAGE_POINTS)
+        return (ph, flat[n_ph:n_ph + n_st].view(nct.value, self.STAGE_TRACE, self.STAGE_POINTS),
+                flat[n_ph + n_st:].view(npz.value, nct.value, 8))
 
 
 # ------------------------------------------------ the context and pool calls by C name

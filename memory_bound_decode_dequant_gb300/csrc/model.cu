@@ -695,7 +695,9 @@ static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
     pa.slot_sc_bytes = ctx->plan.slot_sc_bytes;
     pa.err = ctx->err;
     const size_t need = sizeof(unsigned long long) * ctx->phases.size() * ctx->plan.grid * kTracePoints;
-    const size_t need_st = sizeof(unsigned long long) * ctx->plan.grid * kStageTrace * kStagePoints;
+    // per-stage stamps, then (instrumented build) 8 points per phase and CTA
+    const size_t need_st = sizeof(unsigned long long) * ctx->plan.grid *
+                           ((size_t)kStageTrace * kStagePoints + ctx->phases.size() * 8);
     pa.trace = (ctx->trace && ctx->trace_bytes >= need) ? ctx->trace : nullptr;
     pa.stage_trace = (pa.trace && ctx->trace_bytes >= need + need_st) ? ctx->trace + need / 8 : nullptr;
     pa.wait_polls = ctx->wait_polls;

@@ -71,7 +71,20 @@ __device__ __forceinline__ void stage_stamp(int s, int point) {
   do {                              \
     if (cond) stage_stamp(s, point); \
   } while (0)
+// Points inside a phase, after the stage stamps: [n_phases][grid][8] (thread 0).
+__shared__ int s_cur_phase;
+__device__ __forceinline__ void sub_stamp(int point) {
+  unsigned long long *tr = *reinterpret_cast<unsigned long long *volatile *>(&s_stage_trace);
+  if (tr && threadIdx.x == 0) {
+    tr += (size_t)gridDim.x * kStageTrace * kStagePoints;
+    tr[((size_t)*reinterpret_cast<volatile int *>(&s_cur_phase) * gridDim.x + blockIdx.x) * 8 + point] = globaltimer();
+  }
+}
+#define SUB_STAMP(point) sub_stamp(point)
 #else
+#define SUB_STAMP(point) \
+  do {                   \
+  } while (0)
 #define STAGE_STAMP(cond, s, point) \
   do {                              \
   } while (0)
@@ -245,6 +258,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     }, ph.pro == PRO_NORM ? n_in : 0, &sq);
     if (ph.pro != PRO_EMBED_NORM)
       for (int k = K + tid; k < Kp; k += kPCT) xs[xs_at(k)] = 0.f;
+    SUB_STAMP(0);
     if (ph.pro != PRO_PLAIN) {  // the warps' sums of squares ride on the poll's barrier
       sq = warp_sum(sq);
       if (lane == 0) ps.red[warp] = sq;
@@ -255,6 +269,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
     }
     stamp(pa.trace, pidx, 1);
     normalize_staged<kPCT, ConsSync>(a, ph.pro, xs, K, ps.red, one_batch ? g0 : nullptr, 0.f, true);
+    SUB_STAMP(1);
     ConsSync::sync();
   }
   stamp(pa.trace, pidx, 2);
@@ -274,6 +289,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
       for (int i = 0; i < EPC / 2; ++i) xr[c * (EPC / 2) + i] = make_float2(0.f, 0.f);
     }
   }
+  SUB_STAMP(2);
 
   // stream this CTA's stages of the phase; a wait that gives up stops the math, and a
   // warp hands a slot back only after it saw the slot's copy land, so after a failure
@@ -448,6 +464,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int u, int g, int h0, int sp,
     sm.l[tid] = 0.f;
   }
   if (!tagged_inputs<G, HD, kPCT, ConsSync>(at, h0, g, has_pos, sm, sc.tag, pa.abort, pa.wait_polls)) return false;
+  SUB_STAMP(3);
   float o[NO];
 #pragma unroll
   for (int j = 0; j < NO; ++j) o[j] = 0.f;
@@ -461,6 +478,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int u, int g, int h0, int sp,
       latch_error(pa.err, ERR_TIMEOUT);
     }
     STAGE_STAMP(tid == 0, s_global, 2);
+    if (cb == b0) SUB_STAMP(4);
     const uint32_t kbase = smem_u32(ring.w) + (uint32_t)slot * ring.slot_bytes;
     const uint32_t vbase = kbase + (uint32_t)(cap * kb);
     const int t0 = cb * at.bs, ntok = min(min(cb + cap, b1) * at.bs, t_end) - t0;
@@ -473,6 +491,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int u, int g, int h0, int sp,
         ConsSync::sync();
       }
       chunk_passes<G, HD, kPCT, ConsSync>(kbase, vbase, ntok, at.scale, sm, o);
+      if (cb == b0) SUB_STAMP(5);
     }
     fence_proxy_async_smem();  // the patch above was a generic write into a bulk-copy slot
     __syncwarp();
@@ -490,6 +509,7 @@ __device__ bool attn_ring_item(const AttnArgs &at, int u, int g, int h0, int sp,
         st_tagged(at.out_t + (int64_t)h0 * HD + i, (L > 0.f) ? o[j] / L : 0.f, sc.tag);
       }
     }
+    SUB_STAMP(6);
     ConsSync::sync();  // the scratch is reused by the next item
     return true;
   }
@@ -796,6 +816,9 @@ __global__ void __launch_bounds__(kPThreads, 1) persistent_step(const PersistArg
     const uint32_t next_word =
         (p + 2 < a.n_phases && tid < kPhWords) ? __ldcg(ph_words + (size_t)(p + 2) * kPhWords + tid) : 0u;
     const Phase &ph = s_ph[p & 1];
+#ifdef MIE_STAGE_TRACE
+    if (tid == 0) s_cur_phase = p;
+#endif
     stamp(a.trace, p, 0);
     if (ph.kind == PH_GEMV) {
       // one inlined copy per distinct format: the kernel's code is kept small so that the

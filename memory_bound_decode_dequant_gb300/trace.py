@@ -70,6 +70,24 @@ def summarise_stages(t: np.ndarray, st: np.ndarray, n_layers: int) -> dict:
     return {k: {kk: round(float(np.mean(v)), 3) if v else None for kk, v in a.items()} for k, a in agg.items()}
 
 
+def summarise_points(t: np.ndarray, pts: np.ndarray, n_layers: int) -> dict:
+    """Points inside each phase (instrumented build), per phase kind, mean over layers
+    and CTAs of microseconds since the phase's entry stamp: GEMV phases 0 = input poll
+    returned, 1 = RMSNorm done, 2 = input in registers; attention items 3 = inputs
+    polled, 4 = first K/V stage landed, 5 = first chunk reduced, 6 = outputs written
+    (single-split items).  Points a CTA did not reach are left out."""
+    names = ["qkv", "attn", "o", "gu", "down"] * n_layers + ["head"]
+    out: dict = {}
+    for p, name in enumerate(names):
+        e = t[p, :, 0].astype(np.float64)
+        for k in range(7):
+            v = pts[p, :, k].astype(np.float64)
+            ok = v > 0
+            if np.any(ok):
+                out.setdefault(name, {}).setdefault(k, []).append(float(np.mean(v[ok] - e[ok]) / 1e3))
+    return {n: {str(k): round(float(np.mean(v)), 3) for k, v in d.items()} for n, d in out.items()}
+
+
 def main():
     import torch
 
@@ -82,6 +100,7 @@ def main():
     ap.add_argument("--stages", action="store_true",
                     help="also summarise the per-stage stamps (library built with MIE_STAGE_TRACE=1)")
     ap.add_argument("--layers", type=int, default=0, help="truncate the model (0 = all layers)")
+    ap.add_argument("--save", default="", help="with --stages: also save the raw stamps (.npz)")
     args = ap.parse_args()
     shape = synth.llama32_1b(args.fmt)
     if args.layers:
@@ -99,13 +118,16 @@ def main():
         gm.decode_step(int(tok), pos, bt, logits, am)
     gm.sync()
     got = gm.set_trace(True, stages=args.stages)
-    buf, stb = got if args.stages else (got, None)
+    buf, stb, sub = got if args.stages else (got, None, None)
     gm.decode_step(int(toks[-1]), args.ctx, bt, logits, am)
     gm.decode_continue(3)
     gm.sync()
     out = summarise(buf.cpu().numpy(), shape.n_layers)
     if args.stages:
         out["stages"] = summarise_stages(buf.cpu().numpy(), stb.cpu().numpy(), shape.n_layers)
+        out["points"] = summarise_points(buf.cpu().numpy(), sub.cpu().numpy(), shape.n_layers)
+        if args.save:
+            np.savez_compressed(args.save, phases=buf.cpu().numpy(), stages=stb.cpu().numpy(), points=sub.cpu().numpy())
     print(json.dumps(out))
 
 
