@@ -101,7 +101,9 @@ mie_status mie_q4_0_pack(const uint8_t *blocks, int M, int K, void *packed, void
  *                  y_i = s_i * sum_k q_ik x_k.
  *   mie_gemv_q4_0: packed: device GPU layout from mie_q4_0_pack; any K >= 1.
  * x: device [K] fp32; y: device [M] fp32 (must not alias x).  1 <= K <= 16384,
- * M >= 1.  MIE_E_SHAPE for other sizes or misaligned pointers.
+ * M >= 1.  MIE_E_SHAPE for other sizes or misaligned pointers.  x is fp32 only: the
+ * activations are fp32 ([INFER] design notes), and a bf16 activation vector widens to
+ * fp32 exactly, so an fp32 x carries it without loss.
  * Launched with programmatic dependent launch: when the previous kernel on the stream is
  * one of this library's GEMV, attention or argmax kernels, W starts streaming while that
  * kernel finishes; x is read and y written only after it has completed.  (None of those
@@ -247,7 +249,10 @@ typedef struct mie_config {
   int max_pos;     /* positions 0 .. max_pos-1 are valid */
 } mie_config;
 
-/* Creates a context on the current CUDA device: device KV pool
+/* Creates a context on the current CUDA device ([RUST] "Try it": the engine is loaded
+ * once and hands out a session that owns its KV cache; [INFER] the table of where each
+ * piece lives: one engine object holds the KV cache, the decode step and its CUDA graph):
+ * device KV pool
  * [n_kv_blocks][n_layers][2][n_kv_heads][block_size][head_dim] bf16 (zeroed), RoPE
  * tables, activations, a host block pool of n_kv_blocks blocks.  stream: the stream
  * every step of this context runs on. */
@@ -255,7 +260,9 @@ mie_status mie_create(const mie_config *cfg, void *stream, mie_ctx **out);
 void mie_destroy(mie_ctx *ctx);
 
 /* Copies one weight from host memory into the context and repacks it for the
- * kernels.  name: "l<i>.qkv" [(Hq+2Hkv)*hd][d] (rows q heads, then k, then v),
+ * kernels ([RUST] "Keeping the benchmark fair": the engine quantises the weights itself
+ * when it loads them; [INFER] the table of pieces: weights are converted at load time
+ * and packed by the weight-only quantization kernels).  name: "l<i>.qkv" [(Hq+2Hkv)*hd][d] (rows q heads, then k, then v),
  * "l<i>.o" [d][Hq*hd], "l<i>.gate" [ffn][d], "l<i>.up" [ffn][d], "l<i>.down" [d][ffn],
  * "head" [vocab][d], "embed" [vocab][d] (untied only), "l<i>.attn_norm",
  * "l<i>.mlp_norm", "final_norm" [d] (fp32 gains; all default to 1).

@@ -24,7 +24,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, f"libmie_oracle.{platform.machine()}.so")
 _lib = None
 
-FMT = {"bf16": 0, "i8": 1, "q4_0": 2, "f32": 3}
+FMT = {"bf16": 0, "i8": 1, "q4_0": 2, "f32": 3, "q4_g64": 4, "q4_g128": 5}
+# weights per f16 scale of the 4-bit formats
+Q4_GROUP = {"q4_0": 32, "q4_g64": 64, "q4_g128": 128}
 P = ctypes.c_void_p
 
 
@@ -70,6 +72,9 @@ def lib():
         "or_f16_to_f32_n": (None, [P, i64, P]),
         "or_q4_0_quantize": (None, [P, i, i, P]),
         "or_q4_0_dequantize": (None, [P, i, i, P]),
+        "or_q4_group": (i, [i]),
+        "or_q4_quantize": (None, [P, i, i, i, P]),
+        "or_q4_dequantize": (None, [P, i, i, i, P]),
         "or_i8_quantize": (None, [P, i, i, P, P]),
         "or_i8_dequantize": (None, [P, P, i, i, P]),
         "or_gemv": (None, [i, P, P, P, i, i, P]),
@@ -176,6 +181,25 @@ def q4_0_dequantize(wq, K: int) -> np.ndarray:
     return out
 
 
+def q4_quantize(w, group: int) -> np.ndarray:
+    """fp32 [M, K] -> canonical 4-bit groups [M, ceil(K/group), 2 + group/2] bytes
+    (group 32 is Q4_0)."""
+    w = _c(w, np.float32)
+    M, K = w.shape
+    ng = (K + group - 1) // group
+    out = np.empty((M, ng, 2 + group // 2), np.uint8)
+    lib().or_q4_quantize(_p(w), M, K, group, _p(out))
+    return out
+
+
+def q4_dequantize(wq, K: int, group: int) -> np.ndarray:
+    wq = _c(wq, np.uint8)
+    M = wq.shape[0]
+    out = np.empty((M, K), np.float32)
+    lib().or_q4_dequantize(_p(wq), M, K, group, _p(out))
+    return out
+
+
 def i8_quantize(w):
     w = _c(w, np.float32)
     M, K = w.shape
@@ -209,8 +233,8 @@ class Mat:
         if fmt == "i8":
             q, s = i8_quantize(w)
             return Mat(fmt, q, M, K, s)
-        if fmt == "q4_0":
-            return Mat(fmt, q4_0_quantize(w), M, K)
+        if fmt in Q4_GROUP:
+            return Mat(fmt, q4_quantize(w, Q4_GROUP[fmt]), M, K)
         if fmt == "f32":
             return Mat(fmt, w, M, K)
         raise ValueError(fmt)
@@ -220,8 +244,8 @@ class Mat:
             return from_bf16(self.data).reshape(self.rows, self.cols)
         if self.fmt == "i8":
             return i8_dequantize(self.data, self.scale)
-        if self.fmt == "q4_0":
-            return q4_0_dequantize(self.data, self.cols)
+        if self.fmt in Q4_GROUP:
+            return q4_dequantize(self.data, self.cols, Q4_GROUP[self.fmt])
         return self.data.reshape(self.rows, self.cols).copy()
 
 

@@ -135,68 +135,83 @@ void or_f16_to_f32_n(const uint16_t *x, int64_t n, float *out) {
 
 /* ------------------------------------------------------------------ quantisers */
 
-enum { OR_BF16 = 0, OR_I8 = 1, OR_Q4_0 = 2, OR_F32 = 3 };
-#define Q4_BLOCK 32
-#define Q4_BYTES 18 /* f16 scale (little-endian) + 16 bytes of nibbles */
+enum { OR_BF16 = 0, OR_I8 = 1, OR_Q4_0 = 2, OR_F32 = 3, OR_Q4_G64 = 4, OR_Q4_G128 = 5 };
 
-/* Q4_0 ([RUST] "Lesson 1" and "Is the 4-bit model still good?"; [INFER] design notes,
- * weight-only quantization): blocks of 32 weights, one 2-byte scale, 4-bit values
- * stored as w + 8 in 0..15.  The scale is the block's signed extreme (the element
- * whose magnitude is largest) over -8: that element's code is then exactly -8, the
- * end of the 4-bit range that has no positive twin.
+/* Weights per scale of the 4-bit formats (0 for the others). */
+int or_q4_group(int fmt) {
+  return fmt == OR_Q4_0 ? 32 : fmt == OR_Q4_G64 ? 64 : fmt == OR_Q4_G128 ? 128 : 0;
+}
+
+/* 4-bit groups ([RUST] "Lesson 1" and "Is the 4-bit model still good?"; [INFER] design
+ * notes, weight-only quantization: int4 with one 2-byte scale per group of weights,
+ * 4-bit values stored as w + 8 in 0..15; the scale is the group's signed extreme (the
+ * element whose magnitude is largest) over -8, so that element's code is exactly -8, the
+ * end of the 4-bit range that has no positive twin; the [INFER] page's int4 uses groups
+ * of 32 like Q4_0, started from groups of 128 and also measured groups of 64).
  * READING: first such element on ties; d = m / -8 in fp32 (exact); stored h = f16(d)
  * rounded to nearest even; codes use the stored scale: id = 1/h (0 when h == 0),
  * q = clamp(floor(w*id + 8.5), 0, 15) with the product and the sum each rounded in
- * fp32.  Byte j of the 16 holds element j in its low nibble and element j+16 in its
- * high nibble (the low/high pairing of [RUST] "Lesson 6").  A row whose length is not
- * a multiple of 32 is zero-padded to the next block; zeros code to 8 = exactly 0.
- * Output: rows of ceil(K/32) blocks of 18 bytes, [M][nb][18]. */
-void or_q4_0_quantize(const float *w, int M, int K, uint8_t *out) {
-  const int nb = (K + Q4_BLOCK - 1) / Q4_BLOCK;
+ * fp32.  Every 32 consecutive codes of a group form one 16-byte sub-block whose byte j
+ * holds code j in its low nibble and code j+16 in its high nibble (the low/high pairing
+ * of [RUST] "Lesson 6"); a group is stored as its f16 scale (little-endian) followed by
+ * its GS/32 sub-blocks: 2 + GS/2 bytes, 18 for GS = 32 (Q4_0).  A row whose length is
+ * not a multiple of GS is zero-padded to the next group; zeros code to 8 = exactly 0.
+ * Output: rows of ceil(K/GS) groups, [M][ng][2 + GS/2]. */
+void or_q4_quantize(const float *w, int M, int K, int GS, uint8_t *out) {
+  const int ng = (K + GS - 1) / GS, gbytes = 2 + GS / 2;
 #pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1) /* independent rows */
   for (int r = 0; r < M; ++r) {
-    for (int b = 0; b < nb; ++b) {
-      float v[Q4_BLOCK];
-      for (int j = 0; j < Q4_BLOCK; ++j) {
-        const int k = b * Q4_BLOCK + j;
+    for (int b = 0; b < ng; ++b) {
+      float v[128];
+      for (int j = 0; j < GS; ++j) {
+        const int k = b * GS + j;
         v[j] = (k < K) ? w[(int64_t)r * K + k] : 0.0f;
       }
       float amax = 0.0f, m = 0.0f;
-      for (int j = 0; j < Q4_BLOCK; ++j)
+      for (int j = 0; j < GS; ++j)
         if (fabsf(v[j]) > amax) { amax = fabsf(v[j]); m = v[j]; }
       const float d = m / -8.0f;
       const uint16_t h = or_f32_to_f16(d);
       const float hd = or_f16_to_f32(h);
       const float id = (hd != 0.0f) ? 1.0f / hd : 0.0f;
-      int q[Q4_BLOCK];
-      for (int j = 0; j < Q4_BLOCK; ++j) {
+      int q[128];
+      for (int j = 0; j < GS; ++j) {
         float t = v[j] * id;
         t = t + 8.5f;
         int c = (int)floorf(t);
         q[j] = c < 0 ? 0 : (c > 15 ? 15 : c);
       }
-      uint8_t *blk = out + ((int64_t)r * nb + b) * Q4_BYTES;
-      blk[0] = (uint8_t)(h & 0xFF);
-      blk[1] = (uint8_t)(h >> 8);
-      for (int j = 0; j < 16; ++j) blk[2 + j] = (uint8_t)(q[j] | (q[j + 16] << 4));
+      uint8_t *grp = out + ((int64_t)r * ng + b) * gbytes;
+      grp[0] = (uint8_t)(h & 0xFF);
+      grp[1] = (uint8_t)(h >> 8);
+      for (int sb = 0; sb < GS / 32; ++sb)
+        for (int j = 0; j < 16; ++j)
+          grp[2 + sb * 16 + j] = (uint8_t)(q[sb * 32 + j] | (q[sb * 32 + j + 16] << 4));
     }
   }
 }
 
-/* Element k of row r of a canonical Q4_0 matrix: h * (q - 8). */
-static float q4_0_at(const uint8_t *wq, int nb, int r, int k) {
-  const uint8_t *blk = wq + ((int64_t)r * nb + k / Q4_BLOCK) * Q4_BYTES;
-  const float h = or_f16_to_f32((uint16_t)(blk[0] | (blk[1] << 8)));
-  const int j = k % Q4_BLOCK;
-  const int q = (j < 16) ? (blk[2 + j] & 0x0F) : (blk[2 + j - 16] >> 4);
+/* Q4_0: the 4-bit format with groups of 32. */
+void or_q4_0_quantize(const float *w, int M, int K, uint8_t *out) { or_q4_quantize(w, M, K, 32, out); }
+
+/* Element k of row r of a canonical 4-bit matrix with groups of GS (ng per row):
+ * h * (q - 8). */
+static float q4_at(const uint8_t *wq, int GS, int ng, int r, int k) {
+  const uint8_t *grp = wq + ((int64_t)r * ng + k / GS) * (2 + GS / 2);
+  const float h = or_f16_to_f32((uint16_t)(grp[0] | (grp[1] << 8)));
+  const int j = k % GS, sb = j / 32, i = j % 32;
+  const uint8_t byte = grp[2 + sb * 16 + (i % 16)];
+  const int q = (i < 16) ? (byte & 0x0F) : (byte >> 4);
   return h * (float)(q - 8); /* exact: |q-8| <= 8 */
 }
 
-void or_q4_0_dequantize(const uint8_t *wq, int M, int K, float *w) {
-  const int nb = (K + Q4_BLOCK - 1) / Q4_BLOCK;
+void or_q4_dequantize(const uint8_t *wq, int M, int K, int GS, float *w) {
+  const int ng = (K + GS - 1) / GS;
   for (int r = 0; r < M; ++r)
-    for (int k = 0; k < K; ++k) w[(int64_t)r * K + k] = q4_0_at(wq, nb, r, k);
+    for (int k = 0; k < K; ++k) w[(int64_t)r * K + k] = q4_at(wq, GS, ng, r, k);
 }
+
+void or_q4_0_dequantize(const uint8_t *wq, int M, int K, float *w) { or_q4_dequantize(wq, M, K, 32, w); }
 
 /* int8 with one scale per row ([INFER] design notes, weight-only quantization: each
  * output row carries its own scale).
@@ -233,10 +248,10 @@ void or_i8_dequantize(const int8_t *q, const float *s, int M, int K, float *w) {
  * Each output is the fp64 sum of (dequantised weight) * x over the row, rounded once
  * to fp32.  The int8 scale multiplies the row sum (y_i = s_i * sum_k q_ik x_k), which
  * equals sum_k (s_i q_ik) x_k exactly in real arithmetic.
- * Layouts: bf16 [M][K] uint16; i8 [M][K] int8 + s[M]; Q4_0 canonical [M][nb][18];
- * f32 [M][K]. */
+ * Layouts: bf16 [M][K] uint16; i8 [M][K] int8 + s[M]; 4-bit canonical groups
+ * [M][ng][2 + GS/2] (Q4_0: [M][nb][18]); f32 [M][K]. */
 void or_gemv(int fmt, const void *W, const float *s, const float *x, int M, int K, float *y) {
-  const int nb = (K + Q4_BLOCK - 1) / Q4_BLOCK;
+  const int GS = or_q4_group(fmt), ng = GS ? (K + GS - 1) / GS : 0;
 #pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1 && M >= 64) /* independent rows */
   for (int r = 0; r < M; ++r) {
     double acc = 0.0;
@@ -247,8 +262,8 @@ void or_gemv(int fmt, const void *W, const float *s, const float *x, int M, int 
       const int8_t *row = (const int8_t *)W + (int64_t)r * K;
       for (int k = 0; k < K; ++k) acc += (double)row[k] * (double)x[k];
       acc *= (double)s[r];
-    } else if (fmt == OR_Q4_0) {
-      for (int k = 0; k < K; ++k) acc += (double)q4_0_at((const uint8_t *)W, nb, r, k) * (double)x[k];
+    } else if (GS) {
+      for (int k = 0; k < K; ++k) acc += (double)q4_at((const uint8_t *)W, GS, ng, r, k) * (double)x[k];
     } else {
       const float *row = (const float *)W + (int64_t)r * K;
       for (int k = 0; k < K; ++k) acc += (double)row[k] * (double)x[k];
@@ -261,12 +276,12 @@ void or_gemv(int fmt, const void *W, const float *s, const float *x, int M, int 
  * [INFER] data-flow figure: the token's embedding row starts the fp32 residual). */
 void or_embed_row(int fmt, const void *E, const float *s, int V, int d, int token, float *x) {
   (void)V;
-  const int nb = (d + Q4_BLOCK - 1) / Q4_BLOCK;
+  const int GS = or_q4_group(fmt), ng = GS ? (d + GS - 1) / GS : 0;
   for (int k = 0; k < d; ++k) {
     float v;
     if (fmt == OR_BF16) v = or_bf16_to_f32(((const uint16_t *)E)[(int64_t)token * d + k]);
     else if (fmt == OR_I8) v = (float)((double)s[token] * (double)((const int8_t *)E)[(int64_t)token * d + k]);
-    else if (fmt == OR_Q4_0) v = q4_0_at((const uint8_t *)E, nb, token, k);
+    else if (GS) v = q4_at((const uint8_t *)E, GS, ng, token, k);
     else v = ((const float *)E)[(int64_t)token * d + k];
     x[k] = v;
   }

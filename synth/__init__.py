@@ -105,7 +105,8 @@ def permutation(seed: int, n: int) -> np.ndarray:
 class ModelShape:
     """One Llama-style decoder shape plus its storage formats.
 
-    wfmt / head_fmt are "bf16", "i8" (one fp32 scale per row) or "q4_0" (blocks of 32
+    wfmt / head_fmt are "bf16", "i8" (one fp32 scale per row), "q4_0" (blocks of 32
+    four-bit values with one f16 scale) or "q4_g64" / "q4_g128" (groups of 64 / 128
     four-bit values with one f16 scale).  act_bf16 rounds each GEMV input vector to
     bf16 (the TinyLlama workload's "bf16 activations"); the residual stream stays fp32.
     """
@@ -189,14 +190,19 @@ class ModelShape:
         return self.weight_bytes() + self.kv_bytes_per_token() * mean_ctx
 
 
+# weights per f16 scale of the 4-bit formats
+Q4_GROUP = {"q4_0": 32, "q4_g64": 64, "q4_g128": 128}
+
+
 def matrix_bytes(fmt: str, m: int, k: int) -> int:
     """Algorithmic bytes of an m x k matrix in a storage format (unpadded)."""
     if fmt == "bf16":
         return m * k * 2
     if fmt == "i8":
         return m * k + 4 * m
-    if fmt == "q4_0":
-        return m * ((k + 31) // 32) * 18
+    if fmt in Q4_GROUP:  # one f16 scale and group/2 bytes of 4-bit codes per group
+        g = Q4_GROUP[fmt]
+        return m * ((k + g - 1) // g) * (2 + g // 2)
     if fmt == "f32":
         return m * k * 4
     raise ValueError(fmt)
@@ -219,10 +225,13 @@ LLAMA32_1B = ModelShape("llama-3.2-1b", 2, n_layers=16, d_model=2048, n_heads=32
                         rope_theta=500000.0, wfmt="bf16", head_fmt="bf16")
 
 
-def llama32_1b(fmt: str) -> ModelShape:
-    """The Llama-3.2-1B shape in one of its three storage variants:
-    "bf16", "i8" (per-row scale) or "q4_0" (layers Q4_0, tied head/embedding int8)."""
-    head = {"bf16": "bf16", "i8": "i8", "q4_0": "i8"}[fmt]
+def llama32_1b(fmt: str, head: str | None = None) -> ModelShape:
+    """The Llama-3.2-1B shape in one of its storage variants: "bf16", "i8" (per-row
+    scale), or a 4-bit format ("q4_0", "q4_g64", "q4_g128") for the layers with the
+    tied head/embedding in int8 unless `head` names another format (e.g. the same
+    4-bit format: the all-int4 variants)."""
+    if head is None:
+        head = {"bf16": "bf16", "i8": "i8"}.get(fmt, "i8")
     return replace(LLAMA32_1B, wfmt=fmt, head_fmt=head)
 
 

@@ -154,6 +154,103 @@ def test_q4_0_bias_identity():
     assert lhs == rhs
 
 
+# ----------------------------------------------------------------- 4-bit groups of 64 / 128
+
+def _groups(q, GS):
+    """(scale bits [M, ng], codes [M, ng, GS]) of canonical 4-bit groups: each group is
+    its f16 scale then GS/32 sub-blocks of 16 bytes in the Q4_0 nibble order."""
+    h = q[..., 0].astype(np.uint16) | (q[..., 1].astype(np.uint16) << 8)
+    sub = q[..., 2:].reshape(q.shape[0], q.shape[1], GS // 32, 16)
+    codes = np.concatenate([sub & 0x0F, sub >> 4], axis=-1).reshape(q.shape[0], q.shape[1], GS)
+    return h, codes
+
+
+@pytest.mark.parametrize("shape", [(1, 1), (3, 40), (4, 256), (5, 688), (2, 2048)])
+def test_q4_group_32_is_q4_0(orc, shape):
+    """Groups of 32 are Q4_0 byte for byte, ragged rows included."""
+    M, K = shape
+    w = synth.normal(40 + K, M * K, std=0.02).reshape(M, K)
+    assert np.array_equal(orc.q4_quantize(w, 32), orc.q4_0_quantize(w))
+    assert np.array_equal(orc.q4_dequantize(orc.q4_quantize(w, 32), K, 32),
+                          orc.q4_0_dequantize(orc.q4_0_quantize(w), K))
+
+
+@pytest.mark.parametrize("GS", [64, 128])
+def test_q4_group_one_scale_per_group(orc, GS):
+    """One f16 scale per group of GS: the group's largest-magnitude element codes to 0
+    (value -8h), the stored scale is f16(m / -8), every element of the group dequantises
+    to h * (code - 8) with that one scale, and quantising the dequantised matrix gives
+    the same bytes (idempotence)."""
+    M, K = 96, 512
+    w = synth.normal(41 + GS, M * K, std=0.02).reshape(M, K)
+    q = orc.q4_quantize(w, GS)
+    assert q.shape == (M, K // GS, 2 + GS // 2)
+    h, codes = _groups(q, GS)
+    wg = w.reshape(M, K // GS, GS)
+    idx = np.abs(wg).argmax(axis=-1)
+    assert np.all(np.take_along_axis(codes, idx[..., None], -1) == 0)
+    m = np.take_along_axis(wg, idx[..., None], -1)[..., 0]
+    assert np.array_equal(h, (m / -8).astype(np.float16).view(np.uint16))
+    hv = h.view(np.float16).astype(np.float32)
+    deq = orc.q4_dequantize(q, K, GS).reshape(M, K // GS, GS)
+    assert np.array_equal(deq, hv[..., None] * (codes.astype(np.float32) - 8))
+    assert np.array_equal(orc.q4_quantize(deq.reshape(M, K), GS), q)
+
+
+def test_q4_group_layout_hand_built(orc):
+    """A hand-built group of 128 with every code in every sub-block round-trips, and its
+    bytes are the scale then four 16-byte sub-blocks, byte j of sub-block b holding code
+    32b + j (low nibble) and code 32b + j + 16 (high nibble)."""
+    hv = np.float32(np.float16(0.0078125))  # 2^-7: exact in f16
+    base = np.array([0, 5, 1, 15, 2, 14, 3, 13, 4, 12, 6, 11, 7, 10, 9, 8], np.int64)
+    codes = np.concatenate([np.roll(base, b) if b % 2 == 0 else np.roll(base[::-1], b) for b in range(8)])
+    codes[0] = 0  # the group's extreme (-8h) comes first and is unique
+    codes[1:][codes[1:] == 0] = 1
+    w = (hv * (codes - 8)).astype(np.float32)[None, :]
+    q = orc.q4_quantize(w, 128)
+    assert q.shape == (1, 1, 66)
+    assert (int(q[0, 0, 0]) | (int(q[0, 0, 1]) << 8)) == int(np.float16(hv).view(np.uint16))
+    for b in range(4):
+        sub = codes[32 * b:32 * b + 32]
+        assert np.array_equal(q[0, 0, 2 + 16 * b:18 + 16 * b], (sub[:16] | (sub[16:] << 4)).astype(np.uint8))
+    assert np.array_equal(orc.q4_dequantize(q, 128, 128), w)
+
+
+@pytest.mark.parametrize("GS", [64, 128])
+def test_q4_group_ragged_tail_and_error_bound(orc, GS):
+    """A row whose length is not a multiple of GS is zero-padded (pads code to 8, the
+    real elements as if the zeros were there); every element lies within half a step of
+    its group's grid, up to the saturated top code and the f16 rounding of the scale."""
+    M, K = 7, 688
+    w = synth.normal(43 + GS, M * K, std=0.02).reshape(M, K)
+    q = orc.q4_quantize(w, GS)
+    ng = (K + GS - 1) // GS
+    assert q.shape == (M, ng, 2 + GS // 2)
+    h, codes = _groups(q, GS)
+    assert np.all(codes.reshape(M, ng * GS)[:, K:] == 8)
+    wp = np.zeros((M, ng * GS), np.float32)
+    wp[:, :K] = w
+    assert np.array_equal(orc.q4_quantize(wp, GS), q)
+    deq = orc.q4_dequantize(q, K, GS)
+    hv = np.abs(h.view(np.float16).astype(np.float64))
+    hv_el = np.repeat(hv, GS, axis=1)[:, :K]
+    c_el = codes.reshape(M, ng * GS)[:, :K]
+    wa = np.abs(w.astype(np.float64))
+    err = np.abs(w.astype(np.float64) - deq)
+    bound = np.maximum(hv_el * 0.5, np.where(c_el == 15, wa - 7 * hv_el, 0)) + hv_el * 8 * 2.0**-10 + 1e-12
+    assert np.all(err <= bound)
+
+
+@pytest.mark.parametrize("fmt", ["q4_g64", "q4_g128"])
+def test_q4_group_embedding_row_is_the_dequantised_row(orc, fmt):
+    """The embedding gather from a 4-bit table returns exactly the dequantised row."""
+    w = synth.normal(45, 9 * 300, std=0.02).reshape(9, 300)
+    mat = orc.Mat.quantize(fmt, w)
+    deq = mat.dequantize()
+    for t in (0, 4, 8):
+        assert np.array_equal(orc.embed_row(mat, t), deq[t])
+
+
 # ----------------------------------------------------------------- int8
 
 def test_i8_quantizer(orc):
@@ -175,7 +272,7 @@ def test_i8_quantizer(orc):
 
 # ----------------------------------------------------------------- GEMV
 
-@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "f32"])
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "q4_g64", "q4_g128", "f32"])
 @pytest.mark.parametrize("shape", [(1, 1), (1, 32), (7, 40), (33, 688), (5, 2048), (64, 31)])
 def test_gemv_brute_force(orc, fmt, shape):
     """The oracle GEMV equals the fp64 matrix-vector product of the dequantised
