@@ -47,7 +47,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--impl", default="mie", choices=["mie", "reference"])
-    ap.add_argument("--fmt", default="bf16", choices=["bf16", "i8", "q4_0"])
+    ap.add_argument("--fmt", default="bf16", choices=["bf16", "i8", "q4_0", "q4_g64", "q4_g128"],
+                    help="layer weights; 4-bit formats keep the tied head in int8 unless --head says otherwise")
+    ap.add_argument("--head", default=None, choices=["bf16", "i8", "q4_0", "q4_g64", "q4_g128"],
+                    help="format of the tied LM head / embedding (default: bf16 / i8 by --fmt)")
     ap.add_argument("--ctx", type=int, default=128)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=32)
@@ -537,11 +540,18 @@ def run_mie(args, shape):
     if rank == 0:
         if world == 1 and not args.quick:
             # the other workloads of the decode-step family, each recorded in this line
-            fmts = {"bf16": "i8 q4_0", "i8": "bf16 q4_0", "q4_0": "bf16 i8"}[args.fmt].split()
-            for f in fmts:
-                extras[f"contexts_{f}"] = guarded(lambda f=f: model_contexts(
-                    torch, synth.llama32_1b(f), CONTEXTS["llama-3.2-1b"], args.decode_steps, peak, read_peak,
-                    f"llama-3.2-1b {f} batch-1 decode"))
+            # the other storage variants of the same model (the infer page's decode table):
+            # int8, int4 g32 with an int8 head, int4 g32, int4 g128, int4 g128 with an int8 head
+            variants = [("i8", None), ("q4_0", None), ("q4_0", "q4_0"), ("q4_g128", "q4_g128"),
+                        ("q4_g128", "i8"), ("bf16", None)]
+            for f, h in variants:
+                sh = synth.llama32_1b(f, h)
+                if (sh.wfmt, sh.head_fmt) == (shape.wfmt, shape.head_fmt):
+                    continue
+                key = f"contexts_{f}" + (f"_head_{sh.head_fmt}" if h else "")
+                extras[key] = guarded(lambda sh=sh: model_contexts(
+                    torch, sh, CONTEXTS["llama-3.2-1b"], args.decode_steps, peak, read_peak,
+                    f"llama-3.2-1b {sh.wfmt} layers, {sh.head_fmt} head, batch-1 decode"))
             extras["tinyllama_q4_0"] = guarded(lambda: model_contexts(
                 torch, synth.TINYLLAMA, CONTEXTS["tinyllama-1.1b"], args.decode_steps, peak, read_peak,
                 "tinyllama-1.1b q4_0 (bf16 GEMV inputs) batch-1 decode"))
@@ -589,9 +599,11 @@ def run_mie(args, shape):
 
 def step_config(args, shape, world: int) -> dict:
     """The workload of the batch-1 line, the same dict in both arms."""
-    return {"workload": f"{shape.name} {args.fmt} batch-1 decode step"
+    return {"workload": f"{shape.name} {args.fmt}" + (f" ({shape.head_fmt} head)" if args.head else "")
+                        + " batch-1 decode step"
                         + (f" ({shape.n_layers} layers, profiling case)" if args.layers else ""),
-            "model": shape.name, "weights": args.fmt, "global_batch": world, "seq_len": args.ctx,
+            "model": shape.name, "weights": args.fmt, "head": shape.head_fmt, "global_batch": world,
+            "seq_len": args.ctx,
             "ctx_range": [args.ctx, args.ctx + args.warmup + args.steps],
             "parallelism": "replicas" if world > 1 else "single",
             "l2": "weights 2.47 GB per step >> 129 MB L2: inputs larger than L2",
@@ -924,7 +936,7 @@ def main():
         return
     if args.layers:
         from dataclasses import replace as _replace  # a truncated model for profiling captures
-        synth_shape = _replace(synth.llama32_1b(args.fmt), n_layers=args.layers)
+        synth_shape = _replace(synth.llama32_1b(args.fmt, args.head), n_layers=args.layers)
     else:
         synth_shape = None
     if args.workload == "slots":
@@ -933,7 +945,7 @@ def main():
         else:
             run_slots(args)
         return
-    shape = synth_shape or synth.llama32_1b(args.fmt)
+    shape = synth_shape or synth.llama32_1b(args.fmt, args.head)
     if args.kernel_only:
         import torch
         import memory_bound_decode_dequant_gb300 as mie

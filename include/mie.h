@@ -55,8 +55,10 @@ typedef enum mie_status {
 typedef enum mie_format {
   MIE_FMT_BF16 = 0,
   MIE_FMT_I8 = 1,
-  MIE_FMT_Q4_0 = 2,
-  MIE_FMT_F32 = 3
+  MIE_FMT_Q4_0 = 2,    /* 4-bit, one f16 scale per 32 weights */
+  MIE_FMT_F32 = 3,
+  MIE_FMT_Q4_G64 = 4,  /* 4-bit, one f16 scale per 64 weights */
+  MIE_FMT_Q4_G128 = 5  /* 4-bit, one f16 scale per 128 weights */
 } mie_format;
 
 /* Message for the last failure on the calling thread ("" if none). */
@@ -92,6 +94,26 @@ size_t mie_q4_0_packed_bytes(int M, int K);
 /* Canonical blocks (device) -> GPU layout (device, mie_q4_0_packed_bytes(M, K) bytes). */
 mie_status mie_q4_0_pack(const uint8_t *blocks, int M, int K, void *packed, void *stream);
 
+/* 4-bit weights with one f16 scale per `group` (32, 64 or 128) weights ([INFER] design
+ * notes, weight-only quantization: int4 per 32 weights as in Q4_0, groups of 128 as its
+ * starting point; its perplexity table also measures groups of 64).  The Q4_0 rule
+ * applied to groups of `group` weights: the group's signed extreme over -8 is the scale,
+ * codes q = clamp(floor(w * (1/h) + 8.5), 0, 15).  A row is zero-padded to whole groups.
+ * Canonical layout [M][ceil(K/group)][2 + group/2]: the f16 scale (little-endian), then
+ * group/32 sub-blocks of 16 bytes, byte j of sub-block b holding code 32b+j in its low
+ * nibble and code 32b+j+16 in its high nibble; group 32 is Q4_0.  MIE_E_ARG for another
+ * group size.  w: device [M][K] fp32; groups: device. */
+mie_status mie_quantize_q4(const float *w, int M, int K, int group, uint8_t *groups, void *stream);
+
+/* Size of the GPU layout: a nibble plane [M][ng*group/32][16], ng = ceil(K/group),
+ * followed at the next 256-byte boundary by a scale plane [M][ngp] of f16, ngp = ng
+ * rounded up to a multiple of 8.  0 for an unsupported group. */
+size_t mie_q4_packed_bytes(int M, int K, int group);
+
+/* Canonical groups (device) -> GPU layout (device, mie_q4_packed_bytes bytes, 256-byte
+ * aligned). */
+mie_status mie_q4_pack(const uint8_t *groups, int M, int K, int group, void *packed, void *stream);
+
 /* ============================================================================ GEMV */
 
 /* y = W x with fp32 accumulation ([INFER] per-kernel table, "gemv"; [RUST] "Lesson 1":
@@ -113,6 +135,10 @@ mie_status mie_gemv_bf16(const uint16_t *W, const float *x, float *y, int M, int
 mie_status mie_gemv_i8(const int8_t *W, const float *row_scale, const float *x, float *y, int M,
                        int K, void *stream);
 mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y, int M, int K, void *stream);
+/* The same GEMV over a 4-bit matrix with `group` weights per scale (GPU layout from
+ * mie_q4_pack); group 32 is mie_gemv_q4_0. */
+mie_status mie_gemv_q4(const void *packed, int group, const float *x, float *y, int M, int K,
+                       void *stream);
 
 /* ======================================================================= attention */
 
@@ -241,7 +267,7 @@ typedef struct mie_config {
   int act_bf16;    /* 1: round each GEMV input vector to bf16 (residual stays fp32) */
   float rms_eps;
   float rope_theta;
-  int wfmt;        /* format of the layer matrices (mie_format) */
+  int wfmt;        /* format of the layer matrices (mie_format: bf16, i8 or a 4-bit format) */
   int head_fmt;    /* format of the LM head (and of the embedding when tied) */
   int embed_fmt;   /* format of an untied embedding table */
   int n_kv_blocks; /* device KV pool size in blocks */
@@ -268,7 +294,8 @@ void mie_destroy(mie_ctx *ctx);
  * "l<i>.mlp_norm", "final_norm" [d] (fp32 gains; all default to 1).
  * fmt: MIE_FMT_F32 (fp32 [rows][cols]; quantised on the device into the context's
  * format for that tensor) or that format itself in canonical layout (bf16 [rows][cols];
- * i8 [rows][cols] with host_scale [rows]; Q4_0 blocks [rows][ceil(cols/32)][18]).
+ * i8 [rows][cols] with host_scale [rows]; 4-bit canonical groups, e.g. Q4_0 blocks
+ * [rows][ceil(cols/32)][18]).
  * bytes must equal the canonical size.  shape: {rows, cols} (gains: {d}). */
 mie_status mie_load_weights(mie_ctx *ctx, const char *name, int fmt, const void *host_data,
                             size_t bytes, const int64_t *shape, int ndim,

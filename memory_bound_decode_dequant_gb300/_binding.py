@@ -11,13 +11,15 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmie.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "mie.h")
 
-FMT = {"bf16": 0, "i8": 1, "q4_0": 2, "f32": 3}
+Q4_GROUP = {"q4_0": 32, "q4_g64": 64, "q4_g128": 128}  # weights per f16 scale
+FMT = {"bf16": 0, "i8": 1, "q4_0": 2, "f32": 3, "q4_g64": 4, "q4_g128": 5}
 STATUS = {0: "MIE_OK", 1: "MIE_E_ARG", 2: "MIE_E_SHAPE", 3: "MIE_E_OOM", 4: "MIE_E_CUDA",
           5: "MIE_E_TIMEOUT", 6: "MIE_E_STATE", 7: "MIE_E_DEVICE"}
 
 __all__ = ["lib", "MieError", "FMT", "LIB_PATH", "exported_names", "header_functions",
            "mie_convert_bf16", "mie_quantize_i8", "mie_quantize_q4_0", "mie_q4_0_pack",
            "mie_q4_0_packed_bytes", "mie_gemv_bf16", "mie_gemv_i8", "mie_gemv_q4_0",
+           "mie_quantize_q4", "mie_q4_packed_bytes", "mie_q4_pack", "mie_gemv_q4", "Q4_GROUP",
            "mie_paged_attn_decode", "mie_paged_attn_workspace_bytes", "mie_paged_attn_decode_noalloc",
            "mie_argmax",
            "mie_argmax_workspace_bytes", "mie_check", "mie_hbm_read_probe", "Pool", "Config", "Model",
@@ -50,9 +52,13 @@ _SIGS = {
     "mie_quantize_q4_0": (I, [P, I, I, P, P]),
     "mie_q4_0_packed_bytes": (SZ, [I, I]),
     "mie_q4_0_pack": (I, [P, I, I, P, P]),
+    "mie_quantize_q4": (I, [P, I, I, I, P, P]),
+    "mie_q4_packed_bytes": (SZ, [I, I, I]),
+    "mie_q4_pack": (I, [P, I, I, I, P, P]),
     "mie_gemv_bf16": (I, [P, P, P, I, I, P]),
     "mie_gemv_i8": (I, [P, P, P, P, I, I, P]),
     "mie_gemv_q4_0": (I, [P, P, P, I, I, P]),
+    "mie_gemv_q4": (I, [P, I, P, P, I, I, P]),
     "mie_paged_attn_workspace_bytes": (SZ, [I, I, I, I, I]),
     "mie_paged_attn_decode": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, F, P, P, SZ, P]),
     "mie_paged_attn_decode_noalloc": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, F, P, P]),
@@ -189,6 +195,36 @@ def mie_q4_0_pack(blocks, M: int, K: int, stream=None):
     _check(lib().mie_q4_0_pack(_dev(blocks, torch.uint8, "blocks"), M, K, out.data_ptr(), _stream(stream)),
            "mie_q4_0_pack")
     return out
+
+
+def mie_quantize_q4(w, group: int, stream=None):
+    """fp32 [M, K] device tensor -> canonical 4-bit groups [M, ceil(K/group), 2 + group/2]."""
+    torch = _torch()
+    M, K = w.shape
+    out = torch.empty((M, (K + group - 1) // group, 2 + group // 2), dtype=torch.uint8, device=w.device)
+    _check(lib().mie_quantize_q4(_dev(w, torch.float32, "w"), M, K, group, out.data_ptr(), _stream(stream)),
+           "mie_quantize_q4")
+    return out
+
+
+def mie_q4_packed_bytes(M: int, K: int, group: int) -> int:
+    return int(lib().mie_q4_packed_bytes(M, K, group))
+
+
+def mie_q4_pack(groups, M: int, K: int, group: int, stream=None):
+    torch = _torch()
+    out = torch.empty(mie_q4_packed_bytes(M, K, group), dtype=torch.uint8, device=groups.device)
+    _check(lib().mie_q4_pack(_dev(groups, torch.uint8, "groups"), M, K, group, out.data_ptr(), _stream(stream)),
+           "mie_q4_pack")
+    return out
+
+
+def mie_gemv_q4(packed, group: int, x, M: int, K: int, y=None, stream=None):
+    torch = _torch()
+    y = _y(y, M, packed.device)
+    _check(lib().mie_gemv_q4(_dev(packed, torch.uint8, "packed"), group, _dev(x, torch.float32, "x"),
+                             _dev(y, torch.float32, "y"), M, K, _stream(stream)), "mie_gemv_q4")
+    return y
 
 
 def _y(y, M, device):

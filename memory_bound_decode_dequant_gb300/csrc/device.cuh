@@ -30,7 +30,8 @@ __device__ __forceinline__ float embed_at(const DevMat &m, int row, int k) {
   } else {
     const uint8_t byte = m.w[(int64_t)row * m.row_bytes + (k >> 5) * 16 + (k & 15)];
     const int code = ((k & 31) < 16) ? (byte & 0xF) : (byte >> 4);
-    const float h = __half2float(reinterpret_cast<const __half *>(m.s)[(int64_t)row * m.s_stride + (k >> 5)]);
+    const float h =
+        __half2float(reinterpret_cast<const __half *>(m.s)[(int64_t)row * m.s_stride + (k >> (5 + m.gshift))]);
     return h * (float)(code - 8);
   }
 }
@@ -225,15 +226,16 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 // Dot products of this lane's part of the RPW consecutive weight rows of this warp,
 // staged in shared memory, with its input registers xr: row = shared address of the
 // first row's 2048-column slice (the others at row + i*row_bytes), sc = shared address
-// of its Q4_0 scales (the others at sc + i*s_bytes).  Every chunk and scale of all rows
-// is loaded before any math, so the loads cost one shared-memory latency.  Chunks at or
+// of its 4-bit scales (the others at sc + i*s_bytes; chunk j of the slice uses scale
+// j >> gshift).  Every chunk and scale of all rows is loaded before any math, so the
+// loads cost one shared-memory latency.  Chunks at or
 // past Kp are read from the slice start instead (always staged) and meet zero input
 // registers, so they add exact zeros.  nrows (<= RPW) rows are valid; the others read
 // the first row.
 template <int F>
 __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes, uint32_t sc, uint32_t s_bytes,
                                                int nrows, const float2 *xr, int e0, int Kp, int lane,
-                                               float (&sum)[FmtT<F>::RPW]) {
+                                               float (&sum)[FmtT<F>::RPW], int gshift = 0) {
   using T = FmtT<F>;
   constexpr int EPC = T::EPC, CPL = T::CPL, R = T::RPW, kChunkStride = 32 * EPC;
   uint4 w[R][CPL];
@@ -249,7 +251,8 @@ __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes,
     for (int i = 0; i < R; ++i) {
       const uint32_t sa = sc + (uint32_t)(i < nrows ? i : 0) * s_bytes;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) hb[i][c] = lds16(e0 + c * kChunkStride < Kp ? sa + (uint32_t)(c * 32 + lane) * 2 : sa);
+      for (int c = 0; c < CPL; ++c)
+        hb[i][c] = lds16(e0 + c * kChunkStride < Kp ? sa + (uint32_t)((c * 32 + lane) >> gshift) * 2 : sa);
     }
 #pragma unroll
     for (int i = 0; i < R; ++i) {

@@ -197,9 +197,10 @@ __global__ void __launch_bounds__(32 * (NW + 1), kMinBlocks<F>) gemv_kernel(cons
       const uint32_t rowa = smem_u32(ring) + (uint32_t)slot * stage_bytes + (uint32_t)(ri * RPW * m.row_bytes) +
                             (uint32_t)ks * kSliceBytes;
       const uint32_t sca = smem_u32(sring) + (uint32_t)slot * sc_bytes +
-                           (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice / 32)) * 2;
+                           (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice >> (5 + m.gshift))) * 2;
       float sum[RPW];
-      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, e0, Kp, lane, sum);
+      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, e0, Kp, lane, sum,
+                        m.gshift);
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
         const float v = warp_sum(sum[i]);
@@ -460,18 +461,28 @@ extern "C" mie_status mie_gemv_i8(const int8_t *W, const float *row_scale, const
   return gemv_entry(m, x, y, stream);
 }
 
-extern "C" size_t mie_q4_0_packed_bytes(int M, int K) {
-  if (M < 1 || K < 1) return 0;
-  const size_t nb = (size_t)(K + 31) / 32;
+// GPU layout of a 4-bit matrix with `group` weights per scale: rows padded to whole
+// groups, a nibble plane [M][kp/32][16], then at the next 256-byte boundary a scale plane
+// [M][s_stride] of f16.
+static bool q4_group_ok(int group) { return group == 32 || group == 64 || group == 128; }
+
+extern "C" size_t mie_q4_packed_bytes(int M, int K, int group) {
+  if (M < 1 || K < 1 || !q4_group_ok(group)) return 0;
+  const size_t ng = (size_t)(K + group - 1) / group, nb = ng * (group / 32);
   const size_t nib = ((size_t)M * nb * 16 + 255) & ~(size_t)255;
-  return nib + (size_t)M * q4_scale_stride((int)nb) * 2;
+  return nib + (size_t)M * q4_scale_stride((int)ng) * 2;
 }
 
-extern "C" mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y, int M, int K, void *stream) {
-  if (M < 1 || K < 1) return fail(MIE_E_SHAPE, "mie_gemv_q4_0: bad shape %d x %d", M, K);
-  const int nb = (K + 31) / 32;
+extern "C" size_t mie_q4_0_packed_bytes(int M, int K) { return mie_q4_packed_bytes(M, K, 32); }
+
+extern "C" mie_status mie_gemv_q4(const void *packed, int group, const float *x, float *y, int M, int K,
+                                  void *stream) {
+  if (M < 1 || K < 1) return fail(MIE_E_SHAPE, "mie_gemv_q4: bad shape %d x %d", M, K);
+  if (!q4_group_ok(group)) return fail(MIE_E_ARG, "mie_gemv_q4: group %d not 32, 64 or 128", group);
+  const int ng = (K + group - 1) / group, nb = ng * (group / 32);
   DevMat m;
   m.fmt = MIE_FMT_Q4_0;
+  m.gshift = q4_gshift(group);
   m.rows = M;
   m.cols = K;
   m.kp = nb * 32;
@@ -479,6 +490,10 @@ extern "C" mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y
   m.row_bytes = (int64_t)nb * 16;
   const size_t nib = ((size_t)M * nb * 16 + 255) & ~(size_t)255;
   m.s = reinterpret_cast<const uint8_t *>(packed) + nib;
-  m.s_stride = q4_scale_stride(nb);
+  m.s_stride = q4_scale_stride(ng);
   return gemv_entry(m, x, y, stream);
+}
+
+extern "C" mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y, int M, int K, void *stream) {
+  return mie_gemv_q4(packed, 32, x, y, M, K, stream);
 }

@@ -209,13 +209,15 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
         uint8_t *dst = smem + (size_t)slot * pl.stage_bytes;
         if constexpr (Q4) {
           const int nb = min(kSSlice, Kp - q * kSSlice) / 32;  // blocks of this slice
-          const uint32_t cb = (uint32_t)nb * 16, sb = (uint32_t)((nb + 7) / 8 * 8) * 2;  // scales: whole 16 B
+          const int ns = (nb + (1 << m.gshift) - 1) >> m.gshift;  // its scales (one per group)
+          const uint32_t cb = (uint32_t)nb * 16, sb = (uint32_t)((ns + 7) / 8 * 8) * 2;  // scales: whole 16 B
           mbar_expect_tx(&full_bar[slot], rows * (cb + sb));
           for (int j = 0; j < rows; ++j) {
             bulk_load(dst + (size_t)j * pl.pitch, m.w + (int64_t)(r0 + j) * m.row_bytes + (int64_t)q * (kSSlice / 32) * 16,
                       cb, &full_bar[slot], pol);
             bulk_load(dst + pl.sc_off + (size_t)j * 128,
-                      reinterpret_cast<const uint8_t *>(m.s) + ((int64_t)(r0 + j) * m.s_stride + q * (kSSlice / 32)) * 2,
+                      reinterpret_cast<const uint8_t *>(m.s) +
+                          ((int64_t)(r0 + j) * m.s_stride + q * (kSSlice >> (5 + m.gshift))) * 2,
                       sb, &full_bar[slot], pol);
           }
         } else {
@@ -463,8 +465,8 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
           const int b = warp + kSW * i;
           if (2 * b < nk) {
             const uint32_t w = lds32(nrow + b * 16);  // codes 4t.. (low nibbles) and 4t+16.. (high)
-            const float d0 = __half2float(__ushort_as_half((unsigned short)lds16(srow + b * 2)));
-            const float d1 = __half2float(__ushort_as_half((unsigned short)lds16(srow + 128 + b * 2)));
+            const float d0 = __half2float(__ushort_as_half((unsigned short)lds16(srow + (b >> m.gshift) * 2)));
+            const float d1 = __half2float(__ushort_as_half((unsigned short)lds16(srow + 128 + (b >> m.gshift) * 2)));
             float ct[4] = {0.f, 0.f, 0.f, 0.f};
             const uint32_t lb0 = q4_pair(w & 0xFu, (w >> 8) & 0xFu), lb1 = q4_pair((w >> 16) & 0xFu, (w >> 24) & 0xFu);
             const uint32_t hb0 = q4_pair((w >> 4) & 0xFu, (w >> 12) & 0xFu);

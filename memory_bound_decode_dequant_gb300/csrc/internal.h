@@ -14,10 +14,19 @@ struct DevMat {
   int rows = 0, cols = 0;  // logical shape
   int kp = 0;              // padded columns (multiple of the format's chunk)
   const uint8_t *w = nullptr;  // bf16/i8 row-major [rows][kp]; Q4_0 nibble plane [rows][kp/32][16]
-  const void *s = nullptr;     // i8: float[rows]; Q4_0: half[rows][s_stride]
+  const void *s = nullptr;     // i8: float[rows]; 4-bit: half[rows][s_stride]
   int64_t row_bytes = 0;
-  int s_stride = 0;            // Q4_0: scales per row, kp/32 rounded up to a multiple of 8
+  int s_stride = 0;            // 4-bit: scales per row, kp/group rounded up to a multiple of 8
+  int gshift = 0;              // 4-bit: log2(weights per scale / 32): 0, 1, 2 for groups of 32, 64, 128
+  int pub_fmt = -1;            // the public format (mie_format) the matrix was created with
 };
+
+// Weights per f16 scale of a public 4-bit format (0 for the others); the kernels run all
+// of them as MIE_FMT_Q4_0 with DevMat::gshift selecting the group.
+inline int q4_group(int fmt) {
+  return fmt == MIE_FMT_Q4_0 ? 32 : fmt == MIE_FMT_Q4_G64 ? 64 : fmt == MIE_FMT_Q4_G128 ? 128 : 0;
+}
+inline int q4_gshift(int group) { return group == 128 ? 2 : group == 64 ? 1 : 0; }
 
 // Q4_0 scale-plane row stride: whole 16-byte groups, so a bulk copy of whole rows of
 // scales starts and ends on 16-byte boundaries.
@@ -142,9 +151,9 @@ mie_status launch_gemv_slots(int pro, int epi, const GemvArgs &a, cudaStream_t s
 // Load-time kernels.
 mie_status launch_convert_bf16(const float *w, int64_t n, uint16_t *out, cudaStream_t st);
 mie_status launch_quantize_i8(const float *w, int M, int K, int8_t *q, float *s, cudaStream_t st);
-mie_status launch_quantize_q4_0(const float *w, int M, int K, uint8_t *blocks, cudaStream_t st);
-mie_status launch_q4_0_pack(const uint8_t *blocks, int M, int K, uint8_t *nib, __half *scales, int s_stride,
-                            const int *row_map, cudaStream_t st);
+mie_status launch_quantize_q4(const float *w, int M, int K, int group, uint8_t *groups, cudaStream_t st);
+mie_status launch_q4_pack(const uint8_t *groups, int M, int K, int group, uint8_t *nib, __half *scales, int s_stride,
+                          const int *row_map, cudaStream_t st);
 mie_status launch_row_permute(const uint8_t *src, uint8_t *dst, int64_t row_bytes, int M,
                               const int *row_map, cudaStream_t st);
 mie_status launch_pad_rows(const uint8_t *src, int64_t src_row_bytes, uint8_t *dst,

@@ -182,9 +182,10 @@ static mie_status check_config(const mie_config &c) {
     return fail(MIE_E_SHAPE, "mie_create: a GEMV input is longer than %d", kmax);
   if (c.max_slots < 1 || c.max_slots > kMaxSlots) return fail(MIE_E_SHAPE, "mie_create: max_slots %d", c.max_slots);
   if (c.n_kv_blocks < 1 || c.max_pos < 1) return fail(MIE_E_ARG, "mie_create: n_kv_blocks / max_pos");
+  auto stored = [](int f) { return f == MIE_FMT_BF16 || f == MIE_FMT_I8 || q4_group(f) != 0; };
   for (int f : {c.wfmt, c.head_fmt})
-    if (f != MIE_FMT_BF16 && f != MIE_FMT_I8 && f != MIE_FMT_Q4_0) return fail(MIE_E_ARG, "mie_create: format %d", f);
-  if (!c.tied && c.embed_fmt != MIE_FMT_BF16 && c.embed_fmt != MIE_FMT_I8 && c.embed_fmt != MIE_FMT_Q4_0)
+    if (!stored(f)) return fail(MIE_E_ARG, "mie_create: format %d", f);
+  if (!c.tied && !stored(c.embed_fmt))
     return fail(MIE_E_ARG, "mie_create: embed format %d", c.embed_fmt);
   return MIE_OK;
 }
@@ -310,7 +311,8 @@ namespace {
 
 // Allocates a matrix in its GPU layout (zero-filled so padding reads as zeros).
 mie_status alloc_mat(mie_ctx *ctx, DevMat &m, int fmt, int rows, int cols) {
-  m.fmt = fmt;
+  m.pub_fmt = fmt;
+  m.fmt = q4_group(fmt) ? MIE_FMT_Q4_0 : fmt;  // every 4-bit group size runs as Q4_0 with a group shift
   m.rows = rows;
   m.cols = cols;
   size_t wbytes = 0, sbytes = 0;
@@ -322,9 +324,11 @@ mie_status alloc_mat(mie_ctx *ctx, DevMat &m, int fmt, int rows, int cols) {
     m.row_bytes = m.kp;
     sbytes = sizeof(float) * rows;
   } else {
-    m.kp = pad_to(cols, 32);
+    const int group = q4_group(fmt);
+    m.gshift = q4_gshift(group);
+    m.kp = pad_to(cols, group);  // whole groups
     m.row_bytes = (int64_t)(m.kp / 32) * 16;
-    m.s_stride = q4_scale_stride(m.kp / 32);
+    m.s_stride = q4_scale_stride(m.kp / group);
     sbytes = sizeof(__half) * (size_t)rows * m.s_stride;
   }
   wbytes = (size_t)rows * m.row_bytes;
@@ -356,14 +360,14 @@ struct Temp {
 mie_status fill_mat_body(mie_ctx *ctx, Temp &tmp, DevMat &m, int fmt, const void *host, size_t bytes,
                          const float *host_scale, int rows, int cols, const std::vector<int> &map) {
   cudaStream_t st = ctx->stream;
-  const int nb = (cols + 31) / 32;
+  const int group = q4_group(m.pub_fmt), ng = group ? (cols + group - 1) / group : 0;
   size_t expect = 0;
   if (fmt == MIE_FMT_F32) expect = (size_t)rows * cols * 4;
   else if (fmt == MIE_FMT_BF16) expect = (size_t)rows * cols * 2;
   else if (fmt == MIE_FMT_I8) expect = (size_t)rows * cols;
-  else if (fmt == MIE_FMT_Q4_0) expect = (size_t)rows * nb * 18;
-  if (fmt != MIE_FMT_F32 && fmt != m.fmt)
-    return fail(MIE_E_ARG, "weights: host format %d is neither F32 nor the tensor's format %d", fmt, m.fmt);
+  else if (q4_group(fmt)) expect = (size_t)rows * ng * (2 + group / 2);
+  if (fmt != MIE_FMT_F32 && fmt != m.pub_fmt)
+    return fail(MIE_E_ARG, "weights: host format %d is neither F32 nor the tensor's format %d", fmt, m.pub_fmt);
   if (bytes != expect) return fail(MIE_E_ARG, "weights: %zu bytes given, %zu expected", bytes, expect);
   if (fmt == MIE_FMT_I8 && !host_scale) return fail(MIE_E_ARG, "weights: int8 data without row scales");
   void *src = tmp.get(bytes);
@@ -403,16 +407,16 @@ mie_status fill_mat_body(mie_ctx *ctx, Temp &tmp, DevMat &m, int fmt, const void
       return s;
     return launch_pad_rows((const uint8_t *)canon_scale, 4, (uint8_t *)const_cast<void *>(m.s), 4, rows, dmap, st);
   }
-  // Q4_0
+  // 4-bit groups
   if (fmt == MIE_FMT_F32) {
-    uint8_t *b = (uint8_t *)tmp.get((size_t)rows * nb * 18);
+    uint8_t *b = (uint8_t *)tmp.get((size_t)rows * ng * (2 + group / 2));
     if (!b) return fail(MIE_E_OOM, "weights: staging allocation");
-    if ((s = launch_quantize_q4_0((const float *)src, rows, cols, b, st)) != MIE_OK) return s;
+    if ((s = launch_quantize_q4((const float *)src, rows, cols, group, b, st)) != MIE_OK) return s;
     canon = b;
   }
-  if (m.kp / 32 != nb) return fail(MIE_E_SHAPE, "weights: Q4_0 block count mismatch");
-  return launch_q4_0_pack((const uint8_t *)canon, rows, cols, const_cast<uint8_t *>(m.w),
-                          (__half *)const_cast<void *>(m.s), m.s_stride, dmap, st);
+  if (m.kp / group != ng) return fail(MIE_E_SHAPE, "weights: 4-bit group count mismatch");
+  return launch_q4_pack((const uint8_t *)canon, rows, cols, group, const_cast<uint8_t *>(m.w),
+                        (__half *)const_cast<void *>(m.s), m.s_stride, dmap, st);
 }
 
 mie_status fill_mat(mie_ctx *ctx, DevMat &m, int fmt, const void *host, size_t bytes, const float *host_scale, int rows,

@@ -310,9 +310,10 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
       const uint32_t rowa = smem_u32(ring.w) + (uint32_t)slot * ring.slot_bytes + (uint32_t)(ri * RPW * m.row_bytes) +
                             (uint32_t)ks * kSliceBytes;
       const uint32_t sca = smem_u32(ring.sc) + (uint32_t)slot * ring.slot_sc_bytes +
-                           (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice / 32)) * 2;
+                           (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice >> (5 + m.gshift))) * 2;
       float sum[RPW];
-      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, e0, Kp, lane, sum);
+      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, e0, Kp, lane, sum,
+                        m.gshift);
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
         const float v = warp_sum(sum[i]);

@@ -62,6 +62,37 @@ def test_quantizers_bit_exact(orc, shape):
     assert np.array_equal(b16.view(torch.int16).cpu().numpy().view(np.uint16), orc.to_bf16(w))
 
 
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("shape", [(1, 1), (3, 40), (64, 688), (257, 2048), (4096, 8192)])
+def test_q4_group_quantizer_bit_exact(orc, group, shape):
+    """4-bit groups of 64 / 128 (ragged rows zero-padded) quantise to the oracle's bytes."""
+    M, K = shape
+    w = synth.normal(1100 + M + K + group, M * K, std=0.02).reshape(M, K)
+    w[0, : min(K, group)] = 0.0  # a zero group
+    got = mie.mie_quantize_q4(torch.from_numpy(w).cuda(), group)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), orc.q4_quantize(w, group))
+
+
+@pytest.mark.parametrize("group", [64, 128])
+def test_q4_group_pack_layout(orc, group):
+    """The GPU layout holds the groups' 16-byte sub-blocks in row order and one scale per
+    group, the scale rows padded to a multiple of 8."""
+    M, K = 5, 300
+    w = synth.normal(78, M * K, std=0.02).reshape(M, K)
+    groups = orc.q4_quantize(w, group)
+    ng = groups.shape[1]
+    nb, ngp = ng * group // 32, (ng + 7) // 8 * 8
+    packed = mie.mie_q4_pack(torch.from_numpy(groups).cuda(), M, K, group).cpu().numpy()
+    assert packed.size == mie.mie_q4_packed_bytes(M, K, group)
+    nib = packed[: M * nb * 16].reshape(M, nb, 16)
+    off = ((M * nb * 16 + 255) // 256) * 256
+    sc = packed[off: off + M * ngp * 2].view(np.uint16).reshape(M, ngp)
+    assert np.array_equal(nib, groups[:, :, 2:].reshape(M, ng, group // 32, 16).reshape(M, nb, 16))
+    assert np.array_equal(sc[:, :ng], groups[:, :, 0].astype(np.uint16) | (groups[:, :, 1].astype(np.uint16) << 8))
+    assert np.all(sc[:, ng:] == 0)
+
+
 def test_q4_0_pack_layout(orc):
     """The GPU layout holds the canonical nibbles and scales, plane by plane."""
     M, K = 5, 70
@@ -90,8 +121,11 @@ def _gemv_both(orc, fmt, M, K, seed, rows=None):
     elif fmt == "i8":
         q, s = mie.mie_quantize_i8(wd)
         y = mie.mie_gemv_i8(q, s, xd)
-    else:
+    elif fmt == "q4_0":
         y = mie.mie_gemv_q4_0(mie.mie_q4_0_pack(mie.mie_quantize_q4_0(wd), M, K), xd, M, K)
+    else:
+        g = mie.Q4_GROUP[fmt]
+        y = mie.mie_gemv_q4(mie.mie_q4_pack(mie.mie_quantize_q4(wd, g), M, K, g), g, xd, M, K)
     del wd
     y = y.cpu().numpy()
     sel = np.arange(M) if rows is None else rows
@@ -99,7 +133,7 @@ def _gemv_both(orc, fmt, M, K, seed, rows=None):
     return y[sel], ref
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0"])
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "q4_g64", "q4_g128"])
 @pytest.mark.parametrize("shape", [(1, 32), (7, 48), (33, 688), (300, 2048), (1000, 8192), (77, 5632),
                                    (5, 16384), (2049, 256)])
 def test_gemv_small_and_ragged(orc, fmt, shape):
@@ -108,14 +142,14 @@ def test_gemv_small_and_ragged(orc, fmt, shape):
     gemv_close(y, ref)
 
 
-@pytest.mark.parametrize("fmt", ["q4_0"])
-@pytest.mark.parametrize("K", [1, 31, 33, 40, 100])
+@pytest.mark.parametrize("fmt", ["q4_0", "q4_g64", "q4_g128"])
+@pytest.mark.parametrize("K", [1, 31, 33, 40, 100, 129, 200])
 def test_gemv_q4_0_any_k(orc, fmt, K):
     y, ref = _gemv_both(orc, fmt, 9, K, 3000 + K)
     gemv_close(y, ref)
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0"])
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "q4_g128"])
 @pytest.mark.parametrize("name,M,K", synth.SWEEP_GEMV)
 def test_gemv_full_size_sampled_rows(orc, fmt, name, M, K):
     """Llama-3.2-1B decode shapes; the oracle checks 256 sampled rows plus the first and

@@ -106,13 +106,14 @@ def run_positions(orc, shape, layers, positions, mode=PERSISTENT, n_steps=2, per
     gm.close()
 
 
-@pytest.mark.parametrize("fmt,positions", [
-    ("bf16", (150, 600, 2100, 8250)),
-    ("i8", (150, 600, 2100)),
-    ("q4_0", (150, 600, 2100)),
+@pytest.mark.parametrize("fmt,head,positions", [
+    ("bf16", None, (150, 600, 2100, 8250)),
+    ("i8", None, (150, 600, 2100)),
+    ("q4_0", None, (150, 600, 2100)),
+    ("q4_g128", "q4_g128", (150, 2100)),
 ])
-def test_llama32_shape_long_context_persistent(orc, fmt, positions):
-    run_positions(orc, synth.llama32_1b(fmt), 2, positions)
+def test_llama32_shape_long_context_persistent(orc, fmt, head, positions):
+    run_positions(orc, synth.llama32_1b(fmt, head), 2, positions)
 
 
 def test_llama32_shape_long_context_chain(orc):

@@ -113,7 +113,7 @@ def run_slots(orc, shape, n_slots, max_slots, prompts, n_gen, compare_kv=True, n
     return gm
 
 
-@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0"])
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "q4_g64", "q4_g128"])
 def test_slots_match_single_slot_oracle(orc, fmt):
     shape = replace(synth.TINY, wfmt=fmt, head_fmt=fmt)
     run_slots(orc, shape, n_slots=4, max_slots=4, prompts=[40, 37, 21, 50], n_gen=6)

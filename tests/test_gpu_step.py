@@ -101,6 +101,14 @@ def test_llama32_shape_two_layers(orc, fmt, mode):
 
 
 @pytest.mark.parametrize("mode", [PERSISTENT, CHAIN])
+@pytest.mark.parametrize("fmt,head", [("q4_g128", "q4_g128"), ("q4_g64", "i8"), ("q4_0", "q4_0")])
+def test_llama32_shape_int4_groups(orc, fmt, head, mode):
+    """The int4 variants of the Llama-3.2-1B shape: groups of 128 everywhere (the tied
+    head and embedding too), groups of 64 with the int8 head, and Q4_0 everywhere."""
+    run_parity(orc, synth.llama32_1b(fmt, head), 2, 5, 2, mode=mode)
+
+
+@pytest.mark.parametrize("mode", [PERSISTENT, CHAIN])
 def test_tinyllama_shape_bf16_activations(orc, mode):
     """TinyLlama shapes, Q4_0, bf16 GEMV inputs, 2 of 22 layers."""
     run_parity(orc, synth.TINYLLAMA, 2, 4, 2, mode=mode)
