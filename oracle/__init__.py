@@ -84,6 +84,9 @@ def lib():
         "or_rope_apply": (None, [P, i, i, P, P]),
         "or_swiglu": (None, [P, P, i, P]),
         "or_argmax": (i, [P, i]),
+        "or_splitmix64": (ctypes.c_uint64, [ctypes.c_uint64, ctypes.c_uint64]),
+        "or_sample_uniform": (d, [ctypes.c_uint64, i, i]),
+        "or_sample": (i, [P, i, f, i, f, ctypes.c_uint64, i]),
         "or_attention_paged": (None, [P, P, P, i64, P, i, i, i, i, i, f, P]),
         "or_attention_contig": (None, [P, P, P, i, i, i, i, f, P]),
         "or_pool_create": (P, [i, i64]),
@@ -320,6 +323,22 @@ def attention_contig(q, k, v, ctx: int, Hq: int, Hkv: int, hd: int, scale: float
     out = np.empty(Hq * hd, np.float32)
     lib().or_attention_contig(_p(q), _p(k), _p(v), ctx, Hq, Hkv, hd, scale, _p(out))
     return out
+
+
+# --------------------------------------------------------------------- sampling
+
+def splitmix64(seed: int, i: int) -> int:
+    return int(lib().or_splitmix64(seed & (2**64 - 1), i & (2**64 - 1)))
+
+
+def sample_uniform(seed: int, pos: int, i: int) -> float:
+    return float(lib().or_sample_uniform(seed & (2**64 - 1), pos, i))
+
+
+def sample(logits, temperature: float, top_k: int = 0, top_p: float = 1.0, seed: int = 0, pos: int = 0) -> int:
+    """Token drawn by temperature / top-k / top-p sampling (see or_sample)."""
+    v = _c(logits, np.float32)
+    return int(lib().or_sample(_p(v), v.size, temperature, top_k, top_p, seed & (2**64 - 1), pos))
 
 
 # --------------------------------------------------------------------- block pool

@@ -342,6 +342,90 @@ int or_argmax(const float *v, int n) {
   return n > 0 ? best : -1;
 }
 
+/* ------------------------------------------------------------------ sampling */
+
+/* splitmix64 (Steele, Lea & Flood, "Fast splittable pseudorandom number generators",
+ * 2014): output i (0-based) of the stream started from `seed` -- the state advances by
+ * the golden gamma 0x9E3779B97F4A7C15 before each output, then the finaliser mixes it. */
+uint64_t or_splitmix64(uint64_t seed, uint64_t i) {
+  uint64_t z = seed + (i + 1) * 0x9E3779B97F4A7C15ULL;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBULL;
+  return z ^ (z >> 31);
+}
+
+/* READING: the random number of token i at position pos is (top 24 bits of splitmix64
+ * output (pos << 32 | i) + 1/2) / 2^24, strictly inside (0, 1): one number per token of
+ * each position, drawn from the seed alone, so a step's draw does not depend on any
+ * other step. */
+double or_sample_uniform(uint64_t seed, int pos, int i) {
+  const uint64_t z = or_splitmix64(seed, ((uint64_t)(uint32_t)pos << 32) | (uint32_t)i);
+  return ((double)(z >> 40) + 0.5) / 16777216.0;
+}
+
+typedef struct {
+  float v;
+  int i;
+} or_ranked;
+
+static int ranked_desc(const void *a, const void *b) {
+  const or_ranked *x = (const or_ranked *)a, *y = (const or_ranked *)b;
+  if (x->v != y->v) return x->v > y->v ? -1 : 1;
+  return x->i - y->i;
+}
+
+/* Temperature / top-k / top-p sampling ([INFER] design notes: sampling on the GPU with
+ * radix select for the top-k and top-p cut-offs and per-position random numbers from a
+ * seed, so runs reproduce).
+ * READING: temperature T <= 0 is greedy (argmax).  Otherwise, with q_i = exp((l_i - max)
+ * / T): top-k keeps the tokens whose logit is at least the k-th largest logit (every
+ * token tied with it too; k <= 0 or k >= n keeps all); top-p then keeps, of those, the
+ * tokens whose logit is at least the largest value t for which the kept tokens with
+ * logit >= t hold at least p of the kept mass sum q (ties at t kept; p >= 1 keeps all);
+ * the token is drawn from the kept tokens' renormalised distribution by the Gumbel-max
+ * rule -- argmax over kept i of l_i / T - log(-log(u_i)), u_i = or_sample_uniform(seed,
+ * pos, i), lowest index on ties -- which picks token i with probability q_i / sum q over
+ * the kept set.  Plain definition: a full sort, fp64 masses in descending order. */
+int or_sample(const float *logits, int n, float T, int top_k, float top_p, uint64_t seed, int pos) {
+  if (n <= 0) return -1;
+  if (!(T > 0.0f)) return or_argmax(logits, n);
+  or_ranked *r = (or_ranked *)malloc(sizeof(or_ranked) * (size_t)n);
+  for (int i = 0; i < n; ++i) { r[i].v = logits[i]; r[i].i = i; }
+  qsort(r, (size_t)n, sizeof(or_ranked), ranked_desc);
+  const double mx = r[0].v;
+  int kept = n;
+  if (top_k > 0 && top_k < n) {
+    const float tk = r[top_k - 1].v;
+    kept = top_k;
+    while (kept < n && r[kept].v == tk) ++kept;
+  }
+  if (top_p < 1.0f) {
+    double z = 0.0;
+    for (int j = 0; j < kept; ++j) z += exp(((double)r[j].v - mx) / (double)T);
+    const double target = (double)top_p * z;
+    double cum = 0.0;
+    int j = 0;
+    for (; j < kept; ++j) {
+      cum += exp(((double)r[j].v - mx) / (double)T);
+      if (cum >= target) break;
+    }
+    if (j >= kept) j = kept - 1;
+    const float tp = r[j].v;
+    int k2 = j + 1;
+    while (k2 < kept && r[k2].v == tp) ++k2;
+    kept = k2;
+  }
+  int best = -1;
+  double bs = -INFINITY;
+  for (int j = 0; j < kept; ++j) {
+    const int i = r[j].i;
+    const double sc = (double)logits[i] / (double)T - log(-log(or_sample_uniform(seed, pos, i)));
+    if (sc > bs || (sc == bs && i < best)) { bs = sc; best = i; }
+  }
+  free(r);
+  return best;
+}
+
 /* ------------------------------------------------------------------ attention */
 
 /* Softmax attention of one query head over t = 0..ctx-1 with keys/values supplied by

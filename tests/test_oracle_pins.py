@@ -855,3 +855,86 @@ def test_slots_sharing_without_copy_on_write_diverge(orc):
         alone.decode_step(int(t), pos, bt)
     ref, _ = alone.decode_step(int(a[1]), n_pre + 1, bt)
     assert not np.array_equal(logits[0], ref)
+
+
+# ----------------------------------------------------------------- sampling
+
+def _softmax(v, T):
+    e = np.exp((v.astype(np.float64) - v.max()) / T)
+    return e / e.sum()
+
+
+def test_sampler_generator_known_answers(orc):
+    """splitmix64 from its published first outputs (seed 0); the per-token uniform is
+    (top 24 bits + 1/2) / 2^24 of output (pos << 32 | i)."""
+    want = [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F, 0xF88BB8A8724C81EC]
+    assert [orc.splitmix64(0, i) for i in range(4)] == want
+    assert orc.sample_uniform(0, 0, 0) == ((0xE220A8397B1DCDAF >> 40) + 0.5) / 2**24
+    assert orc.sample_uniform(0, 0, 3) == ((0xF88BB8A8724C81EC >> 40) + 0.5) / 2**24
+    u = np.array([orc.sample_uniform(7, p, i) for p in range(40) for i in range(50)])
+    assert np.all((u > 0) & (u < 1)) and abs(u.mean() - 0.5) < 0.02
+
+
+def test_sampler_greedy_limits(orc):
+    """T = 0, top-k = 1 and a vanishing top-p all give the argmax, whatever the seed."""
+    v = synth.normal(60, 3000)
+    best = int(np.argmax(v))
+    for seed in (1, 2, 3):
+        assert orc.sample(v, 0.0, seed=seed, pos=5) == best
+        assert orc.sample(v, 1.3, top_k=1, seed=seed, pos=5) == best
+        assert orc.sample(v, 0.8, top_p=1e-9, seed=seed, pos=5) == best
+
+
+def test_sampler_support(orc):
+    """Every draw lies in the top-k set, and in the nucleus: the highest logits whose
+    softmax mass first reaches p (computed here by numpy)."""
+    v = synth.normal(61, 500)
+    order = np.argsort(-v, kind="stable")
+    topk = set(order[:7].tolist())
+    pr = _softmax(v, 0.5)[order]
+    nucleus = set(order[: int(np.searchsorted(np.cumsum(pr), 0.4)) + 1].tolist())
+    for pos in range(300):
+        assert orc.sample(v, 1.0, top_k=7, seed=11, pos=pos) in topk
+        assert orc.sample(v, 0.5, top_p=0.4, seed=11, pos=pos) in nucleus
+
+
+def test_sampler_keeps_ties_at_the_top_k_threshold(orc):
+    v = np.array([3.0, 1.0, 2.0, 2.0, 2.0, 0.5], np.float32)
+    seen = {orc.sample(v, 50.0, top_k=2, seed=3, pos=p) for p in range(400)}
+    assert seen == {0, 2, 3, 4}
+
+
+@pytest.mark.parametrize("top_k,top_p", [(0, 1.0), (3, 1.0), (0, 0.6), (4, 0.8)])
+def test_sampler_frequencies_follow_the_kept_softmax(orc, top_k, top_p):
+    """Over 30000 positions the draws follow q_i / sum q over the kept set (chi-square
+    with 5 degrees of freedom at most, below its 99.99 % quantile 25.7)."""
+    v = np.array([1.2, 0.3, -0.4, 2.0, 0.9, -1.1], np.float32)
+    T = 0.9
+    pr = _softmax(v, T)
+    order = np.argsort(-v, kind="stable")
+    keep = np.ones(v.size, bool)
+    if top_k:
+        keep[:] = False
+        keep[order[:top_k]] = True
+    if top_p < 1:
+        kept_sorted = [i for i in order if keep[i]]
+        mass = pr[kept_sorted] / pr[kept_sorted].sum()
+        cut = int(np.searchsorted(np.cumsum(mass), top_p)) + 1
+        keep[:] = False
+        keep[kept_sorted[:cut]] = True
+    want = np.where(keep, pr, 0.0)
+    want /= want.sum()
+    n = 30000
+    counts = np.bincount([orc.sample(v, T, top_k=top_k, top_p=top_p, seed=0x5A, pos=p) for p in range(n)],
+                         minlength=v.size)
+    assert np.all(counts[~keep] == 0)
+    exp_ = want[keep] * n
+    chi2 = float(np.sum((counts[keep] - exp_) ** 2 / exp_))
+    assert chi2 < 25.7, (counts, exp_)
+
+
+def test_sampler_reproduces(orc):
+    v = synth.normal(62, 2000)
+    a = [orc.sample(v, 0.7, 50, 0.9, seed=99, pos=p) for p in range(30)]
+    assert a == [orc.sample(v, 0.7, 50, 0.9, seed=99, pos=p) for p in range(30)]
+    assert len(set(a)) > 5  # different positions draw different tokens
