@@ -407,6 +407,26 @@ def contexts_table(torch, gm, stream, shape, bt, logits, am, pos: int, tok: int,
     return rows, pos, tok
 
 
+def sampled_steps(torch, gm, stream, bt, logits, am, pos: int, tok: int, steps: int) -> dict:
+    """The same step with the next token drawn by temperature 0.6 / top-k 40 / top-p 0.9
+    sampling inside its graph (mie_set_sampling), timed like the greedy step."""
+    T, k, p = 0.6, 40, 0.9
+    gm.set_sampling(T, k, p, 0x5A4D)
+    gm.decode_step(tok, pos, bt, logits, am)
+    gm.decode_continue(3)
+    gm.sync()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    gm.decode_continue(steps)
+    e1.record(stream)
+    e1.synchronize()
+    gm.sync()
+    dt = e0.elapsed_time(e1) / 1e3 / steps
+    gm.set_sampling(0.0)
+    return {"temperature": T, "top_k": k, "top_p": p, "ctx": pos + 4, "steps": steps, "tok_s": 1.0 / dt,
+            "ms_per_step": dt * 1e3, "launches_per_step": gm.launches}
+
+
 def model_contexts(torch, shape, ctxs, steps: int, peak: float, read_peak: float | None, label: str) -> dict:
     """A fresh context for `shape`, prefilled from position 0 by real decode steps,
     timed at each context of ctxs (contexts_table)."""
@@ -507,6 +527,8 @@ def run_mie(args, shape):
         rows, pos, tok = contexts_table(torch, gm, stream, shape, bt, logits, am, pos, tok, ctxs, args.decode_steps,
                                         peak, read_peak)
         extras["contexts"] = [head] + rows
+        extras["sampled"] = guarded(lambda: sampled_steps(torch, gm, stream, bt, logits, am, pos, tok,
+                                                          args.decode_steps))
 
     result = None
     step_mode = "persistent" if gm.step_mode == 0 else "chain"

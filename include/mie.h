@@ -215,6 +215,29 @@ mie_status mie_argmax(const float *v, int n, int32_t *out, void *workspace, size
 mie_status mie_hbm_read_probe(const void *buf, size_t bytes, uint32_t *xor_out, int load_bytes,
                               int blocks_per_sm, void *stream);
 
+/* ======================================================================== sampling */
+
+/* Workspace bytes of mie_sample (independent of the vocabulary size). */
+size_t mie_sample_workspace_bytes(void);
+
+/* Draws the next token from logits v[0..n) (device fp32) ([INFER] design notes:
+ * temperature / top-k / top-p sampling on the GPU, radix select for the top-k and top-p
+ * cut-offs, per-position random numbers from a seed so that runs reproduce).
+ * temperature <= 0: the argmax (lowest index on ties).  Otherwise, with
+ * q_i = exp((v_i - max v) / temperature): top-k keeps the tokens whose value is at least
+ * the top_k-th largest (ties at it kept; top_k 0 or >= n keeps all); top-p then keeps, of
+ * those, the tokens whose value is at least the largest t for which the kept tokens with
+ * value >= t hold at least top_p of the kept mass (ties kept; top_p 1 keeps all); the
+ * token is the Gumbel-max draw argmax over kept i of v_i / temperature - log(-log u_i),
+ * u_i = (top 24 bits of splitmix64(seed, output (pos << 32 | i)) + 1/2) / 2^24, which
+ * picks i with probability q_i / (kept mass).  The masses are summed in 2^-40 fixed
+ * point, so the cut-offs, and the token, are the same on every run.  out: device int32.
+ * workspace: device, mie_sample_workspace_bytes() bytes, 256-byte aligned (zeroed by the
+ * call).  MIE_E_ARG for top_k < 0, top_p outside (0, 1] or a NaN temperature. */
+mie_status mie_sample(const float *logits, int n, float temperature, int top_k, float top_p,
+                      uint64_t seed, int32_t pos, int32_t *out, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
 /* Reads and clears the device error flag that kernels latch when a bounds check
  * fails (stateless kernels share one flag per device).  Synchronises `stream`.
  * MIE_E_DEVICE if a check fired since the last call. */
@@ -396,6 +419,16 @@ mie_status mie_sync(mie_ctx *ctx);
  * for phase 0 (it has no input to withhold), a phase past the LM head, or
  * wait_polls < 1. */
 mie_status mie_debug_stall(mie_ctx *ctx, int phase, long wait_polls);
+
+/* Sampling of the next token inside the step's graph (mie_sample's rule, with seed
+ * `seed` and the step's position pos: the step that writes position pos draws with
+ * u_i(seed, pos, i)).  From the next mie_decode_step on, the draw replaces the argmax:
+ * it goes to argmax_out and, in mie_decode_continue, becomes the next token.  The logits
+ * pass through a buffer of the context when the caller passes none.  temperature <= 0
+ * switches back to greedy decoding.  The few-slot step stays greedy.  MIE_E_ARG as for
+ * mie_sample. */
+mie_status mie_set_sampling(mie_ctx *ctx, float temperature, int top_k, float top_p,
+                            uint64_t seed);
 
 /* Kernel launches one mie_decode_step replay performs (for launch accounting). */
 int mie_step_launches(const mie_ctx *ctx);

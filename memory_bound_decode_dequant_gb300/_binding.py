@@ -22,7 +22,7 @@ __all__ = ["lib", "MieError", "FMT", "LIB_PATH", "exported_names", "header_funct
            "mie_quantize_q4", "mie_q4_packed_bytes", "mie_q4_pack", "mie_gemv_q4", "Q4_GROUP",
            "mie_paged_attn_decode", "mie_paged_attn_workspace_bytes", "mie_paged_attn_decode_noalloc",
            "mie_argmax",
-           "mie_argmax_workspace_bytes", "mie_check", "mie_hbm_read_probe", "Pool", "Config", "Model",
+           "mie_argmax_workspace_bytes", "mie_check", "mie_hbm_read_probe", "mie_sample", "mie_sample_workspace_bytes", "Pool", "Config", "Model",
            "DeviceArray"]
 
 
@@ -66,6 +66,9 @@ _SIGS = {
     "mie_argmax": (I, [P, I, P, P, SZ, P]),
     "mie_check": (I, [P]),
     "mie_hbm_read_probe": (I, [P, SZ, P, I, I, P]),
+    "mie_sample_workspace_bytes": (SZ, []),
+    "mie_sample": (I, [P, I, F, I, F, ctypes.c_uint64, ctypes.c_int32, P, P, SZ, P]),
+    "mie_set_sampling": (I, [P, F, I, F, ctypes.c_uint64]),
     "mie_pool_create": (I, [I, ctypes.POINTER(P)]),
     "mie_pool_destroy": (None, [P]),
     "mie_pool_alloc": (I, [P, ctypes.POINTER(ctypes.c_int32)]),
@@ -323,6 +326,24 @@ def mie_hbm_read_probe(buf, xor_out=None, load_bytes: int = 32, blocks_per_sm: i
     return xor_out
 
 
+def mie_sample_workspace_bytes() -> int:
+    return int(lib().mie_sample_workspace_bytes())
+
+
+def mie_sample(logits, temperature: float, top_k: int = 0, top_p: float = 1.0, seed: int = 0, pos: int = 0,
+               out=None, workspace=None, stream=None):
+    """The token drawn from the device logits tensor (int32 device tensor, returned)."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(1, dtype=torch.int32, device=logits.device)
+    if workspace is None:
+        workspace = torch.empty(mie_sample_workspace_bytes(), dtype=torch.uint8, device=logits.device)
+    _check(lib().mie_sample(_dev(logits, torch.float32, "logits"), logits.numel(), float(temperature), int(top_k),
+                            float(top_p), seed & (2**64 - 1), int(pos), _dev(out, torch.int32, "out"),
+                            workspace.data_ptr(), workspace.numel(), _stream(stream)), "mie_sample")
+    return out
+
+
 def mie_check(stream=None):
     _check(lib().mie_check(_stream(stream)), "mie_check")
 
@@ -491,6 +512,10 @@ class Model:
     def step_mode(self) -> int:
         return int(lib().mie_step_mode(self.h))
 
+    def set_sampling(self, temperature: float, top_k: int = 0, top_p: float = 1.0, seed: int = 0):
+        _check(lib().mie_set_sampling(self.h, float(temperature), int(top_k), float(top_p), seed & (2**64 - 1)),
+               "mie_set_sampling")
+
     def debug_stall(self, phase: int, wait_polls: int = 0):
         """Testing aid: phase `phase` of the persistent step waits for an input nobody
         writes, and every wait gives up after wait_polls rounds (phase < 0 restores)."""
@@ -638,6 +663,10 @@ def mie_sync(ctx: Model) -> None:
     ctx.sync()
 
 
+def mie_set_sampling(ctx: Model, temperature: float, top_k: int = 0, top_p: float = 1.0, seed: int = 0) -> None:
+    ctx.set_sampling(temperature, top_k, top_p, seed)
+
+
 def mie_debug_stall(ctx: Model, phase: int, wait_polls: int = 0) -> None:
     ctx.debug_stall(phase, wait_polls)
 
@@ -655,4 +684,4 @@ __all__ += ["mie_last_error", "mie_status_string", "mie_pool_create", "mie_pool_
             "mie_pool_writable", "mie_create", "mie_destroy", "mie_load_weights", "mie_ctx_pool",
             "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_kv_writable", "mie_decode_step",
             "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
-            "mie_set_trace", "mie_debug_stall", "mie_sync", "mie_step_launches", "mie_slot_step_launches"]
+            "mie_set_trace", "mie_set_sampling", "mie_debug_stall", "mie_sync", "mie_step_launches", "mie_slot_step_launches"]

@@ -78,7 +78,8 @@ struct StepParams {
   float *logits_out;           // [n_slots][vocab] or null
   int32_t *argmax_out;         // [n_slots] or null
   int32_t advance;             // 1: the head kernel sets token = argmax, pos += 1
-  int32_t pad[3];
+  int32_t sample_advance;      // 1: the sampler sets token = its draw, pos += 1 (advance is 0 then)
+  int32_t pad[2];
 };
 
 }  // namespace mie

@@ -148,6 +148,16 @@ mie_status persist_launch(const PersistPlan &plan, const PersistArgs &args, cuda
 mie_status slots_gemv_supported(const DevMat &m, int pro);
 mie_status launch_gemv_slots(int pro, int epi, const GemvArgs &a, cudaStream_t st, bool pdl);
 
+// Sampling (sample.cu).
+struct SampleArgs;
+size_t sample_workspace_bytes();
+int sample_launches(float temperature, int top_k, float top_p, int n);
+// Enqueues the sampler for slot 0 of the step parameters sp: logits sp->logits_out, the
+// RNG position sp->pos[0]; the draw goes to sp->argmax_out and, with sp->sample_advance,
+// into token / pos.  ws: sample_workspace_bytes() of zeroed device memory.
+mie_status launch_step_sample(StepParams *sp, int vocab, float temperature, int top_k, float top_p, uint64_t seed,
+                              void *ws, cudaStream_t st);
+
 // Load-time kernels.
 mie_status launch_convert_bf16(const float *w, int64_t n, uint16_t *out, cudaStream_t st);
 mie_status launch_quantize_i8(const float *w, int M, int K, int8_t *q, float *s, cudaStream_t st);

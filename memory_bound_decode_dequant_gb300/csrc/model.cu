@@ -135,6 +135,12 @@ struct mie_ctx {
   int stall_phase = -1;
   long wait_polls = kWaitPolls;
   uint64_t *stall_words = nullptr;
+  // sampling of the next token (mie_set_sampling); temperature <= 0: greedy
+  float temperature = 0.f, top_p = 1.f;
+  int top_k = 0;
+  uint64_t seed = 0;
+  float *logits_buf = nullptr;  // the step's logits when the caller passes none
+  void *sample_ws = nullptr;
   // few-slot step: its own phase list and graph (always the kernel chain)
   std::vector<Phase> slot_phases;
   cudaGraphExec_t slot_graph = nullptr;
@@ -707,16 +713,23 @@ static mie_status enqueue_step(mie_ctx *ctx, int *launches) {
     pa.wait_polls = ctx->wait_polls;
     if ((s = persist_launch(ctx->plan, pa, st)) != MIE_OK) return s;
     *launches = 1;
-    return MIE_OK;
+  } else {
+    int n = 0;
+    for (const Phase &ph : ctx->phases) {
+      if (ph.kind == PH_GEMV) s = launch_gemv(ph.pro, ph.epi, ph.g, gemv_default_grid(ph.g.m, ph.epi), st, true);
+      else s = launch_attn(ph.at, st, true);
+      if (s != MIE_OK) return s;
+      ++n;
+    }
+    *launches = n;
   }
-  int n = 0;
-  for (const Phase &ph : ctx->phases) {
-    if (ph.kind == PH_GEMV) s = launch_gemv(ph.pro, ph.epi, ph.g, gemv_default_grid(ph.g.m, ph.epi), st, true);
-    else s = launch_attn(ph.at, st, true);
-    if (s != MIE_OK) return s;
-    ++n;
+  if (ctx->temperature > 0.f) {  // the draw replaces the head's argmax as the next token
+    const mie_config &c = ctx->cfg;
+    if ((s = launch_step_sample(ctx->sp, c.vocab, ctx->temperature, ctx->top_k, ctx->top_p, ctx->seed,
+                                ctx->sample_ws, st)) != MIE_OK)
+      return s;
+    *launches += sample_launches(ctx->temperature, ctx->top_k, ctx->top_p, c.vocab);
   }
-  *launches = n;
   return MIE_OK;
 }
 
@@ -812,6 +825,11 @@ extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, 
   p.logits_out = logits_out;
   p.argmax_out = argmax_out;
   p.advance = 1;
+  if (ctx->temperature > 0.f) {  // the sampler reads the logits and advances instead
+    if (!p.logits_out) p.logits_out = ctx->logits_buf;
+    p.advance = 0;
+    p.sample_advance = 1;
+  }
   const mie_status su = upload_params(ctx, p);
   if (su != MIE_OK) return su;
   if (!ctx->primed) {
@@ -982,6 +1000,26 @@ extern "C" mie_status mie_set_trace(mie_ctx *ctx, void *device_buffer, size_t by
   ctx->primed = false;  // the next step re-captures with (or without) the trace
   if (n_phases) *n_phases = 5 * ctx->cfg.n_layers + 1;
   if (n_ctas) *n_ctas = sm_count();
+  return MIE_OK;
+}
+
+// Temperature / top-k / top-p sampling of the next token inside the step's graph.
+extern "C" mie_status mie_set_sampling(mie_ctx *ctx, float temperature, int top_k, float top_p, uint64_t seed) {
+  if (!ctx) return fail(MIE_E_ARG, "mie_set_sampling: null context");
+  if (top_k < 0 || !(top_p > 0.f) || top_p > 1.f || temperature != temperature)
+    return fail(MIE_E_ARG, "mie_set_sampling: top_k %d, top_p %g, temperature %g", top_k, top_p, temperature);
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  if (temperature > 0.f && !ctx->sample_ws) {
+    ctx->logits_buf = (float *)ctx->dalloc(sizeof(float) * (size_t)ctx->cfg.vocab);
+    ctx->sample_ws = ctx->dalloc(sample_workspace_bytes());
+    if (!ctx->logits_buf || !ctx->sample_ws) return fail(MIE_E_OOM, "mie_set_sampling: buffers");
+    MIE_CUDA(cudaMemset(ctx->sample_ws, 0, sample_workspace_bytes()));
+  }
+  ctx->temperature = temperature > 0.f ? temperature : 0.f;
+  ctx->top_k = top_k;
+  ctx->top_p = top_p;
+  ctx->seed = seed;
+  ctx->primed = false;  // the next step re-captures with (or without) the sampler
   return MIE_OK;
 }
 
