@@ -372,6 +372,52 @@ mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int32_t *token
                                  const int32_t *pos, const int32_t *block_tables, int max_blocks,
                                  float *logits_out, int32_t *argmax_out);
 
+/* Verify pass ([RUST] "Speculative decoding without a draft model": several tokens of one
+ * sequence are checked in one batched pass, the weights read once): positions pos .. pos+n-1
+ * of one sequence (tokens[j] host int32 at pos + j) as n slots of the few-slot step,
+ * every slot reading the same block table (device int32 [max_blocks]), slot j attending
+ * to positions 0 .. pos + j including the K/V this pass writes.  1 <= n <= max_slots.
+ * logits_out: device [n][vocab] or NULL; argmax_out: device [n] or NULL.  The few-slot
+ * kernels compute each (row, slot) output on its own, in an order that does not depend
+ * on the number of slots, so a pass of n positions gives the bits of n passes of one
+ * position through the same kernels. */
+mie_status mie_verify_step(mie_ctx *ctx, const int32_t *tokens, int n, int32_t pos,
+                           const int32_t *block_table, int max_blocks, float *logits_out,
+                           int32_t *argmax_out);
+
+/* Prompt lookup ([RUST] "Speculative decoding without a draft model"): the tokens that
+ * followed the most recent earlier occurrence of the last g tokens of ids[0..n), for the
+ * longest g in [min_ngram, max_ngram] that occurs earlier (ending before the last g
+ * tokens begin); at most k of them, never past the end.  Writes them to out (host) and
+ * returns their number (0: no match).  Host only. */
+int mie_lookup_propose(const int32_t *ids, int n, int min_ngram, int max_ngram, int k, int32_t *out);
+
+/* Acceptance gate of speculative decoding ([RUST], same section: acceptance is tracked
+ * over the last 10 attempts; below 30 % speculation pauses for 5 steps, each consecutive
+ * pause doubling up to 80).  A full window of `window` attempts whose accepted / proposed
+ * guesses fall below `threshold` starts a pause of the current length, which then
+ * doubles up to pause_max; a full window at or above the threshold resets the length to
+ * `pause`.  The window keeps its attempts across a pause.  Caller-owned memory of
+ * mie_spec_gate_bytes() bytes.  Host only. */
+typedef struct mie_spec_gate mie_spec_gate;
+size_t mie_spec_gate_bytes(void);
+void mie_spec_gate_init(mie_spec_gate *g, int window, float threshold, int pause, int pause_max);
+int mie_spec_gate_open(mie_spec_gate *g);  /* 1: this pass may guess (a paused gate counts it off) */
+void mie_spec_gate_record(mie_spec_gate *g, int proposed, int accepted);
+
+/* Greedy generation through the few-slot kernels.  ids: host int32 [n_prompt + n_new];
+ * ids[0..n_prompt) is the prompt, ids[n_prompt..) receives the n_new generated tokens.
+ * The prompt but its last token is processed max_slots positions per pass (prefill by
+ * batched passes); each later pass takes the last token and, with spec_max > 1, up to
+ * spec_max - 1 prompt-lookup guesses (2- to 4-token matches, behind the acceptance gate
+ * of 10 attempts / 30 % / pauses of 5 .. 80 passes), verifies them in one mie_verify_step
+ * and keeps the guesses up to the first the model disagrees with, plus the model's own
+ * next token.  Because a pass of several positions equals single-position passes bit for
+ * bit, the tokens do not depend on spec_max.  block_table: device int32 [max_blocks].
+ * stats (host int [3], nullable): passes, guesses proposed, guesses accepted. */
+mie_status mie_generate(mie_ctx *ctx, int32_t *ids, int n_prompt, int n_new, const int32_t *block_table,
+                        int max_blocks, int spec_max, int *stats);
+
 /* How mie_decode_step runs the step.  MIE_STEP_PERSISTENT (the default where the shape
  * is covered): one cooperative kernel of one CTA per SM runs every phase; its producer
  * warps stream all weights and the K/V of old positions through shared-memory rings,

@@ -96,6 +96,13 @@ _SIGS = {
     "mie_slot_step_launches": (I, [P]),
     "mie_set_trace": (I, [P, P, SZ, ctypes.POINTER(I), ctypes.POINTER(I)]),
     "mie_debug_stall": (I, [P, I, ctypes.c_long]),
+    "mie_verify_step": (I, [P, P, I, ctypes.c_int32, P, I, P, P]),
+    "mie_lookup_propose": (I, [P, I, I, I, I, P]),
+    "mie_spec_gate_bytes": (SZ, []),
+    "mie_spec_gate_init": (None, [P, I, F, I, I]),
+    "mie_spec_gate_open": (I, [P]),
+    "mie_spec_gate_record": (None, [P, I, I]),
+    "mie_generate": (I, [P, P, I, I, P, I, I, P]),
 }
 
 _lib = None
@@ -512,6 +519,29 @@ class Model:
     def step_mode(self) -> int:
         return int(lib().mie_step_mode(self.h))
 
+    def verify_step(self, tokens, pos: int, block_table, logits_out=None, argmax_out=None):
+        """Positions pos .. pos+n-1 of one sequence (host tokens) as n slots sharing one
+        block table (device int32 [max_blocks])."""
+        torch = _torch()
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(lib().mie_verify_step(self.h, t.ctypes.data, t.size, int(pos),
+                                     _dev(block_table, torch.int32, "block_table"), block_table.numel(),
+                                     None if logits_out is None else _dev(logits_out, torch.float32, "logits"),
+                                     None if argmax_out is None else _dev(argmax_out, torch.int32, "argmax")),
+               "mie_verify_step")
+
+    def generate(self, prompt, n_new: int, block_table, spec_max: int = 1):
+        """Greedy generation through the few-slot kernels (speculative for spec_max > 1);
+        returns (generated tokens, {passes, proposed, accepted})."""
+        torch = _torch()
+        ids = np.zeros(len(prompt) + n_new, np.int32)
+        ids[: len(prompt)] = prompt
+        stats = (ctypes.c_int * 3)()
+        _check(lib().mie_generate(self.h, ids.ctypes.data, len(prompt), n_new,
+                                  _dev(block_table, torch.int32, "block_table"), block_table.numel(), spec_max, stats),
+               "mie_generate")
+        return ids[len(prompt):].copy(), {"passes": stats[0], "proposed": stats[1], "accepted": stats[2]}
+
     def set_sampling(self, temperature: float, top_k: int = 0, top_p: float = 1.0, seed: int = 0):
         _check(lib().mie_set_sampling(self.h, float(temperature), int(top_k), float(top_p), seed & (2**64 - 1)),
                "mie_set_sampling")
@@ -667,6 +697,52 @@ def mie_set_sampling(ctx: Model, temperature: float, top_k: int = 0, top_p: floa
     ctx.set_sampling(temperature, top_k, top_p, seed)
 
 
+def mie_verify_step(ctx: Model, tokens, pos: int, block_table, logits_out=None, argmax_out=None) -> None:
+    ctx.verify_step(tokens, pos, block_table, logits_out, argmax_out)
+
+
+def mie_generate(ctx: Model, prompt, n_new: int, block_table, spec_max: int = 1):
+    return ctx.generate(prompt, n_new, block_table, spec_max)
+
+
+def mie_lookup_propose(ids, min_ngram: int, max_ngram: int, k: int) -> list:
+    """Prompt-lookup guesses for the context ids (host)."""
+    a = np.ascontiguousarray(ids, dtype=np.int32)
+    out = np.zeros(max(k, 1), np.int32)
+    n = lib().mie_lookup_propose(a.ctypes.data, a.size, min_ngram, max_ngram, k, out.ctypes.data)
+    return [int(v) for v in out[:n]]
+
+
+class SpecGate:
+    """mie_spec_gate: the acceptance gate of speculative decoding (host)."""
+
+    def __init__(self, window: int = 10, threshold: float = 0.3, pause: int = 5, pause_max: int = 80):
+        self._buf = ctypes.create_string_buffer(int(lib().mie_spec_gate_bytes()))
+        lib().mie_spec_gate_init(self._buf, window, threshold, pause, pause_max)
+
+    def open(self) -> bool:
+        return bool(lib().mie_spec_gate_open(self._buf))
+
+    def record(self, proposed: int, accepted: int) -> None:
+        lib().mie_spec_gate_record(self._buf, proposed, accepted)
+
+
+def mie_spec_gate_bytes() -> int:
+    return int(lib().mie_spec_gate_bytes())
+
+
+def mie_spec_gate_init(gate: SpecGate, window: int, threshold: float, pause: int, pause_max: int) -> None:
+    lib().mie_spec_gate_init(gate._buf, window, threshold, pause, pause_max)
+
+
+def mie_spec_gate_open(gate: SpecGate) -> bool:
+    return gate.open()
+
+
+def mie_spec_gate_record(gate: SpecGate, proposed: int, accepted: int) -> None:
+    gate.record(proposed, accepted)
+
+
 def mie_debug_stall(ctx: Model, phase: int, wait_polls: int = 0) -> None:
     ctx.debug_stall(phase, wait_polls)
 
@@ -684,4 +760,6 @@ __all__ += ["mie_last_error", "mie_status_string", "mie_pool_create", "mie_pool_
             "mie_pool_writable", "mie_create", "mie_destroy", "mie_load_weights", "mie_ctx_pool",
             "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_kv_writable", "mie_decode_step",
             "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
-            "mie_set_trace", "mie_set_sampling", "mie_debug_stall", "mie_sync", "mie_step_launches", "mie_slot_step_launches"]
+            "mie_set_trace", "mie_set_sampling", "mie_debug_stall", "mie_sync", "mie_verify_step", "mie_generate",
+            "mie_lookup_propose", "SpecGate", "mie_spec_gate_bytes", "mie_spec_gate_init", "mie_spec_gate_open",
+            "mie_spec_gate_record", "mie_step_launches", "mie_slot_step_launches"]

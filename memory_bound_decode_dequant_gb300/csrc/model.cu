@@ -141,6 +141,10 @@ struct mie_ctx {
   uint64_t seed = 0;
   float *logits_buf = nullptr;  // the step's logits when the caller passes none
   void *sample_ws = nullptr;
+  // verify passes and generation (mie_verify_step, mie_generate)
+  int32_t *verify_table = nullptr;  // [kMaxSlots][verify_cap] copies of one sequence's table
+  int verify_cap = 0;
+  int32_t *gen_argmax = nullptr;    // [kMaxSlots]
   // few-slot step: its own phase list and graph (always the kernel chain)
   std::vector<Phase> slot_phases;
   cudaGraphExec_t slot_graph = nullptr;
@@ -946,6 +950,84 @@ extern "C" mie_status mie_decode_step_slots(mie_ctx *ctx, int n_slots, const int
   }
   int n = 0;
   return enqueue_slots(ctx, &n);
+}
+
+// k consecutive positions of one sequence as k slots of the few-slot step: slot j is
+// token tokens[j] at position pos + j, every slot reading the same block table, so slot j
+// attends to the K/V the pass itself wrote for positions pos .. pos + j - 1.
+extern "C" mie_status mie_verify_step(mie_ctx *ctx, const int32_t *tokens, int n, int32_t pos,
+                                      const int32_t *block_table, int max_blocks, float *logits_out,
+                                      int32_t *argmax_out) {
+  if (!ctx || !tokens || !block_table) return fail(MIE_E_ARG, "mie_verify_step: null pointer");
+  if (n < 1 || n > ctx->cfg.max_slots)
+    return fail(MIE_E_ARG, "mie_verify_step: %d positions outside [1, %d]", n, ctx->cfg.max_slots);
+  if (max_blocks < 1) return fail(MIE_E_ARG, "mie_verify_step: max_blocks %d", max_blocks);
+  if (max_blocks > ctx->verify_cap) {
+    int32_t *t = (int32_t *)ctx->dalloc(sizeof(int32_t) * (size_t)kMaxSlots * max_blocks);
+    if (!t) return fail(MIE_E_OOM, "mie_verify_step: table copies");
+    ctx->verify_table = t;
+    ctx->verify_cap = max_blocks;
+  }
+  for (int s = 0; s < n; ++s)
+    MIE_CUDA(cudaMemcpyAsync(ctx->verify_table + (size_t)s * max_blocks, block_table, sizeof(int32_t) * max_blocks,
+                             cudaMemcpyDeviceToDevice, ctx->stream));
+  int32_t p[kMaxSlots];
+  for (int s = 0; s < n; ++s) p[s] = pos + s;
+  return mie_decode_step_slots(ctx, n, tokens, p, ctx->verify_table, max_blocks, logits_out, argmax_out);
+}
+
+// Greedy generation through the few-slot kernels, speculative when spec_max > 1.
+extern "C" mie_status mie_generate(mie_ctx *ctx, int32_t *ids, int n_prompt, int n_new, const int32_t *block_table,
+                                   int max_blocks, int spec_max, int *stats) {
+  if (!ctx || !ids || !block_table) return fail(MIE_E_ARG, "mie_generate: null pointer");
+  const mie_config &c = ctx->cfg;
+  if (n_prompt < 1 || n_new < 0 || n_prompt + n_new > c.max_pos || (n_prompt + n_new - 1) / c.block_size >= max_blocks)
+    return fail(MIE_E_ARG, "mie_generate: %d + %d tokens do not fit (max_pos %d, %d blocks)", n_prompt, n_new,
+                c.max_pos, max_blocks);
+  if (spec_max < 1) spec_max = 1;
+  if (spec_max > c.max_slots) spec_max = c.max_slots;
+  if (!ctx->gen_argmax && !(ctx->gen_argmax = (int32_t *)ctx->dalloc(sizeof(int32_t) * kMaxSlots)))
+    return fail(MIE_E_OOM, "mie_generate: argmax buffer");
+  int passes = 0, proposed = 0, accepted = 0;
+  mie_status s;
+  // the prompt but its last token, up to max_slots positions a pass
+  for (int p0 = 0; p0 < n_prompt - 1; p0 += c.max_slots) {
+    const int n = std::min(c.max_slots, n_prompt - 1 - p0);
+    if ((s = mie_verify_step(ctx, ids + p0, n, p0, block_table, max_blocks, nullptr, nullptr)) != MIE_OK) return s;
+    ++passes;
+  }
+  std::vector<uint8_t> gate_mem(mie_spec_gate_bytes());
+  mie_spec_gate *gate = reinterpret_cast<mie_spec_gate *>(gate_mem.data());
+  mie_spec_gate_init(gate, 10, 0.3f, 5, 80);
+  int len = n_prompt;
+  const int end = n_prompt + n_new;
+  int32_t toks[kMaxSlots], best[kMaxSlots];
+  while (len < end) {
+    // the anchor (the last token, whose K/V is not computed yet) and the guesses after it
+    int m = 0;
+    toks[0] = ids[len - 1];
+    const int room = std::min(spec_max - 1, c.max_pos - len);
+    if (room > 0 && mie_spec_gate_open(gate)) m = mie_lookup_propose(ids, len, 2, 4, room, toks + 1);
+    if ((s = mie_verify_step(ctx, toks, m + 1, len - 1, block_table, max_blocks, nullptr, ctx->gen_argmax)) != MIE_OK)
+      return s;
+    if ((s = mie_sync(ctx)) != MIE_OK) return s;
+    MIE_CUDA(cudaMemcpy(best, ctx->gen_argmax, sizeof(int32_t) * (m + 1), cudaMemcpyDeviceToHost));
+    ++passes;
+    // the model's token after the anchor is new; each guess it agrees with adds the
+    // model's token after that guess
+    int acc = 0;
+    while (acc < m && toks[1 + acc] == best[acc]) ++acc;
+    if (m > 0) mie_spec_gate_record(gate, m, acc);
+    proposed += m;
+    accepted += acc;
+    for (int j = 0; j <= acc && len < end; ++j) ids[len++] = best[j];
+  }
+  if (stats) {
+    stats[0] = passes;
+    stats[1] = proposed;
+    stats[2] = accepted;
+  }
+  return MIE_OK;
 }
 
 extern "C" mie_status mie_sync(mie_ctx *ctx) {
