@@ -427,6 +427,67 @@ def sampled_steps(torch, gm, stream, bt, logits, am, pos: int, tok: int, steps: 
             "ms_per_step": dt * 1e3, "launches_per_step": gm.launches}
 
 
+def batched_passes(torch, n_prompt: int = 2048, n_spec_prompt: int = 256, n_new: int = 128) -> dict:
+    """Llama-3.2-1B bf16 through the few-slot kernels (mie_generate): prefill of an
+    n_prompt-token prompt in passes of 8 positions (each pass reads the weights once), and
+    greedy generation after a prompt that repeats a 64-token pattern, with prompt-lookup
+    speculation (up to 3 guesses a pass) and without; the two give the same tokens."""
+    from memory_bound_decode_dequant_gb300.workload import build_gpu_model
+    shape = synth.llama32_1b("bf16")
+    bs = shape.block_size
+    n_blocks = (max(n_prompt, n_spec_prompt + n_new) + bs - 1) // bs + 2
+    stream = torch.cuda.Stream()
+    gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=n_blocks * bs, max_slots=8, stream=stream)
+    bt = torch.from_numpy(synth.permutation(0x5045, n_blocks).astype(np.int32)).cuda()
+    out = {"model": "llama-3.2-1b bf16", "kernels": "few-slot step (mma.sync, bf16 hi + lo inputs)"}
+    prompt = [int(t) for t in shape.tokens(n_prompt, stream=11)]
+    gm.generate(prompt[:40], 1, bt, 1)  # captures the few-slot graph
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    _, st = gm.generate(prompt, 1, bt, 1)
+    dt = time.perf_counter() - t0
+    out["prefill"] = {"prompt_tokens": n_prompt, "positions_per_pass": 8, "seconds": dt,
+                      "tok_s": (n_prompt - 1) / dt, "passes": st["passes"],
+                      "note": "wall time through mie_generate, the last prompt token's pass and one generated token included"}
+    pattern = [int(t) for t in shape.tokens(64, stream=12)]
+    rep = (pattern * (n_spec_prompt // 64 + 1))[:n_spec_prompt]
+    res = {}
+    for spec in (1, 4):
+        gm.generate(rep, 1, bt, spec)  # the prompt's K/V, untimed
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        toks, st = gm.generate(rep, n_new, bt, spec)
+        res[spec] = (toks, st, time.perf_counter() - t0)
+    # the payoff the lookup relies on: one pass over k positions against k passes of one
+    per_pass = {}
+    for k in (1, 2, 4, 8):
+        toks = [int(t) for t in shape.tokens(k, stream=13)]
+        for i in range(3):
+            gm.verify_step(toks, 64 + 8 * i, bt)
+        gm.sync()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        n_rep = 24
+        e0.record(stream)
+        for i in range(n_rep):
+            gm.verify_step(toks, 64 + 8 * (i % 8), bt)
+        e1.record(stream)
+        e1.synchronize()
+        gm.sync()
+        per_pass[k] = e0.elapsed_time(e1) / 1e3 / n_rep
+    out["pass_cost"] = {str(k): {"ms_per_pass": t * 1e3, "k_single_passes_over_one_pass": k * per_pass[1] / t}
+                        for k, t in per_pass.items()}
+    gm.close()
+    del gm
+    torch.cuda.empty_cache()
+    same = bool(np.array_equal(res[1][0], res[4][0]))
+    out["speculative"] = {"prompt": f"{n_spec_prompt} tokens repeating a 64-token pattern", "new_tokens": n_new,
+                          "plain": {"seconds": res[1][2], **res[1][1]},
+                          "spec_max_4": {"seconds": res[4][2], **res[4][1]},
+                          "same_tokens": same,
+                          "note": "wall time includes the prompt's prefill passes"}
+    return out
+
+
 def model_contexts(torch, shape, ctxs, steps: int, peak: float, read_peak: float | None, label: str) -> dict:
     """A fresh context for `shape`, prefilled from position 0 by real decode steps,
     timed at each context of ctxs (contexts_table)."""
@@ -459,7 +520,7 @@ def run_mie(args, shape):
     bs = shape.block_size
     ctxs = [c for c in CONTEXTS[shape.name] if c > args.ctx] if not args.quick else []
     total = max([args.ctx + 2 * (args.warmup + args.steps) + args.e2e_steps + 2] +
-                [c + args.decode_steps + 2 for c in ctxs])
+                [c + 2 * args.decode_steps + 16 for c in ctxs])  # room for the sampled steps after the last
     n_blocks = (total + bs - 1) // bs + 1
     max_pos = n_blocks * bs
     stream = torch.cuda.Stream()  # the context's stream: events are recorded on it
@@ -578,6 +639,7 @@ def run_mie(args, shape):
                 torch, synth.TINYLLAMA, CONTEXTS["tinyllama-1.1b"], args.decode_steps, peak, read_peak,
                 "tinyllama-1.1b q4_0 (bf16 GEMV inputs) batch-1 decode"))
             extras["slots"] = guarded(lambda: slots_summary(measure_slots(args, torch)))
+            extras["batched_passes"] = guarded(lambda: batched_passes(torch))
             extras["kernel_sweep"] = guarded(lambda: measure_sweep(args, clocks=False))
         cpu = None
         if not args.no_cpu_baseline and world == 1:
