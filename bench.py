@@ -87,6 +87,16 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+def measured_bf16_peak() -> float:
+    """Dense bf16 tensor TFLOP/s: the driver's burst cuBLAS measurement, else the
+    profiling recipe's fallback of 1.9 PFLOP/s."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f).get("bf16_tflops", 1900.0))
+    return 1900.0
+
+
 class Clocks:
     """Samples nvidia-smi every 200 ms while the timed region runs."""
 
@@ -427,28 +437,91 @@ def sampled_steps(torch, gm, stream, bt, logits, am, pos: int, tok: int, steps: 
             "ms_per_step": dt * 1e3, "launches_per_step": gm.launches}
 
 
-def batched_passes(torch, n_prompt: int = 2048, n_spec_prompt: int = 256, n_new: int = 128) -> dict:
-    """Llama-3.2-1B bf16 through the few-slot kernels (mie_generate): prefill of an
-    n_prompt-token prompt in passes of 8 positions (each pass reads the weights once), and
-    greedy generation after a prompt that repeats a 64-token pattern, with prompt-lookup
-    speculation (up to 3 guesses a pass) and without; the two give the same tokens."""
+GEMM_SHAPES = [("qkv", 3072, 2048), ("o", 2048, 2048), ("gate_up", 16384, 2048), ("down", 2048, 8192)]
+
+
+def prefill_measure(torch, bf16_peak: float, n_prompt: int = 2048, chunk: int = 512) -> dict:
+    """Prompt prefill on the tensor cores (mie_prefill) at the Llama-3.2-1B shape with bf16
+    weights: an n_prompt-token prompt (chunks of 512 positions), timed with events on the
+    model's stream; and the tcgen05 GEMM alone at the four layer shapes for one chunk
+    (three activation planes: three MMAs per product), graph-timed over copies of the
+    weights larger than L2, against the measured bf16 tensor peak."""
+    from memory_bound_decode_dequant_gb300.workload import build_gpu_model
+    import memory_bound_decode_dequant_gb300 as mie
+    shape = synth.llama32_1b("bf16")
+    bs = shape.block_size
+    n_blocks = (n_prompt + bs - 1) // bs + 2
+    stream = torch.cuda.Stream()
+    gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=n_blocks * bs, stream=stream)
+    bt = torch.from_numpy(synth.permutation(0x5046, n_blocks).astype(np.int32)).cuda()
+    toks = [int(t) for t in shape.tokens(n_prompt, stream=14)]
+    gm.prefill(toks[:64], 0, bt)  # buffers
+    gm.sync()
+    times = []
+    for _ in range(3):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        gm.prefill(toks, 0, bt)
+        e1.record(stream)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / 1e3)
+    gm.sync()
+    gm.close()
+    del gm
+    dt = statistics.median(times)
+    L, d, f = shape.n_layers, shape.d_model, shape.ffn
+    na = shape.n_heads * shape.head_dim
+    qkv = shape.qkv_rows * d
+    per_tok = 2 * (L * qkv + (L - 1) * (d * na + 2 * f * d + d * f))  # the last layer stops after K/V
+    attn = (L - 1) * 4 * na * n_prompt * (n_prompt + 1) / 2  # causal QK^T and PV
+    flops = per_tok * n_prompt + attn
+    out = {"workload": f"llama-3.2-1b bf16 prompt prefill, {n_prompt} tokens", "chunk": chunk,
+           "ms": dt * 1e3, "tok_s": n_prompt / dt, "useful_tflops": flops / dt / 1e12,
+           "kernels": "tcgen05 GEMM (TMA, TMEM accumulators, 3 bf16 activation planes) + mma.sync flash attention",
+           "method": "CUDA events on the model's stream around mie_prefill, median of 3"}
+    gemms = []
+    for name, N, K in GEMM_SHAPES:
+        nbytes = N * K * 2
+        copies = max(2, int(np.ceil(300e6 / nbytes)))
+        Ws = [torch.randn(N, K, device="cuda").mul_(0.02).to(torch.bfloat16) for _ in range(copies)]
+        x = torch.randn(chunk, K, device="cuda")
+        planes = mie.mie_split_bf16(x)
+        y = torch.empty(chunk, N, device="cuda")
+        n_launch = 4 * copies
+        t = graph_time(torch, [lambda st, W=Ws[i % copies]: mie.mie_gemm_bf16(W, planes, y, stream=st)
+                               for i in range(n_launch)])
+        useful = 2.0 * N * K * chunk / t / 1e12
+        tensor = 3 * useful
+        gemms.append({"gemm": name, "N": N, "K": K, "T": chunk, "us": t * 1e6, "useful_tflops": useful,
+                      "tensor_tflops": tensor, "frac_of_bf16_peak": tensor / bf16_peak,
+                      "weight_copies": copies})
+        del Ws, x, planes, y
+    torch.cuda.empty_cache()
+    top = max(gemms, key=lambda g: g["us"])
+    out["gemm"] = gemms
+    out["roofline"] = {"bound": "tensor", "kernel": f"gemm_tc_kernel ({top['gemm']} {top['N']}x{top['K']}, "
+                                                    f"T = {chunk})",
+                       "achieved": top["tensor_tflops"], "peak": bf16_peak, "peak_kind": "measured (burst)",
+                       "unit": "TFLOP/s", "frac": top["tensor_tflops"] / bf16_peak,
+                       "note": "tensor-pipe rate: three bf16 MMAs per product (hi, mid, lo planes)"}
+    return out
+
+
+def batched_passes(torch, n_spec_prompt: int = 256, n_new: int = 128) -> dict:
+    """Llama-3.2-1B bf16 through the few-slot kernels: greedy generation (mie_generate)
+    after a prompt that repeats a 64-token pattern, with prompt-lookup speculation (up to
+    3 guesses a pass) and without (the two give the same tokens), and the cost of one
+    verify pass over k positions against k passes of one."""
     from memory_bound_decode_dequant_gb300.workload import build_gpu_model
     shape = synth.llama32_1b("bf16")
     bs = shape.block_size
-    n_blocks = (max(n_prompt, n_spec_prompt + n_new) + bs - 1) // bs + 2
+    n_blocks = (n_spec_prompt + n_new + bs - 1) // bs + 2
     stream = torch.cuda.Stream()
     gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=n_blocks * bs, max_slots=8, stream=stream)
     bt = torch.from_numpy(synth.permutation(0x5045, n_blocks).astype(np.int32)).cuda()
     out = {"model": "llama-3.2-1b bf16", "kernels": "few-slot step (mma.sync, bf16 hi + lo inputs)"}
-    prompt = [int(t) for t in shape.tokens(n_prompt, stream=11)]
-    gm.generate(prompt[:40], 1, bt, 1)  # captures the few-slot graph
+    gm.generate([int(t) for t in shape.tokens(40, stream=11)], 1, bt, 1)  # captures the few-slot graph
     torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    _, st = gm.generate(prompt, 1, bt, 1)
-    dt = time.perf_counter() - t0
-    out["prefill"] = {"prompt_tokens": n_prompt, "positions_per_pass": 8, "seconds": dt,
-                      "tok_s": (n_prompt - 1) / dt, "passes": st["passes"],
-                      "note": "wall time through mie_generate, the last prompt token's pass and one generated token included"}
     pattern = [int(t) for t in shape.tokens(64, stream=12)]
     rep = (pattern * (n_spec_prompt // 64 + 1))[:n_spec_prompt]
     res = {}
@@ -640,6 +713,7 @@ def run_mie(args, shape):
                 "tinyllama-1.1b q4_0 (bf16 GEMV inputs) batch-1 decode"))
             extras["slots"] = guarded(lambda: slots_summary(measure_slots(args, torch)))
             extras["batched_passes"] = guarded(lambda: batched_passes(torch))
+            extras["prefill"] = guarded(lambda: prefill_measure(torch, measured_bf16_peak()))
             extras["kernel_sweep"] = guarded(lambda: measure_sweep(args, clocks=False))
         cpu = None
         if not args.no_cpu_baseline and world == 1:

@@ -140,6 +140,30 @@ mie_status mie_gemv_q4_0(const void *packed, const float *x, float *y, int M, in
 mie_status mie_gemv_q4(const void *packed, int group, const float *x, float *y, int M, int K,
                        void *stream);
 
+/* ============================================================ prompt GEMM (tcgen05) */
+
+/* Cuts x[0..n) (device fp32) into bf16 planes hi = bf16(x), mid = bf16(x - hi),
+ * lo = bf16(x - hi - mid) (round to nearest even; both differences are exact in fp32),
+ * the activation operand of mie_gemm_bf16: hi + mid + lo is x to 2^-25 of x, and every
+ * product of a plane with a bf16 weight is exact in fp32.  mid and lo may be NULL.
+ * 1 <= n < 2^31. */
+mie_status mie_split_bf16(const float *x, int64_t n, uint16_t *hi, uint16_t *mid, uint16_t *lo, void *stream);
+
+/* The prompt's matrix-matrix product on the tensor cores ([INFER] summary table and
+ * "Limitations": prefill multiplies every weight matrix by all prompt positions at once,
+ * a dense contraction that tensor cores make several times faster than the CUDA-core
+ * path):
+ *   y[t * ldy + n] (+)= sum_k W[n][k] * (x_hi + x_mid + x_lo)[t][k],  t < T, n < N,
+ * on tcgen05 (M = 128 weight rows x N = 128 positions per CTA, operands staged by TMA
+ * with 128-byte swizzle, accumulators in tensor memory, drained every 128 columns of K
+ * into fp32 registers).  W: device bf16 [N][K] row-major; x_hi, x_mid, x_lo: device bf16
+ * [T][K] planes (mie_split_bf16; x_mid and x_lo NULL: x_hi alone; x_lo NULL: hi + mid);
+ * y: device fp32, rows ldy >= N floats apart; accumulate != 0 adds to y.  Pointers
+ * 16-byte aligned, K % 8 == 0 (MIE_E_SHAPE otherwise).  A device-side wait that gives
+ * up is latched as a device error (mie_check). */
+mie_status mie_gemm_bf16(const uint16_t *W, int N, int K, const uint16_t *x_hi, const uint16_t *x_mid,
+                         const uint16_t *x_lo, int T, float *y, int64_t ldy, int accumulate, void *stream);
+
 /* ======================================================================= attention */
 
 /* Workspace bytes that mie_paged_attn_decode needs for these sizes. */
@@ -190,6 +214,21 @@ mie_status mie_paged_attn_decode_noalloc(const float *q, const uint16_t *k_pool,
                                          int n_table, int ctx_len, int n_q_heads, int n_kv_heads,
                                          int head_dim, int block_size, float scale, float *out,
                                          void *stream);
+
+/* Causal paged GQA attention of T consecutive positions pos0 .. pos0 + T - 1 of one
+ * sequence, whose K/V (and those of every earlier position) are already in the cache
+ * ([INFER] "Limitations": the prompt's flash-style attention; [MIE] "The KV cache, paged
+ * like virtual memory"):
+ *   out[t][h][d] = sum_{p <= pos0 + t} softmax_p(scale * q[t][h] . k_{g,p}) v_{g,p}[d],
+ * the cache addressed as in mie_paged_attn_decode.  q, out: device fp32 [T][n_q_heads]
+ * [head_dim]; block_table: device int32 [n_table] with pos0 + T <= n_table * block_size.
+ * head_dim in {32, 64, 128}, block_size dividing 64.  Runs on mma.sync with q and the
+ * probabilities as three bf16 planes each.  A block-table entry outside [0, n_pool_blocks)
+ * is read as block 0 and latched as a device error (mie_check). */
+mie_status mie_paged_attn_prefill(const float *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                                  int64_t block_stride, int n_pool_blocks, const int32_t *block_table,
+                                  int n_table, int pos0, int T, int n_q_heads, int n_kv_heads,
+                                  int head_dim, int block_size, float scale, float *out, void *stream);
 
 /* ========================================================================== argmax */
 
@@ -405,10 +444,29 @@ void mie_spec_gate_init(mie_spec_gate *g, int window, float threshold, int pause
 int mie_spec_gate_open(mie_spec_gate *g);  /* 1: this pass may guess (a paused gate counts it off) */
 void mie_spec_gate_record(mie_spec_gate *g, int proposed, int accepted);
 
-/* Greedy generation through the few-slot kernels.  ids: host int32 [n_prompt + n_new];
- * ids[0..n_prompt) is the prompt, ids[n_prompt..) receives the n_new generated tokens.
- * The prompt but its last token is processed max_slots positions per pass (prefill by
- * batched passes); each later pass takes the last token and, with spec_max > 1, up to
+/* Prompt prefill on the tensor cores ([INFER] summary table and "Limitations": the
+ * prompt as matrix-matrix products instead of one decode step per token).  Runs the n
+ * tokens tokens[0..n) (host int32) at positions pos0 .. pos0 + n - 1 of one sequence
+ * through every layer, in chunks of up to 512 positions -- RMSNorm, the QKV product
+ * (mie_gemm_bf16's kernel; int8 and 4-bit matrices are first expanded to bf16 planes),
+ * RoPE, the K/V write into the paged cache through block_table (device int32
+ * [n_blocks]), causal attention (mie_paged_attn_prefill's kernel), the O product, the
+ * MLP -- and leaves their K/V in every layer's cache; the last layer stops after its K/V
+ * write.  It produces no logits: the decode step of the next position (the prompt's last
+ * token) does.  Activations enter the products as three bf16 planes (bf16 alone for
+ * act_bf16 models), so the cache matches the decode step's to within rounding of the
+ * summation order.  Asynchronous on the context's stream; the buffers (about 60 MB at
+ * the Llama-3.2-1B shape, plus the largest weight matrix as bf16 planes for quantised
+ * models) are allocated on the first call.  MIE_E_ARG for a token outside [0, vocab) or
+ * positions outside [0, max_pos) or the table; device bounds checks are reported by the
+ * next mie_sync. */
+mie_status mie_prefill(mie_ctx *ctx, const int32_t *tokens, int n, int32_t pos0, const int32_t *block_table,
+                       int n_blocks);
+
+/* Greedy generation.  ids: host int32 [n_prompt + n_new]; ids[0..n_prompt) is the
+ * prompt, ids[n_prompt..) receives the n_new generated tokens.  The prompt but its last
+ * token goes through mie_prefill; each later pass, through the few-slot kernels, takes
+ * the last token and, with spec_max > 1, up to
  * spec_max - 1 prompt-lookup guesses (2- to 4-token matches, behind the acceptance gate
  * of 10 attempts / 30 % / pauses of 5 .. 80 passes), verifies them in one mie_verify_step
  * and keeps the guesses up to the first the model disagrees with, plus the model's own

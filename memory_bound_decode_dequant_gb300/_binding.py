@@ -21,7 +21,7 @@ __all__ = ["lib", "MieError", "FMT", "LIB_PATH", "exported_names", "header_funct
            "mie_q4_0_packed_bytes", "mie_gemv_bf16", "mie_gemv_i8", "mie_gemv_q4_0",
            "mie_quantize_q4", "mie_q4_packed_bytes", "mie_q4_pack", "mie_gemv_q4", "Q4_GROUP",
            "mie_paged_attn_decode", "mie_paged_attn_workspace_bytes", "mie_paged_attn_decode_noalloc",
-           "mie_argmax",
+           "mie_argmax", "mie_split_bf16", "mie_gemm_bf16", "mie_paged_attn_prefill",
            "mie_argmax_workspace_bytes", "mie_check", "mie_hbm_read_probe", "mie_sample", "mie_sample_workspace_bytes", "Pool", "Config", "Model",
            "DeviceArray"]
 
@@ -59,6 +59,10 @@ _SIGS = {
     "mie_gemv_i8": (I, [P, P, P, P, I, I, P]),
     "mie_gemv_q4_0": (I, [P, P, P, I, I, P]),
     "mie_gemv_q4": (I, [P, I, P, P, I, I, P]),
+    "mie_split_bf16": (I, [P, I64, P, P, P, P]),
+    "mie_gemm_bf16": (I, [P, I, I, P, P, P, I, P, I64, I, P]),
+    "mie_paged_attn_prefill": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, I, F, P, P]),
+    "mie_prefill": (I, [P, P, I, ctypes.c_int32, P, I]),
     "mie_paged_attn_workspace_bytes": (SZ, [I, I, I, I, I]),
     "mie_paged_attn_decode": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, F, P, P, SZ, P]),
     "mie_paged_attn_decode_noalloc": (I, [P, P, P, I64, I, P, I, I, I, I, I, I, F, P, P]),
@@ -267,6 +271,45 @@ def mie_gemv_q4_0(packed, x, M: int, K: int, y=None, stream=None):
     _check(lib().mie_gemv_q4_0(_dev(packed, torch.uint8, "packed"), _dev(x, torch.float32, "x"),
                                _dev(y, torch.float32, "y"), M, K, _stream(stream)), "mie_gemv_q4_0")
     return y
+
+
+def mie_split_bf16(x, planes: int = 3, stream=None):
+    """x (fp32, any shape) -> list of `planes` (1 to 3) bf16 planes hi, mid, lo of x."""
+    torch = _torch()
+    out = [torch.empty(x.shape, dtype=torch.bfloat16, device=x.device) for _ in range(planes)]
+    ptr = [_dev(p, torch.bfloat16, "plane") for p in out] + [None] * (3 - planes)
+    _check(lib().mie_split_bf16(_dev(x, torch.float32, "x"), x.numel(), ptr[0], ptr[1], ptr[2], _stream(stream)),
+           "mie_split_bf16")
+    return out
+
+
+def mie_gemm_bf16(W, planes, y=None, accumulate: bool = False, stream=None):
+    """y[t][n] (+)= sum_k W[n][k] (sum of the planes)[t][k] on the tensor cores; W [N][K],
+    planes: 1 to 3 bf16 [T][K] tensors (hi, mid, lo); y [T][ldy >= N] fp32."""
+    torch = _torch()
+    N, K = W.shape
+    T = planes[0].shape[0]
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.float32, device=W.device)
+    ptr = [_dev(p, torch.bfloat16, "plane") for p in planes] + [None] * (3 - len(planes))
+    _check(lib().mie_gemm_bf16(_dev(W, torch.bfloat16, "W"), N, K, ptr[0], ptr[1], ptr[2], T,
+                               _dev(y, torch.float32, "y"), y.stride(0), int(bool(accumulate)), _stream(stream)),
+           "mie_gemm_bf16")
+    return y
+
+
+def mie_paged_attn_prefill(q, k_pool, v_pool, block_stride: int, n_pool_blocks: int, block_table,
+                           pos0: int, Hq: int, Hkv: int, hd: int, bs: int, scale: float, out=None, stream=None):
+    """Causal attention of the T = q.shape[0] positions pos0 .. pos0+T-1; q [T][Hq*hd] fp32."""
+    torch = _torch()
+    T = q.shape[0]
+    if out is None:
+        out = torch.empty((T, Hq * hd), dtype=torch.float32, device=q.device)
+    _check(lib().mie_paged_attn_prefill(
+        _dev(q, torch.float32, "q"), _dev(k_pool, None, "k_pool"), _dev(v_pool, None, "v_pool"), block_stride,
+        n_pool_blocks, _dev(block_table, torch.int32, "block_table"), block_table.numel(), pos0, T, Hq, Hkv, hd, bs,
+        scale, _dev(out, torch.float32, "out"), _stream(stream)), "mie_paged_attn_prefill")
+    return out
 
 
 def mie_paged_attn_workspace_bytes(Hq, Hkv, hd, ctx_len, bs) -> int:
@@ -530,9 +573,18 @@ class Model:
                                      None if argmax_out is None else _dev(argmax_out, torch.int32, "argmax")),
                "mie_verify_step")
 
+    def prefill(self, tokens, pos0: int, block_table):
+        """K/V of the host tokens at positions pos0 .. pos0+n-1 into the cache, on the
+        tensor cores (no logits: the next decode step gives them)."""
+        torch = _torch()
+        t = np.ascontiguousarray(tokens, dtype=np.int32)
+        _check(lib().mie_prefill(self.h, t.ctypes.data, t.size, int(pos0),
+                                 _dev(block_table, torch.int32, "block_table"), block_table.numel()),
+               "mie_prefill")
+
     def generate(self, prompt, n_new: int, block_table, spec_max: int = 1):
-        """Greedy generation through the few-slot kernels (speculative for spec_max > 1);
-        returns (generated tokens, {passes, proposed, accepted})."""
+        """Greedy generation (prompt through mie_prefill, then few-slot passes, speculative
+        for spec_max > 1); returns (generated tokens, {passes, proposed, accepted})."""
         torch = _torch()
         ids = np.zeros(len(prompt) + n_new, np.int32)
         ids[: len(prompt)] = prompt
@@ -701,6 +753,10 @@ def mie_verify_step(ctx: Model, tokens, pos: int, block_table, logits_out=None, 
     ctx.verify_step(tokens, pos, block_table, logits_out, argmax_out)
 
 
+def mie_prefill(ctx: Model, tokens, pos0: int, block_table) -> None:
+    ctx.prefill(tokens, pos0, block_table)
+
+
 def mie_generate(ctx: Model, prompt, n_new: int, block_table, spec_max: int = 1):
     return ctx.generate(prompt, n_new, block_table, spec_max)
 
@@ -760,6 +816,6 @@ __all__ += ["mie_last_error", "mie_status_string", "mie_pool_create", "mie_pool_
             "mie_pool_writable", "mie_create", "mie_destroy", "mie_load_weights", "mie_ctx_pool",
             "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_kv_writable", "mie_decode_step",
             "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
-            "mie_set_trace", "mie_set_sampling", "mie_debug_stall", "mie_sync", "mie_verify_step", "mie_generate",
+            "mie_set_trace", "mie_set_sampling", "mie_debug_stall", "mie_sync", "mie_verify_step", "mie_prefill", "mie_generate",
             "mie_lookup_propose", "SpecGate", "mie_spec_gate_bytes", "mie_spec_gate_init", "mie_spec_gate_open",
             "mie_spec_gate_record", "mie_step_launches", "mie_slot_step_launches"]

@@ -1,6 +1,8 @@
 // internal.h -- host-side interfaces shared by the translation units of libmie.so.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace mie {
@@ -105,6 +107,60 @@ size_t attn_workspace_bytes(int Hq, int Hkv, int hd, int n_splits);
 size_t attn_counter_bytes(int Hkv);  // the counters at the start of a workspace
 int attn_splits_for(int Hkv, int max_ctx, int bs);
 mie_status launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl);
+
+// Prompt GEMM on tcgen05 (gemm.cu): Y[t][n] (+)= s[n] * sum_k (A0 + A1)[n][k] (B0 + B1 + B2)[t][k]
+// with bf16 planes A (weight rows) and B (activation rows) behind 2-D tensor maps
+// (make_bf16_map: 64-column x 128-row boxes, 128-byte swizzle, zeros outside).
+struct GemmPlan {
+  CUtensorMap a[2], b[3];
+  int na = 1, nb = 1;  // planes in use: na 1 or 2, nb 1 to 3
+  int T = 0, N = 0, K = 0;
+  float *y = nullptr;
+  int64_t ldy = 0;
+  const float *row_scale = nullptr;
+  bool accumulate = false;
+  int *err = nullptr;
+};
+mie_status make_bf16_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t pitch);
+mie_status launch_gemm(const GemmPlan &p, cudaStream_t st);
+
+// The prompt's row-wise kernels and attention (prefill.cu).
+struct RopeKvArgs {
+  const float *Y = nullptr;  // [T][ldy] QKV product rows in the step's pair order
+  int64_t ldy = 0;
+  int T = 0, pos0 = 0;
+  const float *cos_t = nullptr, *sin_t = nullptr;
+  int Hq = 0, Hkv = 0, hd = 0, bs = 0;
+  uint16_t *kv_layer = nullptr;  // this layer's K half of block 0; V follows after Hkv*bs*hd
+  int64_t block_stride = 0;
+  const int32_t *bt = nullptr;
+  int n_table = 0, n_pool = 0;
+  float *Q = nullptr;  // [T][Hq*hd]
+  int *err = nullptr;
+};
+struct PrefillAttnArgs {
+  const float *q = nullptr;  // [T][ldq]
+  int64_t ldq = 0;
+  const uint16_t *k = nullptr, *v = nullptr;  // this layer's K and V bases
+  int64_t block_stride = 0;
+  int n_pool = 0;
+  const int32_t *bt = nullptr;
+  int pos0 = 0, T = 0, Hq = 0, Hkv = 0, hd = 0, bs = 0;
+  float scale = 0.f;
+  float *out = nullptr;  // [T][ldo]
+  int64_t ldo = 0;
+  int *err = nullptr;
+};
+mie_status launch_embed_rows(const DevMat &e, const int32_t *tok, int T, int vocab, int d, float *R, int *err,
+                             cudaStream_t st);
+// The row-wise kernels write their output as bf16 planes hi / mid / lo (mid, lo nullable).
+mie_status launch_norm_split(const float *x, int64_t ldx, int K, const float *g, float eps, int act_bf16, int T,
+                             uint16_t *hi, uint16_t *mid, uint16_t *lo, int64_t ldp, cudaStream_t st);
+mie_status launch_rope_kv(const RopeKvArgs &a, cudaStream_t st);
+mie_status launch_swiglu_split(const float *Y, int64_t ldy, int F, int act_bf16, int T, uint16_t *hi, uint16_t *mid,
+                               uint16_t *lo, int64_t ldp, cudaStream_t st);
+mie_status launch_dequant_planes(const DevMat &m, uint16_t *hi, uint16_t *lo, int64_t ldp, cudaStream_t st);
+mie_status launch_prefill_attn(const PrefillAttnArgs &a, cudaStream_t st);
 
 // Rounds after which a bounded device-side wait gives up (a few seconds).
 constexpr long kWaitPolls = 1L << 22;

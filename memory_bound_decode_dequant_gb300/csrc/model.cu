@@ -145,6 +145,13 @@ struct mie_ctx {
   int32_t *verify_table = nullptr;  // [kMaxSlots][verify_cap] copies of one sequence's table
   int verify_cap = 0;
   int32_t *gen_argmax = nullptr;    // [kMaxSlots]
+  // prompt prefill on the tensor cores (mie_prefill): buffers for chunks of up to
+  // prefill_chunk positions, allocated on the first call
+  int prefill_chunk = 0;
+  int64_t prefill_ldp = 0;      // elements per row of the bf16 activation planes
+  float *pf_R = nullptr, *pf_Y = nullptr, *pf_Q = nullptr, *pf_O = nullptr;
+  uint16_t *pf_xh = nullptr, *pf_xm = nullptr, *pf_xl = nullptr, *pf_wh = nullptr, *pf_wl = nullptr;
+  int32_t *pf_tok = nullptr;
   // few-slot step: its own phase list and graph (always the kernel chain)
   std::vector<Phase> slot_phases;
   cudaGraphExec_t slot_graph = nullptr;
@@ -977,6 +984,173 @@ extern "C" mie_status mie_verify_step(mie_ctx *ctx, const int32_t *tokens, int n
 }
 
 // Greedy generation through the few-slot kernels, speculative when spec_max > 1.
+// ------------------------------------------------------------------ prefill
+
+static constexpr int kPrefillChunk = 512;
+
+static mie_status prefill_alloc(mie_ctx *ctx) {
+  if (ctx->pf_R) return MIE_OK;
+  const mie_config &c = ctx->cfg;
+  const int T = std::min(kPrefillChunk, c.max_pos);
+  const int64_t na = (int64_t)c.n_heads * c.head_dim, nqkv = (int64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int64_t kmax = std::max<int64_t>(std::max<int64_t>(c.d_model, c.ffn), na);
+  ctx->prefill_ldp = (kmax + 7) / 8 * 8;
+  const int64_t ny = std::max<int64_t>(nqkv, 2 * (int64_t)c.ffn);
+  ctx->pf_R = (float *)ctx->dalloc(sizeof(float) * T * c.d_model);
+  ctx->pf_Y = (float *)ctx->dalloc(sizeof(float) * T * ny);
+  ctx->pf_Q = (float *)ctx->dalloc(sizeof(float) * T * na);
+  ctx->pf_O = (float *)ctx->dalloc(sizeof(float) * T * na);
+  ctx->pf_xh = (uint16_t *)ctx->dalloc(2 * T * ctx->prefill_ldp);
+  ctx->pf_xm = (uint16_t *)ctx->dalloc(2 * T * ctx->prefill_ldp);
+  ctx->pf_xl = (uint16_t *)ctx->dalloc(2 * T * ctx->prefill_ldp);
+  ctx->pf_tok = (int32_t *)ctx->dalloc(sizeof(int32_t) * T);
+  bool ok = ctx->pf_R && ctx->pf_Y && ctx->pf_Q && ctx->pf_O && ctx->pf_xh && ctx->pf_xm && ctx->pf_xl && ctx->pf_tok;
+  if (ok && c.wfmt != MIE_FMT_BF16) {  // the largest layer matrix as bf16 planes
+    size_t most = 0;
+    for (const Layer &L : ctx->layers)
+      for (const DevMat *m : {&L.qkv, &L.o, &L.gu, &L.down})
+        most = std::max(most, (size_t)m->rows * (size_t)((m->cols + 7) / 8 * 8));
+    ctx->pf_wh = (uint16_t *)ctx->dalloc(2 * most);
+    ctx->pf_wl = (uint16_t *)ctx->dalloc(2 * most);
+    ok = ctx->pf_wh && ctx->pf_wl;
+  }
+  if (!ok) {
+    ctx->pf_R = nullptr;  // the buffers stay with the context and are freed with it
+    return fail(MIE_E_OOM, "mie_prefill: device buffers");
+  }
+  ctx->prefill_chunk = T;
+  return MIE_OK;
+}
+
+// y[t][n] (+)= (W x_t)[n] for the T rows of the activation planes, on the tensor cores;
+// quantised weights are first expanded to bf16 planes.
+static mie_status prefill_gemm(mie_ctx *ctx, const DevMat &m, int T, float *y, int64_t ldy, bool accumulate) {
+  cudaStream_t st = ctx->stream;
+  GemmPlan p;
+  p.T = T;
+  p.N = m.rows;
+  p.K = m.cols;
+  p.y = y;
+  p.ldy = ldy;
+  p.accumulate = accumulate;
+  p.err = ctx->err;
+  p.nb = ctx->cfg.act_bf16 ? 1 : 3;
+  mie_status s;
+  if (m.fmt == MIE_FMT_BF16) {
+    p.na = 1;
+    s = make_bf16_map(&p.a[0], m.w, m.rows, m.cols, m.row_bytes);
+  } else {
+    const int64_t ld = (m.cols + 7) / 8 * 8;
+    p.na = m.fmt == MIE_FMT_I8 ? 1 : 2;
+    if (m.fmt == MIE_FMT_I8) p.row_scale = reinterpret_cast<const float *>(m.s);
+    s = launch_dequant_planes(m, ctx->pf_wh, p.na == 2 ? ctx->pf_wl : nullptr, ld, st);
+    if (s == MIE_OK) s = make_bf16_map(&p.a[0], ctx->pf_wh, m.rows, m.cols, ld * 2);
+    if (s == MIE_OK && p.na == 2) s = make_bf16_map(&p.a[1], ctx->pf_wl, m.rows, m.cols, ld * 2);
+  }
+  if (s == MIE_OK) s = make_bf16_map(&p.b[0], ctx->pf_xh, T, m.cols, ctx->prefill_ldp * 2);
+  if (s == MIE_OK && p.nb == 3) s = make_bf16_map(&p.b[1], ctx->pf_xm, T, m.cols, ctx->prefill_ldp * 2);
+  if (s == MIE_OK && p.nb == 3) s = make_bf16_map(&p.b[2], ctx->pf_xl, T, m.cols, ctx->prefill_ldp * 2);
+  if (s != MIE_OK) return s;
+  return launch_gemm(p, st);
+}
+
+// One chunk of T prompt positions pos0 .. pos0 + T - 1 through every layer.  The last
+// layer stops after its K/V write: nothing of a prompt position beyond its K/V is kept.
+static mie_status prefill_chunk(mie_ctx *ctx, const int32_t *tokens, int T, int pos0, const int32_t *bt,
+                                int n_table) {
+  const mie_config &c = ctx->cfg;
+  cudaStream_t st = ctx->stream;
+  const int64_t half = (int64_t)c.n_kv_heads * c.block_size * c.head_dim;
+  const int64_t na = (int64_t)c.n_heads * c.head_dim, nqkv = (int64_t)(c.n_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int64_t ldp = ctx->prefill_ldp;
+  uint16_t *xm = c.act_bf16 ? nullptr : ctx->pf_xm, *xl = c.act_bf16 ? nullptr : ctx->pf_xl;
+  mie_status s;
+  MIE_CUDA(cudaMemcpyAsync(ctx->pf_tok, tokens, sizeof(int32_t) * T, cudaMemcpyHostToDevice, st));
+  if ((s = launch_embed_rows(ctx->embed, ctx->pf_tok, T, c.vocab, c.d_model, ctx->pf_R, ctx->err, st)) != MIE_OK)
+    return s;
+  for (int l = 0; l < c.n_layers; ++l) {
+    const Layer &L = ctx->layers[(size_t)l];
+    uint16_t *kv_layer = ctx->kv + (int64_t)l * 2 * half;
+    if ((s = launch_norm_split(ctx->pf_R, c.d_model, c.d_model, L.attn_norm, c.rms_eps, c.act_bf16, T, ctx->pf_xh, xm,
+                               xl, ldp, st)) != MIE_OK)
+      return s;
+    if ((s = prefill_gemm(ctx, L.qkv, T, ctx->pf_Y, nqkv, false)) != MIE_OK) return s;
+    RopeKvArgs r;
+    r.Y = ctx->pf_Y;
+    r.ldy = nqkv;
+    r.T = T;
+    r.pos0 = pos0;
+    r.cos_t = ctx->rope_cos;
+    r.sin_t = ctx->rope_sin;
+    r.Hq = c.n_heads;
+    r.Hkv = c.n_kv_heads;
+    r.hd = c.head_dim;
+    r.bs = c.block_size;
+    r.kv_layer = kv_layer;
+    r.block_stride = ctx->block_elems;
+    r.bt = bt;
+    r.n_table = n_table;
+    r.n_pool = c.n_kv_blocks;
+    r.Q = ctx->pf_Q;
+    r.err = ctx->err;
+    if ((s = launch_rope_kv(r, st)) != MIE_OK) return s;
+    if (l == c.n_layers - 1) break;
+    PrefillAttnArgs a;
+    a.q = ctx->pf_Q;
+    a.ldq = na;
+    a.k = kv_layer;
+    a.v = kv_layer + half;
+    a.block_stride = ctx->block_elems;
+    a.n_pool = c.n_kv_blocks;
+    a.bt = bt;
+    a.pos0 = pos0;
+    a.T = T;
+    a.Hq = c.n_heads;
+    a.Hkv = c.n_kv_heads;
+    a.hd = c.head_dim;
+    a.bs = c.block_size;
+    a.scale = (float)(1.0 / std::sqrt((double)c.head_dim));
+    a.out = ctx->pf_O;
+    a.ldo = na;
+    a.err = ctx->err;
+    if ((s = launch_prefill_attn(a, st)) != MIE_OK) return s;
+    if ((s = launch_norm_split(ctx->pf_O, na, (int)na, nullptr, 0.f, c.act_bf16, T, ctx->pf_xh, xm, xl, ldp, st)) != MIE_OK)
+      return s;
+    if ((s = prefill_gemm(ctx, L.o, T, ctx->pf_R, c.d_model, true)) != MIE_OK) return s;
+    if ((s = launch_norm_split(ctx->pf_R, c.d_model, c.d_model, L.mlp_norm, c.rms_eps, c.act_bf16, T, ctx->pf_xh, xm,
+                               xl, ldp, st)) != MIE_OK)
+      return s;
+    if ((s = prefill_gemm(ctx, L.gu, T, ctx->pf_Y, 2 * (int64_t)c.ffn, false)) != MIE_OK) return s;
+    if ((s = launch_swiglu_split(ctx->pf_Y, 2 * (int64_t)c.ffn, c.ffn, c.act_bf16, T, ctx->pf_xh, xm, xl, ldp, st)) !=
+        MIE_OK)
+      return s;
+    if ((s = prefill_gemm(ctx, L.down, T, ctx->pf_R, c.d_model, true)) != MIE_OK) return s;
+  }
+  return MIE_OK;
+}
+
+extern "C" mie_status mie_prefill(mie_ctx *ctx, const int32_t *tokens, int n, int32_t pos0, const int32_t *block_table,
+                                  int n_blocks) {
+  if (!ctx || !tokens || !block_table) return fail(MIE_E_ARG, "mie_prefill: null pointer");
+  const mie_config &c = ctx->cfg;
+  if (!all_loaded(ctx)) return fail(MIE_E_STATE, "mie_prefill: not every weight is loaded");
+  if (n < 0 || pos0 < 0 || (int64_t)pos0 + n > c.max_pos)
+    return fail(MIE_E_ARG, "mie_prefill: positions %d .. %d outside [0, %d)", pos0, pos0 + n - 1, c.max_pos);
+  if (n == 0) return MIE_OK;
+  if (n_blocks < 1 || (int64_t)(pos0 + n - 1) / c.block_size >= n_blocks)
+    return fail(MIE_E_ARG, "mie_prefill: position %d needs more than %d blocks", pos0 + n - 1, n_blocks);
+  for (int i = 0; i < n; ++i)
+    if (tokens[i] < 0 || tokens[i] >= c.vocab)
+      return fail(MIE_E_ARG, "mie_prefill: token %d outside [0, %d)", tokens[i], c.vocab);
+  mie_status s = prefill_alloc(ctx);
+  if (s != MIE_OK) return s;
+  for (int p = 0; p < n; p += ctx->prefill_chunk) {
+    const int T = std::min(ctx->prefill_chunk, n - p);
+    if ((s = prefill_chunk(ctx, tokens + p, T, pos0 + p, block_table, n_blocks)) != MIE_OK) return s;
+  }
+  return MIE_OK;
+}
+
 extern "C" mie_status mie_generate(mie_ctx *ctx, int32_t *ids, int n_prompt, int n_new, const int32_t *block_table,
                                    int max_blocks, int spec_max, int *stats) {
   if (!ctx || !ids || !block_table) return fail(MIE_E_ARG, "mie_generate: null pointer");
@@ -990,12 +1164,8 @@ extern "C" mie_status mie_generate(mie_ctx *ctx, int32_t *ids, int n_prompt, int
     return fail(MIE_E_OOM, "mie_generate: argmax buffer");
   int passes = 0, proposed = 0, accepted = 0;
   mie_status s;
-  // the prompt but its last token, up to max_slots positions a pass
-  for (int p0 = 0; p0 < n_prompt - 1; p0 += c.max_slots) {
-    const int n = std::min(c.max_slots, n_prompt - 1 - p0);
-    if ((s = mie_verify_step(ctx, ids + p0, n, p0, block_table, max_blocks, nullptr, nullptr)) != MIE_OK) return s;
-    ++passes;
-  }
+  // the prompt but its last token, on the tensor cores
+  if (n_prompt > 1 && (s = mie_prefill(ctx, ids, n_prompt - 1, 0, block_table, max_blocks)) != MIE_OK) return s;
   std::vector<uint8_t> gate_mem(mie_spec_gate_bytes());
   mie_spec_gate *gate = reinterpret_cast<mie_spec_gate *>(gate_mem.data());
   mie_spec_gate_init(gate, 10, 0.3f, 5, 80);

@@ -1,0 +1,230 @@
+"""Prompt prefill on the tensor cores against the oracle (GPU only).
+
+  * mie_split_bf16: bit-exact against numpy's round-to-nearest-even three-plane split.
+  * mie_gemm_bf16 (tcgen05): every checked position's row against the oracle's fp64 GEMV
+    of the same bf16 weights and the fp32 input the planes came from, at sizes spanning
+    several 128 x 128 tiles with ragged T, N and K, with one and with three planes, with
+    accumulation into y and a row pitch wider than N.  Bound |dy| <= 1e-3 * max(|y|,
+    rms(y)) (the GEMV tolerance), and with three planes also |dy| <= 1e-6 * sum_k |w x|
+    (the fp32 class: the GEMV reaches 1.5e-8, a GEMM summing all of K in one tensor-core
+    accumulator measured 8e-7).
+  * mie_paged_attn_prefill: each position's output against the oracle's paged attention
+    at that position's context, through a permuted block table, after a cached prefix
+    (pos0 > 0), for head_dim 32 / 64 / 128 and block sizes 8 / 16 / 32.
+  * mie_prefill: the prompt but its last token on the tensor cores, then the decode step
+    of the last token: its logits against the oracle's after the same prompt one decode
+    step at a time (max |dlogit| <= 2e-2 * std, argmax where the margin exceeds 1e-2),
+    and every prompt position's K/V against the oracle's cache (one bf16 step of the
+    value plus 1e-3 of the RMS, 1e-2 with bf16 activations).  With bf16 activations (the
+    TinyLlama configuration rounds every GEMV input to bf16) any change of summation
+    order flips some of those roundings by a whole bf16 step, and the flips compound over
+    the prompt: on 120-token prompts the decode path itself lands at 0.70-0.99 of the
+    2e-2 bound (measured on GB300, four prompts), so the logits bound there is 4e-2 * std.
+"""
+
+import numpy as np
+import pytest
+
+import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+mie = pytest.importorskip("memory_bound_decode_dequant_gb300")
+from memory_bound_decode_dequant_gb300.workload import build_gpu_model, prompt_tokens  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    torch.cuda.set_device(0)
+    mie.lib()
+
+
+def np_split(orc, x):
+    hi = orc.to_bf16(x)
+    r = x - orc.from_bf16(hi)
+    mid = orc.to_bf16(r)
+    lo = orc.to_bf16(r - orc.from_bf16(mid))
+    return hi, mid, lo
+
+
+def _bits(t):
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def test_split_is_bit_exact(orc):
+    x = synth.normal(501, 70001) * np.float32(3.0)
+    x[:5] = [0.0, -0.0, 1e-30, 1e38, -2.5]  # finite bf16 range: activations never come near it
+    got = mie.mie_split_bf16(torch.from_numpy(x).cuda())
+    for g, r in zip(got, np_split(orc, x)):
+        assert np.array_equal(_bits(g), r)
+    # the planes carry x to 2^-25 of x
+    s = sum(orc.from_bf16(_bits(g)).astype(np.float64) for g in got)
+    ok = np.abs(x) < 1e38
+    assert np.all(np.abs(s[ok] - x[ok]) <= 2.0 ** -25 * np.abs(x[ok]))
+
+
+def _bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+GEMM_SHAPES = [(128, 64, 128), (256, 128, 130), (1376, 688, 77), (3072, 2048, 300), (2048, 8192, 64),
+               (384, 256, 1), (16384, 2048, 257)]
+
+
+@pytest.mark.parametrize("N,K,T", GEMM_SHAPES)
+def test_gemm_matches_oracle_gemv(orc, N, K, T):
+    w = synth.normal(600 + N + K, N * K).reshape(N, K) * np.float32(0.02)
+    mat = orc.Mat.quantize("bf16", w)
+    x = synth.normal(700 + T, T * K).reshape(T, K)
+    W = _bf16_dev(mat.data.reshape(N, K))
+    xd = torch.from_numpy(x).cuda()
+    planes = mie.mie_split_bf16(xd)
+    y = mie.mie_gemm_bf16(W, planes).cpu().numpy()
+    y1 = mie.mie_gemm_bf16(W, planes[:1]).cpu().numpy()  # the hi plane alone
+    rows = range(T) if N * K * T <= 3e8 else sorted(set(np.linspace(0, T - 1, 24).astype(int)))
+    xh = orc.from_bf16(orc.to_bf16(x))
+    wabs = np.abs(orc.from_bf16(mat.data).reshape(N, K))
+    for t in rows:
+        ref = orc.gemv(mat, x[t]).astype(np.float64)
+        bound = 1e-3 * np.maximum(np.abs(ref), np.sqrt(np.mean(ref ** 2)))
+        err = np.abs(y[t] - ref)
+        assert np.all(err <= bound), (t, float(np.max(err / bound)))
+        absum = (wabs @ np.abs(x[t])).astype(np.float64)
+        assert np.all(err <= 1e-6 * absum), (t, float(np.max(err / absum)))
+        ref1 = orc.gemv(mat, xh[t]).astype(np.float64)
+        err1 = np.abs(y1[t] - ref1)
+        assert np.all(err1 <= 1e-3 * np.maximum(np.abs(ref1), np.sqrt(np.mean(ref1 ** 2)))), t
+
+
+def test_gemm_accumulates_with_row_pitch(orc):
+    N, K, T, ld = 256, 192, 70, 300
+    w = synth.normal(801, N * K).reshape(N, K) * np.float32(0.02)
+    mat = orc.Mat.quantize("bf16", w)
+    x = synth.normal(802, T * K).reshape(T, K)
+    y0 = synth.normal(803, T * ld).reshape(T, ld)
+    yd = torch.from_numpy(y0.copy()).cuda()
+    planes = mie.mie_split_bf16(torch.from_numpy(x).cuda())
+    mie.mie_gemm_bf16(_bf16_dev(mat.data.reshape(N, K)), planes, y=yd, accumulate=True)
+    y = yd.cpu().numpy()
+    assert np.array_equal(y[:, N:], y0[:, N:])  # columns past N untouched
+    for t in range(T):
+        ref = orc.gemv(mat, x[t]).astype(np.float64) + y0[t, :N]
+        bound = 1e-3 * np.maximum(np.abs(ref), np.sqrt(np.mean(ref ** 2)))
+        assert np.all(np.abs(y[t, :N] - ref) <= bound), t
+
+
+def test_gemm_rejects_bad_shapes(orc):
+    W = torch.zeros((128, 60), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((4, 60), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(mie.MieError):
+        mie.mie_gemm_bf16(W, [x])  # K % 8 != 0
+
+
+ATTN_CASES = [  # (Hq, Hkv, hd, bs, pos0, T)
+    (32, 8, 64, 16, 37, 150),
+    (32, 8, 64, 16, 0, 64),
+    (8, 2, 32, 8, 5, 70),
+    (16, 16, 128, 32, 100, 33),
+    (32, 4, 64, 16, 1000, 129),
+]
+
+
+@pytest.mark.parametrize("Hq,Hkv,hd,bs,pos0,T", ATTN_CASES)
+def test_prefill_attention_matches_oracle(orc, Hq, Hkv, hd, bs, pos0, T):
+    n_ctx = pos0 + T
+    n_table = (n_ctx + bs - 1) // bs + 1
+    n_pool = n_table + 3
+    block_stride = Hkv * bs * hd
+    seed = 900 + hd + bs + pos0
+    kp = orc.to_bf16(synth.normal(seed, n_pool * block_stride))
+    vp = orc.to_bf16(synth.normal(seed + 1, n_pool * block_stride))
+    q = synth.normal(seed + 2, T * Hq * hd).reshape(T, Hq * hd)
+    bt = synth.permutation(seed + 3, n_pool)[:n_table].astype(np.int32)
+    scale = float(np.float32(1.0 / np.sqrt(hd)))
+    out = mie.mie_paged_attn_prefill(torch.from_numpy(q).cuda(), torch.from_numpy(kp.view(np.int16)).cuda(),
+                                     torch.from_numpy(vp.view(np.int16)).cuda(), block_stride, n_pool,
+                                     torch.from_numpy(bt).cuda(), pos0, Hq, Hkv, hd, bs, scale).cpu().numpy()
+    mie.mie_check()
+    for t in range(T):
+        ref = orc.attention_paged(q[t], kp, vp, block_stride, bt, pos0 + t + 1, Hq, Hkv, hd, bs, scale)
+        ref = ref.astype(np.float64)
+        rms = float(np.sqrt(np.mean(ref ** 2)))
+        err = np.abs(out[t] - ref)
+        assert np.all(err <= 1e-4 * rms + 1e-4 * np.abs(ref)), (t, float(np.max(err)), rms)
+
+
+def check_kv(orc, gm, om, blocks, act_bf16):
+    g = gm.kv().cpu().numpy().view(np.uint16)[blocks]
+    r = om.kv()[blocks]
+    gf = orc.from_bf16(g).astype(np.float64)
+    rf = orc.from_bf16(r).astype(np.float64)
+    rms = float(np.sqrt(np.mean(rf ** 2)))
+    c = 1e-2 if act_bf16 else 1e-3
+    bound = np.abs(rf) * 2.0 ** -7 + c * rms
+    err = np.abs(gf - rf)
+    worst = np.unravel_index(np.argmax(err / bound), err.shape)
+    assert np.all(err <= bound), f"K/V {worst}: gpu {gf[worst]} oracle {rf[worst]} (rms {rms:.3g})"
+
+
+def _prefill_case(orc, shape, layers, n_prompt, splits=(), seed=31):
+    """Prefill the prompt but its last token (in calls split at `splits`), decode the last
+    token; compare with the oracle's one-step-at-a-time decode of the same prompt."""
+    bs = shape.block_size
+    n_blocks = (n_prompt + bs - 1) // bs + 2
+    max_pos = n_blocks * bs
+    bt_host = synth.permutation(seed, n_blocks).astype(np.int32)
+    bt = torch.from_numpy(bt_host).cuda()
+    toks = [int(t) for t in prompt_tokens(shape, n_prompt, stream=seed)]
+    om = orc.Model(shape, n_kv_blocks=n_blocks, max_pos=max_pos, layers=layers)
+    for pos, tok in enumerate(toks):
+        ref, ref_best = om.decode_step(tok, pos, bt_host)
+    gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos, layers=layers)
+    edges = [0, *splits, n_prompt - 1]
+    for a, b in zip(edges[:-1], edges[1:]):
+        gm.prefill(toks[a:b], a, bt)
+    logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+    am = torch.empty(1, dtype=torch.int32, device="cuda")
+    gm.decode_step(toks[-1], n_prompt - 1, bt, logits, am)
+    gm.sync()
+    got = logits.cpu().numpy().astype(np.float64)
+    tol = (4e-2 if shape.act_bf16 else 2e-2) * float(np.std(ref))
+    err = float(np.max(np.abs(got - ref)))
+    assert err <= tol, f"max |dlogit| {err:.3e} > {tol:.3e}"
+    top = np.sort(ref)[-2:]
+    if top[1] - top[0] > 1e-2:
+        assert int(am.item()) == ref_best
+    used = bt_host[: (n_prompt + bs - 1) // bs]
+    check_kv(orc, gm, om, used, shape.act_bf16)
+    gm.close()
+
+
+def test_prefill_tiny_two_chunks(orc):
+    """The tiny Q4_0 model (ragged K = 688, head_dim 32): 600 prompt positions, two chunks
+    of the 512-position prefill, then a second call continuing after a cached prefix."""
+    _prefill_case(orc, synth.TINY, None, 640, splits=(600,))
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "q4_g128"])
+def test_prefill_llama32_shape_two_layers(orc, fmt):
+    shape = synth.llama32_1b(fmt)
+    _prefill_case(orc, shape, 2, 100, splits=(45,))
+
+
+def test_prefill_tinyllama_shape_bf16_activations(orc):
+    """Group 8, head_dim 64, K = 5632, bf16 activations (one plane per product)."""
+    _prefill_case(orc, synth.TINYLLAMA, 2, 120)
+
+
+def test_prefill_rejects_bad_arguments(orc):
+    shape = synth.TINY
+    gm = build_gpu_model(shape, n_kv_blocks=4, max_pos=64)
+    bt = torch.arange(4, dtype=torch.int32, device="cuda")
+    with pytest.raises(mie.MieError):
+        gm.prefill([1, 2, shape.vocab], 0, bt)  # token outside the vocabulary
+    with pytest.raises(mie.MieError):
+        gm.prefill([1] * 10, 60, bt)  # past max_pos
+    gm.prefill([], 0, bt)  # nothing to do
+    gm.close()
