@@ -60,9 +60,13 @@ def parse():
                     help="timed steps of --workload slots (the workload's 256; fewer for profiling)")
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (a small case for profiling; 0 = all)")
-    ap.add_argument("--workload", default="step", choices=["step", "slots", "sweep"],
+    ap.add_argument("--workload", default="step", choices=["step", "slots", "sweep", "prefill"],
                     help="step: batch-1 decode (the headline); slots: 8-slot continuous batching; "
-                         "sweep: the per-kernel sweep at the Llama-3.2-1B shapes")
+                         "sweep: the per-kernel sweep at the Llama-3.2-1B shapes; prefill: the "
+                         "2048-token prompt on the tensor cores and its GEMMs")
+    ap.add_argument("--gemm", default="",
+                    help="with --workload prefill: only the prompt GEMM of this layer shape (qkv, o, "
+                         "gate_up, down) at T = 512, launched --steps times (a profiling case)")
     ap.add_argument("--only", default="",
                     help="sweep: run only the cases whose 'kind:name:fmt' label contains this text "
                          "(e.g. gemv:lm_head:q4_0, attn:512, argmax)")
@@ -1097,6 +1101,23 @@ def main():
         synth_shape = _replace(synth.llama32_1b(args.fmt, args.head), n_layers=args.layers)
     else:
         synth_shape = None
+    if args.workload == "prefill":
+        import torch
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        if args.gemm:
+            import memory_bound_decode_dequant_gb300 as mie
+            _, N, K = next(g for g in GEMM_SHAPES if g[0] == args.gemm)
+            W = torch.randn(N, K, device="cuda").mul_(0.02).to(torch.bfloat16)
+            planes = mie.mie_split_bf16(torch.randn(512, K, device="cuda"))
+            y = torch.empty(512, N, device="cuda")
+            for _ in range(max(1, args.steps)):
+                mie.mie_gemm_bf16(W, planes, y)
+            torch.cuda.synchronize()
+            mie.mie_check()
+            print(json.dumps({"gemm": args.gemm, "N": N, "K": K, "T": 512, "launches": max(1, args.steps)}))
+        else:
+            print(json.dumps(prefill_measure(torch, measured_bf16_peak())), flush=True)
+        return
     if args.workload == "slots":
         if args.impl == "reference":
             run_reference_slots(args)
