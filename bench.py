@@ -66,7 +66,7 @@ def parse():
                          "2048-token prompt on the tensor cores and its GEMMs")
     ap.add_argument("--gemm", default="",
                     help="with --workload prefill: only the prompt GEMM of this layer shape (qkv, o, "
-                         "gate_up, down) at T = 512, launched --steps times (a profiling case)")
+                         "gate_up, down) at T = 2048, launched --steps times (a profiling case)")
     ap.add_argument("--only", default="",
                     help="sweep: run only the cases whose 'kind:name:fmt' label contains this text "
                          "(e.g. gemv:lm_head:q4_0, attn:512, argmax)")
@@ -444,12 +444,12 @@ def sampled_steps(torch, gm, stream, bt, logits, am, pos: int, tok: int, steps: 
 GEMM_SHAPES = [("qkv", 3072, 2048), ("o", 2048, 2048), ("gate_up", 16384, 2048), ("down", 2048, 8192)]
 
 
-def prefill_measure(torch, bf16_peak: float, n_prompt: int = 2048, chunk: int = 512) -> dict:
+def prefill_measure(torch, bf16_peak: float, n_prompt: int = 2048, chunk: int = 2048) -> dict:
     """Prompt prefill on the tensor cores (mie_prefill) at the Llama-3.2-1B shape with bf16
-    weights: an n_prompt-token prompt (chunks of 512 positions), timed with events on the
-    model's stream; and the tcgen05 GEMM alone at the four layer shapes for one chunk
-    (three activation planes: three MMAs per product), graph-timed over copies of the
-    weights larger than L2, against the measured bf16 tensor peak."""
+    weights: an n_prompt-token prompt (one chunk of up to 2048 positions), timed with
+    events on the model's stream; and the tcgen05 GEMM alone at the four layer shapes for
+    one chunk (three activation planes: three MMAs per product), graph-timed over copies
+    of the weights larger than L2, against the measured bf16 tensor peak."""
     from memory_bound_decode_dequant_gb300.workload import build_gpu_model
     import memory_bound_decode_dequant_gb300 as mie
     shape = synth.llama32_1b("bf16")
@@ -1108,13 +1108,13 @@ def main():
             import memory_bound_decode_dequant_gb300 as mie
             _, N, K = next(g for g in GEMM_SHAPES if g[0] == args.gemm)
             W = torch.randn(N, K, device="cuda").mul_(0.02).to(torch.bfloat16)
-            planes = mie.mie_split_bf16(torch.randn(512, K, device="cuda"))
-            y = torch.empty(512, N, device="cuda")
+            planes = mie.mie_split_bf16(torch.randn(2048, K, device="cuda"))
+            y = torch.empty(2048, N, device="cuda")
             for _ in range(max(1, args.steps)):
                 mie.mie_gemm_bf16(W, planes, y)
             torch.cuda.synchronize()
             mie.mie_check()
-            print(json.dumps({"gemm": args.gemm, "N": N, "K": K, "T": 512, "launches": max(1, args.steps)}))
+            print(json.dumps({"gemm": args.gemm, "N": N, "K": K, "T": 2048, "launches": max(1, args.steps)}))
         else:
             print(json.dumps(prefill_measure(torch, measured_bf16_peak())), flush=True)
         return

@@ -154,9 +154,9 @@ mie_status mie_split_bf16(const float *x, int64_t n, uint16_t *hi, uint16_t *mid
  * a dense contraction that tensor cores make several times faster than the CUDA-core
  * path):
  *   y[t * ldy + n] (+)= sum_k W[n][k] * (x_hi + x_mid + x_lo)[t][k],  t < T, n < N,
- * on tcgen05 (M = 128 weight rows x N = 128 positions per CTA, operands staged by TMA
- * with 128-byte swizzle, accumulators in tensor memory, drained every 128 columns of K
- * into fp32 registers).  W: device bf16 [N][K] row-major; x_hi, x_mid, x_lo: device bf16
+ * on tcgen05 (one CTA per SM taking 128 weight rows x 128 positions tiles in turn,
+ * operands staged by TMA with 128-byte swizzle, accumulators in tensor memory, drained
+ * every 128 columns of K into fp32 registers).  W: device bf16 [N][K] row-major; x_hi, x_mid, x_lo: device bf16
  * [T][K] planes (mie_split_bf16; x_mid and x_lo NULL: x_hi alone; x_lo NULL: hi + mid);
  * y: device fp32, rows ldy >= N floats apart; accumulate != 0 adds to y.  Pointers
  * 16-byte aligned, K % 8 == 0 (MIE_E_SHAPE otherwise).  A device-side wait that gives
@@ -447,7 +447,7 @@ void mie_spec_gate_record(mie_spec_gate *g, int proposed, int accepted);
 /* Prompt prefill on the tensor cores ([INFER] summary table and "Limitations": the
  * prompt as matrix-matrix products instead of one decode step per token).  Runs the n
  * tokens tokens[0..n) (host int32) at positions pos0 .. pos0 + n - 1 of one sequence
- * through every layer, in chunks of up to 512 positions -- RMSNorm, the QKV product
+ * through every layer, in chunks of up to 2048 positions -- RMSNorm, the QKV product
  * (mie_gemm_bf16's kernel; int8 and 4-bit matrices are first expanded to bf16 planes),
  * RoPE, the K/V write into the paged cache through block_table (device int32
  * [n_blocks]), causal attention (mie_paged_attn_prefill's kernel), the O product, the
@@ -455,7 +455,7 @@ void mie_spec_gate_record(mie_spec_gate *g, int proposed, int accepted);
  * write.  It produces no logits: the decode step of the next position (the prompt's last
  * token) does.  Activations enter the products as three bf16 planes (bf16 alone for
  * act_bf16 models), so the cache matches the decode step's to within rounding of the
- * summation order.  Asynchronous on the context's stream; the buffers (about 60 MB at
+ * summation order.  Asynchronous on the context's stream; the buffers (about 280 MB at
  * the Llama-3.2-1B shape, plus the largest weight matrix as bf16 planes for quantised
  * models) are allocated on the first call.  MIE_E_ARG for a token outside [0, vocab) or
  * positions outside [0, max_pos) or the table; device bounds checks are reported by the

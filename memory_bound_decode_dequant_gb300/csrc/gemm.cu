@@ -16,7 +16,8 @@
 // products whose levels add up to more than 2 (below 2^-24 of the terms) are skipped.
 // s is an optional per-row scale (int8 rows: the codes are exact in bf16).
 //
-// One CTA computes a 128 (weight rows) x 128 (tokens) tile over the whole K:
+// Persistent: one CTA per SM takes 128 (weight rows) x 128 (tokens) tiles in turn, each
+// over the whole K, its stage ring and accumulators running on from one tile to the next:
 //   warp 0, one lane : TMA producer, 64-column stages of every plane (128-byte swizzle)
 //   warp 1, one lane : issues tcgen05.mma (M = 128, N = 128, K = 16) into one of two TMEM
 //                      accumulators of 128 lanes x 128 fp32 columns, a segment of
@@ -33,6 +34,7 @@
 // MMAs, and frees its TMEM before it exits.
 #include <cuda.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -155,10 +157,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   int *fail_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = blockIdx.x * kTM, t0 = blockIdx.y * kTN;
   const int nk = (g.K + kTK - 1) / kTK;
-  const int nseg = (nk + kSegBlocks - 1) / kSegBlocks;
-
+  const int nseg = (nk + kSegBlocks - 1) / kSegBlocks;  // segments per tile
+  const int tiles_n = (g.N + kTM - 1) / kTM, n_tiles = tiles_n * ((g.T + kTN - 1) / kTN);
+  // persistent: this CTA's tiles are blockIdx.x, + gridDim.x, ... (weight tiles fastest,
+  // so the CTAs running at one time share their activation tile through L2)
+  const int my_tiles = blockIdx.x < n_tiles ? (n_tiles - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
@@ -186,109 +190,125 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer: stage kb of every plane into slot kb % S
-      int issued = 0;
-      for (int kb = 0; kb < nk; ++kb) {
-        const int s = kb % S, r = kb / S;
-        if (r > 0 && !mbar_wait_or_abort(&empty[s], (r - 1) & 1, g.wait_polls, fail_flag)) {
-          *fail_flag = 1;
-          break;
+      // producer: stage c (counted over all of this CTA's tiles) into slot c % S
+      int issued = 0, c = 0;
+      bool ok = true;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+        const int n0 = (tile % tiles_n) * kTM, t0 = (tile / tiles_n) * kTN;
+        for (int kb = 0; kb < nk; ++kb, ++c) {
+          const int s = c % S, r = c / S;
+          if (r > 0 && !mbar_wait_or_abort(&empty[s], (r - 1) & 1, g.wait_polls, fail_flag)) {
+            *fail_flag = 1;
+            ok = false;
+            break;
+          }
+          const uint32_t st = base + (uint32_t)s * kStageBytes, bar = smem_u32(&full[s]);
+          mbar_expect_tx(&full[s], (uint32_t)kStageBytes);
+          tma_load_2d(st, &tmA0, kb * kTK, n0, bar);
+          if (NA == 2) tma_load_2d(st + kPlaneBytes, &tmA1, kb * kTK, n0, bar);
+          tma_load_2d(st + NA * kPlaneBytes, &tmB0, kb * kTK, t0, bar);
+          if (NB >= 2) tma_load_2d(st + (NA + 1) * kPlaneBytes, &tmB1, kb * kTK, t0, bar);
+          if (NB >= 3) tma_load_2d(st + (NA + 2) * kPlaneBytes, &tmB2, kb * kTK, t0, bar);
+          issued = c + 1;
         }
-        const uint32_t st = base + (uint32_t)s * kStageBytes, bar = smem_u32(&full[s]);
-        mbar_expect_tx(&full[s], (uint32_t)kStageBytes);
-        tma_load_2d(st, &tmA0, kb * kTK, n0, bar);
-        if (NA == 2) tma_load_2d(st + kPlaneBytes, &tmA1, kb * kTK, n0, bar);
-        tma_load_2d(st + NA * kPlaneBytes, &tmB0, kb * kTK, t0, bar);
-        if (NB >= 2) tma_load_2d(st + (NA + 1) * kPlaneBytes, &tmB1, kb * kTK, t0, bar);
-        if (NB >= 3) tma_load_2d(st + (NA + 2) * kPlaneBytes, &tmB2, kb * kTK, t0, bar);
-        issued = kb + 1;
       }
       // before the CTA may exit, every issued copy must have landed: wait for the last
       // round of each slot that was filled
-      for (int kb = issued - S < 0 ? 0 : issued - S; kb < issued; ++kb)
-        if (!mbar_wait(&full[kb % S], (kb / S) & 1, g.wait_polls)) *fail_flag = 1;
+      for (int q = issued - S < 0 ? 0 : issued - S; q < issued; ++q)
+        if (!mbar_wait(&full[q % S], (q / S) & 1, g.wait_polls)) *fail_flag = 1;
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // MMA issuer: segment q of kSegBlocks stages into accumulator buffer q & 1
+      // MMA issuer: segment q (counted over all tiles) of kSegBlocks stages into
+      // accumulator buffer q & 1
       constexpr uint32_t idesc = umma_idesc_bf16(kTM, kTN);
       bool ok = true;
-      for (int q = 0; q < nseg && ok; ++q) {
-        const int b = q & 1;
-        if (q >= 2 && !mbar_wait_or_abort(&tempty[b], ((q >> 1) - 1) & 1, g.wait_polls, fail_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t acc = tmem + (uint32_t)(b * kTN);
-        const int kb1 = min(nk, (q + 1) * kSegBlocks);
-        for (int kb = q * kSegBlocks; kb < kb1; ++kb) {
-          const int s = kb % S, r = kb / S;
-          if (!mbar_wait_or_abort(&full[s], r & 1, g.wait_polls, fail_flag)) {
+      int c = 0, q = 0;
+      for (int i = 0; i < my_tiles && ok; ++i) {
+        for (int sg = 0; sg < nseg && ok; ++sg, ++q) {
+          const int b = q & 1;
+          if (q >= 2 && !mbar_wait_or_abort(&tempty[b], ((q >> 1) - 1) & 1, g.wait_polls, fail_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t st = base + (uint32_t)s * kStageBytes;
-          const bool first = kb == q * kSegBlocks;
+          const uint32_t acc = tmem + (uint32_t)(b * kTN);
+          const int kb1 = min(nk, (sg + 1) * kSegBlocks);
+          for (int kb = sg * kSegBlocks; kb < kb1; ++kb, ++c) {
+            const int s = c % S, r = c / S;
+            if (!mbar_wait_or_abort(&full[s], r & 1, g.wait_polls, fail_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
+            const bool first = kb == sg * kSegBlocks;
 #pragma unroll
-          for (int ks = 0; ks < kTK / 16; ++ks) {
+            for (int ks = 0; ks < kTK / 16; ++ks) {
 #pragma unroll
-            for (int a = 0; a < NA; ++a) {
+              for (int a = 0; a < NA; ++a) {
 #pragma unroll
-              for (int c = 0; c < NB; ++c) {
-                if (a + c > 2) continue;  // plane products below 2^-24 of the sum's terms
-                const uint64_t ad = umma_desc_sw128(st + a * kPlaneBytes + ks * 32);
-                const uint64_t bd = umma_desc_sw128(st + (NA + c) * kPlaneBytes + ks * 32);
-                umma_bf16(acc, ad, bd, idesc, !(first && ks == 0 && a == 0 && c == 0));
+                for (int pb = 0; pb < NB; ++pb) {
+                  if (a + pb > 2) continue;  // plane products below 2^-24 of the sum's terms
+                  const uint64_t ad = umma_desc_sw128(st + a * kPlaneBytes + ks * 32);
+                  const uint64_t bd = umma_desc_sw128(st + (NA + pb) * kPlaneBytes + ks * 32);
+                  umma_bf16(acc, ad, bd, idesc, !(first && ks == 0 && a == 0 && pb == 0));
+                }
               }
             }
+            umma_commit(smem_u32(&empty[s]));  // the slot is free once these MMAs have read it
           }
-          umma_commit(smem_u32(&empty[s]));  // the slot is free once these MMAs have read it
+          if (ok) umma_commit(smem_u32(&tfull[b]));  // the segment's sums are complete
         }
-        if (ok) umma_commit(smem_u32(&tfull[b]));  // the segment's sums are complete
       }
       if (!ok) *fail_flag = 1;
       umma_commit(smem_u32(done));  // arrives when every MMA above has completed
     }
   } else {
     // drain warps: warp w reads accumulator lanes 32 (w % 4) .. + 31 = weight rows
-    // n0 + 32 (w % 4) + lane and sums the segments in fp32 registers, so the tensor
-    // cores accumulate only kSegBlocks stages before each sum is rounded to fp32
+    // n0 + 32 (w % 4) + lane and sums a tile's segments in fp32 registers, so the tensor
+    // cores accumulate only kSegBlocks stages before each sum is rounded to fp32; the
+    // stores of one tile overlap the MMAs of the next
     const int quarter = warp & 3;
-    float sum[kTN];
-#pragma unroll
-    for (int c = 0; c < kTN; ++c) sum[c] = 0.f;
     bool ok = true;
-    for (int q = 0; q < nseg; ++q) {
-      const int b = q & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&tfull[b], (q >> 1) & 1, g.wait_polls, fail_flag));
-      if (!ok) {
-        if (lane == 0) *fail_flag = 1;
-        break;
+    int q = 0;
+    for (int i = 0; i < my_tiles && ok; ++i) {
+      const int tile = (int)blockIdx.x + i * (int)gridDim.x;
+      const int n0 = (tile % tiles_n) * kTM, t0 = (tile / tiles_n) * kTN;
+      float sum[kTN];
+#pragma unroll
+      for (int cc = 0; cc < kTN; ++cc) sum[cc] = 0.f;
+      for (int sg = 0; sg < nseg; ++sg, ++q) {
+        const int b = q & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&tfull[b], (q >> 1) & 1, g.wait_polls, fail_flag));
+        if (!ok) {
+          if (lane == 0) *fail_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kTN);
+#pragma unroll
+        for (int c0 = 0; c0 < kTN; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + (uint32_t)c0, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum[c0 + j] += v[j];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[b]);
       }
-      tc_fence_after();
-      const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kTN);
+      const int n = n0 + quarter * 32 + lane;
+      if (ok && !*reinterpret_cast<volatile int *>(fail_flag) && n < g.N) {
+        const float sc = g.row_scale ? g.row_scale[n] : 1.0f;
 #pragma unroll
-      for (int c0 = 0; c0 < kTN; c0 += 32) {
-        float v[32];
-        tmem_ld32(taddr + (uint32_t)c0, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sum[c0 + j] += v[j];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[b]);
-    }
-    const int n = n0 + quarter * 32 + lane;
-    if (ok && !*reinterpret_cast<volatile int *>(fail_flag) && n < g.N) {
-      const float sc = g.row_scale ? g.row_scale[n] : 1.0f;
-#pragma unroll
-      for (int c = 0; c < kTN; ++c) {
-        const int t = t0 + c;
-        if (t < g.T) {
-          float *dst = g.y + (int64_t)t * g.ldy + n;
-          *dst = g.accumulate ? *dst + sum[c] * sc : sum[c] * sc;
+        for (int cc = 0; cc < kTN; ++cc) {
+          const int t = t0 + cc;
+          if (t < g.T) {
+            float *dst = g.y + (int64_t)t * g.ldy + n;
+            *dst = g.accumulate ? *dst + sum[cc] * sc : sum[cc] * sc;
+          }
         }
       }
     }
@@ -362,7 +382,8 @@ static mie_status launch_gemm_t(const GemmPlan &p, cudaStream_t st) {
   g.accumulate = p.accumulate;
   g.err = p.err;
   g.wait_polls = kWaitPolls;
-  const dim3 grid((unsigned)((p.N + kTM - 1) / kTM), (unsigned)((p.T + kTN - 1) / kTN));
+  const int n_tiles = ((p.N + kTM - 1) / kTM) * ((p.T + kTN - 1) / kTN);
+  const dim3 grid((unsigned)std::min(n_tiles, sm_count()));  // persistent: one CTA per SM
   kern<<<grid, kGemmThreads, smem, st>>>(p.a[0], p.a[NA - 1], p.b[0], p.b[NB > 1 ? 1 : 0], p.b[NB - 1], g);
   MIE_CUDA(cudaGetLastError());
   return MIE_OK;

@@ -986,7 +986,7 @@ extern "C" mie_status mie_verify_step(mie_ctx *ctx, const int32_t *tokens, int n
 // Greedy generation through the few-slot kernels, speculative when spec_max > 1.
 // ------------------------------------------------------------------ prefill
 
-static constexpr int kPrefillChunk = 512;
+static constexpr int kPrefillChunk = 2048;
 
 static mie_status prefill_alloc(mie_ctx *ctx) {
   if (ctx->pf_R) return MIE_OK;

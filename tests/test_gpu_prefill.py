@@ -202,9 +202,10 @@ def _prefill_case(orc, shape, layers, n_prompt, splits=(), seed=31):
 
 
 def test_prefill_tiny_two_chunks(orc):
-    """The tiny Q4_0 model (ragged K = 688, head_dim 32): 600 prompt positions, two chunks
-    of the 512-position prefill, then a second call continuing after a cached prefix."""
-    _prefill_case(orc, synth.TINY, None, 640, splits=(600,))
+    """The tiny Q4_0 model (ragged K = 688, head_dim 32): 2080 prompt positions, two
+    chunks of the 2048-position prefill, then a second call continuing after a cached
+    prefix."""
+    _prefill_case(orc, synth.TINY, None, 2120, splits=(2080,))
 
 
 @pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "q4_g128"])
