@@ -19,12 +19,14 @@
 // Persistent: one CTA per SM takes 128 (weight rows) x 128 (tokens) tiles in turn, each
 // over the whole K, its stage ring and accumulators running on from one tile to the next:
 //   warp 0, one lane : TMA producer, 64-column stages of every plane (128-byte swizzle)
-//   warp 1, one lane : issues tcgen05.mma (M = 128, N = 128, K = 16) into one of two TMEM
+//   warp 1, one lane : issues tcgen05.mma (M = 128, N = 128, K = 16) into one of four TMEM
 //                      accumulators of 128 lanes x 128 fp32 columns, a segment of
 //                      kSegBlocks stages each, and tcgen05.commit to hand stages back
-//                      and to announce a finished segment
-//   warps 2-5        : drain: tcgen05.ld of their 32 TMEM lanes after every segment,
-//                      summed in fp32 registers, then scaled and stored
+//                      and to announce a finished segment; four buffers let the MMAs run
+//                      three segments ahead of the drain
+//   warps 2-9        : drain: tcgen05.ld of their 32 TMEM lanes and half of the columns
+//                      after every segment, summed in fp32 registers, then scaled and
+//                      stored
 // The tensor cores' own sums lose about 2^-24 of the accumulator per MMA (measured on
 // GB300: 8e-7 of sum |w x| at K = 2048 when one accumulator takes the whole K, against
 // 1.5e-8 for the fp32-FMA GEMV); draining every 128 columns of K keeps each tensor-core
@@ -48,9 +50,11 @@ constexpr int kTM = 128;        // weight rows per tile (UMMA M)
 constexpr int kTN = 128;        // tokens per tile (UMMA N)
 constexpr int kTK = 64;         // K per stage: one 128-byte swizzle atom of bf16
 constexpr int kPlaneBytes = kTM * kTK * 2;  // 16 KB per plane per stage (kTN == kTM)
-constexpr int kDrainWarps = 4;
+constexpr int kDrainWarps = 8;                       // two per TMEM lane quarter
+constexpr int kDrainCols = kTN * 4 / kDrainWarps;  // accumulator columns a drain warp reads
 constexpr int kGemmThreads = 64 + 32 * kDrainWarps;  // producer warp, MMA warp, drain warps
-constexpr int kTmemCols = 2 * kTN;  // two fp32 accumulator buffers of kTN columns
+constexpr int kAccBufs = 4;                // fp32 accumulator buffers of kTN columns in TMEM
+constexpr int kTmemCols = kAccBufs * kTN;  // all 512 columns: one CTA per SM
 constexpr int kSegBlocks = 2;       // stages summed by the tensor cores before a drain
 constexpr int kSmemBudget = 200 * 1024;
 
@@ -121,9 +125,9 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes, one lane per thread.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes, one lane per thread; the
+// caller waits (tmem_wait_ld) before it reads r.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
       "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
@@ -132,10 +136,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
         "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 template <int NA, int NB>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -150,9 +152,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint8_t *gen = smem_raw + (base - raw);
   uint64_t *full = reinterpret_cast<uint64_t *>(gen + (size_t)S * kStageBytes);
   uint64_t *empty = full + S;
-  uint64_t *tfull = empty + S;   // [2] a segment's sums are in accumulator buffer b
-  uint64_t *tempty = tfull + 2;  // [2] the drain warps have read buffer b
-  uint64_t *done = tempty + 2;   // every MMA has completed
+  uint64_t *tfull = empty + S;          // [kAccBufs] a segment's sums are in buffer b
+  uint64_t *tempty = tfull + kAccBufs;  // [kAccBufs] the drain warps have read buffer b
+  uint64_t *done = tempty + kAccBufs;   // every MMA has completed
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(done + 1);
   int *fail_flag = reinterpret_cast<int *>(tmem_slot + 1);
 
@@ -168,7 +170,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], kDrainWarps);
     }
@@ -221,14 +223,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // MMA issuer: segment q (counted over all tiles) of kSegBlocks stages into
-      // accumulator buffer q & 1
+      // accumulator buffer q % kAccBufs
       constexpr uint32_t idesc = umma_idesc_bf16(kTM, kTN);
       bool ok = true;
       int c = 0, q = 0;
       for (int i = 0; i < my_tiles && ok; ++i) {
         for (int sg = 0; sg < nseg && ok; ++sg, ++q) {
-          const int b = q & 1;
-          if (q >= 2 && !mbar_wait_or_abort(&tempty[b], ((q >> 1) - 1) & 1, g.wait_polls, fail_flag)) {
+          const int b = q % kAccBufs;
+          if (q >= kAccBufs && !mbar_wait_or_abort(&tempty[b], (q / kAccBufs - 1) & 1, g.wait_polls, fail_flag)) {
             ok = false;
             break;
           }
@@ -267,34 +269,36 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
   } else {
     // drain warps: warp w reads accumulator lanes 32 (w % 4) .. + 31 = weight rows
-    // n0 + 32 (w % 4) + lane and sums a tile's segments in fp32 registers, so the tensor
-    // cores accumulate only kSegBlocks stages before each sum is rounded to fp32; the
-    // stores of one tile overlap the MMAs of the next
-    const int quarter = warp & 3;
+    // n0 + 32 (w % 4) + lane, columns (positions) c1 .. c1 + kDrainCols - 1, and sums a
+    // tile's segments in fp32 registers, so the tensor cores accumulate only kSegBlocks
+    // stages before each sum is rounded to fp32; both loads of a segment are in flight
+    // before the one wait; the stores of one tile overlap the MMAs of the next
+    const int quarter = warp & 3, c1 = ((warp - 2) / 4) * kDrainCols;
     bool ok = true;
     int q = 0;
     for (int i = 0; i < my_tiles && ok; ++i) {
       const int tile = (int)blockIdx.x + i * (int)gridDim.x;
       const int n0 = (tile % tiles_n) * kTM, t0 = (tile / tiles_n) * kTN;
-      float sum[kTN];
+      float sum[kDrainCols];
 #pragma unroll
-      for (int cc = 0; cc < kTN; ++cc) sum[cc] = 0.f;
+      for (int cc = 0; cc < kDrainCols; ++cc) sum[cc] = 0.f;
       for (int sg = 0; sg < nseg; ++sg, ++q) {
-        const int b = q & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&tfull[b], (q >> 1) & 1, g.wait_polls, fail_flag));
+        const int b = q % kAccBufs;
+        ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&tfull[b], (q / kAccBufs) & 1, g.wait_polls, fail_flag));
         if (!ok) {
           if (lane == 0) *fail_flag = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kTN);
+        const uint32_t taddr = tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(b * kTN + c1);
+        uint32_t r[kDrainCols / 32][32];
 #pragma unroll
-        for (int c0 = 0; c0 < kTN; c0 += 32) {
-          float v[32];
-          tmem_ld32(taddr + (uint32_t)c0, v);
+        for (int h = 0; h < kDrainCols / 32; ++h) tmem_ld32(taddr + (uint32_t)(h * 32), r[h]);
+        tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum[c0 + j] += v[j];
-        }
+        for (int h = 0; h < kDrainCols / 32; ++h)
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum[h * 32 + j] += __uint_as_float(r[h][j]);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[b]);
@@ -303,8 +307,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       if (ok && !*reinterpret_cast<volatile int *>(fail_flag) && n < g.N) {
         const float sc = g.row_scale ? g.row_scale[n] : 1.0f;
 #pragma unroll
-        for (int cc = 0; cc < kTN; ++cc) {
-          const int t = t0 + cc;
+        for (int cc = 0; cc < kDrainCols; ++cc) {
+          const int t = t0 + c1 + cc;
           if (t < g.T) {
             float *dst = g.y + (int64_t)t * g.ldy + n;
             *dst = g.accumulate ? *dst + sum[cc] * sc : sum[cc] * sc;
