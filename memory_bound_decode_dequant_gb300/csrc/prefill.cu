@@ -14,6 +14,8 @@
 // memory; S = Q K^T and O += P V run on mma.sync m16n8k16 with Q and P as three bf16
 // planes each (K and V are bf16 already), with a running maximum and sum per row; keys
 // after a query's own position are masked (causal).
+#include <mutex>
+
 #include "internal.h"
 #include "device.cuh"
 
@@ -182,30 +184,34 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint3
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-  asm volatile("cp.async.commit_group;\ncp.async.wait_group 0;" ::: "memory");
-}
 
 constexpr int kAttnRows = 64;  // query positions per CTA
 constexpr int kAttnKeys = 64;  // keys per shared-memory tile
 constexpr int kAttnThreads = 128;
 
+// Dynamic shared memory of the kernel: two buffers (the next 64 keys are copied while the
+// current 64 are reduced), each K then V, rows padded to HD*2 + 16 bytes.
+__host__ __device__ constexpr int attn_pitch(int hd) { return hd * 2 + 16; }
+__host__ __device__ constexpr size_t attn_smem_bytes(int hd) { return 2u * 2u * kAttnKeys * attn_pitch(hd); }
+
 template <int HD>
 __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnArgs a) {
-  constexpr int PITCH = HD * 2 + 16;  // bytes per staged key row: conflict-free fragment loads
+  constexpr int PITCH = attn_pitch(HD);  // bytes per staged key row: conflict-free fragment loads
   constexpr int NKS = HD / 16, NOT = HD / 8, CPR = HD / 8;  // Q k-steps, O n-tiles, 16-byte chunks per row
-  __shared__ __align__(16) uint8_t ksm[kAttnKeys * PITCH];
-  __shared__ __align__(16) uint8_t vsm[kAttnKeys * PITCH];
+  constexpr uint32_t kBuf = 2u * kAttnKeys * PITCH;         // one buffer: K then V
+  extern __shared__ __align__(16) uint8_t att_smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quad = lane >> 2, tq4 = lane & 3;
   const int h = blockIdx.y, g = h / (a.Hq / a.Hkv);
   const int qt0 = blockIdx.x * kAttnRows;
   const int qlast = min(qt0 + kAttnRows, a.T) - 1;  // last query row of this CTA
   const int kend = a.pos0 + qlast + 1;               // keys 0 .. kend - 1 are needed
 
-  // Q fragments (hi, lo) of this warp's 16 rows: rows quad and quad + 8
+  // Q fragments of this warp's 16 rows (rows quad and quad + 8), pre-scaled by
+  // scale * log2(e) so that the softmax runs on exp2
   int tr[2];
   tr[0] = qt0 + warp * 16 + quad;
   tr[1] = tr[0] + 8;
+  const float qs = a.scale * 1.4426950408889634f;
   uint32_t qp[3][NKS][4];  // planes hi / mid / lo
 #pragma unroll
   for (int ks = 0; ks < NKS; ++ks) {
@@ -215,8 +221,8 @@ __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnA
       float2 v = make_float2(0.f, 0.f);
       if (row < a.T) v = *reinterpret_cast<const float2 *>(a.q + (int64_t)row * a.ldq + h * HD + d);
       uint16_t p0[3], p1[3];
-      split3(v.x, p0[0], p0[1], p0[2]);
-      split3(v.y, p1[0], p1[1], p1[2]);
+      split3(v.x * qs, p0[0], p0[1], p0[2]);
+      split3(v.y * qs, p1[0], p1[1], p1[2]);
 #pragma unroll
       for (int j = 0; j < 3; ++j) qp[j][ks][r] = pack2(p0[j], p1[j]);
     }
@@ -226,11 +232,13 @@ __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnA
   for (int n = 0; n < NOT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
   const int qpos[2] = {a.pos0 + tr[0], a.pos0 + tr[1]};
+  const int qpos_min = a.pos0 + qt0;  // keys up to it are visible to every row of the CTA
   const uint16_t *kbase = a.k + (int64_t)g * a.bs * HD, *vbase = a.v + (int64_t)g * a.bs * HD;
-  const uint32_t ks0 = smem_u32(ksm), vs0 = smem_u32(vsm);
+  const uint32_t sm0 = smem_u32(att_smem);
 
-  for (int k0 = 0; k0 < kend; k0 += kAttnKeys) {
-    // stage keys k0 .. k0 + 63 (zeros past kend)
+  // keys k0 .. k0 + 63 into buffer b (zeros past kend), as one cp.async group
+  auto stage = [&](int b, int k0) {
+    const uint32_t kb = sm0 + (uint32_t)b * kBuf, vb = kb + (uint32_t)(kAttnKeys * PITCH);
     for (int c = threadIdx.x; c < kAttnKeys * CPR; c += kAttnThreads) {
       const int key = c / CPR, ch = c % CPR, p = k0 + key;
       const uint32_t off = (uint32_t)(key * PITCH + ch * 16);
@@ -241,17 +249,27 @@ __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnA
           blk = 0;
         }
         const int64_t e = (int64_t)blk * a.block_stride + (int64_t)(p % a.bs) * HD + ch * 8;
-        cp_async16(ks0 + off, kbase + e);
-        cp_async16(vs0 + off, vbase + e);
+        cp_async16(kb + off, kbase + e);
+        cp_async16(vb + off, vbase + e);
       } else {
-        *reinterpret_cast<uint4 *>(ksm + off) = make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4 *>(vsm + off) = make_uint4(0u, 0u, 0u, 0u);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(kb + off), "r"(0u) : "memory");
+        asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(vb + off), "r"(0u) : "memory");
       }
     }
-    cp_async_wait_all();
-    __syncthreads();
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
 
-    // S = Q K^T for 8 tiles of 8 keys
+  stage(0, 0);
+  int t = 0;
+  for (int k0 = 0; k0 < kend; k0 += kAttnKeys, ++t) {
+    const bool more = k0 + kAttnKeys < kend;
+    if (more) stage((t + 1) & 1, k0 + kAttnKeys);  // its buffer was released by the last barrier
+    if (more) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncthreads();
+    const uint32_t ks0 = sm0 + (uint32_t)(t & 1) * kBuf, vs0 = ks0 + (uint32_t)(kAttnKeys * PITCH);
+
+    // S = Q K^T for 8 tiles of 8 keys (log2 units)
     float s[8][4];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -265,7 +283,9 @@ __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnA
           mma_bf16(s[j], qp[pl][ks][0], qp[pl][ks][1], qp[pl][ks][2], qp[pl][ks][3], b0, b1);
       }
     }
-    // scale, causal mask, running maximum and sum per row
+    // causal mask (only a tile reaching past the CTA's first position needs it), running
+    // maximum and sum per row
+    const bool masked = k0 + kAttnKeys - 1 > qpos_min;
     float corr[2];
 #pragma unroll
     for (int rh = 0; rh < 2; ++rh) {
@@ -274,8 +294,8 @@ __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnA
       for (int j = 0; j < 8; ++j) {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const int key = k0 + j * 8 + tq4 * 2 + e;
-          const float v = (key <= qpos[rh]) ? s[j][rh * 2 + e] * a.scale : -INFINITY;
+          float v = s[j][rh * 2 + e];
+          if (masked && k0 + j * 8 + tq4 * 2 + e > qpos[rh]) v = -INFINITY;
           s[j][rh * 2 + e] = v;
           mx = fmaxf(mx, v);
         }
@@ -289,12 +309,12 @@ __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnA
 #pragma unroll
         for (int j = 0; j < 8; ++j) s[j][rh * 2] = s[j][rh * 2 + 1] = 0.f;
       } else {
-        corr[rh] = expf(m[rh] - m_new);
+        corr[rh] = exp2f(m[rh] - m_new);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const float p = expf(s[j][rh * 2 + e] - m_new);
+            const float p = exp2f(s[j][rh * 2 + e] - m_new);
             s[j][rh * 2 + e] = p;
             sum += p;
           }
@@ -339,7 +359,7 @@ __global__ void __launch_bounds__(kAttnThreads) prefill_attn_kernel(PrefillAttnA
         }
       }
     }
-    __syncthreads();  // the next tile overwrites the staged keys
+    __syncthreads();  // the buffer is free for the copy two tiles on
   }
   // normalise and store
 #pragma unroll
@@ -403,12 +423,25 @@ mie_status launch_prefill_attn(const PrefillAttnArgs &a, cudaStream_t st) {
   if (a.Hq % a.Hkv) return fail(MIE_E_SHAPE, "prefill attention: Hq %% Hkv != 0");
   if (kAttnKeys % a.bs) return fail(MIE_E_SHAPE, "prefill attention: block size %d", a.bs);
   const dim3 grid((unsigned)blocks_of(a.T, kAttnRows), (unsigned)a.Hq);
+  auto go = [&](auto kern, int hd) -> mie_status {
+    const size_t smem = attn_smem_bytes(hd);
+    if (smem > 48 * 1024) {
+      static std::once_flag once;
+      static cudaError_t set = cudaSuccess;
+      std::call_once(once, [&] { set = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); });
+      if (set != cudaSuccess) return cuda_fail(set, "prefill attention: cudaFuncSetAttribute");
+    }
+    kern<<<grid, kAttnThreads, smem, st>>>(a);
+    return MIE_OK;
+  };
+  mie_status s;
   switch (a.hd) {
-    case 32: prefill_attn_kernel<32><<<grid, kAttnThreads, 0, st>>>(a); break;
-    case 64: prefill_attn_kernel<64><<<grid, kAttnThreads, 0, st>>>(a); break;
-    case 128: prefill_attn_kernel<128><<<grid, kAttnThreads, 0, st>>>(a); break;
+    case 32: s = go(prefill_attn_kernel<32>, 32); break;
+    case 64: s = go(prefill_attn_kernel<64>, 64); break;
+    case 128: s = go(prefill_attn_kernel<128>, 128); break;
     default: return fail(MIE_E_SHAPE, "prefill attention: head_dim %d", a.hd);
   }
+  if (s != MIE_OK) return s;
   MIE_CUDA(cudaGetLastError());
   return MIE_OK;
 }
