@@ -22,6 +22,7 @@ random physical order from the host block pool, 256 steps with one slot retired 
 from __future__ import annotations
 
 import argparse
+import gc
 import json
 import os
 import statistics
@@ -99,6 +100,24 @@ def measured_bf16_peak() -> float:
         with open(p) as f:
             return float(json.load(f).get("bf16_tflops", 1900.0))
     return 1900.0
+
+
+class NoGC:
+    """Pauses Python's cyclic garbage collector inside a timed host loop: collections over
+    the objects the earlier workloads of the default line leave behind stalled the host
+    between launches and left the GPU idle (measured on GB300: the 8-slot loop ran 1.78 ms
+    per step after those workloads, 1.29 ms alone and 1.29 ms after them with the
+    collector paused).  No work is skipped; the collector runs once before the loop."""
+
+    def __enter__(self):
+        self._on = gc.isenabled()
+        gc.collect()
+        gc.disable()
+        return self
+
+    def __exit__(self, *a):
+        if self._on:
+            gc.enable()
 
 
 class Clocks:
@@ -641,14 +660,16 @@ def run_mie(args, shape):
         tok = int(am.item())
     gm.sync()
     barrier(pg)
-    t0 = time.perf_counter()
-    for _ in range(args.e2e_steps):
-        gm.decode_step(tok, pos, bt, logits, am)
-        with torch.cuda.stream(stream):  # the read is ordered after the step on its stream
-            tok = int(am.item())  # device -> host read of the step's result (synchronises)
-        pos += 1
-    gm.sync()
-    e2e_dt = max_over_ranks(pg, (time.perf_counter() - t0) / args.e2e_steps)
+    with NoGC():
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            gm.decode_step(tok, pos, bt, logits, am)
+            with torch.cuda.stream(stream):  # the read is ordered after the step on its stream
+                tok = int(am.item())  # device -> host read of the step's result (synchronises)
+            pos += 1
+        gm.sync()
+        e2e_dt_local = (time.perf_counter() - t0) / args.e2e_steps
+    e2e_dt = max_over_ranks(pg, e2e_dt_local)
 
     # algorithmic bytes of one step: all weights once + the K/V of every position read
     step_bytes = shape.decode_bytes(args.ctx + args.warmup, args.steps)  # the timed steps
@@ -876,7 +897,7 @@ def measure_slots(args, torch, rank: int = 0, world: int = 1, local: int | None 
     kv_tokens = 0
     retired = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with Clocks(local) as clk:
+    with Clocks(local) as clk, NoGC():
         t_wall = time.perf_counter()
         e0.record(stream)
         for i in range(wl.steps):
@@ -905,13 +926,14 @@ def measure_slots(args, torch, rank: int = 0, world: int = 1, local: int | None 
     dt = e0.elapsed_time(e1) / 1e3 / wl.steps
     # end to end: the same call with the argmax read back every step
     e2e_steps = 16
-    t0 = time.perf_counter()
-    for i in range(e2e_steps):
-        gm.decode_step_slots(toks[args.warmup + wl.steps + i], pos, tdev, logits, am)
-        with torch.cuda.stream(stream):  # the read is ordered after the step on its stream
-            _ = am.cpu()  # device -> host read of the step's results (synchronises)
-        pos += 1
-    e2e_dt = (time.perf_counter() - t0) / e2e_steps
+    with NoGC():
+        t0 = time.perf_counter()
+        for i in range(e2e_steps):
+            gm.decode_step_slots(toks[args.warmup + wl.steps + i], pos, tdev, logits, am)
+            with torch.cuda.stream(stream):  # the read is ordered after the step on its stream
+                _ = am.cpu()  # device -> host read of the step's results (synchronises)
+            pos += 1
+        e2e_dt = (time.perf_counter() - t0) / e2e_steps
     gm.sync()
     w_bytes = shape.weight_bytes()
     kv_bytes = shape.kv_bytes_per_token() * kv_tokens / wl.steps
