@@ -18,7 +18,7 @@ OUT = os.path.join(PKG, "libmie.so")
 BUILD_DIR = os.path.join(PKG, "_build", platform.machine())
 STAMP = os.path.join(BUILD_DIR, "libmie.so.stamp")
 SOURCES = ["gemv.cu", "gemv_slots.cu", "attn.cu", "step.cu", "quant.cu", "model.cu", "probe.cu", "sample.cu", "gemm.cu", "prefill.cu", "pool.cpp", "spec.cpp"]
-HEADERS = ["common.cuh", "internal.h", "device.cuh", "attn_core.cuh"]
+HEADERS = ["common.cuh", "internal.h", "device.cuh", "attn_core.cuh", "attn_mma.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 # MIE_STAGE_TRACE=1 builds the instrumented library whose persistent step also stamps
 # every ring stage (mie_set_trace); its objects live in their own build folder.

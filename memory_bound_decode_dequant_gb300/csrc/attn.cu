@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "attn_core.cuh"
+#include "attn_mma.cuh"
 
 namespace mie {
 
@@ -168,7 +169,161 @@ __global__ void __launch_bounds__(kCThreads, 2) attn_chunk_kernel(const AttnArgs
         }
       }
     }
-    attn_merge_splits<G, HD, kCThreads, CSync, false>(a, g, nsplit, sm.last, 0u);
+    attn_merge_splits<G, HD, kCThreads, CSync, false, 16>(a, g, nsplit, sm.last, 0u);
+  }
+}
+
+// Tensor-core variant (head_dim 64 or 128, block stride a multiple of head_dim): the
+// split's K and V arrive by 2-D tensor copies (one per block and 64-dimension half) as
+// 128-byte swizzled tiles, and each warp reduces 32 of its tokens on the tensor cores
+// with its own online softmax (attn_mma.cuh); the CTA then combines its 8 warps and the
+// splits merge as above.  Measured on GB300 for one 256-token split of a KV head with
+// four query heads: the three CUDA-core passes of chunk_passes took 3.1-4.6 us.
+constexpr uint32_t kMmaHalf = (uint32_t)kCTok * 128u;  // bytes of one 64-dim half of a K or V buffer
+
+template <int G, int HD>
+constexpr size_t attn_mma_smem() {
+  return 1024 + 2 * (HD / 64) * (size_t)kMmaHalf + (size_t)(kCThreads / 32) * G * HD * 4;
+}
+
+template <int G, int HD>
+__global__ void __launch_bounds__(kCThreads, HD == 64 ? 2 : 1)
+    attn_mma_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const AttnArgs a_in) {
+  constexpr int MT = (G + 3) / 4, NH = HD / 64, NW = kCThreads / 32;
+  extern __shared__ uint8_t dbuf[];
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int ids[kCSplitTok / 8];
+  __shared__ float wm[NW * G], wl[NW * G];
+  __shared__ float qs[G * HD];
+  __shared__ uint4 qf[MT * (HD / 16) * 32];  // query A fragments per (tile, k-step, lane)
+  __shared__ unsigned last;
+  pdl_trigger();
+  // the few-slot step runs one grid layer per slot: slot z's queries, outputs and
+  // workspace follow those of slot z - 1 (every pointer formed from the launch's own
+  // arguments; measured on GB300, the queries read through a shifted copy of the
+  // argument struct came from slot 0)
+  const int z = a_in.slot_z ? (int)blockIdx.z : a_in.slot;
+  if (a_in.slot_z && z >= a_in.sp->n_slots) return;
+  const int64_t zq = a_in.slot_z ? (int64_t)z * a_in.Hq * HD : 0;
+  const size_t zw = a_in.slot_z ? (size_t)z * a_in.ws_slot_bytes : 0;
+  AttnArgs a = a_in;
+  a.slot = z;
+  a.q = a_in.q + zq;
+  a.out = a_in.out + zq;
+  a.ws_count = reinterpret_cast<unsigned *>(reinterpret_cast<uint8_t *>(a_in.ws_count) + zw);
+  a.ws_part = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(a_in.ws_part) + zw);
+  pdl_wait();
+  const int tid = threadIdx.x, warp = tid >> 5, g = blockIdx.y;
+  int ctx;
+  const int32_t *bt;
+  int n_table;
+  if (a.sp) {
+    ctx = a.sp->pos[a.slot] + 1;
+    bt = a.sp->block_table + (int64_t)a.slot * a.sp->max_blocks;
+    n_table = a.sp->max_blocks;
+  } else {
+    ctx = a.ctx;
+    bt = a.block_table;
+    n_table = a.n_table;
+  }
+  if (ctx > n_table * a.bs) {
+    if (tid == 0 && blockIdx.x == 0 && g == 0) latch_error(a.err, ERR_POS);
+    ctx = n_table * a.bs;
+  }
+  if (ctx < 0) ctx = 0;
+  const int nblk = (ctx + a.bs - 1) / a.bs;
+  const int nsplit = attn_nsplit(nblk, a.n_splits, kCSplitTok / a.bs);
+  if ((int)blockIdx.x >= nsplit) return;
+  // the queries come from the previous kernel: read at L2 (a line this SM's L1 kept from
+  // an earlier kernel could be stale under programmatic dependent launch)
+  for (int i = tid; i < G * HD; i += kCThreads) qs[i] = __ldcg(a_in.q + zq + (int64_t)(g * G) * HD + i);
+  const uint32_t kbuf = (smem_u32(dbuf) + 1023u) & ~1023u, vbuf = kbuf + NH * kMmaHalf;
+  float *wo = reinterpret_cast<float *>(dbuf + (vbuf + NH * kMmaHalf - smem_u32(dbuf)));  // [NW][G][HD]
+  const int64_t rows_per_blk = a.block_stride / HD;
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  int it = 0;
+  for (int sp = blockIdx.x; sp < nsplit; sp += gridDim.x, ++it) {
+    const int b0 = (int)((int64_t)sp * nblk / nsplit), b1 = (int)((int64_t)(sp + 1) * nblk / nsplit);
+    const int nb = b1 - b0, ntok = min(b1 * a.bs, ctx) - b0 * a.bs;
+    if (nb > kCSplitTok / a.bs) {  // a context longer than the workspace's splits were sized for
+      if (tid == 0) latch_error(a.err, ERR_POS);
+      return;
+    }
+    fence_proxy_async_smem();  // this thread's generic accesses of the previous split before the copies
+    if (tid < nb) {
+      int blk = bt[b0 + tid];
+      if (blk < 0 || blk >= a.n_pool_blocks) {
+        latch_error(a.err, ERR_BLOCK_ID);
+        blk = 0;  // a valid block: the result is wrong but the error is reported
+      }
+      ids[tid] = blk;
+    }
+    __syncthreads();  // block ids; every warp is done with the buffers
+    if (tid == 0) {
+      mbar_expect_tx(&bar, (uint32_t)nb * a.bs * HD * 2 * 2);
+      for (int j = 0; j < nb; ++j) {
+        const int y = (int)((int64_t)ids[j] * rows_per_blk + (int64_t)g * a.bs);
+#pragma unroll
+        for (int hh = 0; hh < NH; ++hh) {
+          const uint32_t off = hh * kMmaHalf + (uint32_t)(j * a.bs) * 128u;
+          tma_load_tile(kbuf + off, &tmk, hh * 64, y, smem_u32(&bar));
+          tma_load_tile(vbuf + off, &tmv, hh * 64, y, smem_u32(&bar));
+        }
+      }
+    }
+    // the query fragments, once, while the first split's copies fly (the queries were
+    // stored before the barrier above; the fragments are read after the one below)
+    if (it == 0) q_fragments_shared<G, HD, NW>(qs, a.scale * kLog2e, qf);
+    if (!CSync::all(mbar_wait(&bar, it & 1))) {  // a copy never completed
+      if (tid == 0) {
+        latch_error(a.err, ERR_TIMEOUT);
+        mbar_wait(&bar, it & 1);  // leave no copy writing into shared memory
+      }
+      return;
+    }
+    // V rows from ntok to the next multiple of 16 meet zero probabilities: make them finite
+    const int rz = min((ntok + 15) & ~15, kCTok);
+    for (int i = tid; i < (rz - ntok) * (HD / 8); i += kCThreads)
+      sts128_zero(swz_addr(vbuf, kCTok, ntok + i / (HD / 8), i % (HD / 8)));
+    __syncthreads();
+#pragma unroll 1
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t qa[HD / 16][4];
+#pragma unroll
+      for (int k = 0; k < HD / 16; ++k) {
+        const uint4 f = qf[(mt * (HD / 16) + k) * 32 + (tid & 31)];
+        qa[k][0] = f.x;
+        qa[k][1] = f.y;
+        qa[k][2] = f.z;
+        qa[k][3] = f.w;
+      }
+      WarpAttn<HD> st;
+      st.reset();
+      warp_chunk_mma<HD>(kbuf, vbuf, kCTok, kMmaTokPerWarp * warp, ntok, qa, st);
+      warp_attn_store<G, HD>(st, mt, wm, wl, wo);
+    }
+    __syncthreads();
+    float *part = a.ws_part + ((int64_t)g * a.n_splits + sp) * (G * (2 + HD));
+    for (int i = tid; i < G * HD; i += kCThreads) {
+      float M, L, O;
+      cta_attn_combine<G, HD, NW>(i, wm, wl, wo, M, L, O);
+      if (nsplit == 1) {
+        a.out[(int64_t)(g * G) * HD + i] = (L > 0.f) ? O / L : 0.f;
+      } else {
+        const int h = i / HD;
+        part[2 * G + i] = O;
+        if (i % HD == 0) {
+          part[h] = (M == -INFINITY) ? -INFINITY : M * kLn2;  // the merge works in natural-log units
+          part[G + h] = L;
+        }
+      }
+    }
+    if (nsplit == 1) return;
+    attn_merge_splits<G, HD, kCThreads, CSync, false, 16>(a, g, nsplit, last, 0u);
   }
 }
 
@@ -202,21 +357,36 @@ int attn_splits_for(int Hkv, int max_ctx, int bs) {
 template <int G, int HD>
 static mie_status launch_attn_t(const AttnArgs &a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  const size_t smem = (size_t)kCBufs * 2u * kCTok * HD * 2;
-  auto kern = attn_chunk_kernel<G, HD>;
-  MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
   // few-slot step: the grid is captured once for any context, so it holds at most
   // kCSlotGrid CTAs per (KV head, slot) and each loops over its splits; CTAs past a slot's
   // splits only read its position and leave (a grid of n_splits left ~3/4 of them idle)
   cfg.gridDim = dim3(a.slot_z ? min(a.n_splits, kCSlotGrid) : a.n_splits, a.Hkv, a.slot_z ? a.max_slots : 1);
   cfg.blockDim = dim3(kCThreads);
-  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 1 : 0;
+  if constexpr (HD == 64 || HD == 128) {
+    if (a.block_stride % HD == 0) {  // K/V rows addressable as a 2-D tensor of head_dim columns
+      const int64_t rows = ((int64_t)(a.n_pool_blocks - 1) * a.block_stride + (int64_t)a.Hkv * a.bs * HD) / HD;
+      CUtensorMap mk, mv;
+      mie_status s = make_bf16_map(&mk, a.k, rows, HD, HD * 2, a.bs);
+      if (s == MIE_OK) s = make_bf16_map(&mv, a.v, rows, HD, HD * 2, a.bs);
+      if (s != MIE_OK) return s;
+      auto kern = attn_mma_kernel<G, HD>;
+      constexpr size_t smem = attn_mma_smem<G, HD>();
+      MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+      cfg.dynamicSmemBytes = smem;
+      MIE_CUDA(cudaLaunchKernelEx(&cfg, kern, mk, mv, a));
+      return MIE_OK;
+    }
+  }
+  const size_t smem = (size_t)kCBufs * 2u * kCTok * HD * 2;
+  auto kern = attn_chunk_kernel<G, HD>;
+  MIE_CUDA(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+  cfg.dynamicSmemBytes = smem;
   MIE_CUDA(cudaLaunchKernelEx(&cfg, kern, a));
   return MIE_OK;
 }

@@ -54,7 +54,9 @@ __device__ bool tagged_inputs(const AttnArgs &a, int h0, int g, bool has_pos, SM
 // query head) wrote its partial (m, l, o) to the workspace: the last split of the unit
 // to arrive (atomic counter, no waiting) merges all nsplit partials into the outputs of
 // query heads g*G .. g*G+G-1 and resets the counter.  `last` is a shared-memory flag.
-template <int G, int HD, int NT, class Sync, bool Tagged>
+// B splits' partials are loaded per round trip (the standalone kernels take 16; the
+// persistent step, short of registers, 8).
+template <int G, int HD, int NT, class Sync, bool Tagged, int B = 8>
 __device__ void attn_merge_splits(const AttnArgs &a, int g, int nsplit, unsigned &last, uint32_t tag) {
   constexpr int PART = G * (2 + HD);
   const int tid = threadIdx.x;
@@ -67,12 +69,12 @@ __device__ void attn_merge_splits(const AttnArgs &a, int g, int nsplit, unsigned
   const float *base = a.ws_part + (int64_t)g * a.n_splits * PART;
   for (int i = tid; i < G * HD; i += NT) {
     const int h = i / HD;
-    // one pass with online rescaling, eight splits' partials loaded per round trip
+    // one pass with online rescaling, B splits' partials loaded per round trip
     float M = -INFINITY, O = 0.f, L = 0.f;
-    for (int s0 = 0; s0 < nsplit; s0 += 8) {
-      float ms[8], os[8], ls[8];
+    for (int s0 = 0; s0 < nsplit; s0 += B) {
+      float ms[B], os[B], ls[B];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < B; ++j) {
         const float *p = base + (int64_t)min(s0 + j, nsplit - 1) * PART;
         ms[j] = __ldcg(p + h);
         ls[j] = __ldcg(p + G + h);
@@ -80,14 +82,14 @@ __device__ void attn_merge_splits(const AttnArgs &a, int g, int nsplit, unsigned
       }
       float mb = M;
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
+      for (int j = 0; j < B; ++j)
         if (s0 + j < nsplit) mb = fmaxf(mb, ms[j]);
       if (mb == -INFINITY) continue;
       const float c = (M == -INFINITY) ? 0.f : expf(M - mb);
       O *= c;
       L *= c;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
+      for (int j = 0; j < B; ++j) {
         if (s0 + j < nsplit && ms[j] != -INFINITY) {
           const float f = expf(ms[j] - mb);
           O = fmaf(os[j], f, O);

@@ -352,14 +352,16 @@ EncodeTiledFn encode_tiled() {
 }  // namespace
 
 // A 2-D bf16 tensor map over rows of `cols` elements, `pitch` bytes apart, boxes of 64
-// columns x 128 rows with 128-byte swizzle; reads outside the tensor return zeros.
-mie_status make_bf16_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t pitch) {
+// columns x box_rows rows with 128-byte swizzle; reads outside the tensor return zeros.
+mie_status make_bf16_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t pitch,
+                         int box_rows) {
   EncodeTiledFn enc = encode_tiled();
   if (!enc) return fail(MIE_E_CUDA, "tensor map: cuTensorMapEncodeTiled is not available");
   if (((uintptr_t)base & 15) || (pitch & 15)) return fail(MIE_E_SHAPE, "tensor map: base or pitch not 16-byte aligned");
+  if (box_rows < 1 || box_rows > 256) return fail(MIE_E_SHAPE, "tensor map: box of %d rows", box_rows);
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)pitch};
-  const cuuint32_t box[2] = {(cuuint32_t)kTK, (cuuint32_t)kTM};
+  const cuuint32_t box[2] = {(cuuint32_t)kTK, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,

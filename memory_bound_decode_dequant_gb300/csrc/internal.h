@@ -110,7 +110,7 @@ mie_status launch_attn(const AttnArgs &a, cudaStream_t st, bool pdl);
 
 // Prompt GEMM on tcgen05 (gemm.cu): Y[t][n] (+)= s[n] * sum_k (A0 + A1)[n][k] (B0 + B1 + B2)[t][k]
 // with bf16 planes A (weight rows) and B (activation rows) behind 2-D tensor maps
-// (make_bf16_map: 64-column x 128-row boxes, 128-byte swizzle, zeros outside).
+// (make_bf16_map: 64-column boxes of 128 rows by default, 128-byte swizzle, zeros outside).
 struct GemmPlan {
   CUtensorMap a[2], b[3];
   int na = 1, nb = 1;  // planes in use: na 1 or 2, nb 1 to 3
@@ -121,7 +121,8 @@ struct GemmPlan {
   bool accumulate = false;
   int *err = nullptr;
 };
-mie_status make_bf16_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t pitch);
+mie_status make_bf16_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, int64_t pitch,
+                         int box_rows = 128);
 mie_status launch_gemm(const GemmPlan &p, cudaStream_t st);
 
 // The prompt's row-wise kernels and attention (prefill.cu).

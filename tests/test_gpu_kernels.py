@@ -263,6 +263,71 @@ def test_attention_edge_cases(orc):
         assert np.array_equal(out[h], v0[h // 4])
 
 
+@pytest.mark.parametrize("Hq,Hkv,hd", [(32, 8, 64), (16, 8, 64), (64, 8, 64), (8, 1, 128)])
+@pytest.mark.parametrize("bs", [8, 32])
+@pytest.mark.parametrize("ctx", [1, 23, 300, 777])
+def test_paged_attention_tensor_core_block_sizes(orc, Hq, Hkv, hd, bs, ctx):
+    """The tensor-core kernel (head_dim 64 / 128) with 8- and 32-token blocks: one 2-D
+    tensor copy per block, splits whose token count is no multiple of 16, and group
+    sizes 2, 4 and 8 (two 16-row tiles)."""
+    nblk = (ctx + bs - 1) // bs
+    n_pool = nblk + 3
+    kp, vp = _pool(orc, 6500 + ctx + bs, n_pool, Hkv, bs, hd)
+    bt = synth.permutation(6600 + ctx + bs, n_pool)[:nblk].astype(np.int32)
+    q = synth.normal(6700 + ctx + hd, Hq * hd)
+    scale = float(np.float32(1 / math.sqrt(hd)))
+    stride = Hkv * bs * hd
+    out = _attn_gpu(q, kp, vp, stride, n_pool, bt, ctx, Hq, Hkv, hd, bs, scale)
+    ref = orc.attention_paged(q, kp, vp, stride, bt, ctx, Hq, Hkv, hd, bs, scale)
+    attn_close(out, ref)
+
+
+@pytest.mark.parametrize("hd", [64, 128])
+def test_attention_edge_cases_tensor_core(orc, hd):
+    """Empty context gives zeros; a one-token context gives v_0 exactly (P = 1 in the
+    first bf16 plane, zero in the others)."""
+    Hq, Hkv, bs = 8, 2, 16
+    kp, vp = _pool(orc, 9200 + hd, 4, Hkv, bs, hd)
+    q = synth.normal(9201, Hq * hd)
+    bt = np.array([2, 0, 3, 1], np.int32)
+    out = _attn_gpu(q, kp, vp, Hkv * bs * hd, 4, bt, 0, Hq, Hkv, hd, bs, 0.17)
+    assert np.all(out == 0)
+    out = _attn_gpu(q, kp, vp, Hkv * bs * hd, 4, bt, 1, Hq, Hkv, hd, bs, 0.17).reshape(Hq, hd)
+    v0 = orc.from_bf16(vp[2, :, 0, :])
+    for h in range(Hq):
+        assert np.array_equal(out[h], v0[h // 4])
+
+
+def test_attention_stride_not_a_row_multiple(orc):
+    """A block stride that is no multiple of head_dim cannot be read as rows of a 2-D
+    tensor; the kernel of bulk copies serves it, with the same results."""
+    Hq, Hkv, hd, bs, ctx = 32, 8, 64, 16, 200
+    nblk = (ctx + bs - 1) // bs
+    stride = Hkv * bs * hd + 8
+    raw_k = synth.normal(9300, nblk * stride + 8)
+    raw_v = synth.normal(9301, nblk * stride + 8)
+    kp, vp = orc.to_bf16(raw_k), orc.to_bf16(raw_v)
+    bt = synth.permutation(9302, nblk).astype(np.int32)
+    q = synth.normal(9303, Hq * hd)
+    out = _attn_gpu(q, kp, vp, stride, nblk, bt, ctx, Hq, Hkv, hd, bs, 0.125)
+    ref = orc.attention_paged(q, kp, vp, stride, bt, ctx, Hq, Hkv, hd, bs, 0.125)
+    attn_close(out, ref)
+
+
+@pytest.mark.parametrize("hd", [32, 64])
+def test_attention_bad_block_id_latches_error_any_kernel(orc, hd):
+    Hq, Hkv, bs = 8, 2, 16
+    kp, vp = _pool(orc, 9400 + hd, 4, Hkv, bs, hd)
+    q = synth.normal(9401, Hq * hd)
+    mie.mie_check()
+    bt = np.array([1, 9, 0], np.int32)  # 9 is outside the 4-block pool
+    _attn_gpu(q, kp, vp, Hkv * bs * hd, 4, bt, 40, Hq, Hkv, hd, bs, 0.17)
+    with pytest.raises(mie.MieError) as e:
+        mie.mie_check()
+    assert e.value.status == 7
+    mie.mie_check()
+
+
 def test_attention_bad_block_id_latches_error(orc):
     Hq, Hkv, hd, bs = 8, 2, 32, 16
     kp, vp = _pool(orc, 9100, 4, Hkv, bs, hd)
