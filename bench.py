@@ -654,7 +654,8 @@ def run_mie(args, shape):
     barrier(pg)
     dt = max_over_ranks(pg, dt_local)
 
-    # end to end: host token and position in, argmax read back every step
+    # end to end through mie_decode_step_sync: host token and position in (a pinned upload
+    # of the step parameters), the next token read back to the host every step
     pos = args.ctx + args.warmup + args.steps
     with torch.cuda.stream(stream):
         tok = int(am.item())
@@ -663,9 +664,7 @@ def run_mie(args, shape):
     with NoGC():
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            gm.decode_step(tok, pos, bt, logits, am)
-            with torch.cuda.stream(stream):  # the read is ordered after the step on its stream
-                tok = int(am.item())  # device -> host read of the step's result (synchronises)
+            tok = gm.decode_step_sync(tok, pos, bt, logits)
             pos += 1
         gm.sync()
         e2e_dt_local = (time.perf_counter() - t0) / args.e2e_steps

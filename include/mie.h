@@ -394,6 +394,16 @@ mie_status mie_kv_writable(mie_ctx *ctx, int32_t *table, int pos, int32_t *block
 mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, const int32_t *block_table,
                            int n_blocks, float *logits_out, int32_t *argmax_out);
 
+/* One decode step with host input and output ([RUST] "How a Llama model generates text":
+ * the argmax of a step's logits is the next token): mie_decode_step for the token at
+ * position pos, then the step's next token (its argmax, or the sampler's draw under
+ * mie_set_sampling) copied back to the host int32 *next_token, waiting for the step.
+ * block_table: device int32 [n_blocks]; logits_out: device fp32 [vocab] or NULL.
+ * Errors as mie_decode_step; MIE_E_ARG for a null next_token, MIE_E_OOM if its small
+ * device and pinned host buffers (allocated on the first call) cannot be had. */
+mie_status mie_decode_step_sync(mie_ctx *ctx, int32_t token, int32_t pos, const int32_t *block_table,
+                                int n_blocks, float *logits_out, int32_t *next_token);
+
 /* Greedy continuation: replays the step n_steps times with token = previous argmax
  * and pos = previous pos + 1, all on the device.  Requires one mie_decode_step first
  * (which fixes block table and outputs); the outputs hold the last step's results. */

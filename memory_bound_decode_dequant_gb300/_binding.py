@@ -91,6 +91,7 @@ _SIGS = {
     "mie_kv_copy_block": (I, [P, ctypes.c_int32, ctypes.c_int32]),
     "mie_kv_writable": (I, [P, P, I, ctypes.POINTER(ctypes.c_int32)]),
     "mie_decode_step": (I, [P, ctypes.c_int32, ctypes.c_int32, P, I, P, P]),
+    "mie_decode_step_sync": (I, [P, ctypes.c_int32, ctypes.c_int32, P, I, P, P]),
     "mie_decode_continue": (I, [P, I]),
     "mie_decode_step_slots": (I, [P, I, P, P, P, I, P, P]),
     "mie_sync": (I, [P]),
@@ -528,6 +529,17 @@ class Model:
                                      None if argmax_out is None else _dev(argmax_out, torch.int32, "argmax")),
                "mie_decode_step")
 
+    def decode_step_sync(self, token: int, pos: int, block_table, logits_out=None) -> int:
+        """One step with host token / position in and the next token read back (waits)."""
+        torch = _torch()
+        nxt = ctypes.c_int32(0)
+        _check(lib().mie_decode_step_sync(self.h, int(token), int(pos), _dev(block_table, torch.int32, "block_table"),
+                                          block_table.numel(),
+                                          None if logits_out is None else _dev(logits_out, torch.float32, "logits"),
+                                          ctypes.byref(nxt)),
+               "mie_decode_step_sync")
+        return int(nxt.value)
+
     def decode_continue(self, n_steps: int):
         _check(lib().mie_decode_continue(self.h, n_steps), "mie_decode_continue")
 
@@ -721,6 +733,10 @@ def mie_decode_step(ctx: Model, token: int, pos: int, block_table, logits_out=No
     ctx.decode_step(token, pos, block_table, logits_out, argmax_out)
 
 
+def mie_decode_step_sync(ctx: Model, token: int, pos: int, block_table, logits_out=None) -> int:
+    return ctx.decode_step_sync(token, pos, block_table, logits_out)
+
+
 def mie_decode_continue(ctx: Model, n_steps: int) -> None:
     ctx.decode_continue(n_steps)
 
@@ -815,7 +831,7 @@ __all__ += ["mie_last_error", "mie_status_string", "mie_pool_create", "mie_pool_
             "mie_pool_incref", "mie_pool_decref", "mie_pool_refcount", "mie_pool_free_count",
             "mie_pool_writable", "mie_create", "mie_destroy", "mie_load_weights", "mie_ctx_pool",
             "mie_kv_pool", "mie_kv_block_elems", "mie_kv_copy_block", "mie_kv_writable", "mie_decode_step",
-            "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
+            "mie_decode_step_sync", "mie_decode_continue", "mie_decode_step_slots", "mie_set_step_mode", "mie_step_mode",
             "mie_set_trace", "mie_set_sampling", "mie_debug_stall", "mie_sync", "mie_verify_step", "mie_prefill", "mie_generate",
             "mie_lookup_propose", "SpecGate", "mie_spec_gate_bytes", "mie_spec_gate_init", "mie_spec_gate_open",
             "mie_spec_gate_record", "mie_step_launches", "mie_slot_step_launches"]

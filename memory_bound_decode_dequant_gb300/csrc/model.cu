@@ -145,6 +145,7 @@ struct mie_ctx {
   int32_t *verify_table = nullptr;  // [kMaxSlots][verify_cap] copies of one sequence's table
   int verify_cap = 0;
   int32_t *gen_argmax = nullptr;    // [kMaxSlots]
+  int32_t *next_pinned = nullptr;   // mie_decode_step_sync: the step's token, read back
   // prompt prefill on the tensor cores (mie_prefill): buffers for chunks of up to
   // prefill_chunk positions, allocated on the first call
   int prefill_chunk = 0;
@@ -216,6 +217,7 @@ extern "C" void mie_destroy(mie_ctx *ctx) {
   for (cudaEvent_t ev : ctx->sp_uploaded)
     if (ev) cudaEventDestroy(ev);
   if (ctx->sp_pinned) cudaFreeHost(ctx->sp_pinned);
+  if (ctx->next_pinned) cudaFreeHost(ctx->next_pinned);
   if (ctx->own_stream && ctx->stream) cudaStreamDestroy(ctx->stream);
   mie_pool_destroy(ctx->pool);
   delete ctx;
@@ -848,6 +850,24 @@ extern "C" mie_status mie_decode_step(mie_ctx *ctx, int32_t token, int32_t pos, 
     if (s != MIE_OK) return s;
   }
   return run_step(ctx);
+}
+
+extern "C" mie_status mie_decode_step_sync(mie_ctx *ctx, int32_t token, int32_t pos, const int32_t *block_table,
+                                           int n_blocks, float *logits_out, int32_t *next_token) {
+  if (!ctx || !next_token) return fail(MIE_E_ARG, "mie_decode_step_sync: null pointer");
+  if (!ctx->gen_argmax && !(ctx->gen_argmax = (int32_t *)ctx->dalloc(sizeof(int32_t) * kMaxSlots)))
+    return fail(MIE_E_OOM, "mie_decode_step_sync: device buffer");
+  if (!ctx->next_pinned && cudaMallocHost((void **)&ctx->next_pinned, sizeof(int32_t)) != cudaSuccess) {
+    ctx->next_pinned = nullptr;
+    cudaGetLastError();
+    return fail(MIE_E_OOM, "mie_decode_step_sync: pinned host buffer");
+  }
+  const mie_status s = mie_decode_step(ctx, token, pos, block_table, n_blocks, logits_out, ctx->gen_argmax);
+  if (s != MIE_OK) return s;
+  MIE_CUDA(cudaMemcpyAsync(ctx->next_pinned, ctx->gen_argmax, sizeof(int32_t), cudaMemcpyDeviceToHost, ctx->stream));
+  MIE_CUDA(cudaStreamSynchronize(ctx->stream));
+  *next_token = *ctx->next_pinned;
+  return MIE_OK;
 }
 
 extern "C" mie_status mie_decode_continue(mie_ctx *ctx, int n_steps) {

@@ -172,6 +172,43 @@ def test_device_continuation_matches_host_steps(orc, step_mode):
     assert outs[0][1] == outs[1][1]
 
 
+def test_decode_step_sync_gives_the_steps_tokens(orc):
+    """mie_decode_step_sync (host token in, next token out, waiting) gives the tokens and
+    logit bits of mie_decode_step followed by a read of its argmax."""
+    shape = synth.TINY
+    n_blocks, max_pos = 8, 128
+    bt = torch.from_numpy(synth.permutation(12, n_blocks).astype(np.int32)).cuda()
+    toks = [int(t) for t in prompt_tokens(shape, 6)]
+    outs = []
+    for sync in (False, True):
+        gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+        logits = torch.empty(shape.vocab, dtype=torch.float32, device="cuda")
+        am = torch.empty(1, dtype=torch.int32, device="cuda")
+        seq, tok = [], toks[0]
+        for pos in range(20):
+            if pos < len(toks):
+                tok = toks[pos]
+            if sync:
+                nxt = gm.decode_step_sync(tok, pos, bt, logits)
+            else:
+                gm.decode_step(tok, pos, bt, logits, am)
+                gm.sync()
+                nxt = int(am.item())
+            seq.append(nxt)
+            tok = nxt
+        gm.sync()
+        outs.append((seq, logits.cpu().numpy()))
+        gm.close()
+    assert outs[0][0] == outs[1][0]
+    assert np.array_equal(outs[0][1].view(np.uint32), outs[1][1].view(np.uint32))
+    with pytest.raises(mie.MieError):
+        gm = build_gpu_model(shape, n_kv_blocks=n_blocks, max_pos=max_pos)
+        try:
+            gm.decode_step_sync(shape.vocab, 0, bt)  # token outside the vocabulary
+        finally:
+            gm.close()
+
+
 @pytest.mark.parametrize("step_mode", [PERSISTENT, CHAIN])
 def test_back_to_back_host_steps_without_waiting(orc, step_mode):
     """30 host-driven steps enqueued with no host wait between them (more than the ring
