@@ -115,8 +115,7 @@ __device__ __forceinline__ uint32_t q4_pair(uint32_t n0, uint32_t n1) {
 struct SlotShared {
   float ss[kSW][kMaxSlots];                    // per-warp sums of squares (RMSNorm)
   float rs[kMaxSlots];                         // RMSNorm scale per slot
-  float red[kSMaxNst][kSW][kMaxSlots][kSRows];  // warp partials of the stage in each ring slot
-  unsigned cnt[kSMaxNst];                      // warps done with the stage in each ring slot
+  unsigned cnt[2][kSMaxNst];                   // warps done with the stage, per ring cycle parity and slot
   float acc[kSMaxAccTiles][kMaxSlots][kSRows];  // partial sums across slices
   unsigned long long best[kMaxSlots];          // argmax per slot: orderable value << 32 | ~row
   int pos[kMaxSlots], blk[kMaxSlots], tok[kMaxSlots];
@@ -148,6 +147,7 @@ struct SlotPlan {
   uint32_t x_off = 0, x_pitch = 0;      // the slots' input slice after the ring: [kMaxSlots][x_pitch]
   uint32_t pitch = 0, stage_bytes = 0;  // padded row bytes in shared memory, bytes per slot
   uint32_t sc_off = 0;                  // Q4_0: offset of the stage's scale rows (128 bytes each)
+  uint32_t red_off = 0;                 // warp partials [2 cycle parities][nst][kSW][kMaxSlots][kSRows] floats
   int n_tiles = 0, KS = 1;
   size_t smem = 0;
 };
@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
     s_abort = 0;
     s_x_ready = 0;
     s_x_last = -1;
-    for (int i = 0; i < kSMaxNst; ++i) sh.cnt[i] = 0u;
+    for (int i = 0; i < kSMaxNst; ++i) sh.cnt[0][i] = sh.cnt[1][i] = 0u;
     for (int i = 0; i < kMaxSlots; ++i) sh.best[i] = 0ull;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -501,13 +501,21 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
       }
       // c[0], c[1] = Y[row 2t, 2t+1][slot g] of this warp's k-steps
       // hi + lo parts (Q4_0 carries them summed in c0[0], c0[1])
-      sh.red[slot][warp][g][2 * t] = ((c0[0] + c0[2]) + (c1[0] + c1[2])) + ((c2[0] + c2[2]) + (c3[0] + c3[2]));
-      sh.red[slot][warp][g][2 * t + 1] = ((c0[1] + c0[3]) + (c1[1] + c1[3])) + ((c2[1] + c2[3]) + (c3[1] + c3[3]));
+      const int par = k & 1;  // the stage's ring cycle parity picks its partial buffers
+      float *rs = reinterpret_cast<float *>(smem + pl.red_off) + (size_t)(par * pl.nst + slot) * (kSW * kMaxSlots * kSRows);
+      rs[(warp * kMaxSlots + g) * kSRows + 2 * t] = ((c0[0] + c0[2]) + (c1[0] + c1[2])) + ((c2[0] + c2[2]) + (c3[0] + c3[2]));
+      rs[(warp * kMaxSlots + g) * kSRows + 2 * t + 1] =
+          ((c0[1] + c0[3]) + (c1[1] + c1[3])) + ((c2[1] + c2[3]) + (c3[1] + c3[3]));
       __threadfence_block();
       __syncwarp();
       unsigned prev = 0u;
-      if (lane == 0) prev = atomicAdd(&sh.cnt[slot], 1u);
+      if (lane == 0) prev = atomicAdd(&sh.cnt[par][slot], 1u);
       prev = __shfl_sync(0xffffffffu, prev, 0);
+      // the stage's weights are in registers and consumed: the slot goes back to the
+      // producer now, and the last warp's sums and epilogue below overlap the next stages
+      // (their partials live in buffers of their own, two per slot by ring cycle, reused
+      // only after every warp has passed the next cycle of the slot)
+      if (lane == 0) mbar_arrive(&empty_bar[slot]);
       if (prev == kSW - 1) {  // the last warp of this stage
         __threadfence_block();
         const int r0 = (tt0 + tl) * kSRows;
@@ -516,16 +524,15 @@ __global__ void __launch_bounds__(kST, 1) gemv_slots_kernel(const GemvArgs a, co
           const int i = lane + 32 * h, es = i >> 3, er = i & 7;
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < kSW; ++w) v += sh.red[slot][w][es][er];
+          for (int w = 0; w < kSW; ++w) v += rs[(w * kMaxSlots + es) * kSRows + er];
           if (q > 0) v += sh.acc[tl][es][er];
           if (q + 1 < pl.KS) sh.acc[tl][es][er] = v;
           else epilogue(r0, es, er, v);
         }
-        if (lane == 0) sh.cnt[slot] = 0u;
+        if (lane == 0) sh.cnt[par][slot] = 0u;
         __threadfence_block();
         __syncwarp();
       }
-      if (lane == 0) mbar_arrive(&empty_bar[slot]);
     }
   }
   if (SSync::any(!ok || s_abort)) {
@@ -605,10 +612,12 @@ static SlotPlan slot_plan(const DevMat &m, int grid) {
   p.x_pitch = (uint32_t)(slice * 4 + 64);  // slot rows 16 banks apart: a quarter warp's 16-byte reads cover 2 rows
   const long x_bytes = (long)kMaxSlots * p.x_pitch;
   const long avail = (long)max_smem - (long)sizeof(SlotShared) - 1024 - x_bytes;
-  int nst = (int)(avail / (long)p.stage_bytes);
+  const long red_stage = 2L * kSW * kMaxSlots * kSRows * 4;  // partial buffers of one ring slot
+  int nst = (int)(avail / ((long)p.stage_bytes + red_stage));
   p.nst = nst > kSMaxNst ? kSMaxNst : nst;
   p.x_off = (uint32_t)p.nst * p.stage_bytes;
-  p.smem = (size_t)p.x_off + (size_t)x_bytes;
+  p.red_off = (uint32_t)((p.x_off + x_bytes + 15) / 16 * 16);
+  p.smem = (size_t)p.red_off + (size_t)p.nst * red_stage;
   (void)grid;
   return p;
 }
