@@ -50,58 +50,57 @@ __device__ __forceinline__ void chunk_fma<MIE_FMT_BF16>(const uint4 &w, const fl
   }
 }
 
+// The quantised formats read their codes as subnormal floats.  A code n of b bits left
+// in place at bit offset p, every other bit cleared, is the float n 2^(p-149) as long as
+// the word stays below 2^24 (exponent field 0 or 1, where the value of the bits is the
+// integer times 2^-149).  The input registers hold x 2^(85-p), so one packed FMA adds
+// n x 2^-64 with a single rounding; the chunk's sum times 2^64 plus the lane's bias term
+// (-128 or -8 times the sum of its inputs, formed once when the inputs are loaded) is
+// then the dot product with the signed codes.  This leaves one packed FMA per two
+// codes in the inner loop, where a biased-mantissa form also needs a packed add.
+// Flush-to-zero would erase every code, so these kernels are never built with it.
+#if defined(__USE_FAST_MATH__)
+#error "the quantised dot products need subnormal floats: build without fast math"
+#endif
+template <uint32_t MASK>
+__device__ __forceinline__ float code_bits(uint32_t a) {
+  return __uint_as_float(a & MASK);
+}
+
+// int8 chunk: word t holds elements 4t..4t+3, byte j = element 4t+j; b ^ 0x80 = b + 128
+// is the unsigned code.  Bytes 0..2 are read in place (p = 0, 8, 16); byte 3 is moved
+// down to byte 2 (p = 16), since in place it would reach the exponent's upper bits.
 template <>
 __device__ __forceinline__ void chunk_fma<MIE_FMT_I8>(const uint4 &w, const float2 *xr, float2 *acc) {
   const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-  const float2 bias = make_float2(-8388736.f, -8388736.f);  // -(2^23 + 128)
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
-    const uint32_t u = v[t] ^ 0x80808080u;  // int8 b -> b + 128 in 0..255
-    const float2 a = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7440)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7441)));
-    const float2 b = make_float2(__uint_as_float(__byte_perm(u, 0x4B000000u, 0x7442)),
-                                 __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7443)));
-    acc[t] = __ffma2_rn(__fadd2_rn(a, bias), xr[2 * t], acc[t]);
-    acc[t] = __ffma2_rn(__fadd2_rn(b, bias), xr[2 * t + 1], acc[t]);
+    const uint32_t u = v[t] ^ 0x80808080u;
+    const float2 a = make_float2(code_bits<0xFFu>(u), code_bits<0xFF00u>(u));
+    const float2 b = make_float2(code_bits<0xFF0000u>(u), __uint_as_float(__byte_perm(u, 0u, 0x4344)));
+    acc[t] = __ffma2_rn(a, xr[2 * t], acc[t]);
+    acc[t] = __ffma2_rn(b, xr[2 * t + 1], acc[t]);
   }
-}
-
-// (a & MASK) | bits of 2^23, as one LOP3.  Written with C++ operators, the same
-// expressions were measured on GB300 to cost two integer-pipe instructions per code
-// (69 instead of 38 per 32-code chunk), and that pipe set the pace of the Q4_0 GEMVs.
-template <uint32_t MASK>
-__device__ __forceinline__ float mant_code(uint32_t a) {
-  uint32_t d;
-  asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "n"(MASK), "n"(0x4B000000u));  // (a & b) | c
-  return __uint_as_float(d);
 }
 
 // Q4_0 chunk = one block: word t holds bytes 4t..4t+3; byte j carries element j (low
 // nibble) and element j+16 (high nibble).  Unpack order per word, with the bit offset
 // p the code sits at: 4t(p0) 4t+16(p4) 4t+1(p8) 4t+17(p12) 4t+2(p16), then from
-// w >> 12: 4t+18(p8) 4t+3(p12) 4t+19(p16).  The input registers hold x * 2^-p in
-// that order, so (2^23 + n 2^p) - (2^23 + 8 2^p) = (n - 8) 2^p times them is
-// (n - 8) x.
+// w >> 12: 4t+18(p8) 4t+3(p12) 4t+19(p16); load_xr puts x 2^(85-p) in that order.
 template <>
 __device__ __forceinline__ void chunk_fma<MIE_FMT_Q4_0>(const uint4 &w, const float2 *xr, float2 *acc) {
   const uint32_t v[4] = {w.x, w.y, w.z, w.w};
-  const float2 b01 = make_float2(-8388616.f, -8388736.f);  // -(2^23 + 8 * {1, 16})
-  const float2 b23 = make_float2(-8390656.f, -8421376.f);  // -(2^23 + 8 * {256, 4096})
-  const float2 b45 = make_float2(-8912896.f, -8390656.f);  // -(2^23 + 8 * {65536, 256})
-  const float2 b67 = make_float2(-8421376.f, -8912896.f);  // -(2^23 + 8 * {4096, 65536})
 #pragma unroll
   for (int t = 0; t < 4; ++t) {
     const uint32_t a = v[t], s = v[t] >> 12;
-    const float2 d01 = __fadd2_rn(make_float2(mant_code<0xFu>(a), mant_code<0xF0u>(a)), b01);
-    const float2 d23 = __fadd2_rn(make_float2(mant_code<0xF00u>(a), mant_code<0xF000u>(a)), b23);
-    const float2 d45 = __fadd2_rn(make_float2(mant_code<0xF0000u>(a), mant_code<0xF00u>(s)), b45);
-    const float2 d67 = __fadd2_rn(make_float2(mant_code<0xF000u>(s), mant_code<0xF0000u>(s)), b67);
-    acc[t] = __ffma2_rn(d01, xr[4 * t + 0], acc[t]);
-    acc[t] = __ffma2_rn(d23, xr[4 * t + 1], acc[t]);
-    acc[t] = __ffma2_rn(d45, xr[4 * t + 2], acc[t]);
-    acc[t] = __ffma2_rn(d67, xr[4 * t + 3], acc[t]);
+    acc[t] = __ffma2_rn(make_float2(code_bits<0xFu>(a), code_bits<0xF0u>(a)), xr[4 * t + 0], acc[t]);
+    acc[t] = __ffma2_rn(make_float2(code_bits<0xF00u>(a), code_bits<0xF000u>(a)), xr[4 * t + 1], acc[t]);
+    acc[t] = __ffma2_rn(make_float2(code_bits<0xF0000u>(a), code_bits<0xF00u>(s)), xr[4 * t + 2], acc[t]);
+    acc[t] = __ffma2_rn(make_float2(code_bits<0xF000u>(s), code_bits<0xF0000u>(s)), xr[4 * t + 3], acc[t]);
   }
 }
+
+constexpr float kCodeScale = 18446744073709551616.f;  // 2^64, undoes the registers' 2^-64
 
 // Staged input vectors keep four spare floats after every 32 elements: element k sits
 // at xs_at(k).  A lane's chunk (8, 16 or 32 consecutive elements) then starts 36, 18
@@ -111,22 +110,33 @@ __host__ __device__ constexpr int xs_at(int k) { return k + ((k >> 5) << 2); }
 __host__ __device__ constexpr int xs_floats(int Kp) { return Kp + ((Kp + 31) >> 5) * 4; }
 
 // Input registers of one chunk (elements e .. e+EPC-1, e a multiple of EPC) from the
-// staged vector xs.
+// staged vector xs, in chunk_fma's order and scaling; nb gets the chunk's bias term
+// (-8 or -128 times the sum of its inputs for Q4_0 and int8, 0 for bf16).
 template <int F>
-__device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr) {
+__device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr, float &nb) {
   constexpr int EPC = FmtT<F>::EPC;
   const float4 *q4 = reinterpret_cast<const float4 *>(xs + xs_at(e));
+  float sx = 0.f;
   if constexpr (F == MIE_FMT_Q4_0) {
-    // the unpack order of chunk_fma and the powers of two that undo each code's bit
-    // offset are fixed per register
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
       const float4 a = q4[t], b = q4[t + 4];  // elements 4t.. and 4t+16..
-      xr[4 * t + 0] = make_float2(a.x, b.x * 0.0625f);
-      xr[4 * t + 1] = make_float2(a.y * 0.00390625f, b.y * 0.000244140625f);
-      xr[4 * t + 2] = make_float2(a.z * 1.52587890625e-05f, b.z * 0.00390625f);
-      xr[4 * t + 3] = make_float2(a.w * 0.000244140625f, b.w * 1.52587890625e-05f);
+      xr[4 * t + 0] = make_float2(a.x * 0x1p85f, b.x * 0x1p81f);  // p 0, 4
+      xr[4 * t + 1] = make_float2(a.y * 0x1p77f, b.y * 0x1p73f);  // p 8, 12
+      xr[4 * t + 2] = make_float2(a.z * 0x1p69f, b.z * 0x1p77f);  // p 16, 8
+      xr[4 * t + 3] = make_float2(a.w * 0x1p73f, b.w * 0x1p69f);  // p 12, 16
+      sx += ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
     }
+    nb = -8.f * sx;
+  } else if constexpr (F == MIE_FMT_I8) {
+#pragma unroll
+    for (int i = 0; i < EPC / 4; ++i) {
+      const float4 q = q4[i];
+      xr[2 * i] = make_float2(q.x * 0x1p85f, q.y * 0x1p77f);      // p 0, 8
+      xr[2 * i + 1] = make_float2(q.z * 0x1p69f, q.w * 0x1p69f);  // p 16, 16
+      sx += (q.x + q.y) + (q.z + q.w);
+    }
+    nb = -128.f * sx;
   } else {
 #pragma unroll
     for (int i = 0; i < EPC / 4; ++i) {
@@ -134,6 +144,7 @@ __device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr) {
       xr[2 * i] = make_float2(q.x, q.y);
       xr[2 * i + 1] = make_float2(q.z, q.w);
     }
+    nb = 0.f;
   }
 }
 
@@ -240,11 +251,11 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 // loads cost one shared-memory latency.  Chunks at or
 // past Kp are read from the slice start instead (always staged) and meet zero input
 // registers, so they add exact zeros.  nrows (<= RPW) rows are valid; the others read
-// the first row.
+// the first row.  nb holds load_xr's bias terms of the lane's chunks (0 past Kp).
 template <int F>
 __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes, uint32_t sc, uint32_t s_bytes,
-                                               int nrows, const float2 *xr, int e0, int Kp, int lane,
-                                               float (&sum)[FmtT<F>::RPW], int gshift = 0) {
+                                               int nrows, const float2 *xr, const float *nb, int e0, int Kp,
+                                               int lane, float (&sum)[FmtT<F>::RPW], int gshift = 0) {
   using T = FmtT<F>;
   constexpr int EPC = T::EPC, CPL = T::CPL, R = T::RPW, kChunkStride = 32 * EPC;
   uint4 w[R][CPL];
@@ -271,7 +282,7 @@ __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes,
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         chunk_fma<F>(w[i][c], xr + c * (EPC / 2), acc);
         const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-        acc_s = fmaf(__half2float(__ushort_as_half((unsigned short)hb[i][c])), cs, acc_s);
+        acc_s = fmaf(__half2float(__ushort_as_half((unsigned short)hb[i][c])), fmaf(cs, kCodeScale, nb[c]), acc_s);
       }
       sum[i] = acc_s;
     }
@@ -281,7 +292,15 @@ __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes,
       float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < CPL; ++c) chunk_fma<F>(w[i][c], xr + c * (EPC / 2), acc);
-      sum[i] = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+      const float t = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+      if constexpr (F == MIE_FMT_I8) {
+        float b = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) b += nb[c];
+        sum[i] = fmaf(t, kCodeScale, b);
+      } else {
+        sum[i] = t;
+      }
     }
   }
 }

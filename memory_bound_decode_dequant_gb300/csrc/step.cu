@@ -279,14 +279,16 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   const bool has_slice = warp < rr.WR * rr.KS;
   const int e0 = ks * kSlice + lane * EPC;
   float2 xr[CPL * EPC / 2];
+  float nb[CPL];
 #pragma unroll
   for (int c = 0; c < CPL; ++c) {
     const int e = e0 + c * kChunkStride;
     if (has_slice && e < Kp) {
-      load_xr<F>(xs, e, xr + c * (EPC / 2));
+      load_xr<F>(xs, e, xr + c * (EPC / 2), nb[c]);
     } else {
 #pragma unroll
       for (int i = 0; i < EPC / 2; ++i) xr[c * (EPC / 2) + i] = make_float2(0.f, 0.f);
+      nb[c] = 0.f;
     }
   }
   SUB_STAMP(2);
@@ -312,7 +314,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
       const uint32_t sca = smem_u32(ring.sc) + (uint32_t)slot * ring.slot_sc_bytes +
                            (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice >> (5 + m.gshift))) * 2;
       float sum[RPW];
-      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, e0, Kp, lane, sum,
+      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, nb, e0, Kp, lane, sum,
                         m.gshift);
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {
