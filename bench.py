@@ -131,6 +131,7 @@ class Clocks:
         self.idx = gpu_index
         self.rows = []
         self._stop = threading.Event()
+        self._first = threading.Event()
         self._t = None
 
     def _run(self):
@@ -143,11 +144,15 @@ class Clocks:
                     self.rows.append([c.strip() for c in out.split(",")])
             except Exception:
                 pass
+            self._first.set()
             self._stop.wait(0.2)
 
     def __enter__(self):
         self._t = threading.Thread(target=self._run, daemon=True)
         self._t.start()
+        # the sampler's first query (process start, NVML set-up) ends before the timed
+        # region begins; the later ones fall inside it
+        self._first.wait(timeout=6)
         return self
 
     def __exit__(self, *a):
