@@ -53,12 +53,16 @@ __device__ __forceinline__ void chunk_fma<MIE_FMT_BF16>(const uint4 &w, const fl
 // The quantised formats read their codes as subnormal floats.  A code n of b bits left
 // in place at bit offset p, every other bit cleared, is the float n 2^(p-149) as long as
 // the word stays below 2^24 (exponent field 0 or 1, where the value of the bits is the
-// integer times 2^-149).  The input registers hold x 2^(85-p), so one packed FMA adds
-// n x 2^-64 with a single rounding; the chunk's sum times 2^64 plus the lane's bias term
-// (-128 or -8 times the sum of its inputs, formed once when the inputs are loaded) is
-// then the dot product with the signed codes.  This leaves one packed FMA per two
-// codes in the inner loop, where a biased-mantissa form also needs a packed add.
-// Flush-to-zero would erase every code, so these kernels are never built with it.
+// integer times 2^-149).  The input registers hold x 2^(126-p-E), where E is the binary
+// exponent of the largest |x| of the registers' group (a Q4_0 chunk, or all of an int8
+// lane's chunks) clamped to [-1, 104]: every register stays below 2^127, and one packed
+// FMA adds n x 2^-(E+23) with a single rounding, a normal float for every x down to
+// 2^-103 of the group's largest.  The group's sum times 2^(E+23) plus its bias term (-8
+// or -128 times the sum of its inputs, formed when the inputs are loaded) is then the
+// dot product with the signed codes.  This leaves one packed FMA per two codes in the
+// inner loop, where a biased-mantissa form also needs a packed add.  Inputs of 2^105 or
+// more in magnitude overflow the registers.  Flush-to-zero would erase every code, so
+// these kernels are never built with it.
 #if defined(__USE_FAST_MATH__)
 #error "the quantised dot products need subnormal floats: build without fast math"
 #endif
@@ -100,8 +104,6 @@ __device__ __forceinline__ void chunk_fma<MIE_FMT_Q4_0>(const uint4 &w, const fl
   }
 }
 
-constexpr float kCodeScale = 18446744073709551616.f;  // 2^64, undoes the registers' 2^-64
-
 // Staged input vectors keep four spare floats after every 32 elements: element k sits
 // at xs_at(k).  A lane's chunk (8, 16 or 32 consecutive elements) then starts 36, 18
 // or 9 float4 slots after its neighbour's, so the float4 reads of a warp fill the 32
@@ -109,42 +111,107 @@ constexpr float kCodeScale = 18446744073709551616.f;  // 2^64, undoes the regist
 __host__ __device__ constexpr int xs_at(int k) { return k + ((k >> 5) << 2); }
 __host__ __device__ constexpr int xs_floats(int Kp) { return Kp + ((Kp + 31) >> 5) * 4; }
 
-// Input registers of one chunk (elements e .. e+EPC-1, e a multiple of EPC) from the
-// staged vector xs, in chunk_fma's order and scaling; nb gets the chunk's bias term
-// (-8 or -128 times the sum of its inputs for Q4_0 and int8, 0 for bf16).
+// 2^k for -126 <= k <= 127
+__device__ __forceinline__ float pow2i(int k) { return __uint_as_float((uint32_t)(k + 127) << 23); }
+
+// Largest |value| and sum of the N float pairs v, both by pairwise trees (short
+// dependency chains: this runs at the start of every GEMV phase).
+template <int N>
+__device__ __forceinline__ void group_max_sum(const float2 *v, float &m, float &sum) {
+  float mx[N], sm[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    mx[i] = fmaxf(fabsf(v[i].x), fabsf(v[i].y));
+    sm[i] = v[i].x + v[i].y;
+  }
+#pragma unroll
+  for (int w = N / 2; w >= 1; w /= 2) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      mx[i] = fmaxf(mx[i], mx[i + w]);
+      sm[i] += sm[i + w];
+    }
+  }
+  m = mx[0];
+  sum = sm[0];
+}
+
+// The exponent E of the subnormal-code scaling for a group whose largest |x| is m.
+__device__ __forceinline__ int code_exp(float m) {
+  const int e = (int)((__float_as_uint(m) >> 23) & 0xFFu) - 127;
+  return min(max(e, -1), 104);
+}
+
+// A lane's input registers for a phase, from the staged vector xs: chunk c covers
+// elements e0 + c*32*EPC .. +EPC-1 (zeros where the lane has no slice or the chunk is
+// at or past Kp), in chunk_fma's order and scaling.  nb and cs get the bias terms and
+// the scales 2^(E+23) that stage_rows_dot applies: per chunk for Q4_0, nb[0] and cs[0]
+// for the whole lane for int8, none for bf16.
 template <int F>
-__device__ __forceinline__ void load_xr(const float *xs, int e, float2 *xr, float &nb) {
-  constexpr int EPC = FmtT<F>::EPC;
-  const float4 *q4 = reinterpret_cast<const float4 *>(xs + xs_at(e));
-  float sx = 0.f;
+__device__ __forceinline__ void load_lane_xr(const float *xs, int e0, int Kp, bool has_slice, float2 *xr, float *nb,
+                                             float *cs) {
+  using T = FmtT<F>;
+  constexpr int EPC = T::EPC, CPL = T::CPL, R = EPC / 2;  // R registers per chunk
+#pragma unroll
+  for (int c = 0; c < CPL; ++c) {
+    const int e = e0 + c * 32 * EPC;
+    float2 *r = xr + c * R;
+    if (has_slice && e < Kp) {
+      const float4 *q4 = reinterpret_cast<const float4 *>(xs + xs_at(e));
+      if constexpr (F == MIE_FMT_Q4_0) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {  // register 4t+j pairs elements 4t+j and 4t+16+j
+          const float4 a = q4[t], b = q4[t + 4];
+          r[4 * t + 0] = make_float2(a.x, b.x);
+          r[4 * t + 1] = make_float2(a.y, b.y);
+          r[4 * t + 2] = make_float2(a.z, b.z);
+          r[4 * t + 3] = make_float2(a.w, b.w);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < EPC / 4; ++i) {
+          const float4 q = q4[i];
+          r[2 * i] = make_float2(q.x, q.y);
+          r[2 * i + 1] = make_float2(q.z, q.w);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < R; ++i) r[i] = make_float2(0.f, 0.f);
+    }
+  }
   if constexpr (F == MIE_FMT_Q4_0) {
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const float4 a = q4[t], b = q4[t + 4];  // elements 4t.. and 4t+16..
-      xr[4 * t + 0] = make_float2(a.x * 0x1p85f, b.x * 0x1p81f);  // p 0, 4
-      xr[4 * t + 1] = make_float2(a.y * 0x1p77f, b.y * 0x1p73f);  // p 8, 12
-      xr[4 * t + 2] = make_float2(a.z * 0x1p69f, b.z * 0x1p77f);  // p 16, 8
-      xr[4 * t + 3] = make_float2(a.w * 0x1p73f, b.w * 0x1p69f);  // p 12, 16
-      sx += ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+    for (int c = 0; c < CPL; ++c) {
+      float2 *r = xr + c * R;
+      float m, sx;
+      group_max_sum<R>(r, m, sx);
+      const int E = code_exp(m);
+      // bit offsets of the pairs: (0, 4), (8, 12), (16, 8), (12, 16)
+      const float s0 = pow2i(126 - E), s4 = pow2i(122 - E), s8 = pow2i(118 - E), s12 = pow2i(114 - E),
+                  s16 = pow2i(110 - E);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        r[4 * t + 0] = make_float2(r[4 * t + 0].x * s0, r[4 * t + 0].y * s4);
+        r[4 * t + 1] = make_float2(r[4 * t + 1].x * s8, r[4 * t + 1].y * s12);
+        r[4 * t + 2] = make_float2(r[4 * t + 2].x * s16, r[4 * t + 2].y * s8);
+        r[4 * t + 3] = make_float2(r[4 * t + 3].x * s12, r[4 * t + 3].y * s16);
+      }
+      nb[c] = -8.f * sx;
+      cs[c] = pow2i(E + 23);
     }
-    nb = -8.f * sx;
   } else if constexpr (F == MIE_FMT_I8) {
+    float m, sx;
+    group_max_sum<CPL * R>(xr, m, sx);
+    const int E = code_exp(m);
+    const float s0 = pow2i(126 - E), s8 = pow2i(118 - E), s16 = pow2i(110 - E);  // bytes 0, 1, 2 and 3
 #pragma unroll
-    for (int i = 0; i < EPC / 4; ++i) {
-      const float4 q = q4[i];
-      xr[2 * i] = make_float2(q.x * 0x1p85f, q.y * 0x1p77f);      // p 0, 8
-      xr[2 * i + 1] = make_float2(q.z * 0x1p69f, q.w * 0x1p69f);  // p 16, 16
-      sx += (q.x + q.y) + (q.z + q.w);
+    for (int i = 0; i < CPL * R / 2; ++i) {
+      xr[2 * i] = make_float2(xr[2 * i].x * s0, xr[2 * i].y * s8);
+      xr[2 * i + 1] = make_float2(xr[2 * i + 1].x * s16, xr[2 * i + 1].y * s16);
     }
-    nb = -128.f * sx;
-  } else {
-#pragma unroll
-    for (int i = 0; i < EPC / 4; ++i) {
-      const float4 q = q4[i];
-      xr[2 * i] = make_float2(q.x, q.y);
-      xr[2 * i + 1] = make_float2(q.z, q.w);
-    }
-    nb = 0.f;
+    nb[0] = -128.f * sx;
+    cs[0] = pow2i(E + 23);
   }
 }
 
@@ -251,11 +318,12 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
 // loads cost one shared-memory latency.  Chunks at or
 // past Kp are read from the slice start instead (always staged) and meet zero input
 // registers, so they add exact zeros.  nrows (<= RPW) rows are valid; the others read
-// the first row.  nb holds load_xr's bias terms of the lane's chunks (0 past Kp).
+// the first row.  nb and cs hold load_lane_xr's bias terms and scales.
 template <int F>
 __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes, uint32_t sc, uint32_t s_bytes,
-                                               int nrows, const float2 *xr, const float *nb, int e0, int Kp,
-                                               int lane, float (&sum)[FmtT<F>::RPW], int gshift = 0) {
+                                               int nrows, const float2 *xr, const float *nb, const float *cs,
+                                               int e0, int Kp, int lane, float (&sum)[FmtT<F>::RPW],
+                                               int gshift = 0) {
   using T = FmtT<F>;
   constexpr int EPC = T::EPC, CPL = T::CPL, R = T::RPW, kChunkStride = 32 * EPC;
   uint4 w[R][CPL];
@@ -281,8 +349,8 @@ __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes,
       for (int c = 0; c < CPL; ++c) {
         float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         chunk_fma<F>(w[i][c], xr + c * (EPC / 2), acc);
-        const float cs = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
-        acc_s = fmaf(__half2float(__ushort_as_half((unsigned short)hb[i][c])), fmaf(cs, kCodeScale, nb[c]), acc_s);
+        const float t = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
+        acc_s = fmaf(__half2float(__ushort_as_half((unsigned short)hb[i][c])), fmaf(t, cs[c], nb[c]), acc_s);
       }
       sum[i] = acc_s;
     }
@@ -294,10 +362,7 @@ __device__ __forceinline__ void stage_rows_dot(uint32_t row, uint32_t row_bytes,
       for (int c = 0; c < CPL; ++c) chunk_fma<F>(w[i][c], xr + c * (EPC / 2), acc);
       const float t = (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y) + (acc[2].x + acc[2].y) + (acc[3].x + acc[3].y);
       if constexpr (F == MIE_FMT_I8) {
-        float b = 0.f;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) b += nb[c];
-        sum[i] = fmaf(t, kCodeScale, b);
+        sum[i] = fmaf(t, cs[0], nb[0]);
       } else {
         sum[i] = t;
       }

@@ -169,20 +169,9 @@ __global__ void __launch_bounds__(32 * (NW + 1), kMinBlocks<F>) gemv_kernel(cons
   const int ri = warp / KS, ks = warp % KS;
   const bool has_slice = warp < WR * KS;
   const int e0 = ks * kSlice + lane * EPC;
-  constexpr int kChunkStride = 32 * EPC;
   float2 xr[CPL * EPC / 2];
-  float nb[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    const int e = e0 + c * kChunkStride;
-    if (has_slice && e < Kp) {
-      load_xr<F>(xs, e, xr + c * (EPC / 2), nb[c]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < EPC / 2; ++i) xr[c * (EPC / 2) + i] = make_float2(0.f, 0.f);
-      nb[c] = 0.f;
-    }
-  }
+  float nb[CPL], cs[CPL];
+  load_lane_xr<F>(xs, e0, Kp, has_slice, xr, nb, cs);
 
   int consumed = 0;
   for (int s = 0; s < n_stages; ++s) {
@@ -201,7 +190,7 @@ __global__ void __launch_bounds__(32 * (NW + 1), kMinBlocks<F>) gemv_kernel(cons
       const uint32_t sca = smem_u32(sring) + (uint32_t)slot * sc_bytes +
                            (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice >> (5 + m.gshift))) * 2;
       float sum[RPW];
-      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, nb, e0, Kp, lane, sum,
+      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, nb, cs, e0, Kp, lane, sum,
                         m.gshift);
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {

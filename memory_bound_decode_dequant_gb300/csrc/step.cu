@@ -194,7 +194,6 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   constexpr int EPC = T::EPC, CPL = T::CPL;
   constexpr int kBitsPerElem = (F == MIE_FMT_BF16) ? 16 : (F == MIE_FMT_I8 ? 8 : 4);
   constexpr int kSliceBytes = kSlice * kBitsPerElem / 8;
-  constexpr int kChunkStride = 32 * EPC;
   const GemvArgs &a = ph.g;
   const DevMat &m = a.m;
   const int Kp = m.kp, K = m.cols, M = m.rows;
@@ -279,18 +278,8 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
   const bool has_slice = warp < rr.WR * rr.KS;
   const int e0 = ks * kSlice + lane * EPC;
   float2 xr[CPL * EPC / 2];
-  float nb[CPL];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    const int e = e0 + c * kChunkStride;
-    if (has_slice && e < Kp) {
-      load_xr<F>(xs, e, xr + c * (EPC / 2), nb[c]);
-    } else {
-#pragma unroll
-      for (int i = 0; i < EPC / 2; ++i) xr[c * (EPC / 2) + i] = make_float2(0.f, 0.f);
-      nb[c] = 0.f;
-    }
-  }
+  float nb[CPL], cs[CPL];
+  load_lane_xr<F>(xs, e0, Kp, has_slice, xr, nb, cs);
   SUB_STAMP(2);
 
   // stream this CTA's stages of the phase; a wait that gives up stops the math, and a
@@ -314,7 +303,7 @@ __device__ bool gemv_phase(const Phase &ph, const Ring &ring, int &s_global, flo
       const uint32_t sca = smem_u32(ring.sc) + (uint32_t)slot * ring.slot_sc_bytes +
                            (uint32_t)(ri * RPW * m.s_stride + ks * (kSlice >> (5 + m.gshift))) * 2;
       float sum[RPW];
-      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, nb, e0, Kp, lane, sum,
+      stage_rows_dot<F>(rowa, (uint32_t)m.row_bytes, sca, (uint32_t)m.s_stride * 2, nr, xr, nb, cs, e0, Kp, lane, sum,
                         m.gshift);
 #pragma unroll
       for (int i = 0; i < RPW; ++i) {

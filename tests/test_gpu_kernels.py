@@ -110,10 +110,11 @@ def test_q4_0_pack_layout(orc):
 
 # ------------------------------------------------------------------ GEMV
 
-def _gemv_both(orc, fmt, M, K, seed, rows=None):
+def _gemv_both(orc, fmt, M, K, seed, rows=None, x=None):
     """GPU GEMV over the full matrix; oracle over `rows` (all when None)."""
     w = synth.normal(seed, M * K, std=0.02).reshape(M, K)
-    x = bf16_vector(orc, seed + 1, K)
+    if x is None:
+        x = bf16_vector(orc, seed + 1, K)
     wd = torch.from_numpy(w).cuda()
     xd = torch.from_numpy(x).cuda()
     if fmt == "bf16":
@@ -146,6 +147,24 @@ def test_gemv_small_and_ragged(orc, fmt, shape):
 @pytest.mark.parametrize("K", [1, 31, 33, 40, 100, 129, 200])
 def test_gemv_q4_0_any_k(orc, fmt, K):
     y, ref = _gemv_both(orc, fmt, 9, K, 3000 + K)
+    gemv_close(y, ref)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "i8", "q4_0", "q4_g64", "q4_g128"])
+@pytest.mark.parametrize("xscale", [1e-30, 1e-12, 1e12, 1e30, "mixed"])
+@pytest.mark.parametrize("K", [688, 4096])
+def test_gemv_input_magnitudes(orc, fmt, xscale, K):
+    """Inputs far from unit size: the int8 / Q4_0 dot products scale their input registers
+    by a power of two chosen from each group's largest |x|, so tiny and huge vectors
+    (and a group holding 1e4 beside 1e-4) keep full precision."""
+    x = bf16_vector(orc, 7000 + K, K)
+    if xscale == "mixed":
+        x = (x * 1e-4).astype(np.float32)
+        x[::32] = 1e4
+    else:
+        x = (x * np.float32(xscale)).astype(np.float32)
+    y, ref = _gemv_both(orc, fmt, 65, K, 7100 + K, x=x)
+    assert np.all(np.isfinite(y))
     gemv_close(y, ref)
 
 
