@@ -90,7 +90,7 @@ __device__ __forceinline__ void chunk_fma<MIE_FMT_I8>(const uint4 &w, const floa
 // Q4_0 chunk = one block: word t holds bytes 4t..4t+3; byte j carries element j (low
 // nibble) and element j+16 (high nibble).  Unpack order per word, with the bit offset
 // p the code sits at: 4t(p0) 4t+16(p4) 4t+1(p8) 4t+17(p12) 4t+2(p16), then from
-// w >> 12: 4t+18(p8) 4t+3(p12) 4t+19(p16); load_xr puts x 2^(85-p) in that order.
+// w >> 12: 4t+18(p8) 4t+3(p12) 4t+19(p16); load_lane_xr puts x 2^(126-p-E) in that order.
 template <>
 __device__ __forceinline__ void chunk_fma<MIE_FMT_Q4_0>(const uint4 &w, const float2 *xr, float2 *acc) {
   const uint32_t v[4] = {w.x, w.y, w.z, w.w};
